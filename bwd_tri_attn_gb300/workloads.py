@@ -1,0 +1,126 @@
+"""Seeded synthetic inputs for triangle attention.
+
+This module holds no arithmetic of the method: it only draws random tensors
+(CPU ``torch.Generator``, float32 normal draws rounded to BF16) in the shapes,
+value distributions and padding patterns of the crop sizes that the
+TurboPairFormer paper evaluates (arXiv 2610.05854v1, Abstract: BF16 inputs,
+crops 384/640/768, head dims 16/32). Both the CUDA path's tests and the oracle
+are fed from here.
+
+Layouts: Q, K, V, dO [B,S,N,H,d] (S = number of row-slices, equal to N for a
+square pair tensor); bias [B,H,N,N]; mask [B,S,N] additive BF16 (0 or -inf) or
+None.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    """One named input recipe."""
+
+    name: str
+    B: int
+    N: int
+    H: int
+    d: int
+    seed: int
+    value_std: float = 1.0
+    bias_std: float = 1.0
+    # mask kinds: "none" (NULL mask), "zeros" (all valid but present),
+    # ("tail", n) last n keys masked in every slice, ("random", frac) a random
+    # fraction of keys masked per batch, shared by all slices.
+    mask: tuple = ("none",)
+    S: int | None = None  # number of slices; defaults to N
+    notes: str = field(default="", compare=False)
+
+    @property
+    def slices(self) -> int:
+        return self.N if self.S is None else self.S
+
+    def flops(self) -> float:
+        """Algorithmic fwd+bwd FLOPs: 4 (fwd) + 10 (bwd incl. one recompute) x B*S*H*N^2*d."""
+        return 14.0 * self.B * self.slices * self.H * self.N * self.N * self.d
+
+
+TINY = Workload("tiny_n32_h2_d16", B=1, N=32, H=2, d=16, seed=0, mask=("none",),
+                notes="tiny starting-node case, no mask")
+PAD128 = Workload("pad_n128_h4_d32", B=1, N=128, H=4, d=32, seed=1, value_std=0.5,
+                  mask=("tail", 13), notes="last 13 keys padding-masked in every slice")
+CROP384 = Workload("crop384_h4_d32", B=1, N=384, H=4, d=32, seed=2, bias_std=2.0,
+                   mask=("zeros",), notes="all-valid mask tensor, bias sigma 2")
+CROP640_D16 = Workload("crop640_h4_d16", B=1, N=640, H=4, d=16, seed=3,
+                       mask=("random", 0.05), notes="5% random key mask per batch")
+CROP640_D32 = Workload("crop640_h4_d32", B=1, N=640, H=4, d=32, seed=3,
+                       mask=("random", 0.05), notes="5% random key mask per batch")
+CROP768 = Workload("crop768_h4_d32", B=1, N=768, H=4, d=32, seed=4,
+                   mask=("tail", 48), notes="last 48 keys padding-masked; headline size")
+
+ALL = {w.name: w for w in (TINY, PAD128, CROP384, CROP640_D16, CROP640_D32, CROP768)}
+
+
+def _normal(gen, shape, std):
+    x = torch.randn(shape, generator=gen, dtype=torch.float32)
+    if std != 1.0:
+        x = x * std
+    return x.to(torch.bfloat16)
+
+
+def make_mask(kind, B, S, N, gen) -> torch.Tensor | None:
+    """Additive BF16 key mask [B,S,N] for a mask recipe (see ``Workload.mask``)."""
+    tag = kind[0]
+    if tag == "none":
+        return None
+    m = torch.zeros((B, S, N), dtype=torch.float32)
+    if tag == "zeros":
+        pass
+    elif tag == "tail":
+        n = int(kind[1])
+        if n > 0:
+            m[:, :, N - n:] = float("-inf")
+    elif tag == "random":
+        n = int(round(float(kind[1]) * N))
+        for b in range(B):
+            keys = torch.randperm(N, generator=gen)[:n]
+            m[b, :, keys] = float("-inf")
+    elif tag == "slices":
+        # every key of the listed slices is masked (fully masked rows)
+        for i in kind[1]:
+            m[:, int(i), :] = float("-inf")
+    else:
+        raise ValueError(f"unknown mask kind {kind!r}")
+    return m.to(torch.bfloat16)
+
+
+def make_inputs(B, S, N, H, d, seed, value_std=1.0, bias_std=1.0, mask=("none",)):
+    """Draws Q, K, V, dO, bias and mask (CPU, BF16) for one seed.
+
+    Draw order is fixed: Q, K, V, dO, bias, then the mask's own draws.
+    """
+    gen = torch.Generator().manual_seed(int(seed))
+    shape = (B, S, N, H, d)
+    Q = _normal(gen, shape, value_std)
+    K = _normal(gen, shape, value_std)
+    V = _normal(gen, shape, value_std)
+    dO = _normal(gen, shape, value_std)
+    bias = _normal(gen, (B, H, N, N), bias_std)
+    m = make_mask(mask, B, S, N, gen)
+    return {"Q": Q, "K": K, "V": V, "dO": dO, "bias": bias, "mask": m}
+
+
+def inputs_for(w: Workload, slices: int | None = None):
+    """Inputs of a named workload; ``slices`` overrides S (a bounded sample)."""
+    S = w.slices if slices is None else int(slices)
+    return make_inputs(w.B, S, w.N, w.H, w.d, w.seed, w.value_std, w.bias_std, w.mask)
+
+
+def ending_node(t: torch.Tensor) -> torch.Tensor:
+    """Transposes the pair axes (1 <-> 2) of a [B,S,N,...] tensor, contiguous copy.
+
+    The ending-node variant of triangle attention is the same operation on the
+    transposed pair tensor.
+    """
+    return t.transpose(1, 2).contiguous()
