@@ -1,0 +1,332 @@
+"""Triangle-attention forward + backward throughput on GB300.
+
+One step = one pass of the whole path (forward, D correction, main backward,
+dBias reduction) over one batch of synthetic input of the named workload.
+Prints ONE JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+With N > 1 (torchrun, one process per GPU) every rank runs an independent
+replica of the workload (the path has no cross-GPU exchange at this size):
+weak scaling, the max over ranks of the timed region is used, and value is the
+work of all ranks divided by that time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "triangle-attn fwd+bwd TFLOP/s at N=768,H=4,d=32 (1 GB300; % BF16 peak)"
+UNIT = "TFLOP/s"
+L2_BYTES = 129 * 2**20
+
+# Kernels each step enqueues, in order (the library's per-kernel event order).
+KERNELS = ["fwd", "bwd_d", "bwd_main", "dbias_reduce"]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.file.flush()
+        with open(self.file.name) as f:
+            rows = [r.strip().split(",") for r in f if r.strip()]
+        os.unlink(self.file.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [c.strip() for c in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_oracle_sample(w, slices: int, nthreads: int = 0):
+    """Times the FP64 oracle's forward + backward on `slices` slices of the workload."""
+    import oracle
+    from bwd_tri_attn_gb300 import workloads as wl
+
+    x = wl.inputs_for(w, slices=slices)
+    args = [oracle._f64(x[k]) for k in ("Q", "K", "V", "bias", "mask", "dO")]
+    cores = oracle.num_threads(nthreads)
+    t0 = time.perf_counter()
+    oracle.fwd(*args[:5], nthreads=nthreads)
+    oracle.bwd(*args, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    flops = 14.0 * w.B * slices * w.H * w.N * w.N * w.d
+    return flops / dt / 1e12, dt, cores
+
+
+def run_reference(args, w):
+    """Reference arm: the FP64 oracle on the host cores, one bounded sample per step."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    slices = args.ref_slices
+    for _ in range(args.warmup):
+        cpu_oracle_sample(w, slices)
+    times, cores = [], 1
+    for _ in range(args.steps):
+        _, dt, cores = cpu_oracle_sample(w, slices)
+        times.append(dt)
+    t = sum(times)
+    flops = 14.0 * w.B * slices * w.H * w.N * w.N * w.d
+    value = flops * args.steps / t / 1e12
+    sample = f"{slices} of {w.slices} slices (all {w.H} heads, full N={w.N}) per step"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.name, "B": w.B, "S": w.slices, "N": w.N, "H": w.H, "d": w.d},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    from bwd_tri_attn_gb300 import binding as tb
+    from bwd_tri_attn_gb300 import workloads as wl
+    from bwd_tri_attn_gb300 import _build
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    _build.build()
+    tb.load()
+
+    x = wl.inputs_for(w)
+    d = {k: (None if v is None else v.to(dev)) for k, v in x.items()}
+    shape = tb.shape_of(d["Q"])
+    B, S, N, H, hd = d["Q"].shape
+    O = torch.empty_like(d["Q"])
+    Ores = torch.empty_like(d["Q"])
+    LSE = torch.empty((B, S, H, N), dtype=torch.float32, device=dev)
+    dQ, dK, dV = torch.empty_like(O), torch.empty_like(O), torch.empty_like(O)
+    dBias = torch.empty_like(d["bias"])
+    ws = tb.workspace_for(shape, dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        tb.tri_attn_fwd(shape, d["Q"], d["K"], d["V"], d["bias"], d["mask"], O, LSE, Ores, stream)
+        tb.tri_attn_bwd(shape, d["Q"], d["K"], d["V"], d["bias"], d["mask"], O, Ores, LSE, d["dO"], dQ, dK, dV,
+                        dBias, ws, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # per-kernel events: [start, after fwd] per fwd call and [after D, after main, after reduce] per bwd call
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(len(KERNELS))] for _ in range(K)]
+    for e in starts + [m for ms in marks for m in ms]:
+        e.record(stream)  # materialise the events before handing their handles over
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        t_start.record(stream)
+        for k in range(K):
+            starts[k].record(stream)
+            tb.tri_attn_set_timing_events(marks[k][:1])
+            tb.tri_attn_fwd(shape, d["Q"], d["K"], d["V"], d["bias"], d["mask"], O, LSE, Ores, stream)
+            tb.tri_attn_set_timing_events(marks[k][1:])
+            tb.tri_attn_bwd(shape, d["Q"], d["K"], d["V"], d["bias"], d["mask"], O, Ores, LSE, d["dO"], dQ, dK,
+                            dV, dBias, ws, stream)
+        t_end.record(stream)
+        tb.tri_attn_set_timing_events(None)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    assert tb.tri_attn_device_status() == 0
+
+    per_kernel = {n: [] for n in KERNELS}
+    for k in range(K):
+        chain = [starts[k]] + marks[k]
+        for n, (a, b) in enumerate(zip(chain[:-1], chain[1:])):
+            per_kernel[KERNELS[n]].append(a.elapsed_time(b))
+    kernel_ms = {n: sum(v) / len(v) for n, v in per_kernel.items()}
+
+    flops = w.flops()
+    ms_per_step = elapsed_ms / K
+    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    peaks = load_peaks()
+
+    # roofline of the dominant kernel (tensor-bound contraction; FP16 operands run at the BF16 rate)
+    flops_of = {"fwd": 4.0 * B * S * H * N * N * hd, "bwd_main": 10.0 * B * S * H * N * N * hd}
+    dom = max(("fwd", "bwd_main"), key=lambda n: kernel_ms[n])
+    achieved = flops_of[dom] / (kernel_ms[dom] * 1e-3) / 1e12
+    roofline = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                "peak_source": f"{peaks['source']} bf16 dense burst"}
+
+    # HBM-bound kernels: algorithmic bytes / time
+    nx = B * S * N * H * hd
+    bytes_d = 3 * 2 * nx + 4 * B * S * H * N
+    hbm = {"bwd_d_gbs": bytes_d / (kernel_ms["bwd_d"] * 1e-3) / 1e9}
+
+    # end to end through the public API: pinned host inputs -> device -> fwd+bwd -> gradients back to host
+    e2e = None
+    if not args.no_e2e:
+        host_in = {k: (None if v is None else v.pin_memory()) for k, v in x.items()}
+        host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (dQ, dK, dV, dBias)]
+        h2d = sum(v.numel() * v.element_size() for v in host_in.values() if v is not None)
+        d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+        def e2e_step():
+            for kname, v in host_in.items():
+                if v is not None:
+                    d[kname].copy_(v, non_blocking=True)
+            step()
+            for src, dst in zip((dQ, dK, dV, dBias), host_out):
+                dst.copy_(src, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ke = max(1, min(K, 10))
+        e0.record(stream)
+        for _ in range(ke):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = e0.elapsed_time(e1) / ke
+        if world > 1:
+            t = torch.tensor([ems], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": world * flops / (ems * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": ems}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, dt, cores = cpu_oracle_sample(w, args.cpu_slices)
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "seconds": dt,
+               "sample": f"{args.cpu_slices} of {w.slices} slices (all {w.H} heads, full N={w.N}), fwd+bwd"}
+
+    in_bytes = sum(v.numel() * v.element_size() for v in x.values() if v is not None)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "S": w.slices, "N": w.N, "H": w.H, "d": w.d,
+                       "mask": list(w.mask), "flops_per_step": flops,
+                       "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB of inputs vs {L2_BYTES / 1e6:.0f} MB L2), no flush",
+                       "operands": "BF16 in/out, FP16 tensor-core operands, FP32 accumulation"},
+            "pct_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
+            "kernel_ms": kernel_ms, "hbm": hbm, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": K * len(KERNELS), "clocks": clocks.summary(),
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    from bwd_tri_attn_gb300 import workloads as wl
+
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=wl.CROP768.name, choices=sorted(wl.ALL))
+    ap.add_argument("--cpu-slices", type=int, default=64, help="slices in the timed CPU oracle sample")
+    ap.add_argument("--ref-slices", type=int, default=4, help="slices per step of the reference arm")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    w = wl.ALL[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

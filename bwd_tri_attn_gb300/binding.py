@@ -1,0 +1,163 @@
+"""Thin ctypes binding of the C ABI in ``include/tri_attn.h``.
+
+Argument marshalling only: PyTorch tensors supply device pointers and the
+current CUDA stream; every step of the computation runs in the library's
+kernels. There is no CPU fallback: if the library is missing or a call fails,
+an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+from . import _build
+
+TRI_ATTN_OK = 0
+_lock = threading.Lock()
+_lib = None
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("S", ctypes.c_int), ("N", ctypes.c_int), ("H", ctypes.c_int),
+                ("d", ctypes.c_int), ("scale", ctypes.c_float)]
+
+    def __repr__(self):
+        return f"Shape(B={self.B}, S={self.S}, N={self.N}, H={self.H}, d={self.d}, scale={self.scale})"
+
+
+class TriAttnError(RuntimeError):
+    def __init__(self, fn, code):
+        super().__init__(f"{fn} failed: {code} ({strerror(code)})")
+        self.code = code
+
+
+_VP = ctypes.c_void_p
+EXPORTS = ("tri_attn_strerror", "tri_attn_fwd", "tri_attn_bwd_workspace_size", "tri_attn_bwd",
+           "tri_attn_device_status", "tri_attn_set_timing_events")
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(path: str | None = None):
+    """Loads ``libtriattn.so`` (built by ``__graft_entry__.build()``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = path or _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build the CUDA library first (__graft_entry__.build())")
+        lib = ctypes.CDLL(path)
+        lib.tri_attn_strerror.argtypes = [ctypes.c_int]
+        lib.tri_attn_strerror.restype = ctypes.c_char_p
+        lib.tri_attn_fwd.argtypes = [Shape] + [_VP] * 9
+        lib.tri_attn_fwd.restype = ctypes.c_int
+        lib.tri_attn_bwd_workspace_size.argtypes = [Shape]
+        lib.tri_attn_bwd_workspace_size.restype = ctypes.c_size_t
+        lib.tri_attn_bwd.argtypes = [Shape] + [_VP] * 14 + [ctypes.c_size_t, _VP]
+        lib.tri_attn_bwd.restype = ctypes.c_int
+        lib.tri_attn_device_status.argtypes = [_VP]
+        lib.tri_attn_device_status.restype = ctypes.c_int
+        lib.tri_attn_set_timing_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]
+        lib.tri_attn_set_timing_events.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def strerror(code: int) -> str:
+    return load().tri_attn_strerror(int(code)).decode()
+
+
+def shape_of(Q: torch.Tensor, scale: float | None = None) -> Shape:
+    B, S, N, H, d = (int(x) for x in Q.shape)
+    return Shape(B, S, N, H, d, float(1.0 / math.sqrt(d) if scale is None else scale))
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(fn, rc):
+    if rc != TRI_ATTN_OK:
+        raise TriAttnError(fn, rc)
+
+
+def tri_attn_fwd(shape: Shape, Q, K, V, bias, mask, O, LSE, Ores, stream=None):
+    rc = load().tri_attn_fwd(shape, _p(Q), _p(K), _p(V), _p(bias), _p(mask), _p(O), _p(LSE), _p(Ores),
+                             _stream(stream))
+    _check("tri_attn_fwd", rc)
+
+
+def tri_attn_bwd_workspace_size(shape: Shape) -> int:
+    return int(load().tri_attn_bwd_workspace_size(shape))
+
+
+def tri_attn_bwd(shape: Shape, Q, K, V, bias, mask, O, Ores, LSE, dO, dQ, dK, dV, dBias, workspace,
+                 stream=None):
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().tri_attn_bwd(shape, _p(Q), _p(K), _p(V), _p(bias), _p(mask), _p(O), _p(Ores), _p(LSE),
+                             _p(dO), _p(dQ), _p(dK), _p(dV), _p(dBias), _p(workspace), nbytes,
+                             _stream(stream))
+    _check("tri_attn_bwd", rc)
+
+
+def tri_attn_device_status(stream=None) -> int:
+    return int(load().tri_attn_device_status(_stream(stream)))
+
+
+_event_array = None  # keeps the pointer array alive while instrumentation is on
+
+
+def tri_attn_set_timing_events(events) -> None:
+    """Per-kernel timing: ``events`` is a list of recorded torch.cuda.Event (or None to switch off)."""
+    global _event_array
+    if not events:
+        _event_array = None
+        _check("tri_attn_set_timing_events", load().tri_attn_set_timing_events(None, 0))
+        return
+    arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    _event_array = arr
+    _check("tri_attn_set_timing_events", load().tri_attn_set_timing_events(arr, len(events)))
+
+
+# ----------------------------------------------------------------------------
+# Allocating conveniences (outputs are fresh torch tensors on Q's device).
+# ----------------------------------------------------------------------------
+
+def forward(Q, K, V, bias, mask=None, scale=None, residual=True, stream=None):
+    """Returns (O, LSE, Ores); Ores is None when ``residual`` is False."""
+    shape = shape_of(Q, scale)
+    B, S, N, H, d = Q.shape
+    O = torch.empty_like(Q)
+    LSE = torch.empty((B, S, H, N), dtype=torch.float32, device=Q.device)
+    Ores = torch.empty_like(Q) if residual else None
+    tri_attn_fwd(shape, Q, K, V, bias, mask, O, LSE, Ores, stream)
+    return O, LSE, Ores
+
+
+def workspace_for(shape: Shape, device) -> torch.Tensor:
+    n = tri_attn_bwd_workspace_size(shape)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+
+
+def backward(Q, K, V, bias, mask, O, Ores, LSE, dO, scale=None, workspace=None, stream=None):
+    """Returns (dQ, dK, dV, dBias)."""
+    shape = shape_of(Q, scale)
+    if workspace is None:
+        workspace = workspace_for(shape, Q.device)
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    dBias = torch.empty_like(bias)
+    tri_attn_bwd(shape, Q, K, V, bias, mask, O, Ores, LSE, dO, dQ, dK, dV, dBias, workspace, stream)
+    return dQ, dK, dV, dBias

@@ -1,0 +1,163 @@
+// Host side of the C ABI declared in include/tri_attn.h: argument checks,
+// workspace layout and kernel launches. No device memory is allocated here and
+// nothing synchronises except tri_attn_device_status().
+#include <math.h>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace triattn {
+cudaError_t launch_bwd_d(const Dims &g, const uint16_t *dO, const uint16_t *O, const uint16_t *Ores,
+                         float *Dout, cudaStream_t stream);
+cudaError_t launch_dbias_reduce(const float *partial, int G, int64_t elems, uint16_t *dBias,
+                                cudaStream_t stream);
+cudaError_t launch_simt_fwd(const Dims &g, const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                            const uint16_t *bias, const uint16_t *mask, uint16_t *O, float *LSE,
+                            uint16_t *Ores, cudaStream_t stream);
+cudaError_t launch_simt_bwd(const Dims &g, int G, const uint16_t *Q, const uint16_t *K,
+                            const uint16_t *V, const uint16_t *bias, const uint16_t *mask,
+                            const float *LSE, const float *Dv, const uint16_t *dO, uint16_t *dQ,
+                            uint16_t *dK, uint16_t *dV, float *partial, cudaStream_t stream);
+}  // namespace triattn
+
+using namespace triattn;
+
+// Device status word: bounded waits that expire store a nonzero code here.
+__device__ int g_tri_attn_status;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_shape(const tri_attn_shape &s) {
+  if (s.B < 1 || s.S < 1 || s.N < 1 || s.H < 1 || !isfinite(s.scale)) return TRI_ATTN_ERR_INVALID_ARG;
+  if (s.d != 16 && s.d != 32) return TRI_ATTN_ERR_UNSUPPORTED;
+  if (s.N > TRI_ATTN_MAX_N) return TRI_ATTN_ERR_UNSUPPORTED;
+  // grid dimensions and 32-bit tile coordinates
+  if ((int64_t)s.B * s.S > 65535 || (int64_t)s.B * s.H * s.S > (1ll << 30)) return TRI_ATTN_ERR_UNSUPPORTED;
+  return TRI_ATTN_OK;
+}
+
+Dims to_dims(const tri_attn_shape &s) { return Dims{s.B, s.S, s.N, s.H, s.d, s.scale}; }
+
+// Number of slice groups whose dBias partials the backward pass keeps.
+int dbias_groups(const tri_attn_shape &s) { return s.S < 32 ? s.S : 32; }
+
+struct WorkspaceLayout {
+  size_t d_off, partial_off, total;
+  int groups;
+};
+
+WorkspaceLayout layout_for(const tri_attn_shape &s) {
+  WorkspaceLayout w;
+  const size_t rows = (size_t)s.B * s.S * s.H * s.N;
+  w.groups = dbias_groups(s);
+  w.d_off = 0;
+  w.partial_off = align_up(sizeof(float) * rows);
+  w.total = w.partial_off + align_up(sizeof(float) * (size_t)w.groups * s.B * s.H * s.N * s.N);
+  return w;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? TRI_ATTN_OK : TRI_ATTN_ERR_CUDA; }
+
+// Optional per-kernel timing events of the calling host thread.
+thread_local void *const *t_events = nullptr;
+thread_local int t_nevents = 0;
+
+// Records the caller's k-th timing event after the k-th kernel of a call.
+cudaError_t mark(int k, cudaStream_t st) {
+  if (t_events && k < t_nevents) return cudaEventRecord(static_cast<cudaEvent_t>(t_events[k]), st);
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *tri_attn_strerror(int code) {
+  switch (code) {
+    case TRI_ATTN_OK: return "success";
+    case TRI_ATTN_ERR_INVALID_ARG: return "invalid argument (NULL pointer, non-positive size or non-finite scale)";
+    case TRI_ATTN_ERR_UNSUPPORTED: return "unsupported configuration (d must be 16 or 32, N <= TRI_ATTN_MAX_N, pointers 16-byte aligned)";
+    case TRI_ATTN_ERR_WORKSPACE: return "workspace missing or smaller than tri_attn_bwd_workspace_size()";
+    case TRI_ATTN_ERR_CUDA: return "CUDA runtime error";
+    case TRI_ATTN_ERR_TIMEOUT: return "a bounded device-side wait expired";
+    default: return "unknown error code";
+  }
+}
+
+int tri_attn_fwd(tri_attn_shape shape, const tri_attn_bf16 *Q, const tri_attn_bf16 *K,
+                 const tri_attn_bf16 *V, const tri_attn_bf16 *bias, const tri_attn_bf16 *mask,
+                 tri_attn_bf16 *O, float *LSE, tri_attn_bf16 *Ores, void *stream) {
+  int rc = check_shape(shape);
+  if (rc) return rc;
+  if (!Q || !K || !V || !bias || !O || !LSE) return TRI_ATTN_ERR_INVALID_ARG;
+  const void *ptrs[] = {Q, K, V, bias, mask, O, LSE, Ores};
+  for (const void *p : ptrs)
+    if (p && !aligned16(p)) return TRI_ATTN_ERR_UNSUPPORTED;
+  const Dims g = to_dims(shape);
+  auto st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_simt_fwd(g, Q, K, V, bias, mask, O, LSE, Ores, st);
+  if (e == cudaSuccess) e = mark(0, st);
+  return cuda_rc(e);
+}
+
+size_t tri_attn_bwd_workspace_size(tri_attn_shape shape) {
+  if (check_shape(shape)) return 0;
+  return layout_for(shape).total;
+}
+
+int tri_attn_bwd(tri_attn_shape shape, const tri_attn_bf16 *Q, const tri_attn_bf16 *K,
+                 const tri_attn_bf16 *V, const tri_attn_bf16 *bias, const tri_attn_bf16 *mask,
+                 const tri_attn_bf16 *O, const tri_attn_bf16 *Ores, const float *LSE,
+                 const tri_attn_bf16 *dO, tri_attn_bf16 *dQ, tri_attn_bf16 *dK, tri_attn_bf16 *dV,
+                 tri_attn_bf16 *dBias, void *workspace, size_t workspace_bytes, void *stream) {
+  int rc = check_shape(shape);
+  if (rc) return rc;
+  if (!Q || !K || !V || !bias || !O || !LSE || !dO || !dQ || !dK || !dV || !dBias)
+    return TRI_ATTN_ERR_INVALID_ARG;
+  const void *ptrs[] = {Q, K, V, bias, mask, O, Ores, LSE, dO, dQ, dK, dV, dBias, workspace};
+  for (const void *p : ptrs)
+    if (p && !aligned16(p)) return TRI_ATTN_ERR_UNSUPPORTED;
+  const WorkspaceLayout w = layout_for(shape);
+  if (!workspace || workspace_bytes < w.total) return TRI_ATTN_ERR_WORKSPACE;
+  const Dims g = to_dims(shape);
+  auto st = static_cast<cudaStream_t>(stream);
+  char *ws = static_cast<char *>(workspace);
+  float *Dv = reinterpret_cast<float *>(ws + w.d_off);
+  float *partial = reinterpret_cast<float *>(ws + w.partial_off);
+  cudaError_t e = launch_bwd_d(g, dO, O, Ores, Dv, st);
+  if (e == cudaSuccess) e = mark(0, st);
+  if (e == cudaSuccess)
+    e = launch_simt_bwd(g, w.groups, Q, K, V, bias, mask, LSE, Dv, dO, dQ, dK, dV, partial, st);
+  if (e == cudaSuccess) e = mark(1, st);
+  if (e == cudaSuccess)
+    e = launch_dbias_reduce(partial, w.groups, (int64_t)shape.B * shape.H * shape.N * shape.N, dBias, st);
+  if (e == cudaSuccess) e = mark(2, st);
+  return cuda_rc(e);
+}
+
+int tri_attn_set_timing_events(void *const *events, int n) {
+  if (n < 0) return TRI_ATTN_ERR_INVALID_ARG;
+  t_events = (n > 0) ? events : nullptr;
+  t_nevents = (events != nullptr) ? n : 0;
+  return TRI_ATTN_OK;
+}
+
+int tri_attn_device_status(void *stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return TRI_ATTN_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_tri_attn_status, sizeof(int)) != cudaSuccess) return TRI_ATTN_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_tri_attn_status, &zero, sizeof(int)) != cudaSuccess) return TRI_ATTN_ERR_CUDA;
+    return TRI_ATTN_ERR_TIMEOUT;
+  }
+  return TRI_ATTN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,150 @@
+/*
+ * tri_attn.h - C ABI of the GB300 (sm_103a) triangle-attention library.
+ *
+ * Operation (TurboPairFormer: Fast and Stable Protein Folding Model Training
+ * with an Optimized Triangle Attention Kernel, arXiv 2610.05854v1, Abstract):
+ * every row-slice i of an N x N pair tensor runs multi-head attention over its
+ * N positions, and a pair bias bias[b,h,j,k] is added to the scores of every
+ * slice. Per batch b, slice i, head h, query j, key k:
+ *
+ *   S[j,k] = scale * <Q[b,i,j,h,:], K[b,i,k,h,:]> + bias[b,h,j,k] + mask[b,i,k]
+ *   P      = softmax over k,   O[b,i,j,h,:] = sum_k P[j,k] V[b,i,k,h,:]
+ *
+ * The backward pass returns dQ, dK, dV and dBias = sum over slices of the
+ * per-slice score gradient (the bias is shared by all slices, which adds that
+ * reduction to the usual ones over queries and keys).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Tensors are dense, row-major, on the current CUDA device:
+ *     Q K V O Ores dO dQ dK dV : BF16 [B, S, N, H, d]   (S = number of slices)
+ *     bias dBias               : BF16 [B, H, N, N]
+ *     mask                     : BF16 [B, S, N], additive (0 or -inf), may be NULL
+ *     LSE                      : FP32 [B, S, H, N], natural-log log-sum-exp of the
+ *                                scores of each query row (-inf for a row whose
+ *                                keys are all masked)
+ * - Supported: d in {16, 32}; 1 <= N <= TRI_ATTN_MAX_N; B, S, H >= 1. scale is
+ *   any finite float (1/sqrt(d) is the usual choice). Q, K, V, dO entries must
+ *   have magnitude below 65504 (they are staged as FP16 tensor-core operands).
+ * - Every device pointer must be 16-byte aligned (TMA requirement).
+ * - Ownership: the caller allocates and owns every buffer, including the
+ *   backward workspace. The library allocates no device memory, never
+ *   synchronises, and enqueues all work on `stream` (a cudaStream_t; NULL is
+ *   the legacy default stream). Outputs are overwritten, never accumulated.
+ * - Determinism: for a fixed shape on a fixed GPU model, every output is
+ *   bitwise identical across calls. No floating-point atomics are used; every
+ *   reduction runs in an order fixed by the shape alone.
+ * - Errors: each call returns TRI_ATTN_OK or a negative code, checked on the
+ *   host before anything is enqueued (nothing is launched on an error).
+ *   Kernels never trap: a bounded device-side wait that expires records
+ *   TRI_ATTN_ERR_TIMEOUT in a device status word that
+ *   tri_attn_device_status() reads.
+ * - Ending-node attention is the same call on the pair tensor with its two
+ *   pair axes swapped (the caller passes the transposed tensors).
+ */
+#ifndef TRI_ATTN_H
+#define TRI_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Raw BF16 storage (IEEE binary32 with the low 16 bits dropped). */
+typedef uint16_t tri_attn_bf16;
+
+#define TRI_ATTN_MAX_N 1024
+
+typedef struct tri_attn_shape {
+    int B;       /* batch */
+    int S;       /* row-slices of the pair tensor (N for a square pair tensor) */
+    int N;       /* positions attended over inside a slice */
+    int H;       /* heads */
+    int d;       /* head dimension: 16 or 32 */
+    float scale; /* multiplies Q.K only (not the bias) */
+} tri_attn_shape;
+
+enum {
+    TRI_ATTN_OK = 0,
+    TRI_ATTN_ERR_INVALID_ARG = -1,  /* NULL where required, non-positive or non-finite sizes */
+    TRI_ATTN_ERR_UNSUPPORTED = -2,  /* d not 16/32, N above the limit, misaligned pointer */
+    TRI_ATTN_ERR_WORKSPACE = -3,    /* workspace NULL or smaller than tri_attn_bwd_workspace_size */
+    TRI_ATTN_ERR_CUDA = -4,         /* a CUDA runtime/driver call or launch failed */
+    TRI_ATTN_ERR_TIMEOUT = -5       /* a bounded device wait expired (see tri_attn_device_status) */
+};
+
+/* Human-readable text of a return code (static storage, never NULL). */
+const char *tri_attn_strerror(int code);
+
+/*
+ * Forward pass (arXiv 2610.05854v1, Abstract: BF16 forward outputs plus the
+ * output-residual that the backward correction uses).
+ *
+ * Inputs : Q, K, V, bias; mask may be NULL (no masking).
+ * Outputs: O    = BF16 round-to-nearest of the FP32 attention output;
+ *          LSE  = per-row log-sum-exp (FP32);
+ *          Ores = BF16 round-to-nearest of (O_fp32 - O), the output-rounding
+ *                 residual; may be NULL, in which case it is not written.
+ * Writing Ores never changes O.
+ */
+int tri_attn_fwd(tri_attn_shape shape,
+                 const tri_attn_bf16 *Q, const tri_attn_bf16 *K, const tri_attn_bf16 *V,
+                 const tri_attn_bf16 *bias, const tri_attn_bf16 *mask,
+                 tri_attn_bf16 *O, float *LSE, tri_attn_bf16 *Ores,
+                 void *stream);
+
+/* Bytes of device workspace tri_attn_bwd needs for `shape` (depends on shape only). */
+size_t tri_attn_bwd_workspace_size(tri_attn_shape shape);
+
+/*
+ * Backward pass (arXiv 2610.05854v1, Abstract: key-tile-parallel backward that
+ * recomputes each probability tile once, ordered partial reductions instead of
+ * floating-point atomics, and the softmax correction D computed in FP32 from
+ * the output plus its rounding residual).
+ *
+ * Inputs : Q, K, V, bias, mask (nullable) as given to tri_attn_fwd; O and LSE
+ *          from tri_attn_fwd; Ores from tri_attn_fwd, or NULL for the
+ *          uncompensated variant (D from the BF16 output alone); dO, the
+ *          gradient of the loss with respect to O.
+ * Outputs: dQ, dK, dV (BF16 [B,S,N,H,d]) and dBias (BF16 [B,H,N,N], summed over
+ *          the S slices, not over the batch).
+ * Workspace: `workspace` points to at least tri_attn_bwd_workspace_size(shape)
+ *          bytes of device memory (16-byte aligned) that the call may overwrite;
+ *          its contents on entry do not matter.
+ */
+int tri_attn_bwd(tri_attn_shape shape,
+                 const tri_attn_bf16 *Q, const tri_attn_bf16 *K, const tri_attn_bf16 *V,
+                 const tri_attn_bf16 *bias, const tri_attn_bf16 *mask,
+                 const tri_attn_bf16 *O, const tri_attn_bf16 *Ores, const float *LSE,
+                 const tri_attn_bf16 *dO,
+                 tri_attn_bf16 *dQ, tri_attn_bf16 *dK, tri_attn_bf16 *dV, tri_attn_bf16 *dBias,
+                 void *workspace, size_t workspace_bytes,
+                 void *stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the device status word of the
+ * current device: TRI_ATTN_OK, or TRI_ATTN_ERR_TIMEOUT if a bounded device wait
+ * expired in any call since the last check (that call's outputs are invalid).
+ * Returns TRI_ATTN_ERR_CUDA if the synchronisation itself fails.
+ */
+int tri_attn_device_status(void *stream);
+
+/*
+ * Per-kernel timing instrumentation (off by default). After this call, every
+ * tri_attn_fwd / tri_attn_bwd issued by the calling host thread records
+ * events[k] (a cudaEvent_t created by the caller) on the call's stream right
+ * after enqueuing the call's k-th kernel, for k < n. Kernel order:
+ * tri_attn_fwd = {forward}; tri_attn_bwd = {D correction, main backward,
+ * dBias reduction}. events = NULL or n = 0 switches it off. The events stay
+ * owned by the caller and must stay valid while instrumentation is on.
+ * Returns TRI_ATTN_OK, or TRI_ATTN_ERR_INVALID_ARG for n < 0.
+ */
+int tri_attn_set_timing_events(void *const *events, int n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TRI_ATTN_H */

@@ -53,6 +53,8 @@ def _load():
             lib.oracle_tri_attn_bwd.restype = ctypes.c_int
             lib.oracle_tri_attn_slice.argtypes = shape + [ctypes.c_int] * 3 + [_DP] * 8
             lib.oracle_tri_attn_slice.restype = ctypes.c_int
+            lib.oracle_tri_attn_dbias_rows.argtypes = shape + [_DP] * 6 + [ctypes.POINTER(ctypes.c_int), ctypes.c_int, _DP, ctypes.c_int]
+            lib.oracle_tri_attn_dbias_rows.restype = ctypes.c_int
             lib.oracle_num_threads.argtypes = [ctypes.c_int]
             lib.oracle_num_threads.restype = ctypes.c_int
             _lib = lib
@@ -129,3 +131,19 @@ def slice_matrices(Q, K, V, bias, mask, dO, b, i, h, scale=None):
     if rc != 0:
         raise RuntimeError(f"oracle_tri_attn_slice failed: {rc}")
     return P, dS
+
+
+def dbias_rows(Q, K, V, bias, mask, dO, rows, scale=None, nthreads: int = 0):
+    """dBias[b,h,j,:] for each (b,h,j) in ``rows``, summed over all slices: array [len(rows), N]."""
+    Q, K, V, bias, mask, dO = (_f64(t) for t in (Q, K, V, bias, mask, dO))
+    B, S, N, H, d = _dims(Q)
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 3))
+    out = np.zeros((r.shape[0], N))
+    rc = _load().oracle_tri_attn_dbias_rows(B, S, N, H, d, scale, _ptr(Q), _ptr(K), _ptr(V), _ptr(bias),
+                                            _ptr(mask), _ptr(dO),
+                                            r.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), r.shape[0],
+                                            _ptr(out), int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle_tri_attn_dbias_rows failed: {rc}")
+    return out

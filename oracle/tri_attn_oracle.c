@@ -310,3 +310,73 @@ int oracle_num_threads(int nthreads) {
     }
     return n;
 }
+
+/*
+ * dBias for selected rows: for each requested (b, h, j), returns
+ * dBias[b,h,j,:] = sum over all slices i of dS_i[j,:], computed directly from
+ * query row j of every slice (one row of S, P, dP per slice). Used to check
+ * the bias gradient at sizes where the full backward is too slow to run.
+ * rows holds nrows triples (b, h, j); out is [nrows][N].
+ */
+int oracle_tri_attn_dbias_rows(int B, int S, int N, int H, int d, double scale,
+                               const double *Q, const double *K, const double *V,
+                               const double *bias, const double *mask, const double *dO,
+                               const int *rows, int nrows, double *out, int nthreads) {
+    shape_t s = {B, S, N, H, d, scale};
+    if (check_shape(&s) || !Q || !K || !V || !bias || !dO || !rows || !out || nrows < 0)
+        return ORACLE_EINVAL;
+    for (int r = 0; r < nrows; ++r)
+        if (rows[3 * r] < 0 || rows[3 * r] >= B || rows[3 * r + 1] < 0 || rows[3 * r + 1] >= H ||
+            rows[3 * r + 2] < 0 || rows[3 * r + 2] >= N)
+            return ORACLE_EINVAL;
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+    int err = ORACLE_OK;
+#pragma omp parallel
+    {
+        double *srow = malloc(sizeof(double) * N), *o = malloc(sizeof(double) * d);
+        if (!srow || !o) {
+#pragma omp atomic write
+            err = ORACLE_ENOMEM;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int r = 0; r < nrows; ++r) {
+                const int b = rows[3 * r], h = rows[3 * r + 1], j = rows[3 * r + 2];
+                double *acc = out + (size_t)r * N;
+                for (int kk = 0; kk < N; ++kk) acc[kk] = 0.0;
+                const double *brow = bias + (((size_t)b * H + h) * N + j) * N;
+                for (int i = 0; i < S; ++i) {
+                    const double *mrow = mask ? mask + ((size_t)b * S + i) * N : NULL;
+                    double m = -INFINITY;
+                    for (int kk = 0; kk < N; ++kk) {
+                        double dot = 0.0;
+                        for (int c = 0; c < d; ++c)
+                            dot += Q[x_index(&s, b, i, j, h, c)] * K[x_index(&s, b, i, kk, h, c)];
+                        double sc = scale * dot + brow[kk];
+                        if (mrow) sc += mrow[kk];
+                        srow[kk] = sc;
+                        if (sc > m) m = sc;
+                    }
+                    if (m == -INFINITY) continue; /* fully masked row: no contribution */
+                    double l = 0.0;
+                    for (int kk = 0; kk < N; ++kk) { srow[kk] = exp(srow[kk] - m); l += srow[kk]; }
+                    for (int kk = 0; kk < N; ++kk) srow[kk] /= l; /* srow is now P[j,:] */
+                    for (int c = 0; c < d; ++c) {
+                        double a = 0.0;
+                        for (int kk = 0; kk < N; ++kk) a += srow[kk] * V[x_index(&s, b, i, kk, h, c)];
+                        o[c] = a;
+                    }
+                    double Dj = 0.0;
+                    for (int c = 0; c < d; ++c) Dj += dO[x_index(&s, b, i, j, h, c)] * o[c];
+                    for (int kk = 0; kk < N; ++kk) {
+                        double dp = 0.0;
+                        for (int c = 0; c < d; ++c)
+                            dp += dO[x_index(&s, b, i, j, h, c)] * V[x_index(&s, b, i, kk, h, c)];
+                        acc[kk] += srow[kk] * (dp - Dj);
+                    }
+                }
+            }
+        }
+        free(srow); free(o);
+    }
+    return err;
+}

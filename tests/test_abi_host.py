@@ -1,0 +1,121 @@
+"""Host-side checks of the C ABI (no GPU needed, no compute launched).
+
+The library is built and loaded, every function declared in include/*.h must
+be exported, and argument validation must reject bad calls on the host with
+the documented codes before anything is enqueued.
+"""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from bwd_tri_attn_gb300 import _build, binding
+    _build.build()
+    return binding.load()
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b(?:int|size_t|const char\s*\*|void)\s*\*?\s*(tri_attn_\w+)\s*\(", text):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert {"tri_attn_fwd", "tri_attn_bwd", "tri_attn_bwd_workspace_size", "tri_attn_strerror",
+            "tri_attn_device_status", "tri_attn_set_timing_events"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def test_strerror_covers_codes(lib):
+    from bwd_tri_attn_gb300 import binding
+    for code in (0, -1, -2, -3, -4, -5):
+        s = binding.strerror(code)
+        assert s and s != "unknown error code"
+    assert binding.strerror(-99) == "unknown error code"
+
+
+FAKE = 0x10000  # a 16-byte aligned address that is never dereferenced: validation fails first
+
+
+def _fwd(lib, shape, **ptrs):
+    from bwd_tri_attn_gb300.binding import Shape
+    names = ["Q", "K", "V", "bias", "mask", "O", "LSE", "Ores"]
+    args = [ctypes.c_void_p(ptrs.get(n, FAKE)) for n in names]
+    return lib.tri_attn_fwd(Shape(*shape), *args, None)
+
+
+def _bwd(lib, shape, ws_bytes, **ptrs):
+    from bwd_tri_attn_gb300.binding import Shape
+    names = ["Q", "K", "V", "bias", "mask", "O", "Ores", "LSE", "dO", "dQ", "dK", "dV", "dBias", "ws"]
+    args = [ctypes.c_void_p(ptrs.get(n, FAKE)) for n in names]
+    return lib.tri_attn_bwd(Shape(*shape), *args, ctypes.c_size_t(ws_bytes), None)
+
+
+GOOD = (1, 4, 64, 2, 32, 0.17677669)
+
+
+@pytest.mark.parametrize("shape,code", [
+    ((0, 4, 64, 2, 32, 0.1), -1),          # empty batch
+    ((1, 0, 64, 2, 32, 0.1), -1),          # no slices
+    ((1, 4, 0, 2, 32, 0.1), -1),           # no positions
+    ((1, 4, 64, 0, 32, 0.1), -1),          # no heads
+    ((1, 4, 64, 2, 32, float("nan")), -1),  # non-finite scale
+    ((1, 4, 64, 2, 24, 0.1), -2),          # unsupported head dim
+    ((1, 4, 64, 2, 64, 0.1), -2),
+    ((1, 4, 1025, 2, 32, 0.1), -2),        # N above the limit
+])
+def test_shape_validation(lib, shape, code):
+    assert _fwd(lib, shape) == code
+    assert _bwd(lib, shape, 1 << 40) == code
+
+
+@pytest.mark.parametrize("name", ["Q", "K", "V", "bias", "O", "LSE"])
+def test_fwd_null_required_pointer(lib, name):
+    assert _fwd(lib, GOOD, **{name: 0}) == -1
+
+
+@pytest.mark.parametrize("name", ["Q", "K", "V", "bias", "mask", "O", "LSE", "Ores"])
+def test_fwd_misaligned_pointer(lib, name):
+    assert _fwd(lib, GOOD, **{name: FAKE + 2}) == -2
+
+
+@pytest.mark.parametrize("name", ["Q", "K", "V", "bias", "O", "LSE", "dO", "dQ", "dK", "dV", "dBias"])
+def test_bwd_null_required_pointer(lib, name):
+    assert _bwd(lib, GOOD, 1 << 40, **{name: 0}) == -1
+
+
+def test_bwd_workspace_checks(lib):
+    from bwd_tri_attn_gb300.binding import Shape
+    need = lib.tri_attn_bwd_workspace_size(Shape(*GOOD))
+    assert need > 0
+    assert _bwd(lib, GOOD, need - 1) == -3
+    assert _bwd(lib, GOOD, need, ws=0) == -3
+    assert _bwd(lib, GOOD, need, ws=FAKE + 8) == -2
+
+
+def test_workspace_size_depends_on_shape_only(lib):
+    from bwd_tri_attn_gb300.binding import Shape
+    a = lib.tri_attn_bwd_workspace_size(Shape(1, 768, 768, 4, 32, 0.1))
+    b = lib.tri_attn_bwd_workspace_size(Shape(1, 768, 768, 4, 32, 0.5))
+    assert a == b and a > 0
+    assert lib.tri_attn_bwd_workspace_size(Shape(1, 768, 768, 4, 24, 0.1)) == 0
+    # at least the FP32 correction D [B,S,H,N]
+    assert a >= 4 * 768 * 4 * 768
+
+
+def test_timing_events_validation(lib):
+    assert lib.tri_attn_set_timing_events(None, -1) == -1
+    assert lib.tri_attn_set_timing_events(None, 0) == 0

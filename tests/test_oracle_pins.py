@@ -213,3 +213,14 @@ def test_golden_regression_fixture():
     got = compute()
     for k in want:
         np.testing.assert_allclose(np.array(got[k]), np.array(want[k]), rtol=1e-14, atol=1e-15, err_msg=k)
+
+
+def test_dbias_rows_agree_with_torch_autograd():
+    # the row-wise dBias routine (used at sizes where the full backward is too slow)
+    Q, K, V, bias, mask, dO = _rand_case(2, 6, 7, 2, 3, seed=21, masked_keys=[(0, 2, 6), (1, 5, 0)])
+    o, (q, k, v, bb) = _sdpa_reference(Q, K, V, bias, mask, 1.0 / math.sqrt(3), need_grad=True)
+    (o * torch.tensor(dO)).sum().backward()
+    rows = [(0, 0, 0), (0, 1, 6), (1, 1, 3), (1, 0, 5)]
+    got = oracle.dbias_rows(Q, K, V, bias, mask, dO, rows)
+    for r, (b, h, j) in enumerate(rows):
+        np.testing.assert_allclose(got[r], bb.grad.numpy()[b, h, j], rtol=1e-10, atol=1e-12)
