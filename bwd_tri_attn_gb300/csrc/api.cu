@@ -11,6 +11,9 @@ cudaError_t launch_bwd_d(const Dims &g, const uint16_t *dO, const uint16_t *O, c
                          float *Dout, cudaStream_t stream);
 cudaError_t launch_dbias_reduce(const float *partial, int G, int64_t elems, uint16_t *dBias,
                                 cudaStream_t stream);
+cudaError_t launch_fwd(const Dims &g, const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                       const uint16_t *bias, const uint16_t *mask, uint16_t *O, float *LSE, uint16_t *Ores,
+                       int *status, cudaStream_t stream);
 cudaError_t launch_simt_fwd(const Dims &g, const uint16_t *Q, const uint16_t *K, const uint16_t *V,
                             const uint16_t *bias, const uint16_t *mask, uint16_t *O, float *LSE,
                             uint16_t *Ores, cudaStream_t stream);
@@ -64,6 +67,21 @@ WorkspaceLayout layout_for(const tri_attn_shape &s) {
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? TRI_ATTN_OK : TRI_ATTN_ERR_CUDA; }
 
+// Device address of the status word on the current device (looked up once per device).
+int *status_word() {
+  static std::mutex mu;
+  static int *addr[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_tri_attn_status) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<int *>(p);
+  }
+  return addr[dev];
+}
+
 // Optional per-kernel timing events of the calling host thread.
 thread_local void *const *t_events = nullptr;
 thread_local int t_nevents = 0;
@@ -101,7 +119,9 @@ int tri_attn_fwd(tri_attn_shape shape, const tri_attn_bf16 *Q, const tri_attn_bf
     if (p && !aligned16(p)) return TRI_ATTN_ERR_UNSUPPORTED;
   const Dims g = to_dims(shape);
   auto st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_simt_fwd(g, Q, K, V, bias, mask, O, LSE, Ores, st);
+  int *status = status_word();
+  if (!status) return TRI_ATTN_ERR_CUDA;
+  cudaError_t e = launch_fwd(g, Q, K, V, bias, mask, O, LSE, Ores, status, st);
   if (e == cudaSuccess) e = mark(0, st);
   return cuda_rc(e);
 }

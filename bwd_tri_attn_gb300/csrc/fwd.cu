@@ -1,0 +1,495 @@
+// Forward pass: tcgen05/TMEM flash-style kernel with the pair bias staged in
+// shared memory and reused across the slices of a CTA.
+//
+// TurboPairFormer (arXiv 2610.05854v1, Abstract): each row-slice of the pair
+// tensor runs attention with a pair bias shared by all slices; the forward
+// keeps BF16 outputs and, for the backward correction, a BF16 approximation of
+// the output-rounding residual (O_fp32 - bf16(O)), without changing O.
+//
+// Work unit (one CTA): batch b, head h, query tile jt (128 rows), and a group
+// of GF consecutive slices. For every key tile kt the bias tile
+// bias[b,h,jt,kt] is brought into shared memory once (each softmax thread
+// stages and converts its own query row) and used for all GF slices:
+//   S_i  = Q_i K_i^T           tcgen05 (BF16 x BF16 -> FP32 TMEM), M=128, N=128
+//   P_i  = exp2(S_i*scale*log2e + bias*log2e - m_i)   online softmax, FP32
+//   O_i += P_i V_i             tcgen05 (P: FP16 in TMEM as the A operand, V: FP16)
+// P is rounded to FP16 (11-bit significand) rather than BF16: a second BF16
+// rounding on the output's path would add as much error as the output rounding
+// itself. V is converted BF16 -> FP16 in shared memory (exact in FP16 range).
+//
+// Warp roles (192 threads): warps 0-3 = softmax (thread = query row = TMEM
+// lane), warp 4 = TMA producer + V conversion, warp 5 = MMA issuer + TMEM owner.
+// TMEM columns: S double buffer [0,128) [128,256); O_i at 256 + i*d.
+// The online max is updated lazily (only when it grows by more than 2^8), and
+// O is rescaled in TMEM only then.
+#include "common.cuh"
+#include "sm100.cuh"
+#include "sync.cuh"
+#include "tmap.cuh"
+
+namespace triattn {
+using namespace sm100;
+
+template <int HD>
+struct FwdCfg {
+  static constexpr int GF = HD == 32 ? 4 : 8;  // slices per CTA
+  static constexpr int NST = 4;                // K/V pipeline stages
+  static constexpr int ROWB = HD * 2;          // bytes of one operand row
+  static constexpr int TILE = 128 * ROWB;      // bytes of one 128-row operand tile
+  static constexpr uint32_t SW = HD == 32 ? kSwizzle64B : kSwizzle32B;
+  static constexpr int NMAX = TRI_ATTN_MAX_N;
+  static constexpr int MAXKT = NMAX / 128;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + GF * TILE;
+  static constexpr int OFF_V = OFF_K + NST * TILE;
+  static constexpr int OFF_BF = OFF_V + NST * TILE;         // FP32 bias*log2e rows: 128 x 512 B
+  static constexpr int OFF_BS = OFF_BF + 128 * 512;         // BF16 bias staging rows: 128 x 256 B
+  static constexpr int OFF_MASK = OFF_BS + 128 * 256;       // FP32 mask*log2e [GF][NMAX]
+  static constexpr int OFF_FLAG = OFF_MASK + GF * NMAX * 4; // int [GF][MAXKT]: tile has a nonzero mask
+  static constexpr int OFF_BAR = OFF_FLAG + GF * MAXKT * 4;
+  // barrier indices
+  static constexpr int B_Q = 0;
+  static constexpr int B_KVFULL = 1;
+  static constexpr int B_VREADY = B_KVFULL + NST;
+  static constexpr int B_KVEMPTY = B_VREADY + NST;
+  static constexpr int B_SFULL = B_KVEMPTY + NST;
+  static constexpr int B_PFULL = B_SFULL + 2;
+  static constexpr int B_SFREE = B_PFULL + 2;
+  static constexpr int B_PVDONE = B_SFREE + 2;
+  static constexpr int B_OFINAL = B_PVDONE + GF;
+  static constexpr int NBAR = B_OFINAL + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // [0] TMEM base, [1] abort flag
+  static constexpr int SMEM_ALLOC = OFF_MISC + 16 + 1024;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static_assert(256 + GF * HD <= 512, "TMEM budget");
+  static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+};
+
+// Waits on an mbarrier with every lane of the warp; true only if all lanes succeeded.
+__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, const Abort &ab) {
+  const bool ok = wait_bar(bar, parity, ab);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Bounded wait used at teardown: ignores the abort flag (it only drains work in flight).
+__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+}
+
+template <int HD>
+__global__ void __launch_bounds__(192, 1)
+fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
+           const __grid_constant__ CUtensorMap mV, const Dims g, const uint16_t *__restrict__ bias,
+           const uint16_t *__restrict__ mask, uint16_t *__restrict__ O, float *__restrict__ LSE,
+           uint16_t *__restrict__ Ores, int *status) {
+  using C = FwdCfg<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb0 = smem_u32(sm);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int jt = blockIdx.x, h = blockIdx.y;
+  const int ngroups = (g.S + C::GF - 1) / C::GF;
+  const int b = blockIdx.z / ngroups, i0 = (blockIdx.z % ngroups) * C::GF;
+  const int ng = min(C::GF, g.S - i0);
+  const int nkt = (g.N + 127) / 128;
+  const int T = nkt * ng;
+  auto bar = [&](int k) { return sb0 + C::OFF_BAR + 8u * (uint32_t)k; };
+  volatile uint32_t *misc = reinterpret_cast<volatile uint32_t *>(sm + C::OFF_MISC);
+  const Abort ab{reinterpret_cast<volatile int *>(misc + 1), status};
+
+  if (tid == 0) {
+    mbar_init(bar(C::B_Q), 1);
+    for (int s = 0; s < C::NST; ++s) {
+      mbar_init(bar(C::B_KVFULL + s), 1);
+      mbar_init(bar(C::B_VREADY + s), 1);
+      mbar_init(bar(C::B_KVEMPTY + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(C::B_SFULL + s), 1);
+      mbar_init(bar(C::B_PFULL + s), 128);
+      mbar_init(bar(C::B_SFREE + s), 1);
+    }
+    for (int s = 0; s < C::GF; ++s) mbar_init(bar(C::B_PVDONE + s), 1);
+    mbar_init(bar(C::B_OFINAL), 1);
+    misc[1] = 0;
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(sb0 + C::OFF_MISC, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = misc[0];
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    int issued = 0;
+    if (lane == 0) {
+      tma_prefetch_map(&mQ);
+      tma_prefetch_map(&mK);
+      tma_prefetch_map(&mV);
+      mbar_arrive_expect_tx(bar(C::B_Q), ng * C::TILE);
+      for (int il = 0; il < ng; ++il)
+        tma_load_4d(sb0 + C::OFF_Q + il * C::TILE, &mQ, bar(C::B_Q), 0, h, jt * 128, b * g.S + i0 + il);
+    }
+    constexpr int LAG = C::NST - 1;
+    bool ok = true;
+    for (int t = 0; t < T + LAG && ok; ++t) {
+      if (t < T) {
+        const int st = t % C::NST, use = t / C::NST;
+        if (use > 0) ok = wait_bar_warp(bar(C::B_KVEMPTY + st), (use - 1) & 1, ab);
+        if (!ok) break;
+        if (lane == 0) {
+          const int kt = t / ng, il = t % ng;
+          mbar_arrive_expect_tx(bar(C::B_KVFULL + st), 2 * C::TILE);
+          tma_load_4d(sb0 + C::OFF_K + st * C::TILE, &mK, bar(C::B_KVFULL + st), 0, h, kt * 128, b * g.S + i0 + il);
+          tma_load_4d(sb0 + C::OFF_V + st * C::TILE, &mV, bar(C::B_KVFULL + st), 0, h, kt * 128, b * g.S + i0 + il);
+        }
+        issued = t + 1;
+      }
+      const int tc = t - LAG;
+      if (tc >= 0) {
+        const int st = tc % C::NST, use = tc / C::NST;
+        ok = wait_bar_warp(bar(C::B_KVFULL + st), use & 1, ab);
+        if (!ok) break;
+        uint4 *v = reinterpret_cast<uint4 *>(sm + C::OFF_V + st * C::TILE);
+        for (int e = lane; e < C::TILE / 16; e += 32) {
+          uint4 w = v[e];
+          w.x = bf16x2_to_f16x2(w.x);
+          w.y = bf16x2_to_f16x2(w.y);
+          w.z = bf16x2_to_f16x2(w.z);
+          w.w = bf16x2_to_f16x2(w.w);
+          v[e] = w;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::B_VREADY + st));
+      }
+    }
+    if (!ok && lane == 0) {
+      // drain loads still in flight before the CTA's shared memory goes away
+      drain_bar(bar(C::B_Q), 0);
+      for (int t = max(0, issued - C::NST); t < issued; ++t) drain_bar(bar(C::B_KVFULL + t % C::NST), (t / C::NST) & 1);
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_f16(128, 128, true, true, false, false);
+      constexpr uint32_t idPV = idesc_f16(128, HD, false, false, false, true);
+      auto issue_pv = [&](int t) -> bool {
+        const int kt = t / ng, il = t % ng, sbuf = t & 1, st = t % C::NST;
+        if (!wait_bar(bar(C::B_PFULL + sbuf), (t >> 1) & 1, ab)) return false;
+        if (!wait_bar(bar(C::B_VREADY + st), (t / C::NST) & 1, ab)) return false;
+        tc_fence_after();
+        const uint32_t vaddr = sb0 + C::OFF_V + st * C::TILE;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          mma_ts(tbase + 256 + il * HD, tbase + sbuf * 128 + ks * 8,
+                 smem_desc(vaddr + ks * 16 * C::ROWB, 16, 8 * C::ROWB, C::SW), idPV, (kt > 0 || ks > 0) ? 1u : 0u);
+        mma_commit(bar(C::B_SFREE + sbuf));
+        mma_commit(bar(C::B_KVEMPTY + st));
+        mma_commit(bar(C::B_PVDONE + il));
+        return true;
+      };
+      bool ok = wait_bar(bar(C::B_Q), 0, ab);
+      for (int t = 0; t < T && ok; ++t) {
+        const int st = t % C::NST, sbuf = t & 1, il = t % ng;
+        ok = wait_bar(bar(C::B_KVFULL + st), (t / C::NST) & 1, ab);
+        if (ok && t >= 2) ok = wait_bar(bar(C::B_SFREE + sbuf), ((t - 2) >> 1) & 1, ab);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t qaddr = sb0 + C::OFF_Q + il * C::TILE, kaddr = sb0 + C::OFF_K + st * C::TILE;
+#pragma unroll
+        for (int ks = 0; ks < HD / 16; ++ks)
+          mma_ss(tbase + sbuf * 128, smem_desc(qaddr + ks * 32, 16, 8 * C::ROWB, C::SW),
+                 smem_desc(kaddr + ks * 32, 16, 8 * C::ROWB, C::SW), idS, ks > 0 ? 1u : 0u);
+        mma_commit(bar(C::B_SFULL + sbuf));
+        if (t >= 1) ok = issue_pv(t - 1);
+      }
+      if (ok) ok = issue_pv(T - 1);
+      mma_commit(bar(C::B_OFINAL));
+      drain_bar(bar(C::B_OFINAL), 0);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax / epilogue (warps 0-3)
+    const int row = tid;
+    const int j = jt * 128 + row;
+    const int jr = min(j, g.N - 1);  // rows past N reuse a valid bias row; their outputs are dropped
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    float *maskf = reinterpret_cast<float *>(sm + C::OFF_MASK);
+    int *flags = reinterpret_cast<int *>(sm + C::OFF_FLAG);
+    const float c1 = g.scale * kLog2e;
+
+    // per-slice additive mask (log2 units) and per-tile "has a nonzero entry" flags
+    if (mask) {
+      for (int il = 0; il < ng; ++il)
+        for (int k = row; k < nkt * 128; k += 128)
+          maskf[il * C::NMAX + k] =
+              k < g.N ? bf16_to_f32(mask[((int64_t)b * g.S + i0 + il) * g.N + k]) * kLog2e : 0.f;
+    }
+    named_sync(1, 128);
+    if (row < C::GF * C::MAXKT) {
+      const int il = row / C::MAXKT, kt = row % C::MAXKT;
+      int f = 0;
+      if (mask && il < ng && kt < nkt)
+        for (int k = 0; k < 128; ++k) f |= (maskf[il * C::NMAX + kt * 128 + k] != 0.f);
+      flags[row] = f;
+    }
+    named_sync(1, 128);
+
+    const uint16_t *brow = bias + (((int64_t)b * g.H + h) * g.N + jr) * g.N;
+    const uint32_t stage_row = sb0 + C::OFF_BS + row * 256;
+    const uint32_t sw = row & 7;
+    auto stage_bias = [&](int kt) {
+      const int k0 = kt * 128, nv = min(128, g.N - k0);
+      const uint16_t *src = brow + k0;
+      if ((g.N & 7) == 0) {
+        for (int c = 0; c < nv / 8; ++c) cp_async_16(stage_row + ((c ^ sw) << 4), src + c * 8);
+      } else if ((g.N & 1) == 0) {
+        for (int p = 0; p < nv / 2; ++p) cp_async_4(stage_row + (((p >> 2) ^ sw) << 4) + (p & 3) * 4, src + 2 * p);
+      } else {
+        for (int e = 0; e < nv; ++e) {
+          const uint16_t v = src[e];
+          asm volatile("st.shared.u16 [%0], %1;" ::"r"(stage_row + (((e >> 3) ^ sw) << 4) + (e & 7) * 2), "h"(v));
+        }
+      }
+      cp_async_commit();
+    };
+    const uint32_t bf_row = sb0 + C::OFF_BF + row * 512;
+    auto convert_bias = [&](int kt) {
+      const int nv = min(128, g.N - kt * 128);
+#pragma unroll 4
+      for (int c = 0; c < 16; ++c) {
+        uint32_t w[4];
+        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                     : "r"(stage_row + ((c ^ sw) << 4)));
+        float f[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          f[2 * q] = __uint_as_float(w[q] << 16) * kLog2e;
+          f[2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u) * kLog2e;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          if (c * 8 + e >= nv) f[e] = -INFINITY;
+        asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(bf_row + (((2 * c) ^ sw) << 4)), "f"(f[0]),
+                     "f"(f[1]), "f"(f[2]), "f"(f[3])
+                     : "memory");
+        asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(bf_row + (((2 * c + 1) ^ sw) << 4)),
+                     "f"(f[4]), "f"(f[5]), "f"(f[6]), "f"(f[7])
+                     : "memory");
+      }
+    };
+
+    float m_ref[C::GF], l_sum[C::GF];
+#pragma unroll
+    for (int il = 0; il < C::GF; ++il) {
+      m_ref[il] = -INFINITY;
+      l_sum[il] = 0.f;
+    }
+    stage_bias(0);
+    bool ok = true;
+    for (int kt = 0; kt < nkt && ok; ++kt) {
+      cp_async_wait_all();
+      convert_bias(kt);
+      if (kt + 1 < nkt) stage_bias(kt + 1);
+#pragma unroll 1
+      for (int il = 0; il < ng; ++il) {
+        const int t = kt * ng + il, sbuf = t & 1;
+        ok = wait_bar_warp(bar(C::B_SFULL + sbuf), (t >> 1) & 1, ab);
+        if (!ok) break;
+        tc_fence_after();
+        float x[128];
+        {
+          uint32_t r[128];
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4)
+            tmem_ld32(tbase + lane_base + sbuf * 128 + c4 * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[c4 * 32]));
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 128; ++e) x[e] = __uint_as_float(r[e]);
+        }
+        float mt = -INFINITY;
+#pragma unroll
+        for (int ch = 0; ch < 32; ++ch) {
+          float4 bv;
+          asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+                       : "=f"(bv.x), "=f"(bv.y), "=f"(bv.z), "=f"(bv.w)
+                       : "r"(bf_row + ((ch ^ sw) << 4)));
+          x[4 * ch + 0] = fmaf(x[4 * ch + 0], c1, bv.x);
+          x[4 * ch + 1] = fmaf(x[4 * ch + 1], c1, bv.y);
+          x[4 * ch + 2] = fmaf(x[4 * ch + 2], c1, bv.z);
+          x[4 * ch + 3] = fmaf(x[4 * ch + 3], c1, bv.w);
+        }
+        if (flags[il * C::MAXKT + kt]) {
+          const float *mrow = maskf + il * C::NMAX + kt * 128;
+#pragma unroll
+          for (int k = 0; k < 128; ++k) x[k] += mrow[k];
+        }
+#pragma unroll
+        for (int k = 0; k < 128; ++k) mt = fmaxf(mt, x[k]);
+        // lazy online-softmax rescale
+        float alpha = 1.f;
+        bool resc = false;
+        float mr = m_ref[0];
+#pragma unroll
+        for (int q = 1; q < C::GF; ++q)
+          if (q == il) mr = m_ref[q];
+        if (kt == 0) {
+          mr = mt;
+        } else if (mt > mr + 8.f) {
+          if (mr == -INFINITY) {
+            mr = mt;  // O_i and l_i are still exactly zero
+          } else {
+            alpha = ex2(mr - mt);
+            resc = true;
+            mr = mt;
+          }
+        }
+        if (__any_sync(0xffffffffu, resc)) {
+          ok = wait_bar_warp(bar(C::B_PVDONE + il), (kt - 1) & 1, ab);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t oaddr = tbase + lane_base + 256 + il * HD;
+          if constexpr (HD == 32) {
+            uint32_t r[32];
+            tmem_ld32(oaddr, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+            tmem_st32(oaddr, r);
+          } else {
+            uint32_t r[16];
+            tmem_ld16(oaddr, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+            tmem_st16(oaddr, r);
+          }
+        }
+        const float mu = (mr == -INFINITY) ? 0.f : mr;
+        float ls = 0.f;
+        uint32_t pk[64];
+#pragma unroll
+        for (int e = 0; e < 64; ++e) {
+          const float p0 = ex2(x[2 * e] - mu), p1 = ex2(x[2 * e + 1] - mu);
+          ls += p0;
+          ls += p1;
+          pk[e] = pack_f16x2(p0, p1);
+        }
+#pragma unroll
+        for (int q = 0; q < C::GF; ++q)
+          if (q == il) {
+            m_ref[q] = mr;
+            l_sum[q] = l_sum[q] * alpha + ls;
+          }
+        {
+          uint32_t r0[32], r1[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            r0[e] = pk[e];
+            r1[e] = pk[32 + e];
+          }
+          tmem_st32(tbase + lane_base + sbuf * 128, r0);
+          tmem_st32(tbase + lane_base + sbuf * 128 + 32, r1);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(C::B_PFULL + sbuf));
+      }
+    }
+    // epilogue: O = acc / l -> BF16, residual, LSE
+    if (ok) ok = wait_bar_warp(bar(C::B_OFINAL), 0, ab);
+    if (ok) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int il = 0; il < ng; ++il) {
+        float lsum = 0.f, mref = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < C::GF; ++q)
+          if (q == il) {
+            lsum = l_sum[q];
+            mref = m_ref[q];
+          }
+        uint32_t r[32];
+        if constexpr (HD == 32) {
+          tmem_ld32(tbase + lane_base + 256 + il * HD, r);
+        } else {
+          uint32_t r16[16];
+          tmem_ld16(tbase + lane_base + 256 + il * HD, r16);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) r[e] = r16[e];
+        }
+        tmem_wait_ld();
+        if (j < g.N) {
+          const int i = i0 + il;
+          const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+          uint32_t ob[HD / 2], rb[HD / 2];
+#pragma unroll
+          for (int c = 0; c < HD / 2; ++c) {
+            const float o0 = __uint_as_float(r[2 * c]) * inv, o1 = __uint_as_float(r[2 * c + 1]) * inv;
+            const uint16_t a0 = f32_to_bf16_rn(o0), a1 = f32_to_bf16_rn(o1);
+            ob[c] = (uint32_t)a0 | ((uint32_t)a1 << 16);
+            rb[c] = (uint32_t)f32_to_bf16_rn(o0 - bf16_to_f32(a0)) |
+                    ((uint32_t)f32_to_bf16_rn(o1 - bf16_to_f32(a1)) << 16);
+          }
+          const int64_t off = pos_row(g, b, i, j) * g.H * HD + (int64_t)h * HD;
+          uint4 *od = reinterpret_cast<uint4 *>(O + off);
+#pragma unroll
+          for (int c = 0; c < HD / 8; ++c) od[c] = make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
+          if (Ores) {
+            uint4 *rd = reinterpret_cast<uint4 *>(Ores + off);
+#pragma unroll
+            for (int c = 0; c < HD / 8; ++c)
+              rd[c] = make_uint4(rb[4 * c], rb[4 * c + 1], rb[4 * c + 2], rb[4 * c + 3]);
+          }
+          LSE[(((int64_t)b * g.S + i) * g.H + h) * g.N + j] =
+              lsum > 0.f ? (mref + __log2f(lsum)) * kLn2 : -INFINITY;
+        }
+      }
+    }
+    cp_async_wait_all();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tbase, C::TMEM_COLS);
+  }
+}
+
+template <int HD>
+cudaError_t launch_fwd_t(const Dims &g, const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                         const uint16_t *bias, const uint16_t *mask, uint16_t *O, float *LSE, uint16_t *Ores,
+                         int *status, cudaStream_t stream) {
+  using C = FwdCfg<HD>;
+  CUtensorMap mq, mk, mv;
+  cudaError_t e = make_rows_map(&mq, Q, g, 128);
+  if (e == cudaSuccess) e = make_rows_map(&mk, K, g, 128);
+  if (e == cudaSuccess) e = make_rows_map(&mv, V, g, 128);
+  if (e != cudaSuccess) return e;
+  static bool attr = false;
+  if (!attr) {
+    e = cudaFuncSetAttribute(fwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const int ngroups = (g.S + C::GF - 1) / C::GF;
+  dim3 grid((g.N + 127) / 128, g.H, g.B * ngroups);
+  fwd_kernel<HD><<<grid, 192, C::SMEM_ALLOC, stream>>>(mq, mk, mv, g, bias, mask, O, LSE, Ores, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd(const Dims &g, const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                       const uint16_t *bias, const uint16_t *mask, uint16_t *O, float *LSE, uint16_t *Ores,
+                       int *status, cudaStream_t stream) {
+  if (g.d == 32) return launch_fwd_t<32>(g, Q, K, V, bias, mask, O, LSE, Ores, status, stream);
+  return launch_fwd_t<16>(g, Q, K, V, bias, mask, O, LSE, Ores, status, stream);
+}
+
+}  // namespace triattn

@@ -1,0 +1,41 @@
+// Bounded waits for the warp-specialised kernels.
+//
+// Every spin on an mbarrier has a time limit. When it expires the waiting
+// thread raises the CTA's shared abort flag and the library's device status
+// word, and returns false; every other wait in the CTA then sees the abort flag
+// and returns false at once, so all roles fall through to teardown instead of
+// hanging. The host reads the status word with tri_attn_device_status().
+#pragma once
+
+#include "common.cuh"
+#include "sm100.cuh"
+
+namespace triattn {
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: normal waits last microseconds
+
+struct Abort {
+  volatile int *flag;  // shared memory, one per CTA
+  int *status;         // global device status word
+};
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Abort &ab) {
+  if (sm100::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = sm100::globaltimer_ns();
+  while (true) {
+    if (sm100::mbar_try_wait(bar, parity)) return true;
+    if (*ab.flag) return false;
+    if (sm100::globaltimer_ns() - t0 > kWaitLimitNs) {
+      *ab.flag = 1;
+      atomicExch(ab.status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
+// Named barrier over `count` threads (id 1..15; id 0 is __syncthreads).
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+}  // namespace triattn

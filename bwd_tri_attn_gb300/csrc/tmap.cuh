@@ -1,0 +1,45 @@
+// Host-side TMA tensor-map construction for the [B,S,N,H,d] activations.
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace triattn {
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// 4-D view (d, H, N, B*S) of a BF16 [B,S,N,H,d] tensor; one TMA box is `rows`
+// consecutive positions of one (b, slice, head): `rows` x d elements, swizzled
+// to the operand layout (SW64 for d = 32: 64-byte rows; SW32 for d = 16).
+// Positions past N read as zeros.
+inline cudaError_t make_rows_map(CUtensorMap *m, const void *ptr, const Dims &g, int rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t e = 2;  // bytes per element
+  cuuint64_t dims[4] = {(cuuint64_t)g.d, (cuuint64_t)g.H, (cuuint64_t)g.N, (cuuint64_t)g.B * g.S};
+  cuuint64_t strides[3] = {e * g.d, e * g.d * g.H, e * g.d * g.H * g.N};
+  cuuint32_t box[4] = {(cuuint32_t)g.d, 1, (cuuint32_t)rows, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  const CUtensorMapSwizzle sw = g.d == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace triattn

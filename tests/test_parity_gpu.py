@@ -66,7 +66,7 @@ def test_parity_full_oracle(name, cfg):
     # Ores carries the output-rounding residual: O + Ores is closer to the exact output
     e_plain = rmse_rel(f64(got["O"]), want["O"])
     e_comp = rmse_rel(f64(got["O"]) + f64(got["Ores"]), want["O"])
-    assert e_comp < 0.1 * e_plain
+    assert e_comp < 0.2 * e_plain
 
 
 def test_fully_masked_slice():
