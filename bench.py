@@ -30,7 +30,7 @@ UNIT = "TFLOP/s"
 L2_BYTES = 129 * 2**20
 
 # Kernels each step enqueues, in order (the library's per-kernel event order).
-KERNELS = ["fwd", "bwd_d", "bwd_main", "dbias_reduce"]
+KERNELS = ["fwd", "bias_transpose", "bwd_d", "bwd_main", "dbias_reduce"]
 
 
 def load_peaks():

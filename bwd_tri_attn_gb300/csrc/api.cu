@@ -7,20 +7,19 @@
 #include "common.cuh"
 
 namespace triattn {
-cudaError_t launch_bwd_d(const Dims &g, const uint16_t *dO, const uint16_t *O, const uint16_t *Ores,
-                         float *Dout, cudaStream_t stream);
-cudaError_t launch_dbias_reduce(const float *partial, int G, int64_t elems, uint16_t *dBias,
-                                cudaStream_t stream);
 cudaError_t launch_fwd(const Dims &g, const uint16_t *Q, const uint16_t *K, const uint16_t *V,
                        const uint16_t *bias, const uint16_t *mask, uint16_t *O, float *LSE, uint16_t *Ores,
                        int *status, cudaStream_t stream);
-cudaError_t launch_simt_fwd(const Dims &g, const uint16_t *Q, const uint16_t *K, const uint16_t *V,
-                            const uint16_t *bias, const uint16_t *mask, uint16_t *O, float *LSE,
-                            uint16_t *Ores, cudaStream_t stream);
-cudaError_t launch_simt_bwd(const Dims &g, int G, const uint16_t *Q, const uint16_t *K,
-                            const uint16_t *V, const uint16_t *bias, const uint16_t *mask,
-                            const float *LSE, const float *Dv, const uint16_t *dO, uint16_t *dQ,
-                            uint16_t *dK, uint16_t *dV, float *partial, cudaStream_t stream);
+cudaError_t launch_bwd_d(const Dims &g, const uint16_t *dO, const uint16_t *O, const uint16_t *Ores,
+                         float *Dout, cudaStream_t stream);
+cudaError_t launch_bias_transpose(const Dims &g, const uint16_t *bias, uint16_t *biasT, cudaStream_t stream);
+cudaError_t launch_bwd_main(const Dims &g, int Gp, const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                            const uint16_t *biasT, const uint16_t *mask, const float *LSE, const float *Dv,
+                            const uint16_t *dO, uint16_t *dQ, uint16_t *dK, uint16_t *dV, float *partial,
+                            int *status, cudaStream_t stream);
+cudaError_t launch_dbias_reduce_t(const Dims &g, int Gp, const float *partial, uint16_t *dBias,
+                                  cudaStream_t stream);
+int bwd_groups(const Dims &g);
 }  // namespace triattn
 
 using namespace triattn;
@@ -47,21 +46,24 @@ int check_shape(const tri_attn_shape &s) {
 
 Dims to_dims(const tri_attn_shape &s) { return Dims{s.B, s.S, s.N, s.H, s.d, s.scale}; }
 
-// Number of slice groups whose dBias partials the backward pass keeps.
-int dbias_groups(const tri_attn_shape &s) { return s.S < 32 ? s.S : 32; }
-
+// Backward workspace: the FP32 correction D [B,S,H,N], the transposed and
+// tile-padded BF16 bias [B*H][NP][NP] (NP = N rounded up to 128), and one FP32
+// dBias partial [B*H][NP][NP] per slice supergroup.
 struct WorkspaceLayout {
-  size_t d_off, partial_off, total;
+  size_t d_off, biast_off, partial_off, total;
   int groups;
 };
 
 WorkspaceLayout layout_for(const tri_attn_shape &s) {
   WorkspaceLayout w;
+  const Dims g = to_dims(s);
+  const size_t NP = (size_t)(s.N + 127) / 128 * 128;
   const size_t rows = (size_t)s.B * s.S * s.H * s.N;
-  w.groups = dbias_groups(s);
+  w.groups = bwd_groups(g);
   w.d_off = 0;
-  w.partial_off = align_up(sizeof(float) * rows);
-  w.total = w.partial_off + align_up(sizeof(float) * (size_t)w.groups * s.B * s.H * s.N * s.N);
+  w.biast_off = align_up(sizeof(float) * rows);
+  w.partial_off = w.biast_off + align_up(2 * (size_t)s.B * s.H * NP * NP);
+  w.total = w.partial_off + align_up(sizeof(float) * (size_t)w.groups * s.B * s.H * NP * NP);
   return w;
 }
 
@@ -149,15 +151,19 @@ int tri_attn_bwd(tri_attn_shape shape, const tri_attn_bf16 *Q, const tri_attn_bf
   auto st = static_cast<cudaStream_t>(stream);
   char *ws = static_cast<char *>(workspace);
   float *Dv = reinterpret_cast<float *>(ws + w.d_off);
+  uint16_t *biasT = reinterpret_cast<uint16_t *>(ws + w.biast_off);
   float *partial = reinterpret_cast<float *>(ws + w.partial_off);
-  cudaError_t e = launch_bwd_d(g, dO, O, Ores, Dv, st);
+  int *status = status_word();
+  if (!status) return TRI_ATTN_ERR_CUDA;
+  cudaError_t e = launch_bias_transpose(g, bias, biasT, st);
   if (e == cudaSuccess) e = mark(0, st);
-  if (e == cudaSuccess)
-    e = launch_simt_bwd(g, w.groups, Q, K, V, bias, mask, LSE, Dv, dO, dQ, dK, dV, partial, st);
+  if (e == cudaSuccess) e = launch_bwd_d(g, dO, O, Ores, Dv, st);
   if (e == cudaSuccess) e = mark(1, st);
   if (e == cudaSuccess)
-    e = launch_dbias_reduce(partial, w.groups, (int64_t)shape.B * shape.H * shape.N * shape.N, dBias, st);
+    e = launch_bwd_main(g, w.groups, Q, K, V, biasT, mask, LSE, Dv, dO, dQ, dK, dV, partial, status, st);
   if (e == cudaSuccess) e = mark(2, st);
+  if (e == cudaSuccess) e = launch_dbias_reduce_t(g, w.groups, partial, dBias, st);
+  if (e == cudaSuccess) e = mark(3, st);
   return cuda_rc(e);
 }
 

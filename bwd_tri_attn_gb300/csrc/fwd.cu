@@ -65,19 +65,6 @@ struct FwdCfg {
   static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 };
 
-// Waits on an mbarrier with every lane of the warp; true only if all lanes succeeded.
-__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, const Abort &ab) {
-  const bool ok = wait_bar(bar, parity, ab);
-  return __all_sync(0xffffffffu, ok);
-}
-
-// Bounded wait used at teardown: ignores the abort flag (it only drains work in flight).
-__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity))
-    if (globaltimer_ns() - t0 > kWaitLimitNs) break;
-}
-
 template <int HD>
 __global__ void __launch_bounds__(192, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,

@@ -33,6 +33,34 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ab
   }
 }
 
+// As wait_bar, with acquire at cluster scope (for barriers that peer CTAs arrive on).
+__device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity, const Abort &ab) {
+  if (sm100::mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = sm100::globaltimer_ns();
+  while (true) {
+    if (sm100::mbar_try_wait_cluster(bar, parity)) return true;
+    if (*ab.flag) return false;
+    if (sm100::globaltimer_ns() - t0 > kWaitLimitNs) {
+      *ab.flag = 1;
+      atomicExch(ab.status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
+// Waits on an mbarrier with every lane of the warp; true only if all lanes succeeded.
+__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, const Abort &ab) {
+  const bool ok = wait_bar(bar, parity, ab);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Bounded wait used at teardown: ignores the abort flag (it only drains work in flight).
+__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = sm100::globaltimer_ns();
+  while (!sm100::mbar_try_wait(bar, parity))
+    if (sm100::globaltimer_ns() - t0 > kWaitLimitNs) break;
+}
+
 // Named barrier over `count` threads (id 1..15; id 0 is __syncthreads).
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

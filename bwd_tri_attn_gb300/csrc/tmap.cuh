@@ -42,4 +42,19 @@ inline cudaError_t make_rows_map(CUtensorMap *m, const void *ptr, const Dims &g,
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// 3-D view (j, k, b*H + h) of a BF16 [B*H, NP, NP] square matrix stack with
+// NP a multiple of 128; one box is 64 columns x 128 rows, 128-byte swizzled.
+inline cudaError_t make_square_map(CUtensorMap *m, const void *ptr, int NP, int BH) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  cuuint64_t dims[3] = {(cuuint64_t)NP, (cuuint64_t)NP, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {2ull * NP, 2ull * NP * NP};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace triattn
