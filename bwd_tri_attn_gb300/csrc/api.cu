@@ -20,6 +20,7 @@ cudaError_t launch_bwd_main(const Dims &g, int Gp, const uint16_t *Q, const uint
 cudaError_t launch_dbias_reduce_t(const Dims &g, int Gp, const float *partial, uint16_t *dBias,
                                   cudaStream_t stream);
 int bwd_groups(const Dims &g);
+int bwd_groups_active(const Dims &g);
 }  // namespace triattn
 
 using namespace triattn;
@@ -159,10 +160,11 @@ int tri_attn_bwd(tri_attn_shape shape, const tri_attn_bf16 *Q, const tri_attn_bf
   if (e == cudaSuccess) e = mark(0, st);
   if (e == cudaSuccess) e = launch_bwd_d(g, dO, O, Ores, Dv, st);
   if (e == cudaSuccess) e = mark(1, st);
+  const int groups = bwd_groups_active(g);  // <= w.groups, the workspace bound
   if (e == cudaSuccess)
-    e = launch_bwd_main(g, w.groups, Q, K, V, biasT, mask, LSE, Dv, dO, dQ, dK, dV, partial, status, st);
+    e = launch_bwd_main(g, groups, Q, K, V, biasT, mask, LSE, Dv, dO, dQ, dK, dV, partial, status, st);
   if (e == cudaSuccess) e = mark(2, st);
-  if (e == cudaSuccess) e = launch_dbias_reduce_t(g, w.groups, partial, dBias, st);
+  if (e == cudaSuccess) e = launch_dbias_reduce_t(g, groups, partial, dBias, st);
   if (e == cudaSuccess) e = mark(3, st);
   return cuda_rc(e);
 }

@@ -22,9 +22,12 @@
 //
 // Three reductions, each in a fixed order:
 //  - dK, dV over query tiles: in the CTA's TMEM accumulator, jt = 0, 1, ...
-//  - dQ over key tiles: the N/128 CTAs of one (b, h, supergroup) form a thread-block
-//    cluster; every step each CTA puts its 128 x d FP32 partial in shared memory and
-//    CTA r sums rows [r*128/n, (r+1)*128/n) over the cluster in rank (= kt) order.
+//  - dQ over key tiles: the n = N/128 CTAs of one (b, h, supergroup) form a
+//    thread-block cluster. CTA r owns query rows [r*128/n, (r+1)*128/n) of every
+//    step's tile; each CTA pushes the matching rows of its 128 x d FP32 partial
+//    into the owner's receive buffer with st.async (completing bytes on the
+//    owner's mbarrier), and the owner sums the n partials in rank (= kt) order,
+//    one step later so that the exchange overlaps the next step's work.
 //  - dBias over slices: within a block in slice order (registers), across blocks in
 //    block order (the partial), across supergroups in supergroup order (reduce kernel).
 // Every order depends on the shape only.
@@ -64,8 +67,9 @@ struct BwdCfg {
   static constexpr int OFF_DO = OFF_Q + NQS * TILE;
   static constexpr int OFF_BIAS = OFF_DO + NQS * TILE;     // 2 x [2 halves][128 rows][128 B], SW128
   static constexpr int OFF_DS = OFF_BIAS + 2 * BIAS_TILE;  // FP16 dS, MN-major SW128: [16 key groups][2][8][128 B]
-  static constexpr int OFF_X = OFF_DS + 32768;             // dQ partial: [128 queries][HD] FP32, chunk-swizzled
-  static constexpr int OFF_LSE = OFF_X + 128 * HD * 4;     // [NQS][128]: -LSE*log2e (or -inf)
+  static constexpr int RB_ROWS = 136;                      // >= n * ceil(128 / n) for every cluster size n <= 8
+  static constexpr int OFF_RB = OFF_DS + 32768;            // dQ receive buffer: [sender][row][HD] FP32
+  static constexpr int OFF_LSE = OFF_RB + RB_ROWS * HD * 4; // [NQS][128]: -LSE*log2e (or -inf)
   static constexpr int OFF_D = OFF_LSE + NQS * 512;        // [NQS][128]: D
   static constexpr int OFF_MASK = OFF_D + NQS * 512;       // [GB][128]: mask*log2e of this CTA's keys
   static constexpr int OFF_BAR = OFF_MASK + GB * 512;
@@ -74,7 +78,7 @@ struct BwdCfg {
   static constexpr int B_BFULL = B_QDOFREE + NQS, B_BFREE = B_BFULL + 2;
   static constexpr int B_SFULL = B_BFREE + 2, B_PFULL = B_SFULL + 1, B_M2DONE = B_PFULL + 1;
   static constexpr int B_DQREAD = B_M2DONE + 1, B_DKVREAD = B_DQREAD + 1;
-  static constexpr int B_XFULL = B_DKVREAD + 1, B_XEMPTY = B_XFULL + 1, B_FINAL = B_XEMPTY + 1;
+  static constexpr int B_RFULL = B_DKVREAD + 1, B_XEMPTY = B_RFULL + 1, B_FINAL = B_XEMPTY + 1;
   static constexpr int NBAR = B_FINAL + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_ALLOC = OFF_MISC + 16 + 1024;
@@ -84,13 +88,14 @@ struct BwdCfg {
   static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 };
 
-// Number of slice supergroups (dBias partials) for a shape: enough clusters of
-// N/128 CTAs to fill ~144 SMs once, never more than the number of slice blocks.
-inline int bwd_supergroups(const Dims &g) {
+// Upper bound on the number of slice supergroups (dBias partials) for a shape:
+// clusters of N/128 CTAs filling at most 152 SMs once, never more than the
+// number of slice blocks. The workspace is sized for this bound.
+inline int bwd_supergroups_max(const Dims &g) {
   const int nkt = (g.N + 127) / 128;
   const int gb = g.d == 32 ? BwdCfg<32>::GB : BwdCfg<16>::GB;
   const int blocks = (g.S + gb - 1) / gb;
-  int gp = 144 / (nkt * g.B * g.H);
+  int gp = 152 / (nkt * g.B * g.H);
   if (gp < 1) gp = 1;
   if (gp > blocks) gp = blocks;
   return gp;
@@ -155,8 +160,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
     mbar_init(bar(C::B_M2DONE), 1);
     mbar_init(bar(C::B_DQREAD), C::NEWT);
     mbar_init(bar(C::B_DKVREAD), C::NEWT);
-    mbar_init(bar(C::B_XFULL), C::NEW * nkt);
-    mbar_init(bar(C::B_XEMPTY), C::NEW * nkt);
+    mbar_init(bar(C::B_RFULL), 1);             // + the bytes pushed by all n senders
+    mbar_init(bar(C::B_XEMPTY), C::NEW * nkt);  // one arrive per elementwise warp of every owner
     mbar_init(bar(C::B_FINAL), 1);
     misc[1] = 0;
     fence_barrier_init();
@@ -191,17 +196,20 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
           if (!ok) break;
           float *sl = reinterpret_cast<float *>(sm + C::OFF_LSE + st * 512);
           float *sd = reinterpret_cast<float *>(sm + C::OFF_D + st * 512);
-          for (int q = lane; q < 128; q += 32) {
-            const int j = jt * 128 + q;
-            float uu = -INFINITY, dd = 0.f;
-            if (j < g.N) {
-              const int64_t li = (((int64_t)b * g.S + i) * g.H + h) * g.N + j;
-              const float l = LSE[li];
-              uu = (l == -INFINITY) ? -INFINITY : -l * kLog2e;
-              dd = Dv[li];
+          {
+            float lv[4], dvv[4];
+            const int64_t lrow = (((int64_t)b * g.S + i) * g.H + h) * g.N;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {  // all loads first: one memory round trip
+              const int j = jt * 128 + lane + 32 * m;
+              lv[m] = j < g.N ? LSE[lrow + j] : -INFINITY;
+              dvv[m] = j < g.N ? Dv[lrow + j] : 0.f;
             }
-            sl[q] = uu;
-            sd[q] = dd;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              sl[lane + 32 * m] = (lv[m] == -INFINITY) ? -INFINITY : -lv[m] * kLog2e;
+              sd[lane + 32 * m] = dvv[m];
+            }
           }
           __syncwarp();
           if (lane == 0) {
@@ -318,6 +326,41 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
       mbar_arrive(bar(C::B_QDOREADY + st));
       return true;
     };
+    // owner side of the dQ exchange: rows [r0, r1) of every step's tile
+    const int rows_max = (128 + nkt - 1) / nkt;
+    const uint32_t rb_bytes = (uint32_t)(nkt * (r1 - r0) * HD * 4);
+    int prev_i = 0, prev_jt = 0, red = 0;  // red = steps reduced so far
+    if (tid == 0) mbar_arrive_expect_tx(bar(C::B_RFULL), rb_bytes);  // arm step 0
+    auto reduce_prev = [&]() -> bool {
+      if (!wait_bar_cluster_warp(bar(C::B_RFULL), red & 1, ab)) return false;
+      if (tid == 0 && red + 1 < T) mbar_arrive_expect_tx(bar(C::B_RFULL), rb_bytes);  // arm the next step
+      constexpr int CPR = HD / 4;
+      const int items = (r1 - r0) * CPR;
+      const float *rb = reinterpret_cast<const float *>(sm + C::OFF_RB);
+      for (int it = tid; it < items; it += C::NEWT) {
+        const int rl = it / CPR, c = it % CPR;
+        float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int r = 0; r < nkt; ++r) {  // fixed order: key tile 0, 1, ..., n-1
+          const float4 v = *reinterpret_cast<const float4 *>(rb + ((r * rows_max + rl) * HD + c * 4));
+          s4.x += v.x;
+          s4.y += v.y;
+          s4.z += v.z;
+          s4.w += v.w;
+        }
+        const int j = prev_jt * 128 + r0 + rl;
+        if (j < g.N) {
+          const uint2 o = make_uint2(
+              (uint32_t)f32_to_bf16_rn(s4.x * g.scale) | ((uint32_t)f32_to_bf16_rn(s4.y * g.scale) << 16),
+              (uint32_t)f32_to_bf16_rn(s4.z * g.scale) | ((uint32_t)f32_to_bf16_rn(s4.w * g.scale) << 16));
+          *reinterpret_cast<uint2 *>(dQ + pos_row(g, b, prev_i, j) * g.H * HD + h * HD + c * 4) = o;
+        }
+      }
+      __syncwarp();
+      if (lane == 0)
+        for (int r = 0; r < nkt; ++r) mbar_arrive_cluster_relaxed(mapa_shared(bar(C::B_XEMPTY), r));
+      ++red;
+      return true;
+    };
     float acc[64];
     for (int bi = 0; bi < nblk && ok; ++bi) {
       const int i0 = s0 + bi * C::GB, nb = min(C::GB, s1 - i0);
@@ -400,7 +443,12 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
             ok = convert_qdo(t + 1);
             if (!ok) break;
           }
-          // ---- dQ partial of this step: TMEM lanes = queries
+          // ---- owner duty: reduce the previous step's dQ rows (all n partials have been pushed)
+          if (t > 0) {
+            ok = reduce_prev();
+            if (!ok) break;
+          }
+          // ---- this step's dQ partial: TMEM lanes = queries, this thread has query kl, half of d
           ok = wait_bar_warp(bar(C::B_M2DONE), t & 1, ab);
           if (!ok) break;
           tc_fence_after();
@@ -418,52 +466,25 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
 #pragma unroll
             for (int e = 0; e < 8; ++e) dqv[e] = __uint_as_float(r[e]);
           }
+          tc_fence_before();
+          mbar_arrive(bar(C::B_DQREAD));
+          // every owner has finished reading its receive buffer for the previous step
           if (t > 0) ok = wait_bar_cluster_warp(bar(C::B_XEMPTY), (t - 1) & 1, ab);
           if (!ok) break;
           {
-            constexpr int CPR = HD / 4;  // 16-byte chunks per exchange row
-            const uint32_t xrow = sb0 + C::OFF_X + kl * HD * 4;
+            // push row kl of this partial to its owner: rank o with o*128/n <= kl < (o+1)*128/n
+            int o = (kl * nkt) >> 7;
+            while (o + 1 < nkt && (int)((o + 1) * 128 / nkt) <= kl) ++o;
+            while ((int)(o * 128 / nkt) > kl) --o;
+            const int rl = kl - (int)(o * 128 / nkt);
+            const uint32_t dst = mapa_shared(sb0 + C::OFF_RB + ((rank * rows_max + rl) * HD + half * (HD / 2)) * 4, o);
+            const uint32_t rbar = mapa_shared(bar(C::B_RFULL), o);
 #pragma unroll
-            for (int c = 0; c < HD / 8; ++c) {
-              const int ch = half * (HD / 8) + c;
-              asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(xrow + ((ch ^ (kl & (CPR - 1))) << 4)),
-                           "f"(dqv[4 * c]), "f"(dqv[4 * c + 1]), "f"(dqv[4 * c + 2]), "f"(dqv[4 * c + 3])
-                           : "memory");
-            }
+            for (int c = 0; c < HD / 8; ++c)
+              st_async_f4(dst + c * 16, dqv[4 * c], dqv[4 * c + 1], dqv[4 * c + 2], dqv[4 * c + 3], rbar);
           }
-          tc_fence_before();
-          mbar_arrive(bar(C::B_DQREAD));
-          __syncwarp();
-          if (lane == 0)
-            for (int r = 0; r < nkt; ++r) mbar_arrive_cluster(mapa_shared(bar(C::B_XFULL), r));
-          ok = wait_bar_cluster_warp(bar(C::B_XFULL), t & 1, ab);
-          if (!ok) break;
-          {
-            constexpr int CPR = HD / 4;
-            const int items = (r1 - r0) * CPR;
-            for (int it = tid; it < items; it += C::NEWT) {
-              const int row = r0 + it / CPR, c = it % CPR;
-              const uint32_t la = sb0 + C::OFF_X + row * HD * 4 + ((c ^ (row & (CPR - 1))) << 4);
-              float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
-              for (int r = 0; r < nkt; ++r) {
-                const float4 v = ld_dsmem_f4(mapa_shared(la, r));
-                s4.x += v.x;
-                s4.y += v.y;
-                s4.z += v.z;
-                s4.w += v.w;
-              }
-              const int j = jt * 128 + row;
-              if (j < g.N) {
-                const uint2 o = make_uint2(
-                    (uint32_t)f32_to_bf16_rn(s4.x * g.scale) | ((uint32_t)f32_to_bf16_rn(s4.y * g.scale) << 16),
-                    (uint32_t)f32_to_bf16_rn(s4.z * g.scale) | ((uint32_t)f32_to_bf16_rn(s4.w * g.scale) << 16));
-                *reinterpret_cast<uint2 *>(dQ + pos_row(g, b, i, j) * g.H * HD + h * HD + c * 4) = o;
-              }
-            }
-          }
-          __syncwarp();
-          if (lane == 0)
-            for (int r = 0; r < nkt; ++r) mbar_arrive_cluster(mapa_shared(bar(C::B_XEMPTY), r));
+          prev_i = i;
+          prev_jt = jt;
         }
         if (!ok) break;
         // ---- dBias tile (jt, kt) of this block into the supergroup partial (FP32, [k][j], owned by this CTA)
@@ -519,6 +540,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
       tc_fence_before();
       mbar_arrive(bar(C::B_DKVREAD));
     }
+    if (ok && red < T) ok = reduce_prev();  // the last step's dQ rows
   }
   tc_fence_before();
   __syncthreads();
@@ -627,6 +649,43 @@ cudaError_t launch_bwd_main(const Dims &g, int Gp, const uint16_t *Q, const uint
   return launch_bwd_main_t<16>(g, Gp, Q, K, V, biasT, mask, LSE, Dv, dO, dQ, dK, dV, partial, status, stream);
 }
 
-int bwd_groups(const Dims &g) { return bwd_supergroups(g); }
+int bwd_groups(const Dims &g) { return bwd_supergroups_max(g); }
+
+// Supergroups actually launched: as many (b, h, supergroup) clusters as the
+// device runs at once (one wave), within the workspace bound. Depends only on
+// the shape and the GPU model, so repeated calls reduce in the same order.
+template <int HD>
+int bwd_groups_active_t(const Dims &g) {
+  using C = BwdCfg<HD>;
+  static int cache[65][9];  // [device][cluster size]
+  const int nkt = (g.N + 127) / 128;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev > 64) return 1;
+  int n = cache[dev][nkt];
+  if (n == 0) {
+    if (cudaFuncSetAttribute(bwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) !=
+        cudaSuccess)
+      return 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(nkt, 1, 1);
+    cfg.blockDim = dim3(C::NTHREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_ALLOC;
+    cudaLaunchAttribute attrs[1];
+    attrs[0].id = cudaLaunchAttributeClusterDimension;
+    attrs[0].val.clusterDim.x = nkt;
+    attrs[0].val.clusterDim.y = 1;
+    attrs[0].val.clusterDim.z = 1;
+    cfg.attrs = attrs;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, bwd_kernel<HD>, &cfg) != cudaSuccess || n < 1) n = 1;
+    cache[dev][nkt] = n;
+  }
+  int gp = n / (g.B * g.H);
+  if (gp < 1) gp = 1;
+  const int gmax = bwd_supergroups_max(g);
+  return gp < gmax ? gp : gmax;
+}
+
+int bwd_groups_active(const Dims &g) { return g.d == 32 ? bwd_groups_active_t<32>(g) : bwd_groups_active_t<16>(g); }
 
 }  // namespace triattn

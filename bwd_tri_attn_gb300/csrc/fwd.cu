@@ -212,19 +212,15 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
     const float c1 = g.scale * kLog2e;
 
     // per-slice additive mask (log2 units) and per-tile "has a nonzero entry" flags
+    if (row < C::GF * C::MAXKT) flags[row] = 0;
+    named_sync(1, 128);
     if (mask) {
       for (int il = 0; il < ng; ++il)
-        for (int k = row; k < nkt * 128; k += 128)
-          maskf[il * C::NMAX + k] =
-              k < g.N ? bf16_to_f32(mask[((int64_t)b * g.S + i0 + il) * g.N + k]) * kLog2e : 0.f;
-    }
-    named_sync(1, 128);
-    if (row < C::GF * C::MAXKT) {
-      const int il = row / C::MAXKT, kt = row % C::MAXKT;
-      int f = 0;
-      if (mask && il < ng && kt < nkt)
-        for (int k = 0; k < 128; ++k) f |= (maskf[il * C::NMAX + kt * 128 + k] != 0.f);
-      flags[row] = f;
+        for (int k = row; k < nkt * 128; k += 128) {
+          const float v = k < g.N ? bf16_to_f32(mask[((int64_t)b * g.S + i0 + il) * g.N + k]) * kLog2e : 0.f;
+          maskf[il * C::NMAX + k] = v;
+          if (v != 0.f) flags[il * C::MAXKT + (k >> 7)] = 1;  // every writer stores the same value
+        }
     }
     named_sync(1, 128);
 
