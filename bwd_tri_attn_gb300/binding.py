@@ -37,7 +37,7 @@ class TriAttnError(RuntimeError):
 
 _VP = ctypes.c_void_p
 EXPORTS = ("tri_attn_strerror", "tri_attn_fwd", "tri_attn_bwd_workspace_size", "tri_attn_bwd",
-           "tri_attn_device_status", "tri_attn_set_timing_events")
+           "tri_attn_device_status", "tri_attn_set_timing_events", "tri_attn_bwd_static")
 
 
 def lib_path() -> str:
@@ -64,6 +64,8 @@ def load(path: str | None = None):
         lib.tri_attn_bwd.restype = ctypes.c_int
         lib.tri_attn_device_status.argtypes = [_VP]
         lib.tri_attn_device_status.restype = ctypes.c_int
+        lib.tri_attn_bwd_static.argtypes = [Shape] + [_VP] * 14
+        lib.tri_attn_bwd_static.restype = ctypes.c_int
         lib.tri_attn_set_timing_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]
         lib.tri_attn_set_timing_events.restype = ctypes.c_int
         _lib = lib
@@ -111,6 +113,13 @@ def tri_attn_bwd(shape: Shape, Q, K, V, bias, mask, O, Ores, LSE, dO, dQ, dK, dV
                              _p(dO), _p(dQ), _p(dK), _p(dV), _p(dBias), _p(workspace), nbytes,
                              _stream(stream))
     _check("tri_attn_bwd", rc)
+
+
+def tri_attn_bwd_static(shape: Shape, Q, K, V, bias, mask, O, Ores, LSE, dO, dQ, dK, dV, dBias, stream=None):
+    """Backward pass with the library's static scratch array (no workspace argument)."""
+    rc = load().tri_attn_bwd_static(shape, _p(Q), _p(K), _p(V), _p(bias), _p(mask), _p(O), _p(Ores), _p(LSE),
+                                    _p(dO), _p(dQ), _p(dK), _p(dV), _p(dBias), _stream(stream))
+    _check("tri_attn_bwd_static", rc)
 
 
 def tri_attn_device_status(stream=None) -> int:

@@ -97,6 +97,11 @@ cudaError_t mark(int k, cudaStream_t st) {
 
 }  // namespace
 
+namespace triattn {
+// Status word of the current device, for entry points defined in other files.
+int *device_status_word() { return status_word(); }
+}  // namespace triattn
+
 extern "C" {
 
 const char *tri_attn_strerror(int code) {
@@ -107,6 +112,8 @@ const char *tri_attn_strerror(int code) {
     case TRI_ATTN_ERR_WORKSPACE: return "workspace missing or smaller than tri_attn_bwd_workspace_size()";
     case TRI_ATTN_ERR_CUDA: return "CUDA runtime error";
     case TRI_ATTN_ERR_TIMEOUT: return "a bounded device-side wait expired";
+    case TRI_ATTN_ERR_STATIC_TOO_SMALL:
+      return "the shape needs more scratch than the library's static workspace (TRI_ATTN_STATIC_WORKSPACE_BYTES) holds";
     default: return "unknown error code";
   }
 }

@@ -1,0 +1,90 @@
+// tri_attn_bwd_static: the backward pass with its scratch taken from a
+// file-scope device array instead of a caller-provided workspace, for callers
+// that cannot allocate device memory at call time (see include/tri_attn.h).
+#include <math.h>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace triattn {
+cudaError_t launch_bwd_d(const Dims &g, const uint16_t *dO, const uint16_t *O, const uint16_t *Ores,
+                         float *Dout, cudaStream_t stream);
+cudaError_t launch_bias_transpose(const Dims &g, const uint16_t *bias, uint16_t *biasT, cudaStream_t stream);
+cudaError_t launch_bwd_main(const Dims &g, int Gp, const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                            const uint16_t *biasT, const uint16_t *mask, const float *LSE, const float *Dv,
+                            const uint16_t *dO, uint16_t *dQ, uint16_t *dK, uint16_t *dV, float *partial,
+                            int *status, cudaStream_t stream);
+cudaError_t launch_dbias_reduce_t(const Dims &g, int Gp, const float *partial, uint16_t *dBias,
+                                  cudaStream_t stream);
+int bwd_groups_active(const Dims &g);
+int *device_status_word();
+}  // namespace triattn
+
+using namespace triattn;
+
+// The scratch array. In host code this name is only a stand-in for the symbol:
+// its device address comes from cudaGetSymbolAddress (static_scratch below).
+static __device__ __align__(256) unsigned char g_static_scratch[TRI_ATTN_STATIC_WORKSPACE_BYTES];
+
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Device address of the scratch array on the current device, looked up once per device.
+unsigned char *static_scratch() {
+  static std::mutex mu;
+  static unsigned char *addr[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<unsigned char *>(p);
+  }
+  return addr[dev];
+}
+
+}  // namespace
+
+extern "C" int tri_attn_bwd_static(tri_attn_shape s, const tri_attn_bf16 *Q, const tri_attn_bf16 *K,
+                                   const tri_attn_bf16 *V, const tri_attn_bf16 *bias, const tri_attn_bf16 *mask,
+                                   const tri_attn_bf16 *O, const tri_attn_bf16 *Ores, const float *LSE,
+                                   const tri_attn_bf16 *dO, tri_attn_bf16 *dQ, tri_attn_bf16 *dK, tri_attn_bf16 *dV,
+                                   tri_attn_bf16 *dBias, void *stream) {
+  if (s.B < 1 || s.S < 1 || s.N < 1 || s.H < 1 || !isfinite(s.scale)) return TRI_ATTN_ERR_INVALID_ARG;
+  if ((s.d != 16 && s.d != 32) || s.N > TRI_ATTN_MAX_N) return TRI_ATTN_ERR_UNSUPPORTED;
+  if ((int64_t)s.B * s.S > 65535 || (int64_t)s.B * s.H * s.S > (1ll << 30)) return TRI_ATTN_ERR_UNSUPPORTED;
+  if (!Q || !K || !V || !bias || !O || !LSE || !dO || !dQ || !dK || !dV || !dBias) return TRI_ATTN_ERR_INVALID_ARG;
+  const void *ptrs[] = {Q, K, V, bias, mask, O, Ores, LSE, dO, dQ, dK, dV, dBias};
+  for (const void *p : ptrs)
+    if (p && !aligned16(p)) return TRI_ATTN_ERR_UNSUPPORTED;
+
+  // scratch layout: D [B,S,H,N] FP32 | transposed bias [B*H][NP][NP] BF16 | Gp dBias partials [B*H][NP][NP] FP32
+  const Dims g{s.B, s.S, s.N, s.H, s.d, s.scale};
+  const size_t NP = (size_t)(s.N + 127) / 128 * 128;
+  const size_t d_bytes = align_up(sizeof(float) * (size_t)s.B * s.S * s.H * s.N);
+  const size_t bt_bytes = align_up(2 * (size_t)s.B * s.H * NP * NP);
+  const size_t one_partial = sizeof(float) * (size_t)s.B * s.H * NP * NP;
+  const size_t cap = TRI_ATTN_STATIC_WORKSPACE_BYTES;
+  if (d_bytes + bt_bytes + one_partial > cap) return TRI_ATTN_ERR_STATIC_TOO_SMALL;
+  const size_t fit = (cap - d_bytes - bt_bytes) / one_partial;
+  int groups = bwd_groups_active(g);
+  if ((size_t)groups > fit) groups = (int)fit;
+
+  unsigned char *ws = static_scratch();
+  int *status = device_status_word();
+  if (!ws || !status) return TRI_ATTN_ERR_CUDA;
+  float *Dv = reinterpret_cast<float *>(ws);
+  uint16_t *biasT = reinterpret_cast<uint16_t *>(ws + d_bytes);
+  float *partial = reinterpret_cast<float *>(ws + d_bytes + bt_bytes);
+  auto st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_bias_transpose(g, bias, biasT, st);
+  if (e == cudaSuccess) e = launch_bwd_d(g, dO, O, Ores, Dv, st);
+  if (e == cudaSuccess)
+    e = launch_bwd_main(g, groups, Q, K, V, biasT, mask, LSE, Dv, dO, dQ, dK, dV, partial, status, st);
+  if (e == cudaSuccess) e = launch_dbias_reduce_t(g, groups, partial, dBias, st);
+  return e == cudaSuccess ? TRI_ATTN_OK : TRI_ATTN_ERR_CUDA;
+}

@@ -72,7 +72,8 @@ enum {
     TRI_ATTN_ERR_UNSUPPORTED = -2,  /* d not 16/32, N above the limit, misaligned pointer */
     TRI_ATTN_ERR_WORKSPACE = -3,    /* workspace NULL or smaller than tri_attn_bwd_workspace_size */
     TRI_ATTN_ERR_CUDA = -4,         /* a CUDA runtime/driver call or launch failed */
-    TRI_ATTN_ERR_TIMEOUT = -5       /* a bounded device wait expired (see tri_attn_device_status) */
+    TRI_ATTN_ERR_TIMEOUT = -5,      /* a bounded device wait expired (see tri_attn_device_status) */
+    TRI_ATTN_ERR_STATIC_TOO_SMALL = -6 /* tri_attn_bwd_static: shape needs more than the static workspace */
 };
 
 /* Human-readable text of a return code (static storage, never NULL). */
@@ -130,6 +131,46 @@ int tri_attn_bwd(tri_attn_shape shape,
  * Returns TRI_ATTN_ERR_CUDA if the synchronisation itself fails.
  */
 int tri_attn_device_status(void *stream);
+
+/*
+ * Backward pass that allocates nothing and takes no workspace argument.
+ * (This entry point is a library convenience; the paper has no counterpart.)
+ *
+ * Some callers cannot allocate device memory when they call the backward pass:
+ * a plugin whose host framework hands it only its input and output tensors and
+ * owns every other byte of device memory, or a service that runs on a fixed,
+ * pre-planned memory budget where a cudaMalloc at call time could fail or stall
+ * the stream. For them, this call takes its scratch (the D correction, the
+ * transposed bias and the dBias partials) from one array of
+ * TRI_ATTN_STATIC_WORKSPACE_BYTES bytes that the library defines at file scope
+ * in device memory; every GPU on which the library is loaded holds that array
+ * until the process exits. The call itself allocates nothing.
+ *
+ * Arguments, layouts and outputs are exactly those of tri_attn_bwd minus the
+ * workspace. The slice supergroups (dBias partials) are capped to what fits
+ * in the array, so dBias may be summed in a different (still fixed) order than
+ * tri_attn_bwd uses for the same shape; the results agree within rounding.
+ * Returns TRI_ATTN_ERR_STATIC_TOO_SMALL, before enqueuing anything, when even
+ * one partial does not fit (B = 1, H = 4, S = N = 768 fits with two partials;
+ * S = N = 1024 does not).
+ *
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call before
+ * any stream capture. Sharing: every call uses the same array and leaves its
+ * contents behind. Nothing in it needs to start at zero (each call writes every
+ * byte it reads first), but two calls whose kernels overlap on the GPU (other
+ * streams, other host threads) race on the array and must be serialised by the
+ * caller.
+ */
+#define TRI_ATTN_STATIC_WORKSPACE_BYTES (32u * 1024u * 1024u)
+
+int tri_attn_bwd_static(tri_attn_shape shape,
+                        const tri_attn_bf16 *Q, const tri_attn_bf16 *K, const tri_attn_bf16 *V,
+                        const tri_attn_bf16 *bias, const tri_attn_bf16 *mask,
+                        const tri_attn_bf16 *O, const tri_attn_bf16 *Ores, const float *LSE,
+                        const tri_attn_bf16 *dO,
+                        tri_attn_bf16 *dQ, tri_attn_bf16 *dK, tri_attn_bf16 *dV, tri_attn_bf16 *dBias,
+                        void *stream);
 
 /*
  * Per-kernel timing instrumentation (off by default). After this call, every
