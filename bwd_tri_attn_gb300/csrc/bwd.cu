@@ -9,11 +9,11 @@
 //
 // Work unit (one CTA): batch b, head h, key tile kt (128 keys), and a
 // "supergroup" of consecutive slices, walked in blocks of GB slices:
-//     for block: for query tile jt: for slice i in block:
+//     for block: for query tile jt: for slice i in block:     (one "step")
 //         S^T  = K_i Q_i[jt]^T        (TMEM, lanes = keys)
 //         dP^T = V_i dO_i[jt]^T
 //         P^T  = exp2(S^T*scale*log2e + biasT*log2e - LSE*log2e)   (FP32, written back as FP16)
-//         dS^T = P^T * (dP^T - D)
+//         dS^T = P^T * (dP^T - D)      (P rounded to FP16 first: it is also the dV operand)
 //         dV_i += P^T dO_i[jt],  dK_i += dS^T Q_i[jt]            (TMEM accumulators, one pair per slice of the block)
 //         dQ_i[jt] partial = dS K_i                               (reduced across the cluster, below)
 //         dBias tile (jt, kt) += dS   (registers, summed in slice order over the block)
@@ -30,17 +30,20 @@
 //    one step later so that the exchange overlaps the next step's work.
 //  - dBias over slices: within a block in slice order (registers), across blocks in
 //    block order (the partial), across supergroups in supergroup order (reduce kernel).
-// Every order depends on the shape only.
+// Every order depends on the shape (and, for the supergroup count, the GPU model) only.
 //
 // Operands: all tensor-core operands are FP16 (Q, K, V, dO converted in shared
 // memory, exact in the FP16 range); P and dS need FP16's 11-bit significand.
 //
-// Warps: 0-7 elementwise (thread = key row x 64 query columns; warp w uses the
-// TMEM lane quarter w % 4 and query half w / 4), 8 = TMA producer, 9 = MMA issuer.
-// TMEM: [0,128) S^T, overwritten in place by P^T (FP16 pairs: queries 0-63 in
-// cols 0-31, queries 64-127 in cols 64-95, so each query half writes only
-// columns it has already read) and then by the dQ partial (cols 96..96+d);
-// [128,256) dP^T then dS^T (same packing); 256 + 2*d*il: dK_il, dV_il.
+// Warp roles (16 warps):
+//   0-7   elementwise: thread = key row (TMEM lane quarter w % 4) x 64 queries (half w / 4);
+//         only P and dS are on their path; 176 registers each (setmaxnreg)
+//   8-11  dQ: read the dQ partial from TMEM (lanes = queries), push it to the owners, reduce owned rows
+//   12    TMA producer (+ LSE / D rows), 13 MMA issuer and TMEM owner, 14-15 BF16 -> FP16 conversion
+// TMEM columns: A = [0,128) S^T; B = [128,256) dP^T, then per query half h the packed
+// FP16 dS^T (B + 64h + [0,32)) and P^T (B + 64h + [32,64)), each written only over
+// columns that thread has already read; dQ partial at 256; dK_i, dV_i from 288.
+// S^T(t+1) is computed into A while the elementwise warps still work on step t.
 #include "common.cuh"
 #include "sm100.cuh"
 #include "sync.cuh"
@@ -51,39 +54,42 @@ using namespace sm100;
 
 template <int HD>
 struct BwdCfg {
-  static constexpr int GB = HD == 32 ? 4 : 8;  // slices per block: GB * 2d TMEM columns of dK/dV
+  static constexpr int GB = HD == 32 ? 3 : 7;  // slices per block: dK/dV of GB slices live in TMEM
   static constexpr int NQS = 2;                // Q/dO stages
   static constexpr int ROWB = HD * 2;
   static constexpr int TILE = 128 * ROWB;
   static constexpr uint32_t SW = HD == 32 ? kSwizzle64B : kSwizzle32B;
-  static constexpr int NEW = 8;  // elementwise warps
-  static constexpr int NEWT = NEW * 32;
-  static constexpr int WARP_TMA = NEW, WARP_MMA = NEW + 1;
-  static constexpr int NTHREADS = (NEW + 2) * 32;
+  static constexpr int NEW = 8, NEWT = NEW * 32;  // elementwise warps 0-7
+  static constexpr int WARP_DQ = 8, NDQ = 4, NDQT = NDQ * 32;
+  static constexpr int WARP_TMA = 12, WARP_MMA = 13, WARP_CV = 14, NCV = 2, NCVT = NCV * 32;
+  static constexpr int NTHREADS = 512;
+  static constexpr uint32_t REG_LAUNCH = 128, REG_EW = 176, REG_OTHER = 80;
+  static_assert(NEWT * REG_EW + (NTHREADS - NEWT) * REG_OTHER == NTHREADS * REG_LAUNCH, "register split");
+  static constexpr uint32_t TA = 0, TB = 128, TDQ = 256, TDKV = 288, TMEM_COLS = 512;
+  static_assert(TDKV + GB * 2 * HD <= TMEM_COLS, "TMEM budget");
   static constexpr int BIAS_TILE = 128 * 128 * 2;
+  static constexpr int RB_ROWS = 136;  // >= n * ceil(128 / n) for every cluster size n <= 8
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + GB * TILE;
   static constexpr int OFF_Q = OFF_V + GB * TILE;
   static constexpr int OFF_DO = OFF_Q + NQS * TILE;
   static constexpr int OFF_BIAS = OFF_DO + NQS * TILE;     // 2 x [2 halves][128 rows][128 B], SW128
   static constexpr int OFF_DS = OFF_BIAS + 2 * BIAS_TILE;  // FP16 dS, MN-major SW128: [16 key groups][2][8][128 B]
-  static constexpr int RB_ROWS = 136;                      // >= n * ceil(128 / n) for every cluster size n <= 8
-  static constexpr int OFF_RB = OFF_DS + 32768;            // dQ receive buffer: [sender][row][HD] FP32
-  static constexpr int OFF_LSE = OFF_RB + RB_ROWS * HD * 4; // [NQS][128]: -LSE*log2e (or -inf)
-  static constexpr int OFF_D = OFF_LSE + NQS * 512;        // [NQS][128]: D
-  static constexpr int OFF_MASK = OFF_D + NQS * 512;       // [GB][128]: mask*log2e of this CTA's keys
+  static constexpr int RB_SLOT = RB_ROWS * HD * 4;
+  static constexpr int OFF_RB = OFF_DS + 32768;            // dQ receive buffers: 2 x [sender][row][HD] FP32
+  static constexpr int OFF_LSE = OFF_RB + 2 * RB_SLOT;     // [NQS][128]: -LSE*log2e (or -inf)
+  static constexpr int OFF_D = OFF_LSE + NQS * 512;          // [NQS][128]: D
+  static constexpr int OFF_MASK = OFF_D + NQS * 512;         // [GB][128]: mask*log2e of this CTA's keys
   static constexpr int OFF_BAR = OFF_MASK + GB * 512;
   static constexpr int B_KVFULL = 0, B_KVREADY = 1, B_KVFREE = 2;
   static constexpr int B_QDOFULL = 3, B_QDOREADY = B_QDOFULL + NQS, B_QDOFREE = B_QDOREADY + NQS;
   static constexpr int B_BFULL = B_QDOFREE + NQS, B_BFREE = B_BFULL + 2;
-  static constexpr int B_SFULL = B_BFREE + 2, B_PFULL = B_SFULL + 1, B_M2DONE = B_PFULL + 1;
-  static constexpr int B_DQREAD = B_M2DONE + 1, B_DKVREAD = B_DQREAD + 1;
-  static constexpr int B_RFULL = B_DKVREAD + 1, B_XEMPTY = B_RFULL + 1, B_FINAL = B_XEMPTY + 1;
-  static constexpr int NBAR = B_FINAL + 1;
+  static constexpr int B_SFULL = B_BFREE + 2, B_SREAD = B_SFULL + 1, B_DPFULL = B_SREAD + 1;
+  static constexpr int B_PFULL = B_DPFULL + 1, B_M2DONE = B_PFULL + 1, B_DQREAD = B_M2DONE + 1;
+  static constexpr int B_DKVREAD = B_DQREAD + 1, B_RFULL = B_DKVREAD + 1, B_XEMPTY = B_RFULL + 2;
+  static constexpr int B_FINAL = B_XEMPTY + 2, NBAR = B_FINAL + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_ALLOC = OFF_MISC + 16 + 1024;
-  static constexpr uint32_t TMEM_COLS = 512;
-  static_assert(256 + GB * 2 * HD <= 512, "TMEM budget");
   static_assert(OFF_BIAS % 1024 == 0 && OFF_DS % 1024 == 0, "SW128 tiles need 1 KB alignment");
   static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 };
@@ -119,6 +125,24 @@ __device__ __forceinline__ void convert_to_f16(uint8_t *p, int bytes, int tid, i
   }
 }
 
+template <uint32_t R>
+__device__ __forceinline__ void reg_alloc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
+}
+template <uint32_t R>
+__device__ __forceinline__ void reg_dealloc() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R));
+}
+
+// The step schedule every role walks in the same order: blocks of GB slices of
+// the supergroup [s0, s1), then query tiles, then the slices of the block.
+struct Sched {
+  int s0, s1, njt, GB;
+  __device__ int nblk() const { return (s1 - s0 + GB - 1) / GB; }
+  __device__ int block_first(int bi) const { return s0 + bi * GB; }
+  __device__ int block_size(int bi) const { return min(GB, s1 - block_first(bi)); }
+};
+
 template <int HD>
 __global__ void __launch_bounds__(BwdCfg<HD>::NTHREADS, 1)
 bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
@@ -134,21 +158,23 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
   const int nkt = (g.N + 127) / 128, njt = nkt, NP = nkt * 128;
   const int kt = blockIdx.x, h = blockIdx.y;
   const int b = blockIdx.z / Gp, grp = blockIdx.z % Gp;
-  const uint32_t rank = cluster_ctarank();  // == kt (cluster spans the key tiles)
-  const int s0 = (int)((int64_t)grp * g.S / Gp), s1 = (int)((int64_t)(grp + 1) * g.S / Gp);
-  const int nblk = (s1 - s0 + C::GB - 1) / C::GB;
-  const int T = njt * (s1 - s0);  // steps of this CTA
+  const uint32_t rank = cluster_ctarank();  // == kt (the cluster spans the key tiles)
+  const Sched sc{(int)((int64_t)grp * g.S / Gp), (int)((int64_t)(grp + 1) * g.S / Gp), njt, C::GB};
+  const int nblk = sc.nblk();
+  const int T = njt * (sc.s1 - sc.s0);  // steps of this CTA
   auto bar = [&](int k) { return sb0 + C::OFF_BAR + 8u * (uint32_t)k; };
   volatile uint32_t *misc = reinterpret_cast<volatile uint32_t *>(sm + C::OFF_MISC);
   const Abort ab{reinterpret_cast<volatile int *>(misc + 1), status};
+  const int r0 = (int)(rank * 128 / nkt), r1 = (int)((rank + 1) * 128 / nkt);  // owned dQ rows
+  const int rows_max = (128 + nkt - 1) / nkt;
 
   if (tid == 0) {
     mbar_init(bar(C::B_KVFULL), 1);
-    mbar_init(bar(C::B_KVREADY), C::NEWT);
+    mbar_init(bar(C::B_KVREADY), C::NCV);
     mbar_init(bar(C::B_KVFREE), 1);
     for (int s = 0; s < C::NQS; ++s) {
       mbar_init(bar(C::B_QDOFULL + s), 1);
-      mbar_init(bar(C::B_QDOREADY + s), C::NEWT);
+      mbar_init(bar(C::B_QDOREADY + s), C::NCV);
       mbar_init(bar(C::B_QDOFREE + s), 1);
     }
     for (int s = 0; s < 2; ++s) {
@@ -156,12 +182,16 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
       mbar_init(bar(C::B_BFREE + s), C::NEWT);
     }
     mbar_init(bar(C::B_SFULL), 1);
+    mbar_init(bar(C::B_SREAD), C::NEWT);
+    mbar_init(bar(C::B_DPFULL), 1);
     mbar_init(bar(C::B_PFULL), C::NEWT);
     mbar_init(bar(C::B_M2DONE), 1);
-    mbar_init(bar(C::B_DQREAD), C::NEWT);
+    mbar_init(bar(C::B_DQREAD), C::NDQT);
     mbar_init(bar(C::B_DKVREAD), C::NEWT);
-    mbar_init(bar(C::B_RFULL), 1);             // + the bytes pushed by all n senders
-    mbar_init(bar(C::B_XEMPTY), C::NEW * nkt);  // one arrive per elementwise warp of every owner
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(C::B_RFULL + s), 1);             // + the bytes pushed by all n senders
+      mbar_init(bar(C::B_XEMPTY + s), C::NDQ * nkt);  // one arrive per dQ warp of every owner
+    }
     mbar_init(bar(C::B_FINAL), 1);
     misc[1] = 0;
     fence_barrier_init();
@@ -175,8 +205,11 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
   cluster_sync_all();  // every CTA's barriers exist before any peer arrives on them
   tc_fence_after();
   const uint32_t tb = misc[0];
-
-  if (warp == C::WARP_TMA) {
+  // Register split (setmaxnreg, per warpgroup, at the top of each warpgroup's branch):
+  // warpgroups 2 and 3 give registers up, the two elementwise warpgroups take them.
+  if (warp >= C::WARP_TMA) {
+   reg_dealloc<C::REG_OTHER>();
+   if (warp == C::WARP_TMA) {
     // ---------------------------------------------------------------- producer
     bool ok = true;
     int t = 0, u = 0, kv_issued = 0;
@@ -188,15 +221,15 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
       tma_prefetch_map(&mBT);
     }
     for (int bi = 0; bi < nblk && ok; ++bi) {
-      const int i0 = s0 + bi * C::GB, nb = min(C::GB, s1 - i0);
+      const int i0 = sc.block_first(bi), nb = sc.block_size(bi);
       for (int jt = 0; jt < njt && ok; ++jt) {
         for (int il = 0; il < nb; ++il, ++t) {
           const int st = t % C::NQS, i = i0 + il;
           if (t >= C::NQS) ok = wait_bar_warp(bar(C::B_QDOFREE + st), ((t / C::NQS) - 1) & 1, ab);
           if (!ok) break;
-          float *sl = reinterpret_cast<float *>(sm + C::OFF_LSE + st * 512);
-          float *sd = reinterpret_cast<float *>(sm + C::OFF_D + st * 512);
           {
+            float *sl = reinterpret_cast<float *>(sm + C::OFF_LSE + st * 512);
+            float *sd = reinterpret_cast<float *>(sm + C::OFF_D + st * 512);
             float lv[4], dvv[4];
             const int64_t lrow = (((int64_t)b * g.S + i) * g.H + h) * g.N;
 #pragma unroll
@@ -218,7 +251,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
             tma_load_4d(sb0 + C::OFF_DO + st * C::TILE, &mDO, bar(C::B_QDOFULL + st), 0, h, jt * 128, b * g.S + i);
           }
           if (jt == 0 && il == 0) {
-            // K_i, V_i of the block (single-buffered: wait until the previous block's MMAs are done)
+            // K_i, V_i of the block (single-buffered: the previous block's MMAs must be done)
             if (bi > 0) ok = wait_bar_warp(bar(C::B_KVFREE), (bi - 1) & 1, ab);
             if (!ok) break;
             if (lane == 0) {
@@ -251,93 +284,166 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
       for (int x = max(0, u - 2); x < u; ++x) drain_bar(bar(C::B_BFULL + (x & 1)), (x >> 1) & 1);
       for (int x = max(0, t - C::NQS); x < t; ++x) drain_bar(bar(C::B_QDOFULL + x % C::NQS), (x / C::NQS) & 1);
     }
-  } else if (warp == C::WARP_MMA) {
+   } else if (warp >= C::WARP_CV) {
+    // ---------------------------------------------------------------- BF16 -> FP16 converters (+ mask rows)
+    const int ct = tid - C::WARP_CV * 32;
+    bool ok = true;
+    int t = 0;
+    for (int bi = 0; bi < nblk && ok; ++bi) {
+      const int i0 = sc.block_first(bi), nb = sc.block_size(bi);
+      ok = wait_bar_warp(bar(C::B_KVFULL), bi & 1, ab);
+      if (!ok) break;
+      convert_to_f16(sm + C::OFF_K, nb * C::TILE, ct, C::NCVT);
+      convert_to_f16(sm + C::OFF_V, nb * C::TILE, ct, C::NCVT);
+      float *maskf = reinterpret_cast<float *>(sm + C::OFF_MASK);
+      for (int x = ct; x < nb * 128; x += C::NCVT) {
+        const int il = x >> 7, k = kt * 128 + (x & 127);
+        float mv = -INFINITY;  // keys past N are dead rows
+        if (k < g.N) mv = mask ? bf16_to_f32(mask[((int64_t)b * g.S + i0 + il) * g.N + k]) * kLog2e : 0.f;
+        maskf[x] = mv;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::B_KVREADY));
+      for (int jt = 0; jt < njt && ok; ++jt)
+        for (int il = 0; il < nb; ++il, ++t) {
+          const int st = t % C::NQS;
+          ok = wait_bar_warp(bar(C::B_QDOFULL + st), (t / C::NQS) & 1, ab);
+          if (!ok) break;
+          convert_to_f16(sm + C::OFF_Q + st * C::TILE, C::TILE, ct, C::NCVT);
+          convert_to_f16(sm + C::OFF_DO + st * C::TILE, C::TILE, ct, C::NCVT);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(C::B_QDOREADY + st));
+        }
+    }
+   } else {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idSS = idesc_f16(128, 128, false, false, false, false);
       constexpr uint32_t idTS = idesc_f16(128, HD, false, false, false, true);
       constexpr uint32_t idQ = idesc_f16(128, HD, false, false, true, true);
-      bool ok = true;
-      int t = 0;
-      for (int bi = 0; bi < nblk && ok; ++bi) {
-        const int i0 = s0 + bi * C::GB, nb = min(C::GB, s1 - i0);
-        ok = wait_bar(bar(C::B_KVREADY), bi & 1, ab);
-        if (ok && bi > 0) ok = wait_bar(bar(C::B_DKVREAD), (bi - 1) & 1, ab);
-        for (int jt = 0; jt < njt && ok; ++jt) {
-          for (int il = 0; il < nb && ok; ++il, ++t) {
-            const int st = t % C::NQS;
-            ok = wait_bar(bar(C::B_QDOREADY + st), (t / C::NQS) & 1, ab);
-            if (ok && t > 0) ok = wait_bar(bar(C::B_DQREAD), (t - 1) & 1, ab);
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t kA = sb0 + C::OFF_K + il * C::TILE, vA = sb0 + C::OFF_V + il * C::TILE;
-            const uint32_t qB = sb0 + C::OFF_Q + st * C::TILE, oB = sb0 + C::OFF_DO + st * C::TILE;
-#pragma unroll
-            for (int ks = 0; ks < HD / 16; ++ks)
-              mma_ss(tb, smem_desc(kA + ks * 32, 16, 8 * C::ROWB, C::SW), smem_desc(qB + ks * 32, 16, 8 * C::ROWB, C::SW),
-                     idSS, ks > 0 ? 1u : 0u);
-#pragma unroll
-            for (int ks = 0; ks < HD / 16; ++ks)
-              mma_ss(tb + 128, smem_desc(vA + ks * 32, 16, 8 * C::ROWB, C::SW),
-                     smem_desc(oB + ks * 32, 16, 8 * C::ROWB, C::SW), idSS, ks > 0 ? 1u : 0u);
-            mma_commit(bar(C::B_SFULL));
-            ok = wait_bar(bar(C::B_PFULL), t & 1, ab);
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t dcol = tb + 256 + il * 2 * HD;
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks)  // dV += P^T dO
-              mma_ts(dcol + HD, tb + (ks >> 2) * 64 + (ks & 3) * 8, smem_desc(oB + ks * 16 * C::ROWB, 16, 8 * C::ROWB, C::SW), idTS,
-                     (jt > 0 || ks > 0) ? 1u : 0u);
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks)  // dK += dS^T Q
-              mma_ts(dcol, tb + 128 + (ks >> 2) * 64 + (ks & 3) * 8, smem_desc(qB + ks * 16 * C::ROWB, 16, 8 * C::ROWB, C::SW), idTS,
-                     (jt > 0 || ks > 0) ? 1u : 0u);
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks)  // dQ partial = dS K
-              mma_ss(tb + 96, smem_desc(sb0 + C::OFF_DS + ks * 4096, 1024, 2048, kSwizzle128B),
-                     smem_desc(kA + ks * 16 * C::ROWB, 16, 8 * C::ROWB, C::SW), idQ, ks > 0 ? 1u : 0u);
-            mma_commit(bar(C::B_M2DONE));
-            mma_commit(bar(C::B_QDOFREE + st));
+      // per-step bookkeeping, walked in the common schedule
+      int bi = 0, jt = 0, il = 0;
+      auto advance = [&]() {
+        if (++il == sc.block_size(bi)) {
+          il = 0;
+          if (++jt == njt) {
+            jt = 0;
+            ++bi;
           }
         }
-        mma_commit(bar(C::B_KVFREE));
+      };
+      auto issue_s = [&](int t, int il_, int st) {
+        const uint32_t kA = sb0 + C::OFF_K + il_ * C::TILE, qB = sb0 + C::OFF_Q + st * C::TILE;
+#pragma unroll
+        for (int ks = 0; ks < HD / 16; ++ks)
+          mma_ss(tb + C::TA, smem_desc(kA + ks * 32, 16, 8 * C::ROWB, C::SW),
+                 smem_desc(qB + ks * 32, 16, 8 * C::ROWB, C::SW), idSS, ks > 0 ? 1u : 0u);
+        mma_commit(bar(C::B_SFULL));
+      };
+      auto issue_dp = [&](int il_, int st) {
+        const uint32_t vA = sb0 + C::OFF_V + il_ * C::TILE, oB = sb0 + C::OFF_DO + st * C::TILE;
+#pragma unroll
+        for (int ks = 0; ks < HD / 16; ++ks)
+          mma_ss(tb + C::TB, smem_desc(vA + ks * 32, 16, 8 * C::ROWB, C::SW),
+                 smem_desc(oB + ks * 32, 16, 8 * C::ROWB, C::SW), idSS, ks > 0 ? 1u : 0u);
+        mma_commit(bar(C::B_DPFULL));
+      };
+      bool ok = wait_bar(bar(C::B_KVREADY), 0, ab);
+      if (ok) ok = wait_bar(bar(C::B_QDOREADY), 0, ab);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0, 0);
+        issue_dp(0, 0);
+      }
+      for (int t = 0; t < T && ok; ++t) {
+        const int st = t % C::NQS;
+        const int cbi = bi, cjt = jt, cil = il;  // this step
+        advance();                               // (bi, jt, il) now describe step t + 1
+        const bool has_next = t + 1 < T;
+        const bool next_new_block = has_next && jt == 0 && il == 0;
+        const int st1 = (t + 1) % C::NQS;
+        // S^T(t+1) ahead of this step's second group if region A has been read and Q(t+1) is
+        // ready already (never across a block change: that needs the new K)
+        bool s_early = false;
+        if (has_next && !next_new_block && mbar_try_wait(bar(C::B_QDOREADY + st1), ((t + 1) / C::NQS) & 1) &&
+            mbar_try_wait(bar(C::B_SREAD), t & 1)) {
+          tc_fence_after();
+          issue_s(t + 1, il, st1);
+          s_early = true;
+        }
+        // second MMA group of step t
+        ok = wait_bar(bar(C::B_PFULL), t & 1, ab);
+        if (ok && cjt == 0 && cil == 0 && cbi > 0) ok = wait_bar(bar(C::B_DKVREAD), (cbi - 1) & 1, ab);
+        if (ok && t > 0) ok = wait_bar(bar(C::B_DQREAD), (t - 1) & 1, ab);
+        if (!ok) break;
+        tc_fence_after();
+        {
+          const uint32_t kA = sb0 + C::OFF_K + cil * C::TILE;
+          const uint32_t qB = sb0 + C::OFF_Q + st * C::TILE, oB = sb0 + C::OFF_DO + st * C::TILE;
+          const uint32_t dcol = tb + C::TDKV + cil * 2 * HD;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {  // dV += P^T dO, dK += dS^T Q (A from TMEM region B)
+            const uint32_t half_col = tb + C::TB + (ks >> 2) * 64 + (ks & 3) * 8;
+            mma_ts(dcol + HD, half_col + 32, smem_desc(oB + ks * 16 * C::ROWB, 16, 8 * C::ROWB, C::SW), idTS,
+                   (cjt > 0 || ks > 0) ? 1u : 0u);
+            mma_ts(dcol, half_col, smem_desc(qB + ks * 16 * C::ROWB, 16, 8 * C::ROWB, C::SW), idTS,
+                   (cjt > 0 || ks > 0) ? 1u : 0u);
+          }
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)  // dQ partial = dS K
+            mma_ss(tb + C::TDQ, smem_desc(sb0 + C::OFF_DS + ks * 4096, 1024, 2048, kSwizzle128B),
+                   smem_desc(kA + ks * 16 * C::ROWB, 16, 8 * C::ROWB, C::SW), idQ, ks > 0 ? 1u : 0u);
+          mma_commit(bar(C::B_M2DONE));
+          mma_commit(bar(C::B_QDOFREE + st));
+          if (next_new_block || !has_next) mma_commit(bar(C::B_KVFREE));
+        }
+        if (has_next) {
+          if (!s_early) {
+            if (next_new_block) ok = wait_bar(bar(C::B_KVREADY), bi & 1, ab);
+            if (ok) ok = wait_bar(bar(C::B_QDOREADY + st1), ((t + 1) / C::NQS) & 1, ab);
+            if (ok) ok = wait_bar(bar(C::B_SREAD), t & 1, ab);
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(t + 1, il, st1);
+          }
+          // region B (P^T, dS^T of step t) and the dS tile are free once this step's MMAs completed
+          ok = wait_bar(bar(C::B_M2DONE), t & 1, ab);
+          if (!ok) break;
+          issue_dp(il, st1);
+        }
       }
       mma_commit(bar(C::B_FINAL));
       drain_bar(bar(C::B_FINAL), 0);
     }
-  } else {
-    // ---------------------------------------------------------------- elementwise warps 0-7
-    const int q = warp & 3, half = warp >> 2;
-    const int kl = q * 32 + lane;  // key row of the tile = TMEM lane
-    const int kg = kt * 128 + kl;
-    const uint32_t lb = (uint32_t)(q * 32) << 16;
-    const float c1 = g.scale * kLog2e;
-    float *maskf = reinterpret_cast<float *>(sm + C::OFF_MASK);
-    const int r0 = (int)(rank * 128 / nkt), r1 = (int)((rank + 1) * 128 / nkt);
-    bool ok = true;
-    int t = 0, u = 0;
-    auto convert_qdo = [&](int tt) -> bool {
-      const int st = tt % C::NQS;
-      if (!wait_bar_warp(bar(C::B_QDOFULL + st), (tt / C::NQS) & 1, ab)) return false;
-      convert_to_f16(sm + C::OFF_Q + st * C::TILE, C::TILE, tid, C::NEWT);
-      convert_to_f16(sm + C::OFF_DO + st * C::TILE, C::TILE, tid, C::NEWT);
-      fence_proxy_async_smem();
-      mbar_arrive(bar(C::B_QDOREADY + st));
-      return true;
-    };
-    // owner side of the dQ exchange: rows [r0, r1) of every step's tile
-    const int rows_max = (128 + nkt - 1) / nkt;
+   }
+  } else if (warp >= C::WARP_DQ) {
+    reg_dealloc<C::REG_OTHER>();
+    // ---------------------------------------------------------------- dQ warps: TMEM -> owners -> BF16
+    const int dt = tid - C::WARP_DQ * 32;   // 0..127
+    const int jl = (warp - C::WARP_DQ) * 32 + lane;  // query row of the partial = TMEM lane
+    const uint32_t lb = (uint32_t)((warp - C::WARP_DQ) * 32) << 16;
     const uint32_t rb_bytes = (uint32_t)(nkt * (r1 - r0) * HD * 4);
-    int prev_i = 0, prev_jt = 0, red = 0;  // red = steps reduced so far
-    if (tid == 0) mbar_arrive_expect_tx(bar(C::B_RFULL), rb_bytes);  // arm step 0
+    int o = (jl * nkt) >> 7;  // owner of row jl: o*128/n <= jl < (o+1)*128/n
+    while (o + 1 < nkt && (int)((o + 1) * 128 / nkt) <= jl) ++o;
+    while ((int)(o * 128 / nkt) > jl) --o;
+    // step t's partial goes to receive slot t % 2 of its owner
+    const uint32_t dst0 = mapa_shared(sb0 + C::OFF_RB + ((rank * rows_max + (jl - (int)(o * 128 / nkt))) * HD) * 4, o);
+    const uint32_t rbar0 = mapa_shared(bar(C::B_RFULL), o);
+    if (dt == 0) {  // arm slots 0 and 1 for steps 0 and 1
+      mbar_arrive_expect_tx(bar(C::B_RFULL), rb_bytes);
+      if (T > 1) mbar_arrive_expect_tx(bar(C::B_RFULL + 1), rb_bytes);
+    }
+    int prev_i = 0, prev_jt = 0, red = 0;
     auto reduce_prev = [&]() -> bool {
-      if (!wait_bar_cluster_warp(bar(C::B_RFULL), red & 1, ab)) return false;
-      if (tid == 0 && red + 1 < T) mbar_arrive_expect_tx(bar(C::B_RFULL), rb_bytes);  // arm the next step
+      const int slot = red & 1;
+      if (!wait_bar_cluster_warp(bar(C::B_RFULL + slot), (red >> 1) & 1, ab)) return false;
+      if (dt == 0 && red + 2 < T) mbar_arrive_expect_tx(bar(C::B_RFULL + slot), rb_bytes);  // arm step red + 2
       constexpr int CPR = HD / 4;
       const int items = (r1 - r0) * CPR;
-      const float *rb = reinterpret_cast<const float *>(sm + C::OFF_RB);
-      for (int it = tid; it < items; it += C::NEWT) {
+      const float *rb = reinterpret_cast<const float *>(sm + C::OFF_RB + slot * C::RB_SLOT);
+      for (int it = dt; it < items; it += C::NDQT) {
         const int rl = it / CPR, c = it % CPR;
         float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int r = 0; r < nkt; ++r) {  // fixed order: key tile 0, 1, ..., n-1
@@ -349,142 +455,152 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
         }
         const int j = prev_jt * 128 + r0 + rl;
         if (j < g.N) {
-          const uint2 o = make_uint2(
+          const uint2 w = make_uint2(
               (uint32_t)f32_to_bf16_rn(s4.x * g.scale) | ((uint32_t)f32_to_bf16_rn(s4.y * g.scale) << 16),
               (uint32_t)f32_to_bf16_rn(s4.z * g.scale) | ((uint32_t)f32_to_bf16_rn(s4.w * g.scale) << 16));
-          *reinterpret_cast<uint2 *>(dQ + pos_row(g, b, prev_i, j) * g.H * HD + h * HD + c * 4) = o;
+          *reinterpret_cast<uint2 *>(dQ + pos_row(g, b, prev_i, j) * g.H * HD + h * HD + c * 4) = w;
         }
       }
       __syncwarp();
       if (lane == 0)
-        for (int r = 0; r < nkt; ++r) mbar_arrive_cluster_relaxed(mapa_shared(bar(C::B_XEMPTY), r));
+        for (int r = 0; r < nkt; ++r) mbar_arrive_cluster_relaxed(mapa_shared(bar(C::B_XEMPTY + slot), r));
       ++red;
       return true;
     };
-    float acc[64];
+    bool ok = true;
+    int t = 0;
     for (int bi = 0; bi < nblk && ok; ++bi) {
-      const int i0 = s0 + bi * C::GB, nb = min(C::GB, s1 - i0);
-      ok = wait_bar_warp(bar(C::B_KVFULL), bi & 1, ab);
-      if (!ok) break;
-      convert_to_f16(sm + C::OFF_K, nb * C::TILE, tid, C::NEWT);
-      convert_to_f16(sm + C::OFF_V, nb * C::TILE, tid, C::NEWT);
-      if (half == 0)
-        for (int il = 0; il < nb; ++il) {
-          float mv = -INFINITY;
-          if (kg < g.N) mv = mask ? bf16_to_f32(mask[((int64_t)b * g.S + i0 + il) * g.N + kg]) * kLog2e : 0.f;
-          maskf[il * 128 + kl] = mv;
+      const int i0 = sc.block_first(bi), nb = sc.block_size(bi);
+      for (int jt = 0; jt < njt && ok; ++jt)
+        for (int il = 0; il < nb; ++il, ++t) {
+          ok = wait_bar_warp(bar(C::B_M2DONE), t & 1, ab);
+          if (!ok) break;
+          tc_fence_after();
+          uint32_t r[HD];
+          if constexpr (HD == 32) {
+            tmem_ld32(tb + lb + C::TDQ, r);
+          } else {
+            tmem_ld16(tb + lb + C::TDQ, r);
+          }
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(bar(C::B_DQREAD));
+          if (t > 0) {
+            ok = reduce_prev();  // owner duty for the previous step
+            if (!ok) break;
+          }
+          // slot t % 2 is free once every owner reduced step t - 2 from it
+          if (t > 1) ok = wait_bar_cluster_warp(bar(C::B_XEMPTY + (t & 1)), ((t - 2) >> 1) & 1, ab);
+          if (!ok) break;
+          {
+            const uint32_t dst = dst0 + (t & 1) * C::RB_SLOT, rbar = rbar0 + (t & 1) * 8;
+#pragma unroll
+            for (int c = 0; c < HD / 4; ++c)
+              st_async_f4(dst + c * 16, __uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1]),
+                          __uint_as_float(r[4 * c + 2]), __uint_as_float(r[4 * c + 3]), rbar);
+          }
+          prev_i = i0 + il;
+          prev_jt = jt;
         }
-      fence_proxy_async_smem();
-      mbar_arrive(bar(C::B_KVREADY));
-      named_sync(1, C::NEWT);
-      if (bi == 0) ok = convert_qdo(0);
+    }
+    if (ok && red < T) ok = reduce_prev();  // the last step's rows
+  } else {
+    reg_alloc<C::REG_EW>();
+    // ---------------------------------------------------------------- elementwise warps 0-7
+    const int q = warp & 3, half = warp >> 2;
+    const int kl = q * 32 + lane;  // key row of the tile = TMEM lane
+    const int kg = kt * 128 + kl;
+    const uint32_t lb = (uint32_t)(q * 32) << 16;
+    const uint32_t colA = tb + lb + C::TA + half * 64, colB = tb + lb + C::TB + half * 64;
+    const float c1 = g.scale * kLog2e;
+    const float2 c12 = make_float2(c1, c1), l2e2 = make_float2(kLog2e, kLog2e), m1x2 = make_float2(-1.f, -1.f);
+    const float *maskf = reinterpret_cast<const float *>(sm + C::OFF_MASK);
+    bool ok = true;
+    int t = 0, u = 0;
+    float2 acc[32];  // dBias tile row: queries half*64 + [0,64) as pairs
+    for (int bi = 0; bi < nblk && ok; ++bi) {
+      const int i0 = sc.block_first(bi), nb = sc.block_size(bi);
+      ok = wait_bar_warp(bar(C::B_KVREADY), bi & 1, ab);  // the mask rows of the block are in place
       for (int jt = 0; jt < njt && ok; ++jt) {
         const int bb = u & 1;
         ok = wait_bar_warp(bar(C::B_BFULL + bb), (u >> 1) & 1, ab);
         if (!ok) break;
 #pragma unroll
-        for (int e = 0; e < 64; ++e) acc[e] = 0.f;
+        for (int e = 0; e < 32; ++e) acc[e] = make_float2(0.f, 0.f);
         const uint32_t brow = sb0 + C::OFF_BIAS + bb * C::BIAS_TILE + half * 16384 + kl * 128;
         for (int il = 0; il < nb; ++il, ++t) {
-          const int st = t % C::NQS, i = i0 + il;
+          const int st = t % C::NQS;
           const float mk = maskf[il * 128 + kl];
           const bool dead = (mk == -INFINITY);
-          const float *sl = reinterpret_cast<const float *>(sm + C::OFF_LSE + st * 512);
-          const float *sd = reinterpret_cast<const float *>(sm + C::OFF_D + st * 512);
+          const float2 mk2 = make_float2(dead ? 0.f : mk, dead ? 0.f : mk);
+          const float *sl = reinterpret_cast<const float *>(sm + C::OFF_LSE + st * 512) + half * 64;
+          const float *sd = reinterpret_cast<const float *>(sm + C::OFF_D + st * 512) + half * 64;
           ok = wait_bar_warp(bar(C::B_SFULL), t & 1, ab);
           if (!ok) break;
           tc_fence_after();
-#pragma unroll
-          for (int sc = 0; sc < 4; ++sc) {  // 16 query columns at a time
-            const int jq0 = half * 64 + sc * 16;
-            uint32_t sv[16], dv[16];
-            tmem_ld16(tb + lb + jq0, sv);
-            tmem_ld16(tb + lb + 128 + jq0, dv);
+          uint32_t pw[32];  // P as FP16 pairs: the P^T operand and the factor of dS
+          {
+            uint32_t pv[64];  // S^T values of this thread's 64 queries
+            tmem_ld32(colA, *reinterpret_cast<uint32_t(*)[32]>(&pv[0]));
+            tmem_ld32(colA + 32, *reinterpret_cast<uint32_t(*)[32]>(&pv[32]));
             tmem_wait_ld();
-            uint32_t pw[8], dw[8];
+            tc_fence_before();
+            mbar_arrive(bar(C::B_SREAD));  // region A may now take S^T of the next step
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-              const int ch = sc * 2 + cc;  // 16-byte chunk (8 queries) within this query half
+            for (int ch = 0; ch < 8; ++ch) {  // 8 queries (one 16-byte bias chunk) at a time
               uint32_t bw[4];
               asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
                            : "=r"(bw[0]), "=r"(bw[1]), "=r"(bw[2]), "=r"(bw[3])
                            : "r"(brow + ((ch ^ (kl & 7)) << 4)));
-              float p8[8], ds8[8];
+              const float4 u0 = reinterpret_cast<const float4 *>(sl)[2 * ch];
+              const float4 u1 = reinterpret_cast<const float4 *>(sl)[2 * ch + 1];
+              const float2 uu[4] = {make_float2(u0.x, u0.y), make_float2(u0.z, u0.w), make_float2(u1.x, u1.y),
+                                    make_float2(u1.z, u1.w)};
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const int x = cc * 8 + e, jl = jq0 + x;
-                const float bv = (e & 1) ? __uint_as_float(bw[e >> 1] & 0xffff0000u) : __uint_as_float(bw[e >> 1] << 16);
-                const float arg = fmaf(__uint_as_float(sv[x]), c1, fmaf(bv, kLog2e, sl[jl] + mk));
-                const float p = dead ? 0.f : ex2(arg);
-                const float ds = p * (__uint_as_float(dv[x]) - sd[jl]);
-                acc[sc * 16 + x] += ds;
-                p8[e] = p;
-                ds8[e] = ds;
+              for (int e2 = 0; e2 < 4; ++e2) {
+                const int x = ch * 8 + 2 * e2;
+                const float2 bv = make_float2(__uint_as_float(bw[e2] << 16), __uint_as_float(bw[e2] & 0xffff0000u));
+                const float2 base = __ffma2_rn(bv, l2e2, __fadd2_rn(uu[e2], mk2));
+                const float2 arg = __ffma2_rn(make_float2(__uint_as_float(pv[x]), __uint_as_float(pv[x + 1])), c12, base);
+                pw[x >> 1] = pack_f16x2(dead ? 0.f : ex2(arg.x), dead ? 0.f : ex2(arg.y));
               }
+            }
+          }
+          ok = wait_bar_warp(bar(C::B_DPFULL), t & 1, ab);
+          if (!ok) break;
+          tc_fence_after();
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                pw[cc * 4 + e] = pack_f16x2(p8[2 * e], p8[2 * e + 1]);
-                dw[cc * 4 + e] = pack_f16x2(ds8[2 * e], ds8[2 * e + 1]);
-              }
-              // dS (FP16) into the MN-major SW128 tile read by the dQ MMA: row kl, query chunk ch of half `half`
-              const uint32_t da = sb0 + C::OFF_DS + (kl >> 3) * 2048 + half * 1024 + (kl & 7) * 128 + ((ch ^ (kl & 7)) << 4);
+          for (int c2 = 0; c2 < 4; ++c2) {  // 16 queries at a time
+            uint32_t dv[16];
+            tmem_ld16(colB + c2 * 16, dv);
+            tmem_wait_ld();
+            uint32_t dw[8];
+#pragma unroll
+            for (int e2 = 0; e2 < 8; ++e2) {
+              const int x0 = c2 * 16 + 2 * e2;
+              const float2 dd = reinterpret_cast<const float2 *>(sd)[x0 >> 1];
+              const float2 dp = make_float2(__uint_as_float(dv[2 * e2]), __uint_as_float(dv[2 * e2 + 1]));
+              const float2 pp = __half22float2(*reinterpret_cast<const __half2 *>(&pw[x0 >> 1]));
+              const float2 ds = __fmul2_rn(pp, __ffma2_rn(dd, m1x2, dp));  // p (dp - D)
+              acc[x0 >> 1] = __fadd2_rn(acc[x0 >> 1], ds);
+              dw[e2] = pack_f16x2(ds.x, ds.y);
+            }
+            tmem_st8(colB + c2 * 8, dw);  // over columns already read
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {  // dS (FP16) into the MN-major SW128 tile of the dQ MMA
+              const int ch = c2 * 2 + cc;
+              const uint32_t da =
+                  sb0 + C::OFF_DS + (kl >> 3) * 2048 + half * 1024 + (kl & 7) * 128 + ((ch ^ (kl & 7)) << 4);
               asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(da), "r"(dw[cc * 4]), "r"(dw[cc * 4 + 1]),
                            "r"(dw[cc * 4 + 2]), "r"(dw[cc * 4 + 3])
                            : "memory");
             }
-            tmem_st8(tb + lb + half * 64 + sc * 8, pw);
-            tmem_st8(tb + lb + 128 + half * 64 + sc * 8, dw);
           }
+          tmem_st32(colB + 32, pw);
           fence_proxy_async_smem();
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(bar(C::B_PFULL));
-          if (t + 1 < T) {
-            ok = convert_qdo(t + 1);
-            if (!ok) break;
-          }
-          // ---- owner duty: reduce the previous step's dQ rows (all n partials have been pushed)
-          if (t > 0) {
-            ok = reduce_prev();
-            if (!ok) break;
-          }
-          // ---- this step's dQ partial: TMEM lanes = queries, this thread has query kl, half of d
-          ok = wait_bar_warp(bar(C::B_M2DONE), t & 1, ab);
-          if (!ok) break;
-          tc_fence_after();
-          float dqv[HD / 2];
-          if constexpr (HD == 32) {
-            uint32_t r[16];
-            tmem_ld16(tb + lb + 96 + half * 16, r);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 16; ++e) dqv[e] = __uint_as_float(r[e]);
-          } else {
-            uint32_t r[8];
-            tmem_ld8(tb + lb + 96 + half * 8, r);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 8; ++e) dqv[e] = __uint_as_float(r[e]);
-          }
-          tc_fence_before();
-          mbar_arrive(bar(C::B_DQREAD));
-          // every owner has finished reading its receive buffer for the previous step
-          if (t > 0) ok = wait_bar_cluster_warp(bar(C::B_XEMPTY), (t - 1) & 1, ab);
-          if (!ok) break;
-          {
-            // push row kl of this partial to its owner: rank o with o*128/n <= kl < (o+1)*128/n
-            int o = (kl * nkt) >> 7;
-            while (o + 1 < nkt && (int)((o + 1) * 128 / nkt) <= kl) ++o;
-            while ((int)(o * 128 / nkt) > kl) --o;
-            const int rl = kl - (int)(o * 128 / nkt);
-            const uint32_t dst = mapa_shared(sb0 + C::OFF_RB + ((rank * rows_max + rl) * HD + half * (HD / 2)) * 4, o);
-            const uint32_t rbar = mapa_shared(bar(C::B_RFULL), o);
-#pragma unroll
-            for (int c = 0; c < HD / 8; ++c)
-              st_async_f4(dst + c * 16, dqv[4 * c], dqv[4 * c + 1], dqv[4 * c + 2], dqv[4 * c + 3], rbar);
-          }
-          prev_i = i;
-          prev_jt = jt;
         }
         if (!ok) break;
         // ---- dBias tile (jt, kt) of this block into the supergroup partial (FP32, [k][j], owned by this CTA)
@@ -493,35 +609,33 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
               partial + ((((int64_t)grp * g.B + b) * g.H + h) * NP + kg) * NP + jt * 128 + half * 64);
           if (bi == 0) {
 #pragma unroll
-            for (int c = 0; c < 16; ++c) pp[c] = make_float4(acc[4 * c], acc[4 * c + 1], acc[4 * c + 2], acc[4 * c + 3]);
+            for (int c = 0; c < 16; ++c)
+              pp[c] = make_float4(acc[2 * c].x, acc[2 * c].y, acc[2 * c + 1].x, acc[2 * c + 1].y);
           } else {
+            float4 old[16];
 #pragma unroll
-            for (int c0 = 0; c0 < 16; c0 += 8) {
-              float4 old[8];
+            for (int c = 0; c < 16; ++c) old[c] = pp[c];
 #pragma unroll
-              for (int c = 0; c < 8; ++c) old[c] = pp[c0 + c];
-#pragma unroll
-              for (int c = 0; c < 8; ++c)
-                pp[c0 + c] = make_float4(old[c].x + acc[4 * (c0 + c)], old[c].y + acc[4 * (c0 + c) + 1],
-                                         old[c].z + acc[4 * (c0 + c) + 2], old[c].w + acc[4 * (c0 + c) + 3]);
-            }
+            for (int c = 0; c < 16; ++c)
+              pp[c] = make_float4(old[c].x + acc[2 * c].x, old[c].y + acc[2 * c].y, old[c].z + acc[2 * c + 1].x,
+                                  old[c].w + acc[2 * c + 1].y);
           }
         }
         mbar_arrive(bar(C::B_BFREE + bb));
         ++u;
       }
       if (!ok) break;
-      // ---- dK_i, dV_i of the block -> BF16 (all MMAs of the block are complete: M2DONE of its last step)
+      // ---- dK_i, dV_i of the block -> BF16, once the block's last MMAs are complete
+      ok = wait_bar_warp(bar(C::B_M2DONE), (t - 1) & 1, ab);
+      if (!ok) break;
+      tc_fence_after();
       for (int il = 0; il < nb; ++il) {
         uint32_t r[32];
-        const uint32_t col = tb + lb + 256 + il * 2 * HD + half * HD;
+        const uint32_t col = tb + lb + C::TDKV + il * 2 * HD + half * HD;
         if constexpr (HD == 32) {
           tmem_ld32(col, r);
         } else {
-          uint32_t r16[16];
-          tmem_ld16(col, r16);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) r[e] = r16[e];
+          tmem_ld16(col, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
         }
         tmem_wait_ld();
         if (kg < g.N) {
@@ -540,11 +654,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
       tc_fence_before();
       mbar_arrive(bar(C::B_DKVREAD));
     }
-    if (ok && red < T) ok = reduce_prev();  // the last step's dQ rows
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();  // no CTA leaves while a peer may still read its shared memory
+  cluster_sync_all();  // no CTA leaves while a peer may still write or read its shared memory
   if (warp == C::WARP_MMA) {
     tc_fence_after();
     tmem_dealloc(tb, C::TMEM_COLS);
@@ -622,6 +735,13 @@ cudaError_t launch_bwd_main_t(const Dims &g, int Gp, const uint16_t *Q, const ui
   if (!attr) {
     e = cudaFuncSetAttribute(bwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
+    // The setmaxnreg split moves registers between warpgroups within the block's
+    // launch allocation; it only balances if the kernel was built with exactly
+    // REG_LAUNCH registers per thread, so refuse to launch otherwise.
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, bwd_kernel<HD>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != (int)C::REG_LAUNCH) return cudaErrorInvalidConfiguration;
     attr = true;
   }
   cudaLaunchConfig_t cfg = {};

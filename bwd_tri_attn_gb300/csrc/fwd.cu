@@ -17,9 +17,13 @@
 // rounding on the output's path would add as much error as the output rounding
 // itself. V is converted BF16 -> FP16 in shared memory (exact in FP16 range).
 //
-// Warp roles (192 threads): warps 0-3 = softmax (thread = query row = TMEM
-// lane), warp 4 = TMA producer + V conversion, warp 5 = MMA issuer + TMEM owner.
-// TMEM columns: S double buffer [0,128) [128,256); O_i at 256 + i*d.
+// Warp roles (352 threads): warps 0-7 = softmax (two threads per query row =
+// TMEM lane, each owning 64 of the tile's 128 keys; the row maximum is swapped
+// through shared memory), warp 8 = TMA producer, warp 9 = MMA issuer + TMEM
+// owner, warp 10 = V conversion to FP16. TMEM columns: three S buffers
+// [0,128) [128,256) [256,384), with P written as FP16 pairs over the columns
+// each thread has already read (keys 0-63 -> cols 0-31, keys 64-127 -> cols
+// 64-95 of the buffer); O_i at 384 + i*d.
 // The online max is updated lazily (only when it grows by more than 2^8), and
 // O is rescaled in TMEM only then.
 #include "common.cuh"
@@ -46,27 +50,31 @@ struct FwdCfg {
   static constexpr int OFF_BS = OFF_BF + 128 * 512;         // BF16 bias staging rows: 128 x 256 B
   static constexpr int OFF_MASK = OFF_BS + 128 * 256;       // FP32 mask*log2e [GF][NMAX]
   static constexpr int OFF_FLAG = OFF_MASK + GF * NMAX * 4; // int [GF][MAXKT]: tile has a nonzero mask
-  static constexpr int OFF_BAR = OFF_FLAG + GF * MAXKT * 4;
+  static constexpr int OFF_XCH = OFF_FLAG + GF * MAXKT * 4;  // row-max exchange [2][2][128] + row sums [GF][2][128]
+  static constexpr int OFF_BAR = OFF_XCH + (4 + 2 * GF) * 128 * 4;
   // barrier indices
   static constexpr int B_Q = 0;
   static constexpr int B_KVFULL = 1;
   static constexpr int B_VREADY = B_KVFULL + NST;
   static constexpr int B_KVEMPTY = B_VREADY + NST;
+  static constexpr int NSB = 3;                 // S buffers in TMEM
   static constexpr int B_SFULL = B_KVEMPTY + NST;
-  static constexpr int B_PFULL = B_SFULL + 2;
-  static constexpr int B_SFREE = B_PFULL + 2;
-  static constexpr int B_PVDONE = B_SFREE + 2;
+  static constexpr int B_PFULL = B_SFULL + NSB;
+  static constexpr int B_SFREE = B_PFULL + NSB;
+  static constexpr int B_PVDONE = B_SFREE + NSB;
   static constexpr int B_OFINAL = B_PVDONE + GF;
   static constexpr int NBAR = B_OFINAL + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // [0] TMEM base, [1] abort flag
   static constexpr int SMEM_ALLOC = OFF_MISC + 16 + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
-  static_assert(256 + GF * HD <= 512, "TMEM budget");
+  static constexpr int NSOFT = 8, WARP_TMA = 8, WARP_MMA = 9, WARP_CV = 10, NTHREADS = 352;
+  static constexpr uint32_t TO = NSB * 128;  // O accumulators: TO + i*d
+  static_assert(TO + GF * HD <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 };
 
 template <int HD>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(FwdCfg<HD>::NTHREADS, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
            const __grid_constant__ CUtensorMap mV, const Dims g, const uint16_t *__restrict__ bias,
            const uint16_t *__restrict__ mask, uint16_t *__restrict__ O, float *__restrict__ LSE,
@@ -93,9 +101,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
       mbar_init(bar(C::B_VREADY + s), 1);
       mbar_init(bar(C::B_KVEMPTY + s), 1);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < C::NSB; ++s) {
       mbar_init(bar(C::B_SFULL + s), 1);
-      mbar_init(bar(C::B_PFULL + s), 128);
+      mbar_init(bar(C::B_PFULL + s), 256);
       mbar_init(bar(C::B_SFREE + s), 1);
     }
     for (int s = 0; s < C::GF; ++s) mbar_init(bar(C::B_PVDONE + s), 1);
@@ -103,7 +111,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
     misc[1] = 0;
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == C::WARP_MMA) {
     tmem_alloc(sb0 + C::OFF_MISC, C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -112,7 +120,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
   tc_fence_after();
   const uint32_t tbase = misc[0];
 
-  if (warp == 4) {
+  if (warp == C::WARP_TMA) {
     // ------------------------------------------------------------ producer
     int issued = 0;
     if (lane == 0) {
@@ -123,59 +131,58 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
       for (int il = 0; il < ng; ++il)
         tma_load_4d(sb0 + C::OFF_Q + il * C::TILE, &mQ, bar(C::B_Q), 0, h, jt * 128, b * g.S + i0 + il);
     }
-    constexpr int LAG = C::NST - 1;
     bool ok = true;
-    for (int t = 0; t < T + LAG && ok; ++t) {
-      if (t < T) {
-        const int st = t % C::NST, use = t / C::NST;
-        if (use > 0) ok = wait_bar_warp(bar(C::B_KVEMPTY + st), (use - 1) & 1, ab);
-        if (!ok) break;
-        if (lane == 0) {
-          const int kt = t / ng, il = t % ng;
-          mbar_arrive_expect_tx(bar(C::B_KVFULL + st), 2 * C::TILE);
-          tma_load_4d(sb0 + C::OFF_K + st * C::TILE, &mK, bar(C::B_KVFULL + st), 0, h, kt * 128, b * g.S + i0 + il);
-          tma_load_4d(sb0 + C::OFF_V + st * C::TILE, &mV, bar(C::B_KVFULL + st), 0, h, kt * 128, b * g.S + i0 + il);
-        }
-        issued = t + 1;
+    for (int t = 0; t < T && ok; ++t) {
+      const int st = t % C::NST, use = t / C::NST;
+      if (use > 0) ok = wait_bar_warp(bar(C::B_KVEMPTY + st), (use - 1) & 1, ab);
+      if (!ok) break;
+      if (lane == 0) {
+        const int kt = t / ng, il = t % ng;
+        mbar_arrive_expect_tx(bar(C::B_KVFULL + st), 2 * C::TILE);
+        tma_load_4d(sb0 + C::OFF_K + st * C::TILE, &mK, bar(C::B_KVFULL + st), 0, h, kt * 128, b * g.S + i0 + il);
+        tma_load_4d(sb0 + C::OFF_V + st * C::TILE, &mV, bar(C::B_KVFULL + st), 0, h, kt * 128, b * g.S + i0 + il);
       }
-      const int tc = t - LAG;
-      if (tc >= 0) {
-        const int st = tc % C::NST, use = tc / C::NST;
-        ok = wait_bar_warp(bar(C::B_KVFULL + st), use & 1, ab);
-        if (!ok) break;
-        uint4 *v = reinterpret_cast<uint4 *>(sm + C::OFF_V + st * C::TILE);
-        for (int e = lane; e < C::TILE / 16; e += 32) {
-          uint4 w = v[e];
-          w.x = bf16x2_to_f16x2(w.x);
-          w.y = bf16x2_to_f16x2(w.y);
-          w.z = bf16x2_to_f16x2(w.z);
-          w.w = bf16x2_to_f16x2(w.w);
-          v[e] = w;
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(C::B_VREADY + st));
-      }
+      issued = t + 1;
     }
     if (!ok && lane == 0) {
       // drain loads still in flight before the CTA's shared memory goes away
       drain_bar(bar(C::B_Q), 0);
       for (int t = max(0, issued - C::NST); t < issued; ++t) drain_bar(bar(C::B_KVFULL + t % C::NST), (t / C::NST) & 1);
     }
-  } else if (warp == 5) {
+  } else if (warp == C::WARP_CV) {
+    // ------------------------------------------------------------ V: BF16 -> FP16 in shared memory
+    bool ok = true;
+    for (int t = 0; t < T && ok; ++t) {
+      const int st = t % C::NST, use = t / C::NST;
+      ok = wait_bar_warp(bar(C::B_KVFULL + st), use & 1, ab);
+      if (!ok) break;
+      uint4 *v = reinterpret_cast<uint4 *>(sm + C::OFF_V + st * C::TILE);
+      for (int e = lane; e < C::TILE / 16; e += 32) {
+        uint4 w = v[e];
+        w.x = bf16x2_to_f16x2(w.x);
+        w.y = bf16x2_to_f16x2(w.y);
+        w.z = bf16x2_to_f16x2(w.z);
+        w.w = bf16x2_to_f16x2(w.w);
+        v[e] = w;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::B_VREADY + st));
+    }
+  } else if (warp == C::WARP_MMA) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idS = idesc_f16(128, 128, true, true, false, false);
       constexpr uint32_t idPV = idesc_f16(128, HD, false, false, false, true);
       auto issue_pv = [&](int t) -> bool {
-        const int kt = t / ng, il = t % ng, sbuf = t & 1, st = t % C::NST;
-        if (!wait_bar(bar(C::B_PFULL + sbuf), (t >> 1) & 1, ab)) return false;
+        const int kt = t / ng, il = t % ng, sbuf = t % C::NSB, st = t % C::NST;
+        if (!wait_bar(bar(C::B_PFULL + sbuf), (t / C::NSB) & 1, ab)) return false;
         if (!wait_bar(bar(C::B_VREADY + st), (t / C::NST) & 1, ab)) return false;
         tc_fence_after();
         const uint32_t vaddr = sb0 + C::OFF_V + st * C::TILE;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          mma_ts(tbase + 256 + il * HD, tbase + sbuf * 128 + ks * 8,
+          mma_ts(tbase + C::TO + il * HD, tbase + sbuf * 128 + (ks >> 2) * 64 + (ks & 3) * 8,
                  smem_desc(vaddr + ks * 16 * C::ROWB, 16, 8 * C::ROWB, C::SW), idPV, (kt > 0 || ks > 0) ? 1u : 0u);
         mma_commit(bar(C::B_SFREE + sbuf));
         mma_commit(bar(C::B_KVEMPTY + st));
@@ -184,9 +191,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
       };
       bool ok = wait_bar(bar(C::B_Q), 0, ab);
       for (int t = 0; t < T && ok; ++t) {
-        const int st = t % C::NST, sbuf = t & 1, il = t % ng;
+        const int st = t % C::NST, sbuf = t % C::NSB, il = t % ng;
         ok = wait_bar(bar(C::B_KVFULL + st), (t / C::NST) & 1, ab);
-        if (ok && t >= 2) ok = wait_bar(bar(C::B_SFREE + sbuf), ((t - 2) >> 1) & 1, ab);
+        if (ok && t >= C::NSB) ok = wait_bar(bar(C::B_SFREE + sbuf), ((t / C::NSB) - 1) & 1, ab);
         if (!ok) break;
         tc_fence_after();
         const uint32_t qaddr = sb0 + C::OFF_Q + il * C::TILE, kaddr = sb0 + C::OFF_K + st * C::TILE;
@@ -202,64 +209,63 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
       drain_bar(bar(C::B_OFINAL), 0);
     }
   } else {
-    // ------------------------------------------------------------ softmax / epilogue (warps 0-3)
-    const int row = tid;
+    // ------------------------------------------------------------ softmax / epilogue (warps 0-7)
+    // Two threads per query row: warp w handles TMEM lane quarter q = w % 4 and
+    // the key half w / 4 (64 of the tile's 128 keys).
+    const int q = warp & 3, half = warp >> 2;
+    const int row = q * 32 + lane;
     const int j = jt * 128 + row;
     const int jr = min(j, g.N - 1);  // rows past N reuse a valid bias row; their outputs are dropped
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    const uint32_t pair_bar = 2 + q;  // named barrier of the two warps sharing these rows
     float *maskf = reinterpret_cast<float *>(sm + C::OFF_MASK);
     int *flags = reinterpret_cast<int *>(sm + C::OFF_FLAG);
+    float *xmax = reinterpret_cast<float *>(sm + C::OFF_XCH);  // [2 parities][2 halves][128 rows]
     const float c1 = g.scale * kLog2e;
+    const float2 c1x2 = make_float2(c1, c1);
 
-    // per-slice additive mask (log2 units) and per-tile "has a nonzero entry" flags
-    if (row < C::GF * C::MAXKT) flags[row] = 0;
-    named_sync(1, 128);
-    if (mask) {
-      for (int il = 0; il < ng; ++il)
-        for (int k = row; k < nkt * 128; k += 128) {
-          const float v = k < g.N ? bf16_to_f32(mask[((int64_t)b * g.S + i0 + il) * g.N + k]) * kLog2e : 0.f;
-          maskf[il * C::NMAX + k] = v;
-          if (v != 0.f) flags[il * C::MAXKT + (k >> 7)] = 1;  // every writer stores the same value
-        }
-    }
-    named_sync(1, 128);
-
+    // bias row: this thread stages and converts its half (64 keys) of row jr for every key tile
     const uint16_t *brow = bias + (((int64_t)b * g.H + h) * g.N + jr) * g.N;
     const uint32_t stage_row = sb0 + C::OFF_BS + row * 256;
+    const uint32_t bf_row = sb0 + C::OFF_BF + row * 512;
     const uint32_t sw = row & 7;
     auto stage_bias = [&](int kt) {
-      const int k0 = kt * 128, nv = min(128, g.N - k0);
+      const int k0 = kt * 128 + half * 64, nv = min(64, g.N - k0);
       const uint16_t *src = brow + k0;
-      if ((g.N & 7) == 0) {
-        for (int c = 0; c < nv / 8; ++c) cp_async_16(stage_row + ((c ^ sw) << 4), src + c * 8);
-      } else if ((g.N & 1) == 0) {
-        for (int p = 0; p < nv / 2; ++p) cp_async_4(stage_row + (((p >> 2) ^ sw) << 4) + (p & 3) * 4, src + 2 * p);
-      } else {
-        for (int e = 0; e < nv; ++e) {
-          const uint16_t v = src[e];
-          asm volatile("st.shared.u16 [%0], %1;" ::"r"(stage_row + (((e >> 3) ^ sw) << 4) + (e & 7) * 2), "h"(v));
+      if (nv > 0) {
+        if ((g.N & 7) == 0) {
+          for (int c = 0; c < nv / 8; ++c) cp_async_16(stage_row + (((half * 8 + c) ^ sw) << 4), src + c * 8);
+        } else if ((g.N & 1) == 0) {
+          for (int p = 0; p < nv / 2; ++p)
+            cp_async_4(stage_row + (((half * 8 + (p >> 2)) ^ sw) << 4) + (p & 3) * 4, src + 2 * p);
+        } else {
+          for (int e = 0; e < nv; ++e) {
+            const uint16_t v = src[e];
+            asm volatile("st.shared.u16 [%0], %1;" ::"r"(stage_row + (((half * 8 + (e >> 3)) ^ sw) << 4) + (e & 7) * 2),
+                         "h"(v));
+          }
         }
       }
       cp_async_commit();
     };
-    const uint32_t bf_row = sb0 + C::OFF_BF + row * 512;
     auto convert_bias = [&](int kt) {
-      const int nv = min(128, g.N - kt * 128);
-#pragma unroll 4
-      for (int c = 0; c < 16; ++c) {
+      const int nv = min(64, g.N - kt * 128 - half * 64);
+#pragma unroll 2
+      for (int cl = 0; cl < 8; ++cl) {
+        const int c = half * 8 + cl;
         uint32_t w[4];
         asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
                      : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
                      : "r"(stage_row + ((c ^ sw) << 4)));
         float f[8];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          f[2 * q] = __uint_as_float(w[q] << 16) * kLog2e;
-          f[2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u) * kLog2e;
+        for (int qq = 0; qq < 4; ++qq) {
+          f[2 * qq] = __uint_as_float(w[qq] << 16) * kLog2e;
+          f[2 * qq + 1] = __uint_as_float(w[qq] & 0xffff0000u) * kLog2e;
         }
 #pragma unroll
         for (int e = 0; e < 8; ++e)
-          if (c * 8 + e >= nv) f[e] = -INFINITY;
+          if (cl * 8 + e >= nv) f[e] = -INFINITY;
         asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(bf_row + (((2 * c) ^ sw) << 4)), "f"(f[0]),
                      "f"(f[1]), "f"(f[2]), "f"(f[3])
                      : "memory");
@@ -269,13 +275,40 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
       }
     };
 
-    float m_ref[C::GF], l_sum[C::GF];
+    stage_bias(0);  // first bias tile in flight while the mask rows load
+    // per-slice additive mask (log2 units) and per-tile "has a nonzero entry" flags
+    if (tid < C::GF * C::MAXKT) flags[tid] = 0;
+    named_sync(1, 256);
+    if (mask) {
+      for (int il0 = 0; il0 < ng; il0 += 2) {  // two slices per memory round trip
+        float v[2][C::NMAX / 256];
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+          for (int m = 0; m < C::NMAX / 256; ++m) {
+            const int il = il0 + a, k = tid + 256 * m;
+            v[a][m] = (il < ng && k < g.N) ? bf16_to_f32(mask[((int64_t)b * g.S + i0 + il) * g.N + k]) * kLog2e : 0.f;
+          }
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+          for (int m = 0; m < C::NMAX / 256; ++m) {
+            const int il = il0 + a, k = tid + 256 * m;
+            if (il < ng && k < nkt * 128) {
+              maskf[il * C::NMAX + k] = v[a][m];
+              if (v[a][m] != 0.f) flags[il * C::MAXKT + (k >> 7)] = 1;  // every writer stores the same value
+            }
+          }
+      }
+    }
+    named_sync(1, 256);
+
+    float m_ref[C::GF], l_sum[C::GF];  // m_ref is identical in both threads of a row; l_sum is per half
 #pragma unroll
     for (int il = 0; il < C::GF; ++il) {
       m_ref[il] = -INFINITY;
       l_sum[il] = 0.f;
     }
-    stage_bias(0);
     bool ok = true;
     for (int kt = 0; kt < nkt && ok; ++kt) {
       cp_async_wait_all();
@@ -283,46 +316,55 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
       if (kt + 1 < nkt) stage_bias(kt + 1);
 #pragma unroll 1
       for (int il = 0; il < ng; ++il) {
-        const int t = kt * ng + il, sbuf = t & 1;
-        ok = wait_bar_warp(bar(C::B_SFULL + sbuf), (t >> 1) & 1, ab);
+        const int t = kt * ng + il, sbuf = t % C::NSB;
+        ok = wait_bar_warp(bar(C::B_SFULL + sbuf), (t / C::NSB) & 1, ab);
         if (!ok) break;
         tc_fence_after();
-        float x[128];
+        const uint32_t scol = tbase + lane_base + sbuf * 128 + half * 64;
+        float2 x[32];
         {
-          uint32_t r[128];
-#pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4)
-            tmem_ld32(tbase + lane_base + sbuf * 128 + c4 * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[c4 * 32]));
+          uint32_t r[64];
+          tmem_ld32(scol, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+          tmem_ld32(scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
           tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 128; ++e) x[e] = __uint_as_float(r[e]);
+          for (int e = 0; e < 32; ++e) x[e] = make_float2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
         }
-        float mt = -INFINITY;
+        // scores in log2 units: S*scale*log2e + bias*log2e (+ mask*log2e)
 #pragma unroll
-        for (int ch = 0; ch < 32; ++ch) {
+        for (int ch = 0; ch < 16; ++ch) {
           float4 bv;
           asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
                        : "=f"(bv.x), "=f"(bv.y), "=f"(bv.z), "=f"(bv.w)
-                       : "r"(bf_row + ((ch ^ sw) << 4)));
-          x[4 * ch + 0] = fmaf(x[4 * ch + 0], c1, bv.x);
-          x[4 * ch + 1] = fmaf(x[4 * ch + 1], c1, bv.y);
-          x[4 * ch + 2] = fmaf(x[4 * ch + 2], c1, bv.z);
-          x[4 * ch + 3] = fmaf(x[4 * ch + 3], c1, bv.w);
+                       : "r"(bf_row + (((half * 16 + ch) ^ sw) << 4)));
+          x[2 * ch] = __ffma2_rn(x[2 * ch], c1x2, make_float2(bv.x, bv.y));
+          x[2 * ch + 1] = __ffma2_rn(x[2 * ch + 1], c1x2, make_float2(bv.z, bv.w));
         }
         if (flags[il * C::MAXKT + kt]) {
-          const float *mrow = maskf + il * C::NMAX + kt * 128;
+          const float2 *mrow = reinterpret_cast<const float2 *>(maskf + il * C::NMAX + kt * 128 + half * 64);
 #pragma unroll
-          for (int k = 0; k < 128; ++k) x[k] += mrow[k];
+          for (int e = 0; e < 32; ++e) x[e] = __fadd2_rn(x[e], mrow[e]);
         }
+        float mloc;
+        {
+          float m4[4];
 #pragma unroll
-        for (int k = 0; k < 128; ++k) mt = fmaxf(mt, x[k]);
-        // lazy online-softmax rescale
+          for (int c = 0; c < 4; ++c) m4[c] = fmaxf(x[c].x, x[c].y);
+#pragma unroll
+          for (int e = 4; e < 32; ++e) m4[e & 3] = fmaxf(m4[e & 3], fmaxf(x[e].x, x[e].y));
+          mloc = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        }
+        // the row maximum over both key halves, exchanged through shared memory
+        xmax[((t & 1) * 2 + half) * 128 + row] = mloc;
+        named_sync(pair_bar, 64);
+        const float mt = fmaxf(mloc, xmax[((t & 1) * 2 + (half ^ 1)) * 128 + row]);
+        // lazy online-softmax rescale (the same decision in both threads of the row)
         float alpha = 1.f;
         bool resc = false;
         float mr = m_ref[0];
 #pragma unroll
-        for (int q = 1; q < C::GF; ++q)
-          if (q == il) mr = m_ref[q];
+        for (int qq = 1; qq < C::GF; ++qq)
+          if (qq == il) mr = m_ref[qq];
         if (kt == 0) {
           mr = mt;
         } else if (mt > mr + 8.f) {
@@ -338,49 +380,45 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
           ok = wait_bar_warp(bar(C::B_PVDONE + il), (kt - 1) & 1, ab);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t oaddr = tbase + lane_base + 256 + il * HD;
+          // this thread rescales its half of the row's O columns
+          const uint32_t oaddr = tbase + lane_base + C::TO + il * HD + half * (HD / 2);
           if constexpr (HD == 32) {
-            uint32_t r[32];
-            tmem_ld32(oaddr, r);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-            tmem_st32(oaddr, r);
-          } else {
             uint32_t r[16];
             tmem_ld16(oaddr, r);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
             tmem_st16(oaddr, r);
+          } else {
+            uint32_t r[8];
+            tmem_ld8(oaddr, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 8; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+            tmem_st8(oaddr, r);
           }
         }
         const float mu = (mr == -INFINITY) ? 0.f : mr;
-        float ls = 0.f;
-        uint32_t pk[64];
+        const float2 mu2 = make_float2(-mu, -mu);
+        float2 ls2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 64; ++e) {
-          const float p0 = ex2(x[2 * e] - mu), p1 = ex2(x[2 * e + 1] - mu);
-          ls += p0;
-          ls += p1;
-          pk[e] = pack_f16x2(p0, p1);
+        for (int e = 0; e < 32; ++e) {
+          const float2 a = __fadd2_rn(x[e], mu2);
+          const float2 pv = make_float2(ex2(a.x), ex2(a.y));
+          ls2[e & 3] = __fadd2_rn(ls2[e & 3], pv);
+          pk[e] = pack_f16x2(pv.x, pv.y);
         }
+        const float2 lsa = __fadd2_rn(__fadd2_rn(ls2[0], ls2[1]), __fadd2_rn(ls2[2], ls2[3]));
+        const float ls = lsa.x + lsa.y;
 #pragma unroll
-        for (int q = 0; q < C::GF; ++q)
-          if (q == il) {
-            m_ref[q] = mr;
-            l_sum[q] = l_sum[q] * alpha + ls;
+        for (int qq = 0; qq < C::GF; ++qq)
+          if (qq == il) {
+            m_ref[qq] = mr;
+            l_sum[qq] = l_sum[qq] * alpha + ls;
           }
-        {
-          uint32_t r0[32], r1[32];
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            r0[e] = pk[e];
-            r1[e] = pk[32 + e];
-          }
-          tmem_st32(tbase + lane_base + sbuf * 128, r0);
-          tmem_st32(tbase + lane_base + sbuf * 128 + 32, r1);
-        }
+        // P (FP16 pairs) over this thread's own S columns: keys half*64 + [0,64) -> cols half*64 + [0,32)
+        tmem_st32(scol, pk);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(C::B_PFULL + sbuf));
@@ -390,49 +428,50 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
     if (ok) ok = wait_bar_warp(bar(C::B_OFINAL), 0, ab);
     if (ok) {
       tc_fence_after();
+      float *xl = reinterpret_cast<float *>(sm + C::OFF_XCH) + 4 * 128;  // [GF][2 halves][128 rows]
+#pragma unroll
+      for (int qq = 0; qq < C::GF; ++qq) xl[(qq * 2 + half) * 128 + row] = l_sum[qq];
+      named_sync(pair_bar, 64);
 #pragma unroll 1
       for (int il = 0; il < ng; ++il) {
-        float lsum = 0.f, mref = -INFINITY;
+        const float lsum = xl[(il * 2 + 0) * 128 + row] + xl[(il * 2 + 1) * 128 + row];
+        float mref = -INFINITY;
 #pragma unroll
-        for (int q = 0; q < C::GF; ++q)
-          if (q == il) {
-            lsum = l_sum[q];
-            mref = m_ref[q];
-          }
-        uint32_t r[32];
+        for (int qq = 0; qq < C::GF; ++qq)
+          if (qq == il) mref = m_ref[qq];
+        uint32_t r[HD / 2];
+        const uint32_t oaddr = tbase + lane_base + C::TO + il * HD + half * (HD / 2);
         if constexpr (HD == 32) {
-          tmem_ld32(tbase + lane_base + 256 + il * HD, r);
+          tmem_ld16(oaddr, r);
         } else {
-          uint32_t r16[16];
-          tmem_ld16(tbase + lane_base + 256 + il * HD, r16);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) r[e] = r16[e];
+          tmem_ld8(oaddr, r);
         }
         tmem_wait_ld();
         if (j < g.N) {
           const int i = i0 + il;
           const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-          uint32_t ob[HD / 2], rb[HD / 2];
+          uint32_t ob[HD / 4], rb[HD / 4];
 #pragma unroll
-          for (int c = 0; c < HD / 2; ++c) {
+          for (int c = 0; c < HD / 4; ++c) {
             const float o0 = __uint_as_float(r[2 * c]) * inv, o1 = __uint_as_float(r[2 * c + 1]) * inv;
             const uint16_t a0 = f32_to_bf16_rn(o0), a1 = f32_to_bf16_rn(o1);
             ob[c] = (uint32_t)a0 | ((uint32_t)a1 << 16);
             rb[c] = (uint32_t)f32_to_bf16_rn(o0 - bf16_to_f32(a0)) |
                     ((uint32_t)f32_to_bf16_rn(o1 - bf16_to_f32(a1)) << 16);
           }
-          const int64_t off = pos_row(g, b, i, j) * g.H * HD + (int64_t)h * HD;
+          const int64_t off = pos_row(g, b, i, j) * g.H * HD + (int64_t)h * HD + half * (HD / 2);
           uint4 *od = reinterpret_cast<uint4 *>(O + off);
 #pragma unroll
-          for (int c = 0; c < HD / 8; ++c) od[c] = make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
+          for (int c = 0; c < HD / 16; ++c) od[c] = make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
           if (Ores) {
             uint4 *rd = reinterpret_cast<uint4 *>(Ores + off);
 #pragma unroll
-            for (int c = 0; c < HD / 8; ++c)
+            for (int c = 0; c < HD / 16; ++c)
               rd[c] = make_uint4(rb[4 * c], rb[4 * c + 1], rb[4 * c + 2], rb[4 * c + 3]);
           }
-          LSE[(((int64_t)b * g.S + i) * g.H + h) * g.N + j] =
-              lsum > 0.f ? (mref + __log2f(lsum)) * kLn2 : -INFINITY;
+          if (half == 0)
+            LSE[(((int64_t)b * g.S + i) * g.H + h) * g.N + j] =
+                lsum > 0.f ? (mref + __log2f(lsum)) * kLn2 : -INFINITY;
         }
       }
     }
@@ -440,7 +479,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == C::WARP_MMA) {
     tc_fence_after();
     tmem_dealloc(tbase, C::TMEM_COLS);
   }
@@ -464,7 +503,7 @@ cudaError_t launch_fwd_t(const Dims &g, const uint16_t *Q, const uint16_t *K, co
   }
   const int ngroups = (g.S + C::GF - 1) / C::GF;
   dim3 grid((g.N + 127) / 128, g.H, g.B * ngroups);
-  fwd_kernel<HD><<<grid, 192, C::SMEM_ALLOC, stream>>>(mq, mk, mv, g, bias, mask, O, LSE, Ores, status);
+  fwd_kernel<HD><<<grid, C::NTHREADS, C::SMEM_ALLOC, stream>>>(mq, mk, mv, g, bias, mask, O, LSE, Ores, status);
   return cudaGetLastError();
 }
 
