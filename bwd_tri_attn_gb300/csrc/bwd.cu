@@ -55,7 +55,7 @@ using namespace sm100;
 template <int HD>
 struct BwdCfg {
   static constexpr int GB = HD == 32 ? 3 : 7;  // slices per block: dK/dV of GB slices live in TMEM
-  static constexpr int NQS = 2;                // Q/dO stages
+  static constexpr int NQS = 3;                // Q/dO stages
   static constexpr int ROWB = HD * 2;
   static constexpr int TILE = 128 * ROWB;
   static constexpr uint32_t SW = HD == 32 ? kSwizzle64B : kSwizzle32B;
@@ -76,8 +76,9 @@ struct BwdCfg {
   static constexpr int OFF_BIAS = OFF_DO + NQS * TILE;     // 2 x [2 halves][128 rows][128 B], SW128
   static constexpr int OFF_DS = OFF_BIAS + 2 * BIAS_TILE;  // FP16 dS, MN-major SW128: [16 key groups][2][8][128 B]
   static constexpr int RB_SLOT = RB_ROWS * HD * 4;
-  static constexpr int OFF_RB = OFF_DS + 32768;            // dQ receive buffers: 2 x [sender][row][HD] FP32
-  static constexpr int OFF_LSE = OFF_RB + 2 * RB_SLOT;     // [NQS][128]: -LSE*log2e (or -inf)
+  static constexpr int NRB = 1;                            // dQ receive slots (step t uses slot t % NRB)
+  static constexpr int OFF_RB = OFF_DS + 32768;            // dQ receive buffers: NRB x [sender][row][HD] FP32
+  static constexpr int OFF_LSE = OFF_RB + NRB * RB_SLOT;   // [NQS][128]: -LSE*log2e (or -inf)
   static constexpr int OFF_D = OFF_LSE + NQS * 512;          // [NQS][128]: D
   static constexpr int OFF_MASK = OFF_D + NQS * 512;         // [GB][128]: mask*log2e of this CTA's keys
   static constexpr int OFF_BAR = OFF_MASK + GB * 512;
@@ -86,8 +87,8 @@ struct BwdCfg {
   static constexpr int B_BFULL = B_QDOFREE + NQS, B_BFREE = B_BFULL + 2;
   static constexpr int B_SFULL = B_BFREE + 2, B_SREAD = B_SFULL + 1, B_DPFULL = B_SREAD + 1;
   static constexpr int B_PFULL = B_DPFULL + 1, B_M2DONE = B_PFULL + 1, B_DQREAD = B_M2DONE + 1;
-  static constexpr int B_DKVREAD = B_DQREAD + 1, B_RFULL = B_DKVREAD + 1, B_XEMPTY = B_RFULL + 2;
-  static constexpr int B_FINAL = B_XEMPTY + 2, NBAR = B_FINAL + 1;
+  static constexpr int B_DKVREAD = B_DQREAD + 1, B_RFULL = B_DKVREAD + 1, B_XEMPTY = B_RFULL + NRB;
+  static constexpr int B_FINAL = B_XEMPTY + NRB, NBAR = B_FINAL + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_ALLOC = OFF_MISC + 16 + 1024;
   static_assert(OFF_BIAS % 1024 == 0 && OFF_DS % 1024 == 0, "SW128 tiles need 1 KB alignment");
@@ -188,7 +189,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
     mbar_init(bar(C::B_M2DONE), 1);
     mbar_init(bar(C::B_DQREAD), C::NDQT);
     mbar_init(bar(C::B_DKVREAD), C::NEWT);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < C::NRB; ++s) {
       mbar_init(bar(C::B_RFULL + s), 1);             // + the bytes pushed by all n senders
       mbar_init(bar(C::B_XEMPTY + s), C::NDQ * nkt);  // one arrive per dQ warp of every owner
     }
@@ -213,6 +214,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
     // ---------------------------------------------------------------- producer
     bool ok = true;
     int t = 0, u = 0, kv_issued = 0;
+    const uint64_t stream_pol = policy_evict_first();  // inputs are read once: keep L2 for the dBias partials
     if (lane == 0) {
       tma_prefetch_map(&mQ);
       tma_prefetch_map(&mK);
@@ -247,8 +249,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
           __syncwarp();
           if (lane == 0) {
             mbar_arrive_expect_tx(bar(C::B_QDOFULL + st), 2 * C::TILE);
-            tma_load_4d(sb0 + C::OFF_Q + st * C::TILE, &mQ, bar(C::B_QDOFULL + st), 0, h, jt * 128, b * g.S + i);
-            tma_load_4d(sb0 + C::OFF_DO + st * C::TILE, &mDO, bar(C::B_QDOFULL + st), 0, h, jt * 128, b * g.S + i);
+            tma_load_4d_hint(sb0 + C::OFF_Q + st * C::TILE, &mQ, bar(C::B_QDOFULL + st), 0, h, jt * 128, b * g.S + i,
+                             stream_pol);
+            tma_load_4d_hint(sb0 + C::OFF_DO + st * C::TILE, &mDO, bar(C::B_QDOFULL + st), 0, h, jt * 128,
+                             b * g.S + i, stream_pol);
           }
           if (jt == 0 && il == 0) {
             // K_i, V_i of the block (single-buffered: the previous block's MMAs must be done)
@@ -257,8 +261,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
             if (lane == 0) {
               mbar_arrive_expect_tx(bar(C::B_KVFULL), 2 * nb * C::TILE);
               for (int q = 0; q < nb; ++q) {
-                tma_load_4d(sb0 + C::OFF_K + q * C::TILE, &mK, bar(C::B_KVFULL), 0, h, kt * 128, b * g.S + i0 + q);
-                tma_load_4d(sb0 + C::OFF_V + q * C::TILE, &mV, bar(C::B_KVFULL), 0, h, kt * 128, b * g.S + i0 + q);
+                tma_load_4d_hint(sb0 + C::OFF_K + q * C::TILE, &mK, bar(C::B_KVFULL), 0, h, kt * 128, b * g.S + i0 + q,
+                                 stream_pol);
+                tma_load_4d_hint(sb0 + C::OFF_V + q * C::TILE, &mV, bar(C::B_KVFULL), 0, h, kt * 128, b * g.S + i0 + q,
+                                 stream_pol);
               }
             }
             kv_issued = bi + 1;
@@ -364,11 +370,14 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
         const bool has_next = t + 1 < T;
         const bool next_new_block = has_next && jt == 0 && il == 0;
         const int st1 = (t + 1) % C::NQS;
-        // S^T(t+1) ahead of this step's second group if region A has been read and Q(t+1) is
-        // ready already (never across a block change: that needs the new K)
+        // S^T(t+1) ahead of this step's second group, as soon as region A has been read (never
+        // across a block change: that needs the new K); the MMA thread has nothing else to
+        // issue before P(t) arrives
         bool s_early = false;
-        if (has_next && !next_new_block && mbar_try_wait(bar(C::B_QDOREADY + st1), ((t + 1) / C::NQS) & 1) &&
-            mbar_try_wait(bar(C::B_SREAD), t & 1)) {
+        if (has_next && !next_new_block) {
+          ok = wait_bar(bar(C::B_QDOREADY + st1), ((t + 1) / C::NQS) & 1, ab);
+          if (ok) ok = wait_bar(bar(C::B_SREAD), t & 1, ab);
+          if (!ok) break;
           tc_fence_after();
           issue_s(t + 1, il, st1);
           s_early = true;
@@ -428,18 +437,16 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
     int o = (jl * nkt) >> 7;  // owner of row jl: o*128/n <= jl < (o+1)*128/n
     while (o + 1 < nkt && (int)((o + 1) * 128 / nkt) <= jl) ++o;
     while ((int)(o * 128 / nkt) > jl) --o;
-    // step t's partial goes to receive slot t % 2 of its owner
+    // step t's partial goes to receive slot t % NRB of its owner
     const uint32_t dst0 = mapa_shared(sb0 + C::OFF_RB + ((rank * rows_max + (jl - (int)(o * 128 / nkt))) * HD) * 4, o);
     const uint32_t rbar0 = mapa_shared(bar(C::B_RFULL), o);
-    if (dt == 0) {  // arm slots 0 and 1 for steps 0 and 1
-      mbar_arrive_expect_tx(bar(C::B_RFULL), rb_bytes);
-      if (T > 1) mbar_arrive_expect_tx(bar(C::B_RFULL + 1), rb_bytes);
-    }
+    if (dt == 0)  // arm every slot for its first step
+      for (int s = 0; s < C::NRB && s < T; ++s) mbar_arrive_expect_tx(bar(C::B_RFULL + s), rb_bytes);
     int prev_i = 0, prev_jt = 0, red = 0;
     auto reduce_prev = [&]() -> bool {
-      const int slot = red & 1;
-      if (!wait_bar_cluster_warp(bar(C::B_RFULL + slot), (red >> 1) & 1, ab)) return false;
-      if (dt == 0 && red + 2 < T) mbar_arrive_expect_tx(bar(C::B_RFULL + slot), rb_bytes);  // arm step red + 2
+      const int slot = red % C::NRB;
+      if (!wait_bar_cluster_warp(bar(C::B_RFULL + slot), (red / C::NRB) & 1, ab)) return false;
+      if (dt == 0 && red + C::NRB < T) mbar_arrive_expect_tx(bar(C::B_RFULL + slot), rb_bytes);  // arm its next step
       constexpr int CPR = HD / 4;
       const int items = (r1 - r0) * CPR;
       const float *rb = reinterpret_cast<const float *>(sm + C::OFF_RB + slot * C::RB_SLOT);
@@ -489,11 +496,11 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
             ok = reduce_prev();  // owner duty for the previous step
             if (!ok) break;
           }
-          // slot t % 2 is free once every owner reduced step t - 2 from it
-          if (t > 1) ok = wait_bar_cluster_warp(bar(C::B_XEMPTY + (t & 1)), ((t - 2) >> 1) & 1, ab);
+          // slot t % NRB is free once every owner reduced step t - NRB from it
+          if (t >= C::NRB) ok = wait_bar_cluster_warp(bar(C::B_XEMPTY + t % C::NRB), ((t / C::NRB) - 1) & 1, ab);
           if (!ok) break;
           {
-            const uint32_t dst = dst0 + (t & 1) * C::RB_SLOT, rbar = rbar0 + (t & 1) * 8;
+            const uint32_t dst = dst0 + (t % C::NRB) * C::RB_SLOT, rbar = rbar0 + (t % C::NRB) * 8;
 #pragma unroll
             for (int c = 0; c < HD / 4; ++c)
               st_async_f4(dst + c * 16, __uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1]),
@@ -535,6 +542,11 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
           const float2 mk2 = make_float2(dead ? 0.f : mk, dead ? 0.f : mk);
           const float *sl = reinterpret_cast<const float *>(sm + C::OFF_LSE + st * 512) + half * 64;
           const float *sd = reinterpret_cast<const float *>(sm + C::OFF_D + st * 512) + half * 64;
+          if (il == nb - 1 && bi > 0 && kg < g.N) {  // this group's dBias partial rows into L2 ahead of the flush
+            const float *pp = partial + ((((int64_t)grp * g.B + b) * g.H + h) * NP + kg) * NP + jt * 128 + half * 64;
+            prefetch_l2_keep(pp);
+            prefetch_l2_keep(pp + 32);
+          }
           ok = wait_bar_warp(bar(C::B_SFULL), t & 1, ab);
           if (!ok) break;
           tc_fence_after();
@@ -605,20 +617,18 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
         if (!ok) break;
         // ---- dBias tile (jt, kt) of this block into the supergroup partial (FP32, [k][j], owned by this CTA)
         if (kg < g.N) {
-          float4 *pp = reinterpret_cast<float4 *>(
-              partial + ((((int64_t)grp * g.B + b) * g.H + h) * NP + kg) * NP + jt * 128 + half * 64);
-          if (bi == 0) {
+          float *pp = partial + ((((int64_t)grp * g.B + b) * g.H + h) * NP + kg) * NP + jt * 128 + half * 64;
 #pragma unroll
-            for (int c = 0; c < 16; ++c)
-              pp[c] = make_float4(acc[2 * c].x, acc[2 * c].y, acc[2 * c + 1].x, acc[2 * c + 1].y);
-          } else {
-            float4 old[16];
+          for (int c = 0; c < 8; ++c) {  // 32 bytes = 8 queries at a time
+            uint32_t w[8];
+            if (bi > 0) ld_keep_v8(pp + 8 * c, w);
 #pragma unroll
-            for (int c = 0; c < 16; ++c) old[c] = pp[c];
-#pragma unroll
-            for (int c = 0; c < 16; ++c)
-              pp[c] = make_float4(old[c].x + acc[2 * c].x, old[c].y + acc[2 * c].y, old[c].z + acc[2 * c + 1].x,
-                                  old[c].w + acc[2 * c + 1].y);
+            for (int e = 0; e < 4; ++e) {
+              const float2 a = acc[4 * c + e];
+              w[2 * e] = __float_as_uint(bi > 0 ? __uint_as_float(w[2 * e]) + a.x : a.x);
+              w[2 * e + 1] = __float_as_uint(bi > 0 ? __uint_as_float(w[2 * e + 1]) + a.y : a.y);
+            }
+            st_keep_v8(pp + 8 * c, w);
           }
         }
         mbar_arrive(bar(C::B_BFREE + bb));
