@@ -618,17 +618,25 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
         // ---- dBias tile (jt, kt) of this block into the supergroup partial (FP32, [k][j], owned by this CTA)
         if (kg < g.N) {
           float *pp = partial + ((((int64_t)grp * g.B + b) * g.H + h) * NP + kg) * NP + jt * 128 + half * 64;
+          uint32_t w[8][8];  // all eight 32-byte loads in flight at once, then add and store
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {  // 32 bytes = 8 queries at a time
-            uint32_t w[8];
-            if (bi > 0) ld_keep_v8(pp + 8 * c, w);
+          for (int c = 0; c < 8; ++c) {
+            if (bi > 0) {
+              ld_keep_v8(pp + 8 * c, w[c]);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) w[c][e] = 0u;
+            }
+          }
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const float2 a = acc[4 * c + e];
-              w[2 * e] = __float_as_uint(bi > 0 ? __uint_as_float(w[2 * e]) + a.x : a.x);
-              w[2 * e + 1] = __float_as_uint(bi > 0 ? __uint_as_float(w[2 * e + 1]) + a.y : a.y);
+              w[c][2 * e] = __float_as_uint(__uint_as_float(w[c][2 * e]) + a.x);
+              w[c][2 * e + 1] = __float_as_uint(__uint_as_float(w[c][2 * e + 1]) + a.y);
             }
-            st_keep_v8(pp + 8 * c, w);
+            st_keep_v8(pp + 8 * c, w[c]);
           }
         }
         mbar_arrive(bar(C::B_BFREE + bb));

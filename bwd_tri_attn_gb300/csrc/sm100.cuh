@@ -108,6 +108,7 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
 }
 
 // 32-byte global accesses that ask L2 to keep the lines (data re-read soon by this CTA).
+// (no memory clobber: callers order these loads against their own stores explicitly)
 __device__ __forceinline__ void ld_keep_v8(const void *p, uint32_t (&r)[8]) {
   asm volatile("ld.global.L2::evict_last.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
