@@ -33,6 +33,39 @@ L2_BYTES = 129 * 2**20
 KERNELS = ["fwd", "bias_transpose", "bwd_d", "bwd_main", "dbias_reduce"]
 
 
+# ncu summaries under profiles/ carry, per kernel, the DRAM bytes of one captured
+# launch, the activation size it ran on and a digest of the sources it was built
+# from; traffic is reported only while the sources still match.
+PROFILES = {"fwd": ("fwd_kernel_crop384_h4_d32.md", ["fwd.cu"]),
+            "bwd_main": ("bwd_kernel_crop384_h4_d32.md", ["bwd.cu"])}
+COMMON_SOURCES = ["common.cuh", "sm100.cuh", "sync.cuh", "tmap.cuh"]
+
+
+def profiled_traffic(kernel: str, activation_elements: int):
+    """DRAM bytes per launch from the kernel's ncu capture, scaled to this workload's
+    activation size (all inputs of the square crops grow with S*N*H*d), or None
+    when the summary is missing or the kernel's sources changed since it was taken."""
+    import hashlib
+
+    name, own = PROFILES[kernel]
+    try:
+        text = open(os.path.join(ROOT, "profiles", name)).read()
+        h = hashlib.sha256()
+        for f in own + COMMON_SOURCES:
+            with open(os.path.join(ROOT, "bwd_tri_attn_gb300", "csrc", f), "rb") as fh:
+                h.update(fh.read())
+    except OSError:
+        return None
+    fields = {}
+    for line in text.splitlines():
+        k, _, v = line.strip().partition(": ")
+        if k in ("source_digest", "dram_bytes_per_launch", "activation_elements"):
+            fields[k] = v.strip()
+    if len(fields) != 3 or fields["source_digest"] != h.hexdigest()[:16]:
+        return None
+    return int(fields["dram_bytes_per_launch"]) * activation_elements / int(fields["activation_elements"])
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -236,7 +269,10 @@ def run_ours(args, w):
     dom = max(("fwd", "bwd_main"), key=lambda n: kernel_ms[n])
     achieved = flops_of[dom] / (kernel_ms[dom] * 1e-3) / 1e12
     roofline = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                "traffic": profiled_traffic(dom, B * S * N * H * hd),
+                "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one N=384 launch, "
+                                  "scaled by activation size",
                 "peak_source": f"{peaks['source']} bf16 dense burst"}
 
     # HBM-bound kernels: algorithmic bytes / time

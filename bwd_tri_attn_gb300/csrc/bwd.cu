@@ -148,15 +148,16 @@ template <int HD>
 __global__ void __launch_bounds__(BwdCfg<HD>::NTHREADS, 1)
 bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
            const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mDO,
-           const __grid_constant__ CUtensorMap mBT, const Dims g, const int Gp, const float *__restrict__ LSE,
+           const __grid_constant__ CUtensorMap mBT, const __grid_constant__ CUtensorMap mDK,
+           const __grid_constant__ CUtensorMap mDV, const Dims g, const int Gp, const float *__restrict__ LSE,
            const float *__restrict__ Dv, const uint16_t *__restrict__ mask, uint16_t *__restrict__ dQ,
-           uint16_t *__restrict__ dK, uint16_t *__restrict__ dV, float *__restrict__ partial, int *status) {
+           float *__restrict__ partial, int *status) {
   using C = BwdCfg<HD>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb0 = smem_u32(sm);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nkt = (g.N + 127) / 128, njt = nkt, NP = nkt * 128;
+  const int nkt = (g.N + 127) / 128, njt = nkt;
   const int kt = blockIdx.x, h = blockIdx.y;
   const int b = blockIdx.z / Gp, grp = blockIdx.z % Gp;
   const uint32_t rank = cluster_ctarank();  // == kt (the cluster spans the key tiles)
@@ -525,6 +526,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
     bool ok = true;
     int t = 0, u = 0;
     float2 acc[32];  // dBias tile row: queries half*64 + [0,64) as pairs
+    // offset of this CTA's partial tile (kt, jt): [supergroup][b][h][kt][jt][128 x 128]
+    auto ptile = [&](int jt_) -> int64_t {
+      return (((((int64_t)grp * g.B + b) * g.H + h) * nkt + kt) * njt + jt_) * 16384;
+    };
     for (int bi = 0; bi < nblk && ok; ++bi) {
       const int i0 = sc.block_first(bi), nb = sc.block_size(bi);
       ok = wait_bar_warp(bar(C::B_KVREADY), bi & 1, ab);  // the mask rows of the block are in place
@@ -542,10 +547,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
           const float2 mk2 = make_float2(dead ? 0.f : mk, dead ? 0.f : mk);
           const float *sl = reinterpret_cast<const float *>(sm + C::OFF_LSE + st * 512) + half * 64;
           const float *sd = reinterpret_cast<const float *>(sm + C::OFF_D + st * 512) + half * 64;
-          if (il == nb - 1 && bi > 0 && kg < g.N) {  // this group's dBias partial rows into L2 ahead of the flush
-            const float *pp = partial + ((((int64_t)grp * g.B + b) * g.H + h) * NP + kg) * NP + jt * 128 + half * 64;
-            prefetch_l2_keep(pp);
-            prefetch_l2_keep(pp + 32);
+          if (il == nb - 1 && bi > 0) {  // the warp's 8 KB of the dBias partial tile into L2 ahead of the flush
+            const float *pt = partial + ptile(jt) + ((half * 8) * 128 + q * 32) * 8 + (lane & 7) * 32;
+            prefetch_l2_keep(pt + (lane >> 3) * 1024);
+            prefetch_l2_keep(pt + ((lane >> 3) + 4) * 1024);
           }
           ok = wait_bar_warp(bar(C::B_SFULL), t & 1, ab);
           if (!ok) break;
@@ -615,14 +620,16 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
           mbar_arrive(bar(C::B_PFULL));
         }
         if (!ok) break;
-        // ---- dBias tile (jt, kt) of this block into the supergroup partial (FP32, [k][j], owned by this CTA)
+        // ---- dBias tile (jt, kt) of this block into the supergroup partial (FP32, owned by this CTA).
+        // Tile layout [query half][chunk c of 8 queries][key][8 queries]: lane-consecutive keys make
+        // every warp access one contiguous kilobyte.
         if (kg < g.N) {
-          float *pp = partial + ((((int64_t)grp * g.B + b) * g.H + h) * NP + kg) * NP + jt * 128 + half * 64;
+          float *pp = partial + ptile(jt) + ((half * 8) * 128 + kl) * 8;  // chunk c at + c * 1024
           uint32_t w[8][8];  // all eight 32-byte loads in flight at once, then add and store
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             if (bi > 0) {
-              ld_keep_v8(pp + 8 * c, w[c]);
+              ld_keep_v8(pp + 1024 * c, w[c]);
             } else {
 #pragma unroll
               for (int e = 0; e < 8; ++e) w[c][e] = 0u;
@@ -636,42 +643,64 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
               w[c][2 * e] = __float_as_uint(__uint_as_float(w[c][2 * e]) + a.x);
               w[c][2 * e + 1] = __float_as_uint(__uint_as_float(w[c][2 * e + 1]) + a.y);
             }
-            st_keep_v8(pp + 8 * c, w[c]);
+            st_keep_v8(pp + 1024 * c, w[c]);
           }
         }
         mbar_arrive(bar(C::B_BFREE + bb));
         ++u;
       }
       if (!ok) break;
-      // ---- dK_i, dV_i of the block -> BF16, once the block's last MMAs are complete
+      // ---- dK_i, dV_i of the block -> BF16, once the block's last MMAs are complete. Each warp stages
+      // its 32 key rows in the part of the dS tile that only it writes (four 1 KB pieces, two per
+      // slice, double-buffered over the slices) and stores them with TMA, 16 rows per box.
       ok = wait_bar_warp(bar(C::B_M2DONE), (t - 1) & 1, ab);
       if (!ok) break;
       tc_fence_after();
-      for (int il = 0; il < nb; ++il) {
-        uint32_t r[32];
-        const uint32_t col = tb + lb + C::TDKV + il * 2 * HD + half * HD;
-        if constexpr (HD == 32) {
-          tmem_ld32(col, r);
-        } else {
-          tmem_ld16(col, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
-        }
-        tmem_wait_ld();
-        if (kg < g.N) {
-          const float f = half == 0 ? g.scale : 1.f;
-          uint16_t *out = (half == 0 ? dK : dV) + pos_row(g, b, i0 + il, kg) * g.H * HD + h * HD;
+      {
+        const int r16 = lane >> 4, rr = lane & 15;
+        const uint32_t sw = HD == 32 ? (uint32_t)((rr >> 1) & 3) : (uint32_t)((rr >> 2) & 1);
+        const float f = half == 0 ? g.scale : 1.f;
+        for (int il = 0; il < nb; ++il) {
+          uint32_t r[32];
+          const uint32_t col = tb + lb + C::TDKV + il * 2 * HD + half * HD;
+          if constexpr (HD == 32) {
+            tmem_ld32(col, r);
+          } else {
+            tmem_ld16(col, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
+          }
+          tmem_wait_ld();
           uint32_t w[HD / 2];
 #pragma unroll
           for (int c = 0; c < HD / 2; ++c)
             w[c] = (uint32_t)f32_to_bf16_rn(__uint_as_float(r[2 * c]) * f) |
                    ((uint32_t)f32_to_bf16_rn(__uint_as_float(r[2 * c + 1]) * f) << 16);
+          if (il >= 2) {  // the stores of slice il - 2 have read this slot
+            if (lane == 0) bulk_wait_group_read<1>();
+            __syncwarp();
+          }
+          const uint32_t piece = sb0 + C::OFF_DS + (4 * q + 2 * (il & 1) + r16) * 2048 + half * 1024;
 #pragma unroll
           for (int c = 0; c < HD / 8; ++c)
-            reinterpret_cast<uint4 *>(out)[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(piece + rr * C::ROWB + ((c ^ sw) << 4)),
+                         "r"(w[4 * c]), "r"(w[4 * c + 1]), "r"(w[4 * c + 2]), "r"(w[4 * c + 3])
+                         : "memory");
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const uint32_t p0 = sb0 + C::OFF_DS + (4 * q + 2 * (il & 1)) * 2048 + half * 1024;
+            const CUtensorMap *m = half == 0 ? &mDK : &mDV;
+            tma_store_4d(m, p0, 0, h, kt * 128 + q * 32, b * g.S + i0 + il);
+            tma_store_4d(m, p0 + 2048, 0, h, kt * 128 + q * 32 + 16, b * g.S + i0 + il);
+            bulk_commit_group();
+          }
         }
+        if (lane == 0) bulk_wait_group_read<0>();  // the dS writes of the next step reuse these pieces
+        __syncwarp();
       }
       tc_fence_before();
       mbar_arrive(bar(C::B_DKVREAD));
     }
+    if (lane == 0) bulk_wait_group<0>();  // dK, dV stores performed before the CTA exits
   }
   tc_fence_before();
   __syncthreads();
@@ -698,27 +727,40 @@ __global__ void bias_transpose_kernel(const uint16_t *__restrict__ bias, uint16_
   }
 }
 
-// dBias[bh][j][k] = BF16(sum over g = 0..Gp-1, in order, of partial[g][bh][k][j]).
+// dBias[bh][j][k] = BF16(sum over g = 0..Gp-1, in order, of the partials). Each partial holds,
+// per bh, tiles [kt][jt] of 128 keys x 128 queries laid out [query half][chunk c][key][8 queries].
+// One CTA (256 threads) reduces one [128 keys x 8 queries] chunk and writes its 8 output rows.
 __global__ void dbias_reduce_t_kernel(const float *__restrict__ partial, int Gp, int BH, int N, int NP,
                                       uint16_t *__restrict__ dBias) {
-  __shared__ float tile[32][33];
-  const int bh = blockIdx.z, k0 = blockIdx.y * 32, j0 = blockIdx.x * 32;
-  const int64_t gstride = (int64_t)BH * NP * NP;
-  for (int r = threadIdx.y; r < 32; r += blockDim.y) {
-    const int k = k0 + r, j = j0 + threadIdx.x;
-    float s = 0.f;
-    if (k < N && j < N) {
-      const float *p = partial + ((int64_t)bh * NP + k) * NP + j;
-      s = p[0];
-      for (int gi = 1; gi < Gp; ++gi) s += __ldcs(p + gi * gstride);
+  __shared__ float s[8][129];
+  const int nt = NP / 128, tile = blockIdx.x, kt = tile / nt, jt = tile % nt;
+  const int hc = blockIdx.y, bh = blockIdx.z, tid = threadIdx.x;
+  const int64_t gstride4 = (int64_t)BH * NP * NP / 4;
+  const int kl = tid >> 1, e0 = (tid & 1) * 4;
+  if (kt * 128 + kl < N) {
+    const float4 *p =
+        reinterpret_cast<const float4 *>(partial + ((int64_t)bh * nt * nt + tile) * 16384 + (hc * 128 + kl) * 8 + e0);
+    float4 a = __ldcs(p);
+    for (int gi = 1; gi < Gp; ++gi) {
+      const float4 v = __ldcs(p + gi * gstride4);
+      a.x += v.x;
+      a.y += v.y;
+      a.z += v.z;
+      a.w += v.w;
     }
-    tile[r][threadIdx.x] = s;
+    s[e0][kl] = a.x;
+    s[e0 + 1][kl] = a.y;
+    s[e0 + 2][kl] = a.z;
+    s[e0 + 3][kl] = a.w;
   }
   __syncthreads();
-  for (int r = threadIdx.y; r < 32; r += blockDim.y) {
-    const int j = j0 + r, k = k0 + threadIdx.x;
-    if (j < N && k < N) dBias[((int64_t)bh * N + j) * N + k] = f32_to_bf16_rn(tile[threadIdx.x][r]);
-  }
+  const int e = tid >> 5, j = jt * 128 + hc * 8 + e;
+  if (j < N)
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int kk = (tid & 31) + 32 * m, k = kt * 128 + kk;
+      if (k < N) dBias[((int64_t)bh * N + j) * N + k] = f32_to_bf16_rn(s[e][kk]);
+    }
 }
 
 cudaError_t launch_bias_transpose(const Dims &g, const uint16_t *bias, uint16_t *biasT, cudaStream_t stream) {
@@ -730,8 +772,9 @@ cudaError_t launch_bias_transpose(const Dims &g, const uint16_t *bias, uint16_t 
 
 cudaError_t launch_dbias_reduce_t(const Dims &g, int Gp, const float *partial, uint16_t *dBias, cudaStream_t stream) {
   const int NP = (g.N + 127) / 128 * 128;
-  dim3 grid(NP / 32, NP / 32, g.B * g.H), block(32, 8);
-  dbias_reduce_t_kernel<<<grid, block, 0, stream>>>(partial, Gp, g.B * g.H, g.N, NP, dBias);
+  const int nt = NP / 128;
+  dim3 grid(nt * nt, 16, g.B * g.H);
+  dbias_reduce_t_kernel<<<grid, 256, 0, stream>>>(partial, Gp, g.B * g.H, g.N, NP, dBias);
   return cudaGetLastError();
 }
 
@@ -742,8 +785,10 @@ cudaError_t launch_bwd_main_t(const Dims &g, int Gp, const uint16_t *Q, const ui
                               int *status, cudaStream_t stream) {
   using C = BwdCfg<HD>;
   const int nkt = (g.N + 127) / 128, NP = nkt * 128;
-  CUtensorMap mq, mk, mv, mdo, mbt;
+  CUtensorMap mq, mk, mv, mdo, mbt, mdk, mdv;
   cudaError_t e = make_rows_map(&mq, Q, g, 128);
+  if (e == cudaSuccess) e = make_rows_map(&mdk, dK, g, 16);
+  if (e == cudaSuccess) e = make_rows_map(&mdv, dV, g, 16);
   if (e == cudaSuccess) e = make_rows_map(&mk, K, g, 128);
   if (e == cudaSuccess) e = make_rows_map(&mv, V, g, 128);
   if (e == cudaSuccess) e = make_rows_map(&mdo, dO, g, 128);
@@ -774,7 +819,7 @@ cudaError_t launch_bwd_main_t(const Dims &g, int Gp, const uint16_t *Q, const ui
   attrs[0].val.clusterDim.z = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, bwd_kernel<HD>, mq, mk, mv, mdo, mbt, g, Gp, LSE, Dv, mask, dQ, dK, dV, partial,
+  return cudaLaunchKernelEx(&cfg, bwd_kernel<HD>, mq, mk, mv, mdo, mbt, mdk, mdv, g, Gp, LSE, Dv, mask, dQ, partial,
                             status);
 }
 

@@ -177,8 +177,8 @@ int tri_attn_bwd_static(tri_attn_shape shape,
  * tri_attn_fwd / tri_attn_bwd issued by the calling host thread records
  * events[k] (a cudaEvent_t created by the caller) on the call's stream right
  * after enqueuing the call's k-th kernel, for k < n. Kernel order:
- * tri_attn_fwd = {forward}; tri_attn_bwd = {D correction, main backward,
- * dBias reduction}. events = NULL or n = 0 switches it off. The events stay
+ * tri_attn_fwd = {forward}; tri_attn_bwd = {bias transpose, D correction,
+ * main backward, dBias reduction}. events = NULL or n = 0 switches it off. The events stay
  * owned by the caller and must stay valid while instrumentation is on.
  * Returns TRI_ATTN_OK, or TRI_ATTN_ERR_INVALID_ARG for n < 0.
  */
