@@ -137,11 +137,16 @@ __device__ __forceinline__ void reg_dealloc() {
 
 // The step schedule every role walks in the same order: blocks of GB slices of
 // the supergroup [s0, s1), then query tiles, then the slices of the block.
+// The first block holds f <= GB slices, f set per cluster so that clusters reach
+// their dBias flushes (one per block and query tile) at different steps.
 struct Sched {
-  int s0, s1, njt, GB;
-  __device__ int nblk() const { return (s1 - s0 + GB - 1) / GB; }
-  __device__ int block_first(int bi) const { return s0 + bi * GB; }
-  __device__ int block_size(int bi) const { return min(GB, s1 - block_first(bi)); }
+  int s0, s1, njt, GB, f;
+  __device__ int nblk() const {
+    const int n = s1 - s0;
+    return n <= 0 ? 0 : (n <= f ? 1 : 1 + (n - f + GB - 1) / GB);
+  }
+  __device__ int block_first(int bi) const { return bi == 0 ? s0 : s0 + f + (bi - 1) * GB; }
+  __device__ int block_size(int bi) const { return min(bi == 0 ? f : GB, s1 - block_first(bi)); }
 };
 
 template <int HD>
@@ -161,7 +166,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
   const int kt = blockIdx.x, h = blockIdx.y;
   const int b = blockIdx.z / Gp, grp = blockIdx.z % Gp;
   const uint32_t rank = cluster_ctarank();  // == kt (the cluster spans the key tiles)
-  const Sched sc{(int)((int64_t)grp * g.S / Gp), (int)((int64_t)(grp + 1) * g.S / Gp), njt, C::GB};
+  const Sched sc{(int)((int64_t)grp * g.S / Gp), (int)((int64_t)(grp + 1) * g.S / Gp), njt, C::GB,
+                 C::GB - (int)((blockIdx.y + gridDim.y * blockIdx.z) % C::GB)};
   const int nblk = sc.nblk();
   const int T = njt * (sc.s1 - sc.s0);  // steps of this CTA
   auto bar = [&](int k) { return sb0 + C::OFF_BAR + 8u * (uint32_t)k; };
