@@ -35,15 +35,18 @@
 // Operands: all tensor-core operands are FP16 (Q, K, V, dO converted in shared
 // memory, exact in the FP16 range); P and dS need FP16's 11-bit significand.
 //
-// Warp roles (16 warps):
-//   0-7   elementwise: thread = key row (TMEM lane quarter w % 4) x 64 queries (half w / 4);
-//         only P and dS are on their path; 176 registers each (setmaxnreg)
-//   8-11  dQ: read the dQ partial from TMEM (lanes = queries), push it to the owners, reduce owned rows
-//   12    TMA producer (+ LSE / D rows), 13 MMA issuer and TMEM owner, 14-15 BF16 -> FP16 conversion
-// TMEM columns: A = [0,128) S^T; B = [128,256) dP^T, then per query half h the packed
-// FP16 dS^T (B + 64h + [0,32)) and P^T (B + 64h + [32,64)), each written only over
-// columns that thread has already read; dQ partial at 256; dK_i, dV_i from 288.
-// S^T(t+1) is computed into A while the elementwise warps still work on step t.
+// Warp roles (NEW + 8 warps; NEW = 8 with QPT = 64 queries per elementwise thread):
+//   0..NEW-1  elementwise: thread = key row (TMEM lane quarter w % 4) x QPT queries (column group w / 4);
+//             only P and dS are on their path; the most registers (setmaxnreg)
+//   NEW..+3   dQ: read the dQ partial from TMEM (lanes = queries), push it to the owners, reduce owned rows
+//   NEW+4     TMA producer (+ LSE / D rows), NEW+5 MMA issuer and TMEM owner, NEW+6..7 BF16 -> FP16 conversion
+// TMEM columns: A = [0,128) S^T, then FP16 P^T; B = [128,256) dP^T, then FP16 dS^T; dQ partial
+// at 256; dK_i, dV_i from 288. Each elementwise thread writes P^T (dS^T) as packed FP16 over the
+// S^T (dP^T) columns it has just read: column group g of 32 queries keeps its 16 packed columns at
+// A + 32g (B + 32g). dV = P^T dO is issued as soon as the P phase is done, and its completion frees
+// region A for S^T(t+1); dK = dS^T Q follows the dS phase and its completion frees B for dP^T(t+1);
+// dQ = dS K reads dS from a 128-byte-swizzled FP16 tile in shared memory. So the P phase of step
+// t+1 overlaps step t's dK and dQ, and the tensor pipe rarely waits on the elementwise warps.
 #include "common.cuh"
 #include "sm100.cuh"
 #include "sync.cuh"
@@ -59,11 +62,14 @@ struct BwdCfg {
   static constexpr int ROWB = HD * 2;
   static constexpr int TILE = 128 * ROWB;
   static constexpr uint32_t SW = HD == 32 ? kSwizzle64B : kSwizzle32B;
-  static constexpr int NEW = 8, NEWT = NEW * 32;  // elementwise warps 0-7
-  static constexpr int WARP_DQ = 8, NDQ = 4, NDQT = NDQ * 32;
-  static constexpr int WARP_TMA = 12, WARP_MMA = 13, WARP_CV = 14, NCV = 2, NCVT = NCV * 32;
-  static constexpr int NTHREADS = 512;
-  static constexpr uint32_t REG_LAUNCH = 128, REG_EW = 176, REG_OTHER = 80;
+  static constexpr int QPT = 64;                   // queries per elementwise thread (64: 8 warps, 32: 16)
+  static constexpr int NEW = 4 * 128 / QPT, NEWT = NEW * 32;  // elementwise warps 0 .. NEW-1
+  static constexpr int KPG = QPT / 16;             // K steps of 16 queries per column group
+  static constexpr int WARP_DQ = NEW, NDQ = 4, NDQT = NDQ * 32;
+  static constexpr int WARP_TMA = NEW + 4, WARP_MMA = NEW + 5, WARP_CV = NEW + 6, NCV = 2, NCVT = NCV * 32;
+  static constexpr int NTHREADS = (NEW + 8) * 32;
+  static constexpr uint32_t REG_LAUNCH = QPT == 64 ? 128 : 80, REG_EW = QPT == 64 ? 176 : 96,
+                            REG_OTHER = QPT == 64 ? 80 : 48;
   static_assert(NEWT * REG_EW + (NTHREADS - NEWT) * REG_OTHER == NTHREADS * REG_LAUNCH, "register split");
   static constexpr uint32_t TA = 0, TB = 128, TDQ = 256, TDKV = 288, TMEM_COLS = 512;
   static_assert(TDKV + GB * 2 * HD <= TMEM_COLS, "TMEM budget");
@@ -85,8 +91,9 @@ struct BwdCfg {
   static constexpr int B_KVFULL = 0, B_KVREADY = 1, B_KVFREE = 2;
   static constexpr int B_QDOFULL = 3, B_QDOREADY = B_QDOFULL + NQS, B_QDOFREE = B_QDOREADY + NQS;
   static constexpr int B_BFULL = B_QDOFREE + NQS, B_BFREE = B_BFULL + 2;
-  static constexpr int B_SFULL = B_BFREE + 2, B_SREAD = B_SFULL + 1, B_DPFULL = B_SREAD + 1;
-  static constexpr int B_PFULL = B_DPFULL + 1, B_M2DONE = B_PFULL + 1, B_DQREAD = B_M2DONE + 1;
+  static constexpr int B_SFULL = B_BFREE + 2, B_PAFULL = B_SFULL + 1, B_AFREE = B_PAFULL + 1;
+  static constexpr int B_DPFULL = B_AFREE + 1, B_PFULL = B_DPFULL + 1, B_BFREEM = B_PFULL + 1;
+  static constexpr int B_M2DONE = B_BFREEM + 1, B_DQREAD = B_M2DONE + 1;
   static constexpr int B_DKVREAD = B_DQREAD + 1, B_RFULL = B_DKVREAD + 1, B_XEMPTY = B_RFULL + NRB;
   static constexpr int B_FINAL = B_XEMPTY + NRB, NBAR = B_FINAL + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
@@ -153,10 +160,9 @@ template <int HD>
 __global__ void __launch_bounds__(BwdCfg<HD>::NTHREADS, 1)
 bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
            const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mDO,
-           const __grid_constant__ CUtensorMap mBT, const __grid_constant__ CUtensorMap mDK,
-           const __grid_constant__ CUtensorMap mDV, const Dims g, const int Gp, const float *__restrict__ LSE,
+           const __grid_constant__ CUtensorMap mBT, const Dims g, const int Gp, const float *__restrict__ LSE,
            const float *__restrict__ Dv, const uint16_t *__restrict__ mask, uint16_t *__restrict__ dQ,
-           float *__restrict__ partial, int *status) {
+           uint16_t *__restrict__ dK, uint16_t *__restrict__ dV, float *__restrict__ partial, int *status) {
   using C = BwdCfg<HD>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -190,9 +196,11 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
       mbar_init(bar(C::B_BFREE + s), C::NEWT);
     }
     mbar_init(bar(C::B_SFULL), 1);
-    mbar_init(bar(C::B_SREAD), C::NEWT);
+    mbar_init(bar(C::B_PAFULL), C::NEWT);
+    mbar_init(bar(C::B_AFREE), 1);
     mbar_init(bar(C::B_DPFULL), 1);
     mbar_init(bar(C::B_PFULL), C::NEWT);
+    mbar_init(bar(C::B_BFREEM), 1);
     mbar_init(bar(C::B_M2DONE), 1);
     mbar_init(bar(C::B_DQREAD), C::NDQT);
     mbar_init(bar(C::B_DKVREAD), C::NEWT);
@@ -276,7 +284,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
             }
             kv_issued = bi + 1;
           }
-          if (il == 0) {
+          if (il == 0) {  // bias tile of this query-tile group (double-buffered)
             const int bb = u & 1;
             if (u >= 2) ok = wait_bar_warp(bar(C::B_BFREE + bb), ((u - 2) >> 1) & 1, ab);
             if (!ok) break;
@@ -334,7 +342,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idSS = idesc_f16(128, 128, false, false, false, false);
-      constexpr uint32_t idTS = idesc_f16(128, HD, false, false, false, true);
+      constexpr uint32_t idKV = idesc_f16(128, HD, false, false, false, true);
       constexpr uint32_t idQ = idesc_f16(128, HD, false, false, true, true);
       // per-step bookkeeping, walked in the common schedule
       int bi = 0, jt = 0, il = 0;
@@ -377,38 +385,42 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
         const bool has_next = t + 1 < T;
         const bool next_new_block = has_next && jt == 0 && il == 0;
         const int st1 = (t + 1) % C::NQS;
-        // S^T(t+1) ahead of this step's second group, as soon as region A has been read (never
-        // across a block change: that needs the new K); the MMA thread has nothing else to
-        // issue before P(t) arrives
-        bool s_early = false;
+        const uint32_t dcol = tb + C::TDKV + cil * 2 * HD;
+        // ---- dV += P^T dO as soon as P^T is in region A (A operand: packed FP16 in TMEM)
+        ok = wait_bar(bar(C::B_PAFULL), t & 1, ab);
+        if (ok && cjt == 0 && cil == 0 && cbi > 0) ok = wait_bar(bar(C::B_DKVREAD), (cbi - 1) & 1, ab);
+        if (!ok) break;
+        tc_fence_after();
+        {
+          const uint32_t oB = sb0 + C::OFF_DO + st * C::TILE;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)  // 16 queries per step: column group ks / KPG, packed columns (ks % KPG) * 8
+            mma_ts(dcol + HD, tb + C::TA + (ks / C::KPG) * C::QPT + (ks % C::KPG) * 8,
+                   smem_desc(oB + ks * 16 * C::ROWB, 16, 8 * C::ROWB, C::SW), idKV, (cjt > 0 || ks > 0) ? 1u : 0u);
+          mma_commit(bar(C::B_AFREE));
+        }
+        // ---- S^T(t+1) once dV has read region A (within a block; a new block needs the new K, V first)
         if (has_next && !next_new_block) {
-          ok = wait_bar(bar(C::B_QDOREADY + st1), ((t + 1) / C::NQS) & 1, ab);
-          if (ok) ok = wait_bar(bar(C::B_SREAD), t & 1, ab);
+          ok = wait_bar(bar(C::B_AFREE), t & 1, ab);
+          if (ok) ok = wait_bar(bar(C::B_QDOREADY + st1), ((t + 1) / C::NQS) & 1, ab);
           if (!ok) break;
           tc_fence_after();
           issue_s(t + 1, il, st1);
-          s_early = true;
         }
-        // second MMA group of step t
+        // ---- dK += dS^T Q (A: packed FP16 dS^T in region B) and the dQ partial dS K (A: dS tile, MN-major)
         ok = wait_bar(bar(C::B_PFULL), t & 1, ab);
-        if (ok && cjt == 0 && cil == 0 && cbi > 0) ok = wait_bar(bar(C::B_DKVREAD), (cbi - 1) & 1, ab);
         if (ok && t > 0) ok = wait_bar(bar(C::B_DQREAD), (t - 1) & 1, ab);
         if (!ok) break;
         tc_fence_after();
         {
-          const uint32_t kA = sb0 + C::OFF_K + cil * C::TILE;
-          const uint32_t qB = sb0 + C::OFF_Q + st * C::TILE, oB = sb0 + C::OFF_DO + st * C::TILE;
-          const uint32_t dcol = tb + C::TDKV + cil * 2 * HD;
+          const uint32_t kA = sb0 + C::OFF_K + cil * C::TILE, qB = sb0 + C::OFF_Q + st * C::TILE;
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {  // dV += P^T dO, dK += dS^T Q (A from TMEM region B)
-            const uint32_t half_col = tb + C::TB + (ks >> 2) * 64 + (ks & 3) * 8;
-            mma_ts(dcol + HD, half_col + 32, smem_desc(oB + ks * 16 * C::ROWB, 16, 8 * C::ROWB, C::SW), idTS,
-                   (cjt > 0 || ks > 0) ? 1u : 0u);
-            mma_ts(dcol, half_col, smem_desc(qB + ks * 16 * C::ROWB, 16, 8 * C::ROWB, C::SW), idTS,
-                   (cjt > 0 || ks > 0) ? 1u : 0u);
-          }
+          for (int ks = 0; ks < 8; ++ks)
+            mma_ts(dcol, tb + C::TB + (ks / C::KPG) * C::QPT + (ks % C::KPG) * 8,
+                   smem_desc(qB + ks * 16 * C::ROWB, 16, 8 * C::ROWB, C::SW), idKV, (cjt > 0 || ks > 0) ? 1u : 0u);
+          mma_commit(bar(C::B_BFREEM));
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks)  // dQ partial = dS K
+          for (int ks = 0; ks < 8; ++ks)
             mma_ss(tb + C::TDQ, smem_desc(sb0 + C::OFF_DS + ks * 4096, 1024, 2048, kSwizzle128B),
                    smem_desc(kA + ks * 16 * C::ROWB, 16, 8 * C::ROWB, C::SW), idQ, ks > 0 ? 1u : 0u);
           mma_commit(bar(C::B_M2DONE));
@@ -416,17 +428,18 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
           if (next_new_block || !has_next) mma_commit(bar(C::B_KVFREE));
         }
         if (has_next) {
-          if (!s_early) {
-            if (next_new_block) ok = wait_bar(bar(C::B_KVREADY), bi & 1, ab);
+          if (next_new_block) {
+            ok = wait_bar(bar(C::B_KVREADY), bi & 1, ab);
             if (ok) ok = wait_bar(bar(C::B_QDOREADY + st1), ((t + 1) / C::NQS) & 1, ab);
-            if (ok) ok = wait_bar(bar(C::B_SREAD), t & 1, ab);
+            if (ok) ok = wait_bar(bar(C::B_AFREE), t & 1, ab);
             if (!ok) break;
             tc_fence_after();
             issue_s(t + 1, il, st1);
           }
-          // region B (P^T, dS^T of step t) and the dS tile are free once this step's MMAs completed
-          ok = wait_bar(bar(C::B_M2DONE), t & 1, ab);
+          // ---- dP^T(t+1) once dK has read region B
+          ok = wait_bar(bar(C::B_BFREEM), t & 1, ab);
           if (!ok) break;
+          tc_fence_after();
           issue_dp(il, st1);
         }
       }
@@ -487,6 +500,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
       const int i0 = sc.block_first(bi), nb = sc.block_size(bi);
       for (int jt = 0; jt < njt && ok; ++jt)
         for (int il = 0; il < nb; ++il, ++t) {
+          if (t > 0) {
+            ok = reduce_prev();  // owner duty for the previous step (usually while this step's MMAs run)
+            if (!ok) break;
+          }
           ok = wait_bar_warp(bar(C::B_M2DONE), t & 1, ab);
           if (!ok) break;
           tc_fence_after();
@@ -496,13 +513,9 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
           } else {
             tmem_ld16(tb + lb + C::TDQ, r);
           }
-          tmem_wait_ld();
+          tmem_wait_ld(r);
           tc_fence_before();
           mbar_arrive(bar(C::B_DQREAD));
-          if (t > 0) {
-            ok = reduce_prev();  // owner duty for the previous step
-            if (!ok) break;
-          }
           // slot t % NRB is free once every owner reduced step t - NRB from it
           if (t >= C::NRB) ok = wait_bar_cluster_warp(bar(C::B_XEMPTY + t % C::NRB), ((t / C::NRB) - 1) & 1, ab);
           if (!ok) break;
@@ -520,18 +533,22 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
     if (ok && red < T) ok = reduce_prev();  // the last step's rows
   } else {
     reg_alloc<C::REG_EW>();
-    // ---------------------------------------------------------------- elementwise warps 0-7
-    const int q = warp & 3, half = warp >> 2;
-    const int kl = q * 32 + lane;  // key row of the tile = TMEM lane
+    // ---------------------------------------------------------------- elementwise warps 0-15
+    constexpr int QPT = C::QPT;
+    const int q = warp & 3, cg = warp >> 2;  // TMEM lane quarter, column group of QPT queries
+    const int hf = (cg * QPT) >> 6, c0 = ((cg * QPT) & 63) >> 3;  // query half, first 8-query chunk in it
+    const int kl = q * 32 + lane;            // key row of the tile = TMEM lane
     const int kg = kt * 128 + kl;
     const uint32_t lb = (uint32_t)(q * 32) << 16;
-    const uint32_t colA = tb + lb + C::TA + half * 64, colB = tb + lb + C::TB + half * 64;
+    const uint32_t colA = tb + lb + C::TA + cg * QPT, colB = tb + lb + C::TB + cg * QPT;
     const float c1 = g.scale * kLog2e;
     const float2 c12 = make_float2(c1, c1), l2e2 = make_float2(kLog2e, kLog2e), m1x2 = make_float2(-1.f, -1.f);
     const float *maskf = reinterpret_cast<const float *>(sm + C::OFF_MASK);
+    // 8 queries per 16 bytes in the 128-byte-swizzled tiles: row of key kl, chunk c at ((c ^ (kl & 7)) << 4)
+    const uint32_t trow = (kl >> 3) * 2048 + hf * 1024 + (kl & 7) * 128;
     bool ok = true;
     int t = 0, u = 0;
-    float2 acc[32];  // dBias tile row: queries half*64 + [0,64) as pairs
+    float2 acc[QPT / 2];  // dBias tile row: queries cg*QPT + [0,QPT) as pairs
     // offset of this CTA's partial tile (kt, jt): [supergroup][b][h][kt][jt][128 x 128]
     auto ptile = [&](int jt_) -> int64_t {
       return (((((int64_t)grp * g.B + b) * g.H + h) * nkt + kt) * njt + jt_) * 16384;
@@ -544,60 +561,73 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
         ok = wait_bar_warp(bar(C::B_BFULL + bb), (u >> 1) & 1, ab);
         if (!ok) break;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) acc[e] = make_float2(0.f, 0.f);
-        const uint32_t brow = sb0 + C::OFF_BIAS + bb * C::BIAS_TILE + half * 16384 + kl * 128;
+        for (int e = 0; e < QPT / 2; ++e) acc[e] = make_float2(0.f, 0.f);
+        const uint32_t brow = sb0 + C::OFF_BIAS + bb * C::BIAS_TILE + hf * 16384 + kl * 128;
         for (int il = 0; il < nb; ++il, ++t) {
           const int st = t % C::NQS;
+          // mask*log2e of this key (-inf for masked keys and keys past N: their exponent is -inf, P = +0)
           const float mk = maskf[il * 128 + kl];
-          const bool dead = (mk == -INFINITY);
-          const float2 mk2 = make_float2(dead ? 0.f : mk, dead ? 0.f : mk);
-          const float *sl = reinterpret_cast<const float *>(sm + C::OFF_LSE + st * 512) + half * 64;
-          const float *sd = reinterpret_cast<const float *>(sm + C::OFF_D + st * 512) + half * 64;
-          if (il == nb - 1 && bi > 0) {  // the warp's 8 KB of the dBias partial tile into L2 ahead of the flush
-            const float *pt = partial + ptile(jt) + ((half * 8) * 128 + q * 32) * 8 + (lane & 7) * 32;
-            prefetch_l2_keep(pt + (lane >> 3) * 1024);
-            prefetch_l2_keep(pt + ((lane >> 3) + 4) * 1024);
-          }
+          const bool unmasked = __all_sync(0xffffffffu, mk == 0.f);  // warp-uniform: skip the mask add
+          const float2 mk2 = make_float2(mk, mk);
+          const float *sl = reinterpret_cast<const float *>(sm + C::OFF_LSE + st * 512) + cg * QPT;
+          const float *sd = reinterpret_cast<const float *>(sm + C::OFF_D + st * 512) + cg * QPT;
+          if (il == nb - 1 && bi > 0)  // the warp's QPT/8 KB of the dBias partial tile into L2 ahead of the flush
+#pragma unroll
+            for (int r = 0; r < QPT / 32; ++r) {
+              const int li = lane + 32 * r;  // 128-byte line li of the warp's chunks
+              prefetch_l2_keep(partial + ptile(jt) + ((hf * 8 + c0 + (li >> 3)) * 128 + q * 32) * 8 + (li & 7) * 32);
+            }
           ok = wait_bar_warp(bar(C::B_SFULL), t & 1, ab);
           if (!ok) break;
           tc_fence_after();
-          uint32_t pw[32];  // P as FP16 pairs: the P^T operand and the factor of dS
-          {
-            uint32_t pv[64];  // S^T values of this thread's 64 queries
-            tmem_ld32(colA, *reinterpret_cast<uint32_t(*)[32]>(&pv[0]));
-            tmem_ld32(colA + 32, *reinterpret_cast<uint32_t(*)[32]>(&pv[32]));
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(bar(C::B_SREAD));  // region A may now take S^T of the next step
+          uint32_t pw[QPT / 2];  // P as FP16 pairs: the P^T operand and the factor of dS
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {  // 8 queries (one 16-byte bias chunk) at a time
+          for (int hh = 0; hh < QPT / 32; ++hh) {  // 32 queries at a time
+            uint32_t pv[32];                       // S^T values
+            tmem_ld32(colA + hh * 32, pv);
+            tmem_wait_ld(pv);
+#pragma unroll
+            for (int mq = 0; mq < 4; ++mq) {  // 8 queries (one 16-byte bias chunk) at a time
+              const int m = hh * 4 + mq;
               uint32_t bw[4];
               asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
                            : "=r"(bw[0]), "=r"(bw[1]), "=r"(bw[2]), "=r"(bw[3])
-                           : "r"(brow + ((ch ^ (kl & 7)) << 4)));
-              const float4 u0 = reinterpret_cast<const float4 *>(sl)[2 * ch];
-              const float4 u1 = reinterpret_cast<const float4 *>(sl)[2 * ch + 1];
+                           : "r"(brow + (((c0 + m) ^ (kl & 7)) << 4)));
+              const float4 u0 = reinterpret_cast<const float4 *>(sl)[2 * m];
+              const float4 u1 = reinterpret_cast<const float4 *>(sl)[2 * m + 1];
               const float2 uu[4] = {make_float2(u0.x, u0.y), make_float2(u0.z, u0.w), make_float2(u1.x, u1.y),
                                     make_float2(u1.z, u1.w)};
 #pragma unroll
               for (int e2 = 0; e2 < 4; ++e2) {
-                const int x = ch * 8 + 2 * e2;
+                const int x = mq * 8 + 2 * e2;
                 const float2 bv = make_float2(__uint_as_float(bw[e2] << 16), __uint_as_float(bw[e2] & 0xffff0000u));
-                const float2 base = __ffma2_rn(bv, l2e2, __fadd2_rn(uu[e2], mk2));
+                const float2 base = __ffma2_rn(bv, l2e2, unmasked ? uu[e2] : __fadd2_rn(uu[e2], mk2));
                 const float2 arg = __ffma2_rn(make_float2(__uint_as_float(pv[x]), __uint_as_float(pv[x + 1])), c12, base);
-                pw[x >> 1] = pack_f16x2(dead ? 0.f : ex2(arg.x), dead ? 0.f : ex2(arg.y));
+                pw[m * 4 + e2] = pack_f16x2(ex2(arg.x), ex2(arg.y));
               }
             }
           }
-          ok = wait_bar_warp(bar(C::B_DPFULL), t & 1, ab);
+          if (il == nb - 1) {  // this group's bias tile is no longer read: hand it back to the TMA
+            fence_proxy_async_smem();  // order these generic-proxy reads before the async-proxy overwrite
+            mbar_arrive(bar(C::B_BFREE + bb));
+          }
+          if constexpr (QPT == 64) {  // P^T (FP16 pairs) over this thread's S^T columns: the A operand of dV
+            tmem_st32(colA, pw);
+          } else {
+            tmem_st16(colA, pw);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(bar(C::B_PAFULL));
+          ok = wait_bar_warp(bar(C::B_DPFULL), t & 1, ab);  // (also: dQ of the previous step has read the dS tile)
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
-          for (int c2 = 0; c2 < 4; ++c2) {  // 16 queries at a time
+          for (int c2 = 0; c2 < QPT / 16; ++c2) {  // 16 queries at a time
             uint32_t dv[16];
             tmem_ld16(colB + c2 * 16, dv);
-            tmem_wait_ld();
-            uint32_t dw[8];
+            tmem_wait_ld(dv);
+            uint32_t dw[8];  // dS as FP16 pairs
 #pragma unroll
             for (int e2 = 0; e2 < 8; ++e2) {
               const int x0 = c2 * 16 + 2 * e2;
@@ -608,18 +638,15 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
               acc[x0 >> 1] = __fadd2_rn(acc[x0 >> 1], ds);
               dw[e2] = pack_f16x2(ds.x, ds.y);
             }
-            tmem_st8(colB + c2 * 8, dw);  // over columns already read
+            tmem_st8(colB + c2 * 8, dw);  // dS^T (FP16 pairs) over columns already read: the A operand of dK
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {  // dS (FP16) into the MN-major SW128 tile of the dQ MMA
-              const int ch = c2 * 2 + cc;
-              const uint32_t da =
-                  sb0 + C::OFF_DS + (kl >> 3) * 2048 + half * 1024 + (kl & 7) * 128 + ((ch ^ (kl & 7)) << 4);
-              asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(da), "r"(dw[cc * 4]), "r"(dw[cc * 4 + 1]),
-                           "r"(dw[cc * 4 + 2]), "r"(dw[cc * 4 + 3])
+            for (int cc = 0; cc < 2; ++cc) {  // and into the dS tile, the A operand of dQ
+              const int m = c2 * 2 + cc;
+              asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(sb0 + C::OFF_DS + trow + (((c0 + m) ^ (kl & 7)) << 4)),
+                           "r"(dw[4 * cc]), "r"(dw[4 * cc + 1]), "r"(dw[4 * cc + 2]), "r"(dw[4 * cc + 3])
                            : "memory");
             }
           }
-          tmem_st32(colB + 32, pw);
           fence_proxy_async_smem();
           tmem_wait_st();
           tc_fence_before();
@@ -630,83 +657,68 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
         // Tile layout [query half][chunk c of 8 queries][key][8 queries]: lane-consecutive keys make
         // every warp access one contiguous kilobyte.
         if (kg < g.N) {
-          float *pp = partial + ptile(jt) + ((half * 8) * 128 + kl) * 8;  // chunk c at + c * 1024
-          uint32_t w[8][8];  // all eight 32-byte loads in flight at once, then add and store
+          float *pp = partial + ptile(jt) + ((hf * 8 + c0) * 128 + kl) * 8;  // chunk c0 + m at + m * 1024
+          uint32_t w[QPT / 8][8];  // all the 32-byte loads in flight at once, then add and store
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
+          for (int m = 0; m < QPT / 8; ++m) {
             if (bi > 0) {
-              ld_keep_v8(pp + 1024 * c, w[c]);
+              ld_keep_v8(pp + 1024 * m, w[m]);
             } else {
 #pragma unroll
-              for (int e = 0; e < 8; ++e) w[c][e] = 0u;
+              for (int e = 0; e < 8; ++e) w[m][e] = 0u;
             }
           }
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
+          for (int m = 0; m < QPT / 8; ++m) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float2 a = acc[4 * c + e];
-              w[c][2 * e] = __float_as_uint(__uint_as_float(w[c][2 * e]) + a.x);
-              w[c][2 * e + 1] = __float_as_uint(__uint_as_float(w[c][2 * e + 1]) + a.y);
+              const float2 a = acc[4 * m + e];
+              w[m][2 * e] = __float_as_uint(__uint_as_float(w[m][2 * e]) + a.x);
+              w[m][2 * e + 1] = __float_as_uint(__uint_as_float(w[m][2 * e + 1]) + a.y);
             }
-            st_keep_v8(pp + 1024 * c, w[c]);
+            st_keep_v8(pp + 1024 * m, w[m]);
           }
         }
-        mbar_arrive(bar(C::B_BFREE + bb));
         ++u;
       }
       if (!ok) break;
-      // ---- dK_i, dV_i of the block -> BF16, once the block's last MMAs are complete. Each warp stages
-      // its 32 key rows in the part of the dS tile that only it writes (four 1 KB pieces, two per
-      // slice, double-buffered over the slices) and stores them with TMA, 16 rows per box.
+      // ---- dK_i, dV_i of the block -> BF16, once the block's last MMAs are complete: the first half
+      // of the column groups writes dK, the second dV, each group RC of the HD columns
       ok = wait_bar_warp(bar(C::B_M2DONE), (t - 1) & 1, ab);
       if (!ok) break;
       tc_fence_after();
       {
-        const int r16 = lane >> 4, rr = lane & 15;
-        const uint32_t sw = HD == 32 ? (uint32_t)((rr >> 1) & 3) : (uint32_t)((rr >> 2) & 1);
-        const float f = half == 0 ? g.scale : 1.f;
+        constexpr int NG = C::NEW / 8, RC = HD / NG;  // column groups per tensor, columns per group
+        const int tsel = cg / NG, coff = (cg % NG) * RC;
+        const float f = tsel == 0 ? g.scale : 1.f;
+        uint16_t *outb = tsel == 0 ? dK : dV;
         for (int il = 0; il < nb; ++il) {
-          uint32_t r[32];
-          const uint32_t col = tb + lb + C::TDKV + il * 2 * HD + half * HD;
-          if constexpr (HD == 32) {
+          uint32_t r[RC];
+          const uint32_t col = tb + lb + C::TDKV + il * 2 * HD + tsel * HD + coff;
+          if constexpr (RC == 32) {
             tmem_ld32(col, r);
+          } else if constexpr (RC == 16) {
+            tmem_ld16(col, r);
           } else {
-            tmem_ld16(col, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
+            tmem_ld8(col, r);
           }
-          tmem_wait_ld();
-          uint32_t w[HD / 2];
+          tmem_wait_ld(r);
+          uint32_t w[RC / 2];
 #pragma unroll
-          for (int c = 0; c < HD / 2; ++c)
+          for (int c = 0; c < RC / 2; ++c)
             w[c] = (uint32_t)f32_to_bf16_rn(__uint_as_float(r[2 * c]) * f) |
                    ((uint32_t)f32_to_bf16_rn(__uint_as_float(r[2 * c + 1]) * f) << 16);
-          if (il >= 2) {  // the stores of slice il - 2 have read this slot
-            if (lane == 0) bulk_wait_group_read<1>();
-            __syncwarp();
-          }
-          const uint32_t piece = sb0 + C::OFF_DS + (4 * q + 2 * (il & 1) + r16) * 2048 + half * 1024;
+          if (kg < g.N) {
+            uint16_t *out = outb + pos_row(g, b, i0 + il, kg) * g.H * HD + h * HD + coff;
 #pragma unroll
-          for (int c = 0; c < HD / 8; ++c)
-            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(piece + rr * C::ROWB + ((c ^ sw) << 4)),
-                         "r"(w[4 * c]), "r"(w[4 * c + 1]), "r"(w[4 * c + 2]), "r"(w[4 * c + 3])
-                         : "memory");
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            const uint32_t p0 = sb0 + C::OFF_DS + (4 * q + 2 * (il & 1)) * 2048 + half * 1024;
-            const CUtensorMap *m = half == 0 ? &mDK : &mDV;
-            tma_store_4d(m, p0, 0, h, kt * 128 + q * 32, b * g.S + i0 + il);
-            tma_store_4d(m, p0 + 2048, 0, h, kt * 128 + q * 32 + 16, b * g.S + i0 + il);
-            bulk_commit_group();
+            for (int c = 0; c < RC / 8; ++c)  // 16 bytes = 8 columns at a time
+              reinterpret_cast<uint4 *>(out)[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
           }
         }
-        if (lane == 0) bulk_wait_group_read<0>();  // the dS writes of the next step reuse these pieces
-        __syncwarp();
       }
       tc_fence_before();
       mbar_arrive(bar(C::B_DKVREAD));
     }
-    if (lane == 0) bulk_wait_group<0>();  // dK, dV stores performed before the CTA exits
   }
   tc_fence_before();
   __syncthreads();
@@ -791,10 +803,8 @@ cudaError_t launch_bwd_main_t(const Dims &g, int Gp, const uint16_t *Q, const ui
                               int *status, cudaStream_t stream) {
   using C = BwdCfg<HD>;
   const int nkt = (g.N + 127) / 128, NP = nkt * 128;
-  CUtensorMap mq, mk, mv, mdo, mbt, mdk, mdv;
+  CUtensorMap mq, mk, mv, mdo, mbt;
   cudaError_t e = make_rows_map(&mq, Q, g, 128);
-  if (e == cudaSuccess) e = make_rows_map(&mdk, dK, g, 16);
-  if (e == cudaSuccess) e = make_rows_map(&mdv, dV, g, 16);
   if (e == cudaSuccess) e = make_rows_map(&mk, K, g, 128);
   if (e == cudaSuccess) e = make_rows_map(&mv, V, g, 128);
   if (e == cudaSuccess) e = make_rows_map(&mdo, dO, g, 128);
@@ -825,7 +835,7 @@ cudaError_t launch_bwd_main_t(const Dims &g, int Gp, const uint16_t *Q, const ui
   attrs[0].val.clusterDim.z = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, bwd_kernel<HD>, mq, mk, mv, mdo, mbt, mdk, mdv, g, Gp, LSE, Dv, mask, dQ, partial,
+  return cudaLaunchKernelEx(&cfg, bwd_kernel<HD>, mq, mk, mv, mdo, mbt, g, Gp, LSE, Dv, mask, dQ, dK, dV, partial,
                             status);
 }
 

@@ -326,7 +326,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
           uint32_t r[64];
           tmem_ld32(scol, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
           tmem_ld32(scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-          tmem_wait_ld();
+          tmem_wait_ld(r);
 #pragma unroll
           for (int e = 0; e < 32; ++e) x[e] = make_float2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
         }
@@ -385,14 +385,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
           if constexpr (HD == 32) {
             uint32_t r[16];
             tmem_ld16(oaddr, r);
-            tmem_wait_ld();
+            tmem_wait_ld(r);
 #pragma unroll
             for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
             tmem_st16(oaddr, r);
           } else {
             uint32_t r[8];
             tmem_ld8(oaddr, r);
-            tmem_wait_ld();
+            tmem_wait_ld(r);
 #pragma unroll
             for (int e = 0; e < 8; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
             tmem_st8(oaddr, r);
@@ -446,7 +446,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
         } else {
           tmem_ld8(oaddr, r);
         }
-        tmem_wait_ld();
+        tmem_wait_ld(r);
         if (j < g.N) {
           const int i = i0 + il;
           const float inv = lsum > 0.f ? 1.f / lsum : 0.f;

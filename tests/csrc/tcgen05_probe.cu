@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(128) probe_kernel(const __grid_constant__ CUte
   for (int c = 0; c < 4; ++c) {
     uint32_t r[32];
     tmem_ld32(tbase + lane_off + c * 32, r);
-    tmem_wait_ld();
+    tmem_wait_ld(r);
     for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(r[e]);
   }
   for (int e = 0; e < 128; ++e) S_out[tid * 128 + e] = s[e];
@@ -145,10 +145,10 @@ __global__ void __launch_bounds__(128) probe_kernel(const __grid_constant__ CUte
   {
     uint32_t r[32];
     tmem_ld32(tbase + lane_off + 128, r);
-    tmem_wait_ld();
+    tmem_wait_ld(r);
     for (int e = 0; e < HD; ++e) O_out[tid * HD + e] = __uint_as_float(r[e]);
     tmem_ld32(tbase + lane_off + 128 + 64, r);
-    tmem_wait_ld();
+    tmem_wait_ld(r);
     for (int e = 0; e < HD; ++e) O2_out[tid * HD + e] = __uint_as_float(r[e]);
   }
   tc_fence_before();
