@@ -182,6 +182,14 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[N]) {
 #pragma unroll
   for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
 }
+template <int M, int N>
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[M][N]) {
+  tmem_wait_ld();
+#pragma unroll
+  for (int i = 0; i < M; ++i)
+#pragma unroll
+    for (int k = 0; k < N; ++k) asm volatile("" : "+r"(r[i][k]));
+}
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread t of the warp gets lane
