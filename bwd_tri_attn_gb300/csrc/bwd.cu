@@ -133,14 +133,6 @@ __device__ __forceinline__ void convert_to_f16(uint8_t *p, int bytes, int tid, i
   }
 }
 
-template <uint32_t R>
-__device__ __forceinline__ void reg_alloc() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
-}
-template <uint32_t R>
-__device__ __forceinline__ void reg_dealloc() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R));
-}
 
 // The step schedule every role walks in the same order: blocks of GB slices of
 // the supergroup [s0, s1), then query tiles, then the slices of the block.
