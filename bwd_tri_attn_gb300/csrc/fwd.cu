@@ -10,32 +10,42 @@
 // consecutive slices. The kernel is persistent: one CTA per SM walks units
 // blockIdx.x, blockIdx.x + gridDim.x, ... (units of one slice group and head
 // are adjacent, so concurrent CTAs share K and V tiles in L2), with the K/V
-// ring and the S buffers running on across units. For every key tile kt the bias tile
-// bias[b,h,jt,kt] is brought into shared memory once as BF16 (each softmax thread
-// stages its own query row, one tile ahead, double-buffered) and used for all GF slices:
+// ring, the bias and mask buffers and the S buffers running on across units.
+// For every key tile kt the bias tile bias[b,h,jt,kt] is brought into shared
+// memory once (BF16, by TMA) and used for all GF slices:
 //   S_i  = Q_i K_i^T           tcgen05 (BF16 x BF16 -> FP32 TMEM), M=128, N=128
 //   x    = S_i*scale + bias (+ mask), m_i = running max of x  (natural units)
 //   P_i  = exp2(x*log2e - m_i*log2e)   online softmax, FP32
 //   O_i += P_i V_i             tcgen05 (P: FP16 in TMEM as the A operand, V: FP16)
 // P is rounded to FP16 (11-bit significand) rather than BF16: a second BF16
 // rounding on the output's path would add as much error as the output rounding
-// itself. V is converted BF16 -> FP16 in shared memory (exact in FP16 range).
+// itself. V is converted BF16 -> FP16 in shared memory (exact in FP16 range) by
+// the softmax threads, a slice of the tile each, before they hand P over.
 //
-// Warp roles (352 threads): warps 0-7 = softmax (two threads per query row =
-// TMEM lane, each owning 64 of the tile's 128 keys; the row maximum is swapped
-// through shared memory), warp 8 = TMA producer, warp 9 = MMA issuer + TMEM
-// owner, warp 10 = V conversion to FP16. TMEM columns: three S buffers
-// [0,128) [128,256) [256,384), with P written as FP16 pairs over the columns
-// each thread has already read (keys 0-63 -> cols 0-31, keys 64-127 -> cols
-// 64-95 of the buffer); O_i at 384 + i*d.
+// Warp roles (384 threads): warps 0-7 = softmax, one thread per query row (TMEM
+// lane) over all 128 keys of a tile; warpgroup 0 takes the slices il = 0, 2, ...
+// and warpgroup 1 the slices il = 1, 3, ... of every key tile, so the two work on
+// different S tiles at once and never wait on each other inside a key tile.
+// Warp 8 = producer (TMA for Q, K, V and the bias tiles, bulk copies of the mask
+// rows and their per-tile "nonzero" flags), warp 9 = MMA issuer + TMEM owner,
+// warps 10-11 only donate registers (setmaxnreg: 216 per softmax thread).
+// TMEM columns: three S buffers [0,128) [128,256) [256,384), with P written as
+// FP16 pairs over the columns the thread has already read (keys 0-63 -> cols
+// 0-31, keys 64-127 -> cols 64-95 of the buffer); O_i at 384 + i*d.
 // The online max is updated lazily (only when it grows by more than 2^8), and
 // O is rescaled in TMEM only then. Between units the softmax warps read O out of
 // TMEM (then release it to the next unit's first P.V) before they normalise and
-// store it, and the next unit's first bias tile is staged during the last key tile.
+// store it.
+//
+// Shapes with N not a multiple of 8 (bias rows not 16-byte aligned, so no TMA
+// view) take a fallback where each softmax thread stages its own bias row one
+// key tile ahead with cp.async and the producer copies the mask rows lane by lane.
 #include "common.cuh"
 #include "sm100.cuh"
 #include "sync.cuh"
 #include "tmap.cuh"
+
+#include <string.h>
 
 namespace triattn {
 using namespace sm100;
@@ -43,41 +53,49 @@ using namespace sm100;
 template <int HD>
 struct FwdCfg {
   static constexpr int GF = HD == 32 ? 4 : 8;  // slices per CTA
-  static constexpr int NST = 4;                // K/V pipeline stages
+  static constexpr int NSB = 3;                // S buffers in TMEM = K/V pipeline stages: tile tg uses slot tg % 3
   static constexpr int ROWB = HD * 2;          // bytes of one operand row
   static constexpr int TILE = 128 * ROWB;      // bytes of one 128-row operand tile
   static constexpr uint32_t SW = HD == 32 ? kSwizzle64B : kSwizzle32B;
   static constexpr int NMAX = TRI_ATTN_MAX_N;
   static constexpr int MAXKT = NMAX / 128;
+  static constexpr int BTILE = 128 * 256;                   // BF16 bias tile: [2 halves][128 rows][128 B], SW128
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + GF * TILE;
-  static constexpr int OFF_V = OFF_K + NST * TILE;
-  static constexpr int OFF_BS = OFF_V + NST * TILE;         // 2 x BF16 bias rows: 128 x 256 B (double-buffered)
-  static constexpr int OFF_MASK = OFF_BS + 2 * 128 * 256;   // FP32 mask [GF][NMAX]
-  static constexpr int OFF_FLAG = OFF_MASK + GF * NMAX * 4; // int [GF][MAXKT]: tile has a nonzero mask
-  static constexpr int OFF_XCH = OFF_FLAG + GF * MAXKT * 4;  // row-max exchange [2][2][128] + row sums [GF][2][128]
-  static constexpr int OFF_BAR = OFF_XCH + (4 + 2 * GF) * 128 * 4;
+  static constexpr int OFF_V = OFF_K + NSB * TILE;
+  static constexpr int OFF_BS = OFF_V + NSB * TILE;         // 2 bias tiles (double-buffered by key tile)
+  static constexpr int OFF_MASK = OFF_BS + 2 * BTILE;       // 2 x BF16 mask rows [GF][NMAX] (by unit)
+  static constexpr int OFF_FLAG = OFF_MASK + 2 * GF * NMAX * 2;  // 2 x int [GF][MAXKT]: tile has a nonzero mask entry
+  static constexpr int OFF_BAR = OFF_FLAG + 2 * GF * MAXKT * 4;
   // barrier indices
   static constexpr int B_Q = 0;
   static constexpr int B_KVFULL = 1;
-  static constexpr int B_VREADY = B_KVFULL + NST;
-  static constexpr int B_KVEMPTY = B_VREADY + NST;
-  static constexpr int NSB = 3;                 // S buffers in TMEM
-  static constexpr int B_SFULL = B_KVEMPTY + NST;
-  static constexpr int B_PFULL = B_SFULL + NSB;
-  static constexpr int B_SFREE = B_PFULL + NSB;
-  static constexpr int B_PVDONE = B_SFREE + NSB;
-  static constexpr int B_OFINAL = B_PVDONE + GF;
+  static constexpr int B_SFULL = B_KVFULL + NSB;
+  static constexpr int B_PFULL = B_SFULL + NSB;  // P written and this tile's V converted
+  static constexpr int B_TDONE = B_PFULL + NSB;  // the slot's P.V has completed: S buffer and K/V stage free
+  static constexpr int B_OFINAL = B_TDONE + NSB;
   static constexpr int B_OFREE = B_OFINAL + 1;  // softmax warps have read O of the unit out of TMEM
   static constexpr int B_QFREE = B_OFREE + 1;   // the unit's last S MMA has read Q
   static constexpr int B_MDRAIN = B_QFREE + 1;  // every MMA of the CTA has completed (teardown)
-  static constexpr int NBAR = B_MDRAIN + 1;
+  static constexpr int B_BFULL = B_MDRAIN + 1;  // [2] bias tile landed
+  static constexpr int B_BFREE = B_BFULL + 2;   // [2] every slice of its key tile is done with it
+  static constexpr int B_MFULL = B_BFREE + 2;   // [2] mask rows of a unit landed
+  static constexpr int B_MFREE = B_MFULL + 2;   // [2] the unit is done with them
+  static constexpr int B_MREADY = B_MFREE + 2;  // [2] mask rows and their tile flags in place
+  static constexpr int NBAR = B_MREADY + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // [0] TMEM base, [1] abort flag
   static constexpr int SMEM_ALLOC = OFF_MISC + 16 + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr int NSOFT = 8, WARP_TMA = 8, WARP_MMA = 9, WARP_CV = 10, NTHREADS = 352;
+  static constexpr int NSOFT = 8, WARP_TMA = 8, WARP_MMA = 9, NTHREADS = 384;  // warps 10, 11: register donors
+  // setmaxnreg split: the softmax warpgroups take registers from the third warpgroup (per SMSP:
+  // two softmax warps and one other warp share 16K registers)
+  static constexpr uint32_t REG_LAUNCH = 168, REG_SOFT = 216, REG_OTHER = 72;
+  static_assert(256 * REG_SOFT + (NTHREADS - 256) * REG_OTHER == NTHREADS * REG_LAUNCH, "register split");
   static constexpr uint32_t TO = NSB * 128;  // O accumulators: TO + i*d
   static_assert(TO + GF * HD <= TMEM_COLS, "TMEM budget");
+  static_assert(OFF_BS % 1024 == 0, "SW128 bias tiles need 1 KB alignment");
+  static_assert(TILE % (16 * 128) == 0, "V conversion: whole 16-byte chunks per softmax thread");
+  static_assert(GF % 2 == 0, "slices split evenly over the two softmax warpgroups");
   static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 };
 
@@ -105,9 +123,9 @@ __device__ __forceinline__ FwdUnit fwd_unit(const Dims &g, int u) {
 template <int HD>
 __global__ void __launch_bounds__(FwdCfg<HD>::NTHREADS, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
-           const __grid_constant__ CUtensorMap mV, const Dims g, const uint16_t *__restrict__ bias,
-           const uint16_t *__restrict__ mask, uint16_t *__restrict__ O, float *__restrict__ LSE,
-           uint16_t *__restrict__ Ores, int *status) {
+           const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mB, const Dims g,
+           const uint16_t *__restrict__ bias, const uint16_t *__restrict__ mask, uint16_t *__restrict__ O,
+           float *__restrict__ LSE, uint16_t *__restrict__ Ores, int *status) {
   using C = FwdCfg<HD>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -115,29 +133,38 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nkt = (g.N + 127) / 128;
   const int nunits = g.B * ((g.S + C::GF - 1) / C::GF) * g.H * nkt;
+  const bool tma_bias = (g.N & 7) == 0;  // bias rows 16-byte aligned: TMA tiles; else per-thread staging
   auto bar = [&](int k) { return sb0 + C::OFF_BAR + 8u * (uint32_t)k; };
   volatile uint32_t *misc = reinterpret_cast<volatile uint32_t *>(sm + C::OFF_MISC);
   const Abort ab{reinterpret_cast<volatile int *>(misc + 1), status};
 
   if (tid == 0) {
     mbar_init(bar(C::B_Q), 1);
-    for (int s = 0; s < C::NST; ++s) {
-      mbar_init(bar(C::B_KVFULL + s), 1);
-      mbar_init(bar(C::B_VREADY + s), 1);
-      mbar_init(bar(C::B_KVEMPTY + s), 1);
-    }
     for (int s = 0; s < C::NSB; ++s) {
+      mbar_init(bar(C::B_KVFULL + s), 1);
       mbar_init(bar(C::B_SFULL + s), 1);
-      mbar_init(bar(C::B_PFULL + s), 256);
-      mbar_init(bar(C::B_SFREE + s), 1);
+      mbar_init(bar(C::B_PFULL + s), 128);  // the warpgroup that owns the tile
+      mbar_init(bar(C::B_TDONE + s), 1);
     }
-    for (int s = 0; s < C::GF; ++s) mbar_init(bar(C::B_PVDONE + s), 1);
     mbar_init(bar(C::B_OFINAL), 1);
     mbar_init(bar(C::B_OFREE), 256);
     mbar_init(bar(C::B_QFREE), 1);
     mbar_init(bar(C::B_MDRAIN), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(C::B_BFULL + s), 1);
+      mbar_init(bar(C::B_BFREE + s), 256);
+      mbar_init(bar(C::B_MFULL + s), 1);
+      mbar_init(bar(C::B_MFREE + s), 256);
+      mbar_init(bar(C::B_MREADY + s), 1);
+    }
     misc[1] = 0;
     fence_barrier_init();
+  }
+  if (mask && (g.N & 127) != 0) {
+    // keys in [N, nkt*128) of both mask buffers read as 0 (the copies never write them)
+    uint16_t *mk = reinterpret_cast<uint16_t *>(sm + C::OFF_MASK);
+    const int tail = nkt * 128 - g.N;
+    for (int x = tid; x < 2 * C::GF * tail; x += C::NTHREADS) mk[(x / tail) * C::NMAX + g.N + x % tail] = 0;
   }
   if (warp == C::WARP_MMA) {
     tmem_alloc(sb0 + C::OFF_MISC, C::TMEM_COLS);
@@ -150,12 +177,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
 
   if (warp == C::WARP_TMA) {
     // ------------------------------------------------------------ producer
-    int tg = 0, k = 0;  // tiles and units issued by this CTA
+    reg_dealloc<C::REG_OTHER>();
+    int tg = 0, k = 0, kb = 0;  // tiles, units and bias tiles issued by this CTA
     bool ok = true;
     if (lane == 0) {
       tma_prefetch_map(&mQ);
       tma_prefetch_map(&mK);
       tma_prefetch_map(&mV);
+      if (tma_bias) tma_prefetch_map(&mB);
     }
     for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++k) {
       const FwdUnit w = fwd_unit<HD>(g, u);
@@ -166,10 +195,67 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
         for (int il = 0; il < w.ng; ++il)
           tma_load_4d(sb0 + C::OFF_Q + il * C::TILE, &mQ, bar(C::B_Q), 0, w.h, w.jt * 128, w.b * g.S + w.i0 + il);
       }
+      if (mask) {  // the unit's mask rows into buffer k & 1 (free once unit k - 2 is done)
+        if (k >= 2) ok = wait_bar_warp(bar(C::B_MFREE + (k & 1)), ((k - 2) >> 1) & 1, ab);
+        if (!ok) break;
+        const uint32_t mdst = sb0 + C::OFF_MASK + (k & 1) * (C::GF * C::NMAX * 2);
+        const uint16_t *msrc = mask + ((int64_t)w.b * g.S + w.i0) * g.N;
+        if (tma_bias) {
+          if (lane == 0) {
+            mbar_arrive_expect_tx(bar(C::B_MFULL + (k & 1)), w.ng * g.N * 2);
+            for (int il = 0; il < w.ng; ++il)
+              bulk_load(mdst + il * C::NMAX * 2, msrc + (int64_t)il * g.N, g.N * 2, bar(C::B_MFULL + (k & 1)));
+          }
+        } else {
+          uint16_t *md = reinterpret_cast<uint16_t *>(sm + C::OFF_MASK) + (k & 1) * (C::GF * C::NMAX);
+          for (int il = 0; il < w.ng; ++il)
+            for (int e0 = lane; e0 < g.N; e0 += 256) {  // eight loads in flight per lane
+              uint16_t v[8];
+#pragma unroll
+              for (int m = 0; m < 8; ++m) v[m] = e0 + 32 * m < g.N ? msrc[(int64_t)il * g.N + e0 + 32 * m] : 0;
+#pragma unroll
+              for (int m = 0; m < 8; ++m)
+                if (e0 + 32 * m < g.N) md[il * C::NMAX + e0 + 32 * m] = v[m];
+            }
+        }
+        // per (slice, key tile): does the tile hold a nonzero mask entry (read once here, so that the
+        // softmax threads add mask values only where they change something)
+        if (tma_bias) ok = wait_bar_warp(bar(C::B_MFULL + (k & 1)), (k >> 1) & 1, ab);
+        if (!ok) break;
+        __syncwarp();
+        const uint16_t *mrows = reinterpret_cast<const uint16_t *>(sm + C::OFF_MASK) + (k & 1) * (C::GF * C::NMAX);
+        int *fl = reinterpret_cast<int *>(sm + C::OFF_FLAG) + (k & 1) * (C::GF * C::MAXKT);
+        for (int x = lane; x < w.ng * nkt; x += 32) {
+          const int il = x / nkt, kt = x % nkt;
+          const uint4 *mr = reinterpret_cast<const uint4 *>(mrows + il * C::NMAX + kt * 128);
+          uint32_t any = 0;
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const uint4 v = mr[c];
+            any |= v.x | v.y | v.z | v.w;
+          }
+          fl[il * C::MAXKT + kt] = (any & 0x7fff7fffu) != 0;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::B_MREADY + (k & 1)));
+      }
       const int T = nkt * w.ng;
       for (int t = 0; t < T && ok; ++t, ++tg) {
-        const int st = tg % C::NST, use = tg / C::NST;
-        if (use > 0) ok = wait_bar_warp(bar(C::B_KVEMPTY + st), (use - 1) & 1, ab);
+        if (tma_bias && t % w.ng == 0) {  // bias tile (jt, kt) into buffer kb & 1 (free once tile kb - 2 is done)
+          if (kb >= 2) ok = wait_bar_warp(bar(C::B_BFREE + (kb & 1)), ((kb - 2) >> 1) & 1, ab);
+          if (!ok) break;
+          if (lane == 0) {
+            const int kt = t / w.ng;
+            const uint32_t dst = sb0 + C::OFF_BS + (kb & 1) * C::BTILE;
+            mbar_arrive_expect_tx(bar(C::B_BFULL + (kb & 1)), C::BTILE);
+            tma_load_3d(dst, &mB, bar(C::B_BFULL + (kb & 1)), kt * 128, w.jt * 128, w.b * g.H + w.h);
+            tma_load_3d(dst + C::BTILE / 2, &mB, bar(C::B_BFULL + (kb & 1)), kt * 128 + 64, w.jt * 128,
+                        w.b * g.H + w.h);
+          }
+          ++kb;
+        }
+        const int st = tg % C::NSB, use = tg / C::NSB;
+        if (use > 0) ok = wait_bar_warp(bar(C::B_TDONE + st), (use - 1) & 1, ab);
         if (!ok) break;
         if (lane == 0) {
           const int kt = t / w.ng, il = t % w.ng;
@@ -182,245 +268,252 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
       }
     }
     if (!ok && lane == 0) {
-      // drain loads still in flight before the CTA's shared memory goes away
+      // drain copies still in flight before the CTA's shared memory goes away
       if (k > 0) drain_bar(bar(C::B_Q), (k - 1) & 1);
-      for (int t = max(0, tg - C::NST); t < tg; ++t) drain_bar(bar(C::B_KVFULL + t % C::NST), (t / C::NST) & 1);
-    }
-  } else if (warp == C::WARP_CV) {
-    // ------------------------------------------------------------ V: BF16 -> FP16 in shared memory
-    bool ok = true;
-    int tg = 0;
-    for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
-      const int T = nkt * fwd_unit<HD>(g, u).ng;
-      for (int t = 0; t < T && ok; ++t, ++tg) {
-        const int st = tg % C::NST, use = tg / C::NST;
-        ok = wait_bar_warp(bar(C::B_KVFULL + st), use & 1, ab);
-        if (!ok) break;
-        uint4 *v = reinterpret_cast<uint4 *>(sm + C::OFF_V + st * C::TILE);
-        for (int e = lane; e < C::TILE / 16; e += 32) {
-          uint4 x = v[e];
-          x.x = bf16x2_to_f16x2(x.x);
-          x.y = bf16x2_to_f16x2(x.y);
-          x.z = bf16x2_to_f16x2(x.z);
-          x.w = bf16x2_to_f16x2(x.w);
-          v[e] = x;
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(C::B_VREADY + st));
-      }
+      if (mask && tma_bias && k > 0) drain_bar(bar(C::B_MFULL + ((k - 1) & 1)), ((k - 1) >> 1) & 1);
+      for (int x = max(0, kb - 2); x < kb; ++x) drain_bar(bar(C::B_BFULL + (x & 1)), (x >> 1) & 1);
+      for (int t = max(0, tg - C::NSB); t < tg; ++t) drain_bar(bar(C::B_KVFULL + t % C::NSB), (t / C::NSB) & 1);
     }
   } else if (warp == C::WARP_MMA) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idS = idesc_f16(128, 128, true, true, false, false);
-      constexpr uint32_t idPV = idesc_f16(128, HD, false, false, false, true);
-      struct Pend {  // the tile whose P.V is still to be issued
-        int tg, kt, il, k;
-        bool last;
-      };
-      // O_il += P V for tile p; the first P.V of a unit first waits until the softmax warps
-      // have read the previous unit's O out of TMEM
-      auto issue_pv = [&](const Pend &p) -> bool {
-        const int sbuf = p.tg % C::NSB, st = p.tg % C::NST;
-        if (!wait_bar(bar(C::B_PFULL + sbuf), (p.tg / C::NSB) & 1, ab)) return false;
-        if (!wait_bar(bar(C::B_VREADY + st), (p.tg / C::NST) & 1, ab)) return false;
-        if (p.kt == 0 && p.il == 0 && p.k > 0 && !wait_bar(bar(C::B_OFREE), (p.k - 1) & 1, ab)) return false;
-        tc_fence_after();
-        const uint32_t vaddr = sb0 + C::OFF_V + st * C::TILE;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          mma_ts(tbase + C::TO + p.il * HD, tbase + sbuf * 128 + (ks >> 2) * 64 + (ks & 3) * 8,
-                 smem_desc(vaddr + ks * 16 * C::ROWB, 16, 8 * C::ROWB, C::SW), idPV,
-                 (p.kt > 0 || ks > 0) ? 1u : 0u);
-        mma_commit(bar(C::B_SFREE + sbuf));
-        mma_commit(bar(C::B_KVEMPTY + st));
-        mma_commit(bar(C::B_PVDONE + p.il));
-        if (p.last) mma_commit(bar(C::B_OFINAL));
-        return true;
-      };
-      bool ok = true, pending = false;
-      Pend pv{};
-      int tg = 0, k = 0;
-      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++k) {
-        const int ng = fwd_unit<HD>(g, u).ng, T = nkt * ng;
-        ok = wait_bar(bar(C::B_Q), k & 1, ab);
-        for (int t = 0; t < T && ok; ++t, ++tg) {
-          const int st = tg % C::NST, sbuf = tg % C::NSB, il = t % ng;
-          ok = wait_bar(bar(C::B_KVFULL + st), (tg / C::NST) & 1, ab);
-          if (ok && tg >= C::NSB) ok = wait_bar(bar(C::B_SFREE + sbuf), ((tg / C::NSB) - 1) & 1, ab);
-          if (!ok) break;
+    reg_dealloc<C::REG_OTHER>();
+    // The whole warp runs this loop converged (every decision is warp-uniform) and elect.sync
+    // picks the lane that issues each MMA and commit.
+    constexpr uint32_t idS = idesc_f16(128, 128, true, true, false, false);
+    constexpr uint32_t idPV = idesc_f16(128, HD, false, false, false, true);
+    // Two cursors walk the CTA's tiles (units blockIdx.x, +gridDim.x, ...; in a unit key tile kt,
+    // then slice il). S of the S cursor's tile is issued as soon as its K tile has landed and its
+    // S buffer is free; P.V of the P.V cursor's tile as soon as its P is written (and, for a
+    // unit's first tile, the previous unit's O has been read out). Whichever is ready first goes
+    // first, so the two softmax warpgroups never wait on each other's progress for their S.
+    struct Cur {
+      int u, k, t, T, ng, tg;
+    };
+    auto start = [&](Cur &c, int u, int k, int tg) {
+      c.u = u;
+      c.k = k;
+      c.t = 0;
+      c.tg = tg;
+      c.ng = u < nunits ? fwd_unit<HD>(g, u).ng : 0;
+      c.T = nkt * c.ng;
+    };
+    auto advance = [&](Cur &c) {
+      ++c.tg;
+      if (++c.t == c.T) start(c, c.u + (int)gridDim.x, c.k + 1, c.tg);
+    };
+    // a phase counts as complete only once every lane has observed it (each lane acquires)
+    auto done = [&](int k, int parity) { return __all_sync(0xffffffffu, mbar_test_wait(bar(k), parity)); };
+    Cur cs, cp;
+    start(cs, blockIdx.x, 0, 0);
+    start(cp, blockIdx.x, 0, 0);
+    // descriptor bases: the start-address field is (address >> 4) in the low bits, so an operand
+    // at base + off has descriptor base_desc + (off >> 4) (addresses stay below 256 KB)
+    const uint64_t dq0 = smem_desc(sb0 + C::OFF_Q, 16, 8 * C::ROWB, C::SW);
+    const uint64_t dk0 = smem_desc(sb0 + C::OFF_K, 16, 8 * C::ROWB, C::SW);
+    const uint64_t dv0 = smem_desc(sb0 + C::OFF_V, 16, 8 * C::ROWB, C::SW);
+    bool ok = true, idle = false;
+    uint64_t t_idle = 0;
+    while (ok && cp.u < nunits) {
+      bool progress = false;
+      {  // O_il += P V (P.V needs P written and V converted: both certified by PFULL)
+        const int sbuf = cp.tg % C::NSB;
+        if (done(C::B_PFULL + sbuf, (cp.tg / C::NSB) & 1) &&
+            (cp.t != 0 || cp.k == 0 || done(C::B_OFREE, (cp.k - 1) & 1))) {
           tc_fence_after();
-          const uint32_t qaddr = sb0 + C::OFF_Q + il * C::TILE, kaddr = sb0 + C::OFF_K + st * C::TILE;
+          const int il = cp.t % cp.ng, kt = cp.t / cp.ng;
+          const uint64_t dv = dv0 + (uint64_t)((sbuf * C::TILE) >> 4);
+          const uint32_t dO = tbase + C::TO + il * HD, aP = tbase + sbuf * 128;
+          mma_ts_e(dO, aP, dv, idPV, kt > 0 ? 1u : 0u);
 #pragma unroll
-          for (int ks = 0; ks < HD / 16; ++ks)
-            mma_ss(tbase + sbuf * 128, smem_desc(qaddr + ks * 32, 16, 8 * C::ROWB, C::SW),
-                   smem_desc(kaddr + ks * 32, 16, 8 * C::ROWB, C::SW), idS, ks > 0 ? 1u : 0u);
-          mma_commit(bar(C::B_SFULL + sbuf));
-          if (t == T - 1) mma_commit(bar(C::B_QFREE));
-          if (pending) ok = issue_pv(pv);
-          pv = Pend{tg, t / ng, il, k, t == T - 1};
-          pending = true;
+          for (int ks = 1; ks < 8; ++ks)
+            mma_ts_e(dO, aP + (ks >> 2) * 64 + (ks & 3) * 8, dv + (uint64_t)((ks * 16 * C::ROWB) >> 4), idPV, 1u);
+          mma_commit_e(bar(C::B_TDONE + sbuf));
+          if (cp.t == cp.T - 1) mma_commit_e(bar(C::B_OFINAL));
+          advance(cp);
+          progress = true;
         }
       }
-      if (ok && pending) ok = issue_pv(pv);
-      mma_commit(bar(C::B_MDRAIN));  // lands once every MMA issued above has completed
-      drain_bar(bar(C::B_MDRAIN), 0);
+      // S = Q K^T into a free buffer. S(n) is issued only once P.V of the same slice's previous key
+      // tile (tile n - ng) has been issued, so that the commit of S(n) also covers that P.V: the
+      // softmax threads rely on this when they rescale O after waiting for S(n).
+      if (cs.u < nunits && cs.tg < cp.tg + min(C::NSB, cs.ng)) {
+        const int sbuf = cs.tg % C::NSB;
+        if (done(C::B_Q, cs.k & 1) && done(C::B_KVFULL + sbuf, (cs.tg / C::NSB) & 1) &&
+            (cs.tg < C::NSB || done(C::B_TDONE + sbuf, ((cs.tg / C::NSB) - 1) & 1))) {
+          tc_fence_after();
+          const uint64_t dq = dq0 + (uint64_t)(((cs.t % cs.ng) * C::TILE) >> 4), dk = dk0 + (uint64_t)((sbuf * C::TILE) >> 4);
+          mma_ss_e(tbase + sbuf * 128, dq, dk, idS, 0u);
+#pragma unroll
+          for (int ks = 1; ks < HD / 16; ++ks) mma_ss_e(tbase + sbuf * 128, dq + 2 * ks, dk + 2 * ks, idS, 1u);
+          mma_commit_e(bar(C::B_SFULL + sbuf));
+          if (cs.t == cs.T - 1) mma_commit_e(bar(C::B_QFREE));
+          advance(cs);
+          progress = true;
+        }
+      }
+      if (progress) {
+        idle = false;
+      } else {
+        // nothing ready: sleep briefly on the next P (the usual next event), with a time limit overall
+        mbar_try_wait_for(bar(C::B_PFULL + cp.tg % C::NSB), (cp.tg / C::NSB) & 1, 100);
+        const uint64_t now = __shfl_sync(0xffffffffu, globaltimer_ns(), 0);
+        if (!idle) {
+          idle = true;
+          t_idle = now;
+        } else if (__any_sync(0xffffffffu, *ab.flag != 0)) {
+          ok = false;
+        } else if (now - t_idle > kWaitLimitNs) {
+          if (lane == 0) {
+            *ab.flag = 1;
+            atomicExch(ab.status, kStatusTimeout);
+          }
+          ok = false;
+        }
+      }
     }
-  } else {
+    mma_commit_e(bar(C::B_MDRAIN));  // lands once every MMA issued above has completed
+    if (lane == 0) drain_bar(bar(C::B_MDRAIN), 0);
+    __syncwarp();
+  } else if (warp < C::NSOFT) {
     // ------------------------------------------------------------ softmax / epilogue (warps 0-7)
-    // Two threads per query row: warp w handles TMEM lane quarter q = w % 4 and
-    // the key half w / 4 (64 of the tile's 128 keys).
-    const int q = warp & 3, half = warp >> 2;
+    reg_alloc<C::REG_SOFT>();
+    // One thread per query row (TMEM lane); warpgroup wg = warp / 4 takes the slices
+    // il = wg, wg + 2, ... of every key tile, so the two warpgroups work on different
+    // S tiles at the same time and never wait on each other within a key tile.
+    constexpr int NL = C::GF / 2;  // slices per warpgroup
+    const int q = warp & 3, wg = warp >> 2, wtid = tid & 127;
     const int row = q * 32 + lane;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    const uint32_t pair_bar = 2 + q;  // named barrier of the two warps sharing these rows
-    float *maskf = reinterpret_cast<float *>(sm + C::OFF_MASK);
-    int *flags = reinterpret_cast<int *>(sm + C::OFF_FLAG);
-    float *xmax = reinterpret_cast<float *>(sm + C::OFF_XCH);  // [2 parities][2 halves][128 rows]
     const float2 sc2 = make_float2(g.scale, g.scale), l2e2 = make_float2(kLog2e, kLog2e);
     const uint32_t sw = row & 7;
-    // bias row of a unit: rows past N reuse a valid bias row; their outputs are dropped
-    auto bias_row = [&](const FwdUnit &w) {
+    // this thread's row of a bias tile: [half][row][128 B], 16-byte chunk c at ((c ^ (row & 7)) << 4)
+    const uint32_t brow_off = (uint32_t)(row * 128);
+    // fallback staging (N not a multiple of 8): warpgroup wg copies key half wg of its rows of key
+    // tile kt into bias buffer sb, keys past N as BF16 -inf; rows past N reuse a valid bias row
+    auto stage_bias = [&](const FwdUnit &w, int kt, int sb) {
       const int jr = min(w.jt * 128 + row, g.N - 1);
-      return bias + (((int64_t)w.b * g.H + w.h) * g.N + jr) * g.N;
-    };
-    // this thread stages its half (64 keys) of the bias row for key tile kt into staging buffer
-    // sb; keys past N get BF16 -inf, so that their scores are -inf
-    auto stage_bias = [&](const uint16_t *brow, int kt, int sb) {
-      const int k0 = kt * 128 + half * 64, nv = min(64, g.N - k0);
-      const uint16_t *src = brow + k0;
-      const uint32_t stage_row = sb0 + C::OFF_BS + sb * 32768 + row * 256;
+      const uint16_t *src = bias + (((int64_t)w.b * g.H + w.h) * g.N + jr) * g.N + kt * 128 + wg * 64;
+      const int nv = min(64, g.N - (kt * 128 + wg * 64));
+      const uint32_t dst = sb0 + C::OFF_BS + sb * C::BTILE + wg * (C::BTILE / 2) + brow_off;
       for (int e = max(nv, 0); e < 64; ++e)
-        asm volatile("st.shared.u16 [%0], %1;" ::"r"(stage_row + (((half * 8 + (e >> 3)) ^ sw) << 4) + (e & 7) * 2),
-                     "h"((uint16_t)0xff80u));
-      if (nv > 0) {
-        if ((g.N & 7) == 0) {
-          for (int c = 0; c < nv / 8; ++c) cp_async_16(stage_row + (((half * 8 + c) ^ sw) << 4), src + c * 8);
-        } else if ((g.N & 1) == 0) {
-          for (int p = 0; p < nv / 2; ++p)
-            cp_async_4(stage_row + (((half * 8 + (p >> 2)) ^ sw) << 4) + (p & 3) * 4, src + 2 * p);
-        } else {
-          for (int e = 0; e < nv; ++e) {
-            const uint16_t v = src[e];
-            asm volatile("st.shared.u16 [%0], %1;" ::"r"(stage_row + (((half * 8 + (e >> 3)) ^ sw) << 4) + (e & 7) * 2),
-                         "h"(v));
-          }
+        asm volatile("st.shared.u16 [%0], %1;" ::"r"(dst + (((e >> 3) ^ sw) << 4) + (e & 7) * 2), "h"((uint16_t)0xff80u));
+      if ((g.N & 1) == 0) {
+        for (int p = 0; p < nv / 2; ++p) cp_async_4(dst + (((p >> 2) ^ sw) << 4) + (p & 3) * 4, src + 2 * p);
+      } else {
+        for (int e = 0; e < nv; ++e) {
+          const uint16_t v = src[e];
+          asm volatile("st.shared.u16 [%0], %1;" ::"r"(dst + (((e >> 3) ^ sw) << 4) + (e & 7) * 2), "h"(v));
         }
       }
       cp_async_commit();
     };
-    int pvcnt[C::GF];  // P.V commits per slice of the units before this one (PVDONE phases)
-#pragma unroll
-    for (int il = 0; il < C::GF; ++il) pvcnt[il] = 0;
     bool ok = true;
-    int tg = 0, k = 0;
-    int kb = 0;  // key tiles staged so far: tile n goes to staging buffer n & 1
-    if (blockIdx.x < nunits) stage_bias(bias_row(fwd_unit<HD>(g, blockIdx.x)), 0, kb++ & 1);
+    int tgu = 0, k = 0;  // tiles of the units before this one, units done
+    int kb = 0;          // key tiles of bias used so far: tile n lives in bias buffer n & 1
+    if (!tma_bias && blockIdx.x < nunits) stage_bias(fwd_unit<HD>(g, blockIdx.x), 0, 0);
     for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++k) {
       const FwdUnit w = fwd_unit<HD>(g, u);
       const int b = w.b, h = w.h, jt = w.jt, i0 = w.i0, ng = w.ng;
       const int j = jt * 128 + row;
-      const uint16_t *brow = bias_row(w);
-      // per-slice additive mask (log2 units) and per-tile "has a nonzero entry" flags
-      named_sync(1, 256);  // every thread is done with the previous unit's mask rows and flags
-      if (tid < C::GF * C::MAXKT) flags[tid] = 0;
-      named_sync(1, 256);
-      if (mask) {
-        for (int il0 = 0; il0 < ng; il0 += 2) {  // two slices per memory round trip
-          float v[2][C::NMAX / 256];
-#pragma unroll
-          for (int a = 0; a < 2; ++a)
-#pragma unroll
-            for (int m = 0; m < C::NMAX / 256; ++m) {
-              const int il = il0 + a, kk = tid + 256 * m;
-              v[a][m] = (il < ng && kk < g.N) ? bf16_to_f32(mask[((int64_t)b * g.S + i0 + il) * g.N + kk]) : 0.f;
-            }
-#pragma unroll
-          for (int a = 0; a < 2; ++a)
-#pragma unroll
-            for (int m = 0; m < C::NMAX / 256; ++m) {
-              const int il = il0 + a, kk = tid + 256 * m;
-              if (il < ng && kk < nkt * 128) {
-                maskf[il * C::NMAX + kk] = v[a][m];
-                if (v[a][m] != 0.f) flags[il * C::MAXKT + (kk >> 7)] = 1;  // every writer stores the same value
-              }
-            }
-        }
-      }
-      named_sync(1, 256);
+      const uint16_t *mk = reinterpret_cast<const uint16_t *>(sm + C::OFF_MASK) + (k & 1) * (C::GF * C::NMAX);
+      const int *flags = reinterpret_cast<const int *>(sm + C::OFF_FLAG) + (k & 1) * (C::GF * C::MAXKT);
+      if (mask) ok = wait_bar_warp(bar(C::B_MREADY + (k & 1)), (k >> 1) & 1, ab);
+      if (!ok) break;
 
-      float m_ref[C::GF], l_sum[C::GF];  // m_ref is identical in both threads of a row; l_sum is per half
+      float m_ref[NL], l_sum[NL];
 #pragma unroll
-      for (int il = 0; il < C::GF; ++il) {
-        m_ref[il] = -INFINITY;
-        l_sum[il] = 0.f;
+      for (int s = 0; s < NL; ++s) {
+        m_ref[s] = -INFINITY;
+        l_sum[s] = 0.f;
       }
-      for (int kt = 0; kt < nkt && ok; ++kt) {
-        cp_async_wait_all();  // this key tile's bias row is in staging buffer (kb - 1) & 1
-        const uint32_t brow_s = sb0 + C::OFF_BS + ((kb - 1) & 1) * 32768 + row * 256;
-        if (kt + 1 < nkt) {
-          stage_bias(brow, kt + 1, kb++ & 1);
-        } else if (u + (int)gridDim.x < nunits) {
-          stage_bias(bias_row(fwd_unit<HD>(g, u + gridDim.x)), 0, kb++ & 1);  // the next unit's first tile
+      for (int kt = 0; kt < nkt && ok; ++kt, ++kb) {
+        if (tma_bias) {
+          ok = wait_bar_warp(bar(C::B_BFULL + (kb & 1)), (kb >> 1) & 1, ab);
+          if (!ok) break;
+        } else {
+          cp_async_wait_all();  // this warpgroup's half of the tile is in buffer kb & 1
+          named_sync(1, 256);   // and the other half; every thread is done with tile kb - 1
+          if (kt + 1 < nkt) {
+            stage_bias(w, kt + 1, (kb + 1) & 1);
+          } else if (u + (int)gridDim.x < nunits) {
+            stage_bias(fwd_unit<HD>(g, u + gridDim.x), 0, (kb + 1) & 1);  // the next unit's first tile
+          }
         }
+        const uint32_t brow_s = sb0 + C::OFF_BS + (kb & 1) * C::BTILE + brow_off;
+        const int nvalid = g.N - kt * 128;  // keys past N in the last key tile get score -inf
 #pragma unroll 1
-        for (int il = 0; il < ng; ++il, ++tg) {
-          const int sbuf = tg % C::NSB;
+        for (int il = wg; il < ng; il += 2) {
+          const int tg = tgu + kt * ng + il, sbuf = tg % C::NSB, sl = il >> 1;
           ok = wait_bar_warp(bar(C::B_SFULL + sbuf), (tg / C::NSB) & 1, ab);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t scol = tbase + lane_base + sbuf * 128 + half * 64;
-          float2 x[32];
+          const uint32_t scol = tbase + lane_base + sbuf * 128;
+          float2 x[64];
           {
-            uint32_t r[64];
-            tmem_ld32(scol, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-            tmem_ld32(scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+            uint32_t r[128];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(scol + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&r[32 * c]));
             tmem_wait_ld(r);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) x[e] = make_float2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
+            for (int e = 0; e < 64; ++e) x[e] = make_float2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
           }
           // scores in natural units: S*scale + bias (+ mask)
 #pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {  // 8 keys (16 bytes of BF16 bias) at a time
+          for (int ch = 0; ch < 16; ++ch) {  // 8 keys (16 bytes of BF16 bias) at a time
             uint32_t bw[4];
             asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
                          : "=r"(bw[0]), "=r"(bw[1]), "=r"(bw[2]), "=r"(bw[3])
-                         : "r"(brow_s + (((half * 8 + ch) ^ sw) << 4)));
+                         : "r"(brow_s + (ch >> 3) * (C::BTILE / 2) + (((ch & 7) ^ sw) << 4)));
 #pragma unroll
             for (int m = 0; m < 4; ++m)
               x[4 * ch + m] = __ffma2_rn(x[4 * ch + m], sc2,
                                          make_float2(__uint_as_float(bw[m] << 16), __uint_as_float(bw[m] & 0xffff0000u)));
           }
-          if (flags[il * C::MAXKT + kt]) {
-            const float2 *mrow = reinterpret_cast<const float2 *>(maskf + il * C::NMAX + kt * 128 + half * 64);
+          if (mask && flags[il * C::MAXKT + kt]) {
+            // the slice's mask entries of this key tile (the same for every row: broadcast loads),
+            // 16 keys at a time; each chunk's address depends on the previous chunk's sums so that
+            // the loads are not all hoisted next to the 128 live scores
+            uint32_t maddr = smem_u32(mk + il * C::NMAX + kt * 128);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) x[e] = __fadd2_rn(x[e], mrow[e]);
+            for (int c = 0; c < 8; ++c) {
+              uint32_t mw[8];
+              asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                           : "=r"(mw[0]), "=r"(mw[1]), "=r"(mw[2]), "=r"(mw[3])
+                           : "r"(maddr));
+              asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                           : "=r"(mw[4]), "=r"(mw[5]), "=r"(mw[6]), "=r"(mw[7])
+                           : "r"(maddr + 16));
+#pragma unroll
+              for (int m = 0; m < 8; ++m)
+                x[8 * c + m] = __fadd2_rn(x[8 * c + m], make_float2(__uint_as_float(mw[m] << 16),
+                                                                    __uint_as_float(mw[m] & 0xffff0000u)));
+              maddr += 32;
+              asm volatile("" : "+r"(maddr) : "f"(x[8 * c + 7].y));
+            }
           }
-          float mloc;
+          if (nvalid < 128) {
+#pragma unroll
+            for (int e = 0; e < 64; ++e) {
+              if (2 * e >= nvalid) x[e].x = -INFINITY;
+              if (2 * e + 1 >= nvalid) x[e].y = -INFINITY;
+            }
+          }
+          float mt;
           {
-            float m4[4];
+            float m8[8];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) m4[c] = fmaxf(x[c].x, x[c].y);
+            for (int c = 0; c < 8; ++c) m8[c] = fmaxf(x[c].x, x[c].y);
 #pragma unroll
-            for (int e = 4; e < 32; ++e) m4[e & 3] = fmaxf(m4[e & 3], fmaxf(x[e].x, x[e].y));
-            mloc = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+            for (int e = 8; e < 64; ++e) m8[e & 7] = fmaxf(m8[e & 7], fmaxf(x[e].x, x[e].y));
+            mt = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
           }
-          // the row maximum over both key halves, exchanged through shared memory
-          xmax[((tg & 1) * 2 + half) * 128 + row] = mloc;
-          named_sync(pair_bar, 64);
-          const float mt = fmaxf(mloc, xmax[((tg & 1) * 2 + (half ^ 1)) * 128 + row]);
-          // lazy online-softmax rescale (the same decision in both threads of the row)
+          // lazy online-softmax rescale
           float alpha = 1.f;
           bool resc = false;
           float mr = m_ref[0];
-          int pvc = pvcnt[0];
 #pragma unroll
-          for (int qq = 1; qq < C::GF; ++qq)
-            if (qq == il) {
-              mr = m_ref[qq];
-              pvc = pvcnt[qq];
-            }
+          for (int qq = 1; qq < NL; ++qq)
+            if (qq == sl) mr = m_ref[qq];
           if (kt == 0) {
             mr = mt;
           } else if (mt > mr + 8.f * kLn2) {  // grows by more than 2^8 in P
@@ -433,117 +526,133 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
             }
           }
           if (__any_sync(0xffffffffu, resc)) {
-            ok = wait_bar_warp(bar(C::B_PVDONE + il), (pvc + kt - 1) & 1, ab);  // P.V of key tile kt-1 done
-            if (!ok) break;
-            tc_fence_after();
-            // this thread rescales its half of the row's O columns
-            const uint32_t oaddr = tbase + lane_base + C::TO + il * HD + half * (HD / 2);
-            if constexpr (HD == 32) {
-              uint32_t r[16];
-              tmem_ld16(oaddr, r);
-              tmem_wait_ld(r);
-#pragma unroll
-              for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-              tmem_st16(oaddr, r);
-            } else {
+            // P.V of this slice's key tile kt-1 has completed: it was issued before S of this tile,
+            // whose commit (waited for above) covers every earlier MMA of the issuing thread
+
+            const uint32_t oaddr = tbase + lane_base + C::TO + il * HD;
+#pragma unroll 1
+            for (int c = 0; c < HD; c += 8) {  // 8 columns at a time: few registers next to the live scores
               uint32_t r[8];
-              tmem_ld8(oaddr, r);
+              tmem_ld8(oaddr + c, r);
               tmem_wait_ld(r);
 #pragma unroll
               for (int e = 0; e < 8; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-              tmem_st8(oaddr, r);
+              tmem_st8(oaddr + c, r);
             }
           }
           const float mu = (mr == -INFINITY) ? 0.f : mr * kLog2e;
           const float2 mu2 = make_float2(-mu, -mu);
           float2 ls2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-          uint32_t pk[32];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float2 a = __ffma2_rn(x[e], l2e2, mu2);  // (x - m) in log2 units
-            const float2 pv = make_float2(ex2(a.x), ex2(a.y));
-            ls2[e & 3] = __fadd2_rn(ls2[e & 3], pv);
-            pk[e] = pack_f16x2(pv.x, pv.y);
+          for (int hh = 0; hh < 2; ++hh) {  // keys 64*hh + [0,64): P (FP16 pairs) over S columns 64*hh + [0,32)
+            uint32_t pk[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const float2 a = __ffma2_rn(x[32 * hh + e], l2e2, mu2);  // (x - m) in log2 units
+              const float2 pv = make_float2(ex2(a.x), ex2(a.y));
+              ls2[e & 3] = __fadd2_rn(ls2[e & 3], pv);
+              pk[e] = pack_f16x2(pv.x, pv.y);
+            }
+            tmem_st32(scol + 64 * hh, pk);
           }
           const float2 lsa = __fadd2_rn(__fadd2_rn(ls2[0], ls2[1]), __fadd2_rn(ls2[2], ls2[3]));
           const float ls = lsa.x + lsa.y;
 #pragma unroll
-          for (int qq = 0; qq < C::GF; ++qq)
-            if (qq == il) {
+          for (int qq = 0; qq < NL; ++qq)
+            if (qq == sl) {
               m_ref[qq] = mr;
               l_sum[qq] = l_sum[qq] * alpha + ls;
             }
-          // P (FP16 pairs) over this thread's own S columns: keys half*64 + [0,64) -> cols half*64 + [0,32)
-          tmem_st32(scol, pk);
+          {
+            // the tile's V, BF16 -> FP16 in place (V landed with K, before S), a share per thread
+            const int st = sbuf;
+            ok = wait_bar(bar(C::B_KVFULL + st), (tg / C::NSB) & 1, ab);
+            uint4 *v = reinterpret_cast<uint4 *>(sm + C::OFF_V + st * C::TILE);
+#pragma unroll
+            for (int e = wtid; e < C::TILE / 16; e += 128) {
+              uint4 xv = v[e];
+              xv.x = bf16x2_to_f16x2(xv.x);
+              xv.y = bf16x2_to_f16x2(xv.y);
+              xv.z = bf16x2_to_f16x2(xv.z);
+              xv.w = bf16x2_to_f16x2(xv.w);
+              v[e] = xv;
+            }
+            fence_proxy_async_smem();
+          }
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(bar(C::B_PFULL + sbuf));
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+        }
+        if (!ok) break;
+        if (tma_bias) {  // this thread is done with the key tile's bias
+          fence_proxy_async_smem();  // order the generic-proxy reads before the TMA overwrite
+          mbar_arrive(bar(C::B_BFREE + (kb & 1)));
         }
       }
       if (!ok) break;
-#pragma unroll
-      for (int il = 0; il < C::GF; ++il)
-        if (il < ng) pvcnt[il] += nkt;
-      // epilogue: read O of the unit out of TMEM and release it, then O = acc / l -> BF16, residual, LSE
+      if (mask) {
+        fence_proxy_async_smem();  // (the next copy into this buffer is an async-proxy write)
+        mbar_arrive(bar(C::B_MFREE + (k & 1)));
+      }
+      tgu += nkt * ng;
+      // epilogue: read O of this warpgroup's slices out of TMEM and release it, then
+      // O = acc / l -> BF16, residual, LSE
       ok = wait_bar_warp(bar(C::B_OFINAL), k & 1, ab);
       if (!ok) break;
       tc_fence_after();
-      uint32_t oacc[C::GF][HD / 2] = {};
+      uint32_t oacc[NL][HD] = {};
 #pragma unroll
-      for (int il = 0; il < C::GF; ++il) {
-        if (il < ng) {
-          const uint32_t oaddr = tbase + lane_base + C::TO + il * HD + half * (HD / 2);
+      for (int s = 0; s < NL; ++s) {
+        if (wg + 2 * s < ng) {
+          const uint32_t oaddr = tbase + lane_base + C::TO + (wg + 2 * s) * HD;
           if constexpr (HD == 32) {
-            tmem_ld16(oaddr, oacc[il]);
+            tmem_ld32(oaddr, oacc[s]);
           } else {
-            tmem_ld8(oaddr, oacc[il]);
+            tmem_ld16(oaddr, oacc[s]);
           }
         }
       }
       tmem_wait_ld(oacc);
       tc_fence_before();
       mbar_arrive(bar(C::B_OFREE));
-      float *xl = reinterpret_cast<float *>(sm + C::OFF_XCH) + 4 * 128;  // [GF][2 halves][128 rows]
 #pragma unroll
-      for (int qq = 0; qq < C::GF; ++qq) xl[(qq * 2 + half) * 128 + row] = l_sum[qq];
-      named_sync(pair_bar, 64);
+      for (int s = 0; s < NL; ++s) {
+        const int il = wg + 2 * s;
+        if (il >= ng || j >= g.N) continue;
+        const int i = i0 + il;
+        const float lsum = l_sum[s];
+        const float inv = lsum > 0.f ? __frcp_rn(lsum) : 0.f;
+        uint32_t ob[HD / 2], rb[HD / 2];
 #pragma unroll
-      for (int il = 0; il < C::GF; ++il) {
-        if (il >= ng) continue;
-        const float lsum = xl[(il * 2 + 0) * 128 + row] + xl[(il * 2 + 1) * 128 + row];
-        if (j < g.N) {
-          const int i = i0 + il;
-          const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-          uint32_t ob[HD / 4], rb[HD / 4];
-#pragma unroll
-          for (int c = 0; c < HD / 4; ++c) {
-            const float o0 = __uint_as_float(oacc[il][2 * c]) * inv, o1 = __uint_as_float(oacc[il][2 * c + 1]) * inv;
-            const uint16_t a0 = f32_to_bf16_rn(o0), a1 = f32_to_bf16_rn(o1);
-            ob[c] = (uint32_t)a0 | ((uint32_t)a1 << 16);
-            rb[c] = (uint32_t)f32_to_bf16_rn(o0 - bf16_to_f32(a0)) |
-                    ((uint32_t)f32_to_bf16_rn(o1 - bf16_to_f32(a1)) << 16);
-          }
-          const int64_t off = pos_row(g, b, i, j) * g.H * HD + (int64_t)h * HD + half * (HD / 2);
-          // this thread's half row: 32 bytes (d = 32) or 16 bytes (d = 16), one store each
-          if constexpr (HD == 32) {
-            asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(O + off), "r"(ob[0]), "r"(ob[1]),
-                         "r"(ob[2]), "r"(ob[3]), "r"(ob[4]), "r"(ob[5]), "r"(ob[6]), "r"(ob[7])
-                         : "memory");
-            if (Ores)
-              asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(Ores + off), "r"(rb[0]),
-                           "r"(rb[1]), "r"(rb[2]), "r"(rb[3]), "r"(rb[4]), "r"(rb[5]), "r"(rb[6]), "r"(rb[7])
-                           : "memory");
-          } else {
-            *reinterpret_cast<uint4 *>(O + off) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
-            if (Ores) *reinterpret_cast<uint4 *>(Ores + off) = make_uint4(rb[0], rb[1], rb[2], rb[3]);
-          }
-          if (half == 0)
-            LSE[(((int64_t)b * g.S + i) * g.H + h) * g.N + j] =
-                lsum > 0.f ? m_ref[il] + __log2f(lsum) * kLn2 : -INFINITY;
+        for (int c = 0; c < HD / 2; ++c) {
+          const float o0 = __uint_as_float(oacc[s][2 * c]) * inv, o1 = __uint_as_float(oacc[s][2 * c + 1]) * inv;
+          ob[c] = pack_bf16x2(o0, o1);
+          rb[c] = pack_bf16x2(o0 - __uint_as_float(ob[c] << 16), o1 - __uint_as_float(ob[c] & 0xffff0000u));
         }
+        const int64_t off = pos_row(g, b, i, j) * g.H * HD + (int64_t)h * HD;
+        // the row: 64 bytes (d = 32) or 32 bytes (d = 16), 32-byte stores
+#pragma unroll
+        for (int c = 0; c < HD / 16; ++c) {
+          asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(O + off + 16 * c), "r"(ob[8 * c]),
+                       "r"(ob[8 * c + 1]), "r"(ob[8 * c + 2]), "r"(ob[8 * c + 3]), "r"(ob[8 * c + 4]),
+                       "r"(ob[8 * c + 5]), "r"(ob[8 * c + 6]), "r"(ob[8 * c + 7])
+                       : "memory");
+          if (Ores)
+            asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(Ores + off + 16 * c),
+                         "r"(rb[8 * c]), "r"(rb[8 * c + 1]), "r"(rb[8 * c + 2]), "r"(rb[8 * c + 3]),
+                         "r"(rb[8 * c + 4]), "r"(rb[8 * c + 5]), "r"(rb[8 * c + 6]), "r"(rb[8 * c + 7])
+                         : "memory");
+        }
+        LSE[(((int64_t)b * g.S + i) * g.H + h) * g.N + j] = lsum > 0.f ? m_ref[s] + __log2f(lsum) * kLn2 : -INFINITY;
       }
     }
     cp_async_wait_all();
+  } else {
+    reg_dealloc<C::REG_OTHER>();  // warps 10, 11 only donate registers
   }
   tc_fence_before();
   __syncthreads();
@@ -558,15 +667,27 @@ cudaError_t launch_fwd_t(const Dims &g, const uint16_t *Q, const uint16_t *K, co
                          const uint16_t *bias, const uint16_t *mask, uint16_t *O, float *LSE, uint16_t *Ores,
                          int *status, cudaStream_t stream) {
   using C = FwdCfg<HD>;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mb;
   cudaError_t e = make_rows_map(&mq, Q, g, 128);
   if (e == cudaSuccess) e = make_rows_map(&mk, K, g, 128);
   if (e == cudaSuccess) e = make_rows_map(&mv, V, g, 128);
   if (e != cudaSuccess) return e;
+  if ((g.N & 7) == 0) {
+    e = make_bias_map(&mb, bias, g.N, g.B * g.H);
+    if (e != cudaSuccess) return e;
+  } else {
+    memset(&mb, 0, sizeof(mb));  // unused: the kernel stages the bias itself
+  }
   static bool attr = false;
   if (!attr) {
     e = cudaFuncSetAttribute(fwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
+    // the setmaxnreg split only balances if the kernel was built with exactly REG_LAUNCH
+    // registers per thread, so refuse to launch otherwise
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, fwd_kernel<HD>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != (int)C::REG_LAUNCH) return cudaErrorInvalidConfiguration;
     attr = true;
   }
   // persistent: one CTA per resident slot, each walking units blockIdx.x, +gridDim.x, ...
@@ -585,7 +706,7 @@ cudaError_t launch_fwd_t(const Dims &g, const uint16_t *Q, const uint16_t *K, co
   }
   const int nunits = g.B * ((g.S + C::GF - 1) / C::GF) * g.H * ((g.N + 127) / 128);
   const int grid = min(nunits, slots[dev]);
-  fwd_kernel<HD><<<grid, C::NTHREADS, C::SMEM_ALLOC, stream>>>(mq, mk, mv, g, bias, mask, O, LSE, Ores, status);
+  fwd_kernel<HD><<<grid, C::NTHREADS, C::SMEM_ALLOC, stream>>>(mq, mk, mv, mb, g, bias, mask, O, LSE, Ores, status);
   return cudaGetLastError();
 }
 

@@ -57,4 +57,20 @@ inline cudaError_t make_square_map(CUtensorMap *m, const void *ptr, int NP, int 
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// 3-D view (k, j, b*H + h) of the BF16 pair bias [B*H, N, N] (N a multiple of 8, so
+// that rows start on 16-byte boundaries); one box is 64 keys x 128 query rows,
+// 128-byte swizzled. Rows and keys past N read as zeros.
+inline cudaError_t make_bias_map(CUtensorMap *m, const void *ptr, int N, int BH) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {2ull * N, 2ull * N * N};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace triattn
