@@ -332,10 +332,20 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
     }
    } else {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // The whole warp walks the schedule converged (every decision is warp-uniform) and
+    // elect.sync picks the lane that issues each MMA and commit.
+    {
       constexpr uint32_t idSS = idesc_f16(128, 128, false, false, false, false);
       constexpr uint32_t idKV = idesc_f16(128, HD, false, false, false, true);
       constexpr uint32_t idQ = idesc_f16(128, HD, false, false, true, true);
+      // descriptor bases: the start-address field is (address >> 4) in the low bits, so an operand
+      // at base + off has descriptor base_desc + (off >> 4) (addresses stay below 256 KB)
+      const uint64_t dK0 = smem_desc(sb0 + C::OFF_K, 16, 8 * C::ROWB, C::SW);
+      const uint64_t dV0 = smem_desc(sb0 + C::OFF_V, 16, 8 * C::ROWB, C::SW);
+      const uint64_t dQ0 = smem_desc(sb0 + C::OFF_Q, 16, 8 * C::ROWB, C::SW);
+      const uint64_t dO0 = smem_desc(sb0 + C::OFF_DO, 16, 8 * C::ROWB, C::SW);
+      const uint64_t dS0 = smem_desc(sb0 + C::OFF_DS, 1024, 2048, kSwizzle128B);
+      constexpr uint64_t KS_ROW = (16 * C::ROWB) >> 4;  // 16 rows of an operand tile, descriptor units
       // per-step bookkeeping, walked in the common schedule
       int bi = 0, jt = 0, il = 0;
       auto advance = [&]() {
@@ -347,27 +357,25 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
           }
         }
       };
-      auto issue_s = [&](int t, int il_, int st) {
-        const uint32_t kA = sb0 + C::OFF_K + il_ * C::TILE, qB = sb0 + C::OFF_Q + st * C::TILE;
+      auto issue_s = [&](int il_, int st) {  // S^T = K_i Q_i^T
+        const uint64_t a = dK0 + (uint64_t)((il_ * C::TILE) >> 4), b = dQ0 + (uint64_t)((st * C::TILE) >> 4);
+        mma_ss_e(tb + C::TA, a, b, idSS, 0u);
 #pragma unroll
-        for (int ks = 0; ks < HD / 16; ++ks)
-          mma_ss(tb + C::TA, smem_desc(kA + ks * 32, 16, 8 * C::ROWB, C::SW),
-                 smem_desc(qB + ks * 32, 16, 8 * C::ROWB, C::SW), idSS, ks > 0 ? 1u : 0u);
-        mma_commit(bar(C::B_SFULL));
+        for (int ks = 1; ks < HD / 16; ++ks) mma_ss_e(tb + C::TA, a + 2 * ks, b + 2 * ks, idSS, 1u);
+        mma_commit_e(bar(C::B_SFULL));
       };
-      auto issue_dp = [&](int il_, int st) {
-        const uint32_t vA = sb0 + C::OFF_V + il_ * C::TILE, oB = sb0 + C::OFF_DO + st * C::TILE;
+      auto issue_dp = [&](int il_, int st) {  // dP^T = V_i dO_i^T
+        const uint64_t a = dV0 + (uint64_t)((il_ * C::TILE) >> 4), b = dO0 + (uint64_t)((st * C::TILE) >> 4);
+        mma_ss_e(tb + C::TB, a, b, idSS, 0u);
 #pragma unroll
-        for (int ks = 0; ks < HD / 16; ++ks)
-          mma_ss(tb + C::TB, smem_desc(vA + ks * 32, 16, 8 * C::ROWB, C::SW),
-                 smem_desc(oB + ks * 32, 16, 8 * C::ROWB, C::SW), idSS, ks > 0 ? 1u : 0u);
-        mma_commit(bar(C::B_DPFULL));
+        for (int ks = 1; ks < HD / 16; ++ks) mma_ss_e(tb + C::TB, a + 2 * ks, b + 2 * ks, idSS, 1u);
+        mma_commit_e(bar(C::B_DPFULL));
       };
-      bool ok = wait_bar(bar(C::B_KVREADY), 0, ab);
-      if (ok) ok = wait_bar(bar(C::B_QDOREADY), 0, ab);
+      bool ok = wait_bar_warp(bar(C::B_KVREADY), 0, ab);
+      if (ok) ok = wait_bar_warp(bar(C::B_QDOREADY), 0, ab);
       if (ok) {
         tc_fence_after();
-        issue_s(0, 0, 0);
+        issue_s(0, 0);
         issue_dp(0, 0);
       }
       for (int t = 0; t < T && ok; ++t) {
@@ -379,64 +387,65 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
         const int st1 = (t + 1) % C::NQS;
         const uint32_t dcol = tb + C::TDKV + cil * 2 * HD;
         // ---- dV += P^T dO as soon as P^T is in region A (A operand: packed FP16 in TMEM)
-        ok = wait_bar(bar(C::B_PAFULL), t & 1, ab);
-        if (ok && cjt == 0 && cil == 0 && cbi > 0) ok = wait_bar(bar(C::B_DKVREAD), (cbi - 1) & 1, ab);
+        ok = wait_bar_warp(bar(C::B_PAFULL), t & 1, ab);
+        if (ok && cjt == 0 && cil == 0 && cbi > 0) ok = wait_bar_warp(bar(C::B_DKVREAD), (cbi - 1) & 1, ab);
         if (!ok) break;
         tc_fence_after();
         {
-          const uint32_t oB = sb0 + C::OFF_DO + st * C::TILE;
+          const uint64_t b = dO0 + (uint64_t)((st * C::TILE) >> 4);
+          // 16 queries per step: column group ks / KPG, packed columns (ks % KPG) * 8
+          mma_ts_e(dcol + HD, tb + C::TA, b, idKV, cjt > 0 ? 1u : 0u);
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks)  // 16 queries per step: column group ks / KPG, packed columns (ks % KPG) * 8
-            mma_ts(dcol + HD, tb + C::TA + (ks / C::KPG) * C::QPT + (ks % C::KPG) * 8,
-                   smem_desc(oB + ks * 16 * C::ROWB, 16, 8 * C::ROWB, C::SW), idKV, (cjt > 0 || ks > 0) ? 1u : 0u);
-          mma_commit(bar(C::B_AFREE));
+          for (int ks = 1; ks < 8; ++ks)
+            mma_ts_e(dcol + HD, tb + C::TA + (ks / C::KPG) * C::QPT + (ks % C::KPG) * 8, b + ks * KS_ROW, idKV, 1u);
+          mma_commit_e(bar(C::B_AFREE));
         }
         // ---- S^T(t+1) once dV has read region A (within a block; a new block needs the new K, V first)
         if (has_next && !next_new_block) {
-          ok = wait_bar(bar(C::B_AFREE), t & 1, ab);
-          if (ok) ok = wait_bar(bar(C::B_QDOREADY + st1), ((t + 1) / C::NQS) & 1, ab);
+          ok = wait_bar_warp(bar(C::B_AFREE), t & 1, ab);
+          if (ok) ok = wait_bar_warp(bar(C::B_QDOREADY + st1), ((t + 1) / C::NQS) & 1, ab);
           if (!ok) break;
           tc_fence_after();
-          issue_s(t + 1, il, st1);
+          issue_s(il, st1);
         }
         // ---- dK += dS^T Q (A: packed FP16 dS^T in region B) and the dQ partial dS K (A: dS tile, MN-major)
-        ok = wait_bar(bar(C::B_PFULL), t & 1, ab);
-        if (ok && t > 0) ok = wait_bar(bar(C::B_DQREAD), (t - 1) & 1, ab);
+        ok = wait_bar_warp(bar(C::B_PFULL), t & 1, ab);
+        if (ok && t > 0) ok = wait_bar_warp(bar(C::B_DQREAD), (t - 1) & 1, ab);
         if (!ok) break;
         tc_fence_after();
         {
-          const uint32_t kA = sb0 + C::OFF_K + cil * C::TILE, qB = sb0 + C::OFF_Q + st * C::TILE;
+          const uint64_t bq = dQ0 + (uint64_t)((st * C::TILE) >> 4), bk = dK0 + (uint64_t)((cil * C::TILE) >> 4);
+          mma_ts_e(dcol, tb + C::TB, bq, idKV, cjt > 0 ? 1u : 0u);
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            mma_ts(dcol, tb + C::TB + (ks / C::KPG) * C::QPT + (ks % C::KPG) * 8,
-                   smem_desc(qB + ks * 16 * C::ROWB, 16, 8 * C::ROWB, C::SW), idKV, (cjt > 0 || ks > 0) ? 1u : 0u);
-          mma_commit(bar(C::B_BFREEM));
+          for (int ks = 1; ks < 8; ++ks)
+            mma_ts_e(dcol, tb + C::TB + (ks / C::KPG) * C::QPT + (ks % C::KPG) * 8, bq + ks * KS_ROW, idKV, 1u);
+          mma_commit_e(bar(C::B_BFREEM));
+          mma_ss_e(tb + C::TDQ, dS0, bk, idQ, 0u);
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            mma_ss(tb + C::TDQ, smem_desc(sb0 + C::OFF_DS + ks * 4096, 1024, 2048, kSwizzle128B),
-                   smem_desc(kA + ks * 16 * C::ROWB, 16, 8 * C::ROWB, C::SW), idQ, ks > 0 ? 1u : 0u);
-          mma_commit(bar(C::B_M2DONE));
-          mma_commit(bar(C::B_QDOFREE + st));
-          if (next_new_block || !has_next) mma_commit(bar(C::B_KVFREE));
+          for (int ks = 1; ks < 8; ++ks) mma_ss_e(tb + C::TDQ, dS0 + ks * (4096 >> 4), bk + ks * KS_ROW, idQ, 1u);
+          mma_commit_e(bar(C::B_M2DONE));
+          mma_commit_e(bar(C::B_QDOFREE + st));
+          if (next_new_block || !has_next) mma_commit_e(bar(C::B_KVFREE));
         }
         if (has_next) {
           if (next_new_block) {
-            ok = wait_bar(bar(C::B_KVREADY), bi & 1, ab);
-            if (ok) ok = wait_bar(bar(C::B_QDOREADY + st1), ((t + 1) / C::NQS) & 1, ab);
-            if (ok) ok = wait_bar(bar(C::B_AFREE), t & 1, ab);
+            ok = wait_bar_warp(bar(C::B_KVREADY), bi & 1, ab);
+            if (ok) ok = wait_bar_warp(bar(C::B_QDOREADY + st1), ((t + 1) / C::NQS) & 1, ab);
+            if (ok) ok = wait_bar_warp(bar(C::B_AFREE), t & 1, ab);
             if (!ok) break;
             tc_fence_after();
-            issue_s(t + 1, il, st1);
+            issue_s(il, st1);
           }
           // ---- dP^T(t+1) once dK has read region B
-          ok = wait_bar(bar(C::B_BFREEM), t & 1, ab);
+          ok = wait_bar_warp(bar(C::B_BFREEM), t & 1, ab);
           if (!ok) break;
           tc_fence_after();
           issue_dp(il, st1);
         }
       }
-      mma_commit(bar(C::B_FINAL));
-      drain_bar(bar(C::B_FINAL), 0);
+      mma_commit_e(bar(C::B_FINAL));
+      if (lane == 0) drain_bar(bar(C::B_FINAL), 0);
+      __syncwarp();
     }
    }
   } else if (warp >= C::WARP_DQ) {
