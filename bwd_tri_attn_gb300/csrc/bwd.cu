@@ -40,13 +40,14 @@
 //             only P and dS are on their path; the most registers (setmaxnreg)
 //   NEW..+3   dQ: read the dQ partial from TMEM (lanes = queries), push it to the owners, reduce owned rows
 //   NEW+4     TMA producer (+ LSE / D rows), NEW+5 MMA issuer and TMEM owner, NEW+6..7 BF16 -> FP16 conversion
-// TMEM columns: A = [0,128) S^T, then FP16 P^T; B = [128,256) dP^T, then FP16 dS^T; dQ partial
-// at 256; dK_i, dV_i from 288. Each elementwise thread writes P^T (dS^T) as packed FP16 over the
-// S^T (dP^T) columns it has just read: column group g of 32 queries keeps its 16 packed columns at
-// A + 32g (B + 32g). dV = P^T dO is issued as soon as the P phase is done, and its completion frees
-// region A for S^T(t+1); dK = dS^T Q follows the dS phase and its completion frees B for dP^T(t+1);
-// dQ = dS K reads dS from a 128-byte-swizzled FP16 tile in shared memory. So the P phase of step
-// t+1 overlaps step t's dK and dQ, and the tensor pipe rarely waits on the elementwise warps.
+// TMEM columns: A = [0,128) S^T, then FP16 P^T; B = [128,256) dP^T, then FP16 dS^T; dK_i, dV_i
+// from 256. Each elementwise thread writes P^T (dS^T) as packed FP16 over the S^T (dP^T) columns
+// it has just read: column group g of 64 queries keeps its 32 packed columns at A + 64g (B + 64g).
+// The dQ partial (128 queries x d, FP32) takes B + [32, 64), which dS^T leaves free. dV = P^T dO
+// is issued as soon as the P phase is done, and its completion frees region A for S^T(t+1);
+// dK = dS^T Q follows the dS phase, and once it has completed and the dQ warps have read dQ(t)
+// out of B, dP^T(t+1) may overwrite B; dQ = dS K reads dS from a 128-byte-swizzled FP16 tile in
+// shared memory. So the P phase of step t+1 overlaps step t's dK and dQ.
 #include "common.cuh"
 #include "sm100.cuh"
 #include "sync.cuh"
@@ -57,7 +58,7 @@ using namespace sm100;
 
 template <int HD>
 struct BwdCfg {
-  static constexpr int GB = HD == 32 ? 3 : 7;  // slices per block: dK/dV of GB slices live in TMEM
+  static constexpr int GB = HD == 32 ? 4 : 8;  // slices per block: dK/dV of GB slices live in TMEM
   static constexpr int NQS = 3;                // Q/dO stages
   static constexpr int ROWB = HD * 2;
   static constexpr int TILE = 128 * ROWB;
@@ -71,7 +72,10 @@ struct BwdCfg {
   static constexpr uint32_t REG_LAUNCH = QPT == 64 ? 128 : 80, REG_EW = QPT == 64 ? 176 : 96,
                             REG_OTHER = QPT == 64 ? 80 : 48;
   static_assert(NEWT * REG_EW + (NTHREADS - NEWT) * REG_OTHER == NTHREADS * REG_LAUNCH, "register split");
-  static constexpr uint32_t TA = 0, TB = 128, TDQ = 256, TDKV = 288, TMEM_COLS = 512;
+  // the dQ partial (32 columns) uses the half of region B that dS^T leaves free: column group 0 of
+  // the elementwise threads keeps its packed dS^T in B + [0,32) and group 1 in B + [64,96)
+  static constexpr uint32_t TA = 0, TB = 128, TDQ = TB + 32, TDKV = 256, TMEM_COLS = 512;
+  static_assert(QPT == 64 && HD <= 32, "dQ partial inside region B");
   static_assert(TDKV + GB * 2 * HD <= TMEM_COLS, "TMEM budget");
   static constexpr int BIAS_TILE = 128 * 128 * 2;
   static constexpr int RB_ROWS = 136;  // >= n * ceil(128 / n) for every cluster size n <= 8
@@ -79,8 +83,8 @@ struct BwdCfg {
   static constexpr int OFF_V = OFF_K + GB * TILE;
   static constexpr int OFF_Q = OFF_V + GB * TILE;
   static constexpr int OFF_DO = OFF_Q + NQS * TILE;
-  static constexpr int OFF_BIAS = OFF_DO + NQS * TILE;     // 2 x [2 halves][128 rows][128 B], SW128
-  static constexpr int OFF_DS = OFF_BIAS + 2 * BIAS_TILE;  // FP16 dS, MN-major SW128: [16 key groups][2][8][128 B]
+  static constexpr int OFF_BIAS = OFF_DO + NQS * TILE;     // [2 halves][128 rows][128 B], SW128
+  static constexpr int OFF_DS = OFF_BIAS + BIAS_TILE;      // FP16 dS, MN-major SW128: [16 key groups][2][8][128 B]
   static constexpr int RB_SLOT = RB_ROWS * HD * 4;
   static constexpr int NRB = 1;                            // dQ receive slots (step t uses slot t % NRB)
   static constexpr int OFF_RB = OFF_DS + 32768;            // dQ receive buffers: NRB x [sender][row][HD] FP32
@@ -90,8 +94,8 @@ struct BwdCfg {
   static constexpr int OFF_BAR = OFF_MASK + GB * 512;
   static constexpr int B_KVFULL = 0, B_KVREADY = 1, B_KVFREE = 2;
   static constexpr int B_QDOFULL = 3, B_QDOREADY = B_QDOFULL + NQS, B_QDOFREE = B_QDOREADY + NQS;
-  static constexpr int B_BFULL = B_QDOFREE + NQS, B_BFREE = B_BFULL + 2;
-  static constexpr int B_SFULL = B_BFREE + 2, B_PAFULL = B_SFULL + 1, B_AFREE = B_PAFULL + 1;
+  static constexpr int B_BFULL = B_QDOFREE + NQS, B_BFREE = B_BFULL + 1;  // the (single) bias tile
+  static constexpr int B_SFULL = B_BFREE + 1, B_PAFULL = B_SFULL + 1, B_AFREE = B_PAFULL + 1;
   static constexpr int B_DPFULL = B_AFREE + 1, B_PFULL = B_DPFULL + 1, B_BFREEM = B_PFULL + 1;
   static constexpr int B_M2DONE = B_BFREEM + 1, B_DQREAD = B_M2DONE + 1;
   static constexpr int B_DKVREAD = B_DQREAD + 1, B_RFULL = B_DKVREAD + 1, B_XEMPTY = B_RFULL + NRB;
@@ -183,10 +187,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
       mbar_init(bar(C::B_QDOREADY + s), C::NCV);
       mbar_init(bar(C::B_QDOFREE + s), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(C::B_BFULL + s), 1);
-      mbar_init(bar(C::B_BFREE + s), C::NEWT);
-    }
+    mbar_init(bar(C::B_BFULL), 1);
+    mbar_init(bar(C::B_BFREE), C::NEWT);
     mbar_init(bar(C::B_SFULL), 1);
     mbar_init(bar(C::B_PAFULL), C::NEWT);
     mbar_init(bar(C::B_AFREE), 1);
@@ -276,17 +278,14 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
             }
             kv_issued = bi + 1;
           }
-          if (il == 0) {  // bias tile of this query-tile group (double-buffered)
-            const int bb = u & 1;
-            if (u >= 2) ok = wait_bar_warp(bar(C::B_BFREE + bb), ((u - 2) >> 1) & 1, ab);
-            if (!ok) break;
+          if (t == 0) {  // the first group's bias tile (the MMA warp loads the later ones)
             if (lane == 0) {
-              const uint32_t dst = sb0 + C::OFF_BIAS + bb * C::BIAS_TILE;
-              mbar_arrive_expect_tx(bar(C::B_BFULL + bb), C::BIAS_TILE);
-              tma_load_3d(dst, &mBT, bar(C::B_BFULL + bb), jt * 128, kt * 128, b * g.H + h);
-              tma_load_3d(dst + 16384, &mBT, bar(C::B_BFULL + bb), jt * 128 + 64, kt * 128, b * g.H + h);
+              const uint32_t dst = sb0 + C::OFF_BIAS;
+              mbar_arrive_expect_tx(bar(C::B_BFULL), C::BIAS_TILE);
+              tma_load_3d(dst, &mBT, bar(C::B_BFULL), jt * 128, kt * 128, b * g.H + h);
+              tma_load_3d(dst + 16384, &mBT, bar(C::B_BFULL), jt * 128 + 64, kt * 128, b * g.H + h);
             }
-            ++u;
+            u = 1;
           }
         }
       }
@@ -294,7 +293,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
     if (!ok && lane == 0) {
       // drain copies still in flight before shared memory goes away
       if (kv_issued > 0) drain_bar(bar(C::B_KVFULL), (kv_issued - 1) & 1);
-      for (int x = max(0, u - 2); x < u; ++x) drain_bar(bar(C::B_BFULL + (x & 1)), (x >> 1) & 1);
+      if (u > 0) drain_bar(bar(C::B_BFULL), 0);
       for (int x = max(0, t - C::NQS); x < t; ++x) drain_bar(bar(C::B_QDOFULL + x % C::NQS), (x / C::NQS) & 1);
     }
    } else if (warp >= C::WARP_CV) {
@@ -371,6 +370,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
         for (int ks = 1; ks < HD / 16; ++ks) mma_ss_e(tb + C::TB, a + 2 * ks, b + 2 * ks, idSS, 1u);
         mma_commit_e(bar(C::B_DPFULL));
       };
+      int ug = 0;  // query-tile groups finished: group ug's bias tile is in the buffer
       bool ok = wait_bar_warp(bar(C::B_KVREADY), 0, ab);
       if (ok) ok = wait_bar_warp(bar(C::B_QDOREADY), 0, ab);
       if (ok) {
@@ -389,6 +389,18 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
         // ---- dV += P^T dO as soon as P^T is in region A (A operand: packed FP16 in TMEM)
         ok = wait_bar_warp(bar(C::B_PAFULL), t & 1, ab);
         if (ok && cjt == 0 && cil == 0 && cbi > 0) ok = wait_bar_warp(bar(C::B_DKVREAD), (cbi - 1) & 1, ab);
+        if (ok && has_next && il == 0) {
+          // the group's last P phase is done: every elementwise thread has released the bias tile
+          // (before PAFULL), so the next group's tile (query tile jt of step t + 1) can be loaded
+          ok = wait_bar_warp(bar(C::B_BFREE), ug & 1, ab);
+          if (ok && lane == 0) {
+            mbar_arrive_expect_tx(bar(C::B_BFULL), C::BIAS_TILE);
+            tma_load_3d(sb0 + C::OFF_BIAS, &mBT, bar(C::B_BFULL), jt * 128, kt * 128, b * g.H + h);
+            tma_load_3d(sb0 + C::OFF_BIAS + 16384, &mBT, bar(C::B_BFULL), jt * 128 + 64, kt * 128, b * g.H + h);
+          }
+          __syncwarp();
+          ++ug;
+        }
         if (!ok) break;
         tc_fence_after();
         {
@@ -436,15 +448,19 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
             tc_fence_after();
             issue_s(il, st1);
           }
-          // ---- dP^T(t+1) once dK has read region B
+          // ---- dP^T(t+1) once dK has read region B and the dQ warps have read dQ(t) out of it
           ok = wait_bar_warp(bar(C::B_BFREEM), t & 1, ab);
+          if (ok) ok = wait_bar_warp(bar(C::B_DQREAD), t & 1, ab);
           if (!ok) break;
           tc_fence_after();
           issue_dp(il, st1);
         }
       }
       mma_commit_e(bar(C::B_FINAL));
-      if (lane == 0) drain_bar(bar(C::B_FINAL), 0);
+      if (lane == 0) {
+        drain_bar(bar(C::B_FINAL), 0);
+        if (!ok && ug > 0) drain_bar(bar(C::B_BFULL), ug & 1);  // a bias load that no one waited for
+      }
       __syncwarp();
     }
    }
@@ -484,8 +500,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
         const int j = prev_jt * 128 + r0 + rl;
         if (j < g.N) {
           const uint2 w = make_uint2(
-              (uint32_t)f32_to_bf16_rn(s4.x * g.scale) | ((uint32_t)f32_to_bf16_rn(s4.y * g.scale) << 16),
-              (uint32_t)f32_to_bf16_rn(s4.z * g.scale) | ((uint32_t)f32_to_bf16_rn(s4.w * g.scale) << 16));
+              pack_bf16x2(s4.x * g.scale, s4.y * g.scale), pack_bf16x2(s4.z * g.scale, s4.w * g.scale));
           *reinterpret_cast<uint2 *>(dQ + pos_row(g, b, prev_i, j) * g.H * HD + h * HD + c * 4) = w;
         }
       }
@@ -558,12 +573,11 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
       const int i0 = sc.block_first(bi), nb = sc.block_size(bi);
       ok = wait_bar_warp(bar(C::B_KVREADY), bi & 1, ab);  // the mask rows of the block are in place
       for (int jt = 0; jt < njt && ok; ++jt) {
-        const int bb = u & 1;
-        ok = wait_bar_warp(bar(C::B_BFULL + bb), (u >> 1) & 1, ab);
+        ok = wait_bar_warp(bar(C::B_BFULL), u & 1, ab);
         if (!ok) break;
 #pragma unroll
         for (int e = 0; e < QPT / 2; ++e) acc[e] = make_float2(0.f, 0.f);
-        const uint32_t brow = sb0 + C::OFF_BIAS + bb * C::BIAS_TILE + hf * 16384 + kl * 128;
+        const uint32_t brow = sb0 + C::OFF_BIAS + hf * 16384 + kl * 128;
         for (int il = 0; il < nb; ++il, ++t) {
           const int st = t % C::NQS;
           // mask*log2e of this key (-inf for masked keys and keys past N: their exponent is -inf, P = +0)
@@ -610,7 +624,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
           }
           if (il == nb - 1) {  // this group's bias tile is no longer read: hand it back to the TMA
             fence_proxy_async_smem();  // order these generic-proxy reads before the async-proxy overwrite
-            mbar_arrive(bar(C::B_BFREE + bb));
+            mbar_arrive(bar(C::B_BFREE));
           }
           if constexpr (QPT == 64) {  // P^T (FP16 pairs) over this thread's S^T columns: the A operand of dV
             tmem_st32(colA, pw);
@@ -707,8 +721,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
           uint32_t w[RC / 2];
 #pragma unroll
           for (int c = 0; c < RC / 2; ++c)
-            w[c] = (uint32_t)f32_to_bf16_rn(__uint_as_float(r[2 * c]) * f) |
-                   ((uint32_t)f32_to_bf16_rn(__uint_as_float(r[2 * c + 1]) * f) << 16);
+            w[c] = pack_bf16x2(__uint_as_float(r[2 * c]) * f, __uint_as_float(r[2 * c + 1]) * f);
           if (kg < g.N) {
             uint16_t *out = outb + pos_row(g, b, i0 + il, kg) * g.H * HD + h * HD + coff;
 #pragma unroll
