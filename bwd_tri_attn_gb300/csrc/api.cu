@@ -13,14 +13,14 @@ cudaError_t launch_fwd(const Dims &g, const uint16_t *Q, const uint16_t *K, cons
 cudaError_t launch_bwd_d(const Dims &g, const uint16_t *dO, const uint16_t *O, const uint16_t *Ores,
                          float *Dout, cudaStream_t stream);
 cudaError_t launch_bias_transpose(const Dims &g, const uint16_t *bias, uint16_t *biasT, cudaStream_t stream);
-cudaError_t launch_bwd_main(const Dims &g, int Gp, const uint16_t *Q, const uint16_t *K, const uint16_t *V,
-                            const uint16_t *biasT, const uint16_t *mask, const float *LSE, const float *Dv,
-                            const uint16_t *dO, uint16_t *dQ, uint16_t *dK, uint16_t *dV, float *partial,
-                            int *status, cudaStream_t stream);
-cudaError_t launch_dbias_reduce_t(const Dims &g, int Gp, const float *partial, uint16_t *dBias,
+cudaError_t launch_bwd_main(const Dims &g, const BwdSplit &sp, const uint16_t *Q, const uint16_t *K,
+                            const uint16_t *V, const uint16_t *biasT, const uint16_t *mask, const float *LSE,
+                            const float *Dv, const uint16_t *dO, uint16_t *dQ, uint16_t *dK, uint16_t *dV,
+                            float *partial, int *status, cudaStream_t stream);
+cudaError_t launch_dbias_reduce_t(const Dims &g, const BwdSplit &sp, const float *partial, uint16_t *dBias,
                                   cudaStream_t stream);
-int bwd_groups(const Dims &g);
-int bwd_groups_active(const Dims &g);
+int bwd_slots_max(const Dims &g);
+BwdSplit bwd_split_active(const Dims &g);
 }  // namespace triattn
 
 using namespace triattn;
@@ -48,11 +48,11 @@ int check_shape(const tri_attn_shape &s) {
 Dims to_dims(const tri_attn_shape &s) { return Dims{s.B, s.S, s.N, s.H, s.d, s.scale}; }
 
 // Backward workspace: the FP32 correction D [B,S,H,N], the transposed and
-// tile-padded BF16 bias [B*H][NP][NP] (NP = N rounded up to 128), and one FP32
-// dBias partial [B*H][NP][NP] per slice supergroup.
+// tile-padded BF16 bias [B*H][NP][NP] (NP = N rounded up to 128), and the FP32
+// dBias partials [B*H][slots][NP][NP]: one slot per cluster that works on a head.
 struct WorkspaceLayout {
   size_t d_off, biast_off, partial_off, total;
-  int groups;
+  int slots;
 };
 
 WorkspaceLayout layout_for(const tri_attn_shape &s) {
@@ -60,11 +60,11 @@ WorkspaceLayout layout_for(const tri_attn_shape &s) {
   const Dims g = to_dims(s);
   const size_t NP = (size_t)(s.N + 127) / 128 * 128;
   const size_t rows = (size_t)s.B * s.S * s.H * s.N;
-  w.groups = bwd_groups(g);
+  w.slots = bwd_slots_max(g);
   w.d_off = 0;
   w.biast_off = align_up(sizeof(float) * rows);
   w.partial_off = w.biast_off + align_up(2 * (size_t)s.B * s.H * NP * NP);
-  w.total = w.partial_off + align_up(sizeof(float) * (size_t)w.groups * s.B * s.H * NP * NP);
+  w.total = w.partial_off + align_up(sizeof(float) * (size_t)w.slots * s.B * s.H * NP * NP);
   return w;
 }
 
@@ -167,11 +167,12 @@ int tri_attn_bwd(tri_attn_shape shape, const tri_attn_bf16 *Q, const tri_attn_bf
   if (e == cudaSuccess) e = mark(0, st);
   if (e == cudaSuccess) e = launch_bwd_d(g, dO, O, Ores, Dv, st);
   if (e == cudaSuccess) e = mark(1, st);
-  const int groups = bwd_groups_active(g);  // <= w.groups, the workspace bound
+  BwdSplit sp = bwd_split_active(g);
+  if (sp.KMAX > w.slots) return TRI_ATTN_ERR_CUDA;  // (cannot happen: the workspace covers every split)
   if (e == cudaSuccess)
-    e = launch_bwd_main(g, groups, Q, K, V, biasT, mask, LSE, Dv, dO, dQ, dK, dV, partial, status, st);
+    e = launch_bwd_main(g, sp, Q, K, V, biasT, mask, LSE, Dv, dO, dQ, dK, dV, partial, status, st);
   if (e == cudaSuccess) e = mark(2, st);
-  if (e == cudaSuccess) e = launch_dbias_reduce_t(g, groups, partial, dBias, st);
+  if (e == cudaSuccess) e = launch_dbias_reduce_t(g, sp, partial, dBias, st);
   if (e == cudaSuccess) e = mark(3, st);
   return cuda_rc(e);
 }

@@ -106,19 +106,6 @@ struct BwdCfg {
   static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 };
 
-// Upper bound on the number of slice supergroups (dBias partials) for a shape:
-// clusters of N/128 CTAs filling at most 152 SMs once, never more than the
-// number of slice blocks. The workspace is sized for this bound.
-inline int bwd_supergroups_max(const Dims &g) {
-  const int nkt = (g.N + 127) / 128;
-  const int gb = g.d == 32 ? BwdCfg<32>::GB : BwdCfg<16>::GB;
-  const int blocks = (g.S + gb - 1) / gb;
-  int gp = 152 / (nkt * g.B * g.H);
-  if (gp < 1) gp = 1;
-  if (gp > blocks) gp = blocks;
-  return gp;
-}
-
 __device__ __forceinline__ bool wait_bar_cluster_warp(uint32_t bar, uint32_t parity, const Abort &ab) {
   const bool ok = wait_bar_cluster(bar, parity, ab);
   return __all_sync(0xffffffffu, ok);
@@ -138,25 +125,65 @@ __device__ __forceinline__ void convert_to_f16(uint8_t *p, int bytes, int tid, i
 }
 
 
-// The step schedule every role walks in the same order: blocks of GB slices of
-// the supergroup [s0, s1), then query tiles, then the slices of the block.
-// The first block holds f <= GB slices, f set per cluster so that clusters reach
-// their dBias flushes (one per block and query tile) at different steps.
+// Work split: the B*H*S (head, slice) pairs, ordered head-major (unit x = head * S + slice,
+// head = b * H + h), are cut into NC contiguous ranges, one per cluster: cluster c takes
+// [bwd_unit_start(c), bwd_unit_start(c + 1)). NC is as many clusters as the device runs at once,
+// so every resident cluster has about the same work. A range may cross head boundaries.
+__host__ __device__ inline int bwd_unit_start(int c, int NC, int64_t W) { return (int)((int64_t)c * W / NC); }
+// The cluster whose range holds unit x.
+__host__ __device__ inline int bwd_cluster_of(int64_t x, int NC, int64_t W) {
+  int c = (int)(x * NC / W);
+  while (c + 1 < NC && bwd_unit_start(c + 1, NC, W) <= x) ++c;
+  while (c > 0 && bwd_unit_start(c, NC, W) > x) --c;
+  return c;
+}
+
+// The step schedule every role walks in the same order: the CTA's range is cut at head boundaries
+// into segments, each segment into blocks of GB slices (the first block of a segment holds f <= GB
+// slices, f set per cluster so that clusters reach their dBias flushes at different steps), each
+// block into steps: query tiles, then the slices of the block.
 struct Sched {
-  int s0, s1, njt, GB, f;
-  __device__ int nblk() const {
-    const int n = s1 - s0;
-    return n <= 0 ? 0 : (n <= f ? 1 : 1 + (n - f + GB - 1) / GB);
+  int beg, end, S, GB, f;
+  __device__ static int seg_blocks(int len, int f, int GB) {
+    return len <= 0 ? 0 : (len <= f ? 1 : 1 + (len - f + GB - 1) / GB);
   }
-  __device__ int block_first(int bi) const { return bi == 0 ? s0 : s0 + f + (bi - 1) * GB; }
-  __device__ int block_size(int bi) const { return min(bi == 0 ? f : GB, s1 - block_first(bi)); }
+  __device__ int nblk() const {
+    int n = 0;
+    for (int x = beg; x < end;) {
+      const int e = min(end, (x / S + 1) * S);
+      n += seg_blocks(e - x, f, GB);
+      x = e;
+    }
+    return n;
+  }
+  // block bi: head, first slice, number of slices, and whether it opens its segment
+  __device__ void block(int bi, int &hd, int &i0, int &nb, bool &first) const {
+    for (int x = beg; x < end;) {
+      const int hx = x / S, e = min(end, (hx + 1) * S), n = seg_blocks(e - x, f, GB);
+      if (bi < n) {
+        const int off = bi == 0 ? 0 : f + (bi - 1) * GB;
+        hd = hx;
+        i0 = x - hx * S + off;
+        nb = min(bi == 0 ? f : GB, e - x - off);
+        first = bi == 0;
+        return;
+      }
+      bi -= n;
+      x = e;
+    }
+    hd = 0;
+    i0 = 0;
+    nb = 0;
+    first = true;
+  }
 };
 
 template <int HD>
 __global__ void __launch_bounds__(BwdCfg<HD>::NTHREADS, 1)
 bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
            const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mDO,
-           const __grid_constant__ CUtensorMap mBT, const Dims g, const int Gp, const float *__restrict__ LSE,
+           const __grid_constant__ CUtensorMap mBT, const Dims g, const int NC, const int KMAX,
+           const float *__restrict__ LSE,
            const float *__restrict__ Dv, const uint16_t *__restrict__ mask, uint16_t *__restrict__ dQ,
            uint16_t *__restrict__ dK, uint16_t *__restrict__ dV, float *__restrict__ partial, int *status) {
   using C = BwdCfg<HD>;
@@ -165,13 +192,12 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
   const uint32_t sb0 = smem_u32(sm);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nkt = (g.N + 127) / 128, njt = nkt;
-  const int kt = blockIdx.x, h = blockIdx.y;
-  const int b = blockIdx.z / Gp, grp = blockIdx.z % Gp;
-  const uint32_t rank = cluster_ctarank();  // == kt (the cluster spans the key tiles)
-  const Sched sc{(int)((int64_t)grp * g.S / Gp), (int)((int64_t)(grp + 1) * g.S / Gp), njt, C::GB,
-                 C::GB - (int)((blockIdx.y + gridDim.y * blockIdx.z) % C::GB)};
+  const int kt = blockIdx.x, cl = blockIdx.y;  // key tile = cluster rank, cluster index
+  const uint32_t rank = cluster_ctarank();     // == kt (the cluster spans the key tiles)
+  const int64_t W = (int64_t)g.B * g.H * g.S;
+  const Sched sc{bwd_unit_start(cl, NC, W), bwd_unit_start(cl + 1, NC, W), g.S, C::GB, C::GB - cl % C::GB};
   const int nblk = sc.nblk();
-  const int T = njt * (sc.s1 - sc.s0);  // steps of this CTA
+  const int T = njt * (sc.end - sc.beg);  // steps of this CTA
   auto bar = [&](int k) { return sb0 + C::OFF_BAR + 8u * (uint32_t)k; };
   volatile uint32_t *misc = reinterpret_cast<volatile uint32_t *>(sm + C::OFF_MISC);
   const Abort ab{reinterpret_cast<volatile int *>(misc + 1), status};
@@ -232,7 +258,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
       tma_prefetch_map(&mBT);
     }
     for (int bi = 0; bi < nblk && ok; ++bi) {
-      const int i0 = sc.block_first(bi), nb = sc.block_size(bi);
+      int hd, i0, nb;
+      bool first;
+      sc.block(bi, hd, i0, nb, first);
+      const int b = hd / g.H, h = hd % g.H;
       for (int jt = 0; jt < njt && ok; ++jt) {
         for (int il = 0; il < nb; ++il, ++t) {
           const int st = t % C::NQS, i = i0 + il;
@@ -302,7 +331,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
     bool ok = true;
     int t = 0;
     for (int bi = 0; bi < nblk && ok; ++bi) {
-      const int i0 = sc.block_first(bi), nb = sc.block_size(bi);
+      int hd, i0, nb;
+      bool first;
+      sc.block(bi, hd, i0, nb, first);
+      const int b = hd / g.H;
       ok = wait_bar_warp(bar(C::B_KVFULL), bi & 1, ab);
       if (!ok) break;
       convert_to_f16(sm + C::OFF_K, nb * C::TILE, ct, C::NCVT);
@@ -346,13 +378,21 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
       const uint64_t dS0 = smem_desc(sb0 + C::OFF_DS, 1024, 2048, kSwizzle128B);
       constexpr uint64_t KS_ROW = (16 * C::ROWB) >> 4;  // 16 rows of an operand tile, descriptor units
       // per-step bookkeeping, walked in the common schedule
-      int bi = 0, jt = 0, il = 0;
+      int bi = 0, jt = 0, il = 0, hd = 0, nb = 0;
+      {
+        int i0;
+        bool first;
+        sc.block(0, hd, i0, nb, first);
+      }
       auto advance = [&]() {
-        if (++il == sc.block_size(bi)) {
+        if (++il == nb) {
           il = 0;
           if (++jt == njt) {
             jt = 0;
             ++bi;
+            int i0;
+            bool first;
+            sc.block(bi, hd, i0, nb, first);
           }
         }
       };
@@ -395,8 +435,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
           ok = wait_bar_warp(bar(C::B_BFREE), ug & 1, ab);
           if (ok && lane == 0) {
             mbar_arrive_expect_tx(bar(C::B_BFULL), C::BIAS_TILE);
-            tma_load_3d(sb0 + C::OFF_BIAS, &mBT, bar(C::B_BFULL), jt * 128, kt * 128, b * g.H + h);
-            tma_load_3d(sb0 + C::OFF_BIAS + 16384, &mBT, bar(C::B_BFULL), jt * 128 + 64, kt * 128, b * g.H + h);
+            tma_load_3d(sb0 + C::OFF_BIAS, &mBT, bar(C::B_BFULL), jt * 128, kt * 128, hd);
+            tma_load_3d(sb0 + C::OFF_BIAS + 16384, &mBT, bar(C::B_BFULL), jt * 128 + 64, kt * 128, hd);
           }
           __syncwarp();
           ++ug;
@@ -479,7 +519,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
     const uint32_t rbar0 = mapa_shared(bar(C::B_RFULL), o);
     if (dt == 0)  // arm every slot for its first step
       for (int s = 0; s < C::NRB && s < T; ++s) mbar_arrive_expect_tx(bar(C::B_RFULL + s), rb_bytes);
-    int prev_i = 0, prev_jt = 0, red = 0;
+    int prev_i = 0, prev_jt = 0, prev_hd = 0, red = 0;
     auto reduce_prev = [&]() -> bool {
       const int slot = red % C::NRB;
       if (!wait_bar_cluster_warp(bar(C::B_RFULL + slot), (red / C::NRB) & 1, ab)) return false;
@@ -501,7 +541,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
         if (j < g.N) {
           const uint2 w = make_uint2(
               pack_bf16x2(s4.x * g.scale, s4.y * g.scale), pack_bf16x2(s4.z * g.scale, s4.w * g.scale));
-          *reinterpret_cast<uint2 *>(dQ + pos_row(g, b, prev_i, j) * g.H * HD + h * HD + c * 4) = w;
+          *reinterpret_cast<uint2 *>(dQ + pos_row(g, prev_hd / g.H, prev_i, j) * g.H * HD + (prev_hd % g.H) * HD +
+                                     c * 4) = w;
         }
       }
       __syncwarp();
@@ -513,7 +554,9 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
     bool ok = true;
     int t = 0;
     for (int bi = 0; bi < nblk && ok; ++bi) {
-      const int i0 = sc.block_first(bi), nb = sc.block_size(bi);
+      int hd, i0, nb;
+      bool first;
+      sc.block(bi, hd, i0, nb, first);
       for (int jt = 0; jt < njt && ok; ++jt)
         for (int il = 0; il < nb; ++il, ++t) {
           if (t > 0) {
@@ -544,6 +587,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
           }
           prev_i = i0 + il;
           prev_jt = jt;
+          prev_hd = hd;
         }
     }
     if (ok && red < T) ok = reduce_prev();  // the last step's rows
@@ -565,12 +609,15 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
     bool ok = true;
     int t = 0, u = 0;
     float2 acc[QPT / 2];  // dBias tile row: queries cg*QPT + [0,QPT) as pairs
-    // offset of this CTA's partial tile (kt, jt): [supergroup][b][h][kt][jt][128 x 128]
-    auto ptile = [&](int jt_) -> int64_t {
-      return (((((int64_t)grp * g.B + b) * g.H + h) * nkt + kt) * njt + jt_) * 16384;
-    };
     for (int bi = 0; bi < nblk && ok; ++bi) {
-      const int i0 = sc.block_first(bi), nb = sc.block_size(bi);
+      int hd, i0, nb;
+      bool first;  // the block opens its head's segment: the partial tiles start from zero
+      sc.block(bi, hd, i0, nb, first);
+      const int b = hd / g.H, h = hd % g.H;
+      // this cluster's dBias partial slot for head hd: slot k = cl - (first cluster of the head),
+      // tiles [head][slot][kt][jt][128 x 128]
+      const int64_t pslot = ((int64_t)hd * KMAX + (cl - bwd_cluster_of((int64_t)hd * g.S, NC, W))) * nkt * njt;
+      auto ptile = [&](int jt_) -> int64_t { return (pslot + (int64_t)kt * njt + jt_) * 16384; };
       ok = wait_bar_warp(bar(C::B_KVREADY), bi & 1, ab);  // the mask rows of the block are in place
       for (int jt = 0; jt < njt && ok; ++jt) {
         ok = wait_bar_warp(bar(C::B_BFULL), u & 1, ab);
@@ -586,7 +633,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
           const float2 mk2 = make_float2(mk, mk);
           const float *sl = reinterpret_cast<const float *>(sm + C::OFF_LSE + st * 512) + cg * QPT;
           const float *sd = reinterpret_cast<const float *>(sm + C::OFF_D + st * 512) + cg * QPT;
-          if (il == nb - 1 && bi > 0)  // the warp's QPT/8 KB of the dBias partial tile into L2 ahead of the flush
+          if (il == nb - 1 && !first)  // the warp's QPT/8 KB of the dBias partial tile into L2 ahead of the flush
 #pragma unroll
             for (int r = 0; r < QPT / 32; ++r) {
               const int li = lane + 32 * r;  // 128-byte line li of the warp's chunks
@@ -668,7 +715,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
           mbar_arrive(bar(C::B_PFULL));
         }
         if (!ok) break;
-        // ---- dBias tile (jt, kt) of this block into the supergroup partial (FP32, owned by this CTA).
+        // ---- dBias tile (jt, kt) of this block into the cluster's partial slot (FP32, owned by this CTA).
         // Tile layout [query half][chunk c of 8 queries][key][8 queries]: lane-consecutive keys make
         // every warp access one contiguous kilobyte.
         if (kg < g.N) {
@@ -676,7 +723,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
           uint32_t w[QPT / 8][8];  // all the 32-byte loads in flight at once, then add and store
 #pragma unroll
           for (int m = 0; m < QPT / 8; ++m) {
-            if (bi > 0) {
+            if (!first) {
               ld_keep_v8(pp + 1024 * m, w[m]);
             } else {
 #pragma unroll
@@ -759,22 +806,24 @@ __global__ void bias_transpose_kernel(const uint16_t *__restrict__ bias, uint16_
   }
 }
 
-// dBias[bh][j][k] = BF16(sum over g = 0..Gp-1, in order, of the partials). Each partial holds,
-// per bh, tiles [kt][jt] of 128 keys x 128 queries laid out [query half][chunk c][key][8 queries].
+// dBias[bh][j][k] = BF16(sum, in cluster order, of the partials of head bh): the clusters whose
+// ranges hold slices of head bh wrote slots 0, 1, ... of the head. Each slot holds tiles [kt][jt] of
+// 128 keys x 128 queries laid out [query half][chunk c][key][8 queries].
 // One CTA (256 threads) reduces one [128 keys x 8 queries] chunk and writes its 8 output rows.
-__global__ void dbias_reduce_t_kernel(const float *__restrict__ partial, int Gp, int BH, int N, int NP,
-                                      uint16_t *__restrict__ dBias) {
+__global__ void dbias_reduce_t_kernel(const float *__restrict__ partial, int NC, int KMAX, int S, int64_t W, int N,
+                                      int NP, uint16_t *__restrict__ dBias) {
   __shared__ float s[8][129];
   const int nt = NP / 128, tile = blockIdx.x, kt = tile / nt, jt = tile % nt;
   const int hc = blockIdx.y, bh = blockIdx.z, tid = threadIdx.x;
-  const int64_t gstride4 = (int64_t)BH * NP * NP / 4;
+  const int nslots = bwd_cluster_of((int64_t)bh * S + S - 1, NC, W) - bwd_cluster_of((int64_t)bh * S, NC, W) + 1;
+  const int64_t sstride4 = (int64_t)nt * nt * 16384 / 4;
   const int kl = tid >> 1, e0 = (tid & 1) * 4;
   if (kt * 128 + kl < N) {
-    const float4 *p =
-        reinterpret_cast<const float4 *>(partial + ((int64_t)bh * nt * nt + tile) * 16384 + (hc * 128 + kl) * 8 + e0);
+    const float4 *p = reinterpret_cast<const float4 *>(partial + ((int64_t)bh * KMAX * nt * nt + tile) * 16384 +
+                                                       (hc * 128 + kl) * 8 + e0);
     float4 a = __ldcs(p);
-    for (int gi = 1; gi < Gp; ++gi) {
-      const float4 v = __ldcs(p + gi * gstride4);
+    for (int gi = 1; gi < nslots; ++gi) {
+      const float4 v = __ldcs(p + gi * sstride4);
       a.x += v.x;
       a.y += v.y;
       a.z += v.z;
@@ -802,16 +851,18 @@ cudaError_t launch_bias_transpose(const Dims &g, const uint16_t *bias, uint16_t 
   return cudaGetLastError();
 }
 
-cudaError_t launch_dbias_reduce_t(const Dims &g, int Gp, const float *partial, uint16_t *dBias, cudaStream_t stream) {
+cudaError_t launch_dbias_reduce_t(const Dims &g, const BwdSplit &sp, const float *partial, uint16_t *dBias,
+                                  cudaStream_t stream) {
   const int NP = (g.N + 127) / 128 * 128;
   const int nt = NP / 128;
   dim3 grid(nt * nt, 16, g.B * g.H);
-  dbias_reduce_t_kernel<<<grid, 256, 0, stream>>>(partial, Gp, g.B * g.H, g.N, NP, dBias);
+  dbias_reduce_t_kernel<<<grid, 256, 0, stream>>>(partial, sp.NC, sp.KMAX, g.S, (int64_t)g.B * g.H * g.S, g.N, NP,
+                                                  dBias);
   return cudaGetLastError();
 }
 
 template <int HD>
-cudaError_t launch_bwd_main_t(const Dims &g, int Gp, const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+cudaError_t launch_bwd_main_t(const Dims &g, const BwdSplit &sp, const uint16_t *Q, const uint16_t *K, const uint16_t *V,
                               const uint16_t *biasT, const uint16_t *mask, const float *LSE, const float *Dv,
                               const uint16_t *dO, uint16_t *dQ, uint16_t *dK, uint16_t *dV, float *partial,
                               int *status, cudaStream_t stream) {
@@ -838,7 +889,7 @@ cudaError_t launch_bwd_main_t(const Dims &g, int Gp, const uint16_t *Q, const ui
     attr = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(nkt, g.H, g.B * Gp);
+  cfg.gridDim = dim3(nkt, sp.NC, 1);
   cfg.blockDim = dim3(C::NTHREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_ALLOC;
   cfg.stream = stream;
@@ -849,26 +900,56 @@ cudaError_t launch_bwd_main_t(const Dims &g, int Gp, const uint16_t *Q, const ui
   attrs[0].val.clusterDim.z = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, bwd_kernel<HD>, mq, mk, mv, mdo, mbt, g, Gp, LSE, Dv, mask, dQ, dK, dV, partial,
-                            status);
+  return cudaLaunchKernelEx(&cfg, bwd_kernel<HD>, mq, mk, mv, mdo, mbt, g, sp.NC, sp.KMAX, LSE, Dv, mask, dQ, dK, dV,
+                            partial, status);
 }
 
-cudaError_t launch_bwd_main(const Dims &g, int Gp, const uint16_t *Q, const uint16_t *K, const uint16_t *V,
-                            const uint16_t *biasT, const uint16_t *mask, const float *LSE, const float *Dv,
-                            const uint16_t *dO, uint16_t *dQ, uint16_t *dK, uint16_t *dV, float *partial,
-                            int *status, cudaStream_t stream) {
+cudaError_t launch_bwd_main(const Dims &g, const BwdSplit &sp, const uint16_t *Q, const uint16_t *K,
+                            const uint16_t *V, const uint16_t *biasT, const uint16_t *mask, const float *LSE,
+                            const float *Dv, const uint16_t *dO, uint16_t *dQ, uint16_t *dK, uint16_t *dV,
+                            float *partial, int *status, cudaStream_t stream) {
   if (g.d == 32)
-    return launch_bwd_main_t<32>(g, Gp, Q, K, V, biasT, mask, LSE, Dv, dO, dQ, dK, dV, partial, status, stream);
-  return launch_bwd_main_t<16>(g, Gp, Q, K, V, biasT, mask, LSE, Dv, dO, dQ, dK, dV, partial, status, stream);
+    return launch_bwd_main_t<32>(g, sp, Q, K, V, biasT, mask, LSE, Dv, dO, dQ, dK, dV, partial, status, stream);
+  return launch_bwd_main_t<16>(g, sp, Q, K, V, biasT, mask, LSE, Dv, dO, dQ, dK, dV, partial, status, stream);
 }
 
-int bwd_groups(const Dims &g) { return bwd_supergroups_max(g); }
+// Most clusters a shape is split over: one per 152 / nkt SMs of a GB300, never more than the
+// number of (head, slice) pairs (so that every cluster has at least one slice).
+int bwd_clusters_max(const Dims &g) {
+  const int nkt = (g.N + 127) / 128;
+  const int64_t W = (int64_t)g.B * g.H * g.S;
+  int n = 152 / nkt;
+  if (n < 1) n = 1;
+  return (int)(W < n ? W : n);
+}
 
-// Supergroups actually launched: as many (b, h, supergroup) clusters as the
-// device runs at once (one wave), within the workspace bound. Depends only on
-// the shape and the GPU model, so repeated calls reduce in the same order.
+// dBias partial slots one head needs when the work is split over NC clusters: the most clusters
+// whose ranges hold slices of one head. Only heads that contain a range boundary can reach more
+// than one, so it suffices to look at those.
+int bwd_slots_for(const Dims &g, int NC) {
+  const int64_t W = (int64_t)g.B * g.H * g.S;
+  int k = 1;
+  for (int c = 1; c < NC; ++c) {
+    const int64_t hd = bwd_unit_start(c, NC, W) / g.S;
+    const int n = bwd_cluster_of(hd * g.S + g.S - 1, NC, W) - bwd_cluster_of(hd * g.S, NC, W) + 1;
+    if (n > k) k = n;
+  }
+  return k;
+}
+
+// Slots per head the workspace holds: enough for any split over at most bwd_clusters_max clusters.
+int bwd_slots_max(const Dims &g) {
+  int k = 1;
+  for (int nc = 1; nc <= bwd_clusters_max(g); ++nc) {
+    const int s = bwd_slots_for(g, nc);
+    if (s > k) k = s;
+  }
+  return k;
+}
+
+// Clusters of nkt CTAs the device runs at once for this kernel (cached per device).
 template <int HD>
-int bwd_groups_active_t(const Dims &g) {
+int bwd_resident_clusters_t(const Dims &g) {
   using C = BwdCfg<HD>;
   static int cache[65][9];  // [device][cluster size]
   const int nkt = (g.N + 127) / 128;
@@ -893,12 +974,19 @@ int bwd_groups_active_t(const Dims &g) {
     if (cudaOccupancyMaxActiveClusters(&n, bwd_kernel<HD>, &cfg) != cudaSuccess || n < 1) n = 1;
     cache[dev][nkt] = n;
   }
-  int gp = n / (g.B * g.H);
-  if (gp < 1) gp = 1;
-  const int gmax = bwd_supergroups_max(g);
-  return gp < gmax ? gp : gmax;
+  return n;
 }
 
-int bwd_groups_active(const Dims &g) { return g.d == 32 ? bwd_groups_active_t<32>(g) : bwd_groups_active_t<16>(g); }
+// The split a call uses: as many clusters as the device runs at once (one wave), within the
+// workspace bound. Depends only on the shape and the device, so repeated calls reduce in the
+// same order.
+BwdSplit bwd_split_active(const Dims &g) {
+  const int n = g.d == 32 ? bwd_resident_clusters_t<32>(g) : bwd_resident_clusters_t<16>(g);
+  const int cmax = bwd_clusters_max(g);
+  BwdSplit sp;
+  sp.NC = n < cmax ? n : cmax;
+  sp.KMAX = bwd_slots_for(g, sp.NC);
+  return sp;
+}
 
 }  // namespace triattn

@@ -10,13 +10,14 @@ namespace triattn {
 cudaError_t launch_bwd_d(const Dims &g, const uint16_t *dO, const uint16_t *O, const uint16_t *Ores,
                          float *Dout, cudaStream_t stream);
 cudaError_t launch_bias_transpose(const Dims &g, const uint16_t *bias, uint16_t *biasT, cudaStream_t stream);
-cudaError_t launch_bwd_main(const Dims &g, int Gp, const uint16_t *Q, const uint16_t *K, const uint16_t *V,
-                            const uint16_t *biasT, const uint16_t *mask, const float *LSE, const float *Dv,
-                            const uint16_t *dO, uint16_t *dQ, uint16_t *dK, uint16_t *dV, float *partial,
-                            int *status, cudaStream_t stream);
-cudaError_t launch_dbias_reduce_t(const Dims &g, int Gp, const float *partial, uint16_t *dBias,
+cudaError_t launch_bwd_main(const Dims &g, const BwdSplit &sp, const uint16_t *Q, const uint16_t *K,
+                            const uint16_t *V, const uint16_t *biasT, const uint16_t *mask, const float *LSE,
+                            const float *Dv, const uint16_t *dO, uint16_t *dQ, uint16_t *dK, uint16_t *dV,
+                            float *partial, int *status, cudaStream_t stream);
+cudaError_t launch_dbias_reduce_t(const Dims &g, const BwdSplit &sp, const float *partial, uint16_t *dBias,
                                   cudaStream_t stream);
-int bwd_groups_active(const Dims &g);
+int bwd_slots_for(const Dims &g, int NC);
+BwdSplit bwd_split_active(const Dims &g);
 int *device_status_word();
 }  // namespace triattn
 
@@ -62,7 +63,7 @@ extern "C" int tri_attn_bwd_static(tri_attn_shape s, const tri_attn_bf16 *Q, con
   for (const void *p : ptrs)
     if (p && !aligned16(p)) return TRI_ATTN_ERR_UNSUPPORTED;
 
-  // scratch layout: D [B,S,H,N] FP32 | transposed bias [B*H][NP][NP] BF16 | Gp dBias partials [B*H][NP][NP] FP32
+  // scratch layout: D [B,S,H,N] FP32 | transposed bias [B*H][NP][NP] BF16 | dBias partials [B*H][slots][NP][NP] FP32
   const Dims g{s.B, s.S, s.N, s.H, s.d, s.scale};
   const size_t NP = (size_t)(s.N + 127) / 128 * 128;
   const size_t d_bytes = align_up(sizeof(float) * (size_t)s.B * s.S * s.H * s.N);
@@ -70,9 +71,11 @@ extern "C" int tri_attn_bwd_static(tri_attn_shape s, const tri_attn_bf16 *Q, con
   const size_t one_partial = sizeof(float) * (size_t)s.B * s.H * NP * NP;
   const size_t cap = TRI_ATTN_STATIC_WORKSPACE_BYTES;
   if (d_bytes + bt_bytes + one_partial > cap) return TRI_ATTN_ERR_STATIC_TOO_SMALL;
-  const size_t fit = (cap - d_bytes - bt_bytes) / one_partial;
-  int groups = bwd_groups_active(g);
-  if ((size_t)groups > fit) groups = (int)fit;
+  const size_t fit = (cap - d_bytes - bt_bytes) / one_partial;  // partial slots per head that fit
+  // the device's split, with fewer clusters if a head would need more slots than fit
+  BwdSplit sp = bwd_split_active(g);
+  while (sp.NC > 1 && (size_t)sp.KMAX > fit) sp.KMAX = bwd_slots_for(g, --sp.NC);
+  if ((size_t)sp.KMAX > fit) return TRI_ATTN_ERR_STATIC_TOO_SMALL;
 
   unsigned char *ws = static_scratch();
   int *status = device_status_word();
@@ -84,7 +87,7 @@ extern "C" int tri_attn_bwd_static(tri_attn_shape s, const tri_attn_bf16 *Q, con
   cudaError_t e = launch_bias_transpose(g, bias, biasT, st);
   if (e == cudaSuccess) e = launch_bwd_d(g, dO, O, Ores, Dv, st);
   if (e == cudaSuccess)
-    e = launch_bwd_main(g, groups, Q, K, V, biasT, mask, LSE, Dv, dO, dQ, dK, dV, partial, status, st);
-  if (e == cudaSuccess) e = launch_dbias_reduce_t(g, groups, partial, dBias, st);
+    e = launch_bwd_main(g, sp, Q, K, V, biasT, mask, LSE, Dv, dO, dQ, dK, dV, partial, status, st);
+  if (e == cudaSuccess) e = launch_dbias_reduce_t(g, sp, partial, dBias, st);
   return e == cudaSuccess ? TRI_ATTN_OK : TRI_ATTN_ERR_CUDA;
 }

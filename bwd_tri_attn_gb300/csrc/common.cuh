@@ -41,6 +41,12 @@ __device__ __forceinline__ float ex2(float x) {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+// How the backward spreads its work: NC clusters (one per resident cluster slot of the device),
+// and KMAX dBias partial slots per head in the workspace.
+struct BwdSplit {
+  int NC, KMAX;
+};
+
 // Device status codes written by bounded waits (host reads them lazily).
 constexpr int kStatusTimeout = 1;
 
