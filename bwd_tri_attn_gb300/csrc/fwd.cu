@@ -53,7 +53,8 @@ using namespace sm100;
 template <int HD>
 struct FwdCfg {
   static constexpr int GF = HD == 32 ? 4 : 8;  // slices per CTA
-  static constexpr int NSB = 3;                // S buffers in TMEM = K/V pipeline stages: tile tg uses slot tg % 3
+  static constexpr int NSB = 3;                // S buffers in TMEM: tile tg uses buffer tg % 3
+  static constexpr int NST = 6;                // K/V pipeline stages: tile tg uses stage tg % 6
   static constexpr int ROWB = HD * 2;          // bytes of one operand row
   static constexpr int TILE = 128 * ROWB;      // bytes of one 128-row operand tile
   static constexpr uint32_t SW = HD == 32 ? kSwizzle64B : kSwizzle32B;
@@ -62,17 +63,18 @@ struct FwdCfg {
   static constexpr int BTILE = 128 * 256;                   // BF16 bias tile: [2 halves][128 rows][128 B], SW128
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + GF * TILE;
-  static constexpr int OFF_V = OFF_K + NSB * TILE;
-  static constexpr int OFF_BS = OFF_V + NSB * TILE;         // 2 bias tiles (double-buffered by key tile)
+  static constexpr int OFF_V = OFF_K + NST * TILE;
+  static constexpr int OFF_BS = OFF_V + NST * TILE;         // 2 bias tiles (double-buffered by key tile)
   static constexpr int OFF_MASK = OFF_BS + 2 * BTILE;       // 2 x BF16 mask rows [GF][NMAX] (by unit)
   static constexpr int OFF_FLAG = OFF_MASK + 2 * GF * NMAX * 2;  // 2 x int [GF][MAXKT]: tile has a nonzero mask entry
   static constexpr int OFF_BAR = OFF_FLAG + 2 * GF * MAXKT * 4;
   // barrier indices
   static constexpr int B_Q = 0;
   static constexpr int B_KVFULL = 1;
-  static constexpr int B_SFULL = B_KVFULL + NSB;
+  static constexpr int B_KVEMPTY = B_KVFULL + NST;  // the stage's P.V has completed
+  static constexpr int B_SFULL = B_KVEMPTY + NST;
   static constexpr int B_PFULL = B_SFULL + NSB;  // P written and this tile's V converted
-  static constexpr int B_TDONE = B_PFULL + NSB;  // the slot's P.V has completed: S buffer and K/V stage free
+  static constexpr int B_TDONE = B_PFULL + NSB;  // the buffer's P.V has completed: the S buffer is free
   static constexpr int B_OFINAL = B_TDONE + NSB;
   static constexpr int B_OFREE = B_OFINAL + 1;  // softmax warps have read O of the unit out of TMEM
   static constexpr int B_QFREE = B_OFREE + 1;   // the unit's last S MMA has read Q
@@ -140,8 +142,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
 
   if (tid == 0) {
     mbar_init(bar(C::B_Q), 1);
-    for (int s = 0; s < C::NSB; ++s) {
+    for (int s = 0; s < C::NST; ++s) {
       mbar_init(bar(C::B_KVFULL + s), 1);
+      mbar_init(bar(C::B_KVEMPTY + s), 1);
+    }
+    for (int s = 0; s < C::NSB; ++s) {
       mbar_init(bar(C::B_SFULL + s), 1);
       mbar_init(bar(C::B_PFULL + s), 128);  // the warpgroup that owns the tile
       mbar_init(bar(C::B_TDONE + s), 1);
@@ -254,8 +259,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
           }
           ++kb;
         }
-        const int st = tg % C::NSB, use = tg / C::NSB;
-        if (use > 0) ok = wait_bar_warp(bar(C::B_TDONE + st), (use - 1) & 1, ab);
+        const int st = tg % C::NST, use = tg / C::NST;
+        if (use > 0) ok = wait_bar_warp(bar(C::B_KVEMPTY + st), (use - 1) & 1, ab);
         if (!ok) break;
         if (lane == 0) {
           const int kt = t / w.ng, il = t % w.ng;
@@ -272,7 +277,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
       if (k > 0) drain_bar(bar(C::B_Q), (k - 1) & 1);
       if (mask && tma_bias && k > 0) drain_bar(bar(C::B_MFULL + ((k - 1) & 1)), ((k - 1) >> 1) & 1);
       for (int x = max(0, kb - 2); x < kb; ++x) drain_bar(bar(C::B_BFULL + (x & 1)), (x >> 1) & 1);
-      for (int t = max(0, tg - C::NSB); t < tg; ++t) drain_bar(bar(C::B_KVFULL + t % C::NSB), (t / C::NSB) & 1);
+      for (int t = max(0, tg - C::NST); t < tg; ++t) drain_bar(bar(C::B_KVFULL + t % C::NST), (t / C::NST) & 1);
     }
   } else if (warp == C::WARP_MMA) {
     // ------------------------------------------------------------ MMA issuer
@@ -320,14 +325,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
         if (done(C::B_PFULL + sbuf, (cp.tg / C::NSB) & 1) &&
             (cp.t != 0 || cp.k == 0 || done(C::B_OFREE, (cp.k - 1) & 1))) {
           tc_fence_after();
-          const int il = cp.t % cp.ng, kt = cp.t / cp.ng;
-          const uint64_t dv = dv0 + (uint64_t)((sbuf * C::TILE) >> 4);
+          const int il = cp.t % cp.ng, kt = cp.t / cp.ng, st = cp.tg % C::NST;
+          const uint64_t dv = dv0 + (uint64_t)((st * C::TILE) >> 4);
           const uint32_t dO = tbase + C::TO + il * HD, aP = tbase + sbuf * 128;
-          mma_ts_e(dO, aP, dv, idPV, kt > 0 ? 1u : 0u);
-#pragma unroll
-          for (int ks = 1; ks < 8; ++ks)
-            mma_ts_e(dO, aP + (ks >> 2) * 64 + (ks & 3) * 8, dv + (uint64_t)((ks * 16 * C::ROWB) >> 4), idPV, 1u);
+          // K step ks: P columns (ks >> 2) * 64 + (ks & 3) * 8, V rows 16 ks
+          mma_ts_x8_e<0, 8, 16, 24, 64, 72, 80, 88>(dO, aP, dv, (uint64_t)((16 * C::ROWB) >> 4), idPV, kt > 0 ? 1u : 0u);
           mma_commit_e(bar(C::B_TDONE + sbuf));
+          mma_commit_e(bar(C::B_KVEMPTY + st));
           if (cp.t == cp.T - 1) mma_commit_e(bar(C::B_OFINAL));
           advance(cp);
           progress = true;
@@ -337,11 +341,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
       // tile (tile n - ng) has been issued, so that the commit of S(n) also covers that P.V: the
       // softmax threads rely on this when they rescale O after waiting for S(n).
       if (cs.u < nunits && cs.tg < cp.tg + min(C::NSB, cs.ng)) {
-        const int sbuf = cs.tg % C::NSB;
-        if (done(C::B_Q, cs.k & 1) && done(C::B_KVFULL + sbuf, (cs.tg / C::NSB) & 1) &&
+        const int sbuf = cs.tg % C::NSB, st = cs.tg % C::NST;
+        if (done(C::B_Q, cs.k & 1) && done(C::B_KVFULL + st, (cs.tg / C::NST) & 1) &&
             (cs.tg < C::NSB || done(C::B_TDONE + sbuf, ((cs.tg / C::NSB) - 1) & 1))) {
           tc_fence_after();
-          const uint64_t dq = dq0 + (uint64_t)(((cs.t % cs.ng) * C::TILE) >> 4), dk = dk0 + (uint64_t)((sbuf * C::TILE) >> 4);
+          const uint64_t dq = dq0 + (uint64_t)(((cs.t % cs.ng) * C::TILE) >> 4), dk = dk0 + (uint64_t)((st * C::TILE) >> 4);
           mma_ss_e(tbase + sbuf * 128, dq, dk, idS, 0u);
 #pragma unroll
           for (int ks = 1; ks < HD / 16; ++ks) mma_ss_e(tbase + sbuf * 128, dq + 2 * ks, dk + 2 * ks, idS, 1u);
@@ -565,8 +569,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
             }
           {
             // the tile's V, BF16 -> FP16 in place (V landed with K, before S), a share per thread
-            const int st = sbuf;
-            ok = wait_bar(bar(C::B_KVFULL + st), (tg / C::NSB) & 1, ab);
+            const int st = tg % C::NST;
+            ok = wait_bar(bar(C::B_KVFULL + st), (tg / C::NST) & 1, ab);
             uint4 *v = reinterpret_cast<uint4 *>(sm + C::OFF_V + st * C::TILE);
 #pragma unroll
             for (int e = wtid; e < C::TILE / 16; e += 128) {

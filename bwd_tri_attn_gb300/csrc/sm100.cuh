@@ -425,6 +425,30 @@ __device__ __forceinline__ void mma_commit_e(uint32_t bar) {
       : "memory");
 }
 
+// Eight M=128 MMAs with A from TMEM into one accumulator (a K loop of 8 steps) issued from one
+// asm block with a single elect.sync: A operand k at a_tmem + a_off[k] columns, B descriptor
+// b_desc + b_step * k. The first MMA accumulates if `accumulate` is nonzero, the others always.
+template <int A0, int A1, int A2, int A3, int A4, int A5, int A6, int A7>
+__device__ __forceinline__ void mma_ts_x8_e(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint64_t b_step,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, t, e;\n\t.reg .b32 a;\n\t.reg .b64 b;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\tsetp.eq.b32 t, 0, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %4, p;\n\t"
+      "add.u32 a, %1, %6;\n\tadd.u64 b, %2, %3;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, t;\n\t"
+      "add.u32 a, %1, %7;\n\tadd.u64 b, b, %3;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, t;\n\t"
+      "add.u32 a, %1, %8;\n\tadd.u64 b, b, %3;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, t;\n\t"
+      "add.u32 a, %1, %9;\n\tadd.u64 b, b, %3;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, t;\n\t"
+      "add.u32 a, %1, %10;\n\tadd.u64 b, b, %3;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, t;\n\t"
+      "add.u32 a, %1, %11;\n\tadd.u64 b, b, %3;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, t;\n\t"
+      "add.u32 a, %1, %12;\n\tadd.u64 b, b, %3;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, t;\n\t"
+      "}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "l"(b_step), "r"(idesc), "r"(accumulate), "n"(A1), "n"(A2), "n"(A3), "n"(A4),
+      "n"(A5), "n"(A6), "n"(A7)
+      : "memory");
+  (void)A0;
+}
+
 // Arrives once on `bar` when every tcgen05 op issued so far by this thread completes.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
