@@ -446,10 +446,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
         {
           const uint64_t b = dO0 + (uint64_t)((st * C::TILE) >> 4);
           // 16 queries per step: column group ks / KPG, packed columns (ks % KPG) * 8
-          mma_ts_e(dcol + HD, tb + C::TA, b, idKV, cjt > 0 ? 1u : 0u);
-#pragma unroll
-          for (int ks = 1; ks < 8; ++ks)
-            mma_ts_e(dcol + HD, tb + C::TA + (ks / C::KPG) * C::QPT + (ks % C::KPG) * 8, b + ks * KS_ROW, idKV, 1u);
+          static_assert(C::KPG == 4 && C::QPT == 64, "P^T column pattern");
+          mma_ts_x8_e<0, 8, 16, 24, 64, 72, 80, 88>(dcol + HD, tb + C::TA, b, KS_ROW, idKV, cjt > 0 ? 1u : 0u);
           mma_commit_e(bar(C::B_AFREE));
         }
         // ---- S^T(t+1) once dV has read region A (within a block; a new block needs the new K, V first)
@@ -467,14 +465,9 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
         tc_fence_after();
         {
           const uint64_t bq = dQ0 + (uint64_t)((st * C::TILE) >> 4), bk = dK0 + (uint64_t)((cil * C::TILE) >> 4);
-          mma_ts_e(dcol, tb + C::TB, bq, idKV, cjt > 0 ? 1u : 0u);
-#pragma unroll
-          for (int ks = 1; ks < 8; ++ks)
-            mma_ts_e(dcol, tb + C::TB + (ks / C::KPG) * C::QPT + (ks % C::KPG) * 8, bq + ks * KS_ROW, idKV, 1u);
+          mma_ts_x8_e<0, 8, 16, 24, 64, 72, 80, 88>(dcol, tb + C::TB, bq, KS_ROW, idKV, cjt > 0 ? 1u : 0u);
           mma_commit_e(bar(C::B_BFREEM));
-          mma_ss_e(tb + C::TDQ, dS0, bk, idQ, 0u);
-#pragma unroll
-          for (int ks = 1; ks < 8; ++ks) mma_ss_e(tb + C::TDQ, dS0 + ks * (4096 >> 4), bk + ks * KS_ROW, idQ, 1u);
+          mma_ss_x8_e(tb + C::TDQ, dS0, 4096 >> 4, bk, KS_ROW, idQ, 0u);
           mma_commit_e(bar(C::B_M2DONE));
           mma_commit_e(bar(C::B_QDOFREE + st));
           if (next_new_block || !has_next) mma_commit_e(bar(C::B_KVFREE));

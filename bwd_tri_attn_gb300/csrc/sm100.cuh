@@ -449,6 +449,26 @@ __device__ __forceinline__ void mma_ts_x8_e(uint32_t d_tmem, uint32_t a_tmem, ui
   (void)A0;
 }
 
+// Eight M=128 MMAs with A and B from shared memory into one accumulator (a K loop of 8 steps),
+// one asm block and a single elect.sync: descriptors a_desc + a_step * k and b_desc + b_step * k.
+__device__ __forceinline__ void mma_ss_x8_e(uint32_t d_tmem, uint64_t a_desc, uint64_t a_step, uint64_t b_desc,
+                                            uint64_t b_step, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, t, e;\n\t.reg .b64 a, b;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\tsetp.eq.b32 t, 0, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %3, %5, p;\n\t"
+      "add.u64 a, %1, %2;\n\tadd.u64 b, %3, %4;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %5, t;\n\t"
+      "add.u64 a, a, %2;\n\tadd.u64 b, b, %4;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %5, t;\n\t"
+      "add.u64 a, a, %2;\n\tadd.u64 b, b, %4;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %5, t;\n\t"
+      "add.u64 a, a, %2;\n\tadd.u64 b, b, %4;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %5, t;\n\t"
+      "add.u64 a, a, %2;\n\tadd.u64 b, b, %4;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %5, t;\n\t"
+      "add.u64 a, a, %2;\n\tadd.u64 b, b, %4;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %5, t;\n\t"
+      "add.u64 a, a, %2;\n\tadd.u64 b, b, %4;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %5, t;\n\t"
+      "}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(a_step), "l"(b_desc), "l"(b_step), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrives once on `bar` when every tcgen05 op issued so far by this thread completes.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
