@@ -206,7 +206,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
 
   if (tid == 0) {
     mbar_init(bar(C::B_KVFULL), 1);
-    mbar_init(bar(C::B_KVREADY), C::NCV);
+    mbar_init(bar(C::B_KVREADY), C::NCV + C::NEW);  // converter and elementwise warps share the K/V conversion
     mbar_init(bar(C::B_KVFREE), 1);
     for (int s = 0; s < C::NQS; ++s) {
       mbar_init(bar(C::B_QDOFULL + s), 1);
@@ -337,8 +337,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
       const int b = hd / g.H;
       ok = wait_bar_warp(bar(C::B_KVFULL), bi & 1, ab);
       if (!ok) break;
-      convert_to_f16(sm + C::OFF_K, nb * C::TILE, ct, C::NCVT);
-      convert_to_f16(sm + C::OFF_V, nb * C::TILE, ct, C::NCVT);
+      // this warp's share of the block's K and V (the elementwise warps, idle at a block boundary,
+      // convert the rest)
+      convert_to_f16(sm + C::OFF_K, nb * C::TILE, C::NEWT + ct, C::NEWT + C::NCVT);
+      convert_to_f16(sm + C::OFF_V, nb * C::TILE, C::NEWT + ct, C::NEWT + C::NCVT);
       float *maskf = reinterpret_cast<float *>(sm + C::OFF_MASK);
       for (int x = ct; x < nb * 128; x += C::NCVT) {
         const int il = x >> 7, k = kt * 128 + (x & 127);
@@ -611,7 +613,16 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
       // tiles [head][slot][kt][jt][128 x 128]
       const int64_t pslot = ((int64_t)hd * KMAX + (cl - bwd_cluster_of((int64_t)hd * g.S, NC, W))) * nkt * njt;
       auto ptile = [&](int jt_) -> int64_t { return (pslot + (int64_t)kt * njt + jt_) * 16384; };
-      ok = wait_bar_warp(bar(C::B_KVREADY), bi & 1, ab);  // the mask rows of the block are in place
+      // help convert the block's K and V to FP16 (with the converter warps), then wait until the whole
+      // conversion and the block's mask rows are in place
+      ok = wait_bar_warp(bar(C::B_KVFULL), bi & 1, ab);
+      if (!ok) break;
+      convert_to_f16(sm + C::OFF_K, nb * C::TILE, tid, C::NEWT + C::NCVT);
+      convert_to_f16(sm + C::OFF_V, nb * C::TILE, tid, C::NEWT + C::NCVT);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::B_KVREADY));
+      ok = wait_bar_warp(bar(C::B_KVREADY), bi & 1, ab);
       for (int jt = 0; jt < njt && ok; ++jt) {
         ok = wait_bar_warp(bar(C::B_BFULL), u & 1, ab);
         if (!ok) break;
