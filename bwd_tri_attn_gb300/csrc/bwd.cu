@@ -182,7 +182,8 @@ template <int HD>
 __global__ void __launch_bounds__(BwdCfg<HD>::NTHREADS, 1)
 bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
            const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mDO,
-           const __grid_constant__ CUtensorMap mBT, const Dims g, const int NC, const int KMAX,
+           const __grid_constant__ CUtensorMap mBT, const __grid_constant__ CUtensorMap mDK,
+           const __grid_constant__ CUtensorMap mDV, const Dims g, const int NC, const int KMAX,
            const float *__restrict__ LSE,
            const float *__restrict__ Dv, const uint16_t *__restrict__ mask, uint16_t *__restrict__ dQ,
            uint16_t *__restrict__ dK, uint16_t *__restrict__ dV, float *__restrict__ partial, int *status) {
@@ -748,43 +749,57 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
         ++u;
       }
       if (!ok) break;
-      // ---- dK_i, dV_i of the block -> BF16, once the block's last MMAs are complete: the first half
-      // of the column groups writes dK, the second dV, each group RC of the HD columns
+      // ---- dK_i, dV_i of the block -> BF16, once the block's last MMAs are complete: column group 0
+      // writes dK, group 1 dV. Each warp stages its 32 key rows of a slice in its own 2 KB piece of
+      // the dS tile (free now; two pieces per warp, used alternately over the slices), in the TMA
+      // swizzle, and stores them with one 32-row TMA box; rows past N are clipped by the TMA.
       ok = wait_bar_warp(bar(C::B_M2DONE), (t - 1) & 1, ab);
       if (!ok) break;
       tc_fence_after();
       {
-        constexpr int NG = C::NEW / 8, RC = HD / NG;  // column groups per tensor, columns per group
-        const int tsel = cg / NG, coff = (cg % NG) * RC;
-        const float f = tsel == 0 ? g.scale : 1.f;
-        uint16_t *outb = tsel == 0 ? dK : dV;
+        static_assert(C::NEW == 8 && 2 * C::NEW * 32 * C::ROWB <= 32768, "dK/dV staging in the dS tile");
+        const float f = cg == 0 ? g.scale : 1.f;
+        const CUtensorMap *mo = cg == 0 ? &mDK : &mDV;
+        // 16-byte chunk c of staged row lane: SW64 (64-byte rows) or SW32 (32-byte rows)
+        const uint32_t swz = HD == 32 ? (uint32_t)((lane >> 1) & 3) : (uint32_t)((lane >> 2) & 1);
         for (int il = 0; il < nb; ++il) {
-          uint32_t r[RC];
-          const uint32_t col = tb + lb + C::TDKV + il * 2 * HD + tsel * HD + coff;
-          if constexpr (RC == 32) {
+          uint32_t r[HD];
+          const uint32_t col = tb + lb + C::TDKV + il * 2 * HD + cg * HD;
+          if constexpr (HD == 32) {
             tmem_ld32(col, r);
-          } else if constexpr (RC == 16) {
-            tmem_ld16(col, r);
           } else {
-            tmem_ld8(col, r);
+            tmem_ld16(col, r);
           }
           tmem_wait_ld(r);
-          uint32_t w[RC / 2];
+          uint32_t w[HD / 2];
 #pragma unroll
-          for (int c = 0; c < RC / 2; ++c)
+          for (int c = 0; c < HD / 2; ++c)
             w[c] = pack_bf16x2(__uint_as_float(r[2 * c]) * f, __uint_as_float(r[2 * c + 1]) * f);
-          if (kg < g.N) {
-            uint16_t *out = outb + pos_row(g, b, i0 + il, kg) * g.H * HD + h * HD + coff;
+          if (il >= 2) {  // the store of slice il - 2 has read this piece
+            if (lane == 0) bulk_wait_group_read<1>();
+            __syncwarp();
+          }
+          const uint32_t piece = sb0 + C::OFF_DS + (warp * 2 + (il & 1)) * (32 * C::ROWB);
 #pragma unroll
-            for (int c = 0; c < RC / 8; ++c)  // 16 bytes = 8 columns at a time
-              reinterpret_cast<uint4 *>(out)[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+          for (int c = 0; c < HD / 8; ++c)
+            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(piece + lane * C::ROWB + ((c ^ swz) << 4)),
+                         "r"(w[4 * c]), "r"(w[4 * c + 1]), "r"(w[4 * c + 2]), "r"(w[4 * c + 3])
+                         : "memory");
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_4d(mo, piece, 0, h, kt * 128 + q * 32, b * g.S + i0 + il);
+            bulk_commit_group();
           }
         }
+        if (lane == 0) bulk_wait_group_read<0>();  // the next block's dS tiles overwrite these pieces
+        __syncwarp();
       }
       tc_fence_before();
       mbar_arrive(bar(C::B_DKVREAD));
     }
   }
+  if (warp < C::NEW && lane == 0) bulk_wait_group<0>();  // the dK, dV stores have been performed
   tc_fence_before();
   __syncthreads();
   cluster_sync_all();  // no CTA leaves while a peer may still write or read its shared memory
@@ -872,8 +887,10 @@ cudaError_t launch_bwd_main_t(const Dims &g, const BwdSplit &sp, const uint16_t 
                               int *status, cudaStream_t stream) {
   using C = BwdCfg<HD>;
   const int nkt = (g.N + 127) / 128, NP = nkt * 128;
-  CUtensorMap mq, mk, mv, mdo, mbt;
+  CUtensorMap mq, mk, mv, mdo, mbt, mdk, mdv;
   cudaError_t e = make_rows_map(&mq, Q, g, 128);
+  if (e == cudaSuccess) e = make_rows_map(&mdk, dK, g, 32);
+  if (e == cudaSuccess) e = make_rows_map(&mdv, dV, g, 32);
   if (e == cudaSuccess) e = make_rows_map(&mk, K, g, 128);
   if (e == cudaSuccess) e = make_rows_map(&mv, V, g, 128);
   if (e == cudaSuccess) e = make_rows_map(&mdo, dO, g, 128);
@@ -904,8 +921,8 @@ cudaError_t launch_bwd_main_t(const Dims &g, const BwdSplit &sp, const uint16_t 
   attrs[0].val.clusterDim.z = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, bwd_kernel<HD>, mq, mk, mv, mdo, mbt, g, sp.NC, sp.KMAX, LSE, Dv, mask, dQ, dK, dV,
-                            partial, status);
+  return cudaLaunchKernelEx(&cfg, bwd_kernel<HD>, mq, mk, mv, mdo, mbt, mdk, mdv, g, sp.NC, sp.KMAX, LSE, Dv, mask,
+                            dQ, dK, dV, partial, status);
 }
 
 cudaError_t launch_bwd_main(const Dims &g, const BwdSplit &sp, const uint16_t *Q, const uint16_t *K,
