@@ -69,8 +69,8 @@ struct BwdCfg {
   static constexpr int WARP_DQ = NEW, NDQ = 4, NDQT = NDQ * 32;
   static constexpr int WARP_TMA = NEW + 4, WARP_MMA = NEW + 5, WARP_CV = NEW + 6, NCV = 2, NCVT = NCV * 32;
   static constexpr int NTHREADS = (NEW + 8) * 32;
-  static constexpr uint32_t REG_LAUNCH = QPT == 64 ? 128 : 80, REG_EW = QPT == 64 ? 176 : 96,
-                            REG_OTHER = QPT == 64 ? 80 : 48;
+  static constexpr uint32_t REG_LAUNCH = QPT == 64 ? 128 : 80, REG_EW = QPT == 64 ? 200 : 96,
+                            REG_OTHER = QPT == 64 ? 56 : 48;
   static_assert(NEWT * REG_EW + (NTHREADS - NEWT) * REG_OTHER == NTHREADS * REG_LAUNCH, "register split");
   // the dQ partial (32 columns) uses the half of region B that dS^T leaves free: column group 0 of
   // the elementwise threads keeps its packed dS^T in B + [0,32) and group 1 in B + [64,96)
