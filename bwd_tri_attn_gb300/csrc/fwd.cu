@@ -27,13 +27,14 @@
 // and warpgroup 1 the slices il = 1, 3, ... of every key tile, so the two work on
 // different S tiles at once and never wait on each other inside a key tile.
 // Warp 8 = producer (TMA for Q, K, V and the bias tiles, bulk copies of the mask
-// rows and their per-tile "nonzero" flags), warp 9 = MMA issuer + TMEM owner,
-// warps 10-11 only donate registers (setmaxnreg: 216 per softmax thread).
+// rows and their per-tile "nonzero" flags), warp 9 = P.V issuer + TMEM owner,
+// warp 10 = S issuer, warp 11 only donates registers (setmaxnreg: 216 per
+// softmax thread).
 // TMEM columns: three S buffers [0,128) [128,256) [256,384), with P written as
 // FP16 pairs over the columns the thread has already read (keys 0-63 -> cols
 // 0-31, keys 64-127 -> cols 64-95 of the buffer); O_i at 384 + i*d.
 // The online max is updated lazily (only when it grows by more than 2^8), and
-// O is rescaled in TMEM only then. Between units the softmax warps read O out of
+// O is rescaled in TMEM only then, after the slice's previous P.V has completed. Between units the softmax warps read O out of
 // TMEM (then release it to the next unit's first P.V) before they normalise and
 // store it.
 //
@@ -69,17 +70,18 @@ struct FwdCfg {
   static constexpr int OFF_FLAG = OFF_MASK + 2 * GF * NMAX * 2;  // 2 x int [GF][MAXKT]: tile has a nonzero mask entry
   static constexpr int OFF_BAR = OFF_FLAG + 2 * GF * MAXKT * 4;
   // barrier indices
-  static constexpr int B_Q = 0;
-  static constexpr int B_KVFULL = 1;
+  static constexpr int B_Q = 0;                 // [GF] Q tile of slice il landed
+  static constexpr int B_KVFULL = B_Q + GF;
   static constexpr int B_KVEMPTY = B_KVFULL + NST;  // the stage's P.V has completed
   static constexpr int B_SFULL = B_KVEMPTY + NST;
   static constexpr int B_PFULL = B_SFULL + NSB;  // P written and this tile's V converted
   static constexpr int B_TDONE = B_PFULL + NSB;  // the buffer's P.V has completed: the S buffer is free
-  static constexpr int B_OFINAL = B_TDONE + NSB;
-  static constexpr int B_OFREE = B_OFINAL + 1;  // softmax warps have read O of the unit out of TMEM
-  static constexpr int B_QFREE = B_OFREE + 1;   // the unit's last S MMA has read Q
-  static constexpr int B_MDRAIN = B_QFREE + 1;  // every MMA of the CTA has completed (teardown)
-  static constexpr int B_BFULL = B_MDRAIN + 1;  // [2] bias tile landed
+  static constexpr int B_OFINAL = B_TDONE + NSB;  // [2] the warpgroup's O accumulators of the unit are final
+  static constexpr int B_OFREE = B_OFINAL + 2;    // [2] the warpgroup has read its O of the unit out of TMEM
+  static constexpr int B_QFREE = B_OFREE + 2;     // [GF] the unit's last S MMA of slice il has read Q_il
+  static constexpr int B_MDRAIN = B_QFREE + GF;   // [2] every MMA of the S / P.V issuer has completed (teardown)
+  static constexpr int B_PVDONE = B_MDRAIN + 2;   // [GF] a P.V of slice il has completed (one phase per P.V)
+  static constexpr int B_BFULL = B_PVDONE + GF;  // [2] bias tile landed
   static constexpr int B_BFREE = B_BFULL + 2;   // [2] every slice of its key tile is done with it
   static constexpr int B_MFULL = B_BFREE + 2;   // [2] mask rows of a unit landed
   static constexpr int B_MFREE = B_MFULL + 2;   // [2] the unit is done with them
@@ -88,7 +90,7 @@ struct FwdCfg {
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // [0] TMEM base, [1] abort flag
   static constexpr int SMEM_ALLOC = OFF_MISC + 16 + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr int NSOFT = 8, WARP_TMA = 8, WARP_MMA = 9, NTHREADS = 384;  // warps 10, 11: register donors
+  static constexpr int NSOFT = 8, WARP_TMA = 8, WARP_MMA = 9, WARP_S = 10, NTHREADS = 384;  // warp 11: register donor
   // setmaxnreg split: the softmax warpgroups take registers from the third warpgroup (per SMSP:
   // two softmax warps and one other warp share 16K registers)
   static constexpr uint32_t REG_LAUNCH = 168, REG_SOFT = 216, REG_OTHER = 72;
@@ -141,7 +143,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
   const Abort ab{reinterpret_cast<volatile int *>(misc + 1), status};
 
   if (tid == 0) {
-    mbar_init(bar(C::B_Q), 1);
+    for (int s = 0; s < C::GF; ++s) {
+      mbar_init(bar(C::B_Q + s), 1);
+      mbar_init(bar(C::B_QFREE + s), 1);
+      mbar_init(bar(C::B_PVDONE + s), 1);
+    }
     for (int s = 0; s < C::NST; ++s) {
       mbar_init(bar(C::B_KVFULL + s), 1);
       mbar_init(bar(C::B_KVEMPTY + s), 1);
@@ -151,11 +157,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
       mbar_init(bar(C::B_PFULL + s), 128);  // the warpgroup that owns the tile
       mbar_init(bar(C::B_TDONE + s), 1);
     }
-    mbar_init(bar(C::B_OFINAL), 1);
-    mbar_init(bar(C::B_OFREE), 256);
-    mbar_init(bar(C::B_QFREE), 1);
-    mbar_init(bar(C::B_MDRAIN), 1);
     for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(C::B_MDRAIN + s), 1);
+      mbar_init(bar(C::B_OFINAL + s), 1);
+      mbar_init(bar(C::B_OFREE + s), 128);
       mbar_init(bar(C::B_BFULL + s), 1);
       mbar_init(bar(C::B_BFREE + s), 256);
       mbar_init(bar(C::B_MFULL + s), 1);
@@ -184,6 +189,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
     // ------------------------------------------------------------ producer
     reg_dealloc<C::REG_OTHER>();
     int tg = 0, k = 0, kb = 0;  // tiles, units and bias tiles issued by this CTA
+    uint32_t qcur = 0;          // Q buffers whose phase of the current unit has been started
     bool ok = true;
     if (lane == 0) {
       tma_prefetch_map(&mQ);
@@ -193,13 +199,15 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
     }
     for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++k) {
       const FwdUnit w = fwd_unit<HD>(g, u);
-      if (k > 0) ok = wait_bar_warp(bar(C::B_QFREE), (k - 1) & 1, ab);  // the previous unit's S MMAs read Q
-      if (!ok) break;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bar(C::B_Q), w.ng * C::TILE);
-        for (int il = 0; il < w.ng; ++il)
-          tma_load_4d(sb0 + C::OFF_Q + il * C::TILE, &mQ, bar(C::B_Q), 0, w.h, w.jt * 128, w.b * g.S + w.i0 + il);
+      qcur = 0;
+      // Q buffers of slices the unit does not have complete their phase at once (every buffer
+      // goes through one phase per unit); the others are loaded with the unit's first key tile
+      for (int il = w.ng; il < C::GF && ok; ++il) {
+        if (k > 0) ok = wait_bar_warp(bar(C::B_QFREE + il), (k - 1) & 1, ab);
+        if (ok && lane == 0) mbar_arrive(bar(C::B_Q + il));
+        if (ok) qcur |= 1u << il;
       }
+      if (!ok) break;
       if (mask) {  // the unit's mask rows into buffer k & 1 (free once unit k - 2 is done)
         if (k >= 2) ok = wait_bar_warp(bar(C::B_MFREE + (k & 1)), ((k - 2) >> 1) & 1, ab);
         if (!ok) break;
@@ -259,6 +267,15 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
           }
           ++kb;
         }
+        if (t < w.ng) {  // Q_il, once the previous unit's last S MMA of slice il has read the buffer
+          if (k > 0) ok = wait_bar_warp(bar(C::B_QFREE + t), (k - 1) & 1, ab);
+          if (!ok) break;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(bar(C::B_Q + t), C::TILE);
+            tma_load_4d(sb0 + C::OFF_Q + t * C::TILE, &mQ, bar(C::B_Q + t), 0, w.h, w.jt * 128, w.b * g.S + w.i0 + t);
+          }
+          qcur |= 1u << t;
+        }
         const int st = tg % C::NST, use = tg / C::NST;
         if (use > 0) ok = wait_bar_warp(bar(C::B_KVEMPTY + st), (use - 1) & 1, ab);
         if (!ok) break;
@@ -274,109 +291,82 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
     }
     if (!ok && lane == 0) {
       // drain copies still in flight before the CTA's shared memory goes away
-      if (k > 0) drain_bar(bar(C::B_Q), (k - 1) & 1);
+      for (int il = 0; il < C::GF; ++il) {
+        if ((qcur >> il) & 1) {
+          drain_bar(bar(C::B_Q + il), k & 1);
+        } else if (k > 0) {
+          drain_bar(bar(C::B_Q + il), (k - 1) & 1);
+        }
+      }
       if (mask && tma_bias && k > 0) drain_bar(bar(C::B_MFULL + ((k - 1) & 1)), ((k - 1) >> 1) & 1);
       for (int x = max(0, kb - 2); x < kb; ++x) drain_bar(bar(C::B_BFULL + (x & 1)), (x >> 1) & 1);
       for (int t = max(0, tg - C::NST); t < tg; ++t) drain_bar(bar(C::B_KVFULL + t % C::NST), (t / C::NST) & 1);
     }
-  } else if (warp == C::WARP_MMA) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == C::WARP_MMA || warp == C::WARP_S) {
+    // ------------------------------------------------------------ MMA issuers
+    // Warp 10 issues S = Q K^T, warp 9 P.V, each walking the CTA's tiles in order (units
+    // blockIdx.x, +gridDim.x, ...; in a unit key tile kt, then slice il) with blocking waits on
+    // exactly the barriers that gate its next MMA. Each warp runs converged; elect.sync picks
+    // the lane that issues. A commit covers the MMAs of the issuing thread only, so every
+    // barrier below is committed by the warp whose MMAs it certifies.
     reg_dealloc<C::REG_OTHER>();
-    // The whole warp runs this loop converged (every decision is warp-uniform) and elect.sync
-    // picks the lane that issues each MMA and commit.
     constexpr uint32_t idS = idesc_f16(128, 128, true, true, false, false);
     constexpr uint32_t idPV = idesc_f16(128, HD, false, false, false, true);
-    // Two cursors walk the CTA's tiles (units blockIdx.x, +gridDim.x, ...; in a unit key tile kt,
-    // then slice il). S of the S cursor's tile is issued as soon as its K tile has landed and its
-    // S buffer is free; P.V of the P.V cursor's tile as soon as its P is written (and, for a
-    // unit's first tile, the previous unit's O has been read out). Whichever is ready first goes
-    // first, so the two softmax warpgroups never wait on each other's progress for their S.
-    struct Cur {
-      int u, k, t, T, ng, tg;
-    };
-    auto start = [&](Cur &c, int u, int k, int tg) {
-      c.u = u;
-      c.k = k;
-      c.t = 0;
-      c.tg = tg;
-      c.ng = u < nunits ? fwd_unit<HD>(g, u).ng : 0;
-      c.T = nkt * c.ng;
-    };
-    auto advance = [&](Cur &c) {
-      ++c.tg;
-      if (++c.t == c.T) start(c, c.u + (int)gridDim.x, c.k + 1, c.tg);
-    };
-    // a phase counts as complete only once every lane has observed it (each lane acquires)
-    auto done = [&](int k, int parity) { return __all_sync(0xffffffffu, mbar_test_wait(bar(k), parity)); };
-    Cur cs, cp;
-    start(cs, blockIdx.x, 0, 0);
-    start(cp, blockIdx.x, 0, 0);
     // descriptor bases: the start-address field is (address >> 4) in the low bits, so an operand
     // at base + off has descriptor base_desc + (off >> 4) (addresses stay below 256 KB)
     const uint64_t dq0 = smem_desc(sb0 + C::OFF_Q, 16, 8 * C::ROWB, C::SW);
     const uint64_t dk0 = smem_desc(sb0 + C::OFF_K, 16, 8 * C::ROWB, C::SW);
     const uint64_t dv0 = smem_desc(sb0 + C::OFF_V, 16, 8 * C::ROWB, C::SW);
-    bool ok = true, idle = false;
-    uint64_t t_idle = 0;
-    while (ok && cp.u < nunits) {
-      bool progress = false;
-      {  // O_il += P V (P.V needs P written and V converted: both certified by PFULL)
-        const int sbuf = cp.tg % C::NSB;
-        if (done(C::B_PFULL + sbuf, (cp.tg / C::NSB) & 1) &&
-            (cp.t != 0 || cp.k == 0 || done(C::B_OFREE, (cp.k - 1) & 1))) {
+    const bool is_s = warp == C::WARP_S;
+    bool ok = true;
+    int tg = 0, k = 0;
+    for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++k) {
+      const int ng = fwd_unit<HD>(g, u).ng, T = nkt * ng;
+      int il = 0, kt = 0;
+      for (int t = 0; t < T && ok; ++t, ++tg) {
+        const int sbuf = tg % C::NSB, st = tg % C::NST;
+        if (is_s) {
+          // S into buffer tg % NSB: Q_il and the tile's K landed, the buffer's previous P.V done
+          ok = wait_bar_warp(bar(C::B_Q + il), k & 1, ab) && wait_bar_warp(bar(C::B_KVFULL + st), (tg / C::NST) & 1, ab) &&
+               (tg < C::NSB || wait_bar_warp(bar(C::B_TDONE + sbuf), ((tg / C::NSB) - 1) & 1, ab));
+          if (!ok) break;
           tc_fence_after();
-          const int il = cp.t % cp.ng, kt = cp.t / cp.ng, st = cp.tg % C::NST;
+          const uint64_t dq = dq0 + (uint64_t)((il * C::TILE) >> 4), dk = dk0 + (uint64_t)((st * C::TILE) >> 4);
+          mma_ss_e(tbase + sbuf * 128, dq, dk, idS, 0u);
+#pragma unroll
+          for (int ks = 1; ks < HD / 16; ++ks) mma_ss_e(tbase + sbuf * 128, dq + 2 * ks, dk + 2 * ks, idS, 1u);
+          mma_commit_e(bar(C::B_SFULL + sbuf));
+          if (t >= T - ng) mma_commit_e(bar(C::B_QFREE + il));  // the unit's last S of slice il
+          if (t == T - 1)
+            for (int q = ng; q < C::GF; ++q) mma_commit_e(bar(C::B_QFREE + q));
+        } else {
+          // O_il += P V: P written and V converted (PFULL); a unit's first P.V of a slice overwrites
+          // the accumulator, so the previous unit's O must have been read out (OFREE)
+          ok = wait_bar_warp(bar(C::B_PFULL + sbuf), (tg / C::NSB) & 1, ab) &&
+               (kt > 0 || k == 0 || wait_bar_warp(bar(C::B_OFREE + (il & 1)), (k - 1) & 1, ab));
+          if (!ok) break;
+          tc_fence_after();
           const uint64_t dv = dv0 + (uint64_t)((st * C::TILE) >> 4);
           const uint32_t dO = tbase + C::TO + il * HD, aP = tbase + sbuf * 128;
           // K step ks: P columns (ks >> 2) * 64 + (ks & 3) * 8, V rows 16 ks
           mma_ts_x8_e<0, 8, 16, 24, 64, 72, 80, 88>(dO, aP, dv, (uint64_t)((16 * C::ROWB) >> 4), idPV, kt > 0 ? 1u : 0u);
           mma_commit_e(bar(C::B_TDONE + sbuf));
           mma_commit_e(bar(C::B_KVEMPTY + st));
-          if (cp.t == cp.T - 1) mma_commit_e(bar(C::B_OFINAL));
-          advance(cp);
-          progress = true;
+          mma_commit_e(bar(C::B_PVDONE + il));
+          // the warpgroup's O is final after the P.V of its last slice in the last key tile; a
+          // warpgroup without slices in this unit is released with the unit's last P.V
+          if (kt == nkt - 1 && il + 2 >= ng) mma_commit_e(bar(C::B_OFINAL + (il & 1)));
+          if (t == T - 1 && ng == 1) mma_commit_e(bar(C::B_OFINAL + 1));
         }
-      }
-      // S = Q K^T into a free buffer. S(n) is issued only once P.V of the same slice's previous key
-      // tile (tile n - ng) has been issued, so that the commit of S(n) also covers that P.V: the
-      // softmax threads rely on this when they rescale O after waiting for S(n).
-      if (cs.u < nunits && cs.tg < cp.tg + min(C::NSB, cs.ng)) {
-        const int sbuf = cs.tg % C::NSB, st = cs.tg % C::NST;
-        if (done(C::B_Q, cs.k & 1) && done(C::B_KVFULL + st, (cs.tg / C::NST) & 1) &&
-            (cs.tg < C::NSB || done(C::B_TDONE + sbuf, ((cs.tg / C::NSB) - 1) & 1))) {
-          tc_fence_after();
-          const uint64_t dq = dq0 + (uint64_t)(((cs.t % cs.ng) * C::TILE) >> 4), dk = dk0 + (uint64_t)((st * C::TILE) >> 4);
-          mma_ss_e(tbase + sbuf * 128, dq, dk, idS, 0u);
-#pragma unroll
-          for (int ks = 1; ks < HD / 16; ++ks) mma_ss_e(tbase + sbuf * 128, dq + 2 * ks, dk + 2 * ks, idS, 1u);
-          mma_commit_e(bar(C::B_SFULL + sbuf));
-          if (cs.t == cs.T - 1) mma_commit_e(bar(C::B_QFREE));
-          advance(cs);
-          progress = true;
-        }
-      }
-      if (progress) {
-        idle = false;
-      } else {
-        // nothing ready: sleep briefly on the next P (the usual next event), with a time limit overall
-        mbar_try_wait_for(bar(C::B_PFULL + cp.tg % C::NSB), (cp.tg / C::NSB) & 1, 100);
-        const uint64_t now = __shfl_sync(0xffffffffu, globaltimer_ns(), 0);
-        if (!idle) {
-          idle = true;
-          t_idle = now;
-        } else if (__any_sync(0xffffffffu, *ab.flag != 0)) {
-          ok = false;
-        } else if (now - t_idle > kWaitLimitNs) {
-          if (lane == 0) {
-            *ab.flag = 1;
-            atomicExch(ab.status, kStatusTimeout);
-          }
-          ok = false;
+        if (++il == ng) {
+          il = 0;
+          ++kt;
         }
       }
     }
-    mma_commit_e(bar(C::B_MDRAIN));  // lands once every MMA issued above has completed
-    if (lane == 0) drain_bar(bar(C::B_MDRAIN), 0);
+    const uint32_t drain = bar(C::B_MDRAIN + (is_s ? 1 : 0));
+    mma_commit_e(drain);  // lands once every MMA this warp issued has completed
+    if (lane == 0) drain_bar(drain, 0);
     __syncwarp();
   } else if (warp < C::NSOFT) {
     // ------------------------------------------------------------ softmax / epilogue (warps 0-7)
@@ -414,6 +404,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
     bool ok = true;
     int tgu = 0, k = 0;  // tiles of the units before this one, units done
     int kb = 0;          // key tiles of bias used so far: tile n lives in bias buffer n & 1
+    int pvc[NL];         // P.V of this warpgroup's slice slots in the units before this one
+#pragma unroll
+    for (int s = 0; s < NL; ++s) pvc[s] = 0;
     if (!tma_bias && blockIdx.x < nunits) stage_bias(fwd_unit<HD>(g, blockIdx.x), 0, 0);
     for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++k) {
       const FwdUnit w = fwd_unit<HD>(g, u);
@@ -461,17 +454,28 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
 #pragma unroll
             for (int e = 0; e < 64; ++e) x[e] = make_float2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
           }
-          // scores in natural units: S*scale + bias (+ mask)
+          // scores in natural units: S*scale + bias (+ mask); the bias chunks (8 keys, 16 bytes of
+          // BF16) are loaded four ahead of their use
+          {
+            uint32_t bw[4][4];
+            auto bias_ld = [&](int ch, uint32_t(&w)[4]) {
+              asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                           : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                           : "r"(brow_s + (ch >> 3) * (C::BTILE / 2) + (((ch & 7) ^ sw) << 4)));
+            };
 #pragma unroll
-          for (int ch = 0; ch < 16; ++ch) {  // 8 keys (16 bytes of BF16 bias) at a time
-            uint32_t bw[4];
-            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                         : "=r"(bw[0]), "=r"(bw[1]), "=r"(bw[2]), "=r"(bw[3])
-                         : "r"(brow_s + (ch >> 3) * (C::BTILE / 2) + (((ch & 7) ^ sw) << 4)));
+            for (int ch = 0; ch < 4; ++ch) bias_ld(ch, bw[ch]);
 #pragma unroll
-            for (int m = 0; m < 4; ++m)
-              x[4 * ch + m] = __ffma2_rn(x[4 * ch + m], sc2,
-                                         make_float2(__uint_as_float(bw[m] << 16), __uint_as_float(bw[m] & 0xffff0000u)));
+            for (int ch = 0; ch < 16; ++ch) {
+              uint32_t cur[4];
+#pragma unroll
+              for (int m = 0; m < 4; ++m) cur[m] = bw[ch & 3][m];
+              if (ch + 4 < 16) bias_ld(ch + 4, bw[ch & 3]);
+#pragma unroll
+              for (int m = 0; m < 4; ++m)
+                x[4 * ch + m] = __ffma2_rn(x[4 * ch + m], sc2,
+                                           make_float2(__uint_as_float(cur[m] << 16), __uint_as_float(cur[m] & 0xffff0000u)));
+            }
           }
           if (mask && flags[il * C::MAXKT + kt]) {
             // the slice's mask entries of this key tile (the same for every row: broadcast loads),
@@ -530,9 +534,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
             }
           }
           if (__any_sync(0xffffffffu, resc)) {
-            // P.V of this slice's key tile kt-1 has completed: it was issued before S of this tile,
-            // whose commit (waited for above) covers every earlier MMA of the issuing thread
-
+            // O_il may be touched once the P.V of this slice's key tile kt-1 has completed
+            int pv = pvc[0];
+#pragma unroll
+            for (int qq = 1; qq < NL; ++qq)
+              if (qq == sl) pv = pvc[qq];
+            ok = wait_bar_warp(bar(C::B_PVDONE + il), (pv + kt - 1) & 1, ab);
+            if (!ok) break;
             const uint32_t oaddr = tbase + lane_base + C::TO + il * HD;
 #pragma unroll 1
             for (int c = 0; c < HD; c += 8) {  // 8 columns at a time: few registers next to the live scores
@@ -603,9 +611,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
         mbar_arrive(bar(C::B_MFREE + (k & 1)));
       }
       tgu += nkt * ng;
+#pragma unroll
+      for (int s = 0; s < NL; ++s)
+        if (wg + 2 * s < ng) pvc[s] += nkt;
       // epilogue: read O of this warpgroup's slices out of TMEM and release it, then
       // O = acc / l -> BF16, residual, LSE
-      ok = wait_bar_warp(bar(C::B_OFINAL), k & 1, ab);
+      ok = wait_bar_warp(bar(C::B_OFINAL + wg), k & 1, ab);
       if (!ok) break;
       tc_fence_after();
       uint32_t oacc[NL][HD] = {};
@@ -622,7 +633,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
       }
       tmem_wait_ld(oacc);
       tc_fence_before();
-      mbar_arrive(bar(C::B_OFREE));
+      mbar_arrive(bar(C::B_OFREE + wg));
 #pragma unroll
       for (int s = 0; s < NL; ++s) {
         const int il = wg + 2 * s;
@@ -656,7 +667,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
     }
     cp_async_wait_all();
   } else {
-    reg_dealloc<C::REG_OTHER>();  // warps 10, 11 only donate registers
+    reg_dealloc<C::REG_OTHER>();  // warp 11 only donates registers
   }
   tc_fence_before();
   __syncthreads();
