@@ -35,11 +35,13 @@
 // Operands: all tensor-core operands are FP16 (Q, K, V, dO converted in shared
 // memory, exact in the FP16 range); P and dS need FP16's 11-bit significand.
 //
-// Warp roles (NEW + 8 warps; NEW = 8 with QPT = 64 queries per elementwise thread):
-//   0..NEW-1  elementwise: thread = key row (TMEM lane quarter w % 4) x QPT queries (column group w / 4);
+// Warp roles (8 + NEW warps; NEW = 8 with QPT = 64 queries per elementwise thread). The control
+// warps take the lowest indices (warp schedulers favour low-index warps, and their short
+// instruction sequences gate everyone else's progress):
+//   0         TMA producer (+ LSE / D rows), 1 MMA issuer and TMEM owner, 2..3 BF16 -> FP16 conversion
+//   4..7      dQ: read the dQ partial from TMEM (lanes = queries), push it to the owners, reduce owned rows
+//   8..8+NEW-1 elementwise: thread = key row (TMEM lane quarter w % 4) x QPT queries (column group (w - 8) / 4);
 //             only P and dS are on their path; the most registers (setmaxnreg)
-//   NEW..+3   dQ: read the dQ partial from TMEM (lanes = queries), push it to the owners, reduce owned rows
-//   NEW+4     TMA producer (+ LSE / D rows), NEW+5 MMA issuer and TMEM owner, NEW+6..7 BF16 -> FP16 conversion
 // TMEM columns: A = [0,128) S^T, then FP16 P^T; B = [128,256) dP^T, then FP16 dS^T; dK_i, dV_i
 // from 256. Each elementwise thread writes P^T (dS^T) as packed FP16 over the S^T (dP^T) columns
 // it has just read: column group g of 64 queries keeps its 32 packed columns at A + 64g (B + 64g).
@@ -64,10 +66,10 @@ struct BwdCfg {
   static constexpr int TILE = 128 * ROWB;
   static constexpr uint32_t SW = HD == 32 ? kSwizzle64B : kSwizzle32B;
   static constexpr int QPT = 64;                   // queries per elementwise thread (64: 8 warps, 32: 16)
-  static constexpr int NEW = 4 * 128 / QPT, NEWT = NEW * 32;  // elementwise warps 0 .. NEW-1
+  static constexpr int NEW = 4 * 128 / QPT, NEWT = NEW * 32;  // elementwise warps WARP_EW0 .. WARP_EW0 + NEW - 1
   static constexpr int KPG = QPT / 16;             // K steps of 16 queries per column group
-  static constexpr int WARP_DQ = NEW, NDQ = 4, NDQT = NDQ * 32;
-  static constexpr int WARP_TMA = NEW + 4, WARP_MMA = NEW + 5, WARP_CV = NEW + 6, NCV = 2, NCVT = NCV * 32;
+  static constexpr int WARP_TMA = 0, WARP_MMA = 1, WARP_CV = 2, NCV = 2, NCVT = NCV * 32;
+  static constexpr int WARP_DQ = 4, NDQ = 4, NDQT = NDQ * 32, WARP_EW0 = 8;
   static constexpr int NTHREADS = (NEW + 8) * 32;
   static constexpr uint32_t REG_LAUNCH = QPT == 64 ? 128 : 80, REG_EW = QPT == 64 ? 200 : 96,
                             REG_OTHER = QPT == 64 ? 56 : 48;
@@ -243,8 +245,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
   tc_fence_after();
   const uint32_t tb = misc[0];
   // Register split (setmaxnreg, per warpgroup, at the top of each warpgroup's branch):
-  // warpgroups 2 and 3 give registers up, the two elementwise warpgroups take them.
-  if (warp >= C::WARP_TMA) {
+  // warpgroups 0 and 1 give registers up, the two elementwise warpgroups take them.
+  if (warp < C::WARP_DQ) {
    reg_dealloc<C::REG_OTHER>();
    if (warp == C::WARP_TMA) {
     // ---------------------------------------------------------------- producer
@@ -500,7 +502,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
       __syncwarp();
     }
    }
-  } else if (warp >= C::WARP_DQ) {
+  } else if (warp < C::WARP_EW0) {
     reg_dealloc<C::REG_OTHER>();
     // ---------------------------------------------------------------- dQ warps: TMEM -> owners -> BF16
     const int dt = tid - C::WARP_DQ * 32;   // 0..127
@@ -589,9 +591,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
     if (ok && red < T) ok = reduce_prev();  // the last step's rows
   } else {
     reg_alloc<C::REG_EW>();
-    // ---------------------------------------------------------------- elementwise warps 0-15
+    // ---------------------------------------------------------------- elementwise warps 8-15
     constexpr int QPT = C::QPT;
-    const int q = warp & 3, cg = warp >> 2;  // TMEM lane quarter, column group of QPT queries
+    const int ew = tid - C::WARP_EW0 * 32, ewarp = warp - C::WARP_EW0;  // 0..NEWT-1, 0..NEW-1
+    const int q = warp & 3, cg = ewarp >> 2;  // TMEM lane quarter, column group of QPT queries
     const int hf = (cg * QPT) >> 6, c0 = ((cg * QPT) & 63) >> 3;  // query half, first 8-query chunk in it
     const int kl = q * 32 + lane;            // key row of the tile = TMEM lane
     const int kg = kt * 128 + kl;
@@ -618,8 +621,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
       // conversion and the block's mask rows are in place
       ok = wait_bar_warp(bar(C::B_KVFULL), bi & 1, ab);
       if (!ok) break;
-      convert_to_f16(sm + C::OFF_K, nb * C::TILE, tid, C::NEWT + C::NCVT);
-      convert_to_f16(sm + C::OFF_V, nb * C::TILE, tid, C::NEWT + C::NCVT);
+      convert_to_f16(sm + C::OFF_K, nb * C::TILE, ew, C::NEWT + C::NCVT);
+      convert_to_f16(sm + C::OFF_V, nb * C::TILE, ew, C::NEWT + C::NCVT);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(C::B_KVREADY));
@@ -779,7 +782,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
             if (lane == 0) bulk_wait_group_read<1>();
             __syncwarp();
           }
-          const uint32_t piece = sb0 + C::OFF_DS + (warp * 2 + (il & 1)) * (32 * C::ROWB);
+          const uint32_t piece = sb0 + C::OFF_DS + (ewarp * 2 + (il & 1)) * (32 * C::ROWB);
 #pragma unroll
           for (int c = 0; c < HD / 8; ++c)
             asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(piece + lane * C::ROWB + ((c ^ swz) << 4)),
@@ -799,7 +802,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
       mbar_arrive(bar(C::B_DKVREAD));
     }
   }
-  if (warp < C::NEW && lane == 0) bulk_wait_group<0>();  // the dK, dV stores have been performed
+  if (warp >= C::WARP_EW0 && lane == 0) bulk_wait_group<0>();  // the dK, dV stores have been performed
   tc_fence_before();
   __syncthreads();
   cluster_sync_all();  // no CTA leaves while a peer may still write or read its shared memory

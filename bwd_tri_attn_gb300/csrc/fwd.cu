@@ -22,14 +22,14 @@
 // itself. V is converted BF16 -> FP16 in shared memory (exact in FP16 range) by
 // the softmax threads, a slice of the tile each, before they hand P over.
 //
-// Warp roles (384 threads): warps 0-7 = softmax, one thread per query row (TMEM
-// lane) over all 128 keys of a tile; warpgroup 0 takes the slices il = 0, 2, ...
-// and warpgroup 1 the slices il = 1, 3, ... of every key tile, so the two work on
-// different S tiles at once and never wait on each other inside a key tile.
-// Warp 8 = producer (TMA for Q, K, V and the bias tiles, bulk copies of the mask
-// rows and their per-tile "nonzero" flags), warp 9 = P.V issuer + TMEM owner,
-// warp 10 = S issuer, warp 11 only donates registers (setmaxnreg: 216 per
-// softmax thread).
+// Warp roles (384 threads): warp 0 = producer (TMA for Q, K, V and the bias
+// tiles, bulk copies of the mask rows and their per-tile "nonzero" flags),
+// warp 1 = P.V issuer + TMEM owner, warp 2 = S issuer, warp 3 only donates
+// registers; warps 4-11 = softmax, one thread per query row (TMEM lane) over all
+// 128 keys of a tile: softmax warpgroup 0 (warps 4-7) takes the slices
+// il = 0, 2, ... and softmax warpgroup 1 (warps 8-11) the slices il = 1, 3, ...
+// of every key tile, so the two work on different S tiles at once and never
+// wait on each other inside a key tile (setmaxnreg: 216 per softmax thread).
 // TMEM columns: three S buffers [0,128) [128,256) [256,384), with P written as
 // FP16 pairs over the columns the thread has already read (keys 0-63 -> cols
 // 0-31, keys 64-127 -> cols 64-95 of the buffer); O_i at 384 + i*d.
@@ -90,7 +90,9 @@ struct FwdCfg {
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // [0] TMEM base, [1] abort flag
   static constexpr int SMEM_ALLOC = OFF_MISC + 16 + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr int NSOFT = 8, WARP_TMA = 8, WARP_MMA = 9, WARP_S = 10, NTHREADS = 384;  // warp 11: register donor
+  // the control warps take the lowest warp indices (warpgroup 0): warp schedulers favour low-index
+  // warps, and these warps' short instruction sequences gate everyone else's progress
+  static constexpr int WARP_TMA = 0, WARP_MMA = 1, WARP_S = 2, WARP_SOFT0 = 4, NTHREADS = 384;  // warp 3: donor
   // setmaxnreg split: the softmax warpgroups take registers from the third warpgroup (per SMSP:
   // two softmax warps and one other warp share 16K registers)
   static constexpr uint32_t REG_LAUNCH = 168, REG_SOFT = 216, REG_OTHER = 72;
@@ -304,7 +306,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
     }
   } else if (warp == C::WARP_MMA || warp == C::WARP_S) {
     // ------------------------------------------------------------ MMA issuers
-    // Warp 10 issues S = Q K^T, warp 9 P.V, each walking the CTA's tiles in order (units
+    // Warp 2 issues S = Q K^T, warp 1 P.V, each walking the CTA's tiles in order (units
     // blockIdx.x, +gridDim.x, ...; in a unit key tile kt, then slice il) with blocking waits on
     // exactly the barriers that gate its next MMA. Each warp runs converged; elect.sync picks
     // the lane that issues. A commit covers the MMAs of the issuing thread only, so every
@@ -368,14 +370,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
     mma_commit_e(drain);  // lands once every MMA this warp issued has completed
     if (lane == 0) drain_bar(drain, 0);
     __syncwarp();
-  } else if (warp < C::NSOFT) {
-    // ------------------------------------------------------------ softmax / epilogue (warps 0-7)
+  } else if (warp >= C::WARP_SOFT0) {
+    // ------------------------------------------------------------ softmax / epilogue (warps 4-11)
     reg_alloc<C::REG_SOFT>();
     // One thread per query row (TMEM lane); warpgroup wg = warp / 4 takes the slices
     // il = wg, wg + 2, ... of every key tile, so the two warpgroups work on different
     // S tiles at the same time and never wait on each other within a key tile.
     constexpr int NL = C::GF / 2;  // slices per warpgroup
-    const int q = warp & 3, wg = warp >> 2, wtid = tid & 127;
+    const int q = warp & 3, wg = (warp - C::WARP_SOFT0) >> 2, wtid = tid & 127;
     const int row = q * 32 + lane;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     const float2 sc2 = make_float2(g.scale, g.scale), l2e2 = make_float2(kLog2e, kLog2e);
@@ -667,7 +669,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
     }
     cp_async_wait_all();
   } else {
-    reg_dealloc<C::REG_OTHER>();  // warp 11 only donates registers
+    reg_dealloc<C::REG_OTHER>();  // warp 3 only donates registers
   }
   tc_fence_before();
   __syncthreads();
