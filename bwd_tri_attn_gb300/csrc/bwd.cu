@@ -7,8 +7,8 @@
 // and uses ordered partial reductions, with no floating-point atomics and no
 // full score-gradient storage.
 //
-// Work unit (one CTA): batch b, head h, key tile kt (128 keys), and a
-// "supergroup" of consecutive slices, walked in blocks of GB slices:
+// Work unit (one CTA): key tile kt (128 keys) of a contiguous range of (head, slice) pairs (the
+// range of the CTA's cluster, below), walked head by head in blocks of GB slices:
 //     for block: for query tile jt: for slice i in block:     (one "step")
 //         S^T  = K_i Q_i[jt]^T        (TMEM, lanes = keys)
 //         dP^T = V_i dO_i[jt]^T
@@ -17,20 +17,21 @@
 //         dV_i += P^T dO_i[jt],  dK_i += dS^T Q_i[jt]            (TMEM accumulators, one pair per slice of the block)
 //         dQ_i[jt] partial = dS K_i                               (reduced across the cluster, below)
 //         dBias tile (jt, kt) += dS   (registers, summed in slice order over the block)
-//     after each (block, jt): the dBias tile is added into the supergroup's FP32 partial (this CTA owns it)
+//     after each (block, jt): the dBias tile is added into the cluster's FP32 partial slot for the head
+//     (this CTA owns the tile)
 //     after each block: dK_i, dV_i -> BF16
 //
 // Three reductions, each in a fixed order:
 //  - dK, dV over query tiles: in the CTA's TMEM accumulator, jt = 0, 1, ...
-//  - dQ over key tiles: the n = N/128 CTAs of one (b, h, supergroup) form a
+//  - dQ over key tiles: the n = N/128 CTAs of one key-tile row form a
 //    thread-block cluster. CTA r owns query rows [r*128/n, (r+1)*128/n) of every
 //    step's tile; each CTA pushes the matching rows of its 128 x d FP32 partial
 //    into the owner's receive buffer with st.async (completing bytes on the
 //    owner's mbarrier), and the owner sums the n partials in rank (= kt) order,
 //    one step later so that the exchange overlaps the next step's work.
 //  - dBias over slices: within a block in slice order (registers), across blocks in
-//    block order (the partial), across supergroups in supergroup order (reduce kernel).
-// Every order depends on the shape (and, for the supergroup count, the GPU model) only.
+//    block order (the partial slot), across the slots of a head in slot order (reduce kernel).
+// Every order depends on the shape and the number of resident clusters (the GPU model) only.
 //
 // Operands: all tensor-core operands are FP16 (Q, K, V, dO converted in shared
 // memory, exact in the FP16 range); P and dS need FP16's 11-bit significand.

@@ -147,12 +147,13 @@ int tri_attn_device_status(void *stream);
  * until the process exits. The call itself allocates nothing.
  *
  * Arguments, layouts and outputs are exactly those of tri_attn_bwd minus the
- * workspace. The slice supergroups (dBias partials) are capped to what fits
- * in the array, so dBias may be summed in a different (still fixed) order than
- * tri_attn_bwd uses for the same shape; the results agree within rounding.
+ * workspace. The work is spread over fewer clusters when the dBias partial
+ * slots of the full split do not fit in the array, so dBias may be summed in a
+ * different (still fixed) order than tri_attn_bwd uses for the same shape, and
+ * the call is slower; the results agree within rounding.
  * Returns TRI_ATTN_ERR_STATIC_TOO_SMALL, before enqueuing anything, when even
- * one partial does not fit (B = 1, H = 4, S = N = 768 fits with two partials;
- * S = N = 1024 does not).
+ * one slot per head does not fit (B = 1, H = 4, S = N = 768 fits with two slots
+ * per head; S = N = 1024 does not).
  *
  * Set-up: the first call on each device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current); make that first call before
