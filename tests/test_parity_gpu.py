@@ -80,6 +80,44 @@ def test_fully_masked_slice():
     _compare_all(got, want, "fully_masked_slice")
 
 
+@pytest.mark.parametrize("d", [16, 32])
+def test_lazy_max_raised_in_later_key_tiles(d):
+    # a bias ramp over the keys lifts every key tile's row max by 6.4 over the previous one,
+    # more than the forward's lazy-max threshold (8 ln 2 = 5.5): each row's reference max is
+    # raised, and O rescaled in TMEM, at every key tile after the first
+    x = wl.make_inputs(B=1, S=6, N=512, H=2, d=d, seed=21, mask=("random", 0.05))
+    ramp = 0.05 * torch.arange(512, dtype=torch.float32)
+    x["bias"] = (x["bias"].float() + ramp).to(torch.bfloat16)
+    got = run_cuda(x)
+    want = oracle_full(x)
+    _compare_all(got, want, f"bias_ramp_d{d}")
+
+
+@pytest.mark.parametrize("d", [16, 32])
+def test_rows_without_visible_keys_in_first_key_tiles(d):
+    # slices whose first one or two key tiles are fully masked: the forward takes the row's
+    # reference max only from the first key tile that has a visible key
+    x = wl.make_inputs(B=1, S=5, N=300, H=2, d=d, seed=22, mask=("zeros",))
+    m = x["mask"].float()
+    m[:, 0, :128] = float("-inf")
+    m[:, 2, :128] = float("-inf")
+    m[:, 3, :256] = float("-inf")
+    x["mask"] = m.to(torch.bfloat16)
+    got = run_cuda(x)
+    want = oracle_full(x)
+    _compare_all(got, want, f"masked_first_tiles_d{d}")
+
+
+def test_ragged_slice_groups_across_units():
+    # more work units than SMs (4 x 2 x 4 x 6 = 192), with S = 7 not a multiple of the forward's
+    # slice group: a CTA walks units with four and with three slices in turn, so its per-slice Q
+    # buffers and per-warpgroup O barriers change how many slices they serve between units
+    x = wl.make_inputs(B=4, S=7, N=768, H=4, d=32, seed=23, mask=("tail", 20))
+    got = run_cuda(x)
+    want = oracle_full(x)
+    _compare_all(got, want, "ragged_units")
+
+
 def test_scale_argument_is_used():
     x = wl.make_inputs(B=1, S=4, N=64, H=2, d=16, seed=12, mask=("tail", 3))
     got = run_cuda(x, scale=0.37)
