@@ -115,6 +115,11 @@ class ClockSampler:
         with open(self.file.name) as f:
             rows = [r.strip().split(",") for r in f if r.strip()]
         os.unlink(self.file.name)
+        return self.parse(rows)
+
+    @staticmethod
+    def parse(rows):
+        """Median SM clock, max clock and the throttle reasons seen in nvidia-smi CSV rows."""
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in rows:
@@ -138,6 +143,24 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return world, rank, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest of every rank's value (the slowest rank's time); a no-op on one rank."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, flops_per_step: float, ms_per_step: float) -> float:
+    """Whole-job TFLOP/s: every rank runs the same step on its own data (weak scaling), and the
+    job's step time is the slowest rank's."""
+    return world * flops_per_step / (ms_per_step * 1e-3) / 1e12
 
 
 def cpu_oracle_sample(w, slices: int, nthreads: int = 0):
@@ -245,11 +268,7 @@ def run_ours(args, w):
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    elapsed_ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     assert tb.tri_attn_device_status() == 0
 
     per_kernel = {n: [] for n in KERNELS}
@@ -261,7 +280,7 @@ def run_ours(args, w):
 
     flops = w.flops()
     ms_per_step = elapsed_ms / K
-    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    value = job_throughput(world, flops, ms_per_step)
     peaks = load_peaks()
 
     # roofline of the dominant kernel (tensor-bound contraction; FP16 operands run at the BF16 rate)
@@ -337,13 +356,9 @@ def run_ours(args, w):
         ke = max(2, min(K, 10))
         e0, e1 = e2e_run(ke)
         torch.cuda.synchronize()
-        ems = e0.elapsed_time(e1) / ke
-        if world > 1:
-            t = torch.tensor([ems], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
+        ems = max_over_ranks(e0.elapsed_time(e1) / ke, world, dev)
         assert tb.tri_attn_device_status() == 0
-        e2e = {"value": world * flops / (ems * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        e2e = {"value": job_throughput(world, flops, ems), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": ems, "steps": ke,
                "pipelined": "two device buffer sets; H2D of step k+1 and D2H of step k-1 overlap step k"}
 
