@@ -21,12 +21,16 @@ _lock = threading.Lock()
 _lib = None
 
 
+NODE_STARTING, NODE_ENDING = 0, 1  # tri_attn_shape.node
+
+
 class Shape(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("S", ctypes.c_int), ("N", ctypes.c_int), ("H", ctypes.c_int),
-                ("d", ctypes.c_int), ("scale", ctypes.c_float)]
+                ("d", ctypes.c_int), ("scale", ctypes.c_float), ("node", ctypes.c_int)]
 
     def __repr__(self):
-        return f"Shape(B={self.B}, S={self.S}, N={self.N}, H={self.H}, d={self.d}, scale={self.scale})"
+        return (f"Shape(B={self.B}, S={self.S}, N={self.N}, H={self.H}, d={self.d}, scale={self.scale}, "
+                f"node={self.node})")
 
 
 class TriAttnError(RuntimeError):
@@ -76,9 +80,12 @@ def strerror(code: int) -> str:
     return load().tri_attn_strerror(int(code)).decode()
 
 
-def shape_of(Q: torch.Tensor, scale: float | None = None) -> Shape:
-    B, S, N, H, d = (int(x) for x in Q.shape)
-    return Shape(B, S, N, H, d, float(1.0 / math.sqrt(d) if scale is None else scale))
+def shape_of(Q: torch.Tensor, scale: float | None = None, node: int = NODE_STARTING) -> Shape:
+    """Shape of the attention on the pair tensor Q: [B, S, N, H, d] for the starting node (slices
+    along pair axis 1), [B, N, S, H, d] for the ending node (slices along pair axis 2)."""
+    B, P1, P2, H, d = (int(x) for x in Q.shape)
+    S, N = (P1, P2) if node == NODE_STARTING else (P2, P1)
+    return Shape(B, S, N, H, d, float(1.0 / math.sqrt(d) if scale is None else scale), int(node))
 
 
 def _p(t):
@@ -145,10 +152,11 @@ def tri_attn_set_timing_events(events) -> None:
 # Allocating conveniences (outputs are fresh torch tensors on Q's device).
 # ----------------------------------------------------------------------------
 
-def forward(Q, K, V, bias, mask=None, scale=None, residual=True, stream=None):
-    """Returns (O, LSE, Ores); Ores is None when ``residual`` is False."""
-    shape = shape_of(Q, scale)
-    B, S, N, H, d = Q.shape
+def forward(Q, K, V, bias, mask=None, scale=None, residual=True, stream=None, node=NODE_STARTING):
+    """Returns (O, LSE, Ores); Ores is None when ``residual`` is False. O and Ores have Q's
+    layout; LSE is [B, S, H, N] in terms of the attention's slices and positions."""
+    shape = shape_of(Q, scale, node)
+    B, S, N, H = shape.B, shape.S, shape.N, shape.H
     O = torch.empty_like(Q)
     LSE = torch.empty((B, S, H, N), dtype=torch.float32, device=Q.device)
     Ores = torch.empty_like(Q) if residual else None
@@ -161,9 +169,10 @@ def workspace_for(shape: Shape, device) -> torch.Tensor:
     return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
 
 
-def backward(Q, K, V, bias, mask, O, Ores, LSE, dO, scale=None, workspace=None, stream=None):
+def backward(Q, K, V, bias, mask, O, Ores, LSE, dO, scale=None, workspace=None, stream=None,
+             node=NODE_STARTING):
     """Returns (dQ, dK, dV, dBias)."""
-    shape = shape_of(Q, scale)
+    shape = shape_of(Q, scale, node)
     if workspace is None:
         workspace = workspace_for(shape, Q.device)
     dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)

@@ -38,6 +38,7 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 int check_shape(const tri_attn_shape &s) {
   if (s.B < 1 || s.S < 1 || s.N < 1 || s.H < 1 || !isfinite(s.scale)) return TRI_ATTN_ERR_INVALID_ARG;
+  if (s.node != TRI_ATTN_NODE_STARTING && s.node != TRI_ATTN_NODE_ENDING) return TRI_ATTN_ERR_INVALID_ARG;
   if (s.d != 16 && s.d != 32) return TRI_ATTN_ERR_UNSUPPORTED;
   if (s.N > TRI_ATTN_MAX_N) return TRI_ATTN_ERR_UNSUPPORTED;
   // grid dimensions and 32-bit tile coordinates
@@ -45,7 +46,7 @@ int check_shape(const tri_attn_shape &s) {
   return TRI_ATTN_OK;
 }
 
-Dims to_dims(const tri_attn_shape &s) { return Dims{s.B, s.S, s.N, s.H, s.d, s.scale}; }
+Dims to_dims(const tri_attn_shape &s) { return Dims{s.B, s.S, s.N, s.H, s.d, s.scale, s.node}; }
 
 // Backward workspace: the FP32 correction D [B,S,H,N], the transposed and
 // tile-padded BF16 bias [B*H][NP][NP] (NP = N rounded up to 128), and the FP32
@@ -107,7 +108,7 @@ extern "C" {
 const char *tri_attn_strerror(int code) {
   switch (code) {
     case TRI_ATTN_OK: return "success";
-    case TRI_ATTN_ERR_INVALID_ARG: return "invalid argument (NULL pointer, non-positive size or non-finite scale)";
+    case TRI_ATTN_ERR_INVALID_ARG: return "invalid argument (NULL pointer, non-positive size, non-finite scale or unknown node)";
     case TRI_ATTN_ERR_UNSUPPORTED: return "unsupported configuration (d must be 16 or 32, N <= TRI_ATTN_MAX_N, pointers 16-byte aligned)";
     case TRI_ATTN_ERR_WORKSPACE: return "workspace missing or smaller than tri_attn_bwd_workspace_size()";
     case TRI_ATTN_ERR_CUDA: return "CUDA runtime error";

@@ -181,7 +181,7 @@ struct Sched {
   }
 };
 
-template <int HD>
+template <int HD, int NODE>
 __global__ void __launch_bounds__(BwdCfg<HD>::NTHREADS, 1)
 bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
            const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mDO,
@@ -291,10 +291,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
           __syncwarp();
           if (lane == 0) {
             mbar_arrive_expect_tx(bar(C::B_QDOFULL + st), 2 * C::TILE);
-            tma_load_4d_hint(sb0 + C::OFF_Q + st * C::TILE, &mQ, bar(C::B_QDOFULL + st), 0, h, jt * 128, b * g.S + i,
-                             stream_pol);
-            tma_load_4d_hint(sb0 + C::OFF_DO + st * C::TILE, &mDO, bar(C::B_QDOFULL + st), 0, h, jt * 128,
-                             b * g.S + i, stream_pol);
+            load_rows_hint(sb0 + C::OFF_Q + st * C::TILE, &mQ, bar(C::B_QDOFULL + st), NODE, h, b, g.S, i, jt * 128,
+                           stream_pol);
+            load_rows_hint(sb0 + C::OFF_DO + st * C::TILE, &mDO, bar(C::B_QDOFULL + st), NODE, h, b, g.S, i, jt * 128,
+                           stream_pol);
           }
           if (jt == 0 && il == 0) {
             // K_i, V_i of the block (single-buffered: the previous block's MMAs must be done)
@@ -303,10 +303,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
             if (lane == 0) {
               mbar_arrive_expect_tx(bar(C::B_KVFULL), 2 * nb * C::TILE);
               for (int q = 0; q < nb; ++q) {
-                tma_load_4d_hint(sb0 + C::OFF_K + q * C::TILE, &mK, bar(C::B_KVFULL), 0, h, kt * 128, b * g.S + i0 + q,
-                                 stream_pol);
-                tma_load_4d_hint(sb0 + C::OFF_V + q * C::TILE, &mV, bar(C::B_KVFULL), 0, h, kt * 128, b * g.S + i0 + q,
-                                 stream_pol);
+                load_rows_hint(sb0 + C::OFF_K + q * C::TILE, &mK, bar(C::B_KVFULL), NODE, h, b, g.S, i0 + q, kt * 128,
+                               stream_pol);
+                load_rows_hint(sb0 + C::OFF_V + q * C::TILE, &mV, bar(C::B_KVFULL), NODE, h, b, g.S, i0 + q, kt * 128,
+                               stream_pol);
               }
             }
             kv_issued = bi + 1;
@@ -540,7 +540,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
         if (j < g.N) {
           const uint2 w = make_uint2(
               pack_bf16x2(s4.x * g.scale, s4.y * g.scale), pack_bf16x2(s4.z * g.scale, s4.w * g.scale));
-          *reinterpret_cast<uint2 *>(dQ + pos_row(g, prev_hd / g.H, prev_i, j) * g.H * HD + (prev_hd % g.H) * HD +
+          *reinterpret_cast<uint2 *>(dQ + pos_row(g, prev_hd / g.H, prev_i, j, NODE) * g.H * HD + (prev_hd % g.H) * HD +
                                      c * 4) = w;
         }
       }
@@ -792,7 +792,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_4d(mo, piece, 0, h, kt * 128 + q * 32, b * g.S + i0 + il);
+            store_rows(mo, piece, NODE, h, b, g.S, i0 + il, kt * 128 + q * 32);
             bulk_commit_group();
           }
         }
@@ -900,18 +900,19 @@ cudaError_t launch_bwd_main_t(const Dims &g, const BwdSplit &sp, const uint16_t 
   if (e == cudaSuccess) e = make_rows_map(&mdo, dO, g, 128);
   if (e == cudaSuccess) e = make_square_map(&mbt, biasT, NP, g.B * g.H);
   if (e != cudaSuccess) return e;
-  static bool attr = false;
-  if (!attr) {
-    e = cudaFuncSetAttribute(bwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+  auto *kern = g.node ? bwd_kernel<HD, 1> : bwd_kernel<HD, 0>;
+  static bool attr[2] = {false, false};
+  if (!attr[g.node ? 1 : 0]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     // The setmaxnreg split moves registers between warpgroups within the block's
     // launch allocation; it only balances if the kernel was built with exactly
     // REG_LAUNCH registers per thread, so refuse to launch otherwise.
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, bwd_kernel<HD>);
+    e = cudaFuncGetAttributes(&fa, kern);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != (int)C::REG_LAUNCH) return cudaErrorInvalidConfiguration;
-    attr = true;
+    attr[g.node ? 1 : 0] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(nkt, sp.NC, 1);
@@ -925,7 +926,7 @@ cudaError_t launch_bwd_main_t(const Dims &g, const BwdSplit &sp, const uint16_t 
   attrs[0].val.clusterDim.z = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, bwd_kernel<HD>, mq, mk, mv, mdo, mbt, mdk, mdv, g, sp.NC, sp.KMAX, LSE, Dv, mask,
+  return cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mdo, mbt, mdk, mdv, g, sp.NC, sp.KMAX, LSE, Dv, mask,
                             dQ, dK, dV, partial, status);
 }
 
@@ -982,7 +983,8 @@ int bwd_resident_clusters_t(const Dims &g) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev > 64) return 1;
   int n = cache[dev][nkt];
   if (n == 0) {
-    if (cudaFuncSetAttribute(bwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) !=
+    // (both node instantiations have the same resources: the starting-node one stands for them)
+    if (cudaFuncSetAttribute(bwd_kernel<HD, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) !=
         cudaSuccess)
       return 1;
     cudaLaunchConfig_t cfg = {};
@@ -996,7 +998,7 @@ int bwd_resident_clusters_t(const Dims &g) {
     attrs[0].val.clusterDim.z = 1;
     cfg.attrs = attrs;
     cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&n, bwd_kernel<HD>, &cfg) != cudaSuccess || n < 1) n = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, bwd_kernel<HD, 0>, &cfg) != cudaSuccess || n < 1) n = 1;
     cache[dev][nkt] = n;
   }
   return n;

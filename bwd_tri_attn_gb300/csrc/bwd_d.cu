@@ -76,7 +76,16 @@ bwd_d_kernel(Dims g, const uint4 *__restrict__ dO, const uint4 *__restrict__ O,
     const int pl = t % kDPosPerBlock, h = t / kDPosPerBlock;
     const int64_t p = p0 + pl;
     if (p < positions) {
-      const int64_t bi = p / g.N, j = p % g.N;
+      // memory row p -> (b * S + slice i) and position j; the ending node stores slices innermost
+      int64_t bi, j;
+      if (!g.node) {
+        bi = p / g.N;
+        j = p % g.N;
+      } else {
+        const int64_t sn = (int64_t)g.S * g.N, b = p / sn, r = p % sn;
+        bi = b * g.S + r % g.S;
+        j = r / g.S;
+      }
       Dout[(bi * g.H + h) * g.N + j] = sD[pl * g.H + h];
     }
   }

@@ -56,6 +56,7 @@ extern "C" int tri_attn_bwd_static(tri_attn_shape s, const tri_attn_bf16 *Q, con
                                    const tri_attn_bf16 *dO, tri_attn_bf16 *dQ, tri_attn_bf16 *dK, tri_attn_bf16 *dV,
                                    tri_attn_bf16 *dBias, void *stream) {
   if (s.B < 1 || s.S < 1 || s.N < 1 || s.H < 1 || !isfinite(s.scale)) return TRI_ATTN_ERR_INVALID_ARG;
+  if (s.node != TRI_ATTN_NODE_STARTING && s.node != TRI_ATTN_NODE_ENDING) return TRI_ATTN_ERR_INVALID_ARG;
   if ((s.d != 16 && s.d != 32) || s.N > TRI_ATTN_MAX_N) return TRI_ATTN_ERR_UNSUPPORTED;
   if ((int64_t)s.B * s.S > 65535 || (int64_t)s.B * s.H * s.S > (1ll << 30)) return TRI_ATTN_ERR_UNSUPPORTED;
   if (!Q || !K || !V || !bias || !O || !LSE || !dO || !dQ || !dK || !dV || !dBias) return TRI_ATTN_ERR_INVALID_ARG;
@@ -64,7 +65,7 @@ extern "C" int tri_attn_bwd_static(tri_attn_shape s, const tri_attn_bf16 *Q, con
     if (p && !aligned16(p)) return TRI_ATTN_ERR_UNSUPPORTED;
 
   // scratch layout: D [B,S,H,N] FP32 | transposed bias [B*H][NP][NP] BF16 | dBias partials [B*H][slots][NP][NP] FP32
-  const Dims g{s.B, s.S, s.N, s.H, s.d, s.scale};
+  const Dims g{s.B, s.S, s.N, s.H, s.d, s.scale, s.node};
   const size_t NP = (size_t)(s.N + 127) / 128 * 128;
   const size_t d_bytes = align_up(sizeof(float) * (size_t)s.B * s.S * s.H * s.N);
   const size_t bt_bytes = align_up(2 * (size_t)s.B * s.H * NP * NP);

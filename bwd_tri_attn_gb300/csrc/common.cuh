@@ -10,17 +10,21 @@
 
 namespace triattn {
 
-// Problem description passed by value to every kernel.
+// Problem description passed by value to every kernel. node: 0 = starting node (pair tensors
+// [B,S,N,H,d]: slices along pair axis 1), 1 = ending node (pair tensors [B,N,S,H,d]: slices
+// along pair axis 2).
 struct Dims {
   int B, S, N, H, d;
   float scale;
+  int node;
 };
 
-// Row index of position n of slice (b, i) in the [B*S*N, H*d] view of a
-// [B,S,N,H,d] tensor.
-__host__ __device__ inline int64_t pos_row(const Dims &g, int b, int i, int n) {
-  return ((int64_t)b * g.S + i) * g.N + n;
+// Row index of position n of slice (b, i) in the [rows, H*d] view of a pair tensor of the given
+// node (kernels pass it as a compile-time constant).
+__host__ __device__ inline int64_t pos_row(const Dims &g, int b, int i, int n, int node) {
+  return (int64_t)b * g.S * g.N + (node ? (int64_t)n * g.S + i : (int64_t)i * g.N + n);
 }
+
 
 __device__ __forceinline__ float bf16_to_f32(uint16_t v) {
   return __uint_as_float(((uint32_t)v) << 16);

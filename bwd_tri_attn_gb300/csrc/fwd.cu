@@ -126,7 +126,7 @@ __device__ __forceinline__ FwdUnit fwd_unit(const Dims &g, int u) {
   return w;
 }
 
-template <int HD>
+template <int HD, int NODE>
 __global__ void __launch_bounds__(FwdCfg<HD>::NTHREADS, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
            const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mB, const Dims g,
@@ -274,7 +274,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
           if (!ok) break;
           if (lane == 0) {
             mbar_arrive_expect_tx(bar(C::B_Q + t), C::TILE);
-            tma_load_4d(sb0 + C::OFF_Q + t * C::TILE, &mQ, bar(C::B_Q + t), 0, w.h, w.jt * 128, w.b * g.S + w.i0 + t);
+            load_rows(sb0 + C::OFF_Q + t * C::TILE, &mQ, bar(C::B_Q + t), NODE, w.h, w.b, g.S, w.i0 + t, w.jt * 128);
           }
           qcur |= 1u << t;
         }
@@ -284,10 +284,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
         if (lane == 0) {
           const int kt = t / w.ng, il = t % w.ng;
           mbar_arrive_expect_tx(bar(C::B_KVFULL + st), 2 * C::TILE);
-          tma_load_4d(sb0 + C::OFF_K + st * C::TILE, &mK, bar(C::B_KVFULL + st), 0, w.h, kt * 128,
-                      w.b * g.S + w.i0 + il);
-          tma_load_4d(sb0 + C::OFF_V + st * C::TILE, &mV, bar(C::B_KVFULL + st), 0, w.h, kt * 128,
-                      w.b * g.S + w.i0 + il);
+          load_rows(sb0 + C::OFF_K + st * C::TILE, &mK, bar(C::B_KVFULL + st), NODE, w.h, w.b, g.S, w.i0 + il, kt * 128);
+          load_rows(sb0 + C::OFF_V + st * C::TILE, &mV, bar(C::B_KVFULL + st), NODE, w.h, w.b, g.S, w.i0 + il, kt * 128);
         }
       }
     }
@@ -650,7 +648,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
           ob[c] = pack_bf16x2(o0, o1);
           rb[c] = pack_bf16x2(o0 - __uint_as_float(ob[c] << 16), o1 - __uint_as_float(ob[c] & 0xffff0000u));
         }
-        const int64_t off = pos_row(g, b, i, j) * g.H * HD + (int64_t)h * HD;
+        const int64_t off = pos_row(g, b, i, j, NODE) * g.H * HD + (int64_t)h * HD;
         // the row: 64 bytes (d = 32) or 32 bytes (d = 16), 32-byte stores
 #pragma unroll
         for (int c = 0; c < HD / 16; ++c) {
@@ -695,17 +693,18 @@ cudaError_t launch_fwd_t(const Dims &g, const uint16_t *Q, const uint16_t *K, co
   } else {
     memset(&mb, 0, sizeof(mb));  // unused: the kernel stages the bias itself
   }
-  static bool attr = false;
-  if (!attr) {
-    e = cudaFuncSetAttribute(fwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+  auto *kern = g.node ? fwd_kernel<HD, 1> : fwd_kernel<HD, 0>;
+  static bool attr[2] = {false, false};
+  if (!attr[g.node ? 1 : 0]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     // the setmaxnreg split only balances if the kernel was built with exactly REG_LAUNCH
     // registers per thread, so refuse to launch otherwise
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, fwd_kernel<HD>);
+    e = cudaFuncGetAttributes(&fa, kern);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != (int)C::REG_LAUNCH) return cudaErrorInvalidConfiguration;
-    attr = true;
+    attr[g.node ? 1 : 0] = true;
   }
   // persistent: one CTA per resident slot, each walking units blockIdx.x, +gridDim.x, ...
   static int slots[65];
@@ -717,13 +716,13 @@ cudaError_t launch_fwd_t(const Dims &g, const uint16_t *Q, const uint16_t *K, co
     int nsm = 0, per = 0;
     e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess)
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, fwd_kernel<HD>, C::NTHREADS, C::SMEM_ALLOC);
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kern, C::NTHREADS, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     slots[dev] = max(1, nsm * per);
   }
   const int nunits = g.B * ((g.S + C::GF - 1) / C::GF) * g.H * ((g.N + 127) / 128);
   const int grid = min(nunits, slots[dev]);
-  fwd_kernel<HD><<<grid, C::NTHREADS, C::SMEM_ALLOC, stream>>>(mq, mk, mv, mb, g, bias, mask, O, LSE, Ores, status);
+  kern<<<grid, C::NTHREADS, C::SMEM_ALLOC, stream>>>(mq, mk, mv, mb, g, bias, mask, O, LSE, Ores, status);
   return cudaGetLastError();
 }
 

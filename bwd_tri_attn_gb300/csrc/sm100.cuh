@@ -101,6 +101,15 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1,
+                                            int c2, int c3, int c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6, "
+      "%7}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1,
                                             int c2) {
   asm volatile(
@@ -127,6 +136,14 @@ __device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const CUtensorMap
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(policy)
       : "memory");
 }
+__device__ __forceinline__ void tma_load_5d_hint(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1,
+                                                 int c2, int c3, int c4, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, "
+      "%4, %5, %6, %7}], [%2], %8;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "l"(policy)
+      : "memory");
+}
 // Per-warpgroup register reallocation (setmaxnreg): the warpgroup's registers per thread become
 // R; the shares of all warpgroups must add up to the block's launch allocation.
 template <uint32_t R>
@@ -145,6 +162,39 @@ __device__ __forceinline__ void tma_store_4d(const CUtensorMap *map, uint32_t sr
                    reinterpret_cast<uint64_t>(map)),
                "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
                : "memory");
+}
+__device__ __forceinline__ void tma_store_5d(const CUtensorMap *map, uint32_t src, int c0, int c1, int c2, int c3,
+                                             int c4) {
+  asm volatile("cp.async.bulk.tensor.5d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5, %6}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+               : "memory");
+}
+// Box of positions [n0, n0 + rows) of slice i, batch b, head h of a pair tensor through its
+// make_rows_map view (4-D for the starting node, 5-D for the ending node). node is warp-uniform.
+__device__ __forceinline__ void load_rows(uint32_t dst, const CUtensorMap *map, uint32_t bar, int node, int h,
+                                          int b, int S, int i, int n0) {
+  if (node) {
+    tma_load_5d(dst, map, bar, 0, h, i, n0, b);
+  } else {
+    tma_load_4d(dst, map, bar, 0, h, n0, b * S + i);
+  }
+}
+__device__ __forceinline__ void load_rows_hint(uint32_t dst, const CUtensorMap *map, uint32_t bar, int node, int h,
+                                               int b, int S, int i, int n0, uint64_t policy) {
+  if (node) {
+    tma_load_5d_hint(dst, map, bar, 0, h, i, n0, b, policy);
+  } else {
+    tma_load_4d_hint(dst, map, bar, 0, h, n0, b * S + i, policy);
+  }
+}
+__device__ __forceinline__ void store_rows(const CUtensorMap *map, uint32_t src, int node, int h, int b, int S, int i,
+                                           int n0) {
+  if (node) {
+    tma_store_5d(map, src, 0, h, i, n0, b);
+  } else {
+    tma_store_4d(map, src, 0, h, n0, b * S + i);
+  }
 }
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until at most N of this thread's bulk groups still read shared memory.

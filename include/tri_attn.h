@@ -17,7 +17,10 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  * - Tensors are dense, row-major, on the current CUDA device:
- *     Q K V O Ores dO dQ dK dV : BF16 [B, S, N, H, d]   (S = number of slices)
+ *     Q K V O Ores dO dQ dK dV : BF16 pair tensors, [B, S, N, H, d] for the
+ *                                starting node (slices along pair axis 1),
+ *                                [B, N, S, H, d] for the ending node (slices
+ *                                along pair axis 2); S = number of slices
  *     bias dBias               : BF16 [B, H, N, N]
  *     mask                     : BF16 [B, S, N], additive (0 or -inf), may be NULL
  *     LSE                      : FP32 [B, S, H, N], natural-log log-sum-exp of the
@@ -39,8 +42,11 @@
  *   Kernels never trap: a bounded device-side wait that expires records
  *   TRI_ATTN_ERR_TIMEOUT in a device status word that
  *   tri_attn_device_status() reads.
- * - Ending-node attention is the same call on the pair tensor with its two
- *   pair axes swapped (the caller passes the transposed tensors).
+ * - Ending-node attention (attention along the pair tensor's first axis, one
+ *   slice per entry of its second axis) reads and writes the pair tensors in
+ *   place with shape.node = TRI_ATTN_NODE_ENDING: no transposed copies.
+ *   bias, mask, LSE and dBias keep the shapes above, in terms of the slices
+ *   and positions of the attention that runs.
  */
 #ifndef TRI_ATTN_H
 #define TRI_ATTN_H
@@ -57,18 +63,23 @@ typedef uint16_t tri_attn_bf16;
 
 #define TRI_ATTN_MAX_N 1024
 
+/* Which pair axis holds the slices (shape.node). */
+#define TRI_ATTN_NODE_STARTING 0 /* pair tensors [B, S, N, H, d] */
+#define TRI_ATTN_NODE_ENDING 1   /* pair tensors [B, N, S, H, d] */
+
 typedef struct tri_attn_shape {
     int B;       /* batch */
-    int S;       /* row-slices of the pair tensor (N for a square pair tensor) */
+    int S;       /* slices of the pair tensor (N for a square pair tensor) */
     int N;       /* positions attended over inside a slice */
     int H;       /* heads */
     int d;       /* head dimension: 16 or 32 */
     float scale; /* multiplies Q.K only (not the bias) */
+    int node;    /* TRI_ATTN_NODE_STARTING (0) or TRI_ATTN_NODE_ENDING (1) */
 } tri_attn_shape;
 
 enum {
     TRI_ATTN_OK = 0,
-    TRI_ATTN_ERR_INVALID_ARG = -1,  /* NULL where required, non-positive or non-finite sizes */
+    TRI_ATTN_ERR_INVALID_ARG = -1,  /* NULL where required, non-positive or non-finite sizes, bad node */
     TRI_ATTN_ERR_UNSUPPORTED = -2,  /* d not 16/32, N above the limit, misaligned pointer */
     TRI_ATTN_ERR_WORKSPACE = -3,    /* workspace NULL or smaller than tri_attn_bwd_workspace_size */
     TRI_ATTN_ERR_CUDA = -4,         /* a CUDA runtime/driver call or launch failed */

@@ -24,19 +24,32 @@ def to_device(x: dict, device="cuda") -> dict:
     return {k: (None if v is None else v.to(device).contiguous()) for k, v in x.items()}
 
 
-def run_cuda(x: dict, residual=True, scale=None, workspace=None):
-    """One forward + backward through the C ABI; returns CPU tensors."""
+PAIR = ("Q", "K", "V", "dO", "O", "Ores", "dQ", "dK", "dV")  # tensors laid out as pair tensors
+
+
+def run_cuda(x: dict, residual=True, scale=None, workspace=None, node=0):
+    """One forward + backward through the C ABI; returns CPU tensors.
+
+    ``x`` is in the attention's own terms ([B, S, N, H, d] activations). With node = 1 the
+    activations are handed to the library as ending-node pair tensors ([B, N, S, H, d], slices
+    along the second pair axis) and its outputs are mapped back, so results compare directly.
+    """
     from bwd_tri_attn_gb300 import binding as tb
 
     dx = to_device(x)
-    O, LSE, Ores = tb.forward(dx["Q"], dx["K"], dx["V"], dx["bias"], dx["mask"], scale=scale, residual=True)
+    if node:
+        dx = {k: (v.transpose(1, 2).contiguous() if k in PAIR else v) for k, v in dx.items()}
+    O, LSE, Ores = tb.forward(dx["Q"], dx["K"], dx["V"], dx["bias"], dx["mask"], scale=scale, residual=True,
+                              node=node)
     dQ, dK, dV, dBias = tb.backward(dx["Q"], dx["K"], dx["V"], dx["bias"], dx["mask"], O,
                                     Ores if residual else None, LSE, dx["dO"], scale=scale,
-                                    workspace=workspace)
+                                    workspace=workspace, node=node)
     torch.cuda.synchronize()
     assert tb.tri_attn_device_status() == 0
     out = dict(O=O, LSE=LSE, Ores=Ores, dQ=dQ, dK=dK, dV=dV, dBias=dBias)
-    return {k: v.cpu() for k, v in out.items()}
+    if node:
+        out = {k: (v.transpose(1, 2) if k in PAIR else v) for k, v in out.items()}
+    return {k: v.contiguous().cpu() for k, v in out.items()}
 
 
 def oracle_full(x: dict, scale=None):

@@ -76,6 +76,8 @@ GOOD = (1, 4, 64, 2, 32, 0.17677669)
     ((1, 4, 64, 2, 24, 0.1), -2),          # unsupported head dim
     ((1, 4, 64, 2, 64, 0.1), -2),
     ((1, 4, 1025, 2, 32, 0.1), -2),        # N above the limit
+    ((1, 4, 64, 2, 32, 0.1, 2), -1),       # unknown node
+    ((1, 4, 64, 2, 32, 0.1, -1), -1),
 ])
 def test_shape_validation(lib, shape, code):
     assert _fwd(lib, shape) == code
@@ -119,3 +121,11 @@ def test_workspace_size_depends_on_shape_only(lib):
 def test_timing_events_validation(lib):
     assert lib.tri_attn_set_timing_events(None, -1) == -1
     assert lib.tri_attn_set_timing_events(None, 0) == 0
+
+
+def test_workspace_size_same_for_both_nodes(lib):
+    from bwd_tri_attn_gb300.binding import Shape
+    lib.tri_attn_bwd_workspace_size.restype = ctypes.c_size_t
+    a = lib.tri_attn_bwd_workspace_size(Shape(1, 96, 200, 4, 32, 0.17677669, 0))
+    b = lib.tri_attn_bwd_workspace_size(Shape(1, 96, 200, 4, 32, 0.17677669, 1))
+    assert a == b > 0

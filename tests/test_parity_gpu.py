@@ -140,9 +140,9 @@ def test_residual_compensation_lowers_gradient_error():
     _compare_all(comp, want, "crop384")
 
 
-def _sampled_check(x, slices, bias_rows, what):
+def _sampled_check(x, slices, bias_rows, what, node=0):
     import oracle
-    got = run_cuda(x)
+    got = run_cuda(x, node=node)
     sub = {k: (v[:, slices] if (v is not None and k in ("Q", "K", "V", "dO", "mask")) else v)
            for k, v in x.items()}
     want = oracle_full(sub)
@@ -176,6 +176,35 @@ def test_ending_node_full_size():
         x[k] = wl.ending_node(x[k])
     N = wl.CROP768.N
     _sampled_check(x, [1, N // 2, N - 2], [(0, 1, 5), (0, 3, N - 1), (0, 0, 400)], "ending_node")
+
+
+def test_ending_node_in_place_full_size():
+    # the ending node on the pair tensors as they are in memory (slices along the second pair
+    # axis): no transposed copies
+    x = wl.inputs_for(wl.CROP768)
+    N = wl.CROP768.N
+    _sampled_check(x, [2, N // 2 + 3, N - 1], [(0, 2, 7), (0, 1, N - 1), (0, 3, 333)], "ending_node_in_place",
+                   node=1)
+
+
+ENDING = [
+    ("end_ragged_d32", dict(B=2, S=5, N=200, H=3, d=32, seed=31, mask=("random", 0.1))),
+    ("end_ragged_d16", dict(B=1, S=9, N=77, H=2, d=16, seed=32, mask=("tail", 7))),
+    ("end_tall_d32", dict(B=1, S=3, N=300, H=4, d=32, seed=33, mask=("zeros",))),
+    ("end_wide_d16", dict(B=2, S=40, N=24, H=1, d=16, seed=34, mask=("none",))),
+]
+
+
+@pytest.mark.parametrize("name,cfg", ENDING, ids=[e[0] for e in ENDING])
+def test_ending_node_in_place_full_oracle(name, cfg):
+    x = wl.make_inputs(**cfg)
+    got = run_cuda(x, node=1)
+    want = oracle_full(x)
+    _compare_all(got, want, name)
+    # the same attention through the starting-node layout gives the same bits
+    ref = run_cuda(x)
+    for k in ("O", "LSE", "Ores", "dQ", "dK", "dV", "dBias"):
+        assert torch.equal(got[k].view(torch.uint8), ref[k].view(torch.uint8)), f"{name}: {k} differs by layout"
 
 
 def test_bitwise_determinism_five_calls():
