@@ -4,7 +4,8 @@ One step = one pass of the whole path (forward, D correction, main backward,
 dBias reduction) over one batch of synthetic input of the named workload.
 Prints ONE JSON line on rank 0.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--node starting|ending]
+                  [--impl ours|reference]
 
 With N > 1 (torchrun, one process per GPU) every rank runs an independent
 replica of the workload (the path has no cross-GPU exchange at this size):
@@ -222,9 +223,12 @@ def run_ours(args, w):
     tb.load()
 
     x = wl.inputs_for(w)
+    node = tb.NODE_ENDING if args.node == "ending" else tb.NODE_STARTING
+    if node == tb.NODE_ENDING:  # the ending node's pair tensors hold the slices along the second pair axis
+        x = {k: (v.transpose(1, 2).contiguous() if k in ("Q", "K", "V", "dO") else v) for k, v in x.items()}
     d = {k: (None if v is None else v.to(dev)) for k, v in x.items()}
-    shape = tb.shape_of(d["Q"])
-    B, S, N, H, hd = d["Q"].shape
+    shape = tb.shape_of(d["Q"], node=node)
+    B, S, N, H, hd = shape.B, shape.S, shape.N, shape.H, shape.d
     O = torch.empty_like(d["Q"])
     Ores = torch.empty_like(d["Q"])
     LSE = torch.empty((B, S, H, N), dtype=torch.float32, device=dev)
@@ -374,7 +378,7 @@ def run_ours(args, w):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "S": w.slices, "N": w.N, "H": w.H, "d": w.d,
+            "config": {"workload": w.name, "B": w.B, "S": w.slices, "N": w.N, "H": w.H, "d": w.d, "node": args.node,
                        "mask": list(w.mask), "flops_per_step": flops,
                        "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB of inputs vs {L2_BYTES / 1e6:.0f} MB L2), no flush",
                        "operands": "BF16 in/out, FP16 tensor-core operands, FP32 accumulation"},
@@ -396,6 +400,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=wl.CROP768.name, choices=sorted(wl.ALL))
+    ap.add_argument("--node", choices=["starting", "ending"], default="starting",
+                    help="which pair axis holds the slices (the ending node reads the pair tensors in place)")
     ap.add_argument("--cpu-slices", type=int, default=64, help="slices in the timed CPU oracle sample")
     ap.add_argument("--ref-slices", type=int, default=4, help="slices per step of the reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
