@@ -40,7 +40,7 @@ int check_shape(const tri_attn_shape &s) {
   if (s.B < 1 || s.S < 1 || s.N < 1 || s.H < 1 || !isfinite(s.scale)) return TRI_ATTN_ERR_INVALID_ARG;
   if (s.node != TRI_ATTN_NODE_STARTING && s.node != TRI_ATTN_NODE_ENDING) return TRI_ATTN_ERR_INVALID_ARG;
   if (s.d != 16 && s.d != 32) return TRI_ATTN_ERR_UNSUPPORTED;
-  if (s.N > TRI_ATTN_MAX_N) return TRI_ATTN_ERR_UNSUPPORTED;
+  if (s.N > TRI_ATTN_MAX_N || s.H > TRI_ATTN_MAX_H) return TRI_ATTN_ERR_UNSUPPORTED;
   // grid dimensions and 32-bit tile coordinates
   if ((int64_t)s.B * s.S > 65535 || (int64_t)s.B * s.H * s.S > (1ll << 30)) return TRI_ATTN_ERR_UNSUPPORTED;
   return TRI_ATTN_OK;
@@ -109,7 +109,7 @@ const char *tri_attn_strerror(int code) {
   switch (code) {
     case TRI_ATTN_OK: return "success";
     case TRI_ATTN_ERR_INVALID_ARG: return "invalid argument (NULL pointer, non-positive size, non-finite scale or unknown node)";
-    case TRI_ATTN_ERR_UNSUPPORTED: return "unsupported configuration (d must be 16 or 32, N <= TRI_ATTN_MAX_N, pointers 16-byte aligned)";
+    case TRI_ATTN_ERR_UNSUPPORTED: return "unsupported configuration (d must be 16 or 32, N <= TRI_ATTN_MAX_N, H <= TRI_ATTN_MAX_H, pointers 16-byte aligned)";
     case TRI_ATTN_ERR_WORKSPACE: return "workspace missing or smaller than tri_attn_bwd_workspace_size()";
     case TRI_ATTN_ERR_CUDA: return "CUDA runtime error";
     case TRI_ATTN_ERR_TIMEOUT: return "a bounded device-side wait expired";

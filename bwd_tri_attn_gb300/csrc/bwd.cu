@@ -52,6 +52,7 @@
 // out of B, dP^T(t+1) may overwrite B; dQ = dS K reads dS from a 128-byte-swizzled FP16 tile in
 // shared memory. So the P phase of step t+1 overlaps step t's dK and dQ.
 #include "common.cuh"
+#include "launch.cuh"
 #include "sm100.cuh"
 #include "sync.cuh"
 #include "tmap.cuh"
@@ -901,8 +902,12 @@ cudaError_t launch_bwd_main_t(const Dims &g, const BwdSplit &sp, const uint16_t 
   if (e == cudaSuccess) e = make_square_map(&mbt, biasT, NP, g.B * g.H);
   if (e != cudaSuccess) return e;
   auto *kern = g.node ? bwd_kernel<HD, 1> : bwd_kernel<HD, 0>;
-  static bool attr[2] = {false, false};
-  if (!attr[g.node ? 1 : 0]) {
+  int dev = 0;
+  e = current_device(&dev);
+  if (e != cudaSuccess) return e;
+  static DeviceOnce ready[2];  // per node
+  DeviceOnce &once = ready[g.node ? 1 : 0];
+  if (!once.done(dev)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     // The setmaxnreg split moves registers between warpgroups within the block's
@@ -912,7 +917,7 @@ cudaError_t launch_bwd_main_t(const Dims &g, const BwdSplit &sp, const uint16_t 
     e = cudaFuncGetAttributes(&fa, kern);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != (int)C::REG_LAUNCH) return cudaErrorInvalidConfiguration;
-    attr[g.node ? 1 : 0] = true;
+    once.mark(dev);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(nkt, sp.NC, 1);
@@ -977,11 +982,11 @@ int bwd_slots_max(const Dims &g) {
 template <int HD>
 int bwd_resident_clusters_t(const Dims &g) {
   using C = BwdCfg<HD>;
-  static int cache[65][9];  // [device][cluster size]
+  static DeviceValue cache[9];  // [cluster size][device]
   const int nkt = (g.N + 127) / 128;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev > 64) return 1;
-  int n = cache[dev][nkt];
+  if (current_device(&dev) != cudaSuccess) return 1;
+  int n = cache[nkt].get(dev);
   if (n == 0) {
     // (both node instantiations have the same resources: the starting-node one stands for them)
     if (cudaFuncSetAttribute(bwd_kernel<HD, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) !=
@@ -999,7 +1004,7 @@ int bwd_resident_clusters_t(const Dims &g) {
     cfg.attrs = attrs;
     cfg.numAttrs = 1;
     if (cudaOccupancyMaxActiveClusters(&n, bwd_kernel<HD, 0>, &cfg) != cudaSuccess || n < 1) n = 1;
-    cache[dev][nkt] = n;
+    cache[nkt].set(dev, n);
   }
   return n;
 }

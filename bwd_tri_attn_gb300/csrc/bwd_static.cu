@@ -57,7 +57,7 @@ extern "C" int tri_attn_bwd_static(tri_attn_shape s, const tri_attn_bf16 *Q, con
                                    tri_attn_bf16 *dBias, void *stream) {
   if (s.B < 1 || s.S < 1 || s.N < 1 || s.H < 1 || !isfinite(s.scale)) return TRI_ATTN_ERR_INVALID_ARG;
   if (s.node != TRI_ATTN_NODE_STARTING && s.node != TRI_ATTN_NODE_ENDING) return TRI_ATTN_ERR_INVALID_ARG;
-  if ((s.d != 16 && s.d != 32) || s.N > TRI_ATTN_MAX_N) return TRI_ATTN_ERR_UNSUPPORTED;
+  if ((s.d != 16 && s.d != 32) || s.N > TRI_ATTN_MAX_N || s.H > TRI_ATTN_MAX_H) return TRI_ATTN_ERR_UNSUPPORTED;
   if ((int64_t)s.B * s.S > 65535 || (int64_t)s.B * s.H * s.S > (1ll << 30)) return TRI_ATTN_ERR_UNSUPPORTED;
   if (!Q || !K || !V || !bias || !O || !LSE || !dO || !dQ || !dK || !dV || !dBias) return TRI_ATTN_ERR_INVALID_ARG;
   const void *ptrs[] = {Q, K, V, bias, mask, O, Ores, LSE, dO, dQ, dK, dV, dBias};

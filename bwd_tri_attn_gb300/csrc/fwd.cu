@@ -42,6 +42,7 @@
 // view) take a fallback where each softmax thread stages its own bias row one
 // key tile ahead with cp.async and the producer copies the mask rows lane by lane.
 #include "common.cuh"
+#include "launch.cuh"
 #include "sm100.cuh"
 #include "sync.cuh"
 #include "tmap.cuh"
@@ -694,8 +695,12 @@ cudaError_t launch_fwd_t(const Dims &g, const uint16_t *Q, const uint16_t *K, co
     memset(&mb, 0, sizeof(mb));  // unused: the kernel stages the bias itself
   }
   auto *kern = g.node ? fwd_kernel<HD, 1> : fwd_kernel<HD, 0>;
-  static bool attr[2] = {false, false};
-  if (!attr[g.node ? 1 : 0]) {
+  int dev = 0;
+  e = current_device(&dev);
+  if (e != cudaSuccess) return e;
+  static DeviceOnce ready[2];  // per node
+  DeviceOnce &once = ready[g.node ? 1 : 0];
+  if (!once.done(dev)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     // the setmaxnreg split only balances if the kernel was built with exactly REG_LAUNCH
@@ -704,24 +709,23 @@ cudaError_t launch_fwd_t(const Dims &g, const uint16_t *Q, const uint16_t *K, co
     e = cudaFuncGetAttributes(&fa, kern);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != (int)C::REG_LAUNCH) return cudaErrorInvalidConfiguration;
-    attr[g.node ? 1 : 0] = true;
+    once.mark(dev);
   }
   // persistent: one CTA per resident slot, each walking units blockIdx.x, +gridDim.x, ...
-  static int slots[65];
-  int dev = 0;
-  e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev > 64) return cudaErrorInvalidDevice;
-  if (slots[dev] == 0) {
+  // (both node instantiations have the same resources)
+  static DeviceValue slots;
+  int nslots = slots.get(dev);
+  if (nslots == 0) {
     int nsm = 0, per = 0;
     e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess)
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kern, C::NTHREADS, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    slots[dev] = max(1, nsm * per);
+    nslots = max(1, nsm * per);
+    slots.set(dev, nslots);
   }
   const int nunits = g.B * ((g.S + C::GF - 1) / C::GF) * g.H * ((g.N + 127) / 128);
-  const int grid = min(nunits, slots[dev]);
+  const int grid = min(nunits, nslots);
   kern<<<grid, C::NTHREADS, C::SMEM_ALLOC, stream>>>(mq, mk, mv, mb, g, bias, mask, O, LSE, Ores, status);
   return cudaGetLastError();
 }

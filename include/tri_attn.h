@@ -26,7 +26,8 @@
  *     LSE                      : FP32 [B, S, H, N], natural-log log-sum-exp of the
  *                                scores of each query row (-inf for a row whose
  *                                keys are all masked)
- * - Supported: d in {16, 32}; 1 <= N <= TRI_ATTN_MAX_N; B, S, H >= 1. scale is
+ * - Supported: d in {16, 32}; 1 <= N <= TRI_ATTN_MAX_N; 1 <= H <= TRI_ATTN_MAX_H;
+ *   B, S >= 1. scale is
  *   any finite float (1/sqrt(d) is the usual choice). Q, K, V, dO entries must
  *   have magnitude below 65504 (they are staged as FP16 tensor-core operands).
  * - Every device pointer must be 16-byte aligned (TMA requirement).
@@ -62,6 +63,7 @@ extern "C" {
 typedef uint16_t tri_attn_bf16;
 
 #define TRI_ATTN_MAX_N 1024
+#define TRI_ATTN_MAX_H 256
 
 /* Which pair axis holds the slices (shape.node). */
 #define TRI_ATTN_NODE_STARTING 0 /* pair tensors [B, S, N, H, d] */

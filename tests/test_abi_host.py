@@ -76,6 +76,7 @@ GOOD = (1, 4, 64, 2, 32, 0.17677669)
     ((1, 4, 64, 2, 24, 0.1), -2),          # unsupported head dim
     ((1, 4, 64, 2, 64, 0.1), -2),
     ((1, 4, 1025, 2, 32, 0.1), -2),        # N above the limit
+    ((1, 4, 64, 257, 32, 0.1), -2),        # H above the limit
     ((1, 4, 64, 2, 32, 0.1, 2), -1),       # unknown node
     ((1, 4, 64, 2, 32, 0.1, -1), -1),
 ])
