@@ -90,7 +90,7 @@ struct BwdCfg {
   static constexpr int OFF_BIAS = OFF_DO + NQS * TILE;     // [2 halves][128 rows][128 B], SW128
   static constexpr int OFF_DS = OFF_BIAS + BIAS_TILE;      // FP16 dS, MN-major SW128: [16 key groups][2][8][128 B]
   static constexpr int RB_SLOT = RB_ROWS * HD * 4;
-  static constexpr int NRB = 1;                            // dQ receive slots (step t uses slot t % NRB)
+  static constexpr int NRB = 2;                            // dQ receive slots (step t uses slot t % NRB)
   static constexpr int OFF_RB = OFF_DS + 32768;            // dQ receive buffers: NRB x [sender][row][HD] FP32
   static constexpr int OFF_LSE = OFF_RB + NRB * RB_SLOT;   // [NQS][128]: -LSE*log2e (or -inf)
   static constexpr int OFF_D = OFF_LSE + NQS * 512;          // [NQS][128]: D
