@@ -28,7 +28,9 @@
 //    step's tile; each CTA pushes the matching rows of its 128 x d FP32 partial
 //    into the owner's receive buffer with st.async (completing bytes on the
 //    owner's mbarrier), and the owner sums the n partials in rank (= kt) order,
-//    one step later so that the exchange overlaps the next step's work.
+//    one step later so that the exchange overlaps the next step's work. The
+//    receive buffer has two slots used by alternate steps, so a CTA can push step
+//    t while an owner is still summing step t - 1.
 //  - dBias over slices: within a block in slice order (registers), across blocks in
 //    block order (the partial slot), across the slots of a head in slot order (reduce kernel).
 // Every order depends on the shape and the number of resident clusters (the GPU model) only.
