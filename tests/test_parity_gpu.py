@@ -118,6 +118,25 @@ def test_ragged_slice_groups_across_units():
     _compare_all(got, want, "ragged_units")
 
 
+MAXN = [
+    ("n1024_d32", dict(B=1, S=3, N=1024, H=2, d=32, seed=41, mask=("tail", 30))),
+    ("n1000_d16", dict(B=1, S=2, N=1000, H=3, d=16, seed=42, mask=("random", 0.05))),
+]
+
+
+@pytest.mark.parametrize("name,cfg", MAXN, ids=[m[0] for m in MAXN])
+def test_largest_key_count_full_oracle(name, cfg):
+    # N up to the supported maximum of 1024: eight key tiles, so the backward runs its largest
+    # cluster (eight CTAs, each owning 16 dQ rows of a step); N = 1000 leaves a ragged last tile
+    x = wl.make_inputs(**cfg)
+    got = run_cuda(x)
+    want = oracle_full(x)
+    _compare_all(got, want, name)
+    end = run_cuda(x, node=1)
+    for k in ("O", "LSE", "Ores", "dQ", "dK", "dV", "dBias"):
+        assert torch.equal(end[k].view(torch.uint8), got[k].view(torch.uint8)), f"{name}: {k} differs by layout"
+
+
 def test_scale_argument_is_used():
     x = wl.make_inputs(B=1, S=4, N=64, H=2, d=16, seed=12, mask=("tail", 3))
     got = run_cuda(x, scale=0.37)
