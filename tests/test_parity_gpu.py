@@ -137,6 +137,16 @@ def test_largest_key_count_full_oracle(name, cfg):
         assert torch.equal(end[k].view(torch.uint8), got[k].view(torch.uint8)), f"{name}: {k} differs by layout"
 
 
+@pytest.mark.parametrize("d", [16, 32])
+def test_largest_head_count_full_oracle(d):
+    # H = 256, the supported maximum: 16 KB (d = 32) between a row's heads in the pair tensors,
+    # and the D kernel's per-block head buffer at its largest
+    x = wl.make_inputs(B=1, S=2, N=130, H=256, d=d, seed=43 + d, mask=("random", 0.1))
+    got = run_cuda(x)
+    want = oracle_full(x)
+    _compare_all(got, want, f"h256_d{d}")
+
+
 def test_scale_argument_is_used():
     x = wl.make_inputs(B=1, S=4, N=64, H=2, d=16, seed=12, mask=("tail", 3))
     got = run_cuda(x, scale=0.37)
