@@ -147,6 +147,54 @@ def test_largest_head_count_full_oracle(d):
     _compare_all(got, want, f"h256_d{d}")
 
 
+def test_pair_tensors_above_2_31_elements():
+    # B*S*N*H*d = 257 * 1024 * 256 * 32 > 2^31 elements per pair tensor (4.3 GB in BF16, about
+    # 45 GB on the device in all): element offsets need 64 bits everywhere. The inputs are drawn on
+    # the device. A head's O, LSE, dQ, dK and dV depend only on that head's inputs and bias, so
+    # sampled (slice, head) pairs are checked against the oracle on that sub-problem; dBias rows,
+    # which sum over all slices, are checked for two heads over all 257 slices.
+    import oracle
+    from bwd_tri_attn_gb300 import binding as tb
+
+    B, S, N, H, d = 1, 257, 1024, 256, 32
+    assert B * S * N * H * d > 2 ** 31
+    gen = torch.Generator(device="cuda").manual_seed(61)
+
+    def normal(shape):
+        return torch.randn(shape, generator=gen, device="cuda").to(torch.bfloat16)
+
+    x = {k: normal((B, S, N, H, d)) for k in ("Q", "K", "V", "dO")}
+    x["bias"] = normal((B, H, N, N))
+    x["mask"] = wl.make_mask(("tail", 30), B, S, N, torch.Generator().manual_seed(61)).cuda()
+    O, LSE, Ores = tb.forward(x["Q"], x["K"], x["V"], x["bias"], x["mask"])
+    dQ, dK, dV, dBias = tb.backward(x["Q"], x["K"], x["V"], x["bias"], x["mask"], O, Ores, LSE, x["dO"])
+    torch.cuda.synchronize()
+    assert tb.tri_attn_device_status() == 0
+
+    sl, heads = [0, 129, 256], [0, 255]
+
+    def sub(t):  # [B, S, N, H, d] -> sampled slices and heads, on the host
+        return t[:, sl][:, :, :, heads].cpu()
+
+    xs = {k: sub(x[k]) for k in ("Q", "K", "V", "dO")}
+    xs["bias"] = x["bias"][:, heads].cpu()
+    xs["mask"] = x["mask"][:, sl].cpu()
+    want = oracle_full(xs)
+    for k, t in (("O", O), ("dQ", dQ), ("dK", dK), ("dV", dV)):
+        e = rmse_rel(f64(sub(t)), want[k])
+        assert e <= RMSE_REL_TOL, f"{k} RMSE {e}"
+    check_lse(f64(LSE[:, sl][:, :, heads].cpu()), want["LSE"], "above_2_31")
+
+    xh = {k: x[k][:, :, :, heads].cpu() for k in ("Q", "K", "V", "dO")}
+    rows = [(0, 0, 5), (0, 1, 517), (0, 1, N - 1)]
+    want_rows = oracle.dbias_rows(xh["Q"], xh["K"], xh["V"], xs["bias"], x["mask"].cpu(), xh["dO"], rows)
+    got_rows = np.stack([f64(dBias[b, heads[h], j].cpu()) for (b, h, j) in rows])
+    e = rmse_rel(got_rows, want_rows)
+    assert e <= RMSE_REL_TOL, f"dBias sampled-row RMSE {e}"
+    del x, O, LSE, Ores, dQ, dK, dV, dBias
+    torch.cuda.empty_cache()
+
+
 def test_scale_argument_is_used():
     x = wl.make_inputs(B=1, S=4, N=64, H=2, d=16, seed=12, mask=("tail", 3))
     got = run_cuda(x, scale=0.37)
