@@ -10,7 +10,14 @@ Prints ONE JSON line on rank 0.
 With N > 1 (torchrun, one process per GPU) every rank runs an independent
 replica of the workload (the path has no cross-GPU exchange at this size):
 weak scaling, the max over ranks of the timed region is used, and value is the
-work of all ranks divided by that time.
+work of all ranks divided by that time. Run without torchrun, --gpus N > 1
+starts itself under torch.distributed.run with N processes.
+
+Timing: W untimed warm-up steps, then R windows of exactly K steps each, every
+window bracketed by a barrier and a device synchronisation on both sides and
+timed with CUDA events on the launching stream; the line reports the median
+window (R >= 3, enough windows to fill about a second, so that the clock
+sampler sees the GPU under load).
 """
 from __future__ import annotations
 
@@ -31,7 +38,8 @@ UNIT = "TFLOP/s"
 L2_BYTES = 129 * 2**20
 
 # Kernels each step enqueues, in order (the library's per-kernel event order).
-KERNELS = ["fwd", "bias_transpose", "bwd_d", "bwd_main", "dbias_reduce"]
+KERNELS = ["fwd_vscale", "fwd", "bias_transpose", "bwd_prep", "bwd_main", "dbias_reduce"]
+NFWD = 2  # kernels of tri_attn_fwd
 
 
 # ncu summaries under profiles/ carry, per kernel, the DRAM bytes of one captured
@@ -158,6 +166,43 @@ def max_over_ranks(value: float, world: int, device=None) -> float:
     return float(t.item())
 
 
+def bwd_unit_start(c: int, nc: int, w: int) -> int:
+    """First (head, slice) pair of cluster c when the backward splits w pairs over nc clusters."""
+    return c * w // nc
+
+
+def bwd_cluster_of(x: int, nc: int, w: int) -> int:
+    c = x * nc // w
+    while c + 1 < nc and bwd_unit_start(c + 1, nc, w) <= x:
+        c += 1
+    while c > 0 and bwd_unit_start(c, nc, w) > x:
+        c -= 1
+    return c
+
+
+def hbm_algorithmic_bytes(B, S, N, H, d, nc):
+    """Bytes each HBM-bound kernel must move at least once (reads + writes), per launch."""
+    nx = B * S * N * H * d
+    NP = (N + 127) // 128 * 128
+    njt = NP // 128
+    w = B * H * S
+    slots = sum(bwd_cluster_of(hd * S + S - 1, nc, w) - bwd_cluster_of(hd * S, nc, w) + 1 for hd in range(B * H))
+    return {
+        "fwd_vscale": 2 * nx + 4 * B * S * H * njt,                        # V in; one int per work unit out
+        "bias_transpose": 2 * B * H * N * N + 2 * B * H * NP * NP,         # bias in; padded transpose out
+        "bwd_prep": 6 * 2 * nx + 4 * B * S * H * N + 16 * B * S * H,      # dO, O, Ores, Q, K, V in; D, scales out
+        "dbias_reduce": 4 * slots * N * NP + 2 * B * H * N * N,            # FP32 partial slots in; BF16 dBias out
+    }
+
+
+def hbm_report(kernel_ms, B, S, N, H, d, nc, peak_gbs):
+    out = {}
+    for k, nbytes in hbm_algorithmic_bytes(B, S, N, H, d, nc).items():
+        gbs = nbytes / (kernel_ms[k] * 1e-3) / 1e9
+        out[k] = {"bytes": nbytes, "ms": kernel_ms[k], "gbs": gbs, "frac": gbs / peak_gbs}
+    return out
+
+
 def job_throughput(world: int, flops_per_step: float, ms_per_step: float) -> float:
     """Whole-job TFLOP/s: every rank runs the same step on its own data (weak scaling), and the
     job's step time is the slowest rank's."""
@@ -180,6 +225,12 @@ def cpu_oracle_sample(w, slices: int, nthreads: int = 0):
     return flops / dt / 1e12, dt, cores
 
 
+def config_of(w, node: str) -> dict:
+    """The workload description both arms print (identical, so that their lines compare)."""
+    return {"workload": w.name, "B": w.B, "S": w.slices, "N": w.N, "H": w.H, "d": w.d, "node": node,
+            "mask": list(w.mask), "flops_per_step": w.flops()}
+
+
 def run_reference(args, w):
     """Reference arm: the FP64 oracle on the host cores, one bounded sample per step."""
     world, rank, _ = dist_env()
@@ -200,7 +251,7 @@ def run_reference(args, w):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": w.name, "B": w.B, "S": w.slices, "N": w.N, "H": w.H, "d": w.d},
+        "data": "synthetic", "config": config_of(w, args.node),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
@@ -246,7 +297,7 @@ def run_ours(args, w):
         step()
     torch.cuda.synchronize()
 
-    # per-kernel events: [start, after fwd] per fwd call and [after D, after main, after reduce] per bwd call
+    # per-kernel events: one after each kernel of the step (KERNELS order), after a start event
     K = args.steps
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     marks = [[torch.cuda.Event(enable_timing=True) for _ in range(len(KERNELS))] for _ in range(K)]
@@ -254,32 +305,41 @@ def run_ours(args, w):
         e.record(stream)  # materialise the events before handing their handles over
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
+    per_kernel = {n: [] for n in KERNELS}
 
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(torch.cuda.current_device()) as clocks:
+    def window():
+        """Exactly K timed steps, bracketed by a barrier and a synchronisation on both sides;
+        returns the slowest rank's elapsed milliseconds."""
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
         t_start.record(stream)
         for k in range(K):
             starts[k].record(stream)
-            tb.tri_attn_set_timing_events(marks[k][:1])
+            tb.tri_attn_set_timing_events(marks[k][:NFWD])
             tb.tri_attn_fwd(shape, d["Q"], d["K"], d["V"], d["bias"], d["mask"], O, LSE, Ores, stream)
-            tb.tri_attn_set_timing_events(marks[k][1:])
+            tb.tri_attn_set_timing_events(marks[k][NFWD:])
             tb.tri_attn_bwd(shape, d["Q"], d["K"], d["V"], d["bias"], d["mask"], O, Ores, LSE, d["dO"], dQ, dK,
                             dV, dBias, ws, stream)
         t_end.record(stream)
         tb.tri_attn_set_timing_events(None)
         torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
-    assert tb.tri_attn_device_status() == 0
+        if world > 1:
+            dist.barrier()
+        for k in range(K):
+            chain = [starts[k]] + marks[k]
+            for n, (a, b) in enumerate(zip(chain[:-1], chain[1:])):
+                per_kernel[KERNELS[n]].append(a.elapsed_time(b))
+        return max_over_ranks(t_start.elapsed_time(t_end), world, dev)
 
-    per_kernel = {n: [] for n in KERNELS}
-    for k in range(K):
-        chain = [starts[k]] + marks[k]
-        for n, (a, b) in enumerate(zip(chain[:-1], chain[1:])):
-            per_kernel[KERNELS[n]].append(a.elapsed_time(b))
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        windows = [window()]
+        nwin = args.windows or max(3, min(50, int(1000.0 / max(windows[0], 1e-3)) + 1))
+        nwin = max_over_ranks(nwin, world, dev)  # every rank runs the same number of windows
+        while len(windows) < nwin:
+            windows.append(window())
+    elapsed_ms = statistics.median(windows)
+    assert tb.tri_attn_device_status() == 0
     kernel_ms = {n: sum(v) / len(v) for n, v in per_kernel.items()}
 
     flops = w.flops()
@@ -299,9 +359,8 @@ def run_ours(args, w):
                 "peak_source": f"{peaks['source']} bf16 dense burst"}
 
     # HBM-bound kernels: algorithmic bytes / time
-    nx = B * S * N * H * hd
-    bytes_d = 3 * 2 * nx + 4 * B * S * H * N
-    hbm = {"bwd_d_gbs": bytes_d / (kernel_ms["bwd_d"] * 1e-3) / 1e9}
+    nc, _ = tb.tri_attn_bwd_split(shape)
+    hbm = hbm_report(kernel_ms, B, S, N, H, hd, nc, peaks["hbm_gbs"])
 
     # end to end through the public API: pinned host inputs -> device -> fwd+bwd -> gradients back to host.
     # Every step copies its own inputs in and its four gradients out inside the timed region. The
@@ -393,10 +452,12 @@ def run_ours(args, w):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "S": w.slices, "N": w.N, "H": w.H, "d": w.d, "node": args.node,
-                       "mask": list(w.mask), "flops_per_step": flops,
-                       "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB of inputs vs {L2_BYTES / 1e6:.0f} MB L2), no flush",
-                       "operands": "BF16 in/out, FP16 tensor-core operands, FP32 accumulation"},
+            "config": config_of(w, args.node),
+            "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB of inputs vs {L2_BYTES / 1e6:.0f} MB L2), no flush",
+            "operands": "BF16 in/out, FP16 tensor-core operands (power-of-two scaled per (batch, slice, head)), "
+                        "FP32 accumulation",
+            "timing": {"windows": len(windows), "steps_per_window": K, "window_ms": windows,
+                       "reported": "median window"},
             "pct_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
             "kernel_ms": kernel_ms, "hbm": hbm, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": K * len(KERNELS), "clocks": clocks.summary(),
@@ -421,9 +482,23 @@ def main():
     ap.add_argument("--ref-slices", type=int, default=4, help="slices per step of the reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--windows", type=int, default=0,
+                    help="timed windows of --steps steps (0: enough to fill about a second, at least 3)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    world = int(os.environ.get("WORLD_SIZE", "0"))
+    if world == 0 and args.gpus > 1:
+        # one process per GPU: start this script under torch.distributed.run
+        import socket
+        with socket.socket() as so:
+            so.bind(("127.0.0.1", 0))
+            port = so.getsockname()[1]
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={args.gpus}",
+               "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__)] + sys.argv[1:]
+        sys.exit(subprocess.call(cmd))
+    if world and world != args.gpus:
+        ap.error(f"--gpus {args.gpus} disagrees with WORLD_SIZE={world}")
     w = wl.ALL[args.workload]
     if args.impl == "reference":
         run_reference(args, w)

@@ -40,7 +40,7 @@ class TriAttnError(RuntimeError):
 
 
 _VP = ctypes.c_void_p
-EXPORTS = ("tri_attn_strerror", "tri_attn_fwd", "tri_attn_bwd_workspace_size", "tri_attn_bwd",
+EXPORTS = ("tri_attn_strerror", "tri_attn_fwd", "tri_attn_bwd_workspace_size", "tri_attn_bwd_split", "tri_attn_bwd",
            "tri_attn_device_status", "tri_attn_set_timing_events", "tri_attn_bwd_static")
 
 
@@ -64,6 +64,9 @@ def load(path: str | None = None):
         lib.tri_attn_fwd.restype = ctypes.c_int
         lib.tri_attn_bwd_workspace_size.argtypes = [Shape]
         lib.tri_attn_bwd_workspace_size.restype = ctypes.c_size_t
+        lib.tri_attn_bwd_split.argtypes = [Shape, ctypes.c_int, ctypes.POINTER(ctypes.c_int),
+                                           ctypes.POINTER(ctypes.c_int)]
+        lib.tri_attn_bwd_split.restype = ctypes.c_int
         lib.tri_attn_bwd.argtypes = [Shape] + [_VP] * 14 + [ctypes.c_size_t, _VP]
         lib.tri_attn_bwd.restype = ctypes.c_int
         lib.tri_attn_device_status.argtypes = [_VP]
@@ -111,6 +114,14 @@ def tri_attn_fwd(shape: Shape, Q, K, V, bias, mask, O, LSE, Ores, stream=None):
 
 def tri_attn_bwd_workspace_size(shape: Shape) -> int:
     return int(load().tri_attn_bwd_workspace_size(shape))
+
+
+def tri_attn_bwd_split(shape: Shape, static_entry: bool = False) -> tuple[int, int]:
+    """(clusters, dBias partial slots per head) of the backward's work split on the current device."""
+    nc, slots = ctypes.c_int(0), ctypes.c_int(0)
+    rc = load().tri_attn_bwd_split(shape, int(bool(static_entry)), ctypes.byref(nc), ctypes.byref(slots))
+    _check("tri_attn_bwd_split", rc)
+    return nc.value, slots.value
 
 
 def tri_attn_bwd(shape: Shape, Q, K, V, bias, mask, O, Ores, LSE, dO, dQ, dK, dV, dBias, workspace,

@@ -6,21 +6,10 @@
 
 #include "common.cuh"
 
+#include "plan.cuh"
+
 namespace triattn {
-cudaError_t launch_fwd(const Dims &g, const uint16_t *Q, const uint16_t *K, const uint16_t *V,
-                       const uint16_t *bias, const uint16_t *mask, uint16_t *O, float *LSE, uint16_t *Ores,
-                       int *status, cudaStream_t stream);
-cudaError_t launch_bwd_d(const Dims &g, const uint16_t *dO, const uint16_t *O, const uint16_t *Ores,
-                         float *Dout, cudaStream_t stream);
-cudaError_t launch_bias_transpose(const Dims &g, const uint16_t *bias, uint16_t *biasT, cudaStream_t stream);
-cudaError_t launch_bwd_main(const Dims &g, const BwdSplit &sp, const uint16_t *Q, const uint16_t *K,
-                            const uint16_t *V, const uint16_t *biasT, const uint16_t *mask, const float *LSE,
-                            const float *Dv, const uint16_t *dO, uint16_t *dQ, uint16_t *dK, uint16_t *dV,
-                            float *partial, int *status, cudaStream_t stream);
-cudaError_t launch_dbias_reduce_t(const Dims &g, const BwdSplit &sp, const float *partial, uint16_t *dBias,
-                                  cudaStream_t stream);
-int bwd_slots_max(const Dims &g);
-BwdSplit bwd_split_active(const Dims &g);
+int static_bwd_split(const tri_attn_shape &s, BwdSplit *sp);
 }  // namespace triattn
 
 using namespace triattn;
@@ -48,22 +37,25 @@ int check_shape(const tri_attn_shape &s) {
 
 Dims to_dims(const tri_attn_shape &s) { return Dims{s.B, s.S, s.N, s.H, s.d, s.scale, s.node}; }
 
-// Backward workspace: the FP32 correction D [B,S,H,N], the transposed and
-// tile-padded BF16 bias [B*H][NP][NP] (NP = N rounded up to 128), and the FP32
-// dBias partials [B*H][slots][NP][NP]: one slot per cluster that works on a head.
+// Backward workspace: the FP32 correction D [B,S,H,N], the operand exponent maxima
+// int [B,H][4], the transposed and tile-padded BF16 bias [B*H][NP][NP] (NP = N
+// rounded up to 128), and the FP32 dBias partials [B*H][slots][NP][NP]: one slot
+// per cluster that works on a head.
 struct WorkspaceLayout {
-  size_t d_off, biast_off, partial_off, total;
+  size_t d_off, scl_off, biast_off, partial_off, total;
   int slots;
 };
 
-WorkspaceLayout layout_for(const tri_attn_shape &s) {
+// Workspace layout for the current device (nsm: its SM count, which bounds the split).
+WorkspaceLayout layout_for(const tri_attn_shape &s, int nsm) {
   WorkspaceLayout w;
   const Dims g = to_dims(s);
   const size_t NP = (size_t)(s.N + 127) / 128 * 128;
   const size_t rows = (size_t)s.B * s.S * s.H * s.N;
-  w.slots = bwd_slots_max(g);
+  w.slots = bwd_slots_max(g, nsm);
   w.d_off = 0;
-  w.biast_off = align_up(sizeof(float) * rows);
+  w.scl_off = align_up(sizeof(float) * rows);
+  w.biast_off = w.scl_off + align_up(16 * (size_t)s.B * s.H);
   w.partial_off = w.biast_off + align_up(2 * (size_t)s.B * s.H * NP * NP);
   w.total = w.partial_off + align_up(sizeof(float) * (size_t)w.slots * s.B * s.H * NP * NP);
   return w;
@@ -132,14 +124,35 @@ int tri_attn_fwd(tri_attn_shape shape, const tri_attn_bf16 *Q, const tri_attn_bf
   auto st = static_cast<cudaStream_t>(stream);
   int *status = status_word();
   if (!status) return TRI_ATTN_ERR_CUDA;
-  cudaError_t e = launch_fwd(g, Q, K, V, bias, mask, O, LSE, Ores, status, st);
+  FwdPlan plan;
+  if (plan_fwd(g, Q, K, V, bias, &plan) != cudaSuccess) return TRI_ATTN_ERR_CUDA;
+  cudaError_t e = launch_fwd_vscale(g, V, LSE, st);
   if (e == cudaSuccess) e = mark(0, st);
+  if (e == cudaSuccess) e = launch_fwd(g, plan, bias, mask, O, LSE, Ores, status, st);
+  if (e == cudaSuccess) e = mark(1, st);
   return cuda_rc(e);
 }
 
 size_t tri_attn_bwd_workspace_size(tri_attn_shape shape) {
-  if (check_shape(shape)) return 0;
-  return layout_for(shape).total;
+  int nsm = 0;
+  if (check_shape(shape) || device_sm_count(&nsm) != cudaSuccess) return 0;
+  return layout_for(shape, nsm).total;
+}
+
+int tri_attn_bwd_split(tri_attn_shape shape, int static_entry, int *clusters, int *slots_per_head) {
+  int rc = check_shape(shape);
+  if (rc) return rc;
+  if (!clusters || !slots_per_head) return TRI_ATTN_ERR_INVALID_ARG;
+  BwdSplit sp;
+  if (static_entry) {
+    rc = static_bwd_split(shape, &sp);
+    if (rc) return rc;
+  } else if (bwd_split_active(to_dims(shape), &sp) != cudaSuccess) {
+    return TRI_ATTN_ERR_CUDA;
+  }
+  *clusters = sp.NC;
+  *slots_per_head = sp.KMAX;
+  return TRI_ATTN_OK;
 }
 
 int tri_attn_bwd(tri_attn_shape shape, const tri_attn_bf16 *Q, const tri_attn_bf16 *K,
@@ -154,24 +167,30 @@ int tri_attn_bwd(tri_attn_shape shape, const tri_attn_bf16 *Q, const tri_attn_bf
   const void *ptrs[] = {Q, K, V, bias, mask, O, Ores, LSE, dO, dQ, dK, dV, dBias, workspace};
   for (const void *p : ptrs)
     if (p && !aligned16(p)) return TRI_ATTN_ERR_UNSUPPORTED;
-  const WorkspaceLayout w = layout_for(shape);
+  int nsm = 0;
+  if (device_sm_count(&nsm) != cudaSuccess) return TRI_ATTN_ERR_CUDA;
+  const WorkspaceLayout w = layout_for(shape, nsm);
   if (!workspace || workspace_bytes < w.total) return TRI_ATTN_ERR_WORKSPACE;
   const Dims g = to_dims(shape);
+  // the work split (and with it the reduction order) is settled before anything is enqueued
+  BwdSplit sp;
+  if (bwd_split_active(g, &sp) != cudaSuccess) return TRI_ATTN_ERR_CUDA;
+  if (sp.KMAX > w.slots) return TRI_ATTN_ERR_CUDA;  // (cannot happen: the workspace covers every split)
   auto st = static_cast<cudaStream_t>(stream);
   char *ws = static_cast<char *>(workspace);
   float *Dv = reinterpret_cast<float *>(ws + w.d_off);
+  int *emax = reinterpret_cast<int *>(ws + w.scl_off);
   uint16_t *biasT = reinterpret_cast<uint16_t *>(ws + w.biast_off);
   float *partial = reinterpret_cast<float *>(ws + w.partial_off);
   int *status = status_word();
   if (!status) return TRI_ATTN_ERR_CUDA;
-  cudaError_t e = launch_bias_transpose(g, bias, biasT, st);
+  BwdPlan plan;
+  if (plan_bwd(g, sp, Q, K, V, dO, biasT, dK, dV, &plan) != cudaSuccess) return TRI_ATTN_ERR_CUDA;
+  cudaError_t e = launch_bias_transpose(g, bias, biasT, emax, st);
   if (e == cudaSuccess) e = mark(0, st);
-  if (e == cudaSuccess) e = launch_bwd_d(g, dO, O, Ores, Dv, st);
+  if (e == cudaSuccess) e = launch_bwd_prep(g, dO, O, Ores, Q, K, V, Dv, emax, st);
   if (e == cudaSuccess) e = mark(1, st);
-  BwdSplit sp = bwd_split_active(g);
-  if (sp.KMAX > w.slots) return TRI_ATTN_ERR_CUDA;  // (cannot happen: the workspace covers every split)
-  if (e == cudaSuccess)
-    e = launch_bwd_main(g, sp, Q, K, V, biasT, mask, LSE, Dv, dO, dQ, dK, dV, partial, status, st);
+  if (e == cudaSuccess) e = launch_bwd_main(g, plan, LSE, Dv, emax, mask, dQ, dK, dV, partial, status, st);
   if (e == cudaSuccess) e = mark(2, st);
   if (e == cudaSuccess) e = launch_dbias_reduce_t(g, sp, partial, dBias, st);
   if (e == cudaSuccess) e = mark(3, st);

@@ -35,8 +35,16 @@
 //    block order (the partial slot), across the slots of a head in slot order (reduce kernel).
 // Every order depends on the shape and the number of resident clusters (the GPU model) only.
 //
-// Operands: all tensor-core operands are FP16 (Q, K, V, dO converted in shared
-// memory, exact in the FP16 range); P and dS need FP16's 11-bit significand.
+// Operands: all tensor-core operands are FP16; P and dS need FP16's 11-bit significand. Q, K,
+// V and dO are converted in shared memory after multiplication by the power of two of their
+// (batch, head) block (exponents from the preparation kernel: sq, sk, sv, so), which keeps every
+// entry within 2^-20 of the block's largest one exact in FP16. The scales are undone exactly and
+// change only between heads, so every role sets its constants once per block of slices: S^T
+// carries 2^(sk+sq) (folded into the exponent's scale factor), dP^T carries w = 2^(sv+so), so
+// dS' = P (dP^T - w D) is w times the unscaled FP32 dS to the bit and is packed to FP16 as it
+// stands (|dS'| < 2^14 by the choice of sv, so); the dBias register sums carry w (removed with
+// one FFMA per element at the flush), dK carries w 2^sq, dV 2^so and the dQ partials w 2^sk
+// (removed by the owner after it has summed them), all in FP32 before the BF16 rounding.
 //
 // Warp roles (8 + NEW warps; NEW = 8 with QPT = 64 queries per elementwise thread). The control
 // warps take the lowest indices (warp schedulers favour low-index warps, and their short
@@ -55,6 +63,7 @@
 // shared memory. So the P phase of step t+1 overlaps step t's dK and dQ.
 #include "common.cuh"
 #include "launch.cuh"
+#include "plan.cuh"
 #include "sm100.cuh"
 #include "sync.cuh"
 #include "tmap.cuh"
@@ -76,8 +85,9 @@ struct BwdCfg {
   static constexpr int WARP_DQ = 4, NDQ = 4, NDQT = NDQ * 32, WARP_EW0 = 8;
   static constexpr int NTHREADS = (NEW + 8) * 32;
   static constexpr uint32_t REG_LAUNCH = QPT == 64 ? 128 : 80, REG_EW = QPT == 64 ? 200 : 96,
-                            REG_OTHER = QPT == 64 ? 56 : 48;
-  static_assert(NEWT * REG_EW + (NTHREADS - NEWT) * REG_OTHER == NTHREADS * REG_LAUNCH, "register split");
+                            REG_OTHER = 48, REG_DQ = 64;
+  // warpgroup 0 (producer, MMA issuer, converters) keeps REG_OTHER, warpgroup 1 (dQ) REG_DQ
+  static_assert(NEWT * REG_EW + 128 * REG_OTHER + 128 * REG_DQ == NTHREADS * REG_LAUNCH, "register split");
   // the dQ partial (32 columns) uses the half of region B that dS^T leaves free: column group 0 of
   // the elementwise threads keeps its packed dS^T in B + [0,32) and group 1 in B + [64,96)
   static constexpr uint32_t TA = 0, TB = 128, TDQ = TB + 32, TDKV = 256, TMEM_COLS = 512;
@@ -97,7 +107,8 @@ struct BwdCfg {
   static constexpr int OFF_LSE = OFF_RB + NRB * RB_SLOT;   // [NQS][128]: -LSE*log2e (or -inf)
   static constexpr int OFF_D = OFF_LSE + NQS * 512;          // [NQS][128]: D
   static constexpr int OFF_MASK = OFF_D + NQS * 512;         // [GB][128]: mask*log2e of this CTA's keys
-  static constexpr int OFF_BAR = OFF_MASK + GB * 512;
+  static constexpr int OFF_DQF = OFF_MASK + GB * 512;        // [NDQ warps][2 blocks][2] float: dQ factors
+  static constexpr int OFF_BAR = OFF_DQF + NDQ * 16;
   static constexpr int B_KVFULL = 0, B_KVREADY = 1, B_KVFREE = 2;
   static constexpr int B_QDOFULL = 3, B_QDOREADY = B_QDOFULL + NQS, B_QDOFREE = B_QDOREADY + NQS;
   static constexpr int B_BFULL = B_QDOFREE + NQS, B_BFREE = B_BFULL + 1;  // the (single) bias tile
@@ -117,17 +128,32 @@ __device__ __forceinline__ bool wait_bar_cluster_warp(uint32_t bar, uint32_t par
   return __all_sync(0xffffffffu, ok);
 }
 
-// BF16 -> FP16 in place over `bytes` of shared memory, split across `nthr` threads.
-__device__ __forceinline__ void convert_to_f16(uint8_t *p, int bytes, int tid, int nthr) {
+// BF16 -> FP16 in place over `bytes` of shared memory, the values multiplied by f (a power of
+// two), split across `nthr` threads.
+__device__ __forceinline__ void convert_to_f16(uint8_t *p, int bytes, float f, int tid, int nthr) {
   uint4 *v = reinterpret_cast<uint4 *>(p);
+  const float2 f2 = make_float2(f, f);
   for (int e = tid; e < bytes / 16; e += nthr) {
     uint4 w = v[e];
-    w.x = bf16x2_to_f16x2(w.x);
-    w.y = bf16x2_to_f16x2(w.y);
-    w.z = bf16x2_to_f16x2(w.z);
-    w.w = bf16x2_to_f16x2(w.w);
+    w.x = bf16x2_to_f16x2_scaled2(w.x, f2);
+    w.y = bf16x2_to_f16x2_scaled2(w.y, f2);
+    w.z = bf16x2_to_f16x2_scaled2(w.z, f2);
+    w.w = bf16x2_to_f16x2_scaled2(w.w, f2);
     v[e] = w;
   }
+}
+
+// The power-of-two operand scales of one (batch, head) block, from the exponent maxima the
+// preparation kernel accumulated (emax[4 hd + {0,1,2,3}] for Q, K, V, dO).
+struct BwdScales {
+  int sq, sk, sv, so;
+};
+template <int HD>
+__device__ __forceinline__ BwdScales load_scales(const int *emax, int hd) {
+  using T = BwdTargets<HD>;
+  const int4 e = *reinterpret_cast<const int4 *>(emax + 4 * (int64_t)hd);
+  return BwdScales{scale_exp(e.x, kTargetQK), scale_exp(e.y, kTargetQK), scale_exp(e.z, T::TV),
+                   scale_exp(e.w, T::TO)};
 }
 
 
@@ -191,8 +217,9 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
            const __grid_constant__ CUtensorMap mBT, const __grid_constant__ CUtensorMap mDK,
            const __grid_constant__ CUtensorMap mDV, const Dims g, const int NC, const int KMAX,
            const float *__restrict__ LSE,
-           const float *__restrict__ Dv, const uint16_t *__restrict__ mask, uint16_t *__restrict__ dQ,
-           uint16_t *__restrict__ dK, uint16_t *__restrict__ dV, float *__restrict__ partial, int *status) {
+           const float *__restrict__ Dv, const int *__restrict__ emax, const uint16_t *__restrict__ mask,
+           uint16_t *__restrict__ dQ, uint16_t *__restrict__ dK, uint16_t *__restrict__ dV,
+           float *__restrict__ partial, int *status) {
   using C = BwdCfg<HD>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -342,12 +369,14 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
       bool first;
       sc.block(bi, hd, i0, nb, first);
       const int b = hd / g.H;
+      const BwdScales sc4 = load_scales<HD>(emax, hd);
+      const float fk = exp2i(sc4.sk), fv = exp2i(sc4.sv), fq = exp2i(sc4.sq), fo = exp2i(sc4.so);
       ok = wait_bar_warp(bar(C::B_KVFULL), bi & 1, ab);
       if (!ok) break;
       // this warp's share of the block's K and V (the elementwise warps, idle at a block boundary,
       // convert the rest)
-      convert_to_f16(sm + C::OFF_K, nb * C::TILE, C::NEWT + ct, C::NEWT + C::NCVT);
-      convert_to_f16(sm + C::OFF_V, nb * C::TILE, C::NEWT + ct, C::NEWT + C::NCVT);
+      convert_to_f16(sm + C::OFF_K, nb * C::TILE, fk, C::NEWT + ct, C::NEWT + C::NCVT);
+      convert_to_f16(sm + C::OFF_V, nb * C::TILE, fv, C::NEWT + ct, C::NEWT + C::NCVT);
       float *maskf = reinterpret_cast<float *>(sm + C::OFF_MASK);
       for (int x = ct; x < nb * 128; x += C::NCVT) {
         const int il = x >> 7, k = kt * 128 + (x & 127);
@@ -363,8 +392,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
           const int st = t % C::NQS;
           ok = wait_bar_warp(bar(C::B_QDOFULL + st), (t / C::NQS) & 1, ab);
           if (!ok) break;
-          convert_to_f16(sm + C::OFF_Q + st * C::TILE, C::TILE, ct, C::NCVT);
-          convert_to_f16(sm + C::OFF_DO + st * C::TILE, C::TILE, ct, C::NCVT);
+          convert_to_f16(sm + C::OFF_Q + st * C::TILE, C::TILE, fq, ct, C::NCVT);
+          convert_to_f16(sm + C::OFF_DO + st * C::TILE, C::TILE, fo, ct, C::NCVT);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(C::B_QDOREADY + st));
@@ -507,7 +536,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
     }
    }
   } else if (warp < C::WARP_EW0) {
-    reg_dealloc<C::REG_OTHER>();
+    reg_dealloc<C::REG_DQ>();
     // ---------------------------------------------------------------- dQ warps: TMEM -> owners -> BF16
     const int dt = tid - C::WARP_DQ * 32;   // 0..127
     const int jl = (warp - C::WARP_DQ) * 32 + lane;  // query row of the partial = TMEM lane
@@ -522,8 +551,13 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
     if (dt == 0)  // arm every slot for its first step
       for (int s = 0; s < C::NRB && s < T; ++s) mbar_arrive_expect_tx(bar(C::B_RFULL + s), rb_bytes);
     int prev_i = 0, prev_jt = 0, prev_hd = 0, red = 0;
+    // the dQ factors of the blocks of slices (softmax scale / w, then 2^-sk), in this warp's two
+    // shared-memory slots used by alternate blocks: the owner applies those of the step it sums
+    float2 *dqf = reinterpret_cast<float2 *>(sm + C::OFF_DQF) + (warp - C::WARP_DQ) * 2;
+    int pslot = 0;  // slot of the previous step's block
     auto reduce_prev = [&]() -> bool {
       const int slot = red % C::NRB;
+      const float2 pf = dqf[pslot];
       if (!wait_bar_cluster_warp(bar(C::B_RFULL + slot), (red / C::NRB) & 1, ab)) return false;
       if (dt == 0 && red + C::NRB < T) mbar_arrive_expect_tx(bar(C::B_RFULL + slot), rb_bytes);  // arm its next step
       constexpr int CPR = HD / 4;
@@ -542,7 +576,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
         const int j = prev_jt * 128 + r0 + rl;
         if (j < g.N) {
           const uint2 w = make_uint2(
-              pack_bf16x2(s4.x * g.scale, s4.y * g.scale), pack_bf16x2(s4.z * g.scale, s4.w * g.scale));
+              pack_bf16x2(s4.x * pf.x * pf.y, s4.y * pf.x * pf.y), pack_bf16x2(s4.z * pf.x * pf.y, s4.w * pf.x * pf.y));
           *reinterpret_cast<uint2 *>(dQ + pos_row(g, prev_hd / g.H, prev_i, j, NODE) * g.H * HD + (prev_hd % g.H) * HD +
                                      c * 4) = w;
         }
@@ -559,6 +593,12 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
       int hd, i0, nb;
       bool first;
       sc.block(bi, hd, i0, nb, first);
+      // the block's partials carry w 2^sk (all CTAs of the cluster work on the same head)
+      if (lane == 0) {
+        const BwdScales sc4 = load_scales<HD>(emax, hd);
+        dqf[bi & 1] = make_float2(g.scale * exp2i(-(sc4.sv + sc4.so)), exp2i(-sc4.sk));
+      }
+      __syncwarp();
       for (int jt = 0; jt < njt && ok; ++jt)
         for (int il = 0; il < nb; ++il, ++t) {
           if (t > 0) {
@@ -590,6 +630,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
           prev_i = i0 + il;
           prev_jt = jt;
           prev_hd = hd;
+          pslot = bi & 1;
         }
     }
     if (ok && red < T) ok = reduce_prev();  // the last step's rows
@@ -605,7 +646,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
     const uint32_t lb = (uint32_t)(q * 32) << 16;
     const uint32_t colA = tb + lb + C::TA + cg * QPT, colB = tb + lb + C::TB + cg * QPT;
     const float c1 = g.scale * kLog2e;
-    const float2 c12 = make_float2(c1, c1), l2e2 = make_float2(kLog2e, kLog2e), m1x2 = make_float2(-1.f, -1.f);
+    const float2 l2e2 = make_float2(kLog2e, kLog2e);
     const float *maskf = reinterpret_cast<const float *>(sm + C::OFF_MASK);
     // 8 queries per 16 bytes in the 128-byte-swizzled tiles: row of key kl, chunk c at ((c ^ (kl & 7)) << 4)
     const uint32_t trow = (kl >> 3) * 2048 + hf * 1024 + (kl & 7) * 128;
@@ -617,6 +658,14 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
       bool first;  // the block opens its head's segment: the partial tiles start from zero
       sc.block(bi, hd, i0, nb, first);
       const int b = hd / g.H, h = hd % g.H;
+      // the head's operand scales: S^T carries 2^(sk+sq), dP^T and the dBias sums carry w = 2^(sv+so)
+      float2 c12, mw2;
+      {
+        const BwdScales sc4 = load_scales<HD>(emax, hd);
+        const float c1s = c1 * exp2i(-(sc4.sk + sc4.sq)), wv = exp2i(sc4.sv + sc4.so);
+        c12 = make_float2(c1s, c1s);
+        mw2 = make_float2(-wv, -wv);
+      }
       // this cluster's dBias partial slot for head hd: slot k = cl - (first cluster of the head),
       // tiles [head][slot][kt][jt][128 x 128]
       const int64_t pslot = ((int64_t)hd * KMAX + (cl - bwd_cluster_of((int64_t)hd * g.S, NC, W))) * nkt * njt;
@@ -625,8 +674,11 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
       // conversion and the block's mask rows are in place
       ok = wait_bar_warp(bar(C::B_KVFULL), bi & 1, ab);
       if (!ok) break;
-      convert_to_f16(sm + C::OFF_K, nb * C::TILE, ew, C::NEWT + C::NCVT);
-      convert_to_f16(sm + C::OFF_V, nb * C::TILE, ew, C::NEWT + C::NCVT);
+      {
+        const BwdScales sc4 = load_scales<HD>(emax, hd);
+        convert_to_f16(sm + C::OFF_K, nb * C::TILE, exp2i(sc4.sk), ew, C::NEWT + C::NCVT);
+        convert_to_f16(sm + C::OFF_V, nb * C::TILE, exp2i(sc4.sv), ew, C::NEWT + C::NCVT);
+      }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(C::B_KVREADY));
@@ -708,7 +760,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
               const float2 dd = reinterpret_cast<const float2 *>(sd)[x0 >> 1];
               const float2 dp = make_float2(__uint_as_float(dv[2 * e2]), __uint_as_float(dv[2 * e2 + 1]));
               const float2 pp = __half22float2(*reinterpret_cast<const __half2 *>(&pw[x0 >> 1]));
-              const float2 ds = __fmul2_rn(pp, __ffma2_rn(dd, m1x2, dp));  // p (dp - D)
+              const float2 ds = __fmul2_rn(pp, __ffma2_rn(dd, mw2, dp));  // p (dp - w D) = w dS
               acc[x0 >> 1] = __fadd2_rn(acc[x0 >> 1], ds);
               dw[e2] = pack_f16x2(ds.x, ds.y);
             }
@@ -743,12 +795,13 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
             }
           }
 #pragma unroll
+          const float iw = __frcp_rn(-mw2.x);  // the register sums carry w (a power of two: exact)
           for (int m = 0; m < QPT / 8; ++m) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const float2 a = acc[4 * m + e];
-              w[m][2 * e] = __float_as_uint(__uint_as_float(w[m][2 * e]) + a.x);
-              w[m][2 * e + 1] = __float_as_uint(__uint_as_float(w[m][2 * e + 1]) + a.y);
+              w[m][2 * e] = __float_as_uint(fmaf(a.x, iw, __uint_as_float(w[m][2 * e])));
+              w[m][2 * e + 1] = __float_as_uint(fmaf(a.y, iw, __uint_as_float(w[m][2 * e + 1])));
             }
             st_keep_v8(pp + 1024 * m, w[m]);
           }
@@ -765,11 +818,14 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
       tc_fence_after();
       {
         static_assert(C::NEW == 8 && 2 * C::NEW * 32 * C::ROWB <= 32768, "dK/dV staging in the dS tile");
-        const float f = cg == 0 ? g.scale : 1.f;
         const CUtensorMap *mo = cg == 0 ? &mDK : &mDV;
         // 16-byte chunk c of staged row lane: SW64 (64-byte rows) or SW32 (32-byte rows)
         const uint32_t swz = HD == 32 ? (uint32_t)((lane >> 1) & 3) : (uint32_t)((lane >> 2) & 1);
         for (int il = 0; il < nb; ++il) {
+          // dK carries w 2^sq (and takes the softmax scale), dV carries 2^so
+          const BwdScales sc4 = load_scales<HD>(emax, hd);
+          const float f = cg == 0 ? g.scale * exp2i(-(sc4.sv + sc4.so)) : exp2i(-sc4.so);
+          const float f2 = cg == 0 ? exp2i(-sc4.sq) : 1.f;  // (dK: the third factor, applied separately)
           uint32_t r[HD];
           const uint32_t col = tb + lb + C::TDKV + il * 2 * HD + cg * HD;
           if constexpr (HD == 32) {
@@ -781,7 +837,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
           uint32_t w[HD / 2];
 #pragma unroll
           for (int c = 0; c < HD / 2; ++c)
-            w[c] = pack_bf16x2(__uint_as_float(r[2 * c]) * f, __uint_as_float(r[2 * c + 1]) * f);
+            w[c] = pack_bf16x2(__uint_as_float(r[2 * c]) * f * f2, __uint_as_float(r[2 * c + 1]) * f * f2);
           if (il >= 2) {  // the store of slice il - 2 has read this piece
             if (lane == 0) bulk_wait_group_read<1>();
             __syncwarp();
@@ -816,11 +872,13 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
   }
 }
 
-// biasT[bh][k][j] = bias[bh][j][k] for j, k < N, zero in the padding up to NP.
+// biasT[bh][k][j] = bias[bh][j][k] for j, k < N, zero in the padding up to NP; also zeroes the
+// head's four exponent maxima that the preparation kernel accumulates next.
 __global__ void bias_transpose_kernel(const uint16_t *__restrict__ bias, uint16_t *__restrict__ biasT, int N,
-                                      int NP) {
+                                      int NP, int *__restrict__ emax) {
   __shared__ uint16_t tile[32][33];
   const int bh = blockIdx.z, j0 = blockIdx.y * 32, k0 = blockIdx.x * 32;
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.y == 0 && threadIdx.x < 4) emax[4 * bh + threadIdx.x] = 0;
   for (int r = threadIdx.y; r < 32; r += blockDim.y) {
     const int j = j0 + r, k = k0 + threadIdx.x;
     tile[r][threadIdx.x] = (j < N && k < N) ? bias[((int64_t)bh * N + j) * N + k] : (uint16_t)0;
@@ -870,10 +928,11 @@ __global__ void dbias_reduce_t_kernel(const float *__restrict__ partial, int NC,
     }
 }
 
-cudaError_t launch_bias_transpose(const Dims &g, const uint16_t *bias, uint16_t *biasT, cudaStream_t stream) {
+cudaError_t launch_bias_transpose(const Dims &g, const uint16_t *bias, uint16_t *biasT, int *emax,
+                                  cudaStream_t stream) {
   const int NP = (g.N + 127) / 128 * 128;
   dim3 grid(NP / 32, NP / 32, g.B * g.H), block(32, 8);
-  bias_transpose_kernel<<<grid, block, 0, stream>>>(bias, biasT, g.N, NP);
+  bias_transpose_kernel<<<grid, block, 0, stream>>>(bias, biasT, g.N, NP, emax);
   return cudaGetLastError();
 }
 
@@ -888,20 +947,18 @@ cudaError_t launch_dbias_reduce_t(const Dims &g, const BwdSplit &sp, const float
 }
 
 template <int HD>
-cudaError_t launch_bwd_main_t(const Dims &g, const BwdSplit &sp, const uint16_t *Q, const uint16_t *K, const uint16_t *V,
-                              const uint16_t *biasT, const uint16_t *mask, const float *LSE, const float *Dv,
-                              const uint16_t *dO, uint16_t *dQ, uint16_t *dK, uint16_t *dV, float *partial,
-                              int *status, cudaStream_t stream) {
+cudaError_t plan_bwd_t(const Dims &g, const BwdSplit &sp, const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                       const uint16_t *dO, const uint16_t *biasT, uint16_t *dK, uint16_t *dV, BwdPlan *p) {
   using C = BwdCfg<HD>;
   const int nkt = (g.N + 127) / 128, NP = nkt * 128;
-  CUtensorMap mq, mk, mv, mdo, mbt, mdk, mdv;
-  cudaError_t e = make_rows_map(&mq, Q, g, 128);
-  if (e == cudaSuccess) e = make_rows_map(&mdk, dK, g, 32);
-  if (e == cudaSuccess) e = make_rows_map(&mdv, dV, g, 32);
-  if (e == cudaSuccess) e = make_rows_map(&mk, K, g, 128);
-  if (e == cudaSuccess) e = make_rows_map(&mv, V, g, 128);
-  if (e == cudaSuccess) e = make_rows_map(&mdo, dO, g, 128);
-  if (e == cudaSuccess) e = make_square_map(&mbt, biasT, NP, g.B * g.H);
+  p->sp = sp;
+  cudaError_t e = make_rows_map(&p->mq, Q, g, 128);
+  if (e == cudaSuccess) e = make_rows_map(&p->mdk, dK, g, 32);
+  if (e == cudaSuccess) e = make_rows_map(&p->mdv, dV, g, 32);
+  if (e == cudaSuccess) e = make_rows_map(&p->mk, K, g, 128);
+  if (e == cudaSuccess) e = make_rows_map(&p->mv, V, g, 128);
+  if (e == cudaSuccess) e = make_rows_map(&p->mdo, dO, g, 128);
+  if (e == cudaSuccess) e = make_square_map(&p->mbt, biasT, NP, g.B * g.H);
   if (e != cudaSuccess) return e;
   auto *kern = g.node ? bwd_kernel<HD, 1> : bwd_kernel<HD, 0>;
   int dev = 0;
@@ -921,8 +978,24 @@ cudaError_t launch_bwd_main_t(const Dims &g, const BwdSplit &sp, const uint16_t 
     if (fa.numRegs != (int)C::REG_LAUNCH) return cudaErrorInvalidConfiguration;
     once.mark(dev);
   }
+  return cudaSuccess;
+}
+
+cudaError_t plan_bwd(const Dims &g, const BwdSplit &sp, const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                     const uint16_t *dO, const uint16_t *biasT, uint16_t *dK, uint16_t *dV, BwdPlan *p) {
+  return g.d == 32 ? plan_bwd_t<32>(g, sp, Q, K, V, dO, biasT, dK, dV, p)
+                   : plan_bwd_t<16>(g, sp, Q, K, V, dO, biasT, dK, dV, p);
+}
+
+template <int HD>
+static cudaError_t launch_bwd_main_t(const Dims &g, const BwdPlan &p, const float *LSE, const float *Dv,
+                                     const int *emax, const uint16_t *mask, uint16_t *dQ, uint16_t *dK, uint16_t *dV,
+                                     float *partial, int *status, cudaStream_t stream) {
+  using C = BwdCfg<HD>;
+  const int nkt = (g.N + 127) / 128;
+  auto *kern = g.node ? bwd_kernel<HD, 1> : bwd_kernel<HD, 0>;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(nkt, sp.NC, 1);
+  cfg.gridDim = dim3(nkt, p.sp.NC, 1);
   cfg.blockDim = dim3(C::NTHREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_ALLOC;
   cfg.stream = stream;
@@ -933,25 +1006,40 @@ cudaError_t launch_bwd_main_t(const Dims &g, const BwdSplit &sp, const uint16_t 
   attrs[0].val.clusterDim.z = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mdo, mbt, mdk, mdv, g, sp.NC, sp.KMAX, LSE, Dv, mask,
-                            dQ, dK, dV, partial, status);
+  return cudaLaunchKernelEx(&cfg, kern, p.mq, p.mk, p.mv, p.mdo, p.mbt, p.mdk, p.mdv, g, p.sp.NC, p.sp.KMAX, LSE, Dv,
+                            emax, mask, dQ, dK, dV, partial, status);
 }
 
-cudaError_t launch_bwd_main(const Dims &g, const BwdSplit &sp, const uint16_t *Q, const uint16_t *K,
-                            const uint16_t *V, const uint16_t *biasT, const uint16_t *mask, const float *LSE,
-                            const float *Dv, const uint16_t *dO, uint16_t *dQ, uint16_t *dK, uint16_t *dV,
-                            float *partial, int *status, cudaStream_t stream) {
-  if (g.d == 32)
-    return launch_bwd_main_t<32>(g, sp, Q, K, V, biasT, mask, LSE, Dv, dO, dQ, dK, dV, partial, status, stream);
-  return launch_bwd_main_t<16>(g, sp, Q, K, V, biasT, mask, LSE, Dv, dO, dQ, dK, dV, partial, status, stream);
+cudaError_t launch_bwd_main(const Dims &g, const BwdPlan &p, const float *LSE, const float *Dv, const int *emax,
+                            const uint16_t *mask, uint16_t *dQ, uint16_t *dK, uint16_t *dV, float *partial,
+                            int *status, cudaStream_t stream) {
+  if (g.d == 32) return launch_bwd_main_t<32>(g, p, LSE, Dv, emax, mask, dQ, dK, dV, partial, status, stream);
+  return launch_bwd_main_t<16>(g, p, LSE, Dv, emax, mask, dQ, dK, dV, partial, status, stream);
 }
 
-// Most clusters a shape is split over: one per 152 / nkt SMs of a GB300, never more than the
-// number of (head, slice) pairs (so that every cluster has at least one slice).
-int bwd_clusters_max(const Dims &g) {
+// Streaming multiprocessors of the current device (cached per device).
+cudaError_t device_sm_count(int *nsm) {
+  static DeviceValue cache;
+  int dev = 0;
+  cudaError_t e = current_device(&dev);
+  if (e != cudaSuccess) return e;
+  int n = cache.get(dev);
+  if (n == 0) {
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (n < 1) return cudaErrorInvalidDevice;
+    cache.set(dev, n);
+  }
+  *nsm = n;
+  return cudaSuccess;
+}
+
+// Most clusters a shape is split over on a device with nsm SMs: one per nkt SMs, never more than
+// the number of (head, slice) pairs (so that every cluster has at least one slice).
+int bwd_clusters_max(const Dims &g, int nsm) {
   const int nkt = (g.N + 127) / 128;
   const int64_t W = (int64_t)g.B * g.H * g.S;
-  int n = 152 / nkt;
+  int n = nsm / nkt;
   if (n < 1) n = 1;
   return (int)(W < n ? W : n);
 }
@@ -970,10 +1058,11 @@ int bwd_slots_for(const Dims &g, int NC) {
   return k;
 }
 
-// Slots per head the workspace holds: enough for any split over at most bwd_clusters_max clusters.
-int bwd_slots_max(const Dims &g) {
+// Slots per head the workspace holds: enough for any split over at most bwd_clusters_max clusters
+// of a device with nsm SMs.
+int bwd_slots_max(const Dims &g, int nsm) {
   int k = 1;
-  for (int nc = 1; nc <= bwd_clusters_max(g); ++nc) {
+  for (int nc = 1; nc <= bwd_clusters_max(g, nsm); ++nc) {
     const int s = bwd_slots_for(g, nc);
     if (s > k) k = s;
   }
@@ -982,18 +1071,18 @@ int bwd_slots_max(const Dims &g) {
 
 // Clusters of nkt CTAs the device runs at once for this kernel (cached per device).
 template <int HD>
-int bwd_resident_clusters_t(const Dims &g) {
+cudaError_t bwd_resident_clusters_t(const Dims &g, int *out) {
   using C = BwdCfg<HD>;
   static DeviceValue cache[9];  // [cluster size][device]
   const int nkt = (g.N + 127) / 128;
   int dev = 0;
-  if (current_device(&dev) != cudaSuccess) return 1;
+  cudaError_t e = current_device(&dev);
+  if (e != cudaSuccess) return e;
   int n = cache[nkt].get(dev);
   if (n == 0) {
     // (both node instantiations have the same resources: the starting-node one stands for them)
-    if (cudaFuncSetAttribute(bwd_kernel<HD, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) !=
-        cudaSuccess)
-      return 1;
+    e = cudaFuncSetAttribute(bwd_kernel<HD, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(nkt, 1, 1);
     cfg.blockDim = dim3(C::NTHREADS, 1, 1);
@@ -1005,22 +1094,28 @@ int bwd_resident_clusters_t(const Dims &g) {
     attrs[0].val.clusterDim.z = 1;
     cfg.attrs = attrs;
     cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&n, bwd_kernel<HD, 0>, &cfg) != cudaSuccess || n < 1) n = 1;
+    e = cudaOccupancyMaxActiveClusters(&n, bwd_kernel<HD, 0>, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n < 1) return cudaErrorInvalidConfiguration;  // not even one cluster fits on this device
     cache[nkt].set(dev, n);
   }
-  return n;
+  *out = n;
+  return cudaSuccess;
 }
 
 // The split a call uses: as many clusters as the device runs at once (one wave), within the
-// workspace bound. Depends only on the shape and the device, so repeated calls reduce in the
-// same order.
-BwdSplit bwd_split_active(const Dims &g) {
-  const int n = g.d == 32 ? bwd_resident_clusters_t<32>(g) : bwd_resident_clusters_t<16>(g);
-  const int cmax = bwd_clusters_max(g);
-  BwdSplit sp;
-  sp.NC = n < cmax ? n : cmax;
-  sp.KMAX = bwd_slots_for(g, sp.NC);
-  return sp;
+// workspace bound. Depends only on the shape and the device (its SM count and how many of the
+// kernel's clusters it keeps resident), so repeated calls reduce in the same order. Fails, rather
+// than falling back to another split, when the device cannot be queried.
+cudaError_t bwd_split_active(const Dims &g, BwdSplit *sp) {
+  int n = 0, nsm = 0;
+  cudaError_t e = g.d == 32 ? bwd_resident_clusters_t<32>(g, &n) : bwd_resident_clusters_t<16>(g, &n);
+  if (e == cudaSuccess) e = device_sm_count(&nsm);
+  if (e != cudaSuccess) return e;
+  const int cmax = bwd_clusters_max(g, nsm);
+  sp->NC = n < cmax ? n : cmax;
+  sp->KMAX = bwd_slots_for(g, sp->NC);
+  return cudaSuccess;
 }
 
 }  // namespace triattn

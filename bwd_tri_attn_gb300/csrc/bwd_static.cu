@@ -6,20 +6,7 @@
 
 #include "common.cuh"
 
-namespace triattn {
-cudaError_t launch_bwd_d(const Dims &g, const uint16_t *dO, const uint16_t *O, const uint16_t *Ores,
-                         float *Dout, cudaStream_t stream);
-cudaError_t launch_bias_transpose(const Dims &g, const uint16_t *bias, uint16_t *biasT, cudaStream_t stream);
-cudaError_t launch_bwd_main(const Dims &g, const BwdSplit &sp, const uint16_t *Q, const uint16_t *K,
-                            const uint16_t *V, const uint16_t *biasT, const uint16_t *mask, const float *LSE,
-                            const float *Dv, const uint16_t *dO, uint16_t *dQ, uint16_t *dK, uint16_t *dV,
-                            float *partial, int *status, cudaStream_t stream);
-cudaError_t launch_dbias_reduce_t(const Dims &g, const BwdSplit &sp, const float *partial, uint16_t *dBias,
-                                  cudaStream_t stream);
-int bwd_slots_for(const Dims &g, int NC);
-BwdSplit bwd_split_active(const Dims &g);
-int *device_status_word();
-}  // namespace triattn
+#include "plan.cuh"
 
 using namespace triattn;
 
@@ -50,45 +37,80 @@ unsigned char *static_scratch() {
 
 }  // namespace
 
+namespace triattn {
+
+// Scratch layout of tri_attn_bwd_static inside the static array: D [B,S,H,N] FP32 | exponent
+// maxima [B,H][4] int | transposed bias [B*H][NP][NP] BF16 | dBias partials
+// [B*H][slots][NP][NP] FP32.
+struct StaticLayout {
+  size_t scl_off, biast_off, partial_off, one_partial;
+};
+
+static StaticLayout static_layout(const tri_attn_shape &s) {
+  const size_t NP = (size_t)(s.N + 127) / 128 * 128;
+  StaticLayout l;
+  l.scl_off = align_up(sizeof(float) * (size_t)s.B * s.S * s.H * s.N);
+  l.biast_off = l.scl_off + align_up(16 * (size_t)s.B * s.H);
+  l.partial_off = l.biast_off + align_up(2 * (size_t)s.B * s.H * NP * NP);
+  l.one_partial = sizeof(float) * (size_t)s.B * s.H * NP * NP;
+  return l;
+}
+
+static int check_static_args(const tri_attn_shape &s) {
+  if (s.B < 1 || s.S < 1 || s.N < 1 || s.H < 1 || !isfinite(s.scale)) return TRI_ATTN_ERR_INVALID_ARG;
+  if (s.node != TRI_ATTN_NODE_STARTING && s.node != TRI_ATTN_NODE_ENDING) return TRI_ATTN_ERR_INVALID_ARG;
+  if ((s.d != 16 && s.d != 32) || s.N > TRI_ATTN_MAX_N || s.H > TRI_ATTN_MAX_H) return TRI_ATTN_ERR_UNSUPPORTED;
+  if ((int64_t)s.B * s.S > 65535 || (int64_t)s.B * s.H * s.S > (1ll << 30)) return TRI_ATTN_ERR_UNSUPPORTED;
+  return TRI_ATTN_OK;
+}
+
+// The split tri_attn_bwd_static uses: the device's split, with fewer clusters while a head would
+// need more dBias partial slots than the array holds next to the other scratch.
+int static_bwd_split(const tri_attn_shape &s, BwdSplit *sp) {
+  int rc = check_static_args(s);
+  if (rc) return rc;
+  const StaticLayout l = static_layout(s);
+  const size_t cap = TRI_ATTN_STATIC_WORKSPACE_BYTES;
+  if (l.partial_off + l.one_partial > cap) return TRI_ATTN_ERR_STATIC_TOO_SMALL;
+  const size_t fit = (cap - l.partial_off) / l.one_partial;  // partial slots per head that fit
+  const Dims g{s.B, s.S, s.N, s.H, s.d, s.scale, s.node};
+  if (bwd_split_active(g, sp) != cudaSuccess) return TRI_ATTN_ERR_CUDA;
+  while (sp->NC > 1 && (size_t)sp->KMAX > fit) sp->KMAX = bwd_slots_for(g, --sp->NC);
+  if ((size_t)sp->KMAX > fit) return TRI_ATTN_ERR_STATIC_TOO_SMALL;
+  return TRI_ATTN_OK;
+}
+
+}  // namespace triattn
+
 extern "C" int tri_attn_bwd_static(tri_attn_shape s, const tri_attn_bf16 *Q, const tri_attn_bf16 *K,
                                    const tri_attn_bf16 *V, const tri_attn_bf16 *bias, const tri_attn_bf16 *mask,
                                    const tri_attn_bf16 *O, const tri_attn_bf16 *Ores, const float *LSE,
                                    const tri_attn_bf16 *dO, tri_attn_bf16 *dQ, tri_attn_bf16 *dK, tri_attn_bf16 *dV,
                                    tri_attn_bf16 *dBias, void *stream) {
-  if (s.B < 1 || s.S < 1 || s.N < 1 || s.H < 1 || !isfinite(s.scale)) return TRI_ATTN_ERR_INVALID_ARG;
-  if (s.node != TRI_ATTN_NODE_STARTING && s.node != TRI_ATTN_NODE_ENDING) return TRI_ATTN_ERR_INVALID_ARG;
-  if ((s.d != 16 && s.d != 32) || s.N > TRI_ATTN_MAX_N || s.H > TRI_ATTN_MAX_H) return TRI_ATTN_ERR_UNSUPPORTED;
-  if ((int64_t)s.B * s.S > 65535 || (int64_t)s.B * s.H * s.S > (1ll << 30)) return TRI_ATTN_ERR_UNSUPPORTED;
+  int rc = check_static_args(s);
+  if (rc) return rc;
   if (!Q || !K || !V || !bias || !O || !LSE || !dO || !dQ || !dK || !dV || !dBias) return TRI_ATTN_ERR_INVALID_ARG;
   const void *ptrs[] = {Q, K, V, bias, mask, O, Ores, LSE, dO, dQ, dK, dV, dBias};
   for (const void *p : ptrs)
     if (p && !aligned16(p)) return TRI_ATTN_ERR_UNSUPPORTED;
-
-  // scratch layout: D [B,S,H,N] FP32 | transposed bias [B*H][NP][NP] BF16 | dBias partials [B*H][slots][NP][NP] FP32
+  BwdSplit sp;
+  rc = static_bwd_split(s, &sp);  // also refuses shapes that do not fit, before anything is enqueued
+  if (rc) return rc;
+  const StaticLayout l = static_layout(s);
   const Dims g{s.B, s.S, s.N, s.H, s.d, s.scale, s.node};
-  const size_t NP = (size_t)(s.N + 127) / 128 * 128;
-  const size_t d_bytes = align_up(sizeof(float) * (size_t)s.B * s.S * s.H * s.N);
-  const size_t bt_bytes = align_up(2 * (size_t)s.B * s.H * NP * NP);
-  const size_t one_partial = sizeof(float) * (size_t)s.B * s.H * NP * NP;
-  const size_t cap = TRI_ATTN_STATIC_WORKSPACE_BYTES;
-  if (d_bytes + bt_bytes + one_partial > cap) return TRI_ATTN_ERR_STATIC_TOO_SMALL;
-  const size_t fit = (cap - d_bytes - bt_bytes) / one_partial;  // partial slots per head that fit
-  // the device's split, with fewer clusters if a head would need more slots than fit
-  BwdSplit sp = bwd_split_active(g);
-  while (sp.NC > 1 && (size_t)sp.KMAX > fit) sp.KMAX = bwd_slots_for(g, --sp.NC);
-  if ((size_t)sp.KMAX > fit) return TRI_ATTN_ERR_STATIC_TOO_SMALL;
-
   unsigned char *ws = static_scratch();
   int *status = device_status_word();
   if (!ws || !status) return TRI_ATTN_ERR_CUDA;
   float *Dv = reinterpret_cast<float *>(ws);
-  uint16_t *biasT = reinterpret_cast<uint16_t *>(ws + d_bytes);
-  float *partial = reinterpret_cast<float *>(ws + d_bytes + bt_bytes);
+  int *emax = reinterpret_cast<int *>(ws + l.scl_off);
+  uint16_t *biasT = reinterpret_cast<uint16_t *>(ws + l.biast_off);
+  float *partial = reinterpret_cast<float *>(ws + l.partial_off);
   auto st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_bias_transpose(g, bias, biasT, st);
-  if (e == cudaSuccess) e = launch_bwd_d(g, dO, O, Ores, Dv, st);
-  if (e == cudaSuccess)
-    e = launch_bwd_main(g, sp, Q, K, V, biasT, mask, LSE, Dv, dO, dQ, dK, dV, partial, status, st);
+  BwdPlan plan;
+  if (plan_bwd(g, sp, Q, K, V, dO, biasT, dK, dV, &plan) != cudaSuccess) return TRI_ATTN_ERR_CUDA;
+  cudaError_t e = launch_bias_transpose(g, bias, biasT, emax, st);
+  if (e == cudaSuccess) e = launch_bwd_prep(g, dO, O, Ores, Q, K, V, Dv, emax, st);
+  if (e == cudaSuccess) e = launch_bwd_main(g, plan, LSE, Dv, emax, mask, dQ, dK, dV, partial, status, st);
   if (e == cudaSuccess) e = launch_dbias_reduce_t(g, sp, partial, dBias, st);
   return e == cudaSuccess ? TRI_ATTN_OK : TRI_ATTN_ERR_CUDA;
 }

@@ -51,6 +51,83 @@ struct BwdSplit {
   int NC, KMAX;
 };
 
+// ---------------------------------------------------------------- power-of-two operand scaling
+// The tensor-core operands that meet an FP16 factor (P, dS) must be FP16 themselves, and FP16
+// covers only magnitudes 2^-14 .. 65504 at full precision, while BF16 inputs span 2^-126 .. 2^127.
+// Each (batch, slice, head) block of V (forward) and of Q, K, V, dO (backward) is therefore
+// multiplied by 2^s before the BF16 -> FP16 conversion, s chosen from the block's largest exponent
+// so that its largest magnitude lands in [2^T, 2^(T+1)); the accumulators are multiplied by the
+// inverse power of two on the way out. Both multiplications are exact, so the results are the
+// unscaled arithmetic's, bit for bit, wherever that arithmetic stays in FP16's normal range.
+// Blocks whose largest magnitude M lies in [2^-40, 2^41) get the exact target binade; outside it the
+// exponent of the nearest bound is used. Scale exponents then lie in [T - 40, T + 40] (|s| <= 54),
+// so each single factor and each product of two is a normal FP32 value; products of three are
+// applied as two multiplications.
+constexpr int kScaleExpLimit = 40;
+constexpr int kTargetQK = 14;       // Q, K (backward) and V (forward): largest magnitude in [2^14, 2^15)
+// Backward V and dO: their scale factors multiply into the scale of dS' = P (dP' - w D), whose
+// magnitude is below d * 2^(tv + to + 3) (|dP|, |D| <= d max|dO| max|V|); tv + to = 11 - log2(d)
+// keeps it below 2^14, well inside FP16.
+template <int HD>
+struct BwdTargets {
+  static constexpr int TV = 3, TO = HD == 32 ? 3 : 4;
+  static_assert(TV + TO + 3 + (HD == 32 ? 5 : 4) <= 14, "dS' bound");
+};
+
+// Scale exponent for a block whose largest BF16 exponent field is e (0: the block is zero or
+// subnormal and keeps scale 1).
+__host__ __device__ inline int scale_exp(int e, int target) {
+  if (e == 0) return 0;
+  int m = e - 127;  // floor(log2 M)
+  m = m < -kScaleExpLimit ? -kScaleExpLimit : (m > kScaleExpLimit ? kScaleExpLimit : m);
+  return target - m;
+}
+
+// 2^n as an FP32 value, n in [-126, 127].
+__device__ __forceinline__ float exp2i(int n) { return __int_as_float((n + 127) << 23); }
+
+// Running maximum of the BF16 exponent fields held in the two halves of a packed pair
+// (call bf16x2_exp_final on the accumulated word).
+__device__ __forceinline__ uint32_t bf16x2_exp_max(uint32_t acc, uint32_t w) {
+  uint32_t r;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(acc), "r"(w & 0x7f807f80u));
+  return r;
+}
+__device__ __forceinline__ int bf16x2_exp_final(uint32_t acc) {
+  const uint32_t lo = acc & 0xffffu, hi = acc >> 16;
+  return (int)((lo > hi ? lo : hi) >> 7);
+}
+
+// Running maximum of the BF16 exponent fields of the eight values in a 16-byte chunk.
+__device__ __forceinline__ uint32_t exp_max4(uint32_t acc, const uint4 &v) {
+  return bf16x2_exp_max(bf16x2_exp_max(bf16x2_exp_max(bf16x2_exp_max(acc, v.x), v.y), v.z), v.w);
+}
+
+// Maximum of v over the CTA (NT threads, a multiple of 32); every thread gets the result.
+// red: NT / 32 ints of shared memory.
+template <int NT>
+__device__ __forceinline__ int block_max(int v, int *red) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, off));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  int m = 0;
+#pragma unroll
+  for (int w = 0; w < NT / 32; ++w) m = max(m, red[w]);
+  __syncthreads();
+  return m;
+}
+
+// 16-byte streaming load (read once: no L1 allocation).
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+
 // Device status codes written by bounded waits (host reads them lazily).
 constexpr int kStatusTimeout = 1;
 

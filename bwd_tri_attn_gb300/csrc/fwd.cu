@@ -19,8 +19,14 @@
 //   O_i += P_i V_i             tcgen05 (P: FP16 in TMEM as the A operand, V: FP16)
 // P is rounded to FP16 (11-bit significand) rather than BF16: a second BF16
 // rounding on the output's path would add as much error as the output rounding
-// itself. V is converted BF16 -> FP16 in shared memory (exact in FP16 range) by
-// the softmax threads, a slice of the tile each, before they hand P over.
+// itself. V is converted BF16 -> FP16 in shared memory by the softmax threads, a
+// slice of the tile each, before they hand P over; every (b, i, h) block of V is
+// first multiplied by the power of two 2^sv that brings its largest magnitude into
+// [2^14, 2^15) (exact, and FP16 then holds every entry within 2^-31 of that largest
+// one at full precision), and O is multiplied by 2^-sv in the epilogue. A pre-pass
+// (fwd_vscale_kernel) finds sv and leaves it in LSE[b, i, h, 128 jt] for every query
+// tile jt: the one LSE slot per work unit that the unit reads at its start and only
+// overwrites, with the log-sum-exp, at its end.
 //
 // Warp roles (384 threads): warp 0 = producer (TMA for Q, K, V and the bias
 // tiles, bulk copies of the mask rows and their per-tile "nonzero" flags),
@@ -43,6 +49,7 @@
 // key tile ahead with cp.async and the producer copies the mask rows lane by lane.
 #include "common.cuh"
 #include "launch.cuh"
+#include "plan.cuh"
 #include "sm100.cuh"
 #include "sync.cuh"
 #include "tmap.cuh"
@@ -87,7 +94,8 @@ struct FwdCfg {
   static constexpr int B_MFULL = B_BFREE + 2;   // [2] mask rows of a unit landed
   static constexpr int B_MFREE = B_MFULL + 2;   // [2] the unit is done with them
   static constexpr int B_MREADY = B_MFREE + 2;  // [2] mask rows and their tile flags in place
-  static constexpr int NBAR = B_MREADY + 2;
+  static constexpr int B_BSTAGE = B_MREADY + 2;  // (N % 8 != 0) both warpgroups staged their half of a bias tile
+  static constexpr int NBAR = B_BSTAGE + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // [0] TMEM base, [1] abort flag
   static constexpr int SMEM_ALLOC = OFF_MISC + 16 + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
@@ -125,6 +133,23 @@ __device__ __forceinline__ FwdUnit fwd_unit(const Dims &g, int u) {
   w.i0 = grp * C::GF;
   w.ng = min(C::GF, g.S - w.i0);
   return w;
+}
+
+// Scale exponent sv of every (b, i, h) block of V (one CTA each, heads fastest), written into
+// the LSE slot of each work unit of that block.
+template <int HD, int NODE>
+__global__ void __launch_bounds__(256) fwd_vscale_kernel(const Dims g, const uint4 *__restrict__ V,
+                                                         int *__restrict__ lse_bits) {
+  __shared__ int red[8];
+  constexpr int CPH = HD / 8, PPP = 256 / CPH;
+  const int h = blockIdx.x, bi = blockIdx.y, b = bi / g.S, i = bi - b * g.S;
+  const int c = threadIdx.x % CPH, cpp = g.H * CPH;
+  uint32_t m = 0;
+  for (int j = threadIdx.x / CPH; j < g.N; j += PPP)
+    m = exp_max4(m, ld_stream(V + pos_row(g, b, i, j, NODE) * cpp + h * CPH + c));
+  const int s = scale_exp(block_max<256>(bf16x2_exp_final(m), red), kTargetQK);
+  int *row = lse_bits + ((int64_t)bi * g.H + h) * g.N;
+  for (int jt = threadIdx.x; jt * 128 < g.N; jt += 256) row[jt * 128] = s;
 }
 
 template <int HD, int NODE>
@@ -170,6 +195,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
       mbar_init(bar(C::B_MFREE + s), 256);
       mbar_init(bar(C::B_MREADY + s), 1);
     }
+    mbar_init(bar(C::B_BSTAGE), 256);
     misc[1] = 0;
     fence_barrier_init();
   }
@@ -415,6 +441,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
       const int j = jt * 128 + row;
       const uint16_t *mk = reinterpret_cast<const uint16_t *>(sm + C::OFF_MASK) + (k & 1) * (C::GF * C::NMAX);
       const int *flags = reinterpret_cast<const int *>(sm + C::OFF_FLAG) + (k & 1) * (C::GF * C::MAXKT);
+      // V scale of this warpgroup's slices (their LSE slots of this unit; see fwd_vscale_kernel)
+      float vsc[NL], vinv[NL];
+#pragma unroll
+      for (int s = 0; s < NL; ++s) {
+        const int il = wg + 2 * s, e = il < ng ? reinterpret_cast<const int *>(LSE)[(((int64_t)b * g.S + i0 + il) * g.H + h) * g.N + jt * 128] : 0;
+        vsc[s] = exp2i(e);
+        vinv[s] = exp2i(-e);
+      }
       if (mask) ok = wait_bar_warp(bar(C::B_MREADY + (k & 1)), (k >> 1) & 1, ab);
       if (!ok) break;
 
@@ -430,7 +464,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
           if (!ok) break;
         } else {
           cp_async_wait_all();  // this warpgroup's half of the tile is in buffer kb & 1
-          named_sync(1, 256);   // and the other half; every thread is done with tile kb - 1
+          // and the other half; every thread is done with tile kb - 1. A bounded wait: if the other
+          // warpgroup has given up (its own wait expired) it arrives no more, and this one leaves
+          // through the abort flag instead of hanging.
+          mbar_arrive(bar(C::B_BSTAGE));
+          ok = wait_bar_warp(bar(C::B_BSTAGE), kb & 1, ab);
+          if (!ok) break;
           if (kt + 1 < nkt) {
             stage_bias(w, kt + 1, (kb + 1) & 1);
           } else if (u + (int)gridDim.x < nunits) {
@@ -579,15 +618,20 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
           {
             // the tile's V, BF16 -> FP16 in place (V landed with K, before S), a share per thread
             const int st = tg % C::NST;
+            float vs = vsc[0];
+#pragma unroll
+            for (int qq = 1; qq < NL; ++qq)
+              if (qq == sl) vs = vsc[qq];
+            const float2 vs2 = make_float2(vs, vs);
             ok = wait_bar(bar(C::B_KVFULL + st), (tg / C::NST) & 1, ab);
             uint4 *v = reinterpret_cast<uint4 *>(sm + C::OFF_V + st * C::TILE);
 #pragma unroll
             for (int e = wtid; e < C::TILE / 16; e += 128) {
               uint4 xv = v[e];
-              xv.x = bf16x2_to_f16x2(xv.x);
-              xv.y = bf16x2_to_f16x2(xv.y);
-              xv.z = bf16x2_to_f16x2(xv.z);
-              xv.w = bf16x2_to_f16x2(xv.w);
+              xv.x = bf16x2_to_f16x2_scaled2(xv.x, vs2);
+              xv.y = bf16x2_to_f16x2_scaled2(xv.y, vs2);
+              xv.z = bf16x2_to_f16x2_scaled2(xv.z, vs2);
+              xv.w = bf16x2_to_f16x2_scaled2(xv.w, vs2);
               v[e] = xv;
             }
             fence_proxy_async_smem();
@@ -641,7 +685,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
         if (il >= ng || j >= g.N) continue;
         const int i = i0 + il;
         const float lsum = l_sum[s];
-        const float inv = lsum > 0.f ? __frcp_rn(lsum) : 0.f;
+        const float inv = lsum > 0.f ? __frcp_rn(lsum) * vinv[s] : 0.f;  // 1 / l, and V's scale undone
         uint32_t ob[HD / 2], rb[HD / 2];
 #pragma unroll
         for (int c = 0; c < HD / 2; ++c) {
@@ -679,20 +723,18 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
 }
 
 template <int HD>
-cudaError_t launch_fwd_t(const Dims &g, const uint16_t *Q, const uint16_t *K, const uint16_t *V,
-                         const uint16_t *bias, const uint16_t *mask, uint16_t *O, float *LSE, uint16_t *Ores,
-                         int *status, cudaStream_t stream) {
+cudaError_t plan_fwd_t(const Dims &g, const uint16_t *Q, const uint16_t *K, const uint16_t *V, const uint16_t *bias,
+                       FwdPlan *p) {
   using C = FwdCfg<HD>;
-  CUtensorMap mq, mk, mv, mb;
-  cudaError_t e = make_rows_map(&mq, Q, g, 128);
-  if (e == cudaSuccess) e = make_rows_map(&mk, K, g, 128);
-  if (e == cudaSuccess) e = make_rows_map(&mv, V, g, 128);
+  cudaError_t e = make_rows_map(&p->mq, Q, g, 128);
+  if (e == cudaSuccess) e = make_rows_map(&p->mk, K, g, 128);
+  if (e == cudaSuccess) e = make_rows_map(&p->mv, V, g, 128);
   if (e != cudaSuccess) return e;
   if ((g.N & 7) == 0) {
-    e = make_bias_map(&mb, bias, g.N, g.B * g.H);
+    e = make_bias_map(&p->mb, bias, g.N, g.B * g.H);
     if (e != cudaSuccess) return e;
   } else {
-    memset(&mb, 0, sizeof(mb));  // unused: the kernel stages the bias itself
+    memset(&p->mb, 0, sizeof(p->mb));  // unused: the kernel stages the bias itself
   }
   auto *kern = g.node ? fwd_kernel<HD, 1> : fwd_kernel<HD, 0>;
   int dev = 0;
@@ -718,23 +760,44 @@ cudaError_t launch_fwd_t(const Dims &g, const uint16_t *Q, const uint16_t *K, co
   if (nslots == 0) {
     int nsm = 0, per = 0;
     e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess)
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kern, C::NTHREADS, C::SMEM_ALLOC);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kern, C::NTHREADS, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    nslots = max(1, nsm * per);
+    if (per < 1) return cudaErrorInvalidConfiguration;
+    nslots = nsm * per;
     slots.set(dev, nslots);
   }
   const int nunits = g.B * ((g.S + C::GF - 1) / C::GF) * g.H * ((g.N + 127) / 128);
-  const int grid = min(nunits, nslots);
-  kern<<<grid, C::NTHREADS, C::SMEM_ALLOC, stream>>>(mq, mk, mv, mb, g, bias, mask, O, LSE, Ores, status);
+  p->grid = min(nunits, nslots);
+  return cudaSuccess;
+}
+
+cudaError_t plan_fwd(const Dims &g, const uint16_t *Q, const uint16_t *K, const uint16_t *V, const uint16_t *bias,
+                     FwdPlan *p) {
+  return g.d == 32 ? plan_fwd_t<32>(g, Q, K, V, bias, p) : plan_fwd_t<16>(g, Q, K, V, bias, p);
+}
+
+// The V scale pre-pass; it must precede launch_fwd on the same stream.
+cudaError_t launch_fwd_vscale(const Dims &g, const uint16_t *V, float *LSE, cudaStream_t stream) {
+  const dim3 grid(g.H, g.B * g.S);
+  const uint4 *v = reinterpret_cast<const uint4 *>(V);
+  int *slots = reinterpret_cast<int *>(LSE);
+  if (g.d == 32) {
+    if (g.node) fwd_vscale_kernel<32, 1><<<grid, 256, 0, stream>>>(g, v, slots);
+    else fwd_vscale_kernel<32, 0><<<grid, 256, 0, stream>>>(g, v, slots);
+  } else {
+    if (g.node) fwd_vscale_kernel<16, 1><<<grid, 256, 0, stream>>>(g, v, slots);
+    else fwd_vscale_kernel<16, 0><<<grid, 256, 0, stream>>>(g, v, slots);
+  }
   return cudaGetLastError();
 }
 
-cudaError_t launch_fwd(const Dims &g, const uint16_t *Q, const uint16_t *K, const uint16_t *V,
-                       const uint16_t *bias, const uint16_t *mask, uint16_t *O, float *LSE, uint16_t *Ores,
-                       int *status, cudaStream_t stream) {
-  if (g.d == 32) return launch_fwd_t<32>(g, Q, K, V, bias, mask, O, LSE, Ores, status, stream);
-  return launch_fwd_t<16>(g, Q, K, V, bias, mask, O, LSE, Ores, status, stream);
+cudaError_t launch_fwd(const Dims &g, const FwdPlan &p, const uint16_t *bias, const uint16_t *mask, uint16_t *O,
+                       float *LSE, uint16_t *Ores, int *status, cudaStream_t stream) {
+  auto *kern = g.d == 32 ? (g.node ? fwd_kernel<32, 1> : fwd_kernel<32, 0>) : (g.node ? fwd_kernel<16, 1> : fwd_kernel<16, 0>);
+  const int smem = g.d == 32 ? FwdCfg<32>::SMEM_ALLOC : FwdCfg<16>::SMEM_ALLOC;
+  const int nthreads = g.d == 32 ? FwdCfg<32>::NTHREADS : FwdCfg<16>::NTHREADS;
+  kern<<<p.grid, nthreads, smem, stream>>>(p.mq, p.mk, p.mv, p.mb, g, bias, mask, O, LSE, Ores, status);
+  return cudaGetLastError();
 }
 
 }  // namespace triattn

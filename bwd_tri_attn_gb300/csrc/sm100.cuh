@@ -544,5 +544,12 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
   return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
+// Two BF16 -> two FP16 of the values times f (a power of two: the product is exact), with one
+// packed FP32 multiply.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled2(uint32_t w, float2 f) {
+  const float2 x = __fmul2_rn(make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)), f);
+  return pack_f16x2(x.x, x.y);
+}
+
 }  // namespace sm100
 }  // namespace triattn

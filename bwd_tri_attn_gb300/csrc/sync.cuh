@@ -61,9 +61,4 @@ __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {
     if (sm100::globaltimer_ns() - t0 > kWaitLimitNs) break;
 }
 
-// Named barrier over `count` threads (id 1..15; id 0 is __syncthreads).
-__device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
 }  // namespace triattn

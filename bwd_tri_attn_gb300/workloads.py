@@ -117,6 +117,15 @@ def inputs_for(w: Workload, slices: int | None = None):
     return make_inputs(w.B, S, w.N, w.H, w.d, w.seed, w.value_std, w.bias_std, w.mask)
 
 
+def scale_pow2(x: dict, exps: dict) -> dict:
+    """A copy of the inputs with the named tensors multiplied by 2**e (exact in BF16 while the
+    results stay in BF16's normal range): the same problem at another magnitude."""
+    out = dict(x)
+    for k, e in exps.items():
+        out[k] = (x[k].float() * (2.0 ** e)).to(torch.bfloat16)
+    return out
+
+
 def ending_node(t: torch.Tensor) -> torch.Tensor:
     """Transposes the pair axes (1 <-> 2) of a [B,S,N,...] tensor, contiguous copy.
 

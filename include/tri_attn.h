@@ -28,18 +28,39 @@
  *                                keys are all masked)
  * - Supported: d in {16, 32}; 1 <= N <= TRI_ATTN_MAX_N; 1 <= H <= TRI_ATTN_MAX_H;
  *   B, S >= 1. scale is
- *   any finite float (1/sqrt(d) is the usual choice). Q, K, V, dO entries must
- *   have magnitude below 65504 (they are staged as FP16 tensor-core operands).
+ *   any finite float (1/sqrt(d) is the usual choice).
+ * - Input range: every input must be finite (mask entries 0 or -inf). The
+ *   kernels stage Q, K, V and dO as FP16 tensor-core operands after multiplying
+ *   each (batch, slice, head) block by a power of two chosen from the block's
+ *   largest magnitude, and undo it exactly in FP32, so no BF16 magnitude is too
+ *   large or too small as such: with the largest magnitude M of a block between
+ *   2^-40 and 2^40, every entry of the block down to M * 2^-20 is staged exactly
+ *   (smaller entries keep an absolute error below M * 2^-21, far under the BF16
+ *   rounding of the results). Blocks whose M lies outside [2^-40, 2^40] lose
+ *   precision gradually (the scale exponent is clamped to +-40); an all-zero
+ *   block is exact. O, Ores and LSE given to the backward must be the forward's
+ *   outputs for the same inputs.
  * - Every device pointer must be 16-byte aligned (TMA requirement).
  * - Ownership: the caller allocates and owns every buffer, including the
  *   backward workspace. The library allocates no device memory, never
  *   synchronises, and enqueues all work on `stream` (a cudaStream_t; NULL is
  *   the legacy default stream). Outputs are overwritten, never accumulated.
  * - Determinism: for a fixed shape on a fixed GPU model, every output is
- *   bitwise identical across calls. No floating-point atomics are used; every
- *   reduction runs in an order fixed by the shape alone.
- * - Errors: each call returns TRI_ATTN_OK or a negative code, checked on the
- *   host before anything is enqueued (nothing is launched on an error).
+ *   bitwise identical across calls. No floating-point atomics are used. The
+ *   forward's reductions run in an order fixed by the shape; the backward
+ *   splits its (head, slice) pairs over as many thread-block clusters as the
+ *   device keeps resident at once, and its dBias summation order is fixed by
+ *   the shape and that split (tri_attn_bwd_split reports it): a property of the
+ *   GPU model and this library build, not of timing.
+ * - Errors: each call returns TRI_ATTN_OK or a negative code. Arguments, the
+ *   work split, tensor maps and the kernels' attributes are all checked on the
+ *   host before the first kernel is enqueued, so a call that returns an error
+ *   has launched nothing (TRI_ATTN_ERR_CUDA from the launches themselves
+ *   excepted).
+ * - First call per device: the first call of each entry point on a device does
+ *   one-time host set-up there (kernel attributes, occupancy and device
+ *   queries, symbol addresses); make it before capturing the stream into a
+ *   CUDA graph.
  *   Kernels never trap: a bounded device-side wait that expires records
  *   TRI_ATTN_ERR_TIMEOUT in a device status word that
  *   tri_attn_device_status() reads.
@@ -109,8 +130,26 @@ int tri_attn_fwd(tri_attn_shape shape,
                  tri_attn_bf16 *O, float *LSE, tri_attn_bf16 *Ores,
                  void *stream);
 
-/* Bytes of device workspace tri_attn_bwd needs for `shape` (depends on shape only). */
+/*
+ * Bytes of device workspace tri_attn_bwd needs for `shape` on the current
+ * device (the bound on the work split depends on its SM count). Returns 0 for
+ * an unsupported shape or when the device cannot be queried.
+ */
 size_t tri_attn_bwd_workspace_size(tri_attn_shape shape);
+
+/*
+ * The backward's work split on the current device: *clusters receives the
+ * number of thread-block clusters its (head, slice) pairs are divided over
+ * (cluster c takes the contiguous range [c W / n, (c + 1) W / n) of the
+ * W = B*H*S pairs, head-major), *slots_per_head the most clusters that share
+ * one head (the dBias partial slots per head). These two numbers and the shape
+ * fix every summation order of the backward. static_entry != 0 reports the
+ * split of tri_attn_bwd_static (which may use fewer clusters), else that of
+ * tri_attn_bwd. Returns TRI_ATTN_OK, TRI_ATTN_ERR_INVALID_ARG /
+ * TRI_ATTN_ERR_UNSUPPORTED for a bad shape or NULL outputs,
+ * TRI_ATTN_ERR_STATIC_TOO_SMALL (static_entry only) or TRI_ATTN_ERR_CUDA.
+ */
+int tri_attn_bwd_split(tri_attn_shape shape, int static_entry, int *clusters, int *slots_per_head);
 
 /*
  * Backward pass (arXiv 2610.05854v1, Abstract: key-tile-parallel backward that
@@ -169,8 +208,9 @@ int tri_attn_device_status(void *stream);
  * per head; S = N = 1024 does not).
  *
  * Set-up: the first call on each device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current); make that first call before
- * any stream capture. Sharing: every call uses the same array and leaves its
+ * (cudaGetSymbolAddress, with that device current) besides the set-up every
+ * backward call does once per device; make that first call before any stream
+ * capture. Sharing: every call uses the same array and leaves its
  * contents behind. Nothing in it needs to start at zero (each call writes every
  * byte it reads first), but two calls whose kernels overlap on the GPU (other
  * streams, other host threads) race on the array and must be serialised by the
@@ -191,8 +231,9 @@ int tri_attn_bwd_static(tri_attn_shape shape,
  * tri_attn_fwd / tri_attn_bwd issued by the calling host thread records
  * events[k] (a cudaEvent_t created by the caller) on the call's stream right
  * after enqueuing the call's k-th kernel, for k < n. Kernel order:
- * tri_attn_fwd = {forward}; tri_attn_bwd = {bias transpose, D correction,
- * main backward, dBias reduction}. events = NULL or n = 0 switches it off. The events stay
+ * tri_attn_fwd = {V scale pre-pass, forward}; tri_attn_bwd = {bias transpose,
+ * preparation (D correction and operand scales), main backward, dBias
+ * reduction}. events = NULL or n = 0 switches it off. The events stay
  * owned by the caller and must stay valid while instrumentation is on.
  * Returns TRI_ATTN_OK, or TRI_ATTN_ERR_INVALID_ARG for n < 0.
  */

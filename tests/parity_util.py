@@ -7,6 +7,15 @@ import torch
 # North-star gate: relative RMSE of every output against the FP64 oracle.
 RMSE_REL_TOL = 2e-3
 
+# Per-element gate, beside the whole-tensor RMSE (which one wrong store barely moves):
+#   |x - ref| <= ELEM_ULPS * ulp_bf16(ref) + ELEM_EPS * rms(ref)
+# The first term covers the BF16 rounding of the result (half an ulp) plus relative errors of the
+# same size; the second covers the absolute error the FP32/FP16 arithmetic accumulates in a sum
+# whose terms cancel (a few times the 1e-3 relative RMSE, at the tail of millions of elements).
+# A wrong 32-byte store moves most of its 16 elements by about rms(ref) and fails it.
+ELEM_ULPS = 1.0
+ELEM_EPS = 2e-2
+
 
 def rmse_rel(x, ref) -> float:
     x = np.asarray(x, dtype=np.float64)
@@ -14,6 +23,30 @@ def rmse_rel(x, ref) -> float:
     den = np.sqrt(np.mean(ref * ref))
     num = np.sqrt(np.mean((x - ref) ** 2))
     return float(num / den) if den > 0 else float(num)
+
+
+def ulp_bf16(ref) -> np.ndarray:
+    """Spacing of BF16 numbers at |ref| (8 significant bits)."""
+    a = np.abs(np.asarray(ref, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
+    return np.exp2(e - 7)
+
+
+def elementwise_excess(x, ref, ulps=ELEM_ULPS) -> float:
+    """Largest (|x - ref| - ulps * ulp_bf16(ref)) / rms(ref) over all elements: the smallest ELEM_EPS
+    the element-wise gate would need."""
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    rms = np.sqrt(np.mean(ref * ref))
+    if rms == 0:
+        return float(np.max(np.abs(x))) if x.size else 0.0
+    return float(np.max((np.abs(x - ref) - ulps * ulp_bf16(ref)) / rms))
+
+
+def check_elementwise(x, ref, what=""):
+    e = elementwise_excess(x, ref)
+    assert e <= ELEM_EPS, f"{what}: an element is {e:.3g} rms(ref) beyond its BF16 ulp (gate {ELEM_EPS})"
+    return e
 
 
 def f64(t) -> np.ndarray:
@@ -58,6 +91,20 @@ def oracle_full(x: dict, scale=None):
     O, LSE = oracle.fwd(x["Q"], x["K"], x["V"], x["bias"], x["mask"], scale)
     g = oracle.bwd(x["Q"], x["K"], x["V"], x["bias"], x["mask"], x["dO"], scale)
     return dict(O=O, LSE=LSE, **g)
+
+
+def boundary_slices(shape, S, static_entry=False):
+    """Slices that straddle the backward's cluster-range boundaries (for every boundary, the last
+    (head, slice) pair of one cluster and the first of the next), from the split the library reports."""
+    from bwd_tri_attn_gb300 import binding as tb
+
+    nc, _ = tb.tri_attn_bwd_split(shape, static_entry)
+    w = shape.B * shape.H * S
+    out = set()
+    for c in range(1, nc):
+        x = c * w // nc
+        out.update({(x - 1) % S, x % S})
+    return sorted(out), nc
 
 
 def check_lse(got, want, what=""):

@@ -2,7 +2,10 @@
 
 Gate (the benchmark spec): relative RMSE <= 2e-3 for O, dQ, dK, dV and dBias; LSE to
 FP32 accuracy; residual compensation lowers dQ, dK and dBias error; all
-outputs bitwise identical across repeated calls.
+outputs bitwise identical across repeated calls. Beside the RMSE, every
+compared element must lie within one BF16 ulp of the oracle plus a small
+fraction of the tensor's rms (tests/parity_util.py), which a single wrong store
+fails.
 
 Small and ragged shapes are compared on every element against the full
 oracle; the crop-size shapes run at full size on the GPU and are compared on
@@ -14,7 +17,8 @@ import pytest
 import torch
 
 from bwd_tri_attn_gb300 import workloads as wl
-from tests.parity_util import RMSE_REL_TOL, check_lse, f64, oracle_full, rmse_rel, run_cuda
+from tests.parity_util import (RMSE_REL_TOL, boundary_slices, check_elementwise, check_lse, f64, oracle_full,
+                               rmse_rel, run_cuda)
 
 pytestmark = pytest.mark.gpu
 
@@ -35,6 +39,8 @@ def _compare_all(got, want, what, tol=RMSE_REL_TOL):
     check_lse(f64(got["LSE"]), want["LSE"], what)
     bad = {k: v for k, v in errs.items() if not v <= tol}
     assert not bad, f"{what}: RMSE above {tol}: {errs}"
+    for k in ("O", "dQ", "dK", "dV", "dBias"):
+        check_elementwise(f64(got[k]), want[k], f"{what} {k}")
     return errs
 
 
@@ -202,18 +208,104 @@ def test_scale_argument_is_used():
     _compare_all(got, want, "scale")
 
 
-def test_residual_compensation_lowers_gradient_error():
-    # controlled ablation: same kernels, D from O + Ores versus from O alone
+# The FP16 operand staging against the whole BF16 range: the same problem with one tensor
+# scaled by a power of two (gradients of a loss scaled far down or up, tiny values, large
+# activations). Relative errors must not move.
+RANGE = [
+    ("dO_2^-20", {"dO": -20}),
+    ("dO_2^-12", {"dO": -12}),
+    ("dO_2^8", {"dO": 8}),
+    ("V_2^-16", {"V": -16}),
+    ("V_2^16", {"V": 16}),
+    ("dO_2^14", {"dO": 14}),
+    ("Q_2^-16_K_2^10", {"Q": -16, "K": 10}),
+    ("all_2^-30", {"Q": -30, "K": -30, "V": -30, "dO": -30}),
+]
+
+
+@pytest.mark.parametrize("d", [16, 32])
+@pytest.mark.parametrize("name,exps", RANGE, ids=[r[0] for r in RANGE])
+def test_input_range_full_oracle(name, exps, d):
+    # ragged: N = 200 (two key tiles, the second partial), S = 7, random key mask
+    x = wl.scale_pow2(wl.make_inputs(B=1, S=7, N=200, H=2, d=d, seed=51, mask=("random", 0.1)), exps)
+    got = run_cuda(x)
+    want = oracle_full(x)
+    _compare_all(got, want, f"{name}_d{d}")
+
+
+@pytest.mark.parametrize("name,exps", RANGE[:4], ids=[r[0] for r in RANGE[:4]])
+def test_input_range_crop384_sampled(name, exps):
+    w = wl.CROP384
+    x = wl.scale_pow2(wl.inputs_for(w), exps)
+    N = w.N
+    rows = [(0, h, j) for h in range(w.H) for j in (1, N - 2)]
+    _sampled_check(x, _split_slices(w)[:12], rows, f"crop384_{name}")
+
+
+ABLATION = [wl.CROP384, wl.CROP640_D16, wl.CROP640_D32, wl.CROP768]
+
+
+@pytest.mark.parametrize("w", ABLATION, ids=[w.name for w in ABLATION])
+def test_residual_compensation_lowers_gradient_error(w):
+    # Controlled ablation (same kernels, D from O + Ores versus from O alone) at the pages' crop
+    # sizes and head dimensions. dQ and dK are compared on 32 evenly spaced slices (a slice's dQ,
+    # dK depend on that slice alone), dBias on 32 rows summed over every slice.
+    import json
+    import os
+
+    import oracle
+
+    x = wl.inputs_for(w)
+    comp = run_cuda(x, residual=True)
+    plain = run_cuda(x, residual=False)
+    N = w.N
+    sl = sorted(set(int(round(k * (N - 1) / 31)) for k in range(32)))
+    sub = {k: (v[:, sl] if (v is not None and k in ("Q", "K", "V", "dO", "mask")) else v) for k, v in x.items()}
+    want = oracle_full(sub)
+    rows = [(0, h, j) for h in range(w.H) for j in range(0, N, N // 8)]
+    want_rows = oracle.dbias_rows(x["Q"], x["K"], x["V"], x["bias"], x["mask"], x["dO"], rows)
+    report = {}
+    for k in ("dQ", "dK", "dBias"):
+        if k == "dBias":
+            gc = np.stack([f64(comp[k][b, h, j]) for (b, h, j) in rows])
+            gp = np.stack([f64(plain[k][b, h, j]) for (b, h, j) in rows])
+            ref = want_rows
+        else:
+            gc, gp, ref = f64(comp[k][:, sl]), f64(plain[k][:, sl]), want[k]
+        ec, ep = rmse_rel(gc, ref), rmse_rel(gp, ref)
+        # the gradients are returned in BF16: their error has a floor, the BF16 rounding of the exact
+        # value, which no compensation removes; the residual acts on the error above it
+        floor = rmse_rel(torch.from_numpy(np.asarray(ref)).to(torch.bfloat16).double().numpy(), ref)
+        xc, xp = (max(e * e - floor * floor, 0.0) ** 0.5 for e in (ec, ep))
+        report[k] = {"compensated": ec, "uncompensated": ep, "reduction": 1.0 - ec / ep, "bf16_floor": floor,
+                     "reduction_above_floor": 1.0 - xc / xp if xp > 0 else 0.0}
+        assert ec <= RMSE_REL_TOL, f"{w.name} {k}: compensated RMSE {ec}"
+    print(f"residual ablation {w.name}:", json.dumps(report))
+    out = os.environ.get("TRI_ATTN_ABLATION_LOG")
+    if out:
+        with open(out, "a") as f:
+            f.write(json.dumps({"workload": w.name, **report}) + "\n")
+    for k, r in report.items():
+        assert r["reduction"] > 0.0, f"{w.name} {k}: residual compensation does not lower the error: {r}"
+        assert r["reduction_above_floor"] >= MIN_GAIN_ABOVE_FLOOR, f"{w.name} {k}: {r}"
+
+
+# The pages report 28-47 % lower dQ, dK and dBias RMSE from the residual at these crops. Here the
+# gradients leave the kernels in BF16, whose own rounding (about 1.6e-3 relative RMSE) dominates
+# their error; the residual must lower the total error on every crop and output, and the error
+# above that rounding floor by at least this fraction (measured values in the design notes).
+MIN_GAIN_ABOVE_FLOOR = 0.0
+
+
+def test_residual_compensation_full_tensor_crop384():
+    # the same ablation at crop 384 against the full oracle (every slice, the whole dBias)
     x = wl.inputs_for(wl.CROP384)
     want = oracle_full(x)
     comp = run_cuda(x, residual=True)
     plain = run_cuda(x, residual=False)
-    report = {}
     for k in ("dQ", "dK", "dBias"):
         ec, ep = rmse_rel(f64(comp[k]), want[k]), rmse_rel(f64(plain[k]), want[k])
-        report[k] = (ec, ep, 1.0 - ec / ep)
         assert ec < ep, f"{k}: compensated {ec} not below uncompensated {ep}"
-    print("residual ablation (compensated, uncompensated, reduction):", report)
     _compare_all(comp, want, "crop384")
 
 
@@ -226,12 +318,25 @@ def _sampled_check(x, slices, bias_rows, what, node=0):
     for k in ("O", "dQ", "dK", "dV"):
         e = rmse_rel(f64(got[k][:, slices]), want[k])
         assert e <= RMSE_REL_TOL, f"{what}: {k} RMSE {e}"
+        check_elementwise(f64(got[k][:, slices]), want[k], f"{what} {k}")
     check_lse(f64(got["LSE"][:, slices]), want["LSE"], what)
     rows = oracle.dbias_rows(x["Q"], x["K"], x["V"], x["bias"], x["mask"], x["dO"], bias_rows)
     gb = np.stack([f64(got["dBias"][b, h, j]) for (b, h, j) in bias_rows])
     e = rmse_rel(gb, rows)
     assert e <= RMSE_REL_TOL, f"{what}: dBias sampled-row RMSE {e}"
+    check_elementwise(gb, rows, f"{what} dBias rows")
     return got
+
+
+def _split_slices(w, node=0):
+    """The sampled slices of a full-size case: first, middle and last, plus every slice that
+    straddles one of the backward's cluster-range boundaries on this device."""
+    from bwd_tri_attn_gb300 import binding as tb
+
+    shape = tb.Shape(w.B, w.slices, w.N, w.H, w.d, 1.0 / w.d ** 0.5, node)
+    extra, _ = boundary_slices(shape, w.slices)
+    N = w.N
+    return sorted(set([0, N // 3, N - 1] + extra))
 
 
 FULL = [wl.CROP384, wl.CROP640_D16, wl.CROP640_D32, wl.CROP768]
@@ -241,9 +346,8 @@ FULL = [wl.CROP384, wl.CROP640_D16, wl.CROP640_D32, wl.CROP768]
 def test_full_size_sampled(w):
     x = wl.inputs_for(w)
     N = w.N
-    slices = [0, N // 3, N - 1]
     rows = [(0, h, j) for h in range(w.H) for j in (0, N // 2 + 1, N - 1)]
-    _sampled_check(x, slices, rows, w.name)
+    _sampled_check(x, _split_slices(w), rows, w.name)
 
 
 def test_ending_node_full_size():
@@ -260,8 +364,8 @@ def test_ending_node_in_place_full_size():
     # axis): no transposed copies
     x = wl.inputs_for(wl.CROP768)
     N = wl.CROP768.N
-    _sampled_check(x, [2, N // 2 + 3, N - 1], [(0, 2, 7), (0, 1, N - 1), (0, 3, 333)], "ending_node_in_place",
-                   node=1)
+    slices = sorted(set([2, N // 2 + 3, N - 1] + _split_slices(wl.CROP768, node=1)))
+    _sampled_check(x, slices, [(0, 2, 7), (0, 1, N - 1), (0, 3, 333)], "ending_node_in_place", node=1)
 
 
 ENDING = [
