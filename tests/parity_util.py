@@ -1,6 +1,8 @@
 """Helpers shared by the GPU parity tests: run the CUDA path, run the oracle, compare."""
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import torch
 
@@ -45,6 +47,10 @@ def elementwise_excess(x, ref, ulps=ELEM_ULPS) -> float:
 
 def check_elementwise(x, ref, what=""):
     e = elementwise_excess(x, ref)
+    log = os.environ.get("TRI_ATTN_ELEM_LOG")
+    if log:
+        with open(log, "a") as f:
+            f.write(f"{what}\t{e:.6g}\n")
     assert e <= ELEM_EPS, f"{what}: an element is {e:.3g} rms(ref) beyond its BF16 ulp (gate {ELEM_EPS})"
     return e
 
