@@ -1,4 +1,4 @@
-"""Thin ctypes binding of the C ABI in ``include/tri_attn.h``.
+"""Thin ctypes binding of the C ABI in ``include/tri_attn.h`` and ``include/tri_mul.h``.
 
 Argument marshalling only: PyTorch tensors supply device pointers and the
 current CUDA stream; every step of the computation runs in the library's
@@ -41,7 +41,16 @@ class TriAttnError(RuntimeError):
 
 _VP = ctypes.c_void_p
 EXPORTS = ("tri_attn_strerror", "tri_attn_fwd", "tri_attn_bwd_workspace_size", "tri_attn_bwd_split", "tri_attn_bwd",
-           "tri_attn_device_status", "tri_attn_set_timing_events", "tri_attn_bwd_static")
+           "tri_attn_device_status", "tri_attn_set_timing_events", "tri_attn_bwd_static", "tri_mul_fwd",
+           "tri_mul_bwd_workspace_size", "tri_mul_bwd")
+
+
+class MulShape(ctypes.Structure):
+    """tri_mul_shape: batch, residues, channels, direction (0 outgoing, 1 incoming)."""
+    _fields_ = [("B", ctypes.c_int), ("N", ctypes.c_int), ("C", ctypes.c_int), ("incoming", ctypes.c_int)]
+
+    def __repr__(self):
+        return f"MulShape(B={self.B}, N={self.N}, C={self.C}, incoming={self.incoming})"
 
 
 def lib_path() -> str:
@@ -75,6 +84,12 @@ def load(path: str | None = None):
         lib.tri_attn_bwd_static.restype = ctypes.c_int
         lib.tri_attn_set_timing_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]
         lib.tri_attn_set_timing_events.restype = ctypes.c_int
+        lib.tri_mul_fwd.argtypes = [MulShape] + [_VP] * 8
+        lib.tri_mul_fwd.restype = ctypes.c_int
+        lib.tri_mul_bwd_workspace_size.argtypes = [MulShape]
+        lib.tri_mul_bwd_workspace_size.restype = ctypes.c_size_t
+        lib.tri_mul_bwd.argtypes = [MulShape] + [_VP] * 12 + [ctypes.c_size_t, _VP]
+        lib.tri_mul_bwd.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -140,6 +155,22 @@ def tri_attn_bwd_static(shape: Shape, Q, K, V, bias, mask, O, Ores, LSE, dO, dQ,
     _check("tri_attn_bwd_static", rc)
 
 
+def tri_mul_fwd(shape: MulShape, Pa, Ga, Pb, Gb, A, Bm, X, stream=None):
+    rc = load().tri_mul_fwd(shape, _p(Pa), _p(Ga), _p(Pb), _p(Gb), _p(A), _p(Bm), _p(X), _stream(stream))
+    _check("tri_mul_fwd", rc)
+
+
+def tri_mul_bwd_workspace_size(shape: MulShape) -> int:
+    return int(load().tri_mul_bwd_workspace_size(shape))
+
+
+def tri_mul_bwd(shape: MulShape, Pa, Ga, Pb, Gb, A, Bm, dX, dPa, dGa, dPb, dGb, workspace, stream=None):
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().tri_mul_bwd(shape, _p(Pa), _p(Ga), _p(Pb), _p(Gb), _p(A), _p(Bm), _p(dX), _p(dPa), _p(dGa),
+                            _p(dPb), _p(dGb), _p(workspace), nbytes, _stream(stream))
+    _check("tri_mul_bwd", rc)
+
+
 def tri_attn_device_status(stream=None) -> int:
     return int(load().tri_attn_device_status(_stream(stream)))
 
@@ -190,3 +221,31 @@ def backward(Q, K, V, bias, mask, O, Ores, LSE, dO, scale=None, workspace=None, 
     dBias = torch.empty_like(bias)
     tri_attn_bwd(shape, Q, K, V, bias, mask, O, Ores, LSE, dO, dQ, dK, dV, dBias, workspace, stream)
     return dQ, dK, dV, dBias
+
+
+def mul_shape_of(Pa: torch.Tensor, incoming: bool = False) -> MulShape:
+    """Shape of the triangle multiplicative update on pair-layout projections [B, N, N, C]."""
+    B, N, N2, C = (int(x) for x in Pa.shape)
+    if N2 != N:
+        raise ValueError(f"pair tensor must be [B, N, N, C], got {tuple(Pa.shape)}")
+    return MulShape(B, N, C, int(bool(incoming)))
+
+
+def mul_forward(Pa, Ga, Pb, Gb, incoming=False, stream=None):
+    """Returns (X, A, Bm): X [B, C, N, N] channel-major, and the gated operands A, Bm
+    [B, C, N, N] that mul_backward reads."""
+    shape = mul_shape_of(Pa, incoming)
+    B, N, C = shape.B, shape.N, shape.C
+    A, Bm, X = (torch.empty((B, C, N, N), dtype=torch.bfloat16, device=Pa.device) for _ in range(3))
+    tri_mul_fwd(shape, Pa, Ga, Pb, Gb, A, Bm, X, stream)
+    return X, A, Bm
+
+
+def mul_backward(Pa, Ga, Pb, Gb, A, Bm, dX, incoming=False, workspace=None, stream=None):
+    """Returns (dPa, dGa, dPb, dGb) in the pair layout [B, N, N, C]; dX is channel-major."""
+    shape = mul_shape_of(Pa, incoming)
+    if workspace is None:
+        workspace = torch.empty(max(tri_mul_bwd_workspace_size(shape), 16), dtype=torch.uint8, device=Pa.device)
+    outs = [torch.empty_like(Pa) for _ in range(4)]
+    tri_mul_bwd(shape, Pa, Ga, Pb, Gb, A, Bm, dX, *outs, workspace, stream)
+    return tuple(outs)

@@ -93,6 +93,8 @@ cudaError_t mark(int k, cudaStream_t st) {
 namespace triattn {
 // Status word of the current device, for entry points defined in other files.
 int *device_status_word() { return status_word(); }
+// The calling thread's k-th timing event, for entry points defined in other files.
+cudaError_t timing_mark(int k, cudaStream_t st) { return mark(k, st); }
 }  // namespace triattn
 
 extern "C" {

@@ -547,13 +547,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
             }
           }
           float mt;
-          {
+          {  // row max with three-input max: one instruction per key pair
             float m8[8];
 #pragma unroll
             for (int c = 0; c < 8; ++c) m8[c] = fmaxf(x[c].x, x[c].y);
 #pragma unroll
-            for (int e = 8; e < 64; ++e) m8[e & 7] = fmaxf(m8[e & 7], fmaxf(x[e].x, x[e].y));
-            mt = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            for (int e = 8; e < 64; ++e) m8[e & 7] = fmax3(m8[e & 7], x[e].x, x[e].y);
+            mt = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
           }
           // lazy online-softmax rescale
           float alpha = 1.f;

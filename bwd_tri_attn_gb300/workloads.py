@@ -1,4 +1,4 @@
-"""Seeded synthetic inputs for triangle attention.
+"""Seeded synthetic inputs for triangle attention and the triangle multiplicative update.
 
 This module holds no arithmetic of the method: it only draws random tensors
 (CPU ``torch.Generator``, float32 normal draws rounded to BF16) in the shapes,
@@ -9,7 +9,9 @@ are fed from here.
 
 Layouts: Q, K, V, dO [B,S,N,H,d] (S = number of row-slices, equal to N for a
 square pair tensor); bias [B,H,N,N]; mask [B,S,N] additive BF16 (0 or -inf) or
-None.
+None. Triangle multiplication: projections P_a, G_a, P_b, G_b [B,N,N,C] (pair
+layout) and the output gradient dX [B,C,N,N] (channel-major), with the pair
+channel count of AlphaFold3-style trunks (128) at the attention's crop sizes.
 """
 from __future__ import annotations
 
@@ -133,3 +135,41 @@ def ending_node(t: torch.Tensor) -> torch.Tensor:
     transposed pair tensor.
     """
     return t.transpose(1, 2).contiguous()
+
+
+@dataclass(frozen=True)
+class MulWorkload:
+    """One named input recipe of the triangle multiplicative update."""
+
+    name: str
+    B: int
+    N: int
+    C: int
+    seed: int
+    std: float = 1.0       # projections P_a, P_b
+    gate_std: float = 1.0  # gate logits G_a, G_b
+    notes: str = field(default="", compare=False)
+
+    def flops(self) -> float:
+        """Algorithmic FLOPs of the contraction: 2 B C N^3 forward, twice that backward."""
+        return 2.0 * self.B * self.C * float(self.N) ** 3
+
+
+MUL_TINY = MulWorkload("mul_tiny_n16_c8", B=1, N=16, C=8, seed=10, notes="smallest supported shape")
+MUL_RAGGED = MulWorkload("mul_ragged_b2_n72_c24", B=2, N=72, C=24, seed=11, notes="N and C off every tile size")
+MUL_CROP384 = MulWorkload("mul_crop384_c128", B=1, N=384, C=128, seed=12, notes="crop 384, 128 pair channels")
+MUL_CROP768 = MulWorkload("mul_crop768_c128", B=1, N=768, C=128, seed=13, notes="crop 768, 128 pair channels")
+
+MUL_ALL = {w.name: w for w in (MUL_TINY, MUL_RAGGED, MUL_CROP384, MUL_CROP768)}
+
+
+def make_mul_inputs(B, N, C, seed, std=1.0, gate_std=1.0):
+    """Draws P_a, G_a, P_b, G_b ([B,N,N,C]) and dX ([B,C,N,N]) as BF16 on the CPU, in that order."""
+    gen = torch.Generator().manual_seed(int(seed))
+    pair = (B, N, N, C)
+    return {"Pa": _normal(gen, pair, std), "Ga": _normal(gen, pair, gate_std), "Pb": _normal(gen, pair, std),
+            "Gb": _normal(gen, pair, gate_std), "dX": _normal(gen, (B, C, N, N), 1.0)}
+
+
+def mul_inputs_for(w: MulWorkload):
+    return make_mul_inputs(w.B, w.N, w.C, w.seed, w.std, w.gate_std)

@@ -26,7 +26,7 @@ def _declared_functions():
     for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
         text = open(h).read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-        for m in re.finditer(r"\b(?:int|size_t|const char\s*\*|void)\s*\*?\s*(tri_attn_\w+)\s*\(", text):
+        for m in re.finditer(r"\b(?:int|size_t|const char\s*\*|void)\s*\*?\s*(tri_(?:attn|mul)_\w+)\s*\(", text):
             names.add(m.group(1))
     return sorted(names)
 
@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(lib):
     names = _declared_functions()
     assert {"tri_attn_fwd", "tri_attn_bwd", "tri_attn_bwd_workspace_size", "tri_attn_strerror",
             "tri_attn_device_status", "tri_attn_set_timing_events", "tri_attn_bwd_split",
-            "tri_attn_bwd_static"} <= set(names)
+            "tri_attn_bwd_static", "tri_mul_fwd", "tri_mul_bwd", "tri_mul_bwd_workspace_size"} <= set(names)
     for n in names:
         assert hasattr(lib, n), f"{n} declared in include/ but not exported"
 
@@ -161,3 +161,61 @@ def test_workspace_size_same_for_both_nodes(lib):
     b = lib.tri_attn_bwd_workspace_size(Shape(1, 96, 200, 4, 32, 0.17677669, 1))
     assert a == b
     assert (a > 0) == _has_device()
+
+
+# ---------------------------------------------------------------- triangle multiplication entry points
+MUL_GOOD = (1, 64, 16, 0)
+
+
+def _mul_fwd(lib, shape, **ptrs):
+    from bwd_tri_attn_gb300.binding import MulShape
+    names = ["Pa", "Ga", "Pb", "Gb", "A", "Bm", "X"]
+    args = [ctypes.c_void_p(ptrs.get(n, FAKE)) for n in names]
+    return lib.tri_mul_fwd(MulShape(*shape), *args, None)
+
+
+def _mul_bwd(lib, shape, ws_bytes, **ptrs):
+    from bwd_tri_attn_gb300.binding import MulShape
+    names = ["Pa", "Ga", "Pb", "Gb", "A", "Bm", "dX", "dPa", "dGa", "dPb", "dGb", "ws"]
+    args = [ctypes.c_void_p(ptrs.get(n, FAKE)) for n in names]
+    return lib.tri_mul_bwd(MulShape(*shape), *args, ctypes.c_size_t(ws_bytes), None)
+
+
+@pytest.mark.parametrize("shape,code", [
+    ((0, 64, 16, 0), -1),      # empty batch
+    ((1, 0, 16, 0), -1),       # no residues
+    ((1, 64, 0, 0), -1),       # no channels
+    ((1, 64, 16, 2), -1),      # unknown direction
+    ((1, 64, 16, -1), -1),
+    ((1, 8, 16, 0), -2),       # N below 16
+    ((1, 68, 16, 0), -2),      # N not a multiple of 8
+    ((1, 4104, 16, 0), -2),    # N above TRI_MUL_MAX_N
+    ((1, 64, 12, 0), -2),      # C not a multiple of 8
+    ((1, 64, 1032, 0), -2),    # C above TRI_MUL_MAX_C
+    ((65, 64, 1024, 0), -2),   # B * C above the grid limit
+])
+def test_mul_shape_validation(lib, shape, code):
+    assert _mul_fwd(lib, shape) == code
+    assert _mul_bwd(lib, shape, 1 << 40) == code
+
+
+@pytest.mark.parametrize("name", ["Pa", "Ga", "Pb", "Gb", "A", "Bm", "X"])
+def test_mul_fwd_pointer_checks(lib, name):
+    assert _mul_fwd(lib, MUL_GOOD, **{name: 0}) == -1
+    assert _mul_fwd(lib, MUL_GOOD, **{name: FAKE + 2}) == -2
+
+
+@pytest.mark.parametrize("name", ["Pa", "Ga", "Pb", "Gb", "A", "Bm", "dX", "dPa", "dGa", "dPb", "dGb"])
+def test_mul_bwd_pointer_checks(lib, name):
+    assert _mul_bwd(lib, MUL_GOOD, 1 << 40, **{name: 0}) == -1
+    assert _mul_bwd(lib, MUL_GOOD, 1 << 40, **{name: FAKE + 2}) == -2
+
+
+def test_mul_workspace_checks(lib):
+    from bwd_tri_attn_gb300.binding import MulShape
+    need = lib.tri_mul_bwd_workspace_size(MulShape(*MUL_GOOD))
+    assert need == 2 * 4 * 1 * 16 * 64 * 64  # two FP32 [B, C, N, N] stacks, known without a device
+    assert lib.tri_mul_bwd_workspace_size(MulShape(1, 68, 16, 0)) == 0
+    assert _mul_bwd(lib, MUL_GOOD, need - 1) == -3
+    assert _mul_bwd(lib, MUL_GOOD, need, ws=0) == -3
+    assert _mul_bwd(lib, MUL_GOOD, need, ws=FAKE + 8) == -2

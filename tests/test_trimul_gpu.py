@@ -1,0 +1,207 @@
+"""GPU parity of the triangle multiplicative update against the FP64 oracle (oracle/trimul.py).
+
+The CUDA path runs through the C ABI (tri_mul_fwd / tri_mul_bwd via the ctypes binding); the oracle
+gets the same seeded BF16 inputs. Small shapes compare every element of every output; the crop-768
+workload compares whole channels (each channel of the update is an independent matrix product, so a
+channel slice of the inputs gives the oracle's exact value for that channel).
+
+Tolerances, derived from the arithmetic and computed from oracle values only:
+- gated operands A, Bm: the kernel evaluates sigmoid(G) P in FP32 with a relative error below
+  GATE_REL = 2^-17 (|G| < 16: the exponential's error grows with |G|), then rounds to BF16. Its BF16
+  value therefore equals the FP64 one except where the exact value lies within GATE_REL of a
+  rounding midpoint ("ambiguous" elements, about 0.3 %), where it may be one ulp away. Checked
+  exactly: equal everywhere else, at most one ulp at ambiguous elements.
+- X = sum_k a b with FP32 accumulation of exact BF16 products: per element
+      |X - ref| <= ulp_bf16(ref) + GAMMA * sum_k |a||b| + sum_k (amb_a ulp(a) |b| + |a| amb_b ulp(b))
+  (output rounding; accumulation, GAMMA = N 2^-22, four times the textbook bound since the
+  tensor cores' addition order is not specified; one ulp for every ambiguous operand);
+- dA = dX Bm likewise (dX is exact BF16), dB = dX^T A, then dP = dA sigmoid(G) and
+  dG = dA P sigmoid(G)(1 - sigmoid(G)) in FP32: the dA bound carried through the factors, the
+  FP32 sigmoid's relative error SIG_REL = 2^-20 (and its effect on 1 - sigmoid, relative
+  SIG_REL sigmoid / (1 - sigmoid)), a few FP32 roundings, and the output ulp.
+Whole-tensor relative RMSE <= 2e-3 is checked as well.
+"""
+import numpy as np
+import pytest
+import torch
+
+from bwd_tri_attn_gb300 import workloads as wl
+from oracle import trimul as om
+from tests.parity_util import rmse_rel, ulp_bf16
+
+pytestmark = pytest.mark.gpu
+
+RMSE_TOL = 2e-3
+GATE_REL = 2.0 ** -17
+SIG_REL = 2.0 ** -20
+
+
+def _lib():
+    from bwd_tri_attn_gb300 import _build, binding
+    _build.build()
+    binding.load()
+    return binding
+
+
+def _f64(t):
+    return t.detach().to("cpu").double().numpy()
+
+
+def run_cuda(x, incoming):
+    tb = _lib()
+    d = {k: v.cuda().contiguous() for k, v in x.items()}
+    X, A, Bm = tb.mul_forward(d["Pa"], d["Ga"], d["Pb"], d["Gb"], incoming=incoming)
+    dPa, dGa, dPb, dGb = tb.mul_backward(d["Pa"], d["Ga"], d["Pb"], d["Gb"], A, Bm, d["dX"], incoming=incoming)
+    torch.cuda.synchronize()
+    assert tb.tri_attn_device_status() == 0
+    out = dict(X=X, A=A, Bm=Bm, dPa=dPa, dGa=dGa, dPb=dPb, dGb=dGb)
+    return {k: v.cpu() for k, v in out.items()}
+
+
+def channel_major(a):
+    """[B, N, N, C] -> [B, C, N, N]."""
+    return np.ascontiguousarray(np.moveaxis(a, -1, 1))
+
+
+def ambiguous(exact):
+    """Elements whose exact value lies within GATE_REL (relative) of a BF16 rounding midpoint."""
+    a = np.abs(exact)
+    u = ulp_bf16(exact)
+    frac = np.mod(a, u) / u  # position inside the BF16 interval, in ulps
+    return (np.abs(frac - 0.5) * u <= GATE_REL * a) & (a > 0)
+
+
+def oracle_all(x, incoming):
+    """Oracle outputs (channel-major X, A, Bm; pair-layout gradients) and a per-element tolerance
+    for each, from the oracle's values only."""
+    pa, ga, pb, gb = (_f64(x[k]) for k in ("Pa", "Ga", "Pb", "Gb"))
+    dX = np.moveaxis(_f64(x["dX"]), 1, -1)  # channel-major -> pair layout
+    a, b = om.gated(pa, ga), om.gated(pb, gb)
+    amb_a, amb_b = ambiguous(om.gated(pa, ga, bf16=False)), ambiguous(om.gated(pb, gb, bf16=False))
+    da_ulp, db_ulp = amb_a * ulp_bf16(a), amb_b * ulp_bf16(b)
+    N = pa.shape[1]
+    gamma = N * 2.0 ** -22
+    # bounds go through BLAS-backed contractions (they are tolerances, not the oracle's arithmetic)
+    spec = "bkic,bkjc->bijc" if incoming else "bikc,bjkc->bijc"
+    c = lambda u, v: np.einsum(spec, u, v, optimize=True)
+    X = om.fwd(pa, ga, pb, gb, incoming)
+    tX = ulp_bf16(X) + gamma * c(np.abs(a), np.abs(b)) + c(da_ulp, np.abs(b)) + c(np.abs(a), db_ulp)
+    g = om.bwd(pa, ga, pb, gb, dX, incoming)
+    # bounds on dA = dX Bm and dB = dX^T A (the same contractions as the oracle's gradients)
+    if incoming:
+        tdA = np.einsum("bijc,bkjc->bkic", np.abs(dX), gamma * np.abs(b) + db_ulp, optimize=True)
+        tdB = np.einsum("bijc,bkic->bkjc", np.abs(dX), gamma * np.abs(a) + da_ulp, optimize=True)
+    else:
+        tdA = np.einsum("bijc,bjkc->bikc", np.abs(dX), gamma * np.abs(b) + db_ulp, optimize=True)
+        tdB = np.einsum("bijc,bikc->bjkc", np.abs(dX), gamma * np.abs(a) + da_ulp, optimize=True)
+    sa, sb = om.sigmoid(ga), om.sigmoid(gb)
+    tol = {"X": tX}
+    for name, t, s_, p in (("a", tdA, sa, pa), ("b", tdB, sb, pb)):
+        dP, dG = g["dP" + name], g["dG" + name]
+        tol["dP" + name] = ulp_bf16(dP) + t * s_ + (SIG_REL + 2.0 ** -23) * np.abs(dP)
+        tol["dG" + name] = (ulp_bf16(dG) + t * np.abs(p) * s_ * (1 - s_)
+                            + (SIG_REL * (1 + s_ / (1 - s_)) + 2.0 ** -22) * np.abs(dG))
+    if incoming:  # the stored operands hold the pair axes swapped (summed index innermost)
+        a, b = np.swapaxes(a, 1, 2), np.swapaxes(b, 1, 2)
+        amb_a, amb_b = np.swapaxes(amb_a, 1, 2), np.swapaxes(amb_b, 1, 2)
+    out = dict(X=channel_major(X), A=channel_major(a), Bm=channel_major(b), **g)
+    tol["X"] = channel_major(tol["X"])
+    amb = dict(A=channel_major(amb_a), Bm=channel_major(amb_b))
+    return out, tol, amb
+
+
+def check_operand(got, want, amb, what):
+    got, want = _f64(got), np.asarray(want)
+    diff = np.abs(got - want)
+    assert np.all(diff[~amb] == 0), f"{what}: {np.count_nonzero(diff[~amb])} unambiguous elements differ"
+    assert np.all(diff[amb] <= ulp_bf16(want[amb])), f"{what}: an ambiguous element is more than one ulp off"
+
+
+def check_value(got, want, tol, what):
+    got, want = _f64(got), np.asarray(want, dtype=np.float64)
+    r = rmse_rel(got, want)
+    assert r <= RMSE_TOL, f"{what}: relative RMSE {r:.3e}"
+    ratio = np.abs(got - want) / tol
+    worst = np.unravel_index(np.argmax(ratio), ratio.shape)
+    assert ratio[worst] <= 1.0, (f"{what}: |err| {abs(got[worst] - want[worst]):.3g} exceeds its bound "
+                                 f"{tol[worst]:.3g} at {worst}")
+    return float(ratio.max())
+
+
+def check_all(got, ref, tol, amb):
+    check_operand(got["A"], ref["A"], amb["A"], "A")
+    check_operand(got["Bm"], ref["Bm"], amb["Bm"], "Bm")
+    for k in ("X", "dPa", "dGa", "dPb", "dGb"):
+        check_value(got[k], ref[k], tol[k], k)
+
+
+SMALL = [(1, 16, 8, 10), (2, 72, 24, 11), (1, 136, 72, 14), (1, 264, 16, 15)]
+
+
+@pytest.mark.parametrize("incoming", [False, True])
+@pytest.mark.parametrize("B,N,C,seed", SMALL)
+def test_full_parity_small(B, N, C, seed, incoming):
+    x = wl.make_mul_inputs(B, N, C, seed)
+    got = run_cuda(x, incoming)
+    check_all(got, *oracle_all(x, incoming))
+
+
+@pytest.mark.parametrize("incoming", [False, True])
+def test_crop768_sampled_channels(incoming):
+    """The full crop-768 workload (B=1, N=768, C=128) in one launch configuration; three channels
+    (in both gating channel groups and in three of the gradient kernel's groups) checked whole."""
+    w = wl.MUL_CROP768
+    x = wl.mul_inputs_for(w)
+    got = run_cuda(x, incoming)
+    cs = [0, 77, 127]
+    sl = {k: (v[..., cs] if k != "dX" else v[:, cs]) for k, v in x.items()}
+    sub = {k: (v[:, cs] if k in ("X", "A", "Bm") else v[..., cs]) for k, v in got.items()}
+    check_all(sub, *oracle_all(sl, incoming))
+
+
+def test_zero_projection_gives_exact_zeros():
+    """P_a = 0: a = 0, so X = 0 and dG_a, dP_b, dG_b vanish exactly (dB = dX^T A = 0); dP_a =
+    dA sigmoid(G_a) still carries values (checked against the oracle)."""
+    x = wl.make_mul_inputs(1, 96, 16, 16)
+    x["Pa"] = torch.zeros_like(x["Pa"])
+    got = run_cuda(x, False)
+    assert torch.count_nonzero(got["A"]) == 0 and torch.count_nonzero(got["X"]) == 0
+    assert torch.count_nonzero(got["dGa"]) == 0 and torch.count_nonzero(got["dPb"]) == 0
+    assert torch.count_nonzero(got["dGb"]) == 0  # dG_b = dB P_b s(1-s), dB = dX^T A = 0
+    ref, tol, _ = oracle_all(x, False)
+    check_value(got["dPa"], ref["dPa"], tol["dPa"], "dPa")
+
+
+@pytest.mark.parametrize("incoming", [False, True])
+def test_deterministic(incoming):
+    x = wl.make_mul_inputs(1, 200, 32, 17)
+    a, b = run_cuda(x, incoming), run_cuda(x, incoming)
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
+
+
+def test_incoming_is_outgoing_of_transposed_inputs():
+    """The incoming update on P equals the outgoing update on the pair-transposed P (both computed on
+    the GPU; exact, since both run the same sums in the same order)."""
+    x = wl.make_mul_inputs(1, 80, 16, 18)
+    t = {k: (v.transpose(1, 2).contiguous() if k != "dX" else v) for k, v in x.items()}
+    a, b = run_cuda(x, True), run_cuda(t, False)
+    assert torch.equal(a["X"], b["X"]) and torch.equal(a["A"], b["A"])
+    for k in ("dPa", "dGa", "dPb", "dGb"):
+        assert torch.equal(a[k], b[k].transpose(1, 2)), k
+
+
+def test_device_errors_before_launch():
+    tb = _lib()
+    from bwd_tri_attn_gb300.binding import MulShape, TriAttnError
+    x = {k: v.cuda() for k, v in wl.make_mul_inputs(1, 64, 8, 19).items()}
+    X, A, Bm = tb.mul_forward(x["Pa"], x["Ga"], x["Pb"], x["Gb"])
+    shape = MulShape(1, 64, 8, 0)
+    need = tb.tri_mul_bwd_workspace_size(shape)
+    small = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
+    outs = [torch.empty_like(x["Pa"]) for _ in range(4)]
+    with pytest.raises(TriAttnError) as e:
+        tb.tri_mul_bwd(shape, x["Pa"], x["Ga"], x["Pb"], x["Gb"], A, Bm, x["dX"], *outs, small)
+    assert e.value.code == -3
+    torch.cuda.synchronize()
+    assert tb.tri_attn_device_status() == 0
