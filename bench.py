@@ -257,6 +257,93 @@ def run_reference(args, w):
     }))
 
 
+# Triangle multiplicative update, measured beside the attention (same step discipline):
+# kernels per fwd+bwd step in the library's event order, per layout of the projections.
+MUL_KERNELS = {0: ["mul_gate", "mul_gemm_x", "mul_gemm_da", "mul_gemm_db", "mul_gate_bwd"],
+               1: ["mul_gate", "mul_gemm_x", "mul_gemm_da_gate", "mul_gemm_db_gate"]}
+MUL_NFWD = 2
+
+
+def mul_roofline(kernel_ms, B, N, C, peaks):
+    """Per-kernel roofline of the triangle multiplication: the three contractions against the BF16
+    tensor peak (2 B C N^3 FLOPs each) and all kernels against HBM. Algorithmic bytes per element of
+    one [B, N, N, C] tensor: gating reads P, G of both operands and writes both gated operands
+    (12 B); the X contraction reads A, Bm and writes X (6 B); in the pair layout the dA and dB
+    contractions read two BF16 operands and write FP32 (8 B) and the gating gradient reads dA, dB,
+    P, G of both operands and writes four BF16 gradients (24 B); in the channel-major layout each
+    backward contraction reads two operands, P and G, and writes dP and dG (12 B)."""
+    E = B * N * N * C
+    flops = 2.0 * B * C * float(N) ** 3
+    bytes_of = {"mul_gate": 12 * E, "mul_gemm_x": 6 * E, "mul_gemm_da": 8 * E, "mul_gemm_db": 8 * E,
+                "mul_gate_bwd": 24 * E, "mul_gemm_da_gate": 12 * E, "mul_gemm_db_gate": 12 * E}
+    out = {}
+    for k, ms in kernel_ms.items():
+        gbs = bytes_of[k] / (ms * 1e-3) / 1e9
+        r = {"ms": ms, "hbm_gbs": gbs, "hbm_frac": gbs / peaks["hbm_gbs"], "bytes": bytes_of[k]}
+        if "gemm" in k:
+            tf = flops / (ms * 1e-3) / 1e12
+            r.update({"tflops": tf, "tensor_frac": tf / peaks["bf16_tflops"]})
+        out[k] = r
+    return out
+
+
+def run_trimul(dev, stream, steps, incoming=False, layout=1):
+    """Times the triangle multiplicative update (fwd + bwd) at crop 768, 128 channels."""
+    import torch
+
+    from bwd_tri_attn_gb300 import binding as tb
+    from bwd_tri_attn_gb300 import workloads as wl
+
+    mw = wl.MUL_CROP768
+    x = {k: v.to(dev) for k, v in wl.mul_inputs_for(mw).items()}
+    if layout == tb.LAYOUT_CHANNEL_MAJOR:
+        x = {k: (v.permute(0, 3, 1, 2).contiguous() if k != "dX" else v) for k, v in x.items()}
+    shape = tb.mul_shape_of(x["Pa"], incoming, layout)
+    B, N, C = shape.B, shape.N, shape.C
+    A, Bm, X = (torch.empty((B, C, N, N), dtype=torch.bfloat16, device=dev) for _ in range(3))
+    grads = [torch.empty_like(x["Pa"]) for _ in range(4)]
+    ws = torch.empty(max(16, tb.tri_mul_bwd_workspace_size(shape)), dtype=torch.uint8, device=dev)
+    names = MUL_KERNELS[layout]
+
+    def step(marks=None):
+        if marks:
+            tb.tri_attn_set_timing_events(marks[:MUL_NFWD])
+        tb.tri_mul_fwd(shape, x["Pa"], x["Ga"], x["Pb"], x["Gb"], A, Bm, X, stream)
+        if marks:
+            tb.tri_attn_set_timing_events(marks[MUL_NFWD:])
+        tb.tri_mul_bwd(shape, x["Pa"], x["Ga"], x["Pb"], x["Gb"], A, Bm, x["dX"], *grads, ws, stream)
+
+    for _ in range(3):
+        step()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    marks = [[torch.cuda.Event(enable_timing=True) for _ in names] for _ in range(steps)]
+    for e in starts + [m for ms in marks for m in ms]:
+        e.record(stream)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for k in range(steps):
+        starts[k].record(stream)
+        step(marks[k])
+    t1.record(stream)
+    tb.tri_attn_set_timing_events(None)
+    torch.cuda.synchronize()
+    assert tb.tri_attn_device_status() == 0
+    per = {n: 0.0 for n in names}
+    for k in range(steps):
+        chain = [starts[k]] + marks[k]
+        for n, (a, b) in enumerate(zip(chain[:-1], chain[1:])):
+            per[names[n]] += a.elapsed_time(b) / steps
+    ms = t0.elapsed_time(t1) / steps
+    peaks = load_peaks()
+    return {"workload": mw.name, "direction": "incoming" if incoming else "outgoing",
+            "layout": "channel-major" if layout == tb.LAYOUT_CHANNEL_MAJOR else "pair",
+            "B": B, "N": N, "C": C, "ms_per_step": ms, "tflops": 3 * mw.flops() / (ms * 1e-3) / 1e12,
+            "flops_per_step": 3 * mw.flops(), "steps": steps,
+            "l2": "inputs and operands larger than L2 (each [B,N,N,C] tensor is 151 MB), no flush",
+            "kernels": mul_roofline(per, B, N, C, peaks), "gpu_launches": steps * len(names)}
+
+
 def run_ours(args, w):
     import torch
     import torch.distributed as dist
@@ -446,6 +533,11 @@ def run_ours(args, w):
         cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "seconds": dt,
                "sample": f"{args.cpu_slices} of {w.slices} slices (all {w.H} heads, full N={w.N}), fwd+bwd"}
 
+    mul = None
+    if not args.no_trimul:
+        mul = [run_trimul(dev, stream, max(3, min(K, 20)), layout=lay) for lay in (tb.LAYOUT_CHANNEL_MAJOR,
+                                                                                   tb.LAYOUT_PAIR)]
+
     in_bytes = sum(v.numel() * v.element_size() for v in x.values() if v is not None)
     if rank == 0:
         line = {
@@ -460,7 +552,7 @@ def run_ours(args, w):
                        "reported": "median window"},
             "pct_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
             "kernel_ms": kernel_ms, "hbm": hbm, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": K * len(KERNELS), "clocks": clocks.summary(),
+            "gpu_launches": K * len(KERNELS), "clocks": clocks.summary(), "trimul": mul,
         }
         print(json.dumps(line))
     if world > 1:
@@ -482,6 +574,7 @@ def main():
     ap.add_argument("--ref-slices", type=int, default=4, help="slices per step of the reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-trimul", action="store_true", help="skip the triangle multiplication sub-line")
     ap.add_argument("--windows", type=int, default=0,
                     help="timed windows of --steps steps (0: enough to fill about a second, at least 3)")
     args = ap.parse_args()

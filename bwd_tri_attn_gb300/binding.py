@@ -45,12 +45,18 @@ EXPORTS = ("tri_attn_strerror", "tri_attn_fwd", "tri_attn_bwd_workspace_size", "
            "tri_mul_bwd_workspace_size", "tri_mul_bwd")
 
 
+LAYOUT_PAIR, LAYOUT_CHANNEL_MAJOR = 0, 1  # tri_mul_shape.layout
+
+
 class MulShape(ctypes.Structure):
-    """tri_mul_shape: batch, residues, channels, direction (0 outgoing, 1 incoming)."""
-    _fields_ = [("B", ctypes.c_int), ("N", ctypes.c_int), ("C", ctypes.c_int), ("incoming", ctypes.c_int)]
+    """tri_mul_shape: batch, residues, channels, direction (0 outgoing, 1 incoming), layout of the
+    projections and their gradients (LAYOUT_PAIR [B,N,N,C] or LAYOUT_CHANNEL_MAJOR [B,C,N,N])."""
+    _fields_ = [("B", ctypes.c_int), ("N", ctypes.c_int), ("C", ctypes.c_int), ("incoming", ctypes.c_int),
+                ("layout", ctypes.c_int)]
 
     def __repr__(self):
-        return f"MulShape(B={self.B}, N={self.N}, C={self.C}, incoming={self.incoming})"
+        return (f"MulShape(B={self.B}, N={self.N}, C={self.C}, incoming={self.incoming}, "
+                f"layout={self.layout})")
 
 
 def lib_path() -> str:
@@ -223,27 +229,31 @@ def backward(Q, K, V, bias, mask, O, Ores, LSE, dO, scale=None, workspace=None, 
     return dQ, dK, dV, dBias
 
 
-def mul_shape_of(Pa: torch.Tensor, incoming: bool = False) -> MulShape:
-    """Shape of the triangle multiplicative update on pair-layout projections [B, N, N, C]."""
-    B, N, N2, C = (int(x) for x in Pa.shape)
+def mul_shape_of(Pa: torch.Tensor, incoming: bool = False, layout: int = LAYOUT_PAIR) -> MulShape:
+    """Shape of the triangle multiplicative update on projections [B, N, N, C] (pair layout) or
+    [B, C, N, N] (channel-major)."""
+    if layout == LAYOUT_PAIR:
+        B, N, N2, C = (int(x) for x in Pa.shape)
+    else:
+        B, C, N, N2 = (int(x) for x in Pa.shape)
     if N2 != N:
-        raise ValueError(f"pair tensor must be [B, N, N, C], got {tuple(Pa.shape)}")
-    return MulShape(B, N, C, int(bool(incoming)))
+        raise ValueError(f"projection must be square in its two position axes, got {tuple(Pa.shape)}")
+    return MulShape(B, N, C, int(bool(incoming)), int(layout))
 
 
-def mul_forward(Pa, Ga, Pb, Gb, incoming=False, stream=None):
+def mul_forward(Pa, Ga, Pb, Gb, incoming=False, layout=LAYOUT_PAIR, stream=None):
     """Returns (X, A, Bm): X [B, C, N, N] channel-major, and the gated operands A, Bm
     [B, C, N, N] that mul_backward reads."""
-    shape = mul_shape_of(Pa, incoming)
+    shape = mul_shape_of(Pa, incoming, layout)
     B, N, C = shape.B, shape.N, shape.C
     A, Bm, X = (torch.empty((B, C, N, N), dtype=torch.bfloat16, device=Pa.device) for _ in range(3))
     tri_mul_fwd(shape, Pa, Ga, Pb, Gb, A, Bm, X, stream)
     return X, A, Bm
 
 
-def mul_backward(Pa, Ga, Pb, Gb, A, Bm, dX, incoming=False, workspace=None, stream=None):
-    """Returns (dPa, dGa, dPb, dGb) in the pair layout [B, N, N, C]; dX is channel-major."""
-    shape = mul_shape_of(Pa, incoming)
+def mul_backward(Pa, Ga, Pb, Gb, A, Bm, dX, incoming=False, layout=LAYOUT_PAIR, workspace=None, stream=None):
+    """Returns (dPa, dGa, dPb, dGb) in the projections' layout; dX is channel-major."""
+    shape = mul_shape_of(Pa, incoming, layout)
     if workspace is None:
         workspace = torch.empty(max(tri_mul_bwd_workspace_size(shape), 16), dtype=torch.uint8, device=Pa.device)
     outs = [torch.empty_like(Pa) for _ in range(4)]

@@ -32,16 +32,37 @@
 namespace triattn {
 using namespace sm100;
 
+cudaError_t timing_mark(int k, cudaStream_t st);
+int *device_status_word();
+
 namespace {
 
-__device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + __expf(-x)); }
+// sigmoid in FP32 from the fast exponential and reciprocal: relative error a few ulp for the gate
+// logits of practice (|x| < 16); 0 below x = -87, where 1 + exp(-x) overflows.
+__device__ __forceinline__ float sigmoid_f(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// Both gating kernels run a 1-D grid of (batch, r tile, s tile, channel group, operand) with the
+// operand and then the channel group varying fastest: the CTAs that read the same pair positions
+// (their channel groups share cache lines) run at the same time.
+__device__ __forceinline__ void tile_of(int N, int groups, int &op, int &grp, int &b, int &r0, int &s0) {
+  const int nt = (N + 15) / 16;
+  int u = blockIdx.x;
+  op = u & 1;
+  u >>= 1;
+  grp = u % groups;
+  u /= groups;
+  s0 = (u % nt) * 16;
+  u /= nt;
+  r0 = (u % nt) * 16;
+  b = u / nt;
+}
+
 // ---------------------------------------------------------------- gating: pair -> channel-major
 // One CTA: 16 x 16 output positions (r, s) and a group of up to 64 channels, for one of the two
-// operands (blockIdx.z = (batch * groups + group) * 2 + operand). Input position (x, y) = (r, s),
+// operands. Input position (x, y) = (r, s),
 // or (s, r) when the operand is transposed (incoming update). Each thread reads 16 channel bytes
 // of two neighbouring positions s, s + 1 and writes the gated pairs as 32-bit words
 // (a(s), a(s + 1)) into shared memory [channel][r][s / 2]; the channel stride (145 words) and
@@ -59,9 +80,9 @@ struct GateArgs {
 
 __global__ void __launch_bounds__(kGateThreads) trimul_gate_kernel(const GateArgs g) {
   extern __shared__ uint32_t tw[];  // [64][145] words
-  const int op = blockIdx.z & 1, grp = (blockIdx.z >> 1) % g.groups, b = (blockIdx.z >> 1) / g.groups;
+  int op, grp, b, r0, s0;
+  tile_of(g.N, g.groups, op, grp, b, r0, s0);
   const int N = g.N, C = g.C, c0 = grp * kGateCG, nq = min(kGateCG, C - c0) / 8;
-  const int r0 = blockIdx.y * kGateT, s0 = blockIdx.x * kGateT;
   const uint4 *P = reinterpret_cast<const uint4 *>(op ? g.P[1] : g.P[0]),
               *G = reinterpret_cast<const uint4 *>(op ? g.G[1] : g.G[0]);
   const int64_t cv = C / 8;
@@ -119,9 +140,9 @@ struct GateBwdArgs {
 
 __global__ void __launch_bounds__(kGateThreads) trimul_gate_bwd_kernel(const GateBwdArgs g) {
   extern __shared__ float tf[];  // [32][289]
-  const int op = blockIdx.z & 1, grp = (blockIdx.z >> 1) % g.groups, b = (blockIdx.z >> 1) / g.groups;
+  int op, grp, b, r0, s0;
+  tile_of(g.N, g.groups, op, grp, b, r0, s0);
   const int N = g.N, C = g.C, c0 = grp * kGbCG, nq = min(kGbCG, C - c0) / 8;
-  const int r0 = blockIdx.y * kGateT, s0 = blockIdx.x * kGateT;
   const float *dA = op ? g.dA[1] : g.dA[0];
   for (int e = threadIdx.x; e < kGbCG * kGateT * 4; e += kGateThreads) {
     const int qt = e & 3, rl = (e >> 2) & 15, cl = e >> 6;
@@ -159,35 +180,112 @@ __global__ void __launch_bounds__(kGateThreads) trimul_gate_bwd_kernel(const Gat
   }
 }
 
+// ---------------------------------------------------------------- gating, channel-major layout
+// A = bf16(sigmoid(G) P) element by element when P and G are already channel-major [B, C, N, N]:
+// a streaming kernel, 16-byte loads and stores, four chunks of 8 values per thread in flight.
+struct GateCmArgs {
+  const uint16_t *P[2], *G[2];
+  uint16_t *out[2];
+  int64_t chunks;  // 8-value chunks per operand
+};
+
+__global__ void __launch_bounds__(256) trimul_gate_cm_kernel(const GateCmArgs g) {
+  const int op = blockIdx.y;
+  const uint4 *P = reinterpret_cast<const uint4 *>(op ? g.P[1] : g.P[0]),
+              *G = reinterpret_cast<const uint4 *>(op ? g.G[1] : g.G[0]);
+  uint4 *out = reinterpret_cast<uint4 *>(op ? g.out[1] : g.out[0]);
+  const int64_t base = (int64_t)blockIdx.x * (256 * 4) + threadIdx.x;
+  uint4 pv[4], gv[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int64_t i = base + 256 * k;
+    if (i < g.chunks) pv[k] = P[i], gv[k] = G[i];
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int64_t i = base + 256 * k;
+    if (i >= g.chunks) continue;
+    const uint32_t pw[4] = {pv[k].x, pv[k].y, pv[k].z, pv[k].w}, gw[4] = {gv[k].x, gv[k].y, gv[k].z, gv[k].w};
+    uint32_t o[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w)
+      o[w] = pack_bf16x2(sigmoid_f(bf16_lo(gw[w])) * bf16_lo(pw[w]), sigmoid_f(bf16_hi(gw[w])) * bf16_hi(pw[w]));
+    out[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
 // ---------------------------------------------------------------- batched GEMM D = A B^T
 // D[t][m][n] = sum_k Aop[t][m][k] Bop[t][n][k] for a stack of N x N BF16 matrices (t = batch x
 // channel), FP32 accumulation in TMEM. Operand storage: K-major = [m][k] (k contiguous), MN-major
-// = [k][m] (m contiguous). D is row-major [t][m][n], BF16 or FP32.
+// = [k][m] (m contiguous). The epilogue either stores D (row-major [t][m][n], BF16 or FP32) or,
+// for the backward pass in the channel-major layout, applies the gating gradient to D = dA on
+// the fly: dP = dA sigmoid(G), dG = dA P sigmoid(G) (1 - sigmoid(G)), with P and G read at the
+// same [t][m][n] positions.
 //
 // Persistent CTAs, one per SM, walk the tiles t, m / 128, n / 256 (n fastest). Warp 0 issues the
 // TMA loads of a 4-stage ring (K step 64: one 128-byte swizzle atom of the K-major rows, or 64 rows
 // of the MN-major ones); warp 1 owns TMEM and issues the tcgen05.mma (M = 128, N = 256, K = 16)
-// into one of two accumulators; warps 2-5 read the other accumulator out and store it, so the
-// epilogue of one tile overlaps the main loop of the next.
+// into one of two accumulators; warps 2-9 (two per TMEM lane quarter, one per half of the
+// columns) read the other accumulator out, so the epilogue of one tile overlaps the main loop of
+// the next.
+enum { kEpiBF16 = 0, kEpiF32 = 1, kEpiGate = 2 };
+
+struct GemmIO {
+  void *D;                // kEpiBF16 / kEpiF32: the product
+  const uint16_t *P, *G;  // kEpiGate: projection and gate logits of the gated operand, D's layout
+  uint16_t *dP, *dG;      // kEpiGate: their gradients
+};
+
 struct GemmCfg {
   static constexpr int BM = 128, BN = 256, BK = 64, NST = 4;
   static constexpr int A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2, STAGE = A_BYTES + B_BYTES;
   static constexpr int MN_BOX = BK * 128;  // bytes of one 64-wide MN-major box (BK rows of 128 bytes)
-  static constexpr int OFF_BAR = NST * STAGE;
+  static constexpr int EPI_WARPS = 8;
+  static constexpr int EPI_PITCH = 33;                 // words per row of a warp's 32 x 32 staging tile
+  static constexpr int EPI_TILE = 32 * EPI_PITCH * 4;  // bytes
+  static constexpr int OFF_EPI = NST * STAGE;
+  static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * EPI_TILE;
   static constexpr int B_FULL = 0, B_EMPTY = NST, B_ACCF = 2 * NST, B_ACCE = B_ACCF + 2, B_DONE = B_ACCE + 2,
                        NBAR = B_DONE + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_ALLOC = OFF_MISC + 16 + 1024;
-  static constexpr int NTHREADS = 192;
+  static constexpr int NTHREADS = 64 + 32 * EPI_WARPS;
   static constexpr uint32_t TMEM_COLS = 2 * BN;
   static_assert(STAGE % 1024 == 0 && A_BYTES % 1024 == 0, "SW128 tiles need 1 KB alignment");
   static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 };
 
-template <bool kAMN, bool kBMN, bool kF32>
+// Stores 8 consecutive values v of one row of D at element offset `off` (the epilogue's unit of
+// work after the staging transpose): FP32, BF16, or the gating gradient from P and G (pv, gv).
+template <int kEpi>
+__device__ __forceinline__ void gemm_store8(const GemmIO &io, int64_t off, const float (&v)[8], const uint4 &pv,
+                                            const uint4 &gv) {
+  if constexpr (kEpi == kEpiF32) {
+    float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(io.D) + off);
+    dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+    dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+  } else if constexpr (kEpi == kEpiBF16) {
+    *reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(io.D) + off) =
+        make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+  } else {
+    const uint32_t pw[4] = {pv.x, pv.y, pv.z, pv.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
+    uint32_t op_[4], og[4];
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const float d0 = v[2 * x], d1 = v[2 * x + 1];
+      const float s0 = sigmoid_f(bf16_lo(gw[x])), s1 = sigmoid_f(bf16_hi(gw[x]));
+      op_[x] = pack_bf16x2(d0 * s0, d1 * s1);
+      og[x] = pack_bf16x2(d0 * bf16_lo(pw[x]) * (s0 * (1.f - s0)), d1 * bf16_hi(pw[x]) * (s1 * (1.f - s1)));
+    }
+    *reinterpret_cast<uint4 *>(io.dP + off) = make_uint4(op_[0], op_[1], op_[2], op_[3]);
+    *reinterpret_cast<uint4 *>(io.dG + off) = make_uint4(og[0], og[1], og[2], og[3]);
+  }
+}
+
+template <bool kAMN, bool kBMN, int kEpi>
 __global__ void __launch_bounds__(GemmCfg::NTHREADS, 1)
     trimul_gemm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB,
-                       void *__restrict__ D, int N, int batch, int *status) {
+                       const GemmIO io, int N, int batch, int *status) {
   using C = GemmCfg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -205,7 +303,7 @@ __global__ void __launch_bounds__(GemmCfg::NTHREADS, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(C::B_ACCF + s), 1);
-      mbar_init(bar(C::B_ACCE + s), 128);
+      mbar_init(bar(C::B_ACCE + s), 32 * C::EPI_WARPS);
     }
     mbar_init(bar(C::B_DONE), 1);
     misc[1] = 0;
@@ -302,43 +400,58 @@ __global__ void __launch_bounds__(GemmCfg::NTHREADS, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue: TMEM -> registers -> global
-    const int q = warp & 3;  // the TMEM lane quarter this warp may access
+    // Per 32 x 32 chunk: TMEM rows (one per thread) go through the warp's staging tile, then every
+    // thread takes 8-value pieces of four rows, so that one warp instruction covers 8 rows of 32
+    // contiguous values (conflict-free: pitch 33 words).
+    const int q = warp & 3;                             // the TMEM lane quarter this warp may access
+    const int cbase = ((warp - 2) >> 2) * (C::BN / 2);  // its half of the columns
     const uint32_t lrow = (uint32_t)(q * 32) << 16;
-    bool ok = true;
+    float *stg = reinterpret_cast<float *>(sm + C::OFF_EPI + (warp - 2) * C::EPI_TILE);
+    const int rq = lane >> 2, cq = lane & 3;
     int tl = 0;
     for (int u = blockIdx.x; u < ntiles; u += gridDim.x, ++tl) {
       int t, m0, n0;
       tile_of(u, t, m0, n0);
       const int acc = tl & 1;
-      ok = wait_bar_warp(bar(C::B_ACCF + acc), (tl >> 1) & 1, ab);
-      if (!ok) break;
+      if (!wait_bar_warp(bar(C::B_ACCF + acc), (tl >> 1) & 1, ab)) break;
       tc_fence_after();
-      const int m = m0 + q * 32 + lane;
-      const int64_t rowoff = ((int64_t)t * N + m) * N;
-#pragma unroll 1
-      for (int c0 = 0; c0 < C::BN; c0 += 32) {
-        if (n0 + c0 >= N) break;  // uniform across the warp
+      const int mrow = m0 + q * 32 + rq;  // this thread's rows: mrow + 8 i
+      // P and G of the next chunk are requested before the current one is processed (two sets in
+      // flight per thread)
+      uint4 pv[2][4], gv[2][4];
+      auto load_pg = [&](int c0, uint4(&p)[4], uint4(&g)[4]) {
+        const int col = n0 + c0 + 8 * cq;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (mrow + 8 * i < N && col < N) {
+            const int64_t off = ((int64_t)t * N + mrow + 8 * i) * N + col;
+            p[i] = *reinterpret_cast<const uint4 *>(io.P + off);
+            g[i] = *reinterpret_cast<const uint4 *>(io.G + off);
+          }
+      };
+      if constexpr (kEpi == kEpiGate) load_pg(cbase, pv[0], gv[0]);
+#pragma unroll
+      for (int k = 0; k < C::BN / 64; ++k) {  // this warp's four 32-column chunks
+        const int c0 = cbase + 32 * k, n = n0 + c0;
+        if (n >= N) break;  // uniform across the warp
+        if constexpr (kEpi == kEpiGate)
+          if (k + 1 < C::BN / 64 && n + 32 < N) load_pg(c0 + 32, pv[(k + 1) & 1], gv[(k + 1) & 1]);
+        const int col = n + 8 * cq;
         uint32_t r[32];
         tmem_ld32(tb + lrow + acc * C::BN + c0, r);
         tmem_wait_ld(r);
-        const int n = n0 + c0;
-        if (m >= N) continue;
-        if constexpr (kF32) {
-          float *dst = reinterpret_cast<float *>(D) + rowoff + n;
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            if (n + 4 * k < N)  // N is a multiple of 8: whole 4-value chunks
-              *reinterpret_cast<uint4 *>(dst + 4 * k) = make_uint4(r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]);
-        } else {
-          uint16_t *dst = reinterpret_cast<uint16_t *>(D) + rowoff + n;
-          uint32_t w[16];
+        for (int j = 0; j < 32; ++j) stg[lane * C::EPI_PITCH + j] = __uint_as_float(r[j]);
+        __syncwarp();
 #pragma unroll
-          for (int k = 0; k < 16; ++k) w[k] = pack_bf16x2(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1]));
+        for (int i = 0; i < 4; ++i) {
+          float v[8];
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            if (n + 8 * k < N)  // whole 8-value chunks
-              *reinterpret_cast<uint4 *>(dst + 8 * k) = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+          for (int j = 0; j < 8; ++j) v[j] = stg[(rq + 8 * i) * C::EPI_PITCH + 8 * cq + j];
+          if (mrow + 8 * i < N && col < N)  // N is a multiple of 8: whole 8-value pieces
+            gemm_store8<kEpi>(io, ((int64_t)t * N + mrow + 8 * i) * N + col, v, pv[k & 1][i], gv[k & 1][i]);
         }
+        __syncwarp();  // the staging tile is rewritten by the next chunk
       }
       tc_fence_before();
       mbar_arrive(bar(C::B_ACCE + acc));
@@ -368,7 +481,7 @@ cudaError_t make_stack_map(CUtensorMap *m, const void *ptr, int N, int batch, in
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <bool kAMN, bool kBMN, bool kF32>
+template <bool kAMN, bool kBMN, int kEpi>
 struct Gemm {
   CUtensorMap mA, mB;
   int grid;
@@ -383,7 +496,7 @@ struct Gemm {
     if (e != cudaSuccess) return e;
     static DeviceOnce ready;
     if (!ready.done(dev)) {
-      e = cudaFuncSetAttribute(trimul_gemm_kernel<kAMN, kBMN, kF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      e = cudaFuncSetAttribute(trimul_gemm_kernel<kAMN, kBMN, kEpi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                GemmCfg::SMEM_ALLOC);
       if (e != cudaSuccess) return e;
       ready.mark(dev);
@@ -393,9 +506,9 @@ struct Gemm {
     grid = (int)std::min<int64_t>(tiles, nsm);
     return cudaSuccess;
   }
-  cudaError_t launch(void *D, int N, int batch, int *status, cudaStream_t st) const {
-    trimul_gemm_kernel<kAMN, kBMN, kF32><<<grid, GemmCfg::NTHREADS, GemmCfg::SMEM_ALLOC, st>>>(mA, mB, D, N, batch,
-                                                                                              status);
+  cudaError_t launch(const GemmIO &io, int N, int batch, int *status, cudaStream_t st) const {
+    trimul_gemm_kernel<kAMN, kBMN, kEpi>
+        <<<grid, GemmCfg::NTHREADS, GemmCfg::SMEM_ALLOC, st>>>(mA, mB, io, N, batch, status);
     return cudaGetLastError();
   }
 };
@@ -416,7 +529,9 @@ cudaError_t gate_setup() {
 }
 
 int check_shape(const tri_mul_shape &s) {
-  if (s.B < 1 || s.N < 1 || s.C < 1 || (s.incoming != 0 && s.incoming != 1)) return TRI_ATTN_ERR_INVALID_ARG;
+  if (s.B < 1 || s.N < 1 || s.C < 1 || (s.incoming != 0 && s.incoming != 1) ||
+      (s.layout != TRI_MUL_LAYOUT_PAIR && s.layout != TRI_MUL_LAYOUT_CHANNEL_MAJOR))
+    return TRI_ATTN_ERR_INVALID_ARG;
   if (s.N < 16 || s.N > TRI_MUL_MAX_N || s.N % 8 || s.C < 8 || s.C > TRI_MUL_MAX_C || s.C % 8 ||
       (int64_t)s.B * s.C > 65535)
     return TRI_ATTN_ERR_UNSUPPORTED;
@@ -427,10 +542,29 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 size_t stack_elems(const tri_mul_shape &s) { return (size_t)s.B * s.C * (size_t)s.N * s.N; }
 
-}  // namespace
+// Channel-major backward: both products with the gating gradient fused into their epilogues.
+// Outgoing (X = A Bm^T): dA = dX Bm (dX K-major, Bm MN-major), dB = dX^T A (both MN-major).
+// Incoming (X = A^T Bm, operands stored [k][i]): dA[k][i] = sum_j Bm[k][j] dX[i][j] (both K-major),
+// dB[k][j] = sum_i A[k][i] dX[i][j] (A K-major, dX MN-major).
+template <bool kA1, bool kB1, bool kA2, bool kB2>
+int mul_bwd_cm(const tri_mul_shape &s, const uint16_t *Pa, const uint16_t *Ga, const uint16_t *Pb, const uint16_t *Gb,
+               const uint16_t *A, const uint16_t *Bm, const uint16_t *dX, uint16_t *dPa, uint16_t *dGa, uint16_t *dPb,
+               uint16_t *dGb, int *status, cudaStream_t st) {
+  const int N = s.N, T = s.B * s.C;
+  Gemm<kA1, kB1, kEpiGate> ga_;
+  Gemm<kA2, kB2, kEpiGate> gb_;
+  const uint16_t *a1 = s.incoming ? Bm : dX, *b1 = s.incoming ? dX : Bm;
+  const uint16_t *a2 = s.incoming ? A : dX, *b2 = s.incoming ? dX : A;
+  if (ga_.plan(a1, b1, N, T) != cudaSuccess || gb_.plan(a2, b2, N, T) != cudaSuccess)
+    return TRI_ATTN_ERR_CUDA;
+  cudaError_t e = ga_.launch(GemmIO{nullptr, Pa, Ga, dPa, dGa}, N, T, status, st);
+  if (e == cudaSuccess) e = timing_mark(0, st);
+  if (e == cudaSuccess) e = gb_.launch(GemmIO{nullptr, Pb, Gb, dPb, dGb}, N, T, status, st);
+  if (e == cudaSuccess) e = timing_mark(1, st);
+  return e == cudaSuccess ? TRI_ATTN_OK : TRI_ATTN_ERR_CUDA;
+}
 
-cudaError_t timing_mark(int k, cudaStream_t st);
-int *device_status_word();
+}  // namespace
 
 }  // namespace triattn
 
@@ -450,22 +584,36 @@ int tri_mul_fwd(tri_mul_shape shape, const tri_attn_bf16 *Pa, const tri_attn_bf1
   const int N = shape.N, T = shape.B * shape.C;
   int *status = device_status_word();
   if (!status) return TRI_ATTN_ERR_CUDA;
-  Gemm<false, false, false> gemm;
-  if (gemm.plan(A, Bm, N, T) != cudaSuccess || gate_setup() != cudaSuccess) return TRI_ATTN_ERR_CUDA;
   auto st = static_cast<cudaStream_t>(stream);
-  GateArgs ga{{Pa, Pb}, {Ga, Gb}, {A, Bm}, N, shape.C, (shape.C + kGateCG - 1) / kGateCG, shape.incoming};
-  const dim3 grid((N + kGateT - 1) / kGateT, (N + kGateT - 1) / kGateT, shape.B * ga.groups * 2);
-  trimul_gate_kernel<<<grid, kGateThreads, kGateSmem, st>>>(ga);
-  cudaError_t e = cudaGetLastError();
+  const bool cm = shape.layout == TRI_MUL_LAYOUT_CHANNEL_MAJOR;
+  // the pair layout's gating transposes the incoming operands, so its contraction is always
+  // X = A Bm^T; the channel-major layout keeps them as stored and reads them MN-major instead
+  Gemm<false, false, kEpiBF16> g_out;
+  Gemm<true, true, kEpiBF16> g_in;
+  const bool mn = cm && shape.incoming;
+  if ((mn ? g_in.plan(A, Bm, N, T) : g_out.plan(A, Bm, N, T)) != cudaSuccess || gate_setup() != cudaSuccess)
+    return TRI_ATTN_ERR_CUDA;
+  cudaError_t e;
+  if (cm) {
+    GateCmArgs ga{{Pa, Pb}, {Ga, Gb}, {A, Bm}, (int64_t)(stack_elems(shape) / 8)};
+    const dim3 grid((unsigned)((ga.chunks + 1023) / 1024), 2);
+    trimul_gate_cm_kernel<<<grid, 256, 0, st>>>(ga);
+  } else {
+    GateArgs ga{{Pa, Pb}, {Ga, Gb}, {A, Bm}, N, shape.C, (shape.C + kGateCG - 1) / kGateCG, shape.incoming};
+    const int nt = (N + kGateT - 1) / kGateT;
+    trimul_gate_kernel<<<shape.B * nt * nt * ga.groups * 2, kGateThreads, kGateSmem, st>>>(ga);
+  }
+  e = cudaGetLastError();
   if (e == cudaSuccess) e = timing_mark(0, st);
-  if (e == cudaSuccess) e = gemm.launch(X, N, T, status, st);
+  const GemmIO io{X, nullptr, nullptr, nullptr, nullptr};
+  if (e == cudaSuccess) e = mn ? g_in.launch(io, N, T, status, st) : g_out.launch(io, N, T, status, st);
   if (e == cudaSuccess) e = timing_mark(1, st);
   return e == cudaSuccess ? TRI_ATTN_OK : TRI_ATTN_ERR_CUDA;
 }
 
 size_t tri_mul_bwd_workspace_size(tri_mul_shape shape) {
   if (check_shape(shape)) return 0;
-  return 2 * sizeof(float) * stack_elems(shape);
+  return shape.layout == TRI_MUL_LAYOUT_CHANNEL_MAJOR ? 0 : 2 * sizeof(float) * stack_elems(shape);
 }
 
 int tri_mul_bwd(tri_mul_shape shape, const tri_attn_bf16 *Pa, const tri_attn_bf16 *Ga, const tri_attn_bf16 *Pb,
@@ -480,29 +628,35 @@ int tri_mul_bwd(tri_mul_shape shape, const tri_attn_bf16 *Pa, const tri_attn_bf1
     if (!aligned16(p)) return TRI_ATTN_ERR_UNSUPPORTED;
   }
   if (workspace && !aligned16(workspace)) return TRI_ATTN_ERR_UNSUPPORTED;
-  if (!workspace || workspace_bytes < tri_mul_bwd_workspace_size(shape)) return TRI_ATTN_ERR_WORKSPACE;
+  const size_t need = tri_mul_bwd_workspace_size(shape);
+  if (need && (!workspace || workspace_bytes < need)) return TRI_ATTN_ERR_WORKSPACE;
+  int *status = device_status_word();
+  if (!status) return TRI_ATTN_ERR_CUDA;
+  auto st = static_cast<cudaStream_t>(stream);
+  if (shape.layout == TRI_MUL_LAYOUT_CHANNEL_MAJOR)
+    return shape.incoming ? mul_bwd_cm<false, false, false, true>(shape, Pa, Ga, Pb, Gb, A, Bm, dX, dPa, dGa, dPb,
+                                                                  dGb, status, st)
+                          : mul_bwd_cm<false, true, true, true>(shape, Pa, Ga, Pb, Gb, A, Bm, dX, dPa, dGa, dPb,
+                                                                dGb, status, st);
   const int N = shape.N, T = shape.B * shape.C;
   float *dA = static_cast<float *>(workspace);
   float *dB = dA + stack_elems(shape);
-  int *status = device_status_word();
-  if (!status) return TRI_ATTN_ERR_CUDA;
-  // dA[t] = dX[t] Bm[t]: D[i][k] = sum_j dX[i][j] Bm[j][k], Bm read MN-major
-  // dB[t] = dX[t]^T A[t]: D[j][k] = sum_i dX[i][j] A[i][k], both operands read MN-major
-  Gemm<false, true, true> gemm_a;
-  Gemm<true, true, true> gemm_b;
+  // pair layout: dA[t] = dX[t] Bm[t] (Bm read MN-major) and dB[t] = dX[t]^T A[t] (both operands
+  // MN-major) in FP32, then the gating gradient maps them back to the pair layout
+  Gemm<false, true, kEpiF32> gemm_a;
+  Gemm<true, true, kEpiF32> gemm_b;
   if (gemm_a.plan(dX, Bm, N, T) != cudaSuccess || gemm_b.plan(dX, A, N, T) != cudaSuccess ||
       gate_setup() != cudaSuccess)
     return TRI_ATTN_ERR_CUDA;
-  auto st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = gemm_a.launch(dA, N, T, status, st);
+  cudaError_t e = gemm_a.launch(GemmIO{dA, nullptr, nullptr, nullptr, nullptr}, N, T, status, st);
   if (e == cudaSuccess) e = timing_mark(0, st);
-  if (e == cudaSuccess) e = gemm_b.launch(dB, N, T, status, st);
+  if (e == cudaSuccess) e = gemm_b.launch(GemmIO{dB, nullptr, nullptr, nullptr, nullptr}, N, T, status, st);
   if (e == cudaSuccess) e = timing_mark(1, st);
   if (e == cudaSuccess) {
     GateBwdArgs gg{{dA, dB}, {Pa, Pb}, {Ga, Gb}, {dPa, dPb}, {dGa, dGb}, N, shape.C,
                    (shape.C + kGbCG - 1) / kGbCG, shape.incoming};
-    const dim3 grid((N + kGateT - 1) / kGateT, (N + kGateT - 1) / kGateT, shape.B * gg.groups * 2);
-    trimul_gate_bwd_kernel<<<grid, kGateThreads, kGbSmem, st>>>(gg);
+    const int nt = (N + kGateT - 1) / kGateT;
+    trimul_gate_bwd_kernel<<<shape.B * nt * nt * gg.groups * 2, kGateThreads, kGbSmem, st>>>(gg);
     e = cudaGetLastError();
   }
   if (e == cudaSuccess) e = timing_mark(2, st);

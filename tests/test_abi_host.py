@@ -164,7 +164,7 @@ def test_workspace_size_same_for_both_nodes(lib):
 
 
 # ---------------------------------------------------------------- triangle multiplication entry points
-MUL_GOOD = (1, 64, 16, 0)
+MUL_GOOD = (1, 64, 16, 0, 0)
 
 
 def _mul_fwd(lib, shape, **ptrs):
@@ -182,17 +182,19 @@ def _mul_bwd(lib, shape, ws_bytes, **ptrs):
 
 
 @pytest.mark.parametrize("shape,code", [
-    ((0, 64, 16, 0), -1),      # empty batch
-    ((1, 0, 16, 0), -1),       # no residues
-    ((1, 64, 0, 0), -1),       # no channels
-    ((1, 64, 16, 2), -1),      # unknown direction
-    ((1, 64, 16, -1), -1),
-    ((1, 8, 16, 0), -2),       # N below 16
-    ((1, 68, 16, 0), -2),      # N not a multiple of 8
-    ((1, 4104, 16, 0), -2),    # N above TRI_MUL_MAX_N
-    ((1, 64, 12, 0), -2),      # C not a multiple of 8
-    ((1, 64, 1032, 0), -2),    # C above TRI_MUL_MAX_C
-    ((65, 64, 1024, 0), -2),   # B * C above the grid limit
+    ((0, 64, 16, 0, 0), -1),      # empty batch
+    ((1, 0, 16, 0, 0), -1),       # no residues
+    ((1, 64, 0, 0, 0), -1),       # no channels
+    ((1, 64, 16, 2, 0), -1),      # unknown direction
+    ((1, 64, 16, -1, 0), -1),
+    ((1, 64, 16, 0, 2), -1),      # unknown layout
+    ((1, 64, 16, 0, -1), -1),
+    ((1, 8, 16, 0, 0), -2),       # N below 16
+    ((1, 68, 16, 0, 1), -2),      # N not a multiple of 8
+    ((1, 4104, 16, 0, 0), -2),    # N above TRI_MUL_MAX_N
+    ((1, 64, 12, 0, 1), -2),      # C not a multiple of 8
+    ((1, 64, 1032, 0, 0), -2),    # C above TRI_MUL_MAX_C
+    ((65, 64, 1024, 0, 1), -2),   # B * C above the grid limit
 ])
 def test_mul_shape_validation(lib, shape, code):
     assert _mul_fwd(lib, shape) == code
@@ -215,7 +217,8 @@ def test_mul_workspace_checks(lib):
     from bwd_tri_attn_gb300.binding import MulShape
     need = lib.tri_mul_bwd_workspace_size(MulShape(*MUL_GOOD))
     assert need == 2 * 4 * 1 * 16 * 64 * 64  # two FP32 [B, C, N, N] stacks, known without a device
-    assert lib.tri_mul_bwd_workspace_size(MulShape(1, 68, 16, 0)) == 0
+    assert lib.tri_mul_bwd_workspace_size(MulShape(1, 68, 16, 0, 0)) == 0
+    assert lib.tri_mul_bwd_workspace_size(MulShape(1, 64, 16, 0, 1)) == 0  # channel-major: none
     assert _mul_bwd(lib, MUL_GOOD, need - 1) == -3
     assert _mul_bwd(lib, MUL_GOOD, need, ws=0) == -3
     assert _mul_bwd(lib, MUL_GOOD, need, ws=FAKE + 8) == -2
