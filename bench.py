@@ -287,14 +287,14 @@ def mul_roofline(kernel_ms, B, N, C, peaks):
     return out
 
 
-def run_trimul(dev, stream, steps, incoming=False, layout=1):
-    """Times the triangle multiplicative update (fwd + bwd) at crop 768, 128 channels."""
+def run_trimul(dev, stream, steps, incoming=False, layout=1, mw=None):
+    """Times the triangle multiplicative update (fwd + bwd); default workload crop 768, 128 channels."""
     import torch
 
     from bwd_tri_attn_gb300 import binding as tb
     from bwd_tri_attn_gb300 import workloads as wl
 
-    mw = wl.MUL_CROP768
+    mw = mw or wl.MUL_CROP768
     x = {k: v.to(dev) for k, v in wl.mul_inputs_for(mw).items()}
     if layout == tb.LAYOUT_CHANNEL_MAJOR:
         x = {k: (v.permute(0, 3, 1, 2).contiguous() if k != "dX" else v) for k, v in x.items()}
@@ -340,8 +340,27 @@ def run_trimul(dev, stream, steps, incoming=False, layout=1):
             "layout": "channel-major" if layout == tb.LAYOUT_CHANNEL_MAJOR else "pair",
             "B": B, "N": N, "C": C, "ms_per_step": ms, "tflops": 3 * mw.flops() / (ms * 1e-3) / 1e12,
             "flops_per_step": 3 * mw.flops(), "steps": steps,
-            "l2": "inputs and operands larger than L2 (each [B,N,N,C] tensor is 151 MB), no flush",
+            "l2": f"inputs and operands larger than L2 (each [B,N,N,C] tensor is {2 * B * N * N * C / 1e6:.0f} MB; "
+                  "four projections per step), no flush",
             "kernels": mul_roofline(per, B, N, C, peaks), "gpu_launches": steps * len(names)}
+
+
+def run_trimul_only(args):
+    """``--trimul-only``: the triangle multiplication sub-line alone (one GPU), for profiling."""
+    import torch
+
+    from bwd_tri_attn_gb300 import _build
+    from bwd_tri_attn_gb300 import binding as tb
+    from bwd_tri_attn_gb300 import workloads as wl
+
+    _build.build()
+    tb.load()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    mw = wl.MUL_ALL[args.mul_workload]
+    out = [run_trimul(dev, stream, args.steps, incoming=inc, layout=lay, mw=mw)
+           for lay in (tb.LAYOUT_CHANNEL_MAJOR, tb.LAYOUT_PAIR) for inc in (False, True)]
+    print(json.dumps({"trimul": out}))
 
 
 def run_ours(args, w):
@@ -535,8 +554,9 @@ def run_ours(args, w):
 
     mul = None
     if not args.no_trimul:
-        mul = [run_trimul(dev, stream, max(3, min(K, 20)), layout=lay) for lay in (tb.LAYOUT_CHANNEL_MAJOR,
-                                                                                   tb.LAYOUT_PAIR)]
+        mw = wl.MUL_ALL[args.mul_workload]
+        mul = [run_trimul(dev, stream, max(3, min(K, 20)), layout=lay, mw=mw)
+               for lay in (tb.LAYOUT_CHANNEL_MAJOR, tb.LAYOUT_PAIR)]
 
     in_bytes = sum(v.numel() * v.element_size() for v in x.values() if v is not None)
     if rank == 0:
@@ -575,6 +595,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-trimul", action="store_true", help="skip the triangle multiplication sub-line")
+    ap.add_argument("--trimul-only", action="store_true",
+                    help="time only the triangle multiplication (both layouts, both directions); one JSON line")
+    ap.add_argument("--mul-workload", default=wl.MUL_CROP768.name, choices=sorted(wl.MUL_ALL))
     ap.add_argument("--windows", type=int, default=0,
                     help="timed windows of --steps steps (0: enough to fill about a second, at least 3)")
     args = ap.parse_args()
@@ -593,6 +616,9 @@ def main():
     if world and world != args.gpus:
         ap.error(f"--gpus {args.gpus} disagrees with WORLD_SIZE={world}")
     w = wl.ALL[args.workload]
+    if args.trimul_only:
+        run_trimul_only(args)
+        return
     if args.impl == "reference":
         run_reference(args, w)
     else:
