@@ -43,17 +43,18 @@ NFWD = 2  # kernels of tri_attn_fwd
 
 
 # ncu summaries under profiles/ carry, per kernel, the DRAM bytes of one captured
-# launch, the activation size it ran on and a digest of the sources it was built
-# from; traffic is reported only while the sources still match.
+# launch, the workload and activation size it ran on and a digest of the sources it was
+# built from; traffic is reported only while the sources still match.
 PROFILES = {"fwd": ("fwd_kernel_crop384_h4_d32.md", ["fwd.cu"]),
             "bwd_main": ("bwd_kernel_crop384_h4_d32.md", ["bwd.cu"])}
 COMMON_SOURCES = ["common.cuh", "sm100.cuh", "sync.cuh", "tmap.cuh"]
 
 
 def profiled_traffic(kernel: str, activation_elements: int):
-    """DRAM bytes per launch from the kernel's ncu capture, scaled to this workload's
-    activation size (all inputs of the square crops grow with S*N*H*d), or None
-    when the summary is missing or the kernel's sources changed since it was taken."""
+    """(DRAM bytes per launch, how they were obtained) from the kernel's ncu summary: the captured
+    launch's figure when it ran on a workload of this activation size, else scaled by activation
+    size (every input of the square crops grows with S*N*H*d); (None, reason) when the summary is
+    missing or the kernel's sources changed since it was taken."""
     import hashlib
 
     name, own = PROFILES[kernel]
@@ -64,15 +65,22 @@ def profiled_traffic(kernel: str, activation_elements: int):
             with open(os.path.join(ROOT, "bwd_tri_attn_gb300", "csrc", f), "rb") as fh:
                 h.update(fh.read())
     except OSError:
-        return None
+        return None, "no ncu summary"
     fields = {}
     for line in text.splitlines():
         k, _, v = line.strip().partition(": ")
-        if k in ("source_digest", "dram_bytes_per_launch", "activation_elements"):
+        if k in ("source_digest", "dram_bytes_per_launch", "activation_elements", "workload"):
             fields[k] = v.strip()
-    if len(fields) != 3 or fields["source_digest"] != h.hexdigest()[:16]:
-        return None
-    return int(fields["dram_bytes_per_launch"]) * activation_elements / int(fields["activation_elements"])
+    if len(fields) != 4:
+        return None, "ncu summary incomplete"
+    if fields["source_digest"] != h.hexdigest()[:16]:
+        return None, "kernel sources changed since the ncu capture"
+    captured = int(fields["activation_elements"])
+    bytes_ = int(fields["dram_bytes_per_launch"])
+    if captured == activation_elements:
+        return bytes_, f"ncu dram__bytes_read.sum + dram__bytes_write.sum of one {fields['workload']} launch"
+    return (bytes_ * activation_elements / captured,
+            f"ncu DRAM bytes of one {fields['workload']} launch, scaled by activation size")
 
 
 def load_peaks():
@@ -457,11 +465,10 @@ def run_ours(args, w):
     flops_of = {"fwd": 4.0 * B * S * H * N * N * hd, "bwd_main": 10.0 * B * S * H * N * N * hd}
     dom = max(("fwd", "bwd_main"), key=lambda n: kernel_ms[n])
     achieved = flops_of[dom] / (kernel_ms[dom] * 1e-3) / 1e12
+    traffic, traffic_source = profiled_traffic(dom, B * S * N * H * hd)
     roofline = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-                "traffic": profiled_traffic(dom, B * S * N * H * hd),
-                "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one N=384 launch, "
-                                  "scaled by activation size",
+                "traffic": traffic, "traffic_source": traffic_source,
                 "peak_source": f"{peaks['source']} bf16 dense burst"}
 
     # HBM-bound kernels: algorithmic bytes / time

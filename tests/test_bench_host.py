@@ -97,14 +97,17 @@ def test_traffic_reported_only_for_matching_sources(monkeypatch, tmp_path):
     for f in ["fwd.cu"] + bench.COMMON_SOURCES:
         h.update((csrc / f).read_bytes())
     (tmp_path / "profiles" / "fwd_kernel_crop384_h4_d32.md").write_text(
-        f"    source_digest: {h.hexdigest()[:16]}\n    dram_bytes_per_launch: 1000\n"
+        f"    source_digest: {h.hexdigest()[:16]}\n    workload: tiny\n    dram_bytes_per_launch: 1000\n"
         "    activation_elements: 10\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    # scaled to the caller's activation size
-    assert bench.profiled_traffic("fwd", 40) == pytest.approx(4000.0)
+    # the captured launch's own figure at its size, scaled to another activation size
+    assert bench.profiled_traffic("fwd", 10)[0] == 1000
+    assert "one tiny launch" in bench.profiled_traffic("fwd", 10)[1]
+    assert bench.profiled_traffic("fwd", 40)[0] == pytest.approx(4000.0)
+    assert "scaled" in bench.profiled_traffic("fwd", 40)[1]
     # a changed source invalidates the figure
     with open(csrc / "fwd.cu", "a") as f:
         f.write("\n")
-    assert bench.profiled_traffic("fwd", 40) is None
+    assert bench.profiled_traffic("fwd", 40)[0] is None
     # a missing summary reports nothing
-    assert bench.profiled_traffic("bwd_main", 40) is None
+    assert bench.profiled_traffic("bwd_main", 40)[0] is None
