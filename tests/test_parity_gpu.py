@@ -291,10 +291,11 @@ def test_residual_compensation_lowers_gradient_error(w):
 
 
 # The pages report 28-47 % lower dQ, dK and dBias RMSE from the residual at these crops. Here the
-# gradients leave the kernels in BF16, whose own rounding (about 1.6e-3 relative RMSE) dominates
+# gradients leave the kernels in BF16, whose own rounding (about 1.66e-3 relative RMSE) dominates
 # their error; the residual must lower the total error on every crop and output, and the error
-# above that rounding floor by at least this fraction (measured values in the design notes).
-MIN_GAIN_ABOVE_FLOOR = 0.0
+# above that rounding floor by at least 10 % (measured: 19.8 % at the least, crop 768 dK; up to
+# 85 % at crop 384 dBias).
+MIN_GAIN_ABOVE_FLOOR = 0.10
 
 
 def test_residual_compensation_full_tensor_crop384():
