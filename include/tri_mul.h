@@ -38,6 +38,10 @@
  *                                 pass needs no workspace: the gating
  *                                 gradient runs in the contractions' epilogue.
  *
+ * Accuracy: the gating runs in FP32 (fast exponential and reciprocal), accurate
+ * to a few FP32 ulp plus about one ulp per unit of |G| before the BF16
+ * rounding, for gate logits |G| < 87; below G = -87 the gated value is 0.
+ *
  * Requirements: B >= 1, 16 <= N <= TRI_MUL_MAX_N with N a multiple of 8,
  * 8 <= C <= TRI_MUL_MAX_C with C a multiple of 8, B * C <= 65535, every
  * pointer 16-byte aligned and on the current device, tensors not

@@ -74,3 +74,38 @@ def bwd(pa, ga, pb, gb, dX, incoming: bool = False, bf16: bool = True):
         db = np.einsum("bijc,bikc->bjkc", dX, a)  # dX[i,j] a[i,k] -> dB[j,k]
     sa, sb = sigmoid(ga), sigmoid(gb)
     return {"dPa": da * sa, "dGa": da * pa * sa * (1.0 - sa), "dPb": db * sb, "dGb": db * pb * sb * (1.0 - sb)}
+
+
+def sampled(pa, ga, pb, gb, dX, idx, incoming: bool = False, bf16: bool = True):
+    """X and the four gradients at chosen entries only, for sizes where the full tensors are too
+    large: idx is a list of (b, x, y, c). X is evaluated at [b, x, y, c] (its own index), each
+    gradient at the projection entry [b, x, y, c]; dX is given in the pair layout [B, N, N, C].
+    Every value is the definition written out for that one entry (an N-term dot product of gated
+    rows or columns), so only the rows and columns it touches are gated.
+    Returns a dict of float64 arrays with one value per entry."""
+    pa, ga, pb, gb, dX = (_f64(t) for t in (pa, ga, pb, gb, dX))
+    out = {k: [] for k in ("X", "dPa", "dGa", "dPb", "dGb")}
+    for b, x, y, c in idx:
+        # X[b,x,y,c]: outgoing sum_k a[x,k] b[y,k]; incoming sum_k a[k,x] b[k,y]
+        if incoming:
+            ar, br = gated(pa[b, :, x, c], ga[b, :, x, c], bf16), gated(pb[b, :, y, c], gb[b, :, y, c], bf16)
+        else:
+            ar, br = gated(pa[b, x, :, c], ga[b, x, :, c], bf16), gated(pb[b, y, :, c], gb[b, y, :, c], bf16)
+        out["X"].append(float(np.dot(ar, br)))
+        # gradient of the gated operand a at entry [x, y] (pair indices of the projection):
+        # outgoing: a[x, y] meets b[j, y] in X[x, j] -> dA = sum_j dX[x, j] b[j, y]
+        # incoming: a[x, y] meets b[x, j] in X[y, j] -> dA = sum_j dX[y, j] b[x, j]
+        if incoming:
+            da = float(np.dot(dX[b, y, :, c], gated(pb[b, x, :, c], gb[b, x, :, c], bf16)))
+            # b[x, y] meets a[x, i] in X[i, y] -> dB = sum_i dX[i, y] a[x, i]
+            db = float(np.dot(dX[b, :, y, c], gated(pa[b, x, :, c], ga[b, x, :, c], bf16)))
+        else:
+            da = float(np.dot(dX[b, x, :, c], gated(pb[b, :, y, c], gb[b, :, y, c], bf16)))
+            # b[x, y] meets a[i, y] in X[i, x] -> dB = sum_i dX[i, x] a[i, y]
+            db = float(np.dot(dX[b, :, x, c], gated(pa[b, :, y, c], ga[b, :, y, c], bf16)))
+        sa, sb = sigmoid(ga[b, x, y, c]), sigmoid(gb[b, x, y, c])
+        out["dPa"].append(da * sa)
+        out["dGa"].append(da * pa[b, x, y, c] * sa * (1.0 - sa))
+        out["dPb"].append(db * sb)
+        out["dGb"].append(db * pb[b, x, y, c] * sb * (1.0 - sb))
+    return {k: np.asarray(v) for k, v in out.items()}

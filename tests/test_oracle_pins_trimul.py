@@ -114,3 +114,18 @@ def test_gradients_match_torch_autograd(incoming):
     (X * torch.tensor(dX)).sum().backward()
     for name, tt in zip(("dPa", "dGa", "dPb", "dGb"), t):
         np.testing.assert_allclose(grads[name], tt.grad.numpy(), rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("incoming", [False, True])
+def test_sampled_entries_equal_the_full_tensors(incoming):
+    """The entry-wise evaluation used at sizes too large for the full oracle agrees with the full
+    tensors at every entry of a small case (both directions, B = 2)."""
+    pa, ga, pb, gb = _draw(2, 6, 3, seed=11)
+    dX = np.random.default_rng(12).standard_normal(pa.shape)
+    X = om.fwd(pa, ga, pb, gb, incoming)
+    g = om.bwd(pa, ga, pb, gb, dX, incoming)
+    idx = list(np.ndindex(pa.shape))
+    s = om.sampled(pa, ga, pb, gb, dX, idx, incoming)
+    np.testing.assert_allclose(s["X"], X.reshape(-1), rtol=1e-12, atol=1e-12)
+    for k in ("dPa", "dGa", "dPb", "dGb"):
+        np.testing.assert_allclose(s[k], g[k].reshape(-1), rtol=1e-12, atol=1e-12)

@@ -37,6 +37,12 @@ GATE_REL = 2.0 ** -17
 SIG_REL = 2.0 ** -19
 
 
+def sig_rel(g):
+    """Relative error bound of the kernels' FP32 sigmoid: the fast exponential's documented
+    2 + 1.173 |x| ulp, the fast reciprocal's 2 ulp and the add, with a factor 2 of margin."""
+    return 2.0 * (5.0 + 1.2 * np.abs(g)) * 2.0 ** -24
+
+
 def _lib():
     from bwd_tri_attn_gb300 import _build, binding
     _build.build()
@@ -77,12 +83,12 @@ def channel_major(a):
     return np.ascontiguousarray(np.moveaxis(a, -1, 1))
 
 
-def ambiguous(exact):
-    """Elements whose exact value lies within GATE_REL (relative) of a BF16 rounding midpoint."""
+def ambiguous(exact, rel=GATE_REL):
+    """Elements whose exact value lies within `rel` (relative) of a BF16 rounding midpoint."""
     a = np.abs(exact)
     u = ulp_bf16(exact)
     frac = np.mod(a, u) / u  # position inside the BF16 interval, in ulps
-    return (np.abs(frac - 0.5) * u <= GATE_REL * a) & (a > 0)
+    return (np.abs(frac - 0.5) * u <= rel * a) & (a > 0)
 
 
 def oracle_all(x, incoming, layout=PAIR):
@@ -92,7 +98,9 @@ def oracle_all(x, incoming, layout=PAIR):
     pa, ga, pb, gb = (_f64(x[k]) for k in ("Pa", "Ga", "Pb", "Gb"))
     dX = np.moveaxis(_f64(x["dX"]), 1, -1)  # channel-major -> pair layout
     a, b = om.gated(pa, ga), om.gated(pb, gb)
-    amb_a, amb_b = ambiguous(om.gated(pa, ga, bf16=False)), ambiguous(om.gated(pb, gb, bf16=False))
+    # FP32 gating error: the sigmoid's (grows with |G|) and the product's rounding
+    amb_a = ambiguous(om.gated(pa, ga, bf16=False), np.maximum(GATE_REL, 4 * sig_rel(ga)))
+    amb_b = ambiguous(om.gated(pb, gb, bf16=False), np.maximum(GATE_REL, 4 * sig_rel(gb)))
     da_ulp, db_ulp = amb_a * ulp_bf16(a), amb_b * ulp_bf16(b)
     N = pa.shape[1]
     gamma = N * 2.0 ** -22
@@ -111,11 +119,16 @@ def oracle_all(x, incoming, layout=PAIR):
         tdB = np.einsum("bijc,bikc->bjkc", np.abs(dX), gamma * np.abs(a) + da_ulp, optimize=True)
     sa, sb = om.sigmoid(ga), om.sigmoid(gb)
     tol = {"X": tX}
-    for name, t, s_, p in (("a", tdA, sa, pa), ("b", tdB, sb, pb)):
+    for name, t, s_, p, g_ in (("a", tdA, sa, pa, ga), ("b", tdB, sb, pb, gb)):
         dP, dG = g["dP" + name], g["dG" + name]
-        tol["dP" + name] = ulp_bf16(dP) + t * s_ + (SIG_REL + 2.0 ** -23) * np.abs(dP)
-        tol["dG" + name] = (ulp_bf16(dG) + t * np.abs(p) * s_ * (1 - s_)
-                            + (SIG_REL * (1 + s_ / (1 - s_)) + 2.0 ** -22) * np.abs(dG))
+        r = np.maximum(SIG_REL, sig_rel(g_))
+        with np.errstate(divide="ignore"):
+            amp = s_ / (1 - s_)  # relative error growth of 1 - sigmoid (infinite where it is 0 in FP64)
+        tol["dP" + name] = ulp_bf16(dP) + t * s_ + (r + 2.0 ** -23) * np.abs(dP)
+        # (where 1 - sigmoid is 0 in FP64, dG is 0 and so is the kernel's: no relative term)
+        with np.errstate(invalid="ignore"):
+            rel_g = np.where(np.abs(dG) > 0, (r * (1 + amp) + 2.0 ** -22) * np.abs(dG), 0.0)
+        tol["dG" + name] = ulp_bf16(dG) + t * np.abs(p) * s_ * (1 - s_) + rel_g
     if incoming and layout == PAIR:  # the stored operands hold the pair axes swapped
         a, b = np.swapaxes(a, 1, 2), np.swapaxes(b, 1, 2)
         amb_a, amb_b = np.swapaxes(amb_a, 1, 2), np.swapaxes(amb_b, 1, 2)
@@ -233,3 +246,80 @@ def test_device_errors_before_launch():
     assert e.value.code == -3
     torch.cuda.synchronize()
     assert tb.tri_attn_device_status() == 0
+
+
+# ---------------------------------------------------------------- edge cases: sizes and gate range
+@pytest.mark.parametrize("layout", [PAIR, CM])
+@pytest.mark.parametrize("incoming", [False, True])
+def test_max_channels_full_oracle(incoming, layout):
+    """C = TRI_MUL_MAX_C = 1024 (16 gating channel groups, 32 gradient groups) on a small N."""
+    x = wl.make_mul_inputs(1, 24, 1024, 21)
+    got = run_cuda(x, incoming, layout)
+    check_all(got, *oracle_all(x, incoming, layout))
+
+
+def test_largest_batch_times_channels():
+    """B * C at its limit region (B = 64, C = 1016: 65,024 matrix products in one launch)."""
+    x = wl.make_mul_inputs(64, 16, 1016, 22)
+    for layout in (PAIR, CM):
+        got = run_cuda(x, False, layout)
+        check_all(got, *oracle_all(x, False, layout))
+
+
+@pytest.mark.parametrize("incoming", [False, True])
+def test_max_n_sampled_entries(incoming):
+    """N = TRI_MUL_MAX_N = 4096 (16 x 32 output tiles per channel, 64 K steps): 48 entries of X and
+    of every gradient against the oracle's entry-wise evaluation, with the per-entry bound of the
+    full-oracle tests (output ulp, FP32 accumulation over N terms, ambiguous operand roundings,
+    the sigmoid's error)."""
+    B, N, C = 1, 4096, 8
+    x = wl.make_mul_inputs(B, N, C, 23)
+    got = run_cuda(x, incoming, CM)
+    g = np.random.default_rng(24)
+    idx = [(0, 0, 0, 0), (0, N - 1, N - 1, C - 1), (0, 0, N - 1, 3), (0, N - 1, 0, 4)]
+    idx += [(0, int(a), int(b_), int(c)) for a, b_, c in zip(g.integers(0, N, 44), g.integers(0, N, 44),
+                                                               g.integers(0, C, 44))]
+    f = {k: _f64(v) for k, v in x.items()}
+    dX = np.moveaxis(f["dX"], 1, -1)
+    ref = om.sampled(f["Pa"], f["Ga"], f["Pb"], f["Gb"], dX, idx, incoming)
+    gamma = N * 2.0 ** -22
+    for n, (b, i, j, c) in enumerate(idx):
+        # the rows and columns the entry touches, gated exactly and in BF16
+        def rows(P, G, axis_first, k):
+            sl = (b, slice(None), k, c) if axis_first else (b, k, slice(None), c)
+            return om.gated(P[sl], G[sl]), ambiguous(om.gated(P[sl], G[sl], bf16=False))
+        a_r, amb_a = rows(f["Pa"], f["Ga"], incoming, i)
+        b_r, amb_b = rows(f["Pb"], f["Gb"], incoming, j)
+        tol = (ulp_bf16(ref["X"][n]) + gamma * np.dot(np.abs(a_r), np.abs(b_r))
+               + np.dot(amb_a * ulp_bf16(a_r), np.abs(b_r)) + np.dot(np.abs(a_r), amb_b * ulp_bf16(b_r)))
+        err = abs(float(got["X"][b, c, i, j]) - ref["X"][n])
+        assert err <= tol, f"X{(b, i, j, c)}: |err| {err:.3g} > {tol:.3g}"
+        # gradients at projection entry [b, i, j, c]: bound on dA / dB from the terms they sum
+        if incoming:
+            ta, tb = rows(f["Pb"], f["Gb"], False, i), rows(f["Pa"], f["Ga"], False, i)
+            dxa, dxb = np.abs(dX[b, j, :, c]), np.abs(dX[b, :, j, c])
+        else:
+            ta, tb = rows(f["Pb"], f["Gb"], True, j), rows(f["Pa"], f["Ga"], True, j)
+            dxa, dxb = np.abs(dX[b, i, :, c]), np.abs(dX[b, :, i, c])
+        tda = np.dot(dxa, gamma * np.abs(ta[0]) + ta[1] * ulp_bf16(ta[0]))
+        tdb = np.dot(dxb, gamma * np.abs(tb[0]) + tb[1] * ulp_bf16(tb[0]))
+        for name, td, P, G in (("a", tda, f["Pa"], f["Ga"]), ("b", tdb, f["Pb"], f["Gb"])):
+            s_ = om.sigmoid(G[b, i, j, c])
+            r = sig_rel(G[b, i, j, c])
+            dP, dG = ref["dP" + name][n], ref["dG" + name][n]
+            tolP = ulp_bf16(dP) + td * s_ + (r + 2.0 ** -23) * abs(dP)
+            tolG = ulp_bf16(dG) + td * abs(P[b, i, j, c]) * s_ * (1 - s_) + (r * (1 + s_ / (1 - s_)) + 2.0 ** -22) * abs(dG)
+            for k, want, t in (("dP" + name, dP, tolP), ("dG" + name, dG, tolG)):
+                e = abs(float(got[k][b, i, j, c]) - want)
+                assert e <= t, f"{k}{(b, i, j, c)}: |err| {e:.3g} > {t:.3g}"
+
+
+@pytest.mark.parametrize("layout", [PAIR, CM])
+def test_saturated_gates(layout):
+    """Gate logits N(0, 12) (|G| up to about 55: sigmoid saturates to 0 and 1 in FP32): the gated
+    operands still match the FP64 rounding away from ambiguous entries, and X and the gradients
+    stay within their bounds, where 1 - sigmoid loses its relative precision."""
+    x = wl.make_mul_inputs(1, 72, 16, 25, gate_std=12.0)
+    assert float(x["Ga"].float().abs().max()) < 80.0  # inside the kernels' documented gate range
+    got = run_cuda(x, False, layout)
+    check_all(got, *oracle_all(x, False, layout))
