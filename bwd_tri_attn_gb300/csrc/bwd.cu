@@ -113,8 +113,8 @@ struct BwdCfg {
   static constexpr int B_QDOFULL = 3, B_QDOREADY = B_QDOFULL + NQS, B_QDOFREE = B_QDOREADY + NQS;
   static constexpr int B_BFULL = B_QDOFREE + NQS, B_BFREE = B_BFULL + 1;  // the (single) bias tile
   static constexpr int B_SFULL = B_BFREE + 1, B_PAFULL = B_SFULL + 1, B_AFREE = B_PAFULL + 1;
-  static constexpr int B_DPFULL = B_AFREE + 1, B_PFULL = B_DPFULL + 1, B_BFREEM = B_PFULL + 1;
-  static constexpr int B_M2DONE = B_BFREEM + 1, B_DQREAD = B_M2DONE + 1;
+  static constexpr int B_DPFULL = B_AFREE + 1, B_PFULL = B_DPFULL + 1;
+  static constexpr int B_M2DONE = B_PFULL + 1, B_DQREAD = B_M2DONE + 1;
   static constexpr int B_DKVREAD = B_DQREAD + 1, B_RFULL = B_DKVREAD + 1, B_XEMPTY = B_RFULL + NRB;
   static constexpr int B_FINAL = B_XEMPTY + NRB, NBAR = B_FINAL + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
@@ -254,7 +254,6 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
     mbar_init(bar(C::B_AFREE), 1);
     mbar_init(bar(C::B_DPFULL), 1);
     mbar_init(bar(C::B_PFULL), C::NEWT);
-    mbar_init(bar(C::B_BFREEM), 1);
     mbar_init(bar(C::B_M2DONE), 1);
     mbar_init(bar(C::B_DQREAD), C::NDQT);
     mbar_init(bar(C::B_DKVREAD), C::NEWT);
@@ -488,10 +487,11 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
           mma_ts_x8_e<0, 8, 16, 24, 64, 72, 80, 88>(dcol + HD, tb + C::TA, b, KS_ROW, idKV, cjt > 0 ? 1u : 0u);
           mma_commit_e(bar(C::B_AFREE));
         }
-        // ---- S^T(t+1) once dV has read region A (within a block; a new block needs the new K, V first)
+        // ---- S^T(t+1) into region A right behind dV(t), which reads P^T from it: tcgen05.mma
+        // operations issued by one thread are performed in issue order, so the write cannot overtake
+        // the read and no completion wait is needed (within a block; a new block needs the new K, V)
         if (has_next && !next_new_block) {
-          ok = wait_bar_warp(bar(C::B_AFREE), t & 1, ab);
-          if (ok) ok = wait_bar_warp(bar(C::B_QDOREADY + st1), ((t + 1) / C::NQS) & 1, ab);
+          ok = wait_bar_warp(bar(C::B_QDOREADY + st1), ((t + 1) / C::NQS) & 1, ab);
           if (!ok) break;
           tc_fence_after();
           issue_s(il, st1);
@@ -504,7 +504,6 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
         {
           const uint64_t bq = dQ0 + (uint64_t)((st * C::TILE) >> 4), bk = dK0 + (uint64_t)((cil * C::TILE) >> 4);
           mma_ts_x8_e<0, 8, 16, 24, 64, 72, 80, 88>(dcol, tb + C::TB, bq, KS_ROW, idKV, cjt > 0 ? 1u : 0u);
-          mma_commit_e(bar(C::B_BFREEM));
           mma_ss_x8_e(tb + C::TDQ, dS0, 4096 >> 4, bk, KS_ROW, idQ, 0u);
           mma_commit_e(bar(C::B_M2DONE));
           mma_commit_e(bar(C::B_QDOFREE + st));
@@ -519,9 +518,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
             tc_fence_after();
             issue_s(il, st1);
           }
-          // ---- dP^T(t+1) once dK has read region B and the dQ warps have read dQ(t) out of it
-          ok = wait_bar_warp(bar(C::B_BFREEM), t & 1, ab);
-          if (ok) ok = wait_bar_warp(bar(C::B_DQREAD), t & 1, ab);
+          // ---- dP^T(t+1) once the dQ warps have read dQ(t) out of region B (tcgen05.ld by other
+          // warps); dK(t), which reads dS^T from it, was issued earlier by this thread and is
+          // performed first
+          ok = wait_bar_warp(bar(C::B_DQREAD), t & 1, ab);
           if (!ok) break;
           tc_fence_after();
           issue_dp(il, st1);
