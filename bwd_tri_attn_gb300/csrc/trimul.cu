@@ -8,14 +8,19 @@
 //   outgoing:  X[b,i,j,c] = sum_k a[b,i,k,c] b[b,j,k,c]
 //   incoming:  X[b,i,j,c] = sum_k a[b,k,i,c] b[b,k,j,c]
 //
-// The projections are pair tensors [B, N, N, C] (channels innermost). The contraction is one
-// N x N matrix product per (batch, channel), so the gating kernel writes the gated operands
-// channel-major, [B, C, N, N], with the summed index innermost: A[b,c,i,k] = a[b,i,k,c] for the
-// outgoing update and a[b,k,i,c] for the incoming one (the pair axes swapped while gating), and
-// likewise B. Both directions are then X_bc = A_bc B_bc^T, a batched GEMM with K-major operands.
-// The backward products dA_bc = dX_bc B_bc and dB_bc = dX_bc^T A_bc are the same GEMM with one or
-// both operands read MN-major (the tensor cores' transposed operand mode, no transposed copies),
-// and the gating gradient maps them back to the pair layout.
+// The contraction is one N x N matrix product per (batch, channel), so the gated operands are
+// stored channel-major, [B, C, N, N]. Two layouts of the projections and their gradients:
+//
+// - pair layout [B, N, N, C] (channels innermost): the gating kernel transposes while it gates,
+//   A[b,c,i,k] = a[b,i,k,c] for the outgoing update and a[b,k,i,c] for the incoming one (the pair
+//   axes swapped), likewise B, so both directions are X_bc = A_bc B_bc^T with K-major operands.
+//   The backward products dA_bc = dX_bc B_bc and dB_bc = dX_bc^T A_bc are the same GEMM with one
+//   or both operands read MN-major (the tensor cores' transposed operand mode, no transposed
+//   copies), written in FP32 to a workspace, and a gradient kernel maps them back to the pair
+//   layout while applying the gating gradient.
+// - channel-major layout [B, C, N, N]: gating is element-wise; the incoming update reads its
+//   operands MN-major instead (X_bc = A_bc^T B_bc), and each backward product applies the gating
+//   gradient in its epilogue, so dA and dB never reach memory.
 //
 // Gating is bound by HBM bandwidth (one read of P and G, one write of the operand); folding it
 // into the GEMM's operand loads would recompute each sigmoid once per output tile that reads it
