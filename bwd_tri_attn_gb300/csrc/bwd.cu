@@ -794,8 +794,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUten
               for (int e = 0; e < 8; ++e) w[m][e] = 0u;
             }
           }
-#pragma unroll
           const float iw = __frcp_rn(-mw2.x);  // the register sums carry w (a power of two: exact)
+#pragma unroll
           for (int m = 0; m < QPT / 8; ++m) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
