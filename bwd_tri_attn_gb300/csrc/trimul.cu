@@ -42,38 +42,41 @@ int *device_status_word();
 
 namespace {
 
-// sigmoid in FP32 from the fast exponential and reciprocal: relative error a few ulp for the gate
-// logits of practice (|x| < 16); 0 below x = -87, where 1 + exp(-x) overflows.
+// sigmoid in FP32 from the fast exponential and reciprocal: relative error a few FP32 ulp plus
+// about one per unit of |x| (the fast exponential's error grows with its argument); 0 below
+// x = -87, where 1 + exp(-x) leaves the reciprocal's range.
 __device__ __forceinline__ float sigmoid_f(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// Both gating kernels run a 1-D grid of (batch, r tile, s tile, channel group, operand) with the
-// operand and then the channel group varying fastest: the CTAs that read the same pair positions
-// (their channel groups share cache lines) run at the same time.
+constexpr int kGateT = 16, kGateThreads = 256;  // positions per tile side, threads per CTA
+
+// Both pair-layout gating kernels run a 1-D grid of (batch, r tile, s tile, channel group,
+// operand) with the operand and then the channel group varying fastest: the CTAs that read the
+// same pair positions (their channel groups share cache lines) run at the same time.
 __device__ __forceinline__ void tile_of(int N, int groups, int &op, int &grp, int &b, int &r0, int &s0) {
-  const int nt = (N + 15) / 16;
+  const int nt = (N + kGateT - 1) / kGateT;
   int u = blockIdx.x;
   op = u & 1;
   u >>= 1;
   grp = u % groups;
   u /= groups;
-  s0 = (u % nt) * 16;
+  s0 = (u % nt) * kGateT;
   u /= nt;
-  r0 = (u % nt) * 16;
+  r0 = (u % nt) * kGateT;
   b = u / nt;
 }
 
 // ---------------------------------------------------------------- gating: pair -> channel-major
 // One CTA: 16 x 16 output positions (r, s) and a group of up to 64 channels, for one of the two
-// operands. Input position (x, y) = (r, s),
-// or (s, r) when the operand is transposed (incoming update). Each thread reads 16 channel bytes
+// operands. Input position (x, y) = (r, s), or (s, r) when the operand is transposed (incoming
+// update). Each thread reads 16 channel bytes
 // of two neighbouring positions s, s + 1 and writes the gated pairs as 32-bit words
 // (a(s), a(s + 1)) into shared memory [channel][r][s / 2]; the channel stride (145 words) and
 // row pitch (9 words) keep both the scattered writes and the row reads free of most bank
 // conflicts. Output rows (c, r) of 16 values (32 bytes) are then stored with 16-byte stores.
-constexpr int kGateT = 16, kGateCG = 64, kGateThreads = 256;
+constexpr int kGateCG = 64;                    // channels per CTA
 constexpr int kGateRowW = 9, kGateChW = 145;  // words
 constexpr int kGateSmem = kGateCG * kGateChW * 4;
 
