@@ -152,6 +152,7 @@ __global__ void __launch_bounds__(kGateThreads) trimul_gate_bwd_kernel(const Gat
   tile_of(g.N, g.groups, op, grp, b, r0, s0);
   const int N = g.N, C = g.C, c0 = grp * kGbCG, nq = min(kGbCG, C - c0) / 8;
   const float *dA = op ? g.dA[1] : g.dA[0];
+#pragma unroll
   for (int e = threadIdx.x; e < kGbCG * kGateT * 4; e += kGateThreads) {
     const int qt = e & 3, rl = (e >> 2) & 15, cl = e >> 6;
     const int r = r0 + rl, s = s0 + 4 * qt;
@@ -166,6 +167,7 @@ __global__ void __launch_bounds__(kGateThreads) trimul_gate_bwd_kernel(const Gat
               *G = reinterpret_cast<const uint4 *>(op ? g.G[1] : g.G[0]);
   uint4 *dP = reinterpret_cast<uint4 *>(op ? g.dP[1] : g.dP[0]), *dG = reinterpret_cast<uint4 *>(op ? g.dG[1] : g.dG[0]);
   const int64_t cv = C / 8;
+#pragma unroll
   for (int e = threadIdx.x; e < kGateT * kGateT * 4; e += kGateThreads) {
     const int q = e & 3, sl = (e >> 2) & 15, rl = e >> 6;
     const int r = r0 + rl, s = s0 + sl;
