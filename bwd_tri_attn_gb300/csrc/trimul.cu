@@ -250,7 +250,8 @@ struct GemmCfg {
   static constexpr int BM = 128, BN = 256, BK = 64, NST = 4;
   static constexpr int A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2, STAGE = A_BYTES + B_BYTES;
   static constexpr int MN_BOX = BK * 128;  // bytes of one 64-wide MN-major box (BK rows of 128 bytes)
-  static constexpr int EPI_WARPS = 8;
+  static constexpr int EPI_WARPS = 8;                  // a multiple of 4: whole TMEM lane quarters
+  static constexpr int EPI_CPW = BN / 32 / (EPI_WARPS / 4);  // 32-column chunks per epilogue warp
   static constexpr int EPI_PITCH = 33;                 // words per row of a warp's 32 x 32 staging tile
   static constexpr int EPI_TILE = 32 * EPI_PITCH * 4;  // bytes
   static constexpr int OFF_EPI = NST * STAGE;
@@ -414,7 +415,7 @@ __global__ void __launch_bounds__(GemmCfg::NTHREADS, 1)
     // thread takes 8-value pieces of four rows, so that one warp instruction covers 8 rows of 32
     // contiguous values (conflict-free: pitch 33 words).
     const int q = warp & 3;                             // the TMEM lane quarter this warp may access
-    const int cbase = ((warp - 2) >> 2) * (C::BN / 2);  // its half of the columns
+    const int cbase = ((warp - 2) >> 2) * (32 * C::EPI_CPW);  // its share of the columns
     const uint32_t lrow = (uint32_t)(q * 32) << 16;
     float *stg = reinterpret_cast<float *>(sm + C::OFF_EPI + (warp - 2) * C::EPI_TILE);
     const int rq = lane >> 2, cq = lane & 3;
@@ -441,11 +442,11 @@ __global__ void __launch_bounds__(GemmCfg::NTHREADS, 1)
       };
       if constexpr (kEpi == kEpiGate) load_pg(cbase, pv[0], gv[0]);
 #pragma unroll
-      for (int k = 0; k < C::BN / 64; ++k) {  // this warp's four 32-column chunks
+      for (int k = 0; k < C::EPI_CPW; ++k) {  // this warp's 32-column chunks
         const int c0 = cbase + 32 * k, n = n0 + c0;
         if (n >= N) break;  // uniform across the warp
         if constexpr (kEpi == kEpiGate)
-          if (k + 1 < C::BN / 64 && n + 32 < N) load_pg(c0 + 32, pv[(k + 1) & 1], gv[(k + 1) & 1]);
+          if (k + 1 < C::EPI_CPW && n + 32 < N) load_pg(c0 + 32, pv[(k + 1) & 1], gv[(k + 1) & 1]);
         const int col = n + 8 * cq;
         uint32_t r[32];
         tmem_ld32(tb + lrow + acc * C::BN + c0, r);
