@@ -50,20 +50,32 @@ PROFILES = {"fwd": ("fwd_kernel_crop384_h4_d32.md", ["fwd.cu"]),
 COMMON_SOURCES = ["common.cuh", "sm100.cuh", "sync.cuh", "tmap.cuh"]
 
 
+def source_digest(own) -> str:
+    """First 16 hex digits of the SHA-256 of a kernel's sources and the shared headers, with
+    comments removed and whitespace collapsed: a change to the code renews it, a change to a
+    comment does not."""
+    import hashlib
+    import re
+
+    h = hashlib.sha256()
+    for f in list(own) + COMMON_SOURCES:
+        with open(os.path.join(ROOT, "bwd_tri_attn_gb300", "csrc", f)) as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update((" ".join(src.split()) + "\n").encode())
+    return h.hexdigest()[:16]
+
+
 def profiled_traffic(kernel: str, activation_elements: int):
     """(DRAM bytes per launch, how they were obtained) from the kernel's ncu summary: the captured
     launch's figure when it ran on a workload of this activation size, else scaled by activation
     size (every input of the square crops grows with S*N*H*d); (None, reason) when the summary is
     missing or the kernel's sources changed since it was taken."""
-    import hashlib
-
     name, own = PROFILES[kernel]
     try:
         text = open(os.path.join(ROOT, "profiles", name)).read()
-        h = hashlib.sha256()
-        for f in own + COMMON_SOURCES:
-            with open(os.path.join(ROOT, "bwd_tri_attn_gb300", "csrc", f), "rb") as fh:
-                h.update(fh.read())
+        digest = source_digest(own)
     except OSError:
         return None, "no ncu summary"
     fields = {}
@@ -73,7 +85,7 @@ def profiled_traffic(kernel: str, activation_elements: int):
             fields[k] = v.strip()
     if len(fields) != 4:
         return None, "ncu summary incomplete"
-    if fields["source_digest"] != h.hexdigest()[:16]:
+    if fields["source_digest"] != digest:
         return None, "kernel sources changed since the ncu capture"
     captured = int(fields["activation_elements"])
     bytes_ = int(fields["dram_bytes_per_launch"])

@@ -57,10 +57,13 @@
 // from 256. Each elementwise thread writes P^T (dS^T) as packed FP16 over the S^T (dP^T) columns
 // it has just read: column group g of 64 queries keeps its 32 packed columns at A + 64g (B + 64g).
 // The dQ partial (128 queries x d, FP32) takes B + [32, 64), which dS^T leaves free. dV = P^T dO
-// is issued as soon as the P phase is done, and its completion frees region A for S^T(t+1);
-// dK = dS^T Q follows the dS phase, and once it has completed and the dQ warps have read dQ(t)
-// out of B, dP^T(t+1) may overwrite B; dQ = dS K reads dS from a 128-byte-swizzled FP16 tile in
-// shared memory. So the P phase of step t+1 overlaps step t's dK and dQ.
+// is issued as soon as the P phase is done and S^T(t+1) right behind it: the MMAs of one issuing
+// thread are performed in issue order, so S^T(t+1) cannot overwrite region A before dV(t) has
+// read it. dK = dS^T Q follows the dS phase, and dP^T(t+1) follows dK(t) into region B once the
+// dQ warps have read dQ(t) out of B (their tcgen05.ld is the one wait this needs); dQ = dS K reads
+// dS from a 128-byte-swizzled FP16 tile in shared memory. So the P phase of step t+1 overlaps
+// step t's dK and dQ. A new block of slices waits for dV(t) to complete before its S^T, since
+// it needs the block's new K and V in shared memory.
 #include "common.cuh"
 #include "launch.cuh"
 #include "plan.cuh"

@@ -4,6 +4,7 @@ parsing, the measured-peak lookup and the profile-digest check behind roofline.t
 """
 import hashlib
 import json
+import re
 import os
 import shutil
 import socket
@@ -95,7 +96,8 @@ def test_traffic_reported_only_for_matching_sources(monkeypatch, tmp_path):
     (tmp_path / "profiles").mkdir()
     h = hashlib.sha256()
     for f in ["fwd.cu"] + bench.COMMON_SOURCES:
-        h.update((csrc / f).read_bytes())
+        code = re.sub(r"//[^\n]*", " ", re.sub(r"/\*.*?\*/", " ", (csrc / f).read_text(), flags=re.S))
+        h.update((" ".join(code.split()) + "\n").encode())
     (tmp_path / "profiles" / "fwd_kernel_crop384_h4_d32.md").write_text(
         f"    source_digest: {h.hexdigest()[:16]}\n    workload: tiny\n    dram_bytes_per_launch: 1000\n"
         "    activation_elements: 10\n")
@@ -105,9 +107,13 @@ def test_traffic_reported_only_for_matching_sources(monkeypatch, tmp_path):
     assert "one tiny launch" in bench.profiled_traffic("fwd", 10)[1]
     assert bench.profiled_traffic("fwd", 40)[0] == pytest.approx(4000.0)
     assert "scaled" in bench.profiled_traffic("fwd", 40)[1]
-    # a changed source invalidates the figure
+    # a comment or blank line added to a source leaves the code, and the figure, as it was
+    with open(csrc / "common.cuh", "a") as f:
+        f.write("\n// a remark\n/* and a block\n   comment */\n\n")
+    assert bench.profiled_traffic("fwd", 10)[0] == 1000
+    # a changed line of code invalidates it
     with open(csrc / "fwd.cu", "a") as f:
-        f.write("\n")
+        f.write("\nstatic const int unused_probe = 0;\n")
     assert bench.profiled_traffic("fwd", 40)[0] is None
     # a missing summary reports nothing
     assert bench.profiled_traffic("bwd_main", 40)[0] is None
