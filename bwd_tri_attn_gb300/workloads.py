@@ -173,3 +173,61 @@ def make_mul_inputs(B, N, C, seed, std=1.0, gate_std=1.0):
 
 def mul_inputs_for(w: MulWorkload):
     return make_mul_inputs(w.B, w.N, w.C, w.seed, w.std, w.gate_std)
+
+
+@dataclass(frozen=True)
+class ModWorkload:
+    """One named input recipe of the triangle-attention block (LayerNorm, projections, attention,
+    gate, output projection) around the attention core."""
+
+    name: str
+    B: int
+    N: int
+    c: int   # pair channels
+    H: int
+    d: int
+    seed: int
+    mask: tuple = ("none",)
+    node: int = 0
+    notes: str = field(default="", compare=False)
+
+    def flops(self) -> float:
+        """Algorithmic fwd+bwd FLOPs: the attention's 14 B N^3 H d, plus the projections' GEMMs
+        (2 M c (5 H d + H) forward, twice that backward, M = B N^2)."""
+        m = float(self.B) * self.N * self.N
+        hd = self.H * self.d
+        return 14.0 * m * self.N * hd + 3 * 2.0 * m * self.c * (5 * hd + self.H)
+
+
+MOD_TINY = ModWorkload("mod_tiny_n24_c64_h2_d32", B=1, N=24, c=64, H=2, d=32, seed=20, notes="smallest tile case")
+MOD_RAGGED = ModWorkload("mod_ragged_b2_n72_c128_h4_d16", B=2, N=72, c=128, H=4, d=16, seed=21,
+                         mask=("tail", 5), notes="N off every tile size, d = 16, tail mask")
+MOD_ENDING = ModWorkload("mod_ending_n136_c128_h4_d32", B=1, N=136, c=128, H=4, d=32, seed=22,
+                         mask=("random", 0.1), node=1, notes="ending node, ragged N, random key mask")
+MOD_CROP384 = ModWorkload("mod_crop384_c128_h4_d32", B=1, N=384, c=128, H=4, d=32, seed=23, mask=("zeros",),
+                          notes="crop 384 with AlphaFold3-style pair width 128")
+MOD_CROP768 = ModWorkload("mod_crop768_c128_h4_d32", B=1, N=768, c=128, H=4, d=32, seed=24, mask=("tail", 48),
+                          notes="crop 768, last 48 keys padding-masked")
+
+MOD_ALL = {w.name: w for w in (MOD_TINY, MOD_RAGGED, MOD_ENDING, MOD_CROP384, MOD_CROP768)}
+
+
+def make_module_inputs(B, N, c, H, d, seed, mask=("none",)):
+    """Draws, in this order: z [B,N,N,c], dout [B,N,N,c] (BF16, unit normal), the LayerNorm scale
+    and shift (FP32, 1 + 0.1 n and 0.1 n), the projection weights W [4 H d, c] and wb [H, c] (BF16,
+    normal / sqrt(c)) and Wo [c, H d] (BF16, normal / sqrt(H d)), then the mask's own draws."""
+    gen = torch.Generator().manual_seed(int(seed))
+    hd = H * d
+    z = _normal(gen, (B, N, N, c), 1.0)
+    dout = _normal(gen, (B, N, N, c), 1.0)
+    gamma = 1.0 + 0.1 * torch.randn((c,), generator=gen, dtype=torch.float32)
+    beta = 0.1 * torch.randn((c,), generator=gen, dtype=torch.float32)
+    W = _normal(gen, (4 * hd, c), c ** -0.5)
+    wb = _normal(gen, (H, c), c ** -0.5)
+    Wo = _normal(gen, (c, hd), hd ** -0.5)
+    m = make_mask(mask, B, N, N, gen)
+    return {"z": z, "dout": dout, "gamma": gamma, "beta": beta, "W": W, "wb": wb, "Wo": Wo, "mask": m}
+
+
+def module_inputs_for(w: ModWorkload):
+    return make_module_inputs(w.B, w.N, w.c, w.H, w.d, w.seed, w.mask)
