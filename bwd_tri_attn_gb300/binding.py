@@ -1,4 +1,5 @@
-"""Thin ctypes binding of the C ABI in ``include/tri_attn.h`` and ``include/tri_mul.h``.
+"""Thin ctypes binding of the C ABI in ``include/tri_attn.h``, ``include/tri_mul.h`` and
+``include/tri_module.h``.
 
 Argument marshalling only: PyTorch tensors supply device pointers and the
 current CUDA stream; every step of the computation runs in the library's
@@ -42,7 +43,8 @@ class TriAttnError(RuntimeError):
 _VP = ctypes.c_void_p
 EXPORTS = ("tri_attn_strerror", "tri_attn_fwd", "tri_attn_bwd_workspace_size", "tri_attn_bwd_split", "tri_attn_bwd",
            "tri_attn_device_status", "tri_attn_set_timing_events", "tri_attn_bwd_static", "tri_mul_fwd",
-           "tri_mul_bwd_workspace_size", "tri_mul_bwd")
+           "tri_mul_bwd_workspace_size", "tri_mul_bwd", "tri_module_saved_size", "tri_module_bwd_workspace_size",
+           "tri_module_fwd", "tri_module_bwd")
 
 
 LAYOUT_PAIR, LAYOUT_CHANNEL_MAJOR = 0, 1  # tri_mul_shape.layout
@@ -57,6 +59,16 @@ class MulShape(ctypes.Structure):
     def __repr__(self):
         return (f"MulShape(B={self.B}, N={self.N}, C={self.C}, incoming={self.incoming}, "
                 f"layout={self.layout})")
+
+
+class ModuleShape(ctypes.Structure):
+    """tri_module_shape: batch, residues, pair channels, heads, head dimension, node, LayerNorm eps."""
+    _fields_ = [("B", ctypes.c_int), ("N", ctypes.c_int), ("c", ctypes.c_int), ("H", ctypes.c_int),
+                ("d", ctypes.c_int), ("node", ctypes.c_int), ("eps", ctypes.c_float)]
+
+    def __repr__(self):
+        return (f"ModuleShape(B={self.B}, N={self.N}, c={self.c}, H={self.H}, d={self.d}, node={self.node}, "
+                f"eps={self.eps})")
 
 
 def lib_path() -> str:
@@ -96,6 +108,14 @@ def load(path: str | None = None):
         lib.tri_mul_bwd_workspace_size.restype = ctypes.c_size_t
         lib.tri_mul_bwd.argtypes = [MulShape] + [_VP] * 12 + [ctypes.c_size_t, _VP]
         lib.tri_mul_bwd.restype = ctypes.c_int
+        lib.tri_module_saved_size.argtypes = [ModuleShape]
+        lib.tri_module_saved_size.restype = ctypes.c_size_t
+        lib.tri_module_bwd_workspace_size.argtypes = [ModuleShape]
+        lib.tri_module_bwd_workspace_size.restype = ctypes.c_size_t
+        lib.tri_module_fwd.argtypes = [ModuleShape] + [_VP] * 9 + [ctypes.c_size_t, _VP]
+        lib.tri_module_fwd.restype = ctypes.c_int
+        lib.tri_module_bwd.argtypes = [ModuleShape] + [_VP] * 8 + [ctypes.c_size_t] + [_VP] * 8 + [ctypes.c_size_t, _VP]
+        lib.tri_module_bwd.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -175,6 +195,32 @@ def tri_mul_bwd(shape: MulShape, Pa, Ga, Pb, Gb, A, Bm, dX, dPa, dGa, dPb, dGb, 
     rc = load().tri_mul_bwd(shape, _p(Pa), _p(Ga), _p(Pb), _p(Gb), _p(A), _p(Bm), _p(dX), _p(dPa), _p(dGa),
                             _p(dPb), _p(dGb), _p(workspace), nbytes, _stream(stream))
     _check("tri_mul_bwd", rc)
+
+
+def tri_module_saved_size(shape: ModuleShape) -> int:
+    return int(load().tri_module_saved_size(shape))
+
+
+def tri_module_bwd_workspace_size(shape: ModuleShape) -> int:
+    return int(load().tri_module_bwd_workspace_size(shape))
+
+
+def _nbytes(t):
+    return 0 if t is None else t.numel() * t.element_size()
+
+
+def tri_module_fwd(shape: ModuleShape, z, gamma, beta, W, wb, Wo, mask, out, saved, stream=None):
+    rc = load().tri_module_fwd(shape, _p(z), _p(gamma), _p(beta), _p(W), _p(wb), _p(Wo), _p(mask), _p(out),
+                               _p(saved), _nbytes(saved), _stream(stream))
+    _check("tri_module_fwd", rc)
+
+
+def tri_module_bwd(shape: ModuleShape, z, gamma, beta, W, wb, Wo, mask, saved, dout, dz, dgamma, dbeta, dW, dwb,
+                   dWo, workspace, stream=None):
+    rc = load().tri_module_bwd(shape, _p(z), _p(gamma), _p(beta), _p(W), _p(wb), _p(Wo), _p(mask), _p(saved),
+                               _nbytes(saved), _p(dout), _p(dz), _p(dgamma), _p(dbeta), _p(dW), _p(dwb), _p(dWo),
+                               _p(workspace), _nbytes(workspace), _stream(stream))
+    _check("tri_module_bwd", rc)
 
 
 def tri_attn_device_status(stream=None) -> int:
@@ -259,3 +305,35 @@ def mul_backward(Pa, Ga, Pb, Gb, A, Bm, dX, incoming=False, layout=LAYOUT_PAIR, 
     outs = [torch.empty_like(Pa) for _ in range(4)]
     tri_mul_bwd(shape, Pa, Ga, Pb, Gb, A, Bm, dX, *outs, workspace, stream)
     return tuple(outs)
+
+
+def module_shape_of(z: torch.Tensor, H: int, d: int, node: int = NODE_STARTING, eps: float = 1e-5) -> ModuleShape:
+    """Shape of the triangle-attention block on the pair representation z [B, N, N, c]."""
+    B, N, N2, c = (int(x) for x in z.shape)
+    if N2 != N:
+        raise ValueError(f"pair representation must be square, got {tuple(z.shape)}")
+    return ModuleShape(B, N, c, int(H), int(d), int(node), float(eps))
+
+
+def module_forward(z, gamma, beta, W, wb, Wo, mask, H, d, node=NODE_STARTING, eps=1e-5, stream=None):
+    """Returns (out, saved): out [B, N, N, c] and the activations module_backward reads."""
+    shape = module_shape_of(z, H, d, node, eps)
+    saved = torch.empty(max(tri_module_saved_size(shape), 16), dtype=torch.uint8, device=z.device)
+    out = torch.empty_like(z)
+    tri_module_fwd(shape, z, gamma, beta, W, wb, Wo, mask, out, saved, stream)
+    return out, saved
+
+
+def module_backward(z, gamma, beta, W, wb, Wo, mask, saved, dout, H, d, node=NODE_STARTING, eps=1e-5,
+                    workspace=None, stream=None):
+    """Returns (dz, dgamma, dbeta, dW, dwb, dWo); the weight gradients are FP32."""
+    shape = module_shape_of(z, H, d, node, eps)
+    if workspace is None:
+        workspace = torch.empty(max(tri_module_bwd_workspace_size(shape), 16), dtype=torch.uint8, device=z.device)
+    dz = torch.empty_like(z)
+    f32 = dict(dtype=torch.float32, device=z.device)
+    dgamma, dbeta = torch.empty(gamma.shape, **f32), torch.empty(beta.shape, **f32)
+    dW, dwb, dWo = torch.empty(W.shape, **f32), torch.empty(wb.shape, **f32), torch.empty(Wo.shape, **f32)
+    tri_module_bwd(shape, z, gamma, beta, W, wb, Wo, mask, saved, dout, dz, dgamma, dbeta, dW, dwb, dWo, workspace,
+                   stream)
+    return dz, dgamma, dbeta, dW, dwb, dWo

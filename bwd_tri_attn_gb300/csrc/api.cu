@@ -95,6 +95,96 @@ namespace triattn {
 int *device_status_word() { return status_word(); }
 // The calling thread's k-th timing event, for entry points defined in other files.
 cudaError_t timing_mark(int k, cudaStream_t st) { return mark(k, st); }
+
+// Every check and the launch plan of a forward call, with nothing enqueued.
+int attn_fwd_prepare(const tri_attn_shape &shape, const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                     const uint16_t *bias, const uint16_t *mask, uint16_t *O, float *LSE, uint16_t *Ores,
+                     AttnFwdCall *c) {
+  int rc = check_shape(shape);
+  if (rc) return rc;
+  if (!Q || !K || !V || !bias || !O || !LSE) return TRI_ATTN_ERR_INVALID_ARG;
+  const void *ptrs[] = {Q, K, V, bias, mask, O, LSE, Ores};
+  for (const void *p : ptrs)
+    if (p && !aligned16(p)) return TRI_ATTN_ERR_UNSUPPORTED;
+  c->g = to_dims(shape);
+  c->V = V;
+  c->bias = bias;
+  c->mask = mask;
+  c->O = O;
+  c->LSE = LSE;
+  c->Ores = Ores;
+  c->status = status_word();
+  if (!c->status) return TRI_ATTN_ERR_CUDA;
+  if (plan_fwd(c->g, Q, K, V, bias, &c->plan) != cudaSuccess) return TRI_ATTN_ERR_CUDA;
+  return TRI_ATTN_OK;
+}
+
+// The forward's kernels; the caller's timing events mark0, mark0 + 1 follow them.
+cudaError_t attn_fwd_enqueue(const AttnFwdCall &c, int mark0, cudaStream_t st) {
+  cudaError_t e = launch_fwd_vscale(c.g, c.V, c.LSE, st);
+  if (e == cudaSuccess) e = mark(mark0, st);
+  if (e == cudaSuccess) e = launch_fwd(c.g, c.plan, c.bias, c.mask, c.O, c.LSE, c.Ores, c.status, st);
+  if (e == cudaSuccess) e = mark(mark0 + 1, st);
+  return e;
+}
+
+// Every check, the work split and the launch plan of a backward call, with nothing enqueued.
+int attn_bwd_prepare(const tri_attn_shape &shape, const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                     const uint16_t *bias, const uint16_t *mask, const uint16_t *O, const uint16_t *Ores,
+                     const float *LSE, const uint16_t *dO, uint16_t *dQ, uint16_t *dK, uint16_t *dV,
+                     uint16_t *dBias, void *workspace, size_t workspace_bytes, AttnBwdCall *c) {
+  int rc = check_shape(shape);
+  if (rc) return rc;
+  if (!Q || !K || !V || !bias || !O || !LSE || !dO || !dQ || !dK || !dV || !dBias)
+    return TRI_ATTN_ERR_INVALID_ARG;
+  const void *ptrs[] = {Q, K, V, bias, mask, O, Ores, LSE, dO, dQ, dK, dV, dBias, workspace};
+  for (const void *p : ptrs)
+    if (p && !aligned16(p)) return TRI_ATTN_ERR_UNSUPPORTED;
+  int nsm = 0;
+  if (device_sm_count(&nsm) != cudaSuccess) return TRI_ATTN_ERR_CUDA;
+  const WorkspaceLayout w = layout_for(shape, nsm);
+  if (!workspace || workspace_bytes < w.total) return TRI_ATTN_ERR_WORKSPACE;
+  c->g = to_dims(shape);
+  // the work split (and with it the reduction order) is settled before anything is enqueued
+  if (bwd_split_active(c->g, &c->sp) != cudaSuccess) return TRI_ATTN_ERR_CUDA;
+  if (c->sp.KMAX > w.slots) return TRI_ATTN_ERR_CUDA;  // (cannot happen: the workspace covers every split)
+  char *ws = static_cast<char *>(workspace);
+  c->Dv = reinterpret_cast<float *>(ws + w.d_off);
+  c->emax = reinterpret_cast<int *>(ws + w.scl_off);
+  c->biasT = reinterpret_cast<uint16_t *>(ws + w.biast_off);
+  c->partial = reinterpret_cast<float *>(ws + w.partial_off);
+  c->Q = Q;
+  c->K = K;
+  c->V = V;
+  c->bias = bias;
+  c->mask = mask;
+  c->O = O;
+  c->Ores = Ores;
+  c->LSE = LSE;
+  c->dO = dO;
+  c->dQ = dQ;
+  c->dK = dK;
+  c->dV = dV;
+  c->dBias = dBias;
+  c->status = status_word();
+  if (!c->status) return TRI_ATTN_ERR_CUDA;
+  if (plan_bwd(c->g, c->sp, Q, K, V, dO, c->biasT, dK, dV, &c->plan) != cudaSuccess) return TRI_ATTN_ERR_CUDA;
+  return TRI_ATTN_OK;
+}
+
+// The backward's four kernels; the caller's timing events mark0 .. mark0 + 3 follow them.
+cudaError_t attn_bwd_enqueue(const AttnBwdCall &c, int mark0, cudaStream_t st) {
+  cudaError_t e = launch_bias_transpose(c.g, c.bias, c.biasT, c.emax, st);
+  if (e == cudaSuccess) e = mark(mark0, st);
+  if (e == cudaSuccess) e = launch_bwd_prep(c.g, c.dO, c.O, c.Ores, c.Q, c.K, c.V, c.Dv, c.emax, st);
+  if (e == cudaSuccess) e = mark(mark0 + 1, st);
+  if (e == cudaSuccess)
+    e = launch_bwd_main(c.g, c.plan, c.LSE, c.Dv, c.emax, c.mask, c.dQ, c.dK, c.dV, c.partial, c.status, st);
+  if (e == cudaSuccess) e = mark(mark0 + 2, st);
+  if (e == cudaSuccess) e = launch_dbias_reduce_t(c.g, c.sp, c.partial, c.dBias, st);
+  if (e == cudaSuccess) e = mark(mark0 + 3, st);
+  return e;
+}
 }  // namespace triattn
 
 extern "C" {
@@ -116,23 +206,10 @@ const char *tri_attn_strerror(int code) {
 int tri_attn_fwd(tri_attn_shape shape, const tri_attn_bf16 *Q, const tri_attn_bf16 *K,
                  const tri_attn_bf16 *V, const tri_attn_bf16 *bias, const tri_attn_bf16 *mask,
                  tri_attn_bf16 *O, float *LSE, tri_attn_bf16 *Ores, void *stream) {
-  int rc = check_shape(shape);
+  AttnFwdCall c;
+  const int rc = attn_fwd_prepare(shape, Q, K, V, bias, mask, O, LSE, Ores, &c);
   if (rc) return rc;
-  if (!Q || !K || !V || !bias || !O || !LSE) return TRI_ATTN_ERR_INVALID_ARG;
-  const void *ptrs[] = {Q, K, V, bias, mask, O, LSE, Ores};
-  for (const void *p : ptrs)
-    if (p && !aligned16(p)) return TRI_ATTN_ERR_UNSUPPORTED;
-  const Dims g = to_dims(shape);
-  auto st = static_cast<cudaStream_t>(stream);
-  int *status = status_word();
-  if (!status) return TRI_ATTN_ERR_CUDA;
-  FwdPlan plan;
-  if (plan_fwd(g, Q, K, V, bias, &plan) != cudaSuccess) return TRI_ATTN_ERR_CUDA;
-  cudaError_t e = launch_fwd_vscale(g, V, LSE, st);
-  if (e == cudaSuccess) e = mark(0, st);
-  if (e == cudaSuccess) e = launch_fwd(g, plan, bias, mask, O, LSE, Ores, status, st);
-  if (e == cudaSuccess) e = mark(1, st);
-  return cuda_rc(e);
+  return cuda_rc(attn_fwd_enqueue(c, 0, static_cast<cudaStream_t>(stream)));
 }
 
 size_t tri_attn_bwd_workspace_size(tri_attn_shape shape) {
@@ -162,41 +239,11 @@ int tri_attn_bwd(tri_attn_shape shape, const tri_attn_bf16 *Q, const tri_attn_bf
                  const tri_attn_bf16 *O, const tri_attn_bf16 *Ores, const float *LSE,
                  const tri_attn_bf16 *dO, tri_attn_bf16 *dQ, tri_attn_bf16 *dK, tri_attn_bf16 *dV,
                  tri_attn_bf16 *dBias, void *workspace, size_t workspace_bytes, void *stream) {
-  int rc = check_shape(shape);
+  AttnBwdCall c;
+  const int rc = attn_bwd_prepare(shape, Q, K, V, bias, mask, O, Ores, LSE, dO, dQ, dK, dV, dBias, workspace,
+                                  workspace_bytes, &c);
   if (rc) return rc;
-  if (!Q || !K || !V || !bias || !O || !LSE || !dO || !dQ || !dK || !dV || !dBias)
-    return TRI_ATTN_ERR_INVALID_ARG;
-  const void *ptrs[] = {Q, K, V, bias, mask, O, Ores, LSE, dO, dQ, dK, dV, dBias, workspace};
-  for (const void *p : ptrs)
-    if (p && !aligned16(p)) return TRI_ATTN_ERR_UNSUPPORTED;
-  int nsm = 0;
-  if (device_sm_count(&nsm) != cudaSuccess) return TRI_ATTN_ERR_CUDA;
-  const WorkspaceLayout w = layout_for(shape, nsm);
-  if (!workspace || workspace_bytes < w.total) return TRI_ATTN_ERR_WORKSPACE;
-  const Dims g = to_dims(shape);
-  // the work split (and with it the reduction order) is settled before anything is enqueued
-  BwdSplit sp;
-  if (bwd_split_active(g, &sp) != cudaSuccess) return TRI_ATTN_ERR_CUDA;
-  if (sp.KMAX > w.slots) return TRI_ATTN_ERR_CUDA;  // (cannot happen: the workspace covers every split)
-  auto st = static_cast<cudaStream_t>(stream);
-  char *ws = static_cast<char *>(workspace);
-  float *Dv = reinterpret_cast<float *>(ws + w.d_off);
-  int *emax = reinterpret_cast<int *>(ws + w.scl_off);
-  uint16_t *biasT = reinterpret_cast<uint16_t *>(ws + w.biast_off);
-  float *partial = reinterpret_cast<float *>(ws + w.partial_off);
-  int *status = status_word();
-  if (!status) return TRI_ATTN_ERR_CUDA;
-  BwdPlan plan;
-  if (plan_bwd(g, sp, Q, K, V, dO, biasT, dK, dV, &plan) != cudaSuccess) return TRI_ATTN_ERR_CUDA;
-  cudaError_t e = launch_bias_transpose(g, bias, biasT, emax, st);
-  if (e == cudaSuccess) e = mark(0, st);
-  if (e == cudaSuccess) e = launch_bwd_prep(g, dO, O, Ores, Q, K, V, Dv, emax, st);
-  if (e == cudaSuccess) e = mark(1, st);
-  if (e == cudaSuccess) e = launch_bwd_main(g, plan, LSE, Dv, emax, mask, dQ, dK, dV, partial, status, st);
-  if (e == cudaSuccess) e = mark(2, st);
-  if (e == cudaSuccess) e = launch_dbias_reduce_t(g, sp, partial, dBias, st);
-  if (e == cudaSuccess) e = mark(3, st);
-  return cuda_rc(e);
+  return cuda_rc(attn_bwd_enqueue(c, 0, static_cast<cudaStream_t>(stream)));
 }
 
 int tri_attn_set_timing_events(void *const *events, int n) {

@@ -1,0 +1,881 @@
+// Triangle-attention block around the attention core: LayerNorm, the q/k/v, pair-bias and gate
+// projections, the attention (fwd.cu, bwd.cu), the sigmoid gate and the output projection,
+// forward and backward.
+//
+// TurboPairFormer (arXiv 2610.05854v1, Abstract, first sentence) places the attention in
+// AlphaFold3-style models without describing the layers around it; this is the plainest reading
+// of that model family's triangle-attention layer (include/tri_module.h states it in full).
+//
+// Forward (M = B N^2 pair positions, hd = H d):
+//   mod_ln_fwd_kernel     z -> zt (BF16), mean, 1/std; pair bias zt . wb (transposed for the ending node)
+//   GEMM                  zt W^T -> q | k | v | gl (one product, the epilogue routes each 128- or
+//                         64-column block to its tensor)
+//   attention             tri_attn forward on q, k, v, bias, mask
+//   mod_gate_kernel       go = sigmoid(gl) O
+//   GEMM                  go Wo^T -> out
+// Backward:
+//   GEMM + gate epilogue  dgo = dout Wo; the epilogue writes dO = dgo s and dgl = dgo O s (1 - s)
+//                         (s = sigmoid(gl)): dgo never reaches memory
+//   GEMM (split over M)   dWo partials = dout^T go, then an ordered sum over the splits
+//   attention             tri_attn backward -> dq, dk, dv, dbias
+//   GEMM                  dzt = [dq | dk | dv | dgl] W (FP32), the four tensors read as one K-segmented operand
+//   mod_ln_bwd_kernel     dzt + dbias wb -> dz; per-CTA partial sums of dgamma, dbeta, dwb
+//   GEMM (split over M)   dW partials = [dq | dk | dv | dgl]^T zt, then ordered sums
+//
+// The GEMM is one persistent tcgen05 kernel for every product: M = 128 x N = 256 tiles, K steps
+// of 64 through a 4-stage TMA ring, two TMEM accumulators so that one tile's epilogue overlaps
+// the next tile's main loop. Operands are K-major (row-major [rows][K]) or MN-major (the
+// transposed operand mode, [K][rows]); one operand may be split into up to four tensors along K
+// (K-major) or M (MN-major), so [dq | dk | dv | dgl] is read where the attention left it. Products
+// summed over the pair positions split K into fixed chunks of rows; each chunk's FP32 partial is
+// written out and the partials are added in chunk order, so every weight gradient is the same
+// bits on every call.
+#include <math.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "launch.cuh"
+#include "plan.cuh"
+#include "sm100.cuh"
+#include "sync.cuh"
+#include "tmap.cuh"
+#include "tri_module.h"
+
+namespace triattn {
+using namespace sm100;
+
+int *device_status_word();
+
+namespace {
+
+// sigmoid in FP32 from the fast exponential and reciprocal (a few FP32 ulp plus about one per
+// unit of |x|; 0 below x = -87)
+__device__ __forceinline__ float sigm(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
+__device__ __forceinline__ float lo_bf(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float hi_bf(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// ================================================================ GEMM
+enum { kOutBF16 = 0, kOutF32 = 1, kOutGate = 2 };
+
+struct MGemmArgs {
+  int M, N, K, Kc, T;     // D[t][m][n] = sum over k in [t Kc, min(K, t Kc + Kc)) of A(m, k) B(n, k)
+  int segA, nsegA;        // A's tensors hold segA elements each along K (K-major A) or M (MN-major A)
+  void *D0, *D1, *D2, *D3;  // kOutBF16: column segments of segD columns, row stride segD; kOutF32: [T][M][N]
+  int segD;
+  const uint16_t *P, *G;  // kOutGate: [M][N] attention output and gate logits
+  uint16_t *dP, *dG;      // kOutGate: [M][N] their gradients
+};
+
+struct MGemmCfg {
+  static constexpr int BM = 128, BN = 256, BK = 64, NST = 4;
+  static constexpr int A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2, STAGE = A_BYTES + B_BYTES;
+  static constexpr int MN_BOX = BK * 128;  // one 64-wide MN-major box: BK rows of 128 bytes
+  static constexpr int EPI_WARPS = 8;
+  static constexpr int EPI_CPW = BN / 32 / (EPI_WARPS / 4);  // 32-column chunks per epilogue warp
+  static constexpr int EPI_PITCH = 33;
+  static constexpr int EPI_TILE = 32 * EPI_PITCH * 4;
+  static constexpr int OFF_EPI = NST * STAGE;
+  static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * EPI_TILE;
+  static constexpr int B_FULL = 0, B_EMPTY = NST, B_ACCF = 2 * NST, B_ACCE = B_ACCF + 2, B_DONE = B_ACCE + 2,
+                       NBAR = B_DONE + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM_ALLOC = OFF_MISC + 16 + 1024;
+  static constexpr int NTHREADS = 64 + 32 * EPI_WARPS;
+  static constexpr uint32_t TMEM_COLS = 2 * BN;
+  static_assert(STAGE % 1024 == 0 && A_BYTES % 1024 == 0, "SW128 tiles need 1 KB alignment");
+  static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+};
+
+template <int kOut>
+__device__ __forceinline__ void mgemm_store8(const MGemmArgs &a, int t, int m, int n, const float (&v)[8]) {
+  if constexpr (kOut == kOutF32) {
+    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(a.D0) + ((int64_t)t * a.M + m) * a.N + n);
+    dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+    dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+  } else if constexpr (kOut == kOutBF16) {
+    const int s = n / a.segD;
+    void *base = s == 0 ? a.D0 : s == 1 ? a.D1 : s == 2 ? a.D2 : a.D3;
+    *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(base) + (int64_t)m * a.segD + (n - s * a.segD)) =
+        make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+  } else {
+    const int64_t off = (int64_t)m * a.N + n;
+    const uint4 pv = *reinterpret_cast<const uint4 *>(a.P + off), gv = *reinterpret_cast<const uint4 *>(a.G + off);
+    const uint32_t pw[4] = {pv.x, pv.y, pv.z, pv.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
+    uint32_t od[4], og[4];
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const float d0 = v[2 * x], d1 = v[2 * x + 1];
+      const float s0 = sigm(lo_bf(gw[x])), s1 = sigm(hi_bf(gw[x]));
+      od[x] = pack_bf16x2(d0 * s0, d1 * s1);
+      og[x] = pack_bf16x2(d0 * lo_bf(pw[x]) * (s0 * (1.f - s0)), d1 * hi_bf(pw[x]) * (s1 * (1.f - s1)));
+    }
+    *reinterpret_cast<uint4 *>(a.dP + off) = make_uint4(od[0], od[1], od[2], od[3]);
+    *reinterpret_cast<uint4 *>(a.dG + off) = make_uint4(og[0], og[1], og[2], og[3]);
+  }
+}
+
+template <bool kAMN, bool kBMN, int kOut>
+__global__ void __launch_bounds__(MGemmCfg::NTHREADS, 1)
+    mod_gemm_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
+                    const __grid_constant__ CUtensorMap mA2, const __grid_constant__ CUtensorMap mA3,
+                    const __grid_constant__ CUtensorMap mB, const MGemmArgs a, int *status) {
+  using C = MGemmCfg;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb0 = smem_u32(sm);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto bar = [&](int k) { return sb0 + C::OFF_BAR + 8u * (uint32_t)k; };
+  volatile uint32_t *misc = reinterpret_cast<volatile uint32_t *>(sm + C::OFF_MISC);
+  const Abort ab{reinterpret_cast<volatile int *>(misc + 1), status};
+  const int mt = (a.M + C::BM - 1) / C::BM, nt = (a.N + C::BN - 1) / C::BN;
+  const int ntiles = a.T * mt * nt;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::NST; ++s) {
+      mbar_init(bar(C::B_FULL + s), 1);
+      mbar_init(bar(C::B_EMPTY + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(C::B_ACCF + s), 1);
+      mbar_init(bar(C::B_ACCE + s), 32 * C::EPI_WARPS);
+    }
+    mbar_init(bar(C::B_DONE), 1);
+    misc[1] = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(sb0 + C::OFF_MISC, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = misc[0];
+  auto tile_of = [&](int u, int &t, int &m0, int &n0) {
+    t = u / (mt * nt);
+    const int r = u - t * (mt * nt);
+    m0 = (r / nt) * C::BM;
+    n0 = (r % nt) * C::BN;
+  };
+  // K blocks of split t (at least one: the host picks T = ceil(K / Kc))
+  auto kblocks = [&](int t, int &k0) {
+    k0 = t * a.Kc;
+    return (min(a.K, k0 + a.Kc) - k0 + C::BK - 1) / C::BK;
+  };
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    bool ok = true;
+    int it = 0;
+    if (lane == 0) {
+      tma_prefetch_map(&mA0);
+      tma_prefetch_map(&mB);
+    }
+    for (int u = blockIdx.x; u < ntiles && ok; u += gridDim.x) {
+      int t, m0, n0, kbeg;
+      tile_of(u, t, m0, n0);
+      const int nk = kblocks(t, kbeg);
+      for (int kb = 0; kb < nk; ++kb, ++it) {
+        const int st = it % C::NST;
+        if (it >= C::NST) ok = wait_bar_warp(bar(C::B_EMPTY + st), ((it / C::NST) - 1) & 1, ab);
+        if (!ok) break;
+        if (lane == 0) {
+          const uint32_t dst = sb0 + st * C::STAGE, fb = bar(C::B_FULL + st);
+          const int k0 = kbeg + kb * C::BK;
+          mbar_arrive_expect_tx(fb, C::STAGE);
+          if constexpr (kAMN) {
+#pragma unroll
+            for (int x = 0; x < C::BM / 64; ++x) {
+              const int mm = m0 + 64 * x, s = min(mm / a.segA, a.nsegA - 1);
+              const CUtensorMap *pa = s == 0 ? &mA0 : s == 1 ? &mA1 : s == 2 ? &mA2 : &mA3;
+              tma_load_3d(dst + x * C::MN_BOX, pa, fb, mm - s * a.segA, k0, 0);
+            }
+          } else {
+            const int s = min(k0 / a.segA, a.nsegA - 1);
+            const CUtensorMap *pa = s == 0 ? &mA0 : s == 1 ? &mA1 : s == 2 ? &mA2 : &mA3;
+            tma_load_3d(dst, pa, fb, k0 - s * a.segA, m0, 0);
+          }
+          if constexpr (kBMN) {
+#pragma unroll
+            for (int x = 0; x < C::BN / 64; ++x) tma_load_3d(dst + C::A_BYTES + x * C::MN_BOX, &mB, fb, n0 + 64 * x, k0, 0);
+          } else {
+            tma_load_3d(dst + C::A_BYTES, &mB, fb, k0, n0, 0);
+          }
+        }
+        __syncwarp();
+      }
+    }
+    if (!ok && lane == 0)  // let the copies in flight land before the CTA exits
+      for (int x = max(0, it - C::NST); x < it; ++x) drain_bar(bar(C::B_FULL + x % C::NST), (x / C::NST) & 1);
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (whole warp, elect.sync)
+    constexpr uint32_t idesc = idesc_f16(C::BM, C::BN, true, true, kAMN, kBMN);
+    constexpr uint64_t a_step = kAMN ? (16 * 128) >> 4 : 32 >> 4;
+    constexpr uint64_t b_step = kBMN ? (16 * 128) >> 4 : 32 >> 4;
+    bool ok = true;
+    int it = 0, tl = 0;
+    for (int u = blockIdx.x; u < ntiles && ok; u += gridDim.x, ++tl) {
+      int t, m0, n0, kbeg;
+      tile_of(u, t, m0, n0);
+      const int nk = kblocks(t, kbeg);
+      const int acc = tl & 1;
+      if (tl >= 2) ok = wait_bar_warp(bar(C::B_ACCE + acc), ((tl >> 1) - 1) & 1, ab);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t dacc = tb + acc * C::BN;
+      for (int kb = 0; kb < nk; ++kb, ++it) {
+        const int st = it % C::NST;
+        ok = wait_bar_warp(bar(C::B_FULL + st), (it / C::NST) & 1, ab);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t sa = sb0 + st * C::STAGE, sbb = sa + C::A_BYTES;
+        const uint64_t da = kAMN ? smem_desc(sa, C::MN_BOX, 1024, kSwizzle128B) : smem_desc(sa, 16, 1024, kSwizzle128B);
+        const uint64_t db =
+            kBMN ? smem_desc(sbb, C::MN_BOX, 1024, kSwizzle128B) : smem_desc(sbb, 16, 1024, kSwizzle128B);
+#pragma unroll
+        for (int ks = 0; ks < C::BK / 16; ++ks)
+          mma_ss_e(dacc, da + a_step * ks, db + b_step * ks, idesc, (kb > 0 || ks > 0) ? 1u : 0u);
+        mma_commit_e(bar(C::B_EMPTY + st));
+      }
+      if (!ok) break;
+      mma_commit_e(bar(C::B_ACCF + acc));
+    }
+    mma_commit_e(bar(C::B_DONE));
+    if (lane == 0) drain_bar(bar(C::B_DONE), 0);
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue: TMEM -> registers -> global
+    // Per 32 x 32 chunk the TMEM rows go through the warp's staging tile, so that each thread then
+    // holds 8 consecutive values of four rows (whole 16-byte or 32-byte stores).
+    const int q = warp & 3;
+    const int cbase = ((warp - 2) >> 2) * (32 * C::EPI_CPW);
+    const uint32_t lrow = (uint32_t)(q * 32) << 16;
+    float *stg = reinterpret_cast<float *>(sm + C::OFF_EPI + (warp - 2) * C::EPI_TILE);
+    const int rq = lane >> 2, cq = lane & 3;
+    int tl = 0;
+    for (int u = blockIdx.x; u < ntiles; u += gridDim.x, ++tl) {
+      int t, m0, n0;
+      tile_of(u, t, m0, n0);
+      const int acc = tl & 1;
+      if (!wait_bar_warp(bar(C::B_ACCF + acc), (tl >> 1) & 1, ab)) break;
+      tc_fence_after();
+      const int mrow = m0 + q * 32 + rq;
+#pragma unroll 1
+      for (int k = 0; k < C::EPI_CPW; ++k) {
+        const int c0 = cbase + 32 * k, n = n0 + c0;
+        if (n >= a.N) break;  // uniform across the warp
+        uint32_t r[32];
+        tmem_ld32(tb + lrow + acc * C::BN + c0, r);
+        tmem_wait_ld(r);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) stg[lane * C::EPI_PITCH + j] = __uint_as_float(r[j]);
+        __syncwarp();
+        const int col = n + 8 * cq;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float v[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v[j] = stg[(rq + 8 * i) * C::EPI_PITCH + 8 * cq + j];
+          if (mrow + 8 * i < a.M && col < a.N) mgemm_store8<kOut>(a, t, mrow + 8 * i, col, v);
+        }
+        __syncwarp();
+      }
+      tc_fence_before();
+      mbar_arrive(bar(C::B_ACCE + acc));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tb, C::TMEM_COLS);
+  }
+}
+
+// 2-D TMA view (inner, outer) of a BF16 row-major matrix with `pitch` elements per row, as a 3-D
+// map with one batch; one box is 64 inner elements (128 bytes, 128-byte swizzled) x `rows`.
+// Elements past the extents read as zeros.
+cudaError_t make_mat_map(CUtensorMap *m, const void *ptr, int64_t inner, int64_t outer, int64_t pitch, int rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)outer, 1};
+  cuuint64_t strides[2] = {(cuuint64_t)(2 * pitch), (cuuint64_t)(2 * pitch * outer)};
+  cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// One planned product. A(m, k): K-major A is row-major [M][K] (split along K into the given
+// tensors of segA columns each), MN-major A is row-major [K][M] (split along M into tensors of
+// segA columns each); B(n, k): K-major [N][K] or MN-major [K][N].
+template <bool kAMN, bool kBMN, int kOut>
+struct MGemm {
+  CUtensorMap mA[4], mB;
+  MGemmArgs a;
+  int grid;
+  cudaError_t plan(const uint16_t *const *A, int nA, int segA, const uint16_t *B, int M, int N, int K, int Kc) {
+    using C = MGemmCfg;
+    cudaError_t e = cudaSuccess;
+    for (int s = 0; s < 4 && e == cudaSuccess; ++s) {
+      const uint16_t *p = A[s < nA ? s : 0];
+      e = kAMN ? make_mat_map(&mA[s], p, segA, K, segA, C::BK) : make_mat_map(&mA[s], p, segA, M, segA, C::BM);
+    }
+    if (e == cudaSuccess) e = kBMN ? make_mat_map(&mB, B, N, K, N, C::BK) : make_mat_map(&mB, B, K, N, K, C::BN);
+    if (e != cudaSuccess) return e;
+    int dev = 0, nsm = 0;
+    e = current_device(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    static DeviceOnce ready;
+    if (!ready.done(dev)) {
+      e = cudaFuncSetAttribute(mod_gemm_kernel<kAMN, kBMN, kOut>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               C::SMEM_ALLOC);
+      if (e != cudaSuccess) return e;
+      ready.mark(dev);
+    }
+    a = MGemmArgs{};
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.Kc = Kc;
+    a.T = (K + Kc - 1) / Kc;
+    a.segA = segA;
+    a.nsegA = nA;
+    const int64_t tiles = (int64_t)a.T * ((M + C::BM - 1) / C::BM) * ((N + C::BN - 1) / C::BN);
+    grid = (int)std::min<int64_t>(tiles, nsm);
+    return cudaSuccess;
+  }
+  cudaError_t launch(const MGemmArgs &io, int *status, cudaStream_t st) const {
+    MGemmArgs x = a;
+    x.D0 = io.D0;
+    x.D1 = io.D1;
+    x.D2 = io.D2;
+    x.D3 = io.D3;
+    x.segD = io.segD;
+    x.P = io.P;
+    x.G = io.G;
+    x.dP = io.dP;
+    x.dG = io.dG;
+    mod_gemm_kernel<kAMN, kBMN, kOut>
+        <<<grid, MGemmCfg::NTHREADS, MGemmCfg::SMEM_ALLOC, st>>>(mA[0], mA[1], mA[2], mA[3], mB, x, status);
+    return cudaGetLastError();
+  }
+};
+
+MGemmArgs out_bf16(void *d0, void *d1, void *d2, void *d3, int seg) {
+  MGemmArgs o{};
+  o.D0 = d0;
+  o.D1 = d1;
+  o.D2 = d2;
+  o.D3 = d3;
+  o.segD = seg;
+  return o;
+}
+
+// ================================================================ LayerNorm and pair bias
+// One warp per pair position, CC / 32 consecutive channels per lane; sums over the channels by a
+// fixed xor-shuffle tree. The bias of head h is the dot product of the BF16-rounded zt row (the
+// values the projections read) with wb[h], written by lane h.
+template <int CC>
+__global__ void __launch_bounds__(256) mod_ln_fwd_kernel(const uint16_t *__restrict__ z, const float *__restrict__ gamma,
+                                                         const float *__restrict__ beta, const uint16_t *__restrict__ wb,
+                                                         int H, int N, int node, float eps, int64_t M,
+                                                         uint16_t *__restrict__ zt, float *__restrict__ mu,
+                                                         float *__restrict__ rstd, uint16_t *__restrict__ bias) {
+  constexpr int CPL = CC / 32;
+  const int lane = threadIdx.x & 31;
+  const int64_t w0 = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5), ws = (int64_t)gridDim.x * 8;
+  float gm[CPL], bt[CPL], wv[8][CPL];
+#pragma unroll
+  for (int j = 0; j < CPL; ++j) {
+    gm[j] = gamma[lane * CPL + j];
+    bt[j] = beta[lane * CPL + j];
+  }
+#pragma unroll
+  for (int h = 0; h < 8; ++h)
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) wv[h][j] = h < H ? __uint_as_float((uint32_t)wb[h * CC + lane * CPL + j] << 16) : 0.f;
+  const int64_t NN = (int64_t)N * N;
+  for (int64_t m = w0; m < M; m += ws) {
+    float x[CPL];
+    const uint16_t *src = z + m * CC + lane * CPL;
+    if constexpr (CPL == 2) {
+      const uint32_t w = *reinterpret_cast<const uint32_t *>(src);
+      x[0] = lo_bf(w);
+      x[1] = hi_bf(w);
+    } else if constexpr (CPL == 4) {
+      const uint2 w = *reinterpret_cast<const uint2 *>(src);
+      x[0] = lo_bf(w.x), x[1] = hi_bf(w.x), x[2] = lo_bf(w.y), x[3] = hi_bf(w.y);
+    } else {
+      const uint4 w = *reinterpret_cast<const uint4 *>(src);
+      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) x[2 * j] = lo_bf(ww[j]), x[2 * j + 1] = hi_bf(ww[j]);
+    }
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) s += x[j];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    const float mean = s * (1.f / CC);
+    float q = 0.f;
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) q = fmaf(x[j] - mean, x[j] - mean, q);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+    const float r = 1.f / sqrtf(q * (1.f / CC) + eps);
+    uint32_t yw[CPL / 2];
+    float y[CPL];
+#pragma unroll
+    for (int j = 0; j < CPL / 2; ++j) {
+      yw[j] = pack_bf16x2(fmaf((x[2 * j] - mean) * r, gm[2 * j], bt[2 * j]),
+                          fmaf((x[2 * j + 1] - mean) * r, gm[2 * j + 1], bt[2 * j + 1]));
+      y[2 * j] = lo_bf(yw[j]);
+      y[2 * j + 1] = hi_bf(yw[j]);
+    }
+    uint16_t *dst = zt + m * CC + lane * CPL;
+    if constexpr (CPL == 2) {
+      *reinterpret_cast<uint32_t *>(dst) = yw[0];
+    } else if constexpr (CPL == 4) {
+      *reinterpret_cast<uint2 *>(dst) = make_uint2(yw[0], yw[1]);
+    } else {
+      *reinterpret_cast<uint4 *>(dst) = make_uint4(yw[0], yw[1], yw[2], yw[3]);
+    }
+    if (lane == 0) {
+      mu[m] = mean;
+      rstd[m] = r;
+    }
+    const int64_t b = m / NN, xy = m - b * NN;
+    const int px = (int)(xy / N), py = (int)(xy - (int64_t)px * N);
+    const int64_t boff = node == 0 ? (int64_t)px * N + py : (int64_t)py * N + px;
+#pragma unroll
+    for (int h = 0; h < 8; ++h) {
+      if (h >= H) break;
+      float p = 0.f;
+#pragma unroll
+      for (int j = 0; j < CPL; ++j) p = fmaf(y[j], wv[h][j], p);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
+      if (lane == h) bias[(b * H + h) * NN + boff] = (uint16_t)(pack_bf16x2(p, 0.f) & 0xffffu);
+    }
+  }
+}
+
+// ================================================================ gate: go = sigmoid(gl) O
+__global__ void __launch_bounds__(256) mod_gate_kernel(const uint16_t *__restrict__ gl, const uint16_t *__restrict__ O,
+                                                       uint16_t *__restrict__ go, int64_t chunks) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < chunks; i += (int64_t)gridDim.x * blockDim.x) {
+    const uint4 g = reinterpret_cast<const uint4 *>(gl)[i], o = reinterpret_cast<const uint4 *>(O)[i];
+    const uint32_t gw[4] = {g.x, g.y, g.z, g.w}, ow[4] = {o.x, o.y, o.z, o.w};
+    uint32_t r[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      r[j] = pack_bf16x2(sigm(lo_bf(gw[j])) * lo_bf(ow[j]), sigm(hi_bf(gw[j])) * hi_bf(ow[j]));
+    reinterpret_cast<uint4 *>(go)[i] = make_uint4(r[0], r[1], r[2], r[3]);
+  }
+}
+
+// ================================================================ LayerNorm backward
+// One CTA per fixed chunk of `rpc` pair positions (one warp per position, positions strided over
+// the eight warps). g = dzt + sum_h dbias_h wb[h] is the full gradient of zt; with zh = (z - mean)
+// rstd and dzh = g gamma, dz = rstd (dzh - mean(dzh) - zh mean(dzh zh)). The CTA's partial sums of
+// dgamma (g zh), dbeta (g) and dwb[h] (dbias_h zt) are added over its warps in warp order and
+// written to part[blockIdx.x][2 + H][CC].
+template <int CC>
+__global__ void __launch_bounds__(256) mod_ln_bwd_kernel(const float *__restrict__ dzt, const uint16_t *__restrict__ dbias,
+                                                         const uint16_t *__restrict__ z, const uint16_t *__restrict__ zt,
+                                                         const float *__restrict__ mu, const float *__restrict__ rstd,
+                                                         const float *__restrict__ gamma, const uint16_t *__restrict__ wb,
+                                                         int H, int N, int node, int64_t M, int rpc,
+                                                         uint16_t *__restrict__ dz, float *__restrict__ part) {
+  constexpr int CPL = CC / 32;
+  __shared__ float red[10 * CC];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float gm[CPL], wv[8][CPL];
+#pragma unroll
+  for (int j = 0; j < CPL; ++j) gm[j] = gamma[lane * CPL + j];
+#pragma unroll
+  for (int h = 0; h < 8; ++h)
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) wv[h][j] = h < H ? __uint_as_float((uint32_t)wb[h * CC + lane * CPL + j] << 16) : 0.f;
+  float ag[CPL], ab[CPL], aw[8][CPL];
+#pragma unroll
+  for (int j = 0; j < CPL; ++j) {
+    ag[j] = 0.f;
+    ab[j] = 0.f;
+#pragma unroll
+    for (int h = 0; h < 8; ++h) aw[h][j] = 0.f;
+  }
+  const int64_t NN = (int64_t)N * N;
+  const int64_t r0 = (int64_t)blockIdx.x * rpc, r1 = min(M, r0 + rpc);
+  auto ld_bf = [](const uint16_t *src, float (&v)[CPL]) {
+    if constexpr (CPL == 2) {
+      const uint32_t w = *reinterpret_cast<const uint32_t *>(src);
+      v[0] = lo_bf(w), v[1] = hi_bf(w);
+    } else if constexpr (CPL == 4) {
+      const uint2 w = *reinterpret_cast<const uint2 *>(src);
+      v[0] = lo_bf(w.x), v[1] = hi_bf(w.x), v[2] = lo_bf(w.y), v[3] = hi_bf(w.y);
+    } else {
+      const uint4 w = *reinterpret_cast<const uint4 *>(src);
+      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[2 * j] = lo_bf(ww[j]), v[2 * j + 1] = hi_bf(ww[j]);
+    }
+  };
+  for (int64_t m = r0 + warp; m < r1; m += 8) {
+    const int64_t b = m / NN, xy = m - b * NN;
+    const int px = (int)(xy / N), py = (int)(xy - (int64_t)px * N);
+    const int64_t boff = node == 0 ? (int64_t)px * N + py : (int64_t)py * N + px;
+    float db[8];
+#pragma unroll
+    for (int h = 0; h < 8; ++h) db[h] = h < H ? __uint_as_float((uint32_t)dbias[(b * H + h) * NN + boff] << 16) : 0.f;
+    float g[CPL], zv[CPL], tv[CPL];
+    const float *gs = dzt + m * CC + lane * CPL;
+#pragma unroll
+    for (int j = 0; j < CPL; j += 2) {
+      const float2 t = *reinterpret_cast<const float2 *>(gs + j);
+      g[j] = t.x;
+      g[j + 1] = t.y;
+    }
+#pragma unroll
+    for (int h = 0; h < 8; ++h)
+#pragma unroll
+      for (int j = 0; j < CPL; ++j) g[j] = fmaf(db[h], wv[h][j], g[j]);
+    ld_bf(z + m * CC + lane * CPL, zv);
+    ld_bf(zt + m * CC + lane * CPL, tv);
+    const float mean = mu[m], r = rstd[m];
+    float zh[CPL], dzh[CPL], s1 = 0.f, s2 = 0.f;
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) {
+      zh[j] = (zv[j] - mean) * r;
+      dzh[j] = g[j] * gm[j];
+      s1 += dzh[j];
+      s2 = fmaf(dzh[j], zh[j], s2);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+      s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+    }
+    s1 *= (1.f / CC);
+    s2 *= (1.f / CC);
+    uint32_t ow[CPL / 2];
+#pragma unroll
+    for (int j = 0; j < CPL / 2; ++j)
+      ow[j] = pack_bf16x2(r * (dzh[2 * j] - s1 - zh[2 * j] * s2), r * (dzh[2 * j + 1] - s1 - zh[2 * j + 1] * s2));
+    uint16_t *dst = dz + m * CC + lane * CPL;
+    if constexpr (CPL == 2) {
+      *reinterpret_cast<uint32_t *>(dst) = ow[0];
+    } else if constexpr (CPL == 4) {
+      *reinterpret_cast<uint2 *>(dst) = make_uint2(ow[0], ow[1]);
+    } else {
+      *reinterpret_cast<uint4 *>(dst) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+    }
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) {
+      ag[j] = fmaf(g[j], zh[j], ag[j]);
+      ab[j] += g[j];
+#pragma unroll
+      for (int h = 0; h < 8; ++h) aw[h][j] = fmaf(db[h], tv[j], aw[h][j]);
+    }
+  }
+  // the CTA's partial: warps added in warp order
+  const int nrow = 2 + H;
+  for (int w = 0; w < 8; ++w) {
+    if (warp == w) {
+#pragma unroll
+      for (int j = 0; j < CPL; ++j) {
+        const int c = lane * CPL + j;
+        red[c] = w ? red[c] + ag[j] : ag[j];
+        red[CC + c] = w ? red[CC + c] + ab[j] : ab[j];
+#pragma unroll
+        for (int h = 0; h < 8; ++h)
+          if (h < H) red[(2 + h) * CC + c] = w ? red[(2 + h) * CC + c] + aw[h][j] : aw[h][j];
+      }
+    }
+    __syncthreads();
+  }
+  for (int i = threadIdx.x; i < nrow * CC; i += blockDim.x) part[(int64_t)blockIdx.x * nrow * CC + i] = red[i];
+}
+
+// ================================================================ ordered sum of partials
+// out[i] = sum over t = 0, 1, ..., T - 1 of part[t][i] (in that order), for i < n; the result is
+// written in up to three pieces: i < n0 to o0, i < n0 + n1 to o1, the rest to o2.
+__global__ void __launch_bounds__(256) mod_reduce_kernel(const float *__restrict__ part, int T, int64_t n, float *o0,
+                                                         int64_t n0, float *o1, int64_t n1, float *o2) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    float s = 0.f;
+    for (int t = 0; t < T; ++t) s += part[(int64_t)t * n + i];
+    if (i < n0)
+      o0[i] = s;
+    else if (i < n0 + n1)
+      o1[i - n0] = s;
+    else
+      o2[i - n0 - n1] = s;
+  }
+}
+
+// ================================================================ host side
+constexpr size_t kAlign = 256;
+size_t aup(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_shape(const tri_module_shape &s) {
+  if (s.B < 1 || s.N < 1 || s.c < 1 || s.H < 1 || s.d < 1 || !(s.eps > 0.f) || !isfinite(s.eps) ||
+      (s.node != TRI_ATTN_NODE_STARTING && s.node != TRI_ATTN_NODE_ENDING))
+    return TRI_ATTN_ERR_INVALID_ARG;
+  if ((s.c != 64 && s.c != 128 && s.c != 256) || (s.d != 16 && s.d != 32) || s.H > 8 || (s.H * s.d) % 64 ||
+      s.N < 16 || s.N > TRI_ATTN_MAX_N || (int64_t)s.B * s.N > 65535)
+    return TRI_ATTN_ERR_UNSUPPORTED;
+  return TRI_ATTN_OK;
+}
+
+tri_attn_shape attn_shape(const tri_module_shape &s) {
+  return tri_attn_shape{s.B, s.N, s.N, s.H, s.d, 1.f / sqrtf((float)s.d), s.node};
+}
+
+int64_t rows_of(const tri_module_shape &s) { return (int64_t)s.B * s.N * s.N; }
+
+// Fixed chunks of pair positions for the sums over positions: about 144 chunks of a multiple of
+// 64 rows (the GEMM's K step), chosen from the shape alone.
+int split_rows(int64_t M) { return (int)std::max<int64_t>(64, ((M + 143) / 144 + 63) / 64 * 64); }
+int ln_rows(int64_t M) { return (int)std::max<int64_t>(8, ((M + 295) / 296 + 7) / 8 * 8); }
+
+struct SavedLayout {
+  size_t zt, mu, rstd, q, k, v, gl, bias, O, Ores, LSE, go, total;
+};
+
+SavedLayout saved_layout(const tri_module_shape &s) {
+  const size_t M = (size_t)rows_of(s), hd = (size_t)s.H * s.d;
+  const size_t act = aup(2 * M * hd);
+  SavedLayout L;
+  L.zt = 0;
+  L.mu = aup(2 * M * s.c);
+  L.rstd = L.mu + aup(4 * M);
+  L.q = L.rstd + aup(4 * M);
+  L.k = L.q + act;
+  L.v = L.k + act;
+  L.gl = L.v + act;
+  L.bias = L.gl + act;
+  L.O = L.bias + aup(2 * (size_t)s.B * s.H * s.N * s.N);
+  L.Ores = L.O + act;
+  L.LSE = L.Ores + act;
+  L.go = L.LSE + aup(4 * (size_t)s.B * s.N * s.H * s.N);
+  L.total = L.go + act;
+  return L;
+}
+
+struct BwdLayout {
+  size_t dO, dgl, dq, dk, dv, dbias, dzt, attn, pWo, pW, pLN, total;
+  size_t attn_bytes;
+  int Kc, Tsplit, rpc, nln;
+};
+
+BwdLayout bwd_layout(const tri_module_shape &s) {
+  const size_t M = (size_t)rows_of(s), hd = (size_t)s.H * s.d;
+  const size_t act = aup(2 * M * hd);
+  BwdLayout L;
+  L.Kc = split_rows((int64_t)M);
+  L.Tsplit = (int)((M + L.Kc - 1) / L.Kc);
+  L.rpc = ln_rows((int64_t)M);
+  L.nln = (int)((M + L.rpc - 1) / L.rpc);
+  L.attn_bytes = tri_attn_bwd_workspace_size(attn_shape(s));
+  L.dO = 0;
+  L.dgl = act;
+  L.dq = 2 * act;
+  L.dk = 3 * act;
+  L.dv = 4 * act;
+  L.dbias = 5 * act;
+  L.dzt = L.dbias + aup(2 * (size_t)s.B * s.H * s.N * s.N);
+  L.attn = L.dzt + aup(4 * M * s.c);
+  L.pWo = L.attn + aup(L.attn_bytes);
+  L.pW = L.pWo + aup(4 * (size_t)L.Tsplit * s.c * hd);
+  L.pLN = L.pW + aup(4 * (size_t)L.Tsplit * 4 * hd * s.c);
+  L.total = L.pLN + aup(4 * (size_t)L.nln * (2 + s.H) * s.c);
+  return L;
+}
+
+template <typename T>
+T *at(void *base, size_t off) {
+  return reinterpret_cast<T *>(static_cast<char *>(base) + off);
+}
+
+cudaError_t launch_ln_fwd(const tri_module_shape &s, const uint16_t *z, const float *gamma, const float *beta,
+                          const uint16_t *wb, uint16_t *zt, float *mu, float *rstd, uint16_t *bias, cudaStream_t st) {
+  const int64_t M = rows_of(s);
+  const int grid = (int)std::min<int64_t>((M + 7) / 8, 152 * 16);
+  switch (s.c) {
+    case 64: mod_ln_fwd_kernel<64><<<grid, 256, 0, st>>>(z, gamma, beta, wb, s.H, s.N, s.node, s.eps, M, zt, mu, rstd, bias); break;
+    case 128: mod_ln_fwd_kernel<128><<<grid, 256, 0, st>>>(z, gamma, beta, wb, s.H, s.N, s.node, s.eps, M, zt, mu, rstd, bias); break;
+    default: mod_ln_fwd_kernel<256><<<grid, 256, 0, st>>>(z, gamma, beta, wb, s.H, s.N, s.node, s.eps, M, zt, mu, rstd, bias); break;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ln_bwd(const tri_module_shape &s, const BwdLayout &L, const float *dzt, const uint16_t *dbias,
+                          const uint16_t *z, const uint16_t *zt, const float *mu, const float *rstd, const float *gamma,
+                          const uint16_t *wb, uint16_t *dz, float *part, cudaStream_t st) {
+  const int64_t M = rows_of(s);
+  switch (s.c) {
+    case 64: mod_ln_bwd_kernel<64><<<L.nln, 256, 0, st>>>(dzt, dbias, z, zt, mu, rstd, gamma, wb, s.H, s.N, s.node, M, L.rpc, dz, part); break;
+    case 128: mod_ln_bwd_kernel<128><<<L.nln, 256, 0, st>>>(dzt, dbias, z, zt, mu, rstd, gamma, wb, s.H, s.N, s.node, M, L.rpc, dz, part); break;
+    default: mod_ln_bwd_kernel<256><<<L.nln, 256, 0, st>>>(dzt, dbias, z, zt, mu, rstd, gamma, wb, s.H, s.N, s.node, M, L.rpc, dz, part); break;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reduce(const float *part, int T, int64_t n, float *o0, int64_t n0, float *o1, int64_t n1, float *o2,
+                          cudaStream_t st) {
+  const int grid = (int)std::min<int64_t>((n + 255) / 256, 152 * 8);
+  mod_reduce_kernel<<<grid, 256, 0, st>>>(part, T, n, o0, n0, o1 ? o1 : o0, n1, o2 ? o2 : o0);
+  return cudaGetLastError();
+}
+
+cudaError_t mark_ok(cudaError_t e, int k, cudaStream_t st) { return e == cudaSuccess ? timing_mark(k, st) : e; }
+
+}  // namespace
+}  // namespace triattn
+
+using namespace triattn;
+
+extern "C" {
+
+size_t tri_module_saved_size(tri_module_shape shape) {
+  if (check_shape(shape)) return 0;
+  return saved_layout(shape).total;
+}
+
+size_t tri_module_bwd_workspace_size(tri_module_shape shape) {
+  if (check_shape(shape)) return 0;
+  const BwdLayout L = bwd_layout(shape);
+  return L.attn_bytes ? L.total : 0;
+}
+
+int tri_module_fwd(tri_module_shape shape, const tri_attn_bf16 *z, const float *gamma, const float *beta,
+                   const tri_attn_bf16 *W, const tri_attn_bf16 *wb, const tri_attn_bf16 *Wo,
+                   const tri_attn_bf16 *mask, tri_attn_bf16 *out, void *saved, size_t saved_bytes, void *stream) {
+  int rc = check_shape(shape);
+  if (rc) return rc;
+  const void *ptrs[] = {z, gamma, beta, W, wb, Wo, out, saved};
+  for (const void *p : ptrs) {
+    if (!p) return TRI_ATTN_ERR_INVALID_ARG;
+    if (!aligned16(p)) return TRI_ATTN_ERR_UNSUPPORTED;
+  }
+  if (mask && !aligned16(mask)) return TRI_ATTN_ERR_UNSUPPORTED;
+  const SavedLayout L = saved_layout(shape);
+  if (saved_bytes < L.total) return TRI_ATTN_ERR_WORKSPACE;
+  const int64_t M = rows_of(shape);
+  const int hd = shape.H * shape.d, c = shape.c;
+  uint16_t *zt = at<uint16_t>(saved, L.zt), *q = at<uint16_t>(saved, L.q), *k = at<uint16_t>(saved, L.k),
+           *v = at<uint16_t>(saved, L.v), *gl = at<uint16_t>(saved, L.gl), *bias = at<uint16_t>(saved, L.bias),
+           *O = at<uint16_t>(saved, L.O), *Ores = at<uint16_t>(saved, L.Ores), *go = at<uint16_t>(saved, L.go);
+  float *mu = at<float>(saved, L.mu), *rstd = at<float>(saved, L.rstd), *LSE = at<float>(saved, L.LSE);
+  int *status = device_status_word();
+  if (!status) return TRI_ATTN_ERR_CUDA;
+  // every plan before the first launch
+  MGemm<false, false, kOutBF16> g_in, g_out;
+  const uint16_t *a_in[1] = {zt}, *a_out[1] = {go};
+  if (g_in.plan(a_in, 1, c, W, (int)M, 4 * hd, c, c) != cudaSuccess ||
+      g_out.plan(a_out, 1, hd, Wo, (int)M, c, hd, hd) != cudaSuccess)
+    return TRI_ATTN_ERR_CUDA;
+  AttnFwdCall ac;
+  rc = attn_fwd_prepare(attn_shape(shape), q, k, v, bias, mask, O, LSE, Ores, &ac);
+  if (rc) return rc;
+  auto st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_ln_fwd(shape, z, gamma, beta, wb, zt, mu, rstd, bias, st);
+  e = mark_ok(e, 0, st);
+  if (e == cudaSuccess) e = g_in.launch(out_bf16(q, k, v, gl, hd), status, st);
+  e = mark_ok(e, 1, st);
+  if (e == cudaSuccess) e = attn_fwd_enqueue(ac, 2, st);
+  if (e == cudaSuccess) {
+    const int64_t chunks = M * hd / 8;
+    mod_gate_kernel<<<(int)std::min<int64_t>((chunks + 255) / 256, 152 * 8), 256, 0, st>>>(gl, O, go, chunks);
+    e = cudaGetLastError();
+  }
+  e = mark_ok(e, 4, st);
+  if (e == cudaSuccess) e = g_out.launch(out_bf16(out, nullptr, nullptr, nullptr, c), status, st);
+  e = mark_ok(e, 5, st);
+  return e == cudaSuccess ? TRI_ATTN_OK : TRI_ATTN_ERR_CUDA;
+}
+
+int tri_module_bwd(tri_module_shape shape, const tri_attn_bf16 *z, const float *gamma, const float *beta,
+                   const tri_attn_bf16 *W, const tri_attn_bf16 *wb, const tri_attn_bf16 *Wo,
+                   const tri_attn_bf16 *mask, const void *saved, size_t saved_bytes, const tri_attn_bf16 *dout,
+                   tri_attn_bf16 *dz, float *dgamma, float *dbeta, float *dW, float *dwb, float *dWo,
+                   void *workspace, size_t workspace_bytes, void *stream) {
+  int rc = check_shape(shape);
+  if (rc) return rc;
+  const void *ptrs[] = {z, gamma, beta, W, wb, Wo, saved, dout, dz, dgamma, dbeta, dW, dwb, dWo, workspace};
+  for (const void *p : ptrs) {
+    if (!p) return p == workspace ? TRI_ATTN_ERR_WORKSPACE : TRI_ATTN_ERR_INVALID_ARG;
+    if (!aligned16(p)) return TRI_ATTN_ERR_UNSUPPORTED;
+  }
+  if (mask && !aligned16(mask)) return TRI_ATTN_ERR_UNSUPPORTED;
+  const SavedLayout S = saved_layout(shape);
+  if (saved_bytes < S.total) return TRI_ATTN_ERR_WORKSPACE;
+  const BwdLayout L = bwd_layout(shape);
+  if (!L.attn_bytes) return TRI_ATTN_ERR_CUDA;
+  if (workspace_bytes < L.total) return TRI_ATTN_ERR_WORKSPACE;
+  const int64_t M = rows_of(shape);
+  const int hd = shape.H * shape.d, c = shape.c, H = shape.H;
+  void *sv = const_cast<void *>(saved);
+  const uint16_t *zt = at<uint16_t>(sv, S.zt), *q = at<uint16_t>(sv, S.q), *k = at<uint16_t>(sv, S.k),
+                 *v = at<uint16_t>(sv, S.v), *gl = at<uint16_t>(sv, S.gl), *bias = at<uint16_t>(sv, S.bias),
+                 *O = at<uint16_t>(sv, S.O), *Ores = at<uint16_t>(sv, S.Ores), *go = at<uint16_t>(sv, S.go);
+  const float *mu = at<float>(sv, S.mu), *rstd = at<float>(sv, S.rstd), *LSE = at<float>(sv, S.LSE);
+  uint16_t *dO = at<uint16_t>(workspace, L.dO), *dgl = at<uint16_t>(workspace, L.dgl),
+           *dq = at<uint16_t>(workspace, L.dq), *dk = at<uint16_t>(workspace, L.dk), *dv = at<uint16_t>(workspace, L.dv),
+           *dbias = at<uint16_t>(workspace, L.dbias);
+  float *dzt = at<float>(workspace, L.dzt), *pWo = at<float>(workspace, L.pWo), *pW = at<float>(workspace, L.pW),
+        *pLN = at<float>(workspace, L.pLN);
+  int *status = device_status_word();
+  if (!status) return TRI_ATTN_ERR_CUDA;
+  // every plan before the first launch
+  MGemm<false, true, kOutGate> g_dgo;   // dgo[m][j] = sum_c dout[m][c] Wo[c][j]
+  MGemm<true, true, kOutF32> g_dwo;     // dWo[c][j] = sum_m dout[m][c] go[m][j]
+  MGemm<false, true, kOutF32> g_dzt;    // dzt[m][c] = sum_r dproj[m][r] W[r][c]
+  MGemm<true, true, kOutF32> g_dw;      // dW[r][c] = sum_m dproj[m][r] zt[m][c]
+  const uint16_t *a_dout[1] = {dout}, *a_proj[4] = {dq, dk, dv, dgl};
+  if (g_dgo.plan(a_dout, 1, c, Wo, (int)M, hd, c, c) != cudaSuccess ||
+      g_dwo.plan(a_dout, 1, c, go, c, hd, (int)M, L.Kc) != cudaSuccess ||
+      g_dzt.plan(a_proj, 4, hd, W, (int)M, c, 4 * hd, 4 * hd) != cudaSuccess ||
+      g_dw.plan(a_proj, 4, hd, zt, 4 * hd, c, (int)M, L.Kc) != cudaSuccess)
+    return TRI_ATTN_ERR_CUDA;
+  AttnBwdCall ac;
+  rc = attn_bwd_prepare(attn_shape(shape), q, k, v, bias, mask, O, Ores, LSE, dO, dq, dk, dv, dbias,
+                        at<void>(workspace, L.attn), L.attn_bytes, &ac);
+  if (rc) return rc;
+  auto st = static_cast<cudaStream_t>(stream);
+  MGemmArgs gate{};
+  gate.P = O;
+  gate.G = gl;
+  gate.dP = dO;
+  gate.dG = dgl;
+  cudaError_t e = g_dgo.launch(gate, status, st);
+  e = mark_ok(e, 0, st);
+  MGemmArgs f32{};
+  f32.D0 = pWo;
+  if (e == cudaSuccess) e = g_dwo.launch(f32, status, st);
+  e = mark_ok(e, 1, st);
+  if (e == cudaSuccess) e = launch_reduce(pWo, L.Tsplit, (int64_t)c * hd, dWo, (int64_t)c * hd, nullptr, 0, nullptr, st);
+  e = mark_ok(e, 2, st);
+  if (e == cudaSuccess) e = attn_bwd_enqueue(ac, 3, st);
+  f32.D0 = dzt;
+  if (e == cudaSuccess) e = g_dzt.launch(f32, status, st);
+  e = mark_ok(e, 7, st);
+  if (e == cudaSuccess) e = launch_ln_bwd(shape, L, dzt, dbias, z, zt, mu, rstd, gamma, wb, dz, pLN, st);
+  e = mark_ok(e, 8, st);
+  if (e == cudaSuccess) e = launch_reduce(pLN, L.nln, (int64_t)(2 + H) * c, dgamma, c, dbeta, c, dwb, st);
+  e = mark_ok(e, 9, st);
+  f32.D0 = pW;
+  if (e == cudaSuccess) e = g_dw.launch(f32, status, st);
+  e = mark_ok(e, 10, st);
+  if (e == cudaSuccess)
+    e = launch_reduce(pW, L.Tsplit, (int64_t)4 * hd * c, dW, (int64_t)4 * hd * c, nullptr, 0, nullptr, st);
+  e = mark_ok(e, 11, st);
+  return e == cudaSuccess ? TRI_ATTN_OK : TRI_ATTN_ERR_CUDA;
+}
+
+}  // extern "C"

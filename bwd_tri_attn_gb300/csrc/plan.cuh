@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include "common.cuh"
+#include "tri_attn.h"
 
 namespace triattn {
 
@@ -40,6 +41,39 @@ cudaError_t launch_bwd_main(const Dims &g, const BwdPlan &p, const float *LSE, c
                             int *status, cudaStream_t stream);
 cudaError_t launch_dbias_reduce_t(const Dims &g, const BwdSplit &sp, const float *partial, uint16_t *dBias,
                                   cudaStream_t stream);
+
+// A checked and planned attention call, ready to enqueue (entry points of other files, such as
+// the surrounding block, prepare every call before they launch anything).
+struct AttnFwdCall {
+  Dims g;
+  FwdPlan plan;
+  const uint16_t *V, *bias, *mask;
+  uint16_t *O, *Ores;
+  float *LSE;
+  int *status;
+};
+
+struct AttnBwdCall {
+  Dims g;
+  BwdSplit sp;
+  BwdPlan plan;
+  const uint16_t *Q, *K, *V, *bias, *mask, *O, *Ores, *dO;
+  const float *LSE;
+  uint16_t *dQ, *dK, *dV, *dBias, *biasT;
+  float *Dv, *partial;
+  int *emax, *status;
+};
+
+int attn_fwd_prepare(const tri_attn_shape &shape, const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                     const uint16_t *bias, const uint16_t *mask, uint16_t *O, float *LSE, uint16_t *Ores,
+                     AttnFwdCall *c);
+cudaError_t attn_fwd_enqueue(const AttnFwdCall &c, int mark0, cudaStream_t st);
+int attn_bwd_prepare(const tri_attn_shape &shape, const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                     const uint16_t *bias, const uint16_t *mask, const uint16_t *O, const uint16_t *Ores,
+                     const float *LSE, const uint16_t *dO, uint16_t *dQ, uint16_t *dK, uint16_t *dV,
+                     uint16_t *dBias, void *workspace, size_t workspace_bytes, AttnBwdCall *c);
+cudaError_t attn_bwd_enqueue(const AttnBwdCall &c, int mark0, cudaStream_t st);
+cudaError_t timing_mark(int k, cudaStream_t st);
 
 cudaError_t device_sm_count(int *nsm);
 cudaError_t bwd_split_active(const Dims &g, BwdSplit *sp);

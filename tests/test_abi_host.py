@@ -26,7 +26,7 @@ def _declared_functions():
     for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
         text = open(h).read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-        for m in re.finditer(r"\b(?:int|size_t|const char\s*\*|void)\s*\*?\s*(tri_(?:attn|mul)_\w+)\s*\(", text):
+        for m in re.finditer(r"\b(?:int|size_t|const char\s*\*|void)\s*\*?\s*(tri_(?:attn|mul|module)_\w+)\s*\(", text):
             names.add(m.group(1))
     return sorted(names)
 
@@ -40,7 +40,8 @@ def test_every_declared_symbol_is_exported(lib):
     names = _declared_functions()
     assert {"tri_attn_fwd", "tri_attn_bwd", "tri_attn_bwd_workspace_size", "tri_attn_strerror",
             "tri_attn_device_status", "tri_attn_set_timing_events", "tri_attn_bwd_split",
-            "tri_attn_bwd_static", "tri_mul_fwd", "tri_mul_bwd", "tri_mul_bwd_workspace_size"} <= set(names)
+            "tri_attn_bwd_static", "tri_mul_fwd", "tri_mul_bwd", "tri_mul_bwd_workspace_size", "tri_module_fwd",
+            "tri_module_bwd", "tri_module_saved_size", "tri_module_bwd_workspace_size"} <= set(names)
     for n in names:
         assert hasattr(lib, n), f"{n} declared in include/ but not exported"
 
@@ -222,3 +223,79 @@ def test_mul_workspace_checks(lib):
     assert _mul_bwd(lib, MUL_GOOD, need - 1) == -3
     assert _mul_bwd(lib, MUL_GOOD, need, ws=0) == -3
     assert _mul_bwd(lib, MUL_GOOD, need, ws=FAKE + 8) == -2
+
+
+# ---------------------------------------------------------------- triangle-attention block entry points
+MOD_GOOD = (1, 64, 128, 4, 32, 0, 1e-5)
+
+
+def _mod_saved(lib, shape):
+    from bwd_tri_attn_gb300.binding import ModuleShape
+    return lib.tri_module_saved_size(ModuleShape(*shape))
+
+
+def _mod_fwd(lib, shape, saved_bytes, **ptrs):
+    from bwd_tri_attn_gb300.binding import ModuleShape
+    names = ["z", "gamma", "beta", "W", "wb", "Wo", "mask", "out", "saved"]
+    args = [ctypes.c_void_p(ptrs.get(n, FAKE)) for n in names]
+    return lib.tri_module_fwd(ModuleShape(*shape), *args[:9], ctypes.c_size_t(saved_bytes), None)
+
+
+def _mod_bwd(lib, shape, saved_bytes, ws_bytes, **ptrs):
+    from bwd_tri_attn_gb300.binding import ModuleShape
+    pre = [ctypes.c_void_p(ptrs.get(n, FAKE)) for n in ["z", "gamma", "beta", "W", "wb", "Wo", "mask", "saved"]]
+    post = [ctypes.c_void_p(ptrs.get(n, FAKE)) for n in ["dout", "dz", "dgamma", "dbeta", "dW", "dwb", "dWo", "ws"]]
+    return lib.tri_module_bwd(ModuleShape(*shape), *pre, ctypes.c_size_t(saved_bytes), *post,
+                              ctypes.c_size_t(ws_bytes), None)
+
+
+@pytest.mark.parametrize("shape,code", [
+    ((0, 64, 128, 4, 32, 0, 1e-5), -1),     # empty batch
+    ((1, 64, 128, 0, 32, 0, 1e-5), -1),     # no heads
+    ((1, 64, 128, 4, 32, 2, 1e-5), -1),     # unknown node
+    ((1, 64, 128, 4, 32, 0, 0.0), -1),      # eps must be positive
+    ((1, 64, 128, 4, 32, 0, float("nan")), -1),
+    ((1, 64, 96, 4, 32, 0, 1e-5), -2),      # c not 64, 128 or 256
+    ((1, 64, 128, 4, 24, 0, 1e-5), -2),     # d not 16 or 32
+    ((1, 64, 128, 2, 16, 0, 1e-5), -2),     # H d not a multiple of 64
+    ((1, 64, 128, 16, 32, 0, 1e-5), -2),    # more than 8 heads
+    ((1, 8, 128, 4, 32, 0, 1e-5), -2),      # N below 16
+    ((1, 1032, 128, 4, 32, 0, 1e-5), -2),   # N above the attention's limit
+    ((128, 1024, 64, 4, 16, 0, 1e-5), -2),  # B N above the grid limit
+])
+def test_module_shape_validation(lib, shape, code):
+    assert _mod_saved(lib, shape) == 0
+    from bwd_tri_attn_gb300.binding import ModuleShape
+    assert lib.tri_module_bwd_workspace_size(ModuleShape(*shape)) == 0
+    assert _mod_fwd(lib, shape, 1 << 40) == code
+    assert _mod_bwd(lib, shape, 1 << 40, 1 << 40) == code
+
+
+@pytest.mark.parametrize("name", ["z", "gamma", "beta", "W", "wb", "Wo", "out", "saved"])
+def test_module_fwd_pointer_checks(lib, name):
+    assert _mod_fwd(lib, MOD_GOOD, 1 << 40, **{name: 0}) == -1
+    assert _mod_fwd(lib, MOD_GOOD, 1 << 40, **{name: FAKE + 2}) == -2
+
+
+@pytest.mark.parametrize("name", ["z", "gamma", "beta", "W", "wb", "Wo", "saved", "dout", "dz", "dgamma", "dbeta",
+                                  "dW", "dwb", "dWo"])
+def test_module_bwd_pointer_checks(lib, name):
+    assert _mod_bwd(lib, MOD_GOOD, 1 << 40, 1 << 40, **{name: 0}) == -1
+    assert _mod_bwd(lib, MOD_GOOD, 1 << 40, 1 << 40, **{name: FAKE + 2}) == -2
+
+
+def test_module_saved_and_workspace_checks(lib):
+    saved = _mod_saved(lib, MOD_GOOD)
+    # at least zt, q, k, v, gl, O, Ores and go (BF16) plus the statistics, bias and log-sum-exp
+    M, hd, c = 64 * 64, 128, 128
+    assert saved >= 2 * M * c + 7 * 2 * M * hd + 2 * 4 * M + 2 * 4 * 64 * 64 + 4 * 64 * 4 * 64
+    assert _mod_saved(lib, (1, 64, 128, 4, 32, 1, 1e-5)) == saved  # the node changes no size
+    assert _mod_fwd(lib, MOD_GOOD, saved - 1) == -3
+    assert _mod_bwd(lib, MOD_GOOD, saved - 1, 1 << 40) == -3
+    assert _mod_fwd(lib, MOD_GOOD, saved, mask=FAKE + 4) == -2  # the optional mask is still checked
+    assert _mod_bwd(lib, MOD_GOOD, saved, 1 << 40, ws=0) == -3
+    if _has_device():
+        from bwd_tri_attn_gb300.binding import ModuleShape
+        need = lib.tri_module_bwd_workspace_size(ModuleShape(*MOD_GOOD))
+        assert need > 0
+        assert _mod_bwd(lib, MOD_GOOD, saved, need - 1) == -3
