@@ -383,6 +383,124 @@ def run_trimul_only(args):
     print(json.dumps({"trimul": out}))
 
 
+MOD_KERNELS = ["mod_ln_fwd", "mod_proj_gemm", "fwd_vscale", "fwd", "mod_gate", "mod_out_gemm",
+               "mod_dgo_gemm", "mod_dwo_gemm", "mod_dwo_reduce", "bias_transpose", "bwd_prep", "bwd_main",
+               "dbias_reduce", "mod_dzt_gemm", "mod_ln_bwd", "mod_ln_reduce", "mod_dw_gemm", "mod_dw_reduce"]
+MOD_NFWD = 6
+
+
+def mod_roofline(kernel_ms, B, N, c, H, d, peaks):
+    """Per-kernel figures of the triangle-attention block's own kernels (the attention's are reported
+    by the main line). M = B N^2 pair positions, hd = H d; algorithmic bytes (each tensor read or
+    written once) and GEMM FLOPs:
+      LayerNorm forward: z in, zt out (2 M c each), mean and 1/std (8 M), pair bias (2 M H);
+      input projections: zt in (2 M c), q, k, v, gl out (8 M hd); 2 M c 4hd FLOPs;
+      gate: gl and O in, go out (6 M hd); output projection: go in (2 M hd), out (2 M c), 2 M hd c FLOPs;
+      dgo with the gate gradient: dout (2 M c), O and gl in, dO and dgl out (8 M hd), 2 M c hd FLOPs;
+      dWo partials: dout and go in (2 M c + 2 M hd), 2 M c hd FLOPs;
+      dzt: dq, dk, dv, dgl in (8 M hd), dzt out in FP32 (4 M c), 2 M 4hd c FLOPs;
+      LayerNorm backward: dzt (4 M c), z, zt (4 M c), statistics (8 M), dbias (2 M H) in, dz out (2 M c);
+      dW partials: dq, dk, dv, dgl and zt in (8 M hd + 2 M c), 2 M 4hd c FLOPs."""
+    M = B * N * N
+    hd = H * d
+    spec = {"mod_ln_fwd": (4 * M * c + 8 * M + 2 * M * H, 0),
+            "mod_proj_gemm": (2 * M * c + 8 * M * hd, 2.0 * M * c * 4 * hd),
+            "mod_gate": (6 * M * hd, 0),
+            "mod_out_gemm": (2 * M * hd + 2 * M * c, 2.0 * M * hd * c),
+            "mod_dgo_gemm": (2 * M * c + 8 * M * hd, 2.0 * M * c * hd),
+            "mod_dwo_gemm": (2 * M * c + 2 * M * hd, 2.0 * M * c * hd),
+            "mod_dzt_gemm": (8 * M * hd + 4 * M * c, 2.0 * M * 4 * hd * c),
+            "mod_ln_bwd": (10 * M * c + 8 * M + 2 * M * H, 0),
+            "mod_dw_gemm": (8 * M * hd + 2 * M * c, 2.0 * M * 4 * hd * c)}
+    out = {}
+    for k, (nbytes, flops) in spec.items():
+        ms = kernel_ms[k]
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        r = {"ms": ms, "bytes": nbytes, "hbm_gbs": gbs, "hbm_frac": gbs / peaks["hbm_gbs"]}
+        if flops:
+            tf = flops / (ms * 1e-3) / 1e12
+            r.update({"tflops": tf, "tensor_frac": tf / peaks["bf16_tflops"]})
+        out[k] = r
+    return out
+
+
+def run_module(dev, stream, steps, mw=None):
+    """Times the triangle-attention block (LayerNorm, projections, attention, gate, output projection),
+    forward and backward; default workload crop 768, 128 pair channels, H = 4, d = 32."""
+    import torch
+
+    from bwd_tri_attn_gb300 import binding as tb
+    from bwd_tri_attn_gb300 import workloads as wl
+
+    mw = mw or wl.MOD_CROP768
+    x = {k: (None if v is None else v.to(dev)) for k, v in wl.module_inputs_for(mw).items()}
+    args = [x[k] for k in ("z", "gamma", "beta", "W", "wb", "Wo")]
+    shape = tb.module_shape_of(x["z"], mw.H, mw.d, mw.node)
+    saved = torch.empty(tb.tri_module_saved_size(shape), dtype=torch.uint8, device=dev)
+    ws = torch.empty(tb.tri_module_bwd_workspace_size(shape), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(x["z"])
+    f32 = dict(dtype=torch.float32, device=dev)
+    grads = [torch.empty_like(x["z"]), torch.empty(mw.c, **f32), torch.empty(mw.c, **f32),
+             torch.empty(x["W"].shape, **f32), torch.empty(x["wb"].shape, **f32), torch.empty(x["Wo"].shape, **f32)]
+
+    def step(marks=None):
+        if marks:
+            tb.tri_attn_set_timing_events(marks[:MOD_NFWD])
+        tb.tri_module_fwd(shape, *args, x["mask"], out, saved, stream)
+        if marks:
+            tb.tri_attn_set_timing_events(marks[MOD_NFWD:])
+        tb.tri_module_bwd(shape, *args, x["mask"], saved, x["dout"], *grads, ws, stream)
+
+    for _ in range(3):
+        step()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    marks = [[torch.cuda.Event(enable_timing=True) for _ in MOD_KERNELS] for _ in range(steps)]
+    for e in starts + [m for ms in marks for m in ms]:
+        e.record(stream)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for k in range(steps):
+        starts[k].record(stream)
+        step(marks[k])
+    t1.record(stream)
+    tb.tri_attn_set_timing_events(None)
+    torch.cuda.synchronize()
+    assert tb.tri_attn_device_status() == 0
+    per = {n: 0.0 for n in MOD_KERNELS}
+    for k in range(steps):
+        chain = [starts[k]] + marks[k]
+        for n, (a, b) in enumerate(zip(chain[:-1], chain[1:])):
+            per[MOD_KERNELS[n]] += a.elapsed_time(b) / steps
+    ms = t0.elapsed_time(t1) / steps
+    peaks = load_peaks()
+    M = mw.B * mw.N * mw.N
+    attn = ("fwd_vscale", "fwd", "bias_transpose", "bwd_prep", "bwd_main", "dbias_reduce")
+    around = sum(v for k, v in per.items() if k not in attn)
+    return {"workload": mw.name, "B": mw.B, "N": mw.N, "c": mw.c, "H": mw.H, "d": mw.d,
+            "node": "starting" if mw.node == 0 else "ending", "ms_per_step": ms,
+            "tflops": mw.flops() / (ms * 1e-3) / 1e12, "flops_per_step": mw.flops(), "steps": steps,
+            "attention_ms": sum(per[k] for k in attn), "around_attention_ms": around,
+            "l2": f"inputs and activations larger than L2 (z alone is {2 * M * mw.c / 1e6:.0f} MB), no flush",
+            "kernel_ms": per, "kernels": mod_roofline(per, mw.B, mw.N, mw.c, mw.H, mw.d, peaks),
+            "gpu_launches": steps * len(MOD_KERNELS)}
+
+
+def run_module_only(args):
+    """``--module-only``: the triangle-attention block sub-line alone (one GPU), for profiling."""
+    import torch
+
+    from bwd_tri_attn_gb300 import _build
+    from bwd_tri_attn_gb300 import binding as tb
+    from bwd_tri_attn_gb300 import workloads as wl
+
+    _build.build()
+    tb.load()
+    dev = torch.device("cuda", 0)
+    print(json.dumps({"module": run_module(dev, torch.cuda.current_stream(), args.steps,
+                                           wl.MOD_ALL[args.mod_workload])}))
+
+
 def run_ours(args, w):
     import torch
     import torch.distributed as dist
@@ -583,6 +701,10 @@ def run_ours(args, w):
         mul = [run_trimul(dev, stream, max(3, min(K, 20)), layout=lay, mw=mw)
                for lay in (tb.LAYOUT_CHANNEL_MAJOR, tb.LAYOUT_PAIR)]
 
+    mod = None
+    if not args.no_module:
+        mod = run_module(dev, stream, max(3, min(K, 20)), wl.MOD_ALL[args.mod_workload])
+
     in_bytes = sum(v.numel() * v.element_size() for v in x.values() if v is not None)
     if rank == 0:
         line = {
@@ -600,7 +722,7 @@ def run_ours(args, w):
             # the same step counted without the backward's P recompute (12 instead of 14 x B S H N^2 d)
             "value_12x_count": value * 12.0 / 14.0,
             "kernel_ms": kernel_ms, "hbm": hbm, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": K * len(KERNELS), "clocks": clocks.summary(), "trimul": mul,
+            "gpu_launches": K * len(KERNELS), "clocks": clocks.summary(), "trimul": mul, "module": mod,
         }
         print(json.dumps(line))
     if world > 1:
@@ -626,6 +748,10 @@ def main():
     ap.add_argument("--trimul-only", action="store_true",
                     help="time only the triangle multiplication (both layouts, both directions); one JSON line")
     ap.add_argument("--mul-workload", default=wl.MUL_CROP768.name, choices=sorted(wl.MUL_ALL))
+    ap.add_argument("--no-module", action="store_true", help="skip the triangle-attention block sub-line")
+    ap.add_argument("--module-only", action="store_true",
+                    help="time only the triangle-attention block (forward and backward); one JSON line")
+    ap.add_argument("--mod-workload", default=wl.MOD_CROP768.name, choices=sorted(wl.MOD_ALL))
     ap.add_argument("--windows", type=int, default=0,
                     help="timed windows of --steps steps (0: enough to fill about a second, at least 3)")
     args = ap.parse_args()
@@ -646,6 +772,9 @@ def main():
     w = wl.ALL[args.workload]
     if args.trimul_only:
         run_trimul_only(args)
+        return
+    if args.module_only:
+        run_module_only(args)
         return
     if args.impl == "reference":
         run_reference(args, w)

@@ -78,6 +78,15 @@ def test_crop384_full_oracle():
     _check(got, _oracle(x, w.H, w.d, w.node, False), _oracle(x, w.H, w.d, w.node, True))
 
 
+def test_crop768_full_oracle():
+    """The benchmark's workload and launch configuration (crop 768, 48 masked keys), every output
+    against the full oracle (about a minute of host time per oracle run)."""
+    w = wl.MOD_CROP768
+    x = wl.module_inputs_for(w)
+    got = _run_cuda(x, w.H, w.d, w.node)
+    _check(got, _oracle(x, w.H, w.d, w.node, False), _oracle(x, w.H, w.d, w.node, True))
+
+
 def test_deterministic_across_calls():
     w = wl.MOD_RAGGED
     x = wl.module_inputs_for(w)
