@@ -22,9 +22,9 @@
 //   mod_ln_bwd_kernel     dzt + dbias wb -> dz; per-CTA partial sums of dgamma, dbeta, dwb
 //   GEMM (split over M)   dW partials = [dq | dk | dv | dgl]^T zt, then ordered sums
 //
-// The GEMM is one persistent tcgen05 kernel for every product: M = 128 x N = 256 tiles, K steps
-// of 64 through a 4-stage TMA ring, two TMEM accumulators so that one tile's epilogue overlaps
-// the next tile's main loop. Operands are K-major (row-major [rows][K]) or MN-major (the
+// The GEMM is one persistent tcgen05 kernel for every product: M = 128 x N = 128 or 256 tiles (the
+// narrower for products at most 128 wide), K steps of 64 through a TMA ring, two TMEM
+// accumulators so that one tile's epilogue overlaps the next tile's main loop. Operands are K-major (row-major [rows][K]) or MN-major (the
 // transposed operand mode, [K][rows]); one operand may be split into up to four tensors along K
 // (K-major) or M (MN-major), so [dq | dk | dv | dgl] is read where the attention left it. Products
 // summed over the pair positions split K into fixed chunks of rows; each chunk's FP32 partial is
@@ -67,14 +67,21 @@ struct MGemmArgs {
   uint16_t *dP, *dG;      // kOutGate: [M][N] their gradients
 };
 
+template <int BN_, int kOut_>
 struct MGemmCfg {
-  static constexpr int BM = 128, BN = 256, BK = 64, NST = 4;
+  static constexpr int BM = 128, BN = BN_, BK = 64;
+  // BF16 and FP32 outputs leave through TMA stores of 32 x 32 pieces staged per warp (two pieces,
+  // 64- or 128-byte rows, swizzled like the store's tensor map); the gate epilogue transposes
+  // through a padded 32 x 33 FP32 tile instead
+  static constexpr bool TMA_OUT = kOut_ != 2;
+  static constexpr int PIECE = 32 * 32 * (kOut_ == 1 ? 4 : 2);
+  static constexpr int NST = BN == 256 ? (kOut_ == 1 ? 3 : 4) : (kOut_ == 0 ? 6 : 5);
   static constexpr int A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2, STAGE = A_BYTES + B_BYTES;
   static constexpr int MN_BOX = BK * 128;  // one 64-wide MN-major box: BK rows of 128 bytes
   static constexpr int EPI_WARPS = 8;
   static constexpr int EPI_CPW = BN / 32 / (EPI_WARPS / 4);  // 32-column chunks per epilogue warp
   static constexpr int EPI_PITCH = 33;
-  static constexpr int EPI_TILE = 32 * EPI_PITCH * 4;
+  static constexpr int EPI_TILE = TMA_OUT ? 2 * PIECE : 32 * EPI_PITCH * 4;
   static constexpr int OFF_EPI = NST * STAGE;
   static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * EPI_TILE;
   static constexpr int B_FULL = 0, B_EMPTY = NST, B_ACCF = 2 * NST, B_ACCE = B_ACCF + 2, B_DONE = B_ACCE + 2,
@@ -83,44 +90,47 @@ struct MGemmCfg {
   static constexpr int SMEM_ALLOC = OFF_MISC + 16 + 1024;
   static constexpr int NTHREADS = 64 + 32 * EPI_WARPS;
   static constexpr uint32_t TMEM_COLS = 2 * BN;
-  static_assert(STAGE % 1024 == 0 && A_BYTES % 1024 == 0, "SW128 tiles need 1 KB alignment");
+  static_assert(BN == 128 || BN == 256, "tile width");
+  static_assert(STAGE % 1024 == 0 && A_BYTES % 1024 == 0 && OFF_EPI % 1024 == 0, "1 KB alignment (swizzle atoms)");
+  static_assert(EPI_TILE % 1024 == 0 || !TMA_OUT, "staging pieces on 1 KB boundaries");
   static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 };
 
-template <int kOut>
-__device__ __forceinline__ void mgemm_store8(const MGemmArgs &a, int t, int m, int n, const float (&v)[8]) {
-  if constexpr (kOut == kOutF32) {
-    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(a.D0) + ((int64_t)t * a.M + m) * a.N + n);
-    dst[0] = make_float4(v[0], v[1], v[2], v[3]);
-    dst[1] = make_float4(v[4], v[5], v[6], v[7]);
-  } else if constexpr (kOut == kOutBF16) {
-    const int s = n / a.segD;
-    void *base = s == 0 ? a.D0 : s == 1 ? a.D1 : s == 2 ? a.D2 : a.D3;
-    *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(base) + (int64_t)m * a.segD + (n - s * a.segD)) =
-        make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
-  } else {
-    const int64_t off = (int64_t)m * a.N + n;
-    const uint4 pv = *reinterpret_cast<const uint4 *>(a.P + off), gv = *reinterpret_cast<const uint4 *>(a.G + off);
-    const uint32_t pw[4] = {pv.x, pv.y, pv.z, pv.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
-    uint32_t od[4], og[4];
-#pragma unroll
-    for (int x = 0; x < 4; ++x) {
-      const float d0 = v[2 * x], d1 = v[2 * x + 1];
-      const float s0 = sigm(lo_bf(gw[x])), s1 = sigm(hi_bf(gw[x]));
-      od[x] = pack_bf16x2(d0 * s0, d1 * s1);
-      og[x] = pack_bf16x2(d0 * lo_bf(pw[x]) * (s0 * (1.f - s0)), d1 * hi_bf(pw[x]) * (s1 * (1.f - s1)));
-    }
-    *reinterpret_cast<uint4 *>(a.dP + off) = make_uint4(od[0], od[1], od[2], od[3]);
-    *reinterpret_cast<uint4 *>(a.dG + off) = make_uint4(og[0], og[1], og[2], og[3]);
-  }
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
 }
 
-template <bool kAMN, bool kBMN, int kOut>
-__global__ void __launch_bounds__(MGemmCfg::NTHREADS, 1)
+// The gate epilogue's 8 consecutive values v = dgo of row m, columns n .. n + 7, with the attention
+// output pv and gate logits gv there: dP = dgo s and dG = dgo O s (1 - s), s = sigmoid(gl).
+template <int kOut>
+__device__ __forceinline__ void mgemm_store8(const MGemmArgs &a, int, int m, int n, const float (&v)[8],
+                                             const uint4 &pv, const uint4 &gv) {
+  static_assert(kOut == kOutGate, "BF16 and FP32 outputs leave through TMA stores");
+  const int64_t off = (int64_t)m * a.N + n;
+  const uint32_t pw[4] = {pv.x, pv.y, pv.z, pv.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
+  uint32_t od[4], og[4];
+#pragma unroll
+  for (int x = 0; x < 4; ++x) {
+    const float d0 = v[2 * x], d1 = v[2 * x + 1];
+    const float s0 = sigm(lo_bf(gw[x])), s1 = sigm(hi_bf(gw[x]));
+    od[x] = pack_bf16x2(d0 * s0, d1 * s1);
+    og[x] = pack_bf16x2(d0 * lo_bf(pw[x]) * (s0 * (1.f - s0)), d1 * hi_bf(pw[x]) * (s1 * (1.f - s1)));
+  }
+  *reinterpret_cast<uint4 *>(a.dP + off) = make_uint4(od[0], od[1], od[2], od[3]);
+  *reinterpret_cast<uint4 *>(a.dG + off) = make_uint4(og[0], og[1], og[2], og[3]);
+}
+
+template <bool kAMN, bool kBMN, int kOut, int BN>
+__global__ void __launch_bounds__(MGemmCfg<BN, kOut>::NTHREADS, 1)
     mod_gemm_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
                     const __grid_constant__ CUtensorMap mA2, const __grid_constant__ CUtensorMap mA3,
-                    const __grid_constant__ CUtensorMap mB, const MGemmArgs a, int *status) {
-  using C = MGemmCfg;
+                    const __grid_constant__ CUtensorMap mB, const __grid_constant__ CUtensorMap mO0,
+                    const __grid_constant__ CUtensorMap mO1, const __grid_constant__ CUtensorMap mO2,
+                    const __grid_constant__ CUtensorMap mO3, const MGemmArgs a, int *status) {
+  using C = MGemmCfg<BN, kOut>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb0 = smem_u32(sm);
@@ -244,43 +254,123 @@ __global__ void __launch_bounds__(MGemmCfg::NTHREADS, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue: TMEM -> registers -> global
-    // Per 32 x 32 chunk the TMEM rows go through the warp's staging tile, so that each thread then
-    // holds 8 consecutive values of four rows (whole 16-byte or 32-byte stores).
+    // Each warp reads its chunks (EPI_CPW x 32 columns of its TMEM lane quarter, thread = row) into
+    // registers and hands the accumulator back before its last stores, so the next tile's MMAs
+    // overlap them. BF16 and FP32 outputs: the thread writes its row of a chunk into a staging piece
+    // in the store map's swizzle and one lane issues a TMA store of the 32 x 32 piece (two pieces
+    // per warp in turn). Gate epilogue: the rows go through a padded transpose tile, so that each
+    // thread holds 8 consecutive values of four rows for its loads of O and gl and its stores.
     const int q = warp & 3;
     const int cbase = ((warp - 2) >> 2) * (32 * C::EPI_CPW);
     const uint32_t lrow = (uint32_t)(q * 32) << 16;
+    const uint32_t stg_s = sb0 + C::OFF_EPI + (warp - 2) * C::EPI_TILE;
     float *stg = reinterpret_cast<float *>(sm + C::OFF_EPI + (warp - 2) * C::EPI_TILE);
     const int rq = lane >> 2, cq = lane & 3;
-    int tl = 0;
+    int tl = 0, pc = 0;  // tiles, staged pieces of this warp
     for (int u = blockIdx.x; u < ntiles; u += gridDim.x, ++tl) {
       int t, m0, n0;
       tile_of(u, t, m0, n0);
       const int acc = tl & 1;
-      if (!wait_bar_warp(bar(C::B_ACCF + acc), (tl >> 1) & 1, ab)) break;
-      tc_fence_after();
       const int mrow = m0 + q * 32 + rq;
-#pragma unroll 1
-      for (int k = 0; k < C::EPI_CPW; ++k) {
-        const int c0 = cbase + 32 * k, n = n0 + c0;
-        if (n >= a.N) break;  // uniform across the warp
-        uint32_t r[32];
-        tmem_ld32(tb + lrow + acc * C::BN + c0, r);
-        tmem_wait_ld(r);
+      const bool rows_live = m0 + q * 32 < a.M;  // (warp-uniform) this warp's 32 rows reach into the product
+      // Chunks are read in groups of GRP (all of them, or two at a time where the registers of
+      // four would spill); the accumulator goes back to the MMA warp once the last group is in
+      // registers.
+      constexpr int GRP = (C::EPI_CPW > 2 && kOut != kOutBF16) ? 2 : C::EPI_CPW;
+      bool ok = true;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) stg[lane * C::EPI_PITCH + j] = __uint_as_float(r[j]);
-        __syncwarp();
-        const int col = n + 8 * cq;
+      for (int g0 = 0; g0 < C::EPI_CPW; g0 += GRP) {
+        // the gate epilogue's inputs at this thread's store positions, requested before the waits
+        uint4 pv[GRP][4], gv[GRP][4];
+        if constexpr (kOut == kOutGate) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          float v[8];
+          for (int k = 0; k < GRP; ++k) {
+            const int col = n0 + cbase + 32 * (g0 + k) + 8 * cq;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) v[j] = stg[(rq + 8 * i) * C::EPI_PITCH + 8 * cq + j];
-          if (mrow + 8 * i < a.M && col < a.N) mgemm_store8<kOut>(a, t, mrow + 8 * i, col, v);
+            for (int i = 0; i < 4; ++i)
+              if (mrow + 8 * i < a.M && col < a.N) {
+                const int64_t off = (int64_t)(mrow + 8 * i) * a.N + col;
+                pv[k][i] = *reinterpret_cast<const uint4 *>(a.P + off);
+                gv[k][i] = *reinterpret_cast<const uint4 *>(a.G + off);
+              }
+          }
         }
-        __syncwarp();
+        if (g0 == 0) {
+          ok = wait_bar_warp(bar(C::B_ACCF + acc), (tl >> 1) & 1, ab);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        uint32_t r[GRP][32];
+#pragma unroll
+        for (int k = 0; k < GRP; ++k)
+          if (n0 + cbase + 32 * (g0 + k) < a.N) tmem_ld32(tb + lrow + acc * C::BN + cbase + 32 * (g0 + k), r[k]);
+        tmem_wait_ld(r);
+        if (g0 + GRP >= C::EPI_CPW) {
+          tc_fence_before();
+          mbar_arrive(bar(C::B_ACCE + acc));
+        }
+#pragma unroll
+        for (int k = 0; k < GRP; ++k) {
+          const int n = n0 + cbase + 32 * (g0 + k);
+          if (n >= a.N || !rows_live) break;  // uniform across the warp
+          if constexpr (C::TMA_OUT) {
+            const uint32_t piece = stg_s + (uint32_t)(pc & 1) * C::PIECE;
+            if (pc >= 2) {  // the store issued from this piece two pieces ago has read it
+              if (lane == 0) bulk_wait_group_read<1>();
+              __syncwarp();
+            }
+            if constexpr (kOut == kOutBF16) {
+              // row = lane: 64 bytes, 16-byte chunk c at c ^ ((row / 2) mod 4) (64-byte swizzle)
+#pragma unroll
+              for (int c = 0; c < 4; ++c)
+                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(piece + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)),
+                             "r"(pack_bf16x2(__uint_as_float(r[k][8 * c]), __uint_as_float(r[k][8 * c + 1]))),
+                             "r"(pack_bf16x2(__uint_as_float(r[k][8 * c + 2]), __uint_as_float(r[k][8 * c + 3]))),
+                             "r"(pack_bf16x2(__uint_as_float(r[k][8 * c + 4]), __uint_as_float(r[k][8 * c + 5]))),
+                             "r"(pack_bf16x2(__uint_as_float(r[k][8 * c + 6]), __uint_as_float(r[k][8 * c + 7])))
+                             : "memory");
+            } else {
+              // row = lane: 128 bytes, 16-byte chunk c at c ^ (row mod 8) (128-byte swizzle)
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(piece + lane * 128 + ((c ^ (lane & 7)) << 4)),
+                             "r"(r[k][4 * c]), "r"(r[k][4 * c + 1]), "r"(r[k][4 * c + 2]), "r"(r[k][4 * c + 3])
+                             : "memory");
+            }
+            fence_proxy_async_smem();  // the generic-proxy writes before the async-proxy read
+            __syncwarp();
+            if (lane == 0) {
+              if constexpr (kOut == kOutBF16) {
+                const int sg = n / a.segD;
+                const CUtensorMap *mo = sg == 0 ? &mO0 : sg == 1 ? &mO1 : sg == 2 ? &mO2 : &mO3;
+                tma_store_3d(mo, piece, n - sg * a.segD, m0 + q * 32, 0);
+              } else {
+                tma_store_3d(&mO0, piece, n, m0 + q * 32, t);
+              }
+              bulk_commit_group();
+            }
+            ++pc;
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) stg[lane * C::EPI_PITCH + j] = __uint_as_float(r[k][j]);
+            __syncwarp();
+            const int col = n + 8 * cq;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              float v[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) v[j] = stg[(rq + 8 * i) * C::EPI_PITCH + 8 * cq + j];
+              if (mrow + 8 * i < a.M && col < a.N) mgemm_store8<kOut>(a, t, mrow + 8 * i, col, v, pv[k][i], gv[k][i]);
+            }
+            __syncwarp();
+          }
+        }
       }
-      tc_fence_before();
-      mbar_arrive(bar(C::B_ACCE + acc));
+      if (!ok) break;
+    }
+    if constexpr (C::TMA_OUT) {
+      if (lane == 0) bulk_wait_group<0>();  // every store has been performed before the CTA exits
+      __syncwarp();
     }
   }
   tc_fence_before();
@@ -307,35 +397,42 @@ cudaError_t make_mat_map(CUtensorMap *m, const void *ptr, int64_t inner, int64_t
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// 3-D TMA view (inner, outer, batch) of a row-major output for 32 x 32 stores: BF16 with 64-byte
+// box rows (64-byte swizzle) or FP32 with 128-byte box rows (128-byte swizzle). Rows past `outer`
+// within a batch are not written.
+cudaError_t make_out_map(CUtensorMap *m, void *ptr, bool f32, int64_t inner, int64_t outer, int64_t batch) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  const int64_t es_bytes = f32 ? 4 : 2;
+  cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)outer, (cuuint64_t)batch};
+  cuuint64_t strides[2] = {(cuuint64_t)(es_bytes * inner), (cuuint64_t)(es_bytes * inner * outer)};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, strides,
+                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 // One planned product. A(m, k): K-major A is row-major [M][K] (split along K into the given
 // tensors of segA columns each), MN-major A is row-major [K][M] (split along M into tensors of
 // segA columns each); B(n, k): K-major [N][K] or MN-major [K][N].
-template <bool kAMN, bool kBMN, int kOut>
-struct MGemm {
-  CUtensorMap mA[4], mB;
+template <bool kAMN, bool kBMN, int kOut, int BN>
+struct MGemmT {
+  using C = MGemmCfg<BN, kOut>;
+  CUtensorMap mA[4], mB, mO[4];
   MGemmArgs a;
   int grid;
-  cudaError_t plan(const uint16_t *const *A, int nA, int segA, const uint16_t *B, int M, int N, int K, int Kc) {
-    using C = MGemmCfg;
+  // io: the outputs (kOutBF16: D0..D3 and segD; kOutF32: D0; kOutGate: P, G, dP, dG)
+  cudaError_t plan(const uint16_t *const *A, int nA, int segA, const uint16_t *B, int M, int N, int K, int Kc,
+                   const MGemmArgs &io) {
     cudaError_t e = cudaSuccess;
     for (int s = 0; s < 4 && e == cudaSuccess; ++s) {
       const uint16_t *p = A[s < nA ? s : 0];
       e = kAMN ? make_mat_map(&mA[s], p, segA, K, segA, C::BK) : make_mat_map(&mA[s], p, segA, M, segA, C::BM);
     }
     if (e == cudaSuccess) e = kBMN ? make_mat_map(&mB, B, N, K, N, C::BK) : make_mat_map(&mB, B, K, N, K, C::BN);
-    if (e != cudaSuccess) return e;
-    int dev = 0, nsm = 0;
-    e = current_device(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    static DeviceOnce ready;
-    if (!ready.done(dev)) {
-      e = cudaFuncSetAttribute(mod_gemm_kernel<kAMN, kBMN, kOut>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               C::SMEM_ALLOC);
-      if (e != cudaSuccess) return e;
-      ready.mark(dev);
-    }
-    a = MGemmArgs{};
+    a = io;
     a.M = M;
     a.N = N;
     a.K = K;
@@ -343,24 +440,54 @@ struct MGemm {
     a.T = (K + Kc - 1) / Kc;
     a.segA = segA;
     a.nsegA = nA;
+    void *d[4] = {io.D0, io.D1, io.D2, io.D3};
+    for (int s = 0; s < 4 && e == cudaSuccess; ++s) {
+      if (kOut == kOutBF16) {
+        const int nseg = (N + io.segD - 1) / io.segD;
+        e = make_out_map(&mO[s], d[s < nseg ? s : 0], false, io.segD, M, 1);
+      } else if (kOut == kOutF32) {
+        e = make_out_map(&mO[s], d[0], true, N, M, a.T);
+      } else {
+        mO[s] = mB;  // (unused by the gate epilogue)
+      }
+    }
+    if (e != cudaSuccess) return e;
+    int dev = 0, nsm = 0;
+    e = current_device(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    static DeviceOnce ready;
+    if (!ready.done(dev)) {
+      e = cudaFuncSetAttribute(mod_gemm_kernel<kAMN, kBMN, kOut, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               C::SMEM_ALLOC);
+      if (e != cudaSuccess) return e;
+      ready.mark(dev);
+    }
     const int64_t tiles = (int64_t)a.T * ((M + C::BM - 1) / C::BM) * ((N + C::BN - 1) / C::BN);
     grid = (int)std::min<int64_t>(tiles, nsm);
     return cudaSuccess;
   }
-  cudaError_t launch(const MGemmArgs &io, int *status, cudaStream_t st) const {
-    MGemmArgs x = a;
-    x.D0 = io.D0;
-    x.D1 = io.D1;
-    x.D2 = io.D2;
-    x.D3 = io.D3;
-    x.segD = io.segD;
-    x.P = io.P;
-    x.G = io.G;
-    x.dP = io.dP;
-    x.dG = io.dG;
-    mod_gemm_kernel<kAMN, kBMN, kOut>
-        <<<grid, MGemmCfg::NTHREADS, MGemmCfg::SMEM_ALLOC, st>>>(mA[0], mA[1], mA[2], mA[3], mB, x, status);
+  cudaError_t launch(int *status, cudaStream_t st) const {
+    mod_gemm_kernel<kAMN, kBMN, kOut, BN><<<grid, C::NTHREADS, C::SMEM_ALLOC, st>>>(
+        mA[0], mA[1], mA[2], mA[3], mB, mO[0], mO[1], mO[2], mO[3], a, status);
     return cudaGetLastError();
+  }
+};
+
+// The tile width follows the product's width: N <= 128 takes 128-column tiles (no MMA work or
+// epilogue warps spent on empty columns), wider products 256-column tiles.
+template <bool kAMN, bool kBMN, int kOut>
+struct MGemm {
+  MGemmT<kAMN, kBMN, kOut, 128> narrow;
+  MGemmT<kAMN, kBMN, kOut, 256> wide;
+  bool use_narrow = false;
+  cudaError_t plan(const uint16_t *const *A, int nA, int segA, const uint16_t *B, int M, int N, int K, int Kc,
+                   const MGemmArgs &io) {
+    use_narrow = N <= 128;
+    return use_narrow ? narrow.plan(A, nA, segA, B, M, N, K, Kc, io) : wide.plan(A, nA, segA, B, M, N, K, Kc, io);
+  }
+  cudaError_t launch(int *status, cudaStream_t st) const {
+    return use_narrow ? narrow.launch(status, st) : wide.launch(status, st);
   }
 };
 
@@ -375,90 +502,145 @@ MGemmArgs out_bf16(void *d0, void *d1, void *d2, void *d3, int seg) {
 }
 
 // ================================================================ LayerNorm and pair bias
-// One warp per pair position, CC / 32 consecutive channels per lane; sums over the channels by a
-// fixed xor-shuffle tree. The bias of head h is the dot product of the BF16-rounded zt row (the
-// values the projections read) with wb[h], written by lane h.
+// CC / 8 lanes per pair position, 8 consecutive channels (16 bytes) per lane, 32 / (CC / 8)
+// positions per warp at a time; sums over a position's channels by a fixed xor-shuffle tree
+// within its lane group. The bias of head h is the dot product of the BF16-rounded zt row (the
+// values the projections read) with wb[h], written by lane h of the group.
 template <int CC>
+struct LnLanes {
+  static constexpr int LPR = CC / 8, RPW = 32 / LPR;
+  static_assert(CC == 64 || CC == 128 || CC == 256, "channels");
+};
+
+__device__ __forceinline__ void unpack8(const uint4 &w, float (&v)[8]) {
+  const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) v[2 * j] = lo_bf(ww[j]), v[2 * j + 1] = hi_bf(ww[j]);
+}
+
+template <int LPR>
+__device__ __forceinline__ float group_sum(float x) {
+#pragma unroll
+  for (int o = LPR / 2; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// The HM per-lane values v[h] summed over a lane group of LPR lanes (LPR >= HM), by recursive
+// halving: at each of the first log2(HM) levels a lane keeps half of its heads and receives the
+// partner's partial sums of them, then plain xor steps finish. Returns the sum for head
+// head_of_lane<LPR, HM>(sl); a fixed tree, HM - 1 + log2(LPR / HM) shuffles instead of HM log2(LPR).
+template <int LPR, int HM>
+__device__ __forceinline__ float group_sum_scatter(float (&v)[HM], int sl) {
+  int count = HM;
+#pragma unroll
+  for (int o = LPR / 2; o > 0; o >>= 1) {
+    if (count > 1) {
+      const int half = count / 2;
+      const bool upper = (sl & o) != 0;
+#pragma unroll
+      for (int i = 0; i < HM / 2; ++i) {
+        if (i < half) {
+          const float send = upper ? v[i] : v[i + half], keep = upper ? v[i + half] : v[i];
+          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+      }
+      count = half;
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+    }
+  }
+  return v[0];
+}
+
+// The head whose sum group_sum_scatter leaves in lane sl of its group.
+template <int LPR, int HM>
+__device__ __forceinline__ int head_of_lane(int sl) {
+  int h = 0, w = HM / 2;
+#pragma unroll
+  for (int o = LPR / 2; o > 0 && w > 0; o >>= 1, w >>= 1)
+    if (sl & o) h += w;
+  return h;
+}
+
+template <int CC, int HM>
 __global__ void __launch_bounds__(256) mod_ln_fwd_kernel(const uint16_t *__restrict__ z, const float *__restrict__ gamma,
                                                          const float *__restrict__ beta, const uint16_t *__restrict__ wb,
                                                          int H, int N, int node, float eps, int64_t M,
                                                          uint16_t *__restrict__ zt, float *__restrict__ mu,
                                                          float *__restrict__ rstd, uint16_t *__restrict__ bias) {
-  constexpr int CPL = CC / 32;
-  const int lane = threadIdx.x & 31;
+  using L = LnLanes<CC>;
+  const int lane = threadIdx.x & 31, sl = lane % L::LPR, rs = lane / L::LPR;
   const int64_t w0 = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5), ws = (int64_t)gridDim.x * 8;
-  float gm[CPL], bt[CPL], wv[8][CPL];
+  float gm[8], bt[8], wv[HM][8];
 #pragma unroll
-  for (int j = 0; j < CPL; ++j) {
-    gm[j] = gamma[lane * CPL + j];
-    bt[j] = beta[lane * CPL + j];
+  for (int j = 0; j < 8; ++j) {
+    gm[j] = gamma[sl * 8 + j];
+    bt[j] = beta[sl * 8 + j];
   }
 #pragma unroll
-  for (int h = 0; h < 8; ++h)
+  for (int h = 0; h < HM; ++h) {
+    if (h < H) {
+      unpack8(*reinterpret_cast<const uint4 *>(wb + h * CC + sl * 8), wv[h]);
+    } else {
 #pragma unroll
-    for (int j = 0; j < CPL; ++j) wv[h][j] = h < H ? __uint_as_float((uint32_t)wb[h * CC + lane * CPL + j] << 16) : 0.f;
+      for (int j = 0; j < 8; ++j) wv[h][j] = 0.f;
+    }
+  }
   const int64_t NN = (int64_t)N * N;
-  for (int64_t m = w0; m < M; m += ws) {
-    float x[CPL];
-    const uint16_t *src = z + m * CC + lane * CPL;
-    if constexpr (CPL == 2) {
-      const uint32_t w = *reinterpret_cast<const uint32_t *>(src);
-      x[0] = lo_bf(w);
-      x[1] = hi_bf(w);
-    } else if constexpr (CPL == 4) {
-      const uint2 w = *reinterpret_cast<const uint2 *>(src);
-      x[0] = lo_bf(w.x), x[1] = hi_bf(w.x), x[2] = lo_bf(w.y), x[3] = hi_bf(w.y);
-    } else {
-      const uint4 w = *reinterpret_cast<const uint4 *>(src);
-      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+  const uint32_t nn32 = (uint32_t)NN, n32 = (uint32_t)N;
+  // U position groups per warp at a time, their loads issued together (bytes in flight)
+  constexpr int U = 4;
+  for (int64_t g = w0 * U; g * L::RPW < M; g += ws * U) {
+    uint4 raw[U];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) x[2 * j] = lo_bf(ww[j]), x[2 * j + 1] = hi_bf(ww[j]);
+    for (int u = 0; u < U; ++u) {
+      const int64_t m = (g + u) * L::RPW + rs;
+      raw[u] = m < M ? *reinterpret_cast<const uint4 *>(z + m * CC + sl * 8) : make_uint4(0u, 0u, 0u, 0u);
     }
-    float s = 0.f;
 #pragma unroll
-    for (int j = 0; j < CPL; ++j) s += x[j];
+    for (int u = 0; u < U; ++u) {
+      const int64_t m = (g + u) * L::RPW + rs;
+      const bool live = m < M;  // (lane groups past the last position idle, but join the shuffles)
+      float x[8];
+      unpack8(raw[u], x);
+      float s = 0.f;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    const float mean = s * (1.f / CC);
-    float q = 0.f;
+      for (int j = 0; j < 8; ++j) s += x[j];
+      const float mean = group_sum<L::LPR>(s) * (1.f / CC);
+      float q = 0.f;
 #pragma unroll
-    for (int j = 0; j < CPL; ++j) q = fmaf(x[j] - mean, x[j] - mean, q);
+      for (int j = 0; j < 8; ++j) q = fmaf(x[j] - mean, x[j] - mean, q);
+      const float r = rsqrtf(group_sum<L::LPR>(q) * (1.f / CC) + eps);
+      uint32_t yw[4];
+      float y[8];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
-    const float r = 1.f / sqrtf(q * (1.f / CC) + eps);
-    uint32_t yw[CPL / 2];
-    float y[CPL];
+      for (int j = 0; j < 4; ++j) {
+        yw[j] = pack_bf16x2(fmaf((x[2 * j] - mean) * r, gm[2 * j], bt[2 * j]),
+                            fmaf((x[2 * j + 1] - mean) * r, gm[2 * j + 1], bt[2 * j + 1]));
+        y[2 * j] = lo_bf(yw[j]);
+        y[2 * j + 1] = hi_bf(yw[j]);
+      }
+      if (live) {
+        *reinterpret_cast<uint4 *>(zt + m * CC + sl * 8) = make_uint4(yw[0], yw[1], yw[2], yw[3]);
+        if (sl == 0) {
+          mu[m] = mean;
+          rstd[m] = r;
+        }
+      }
+      // (b, x, y) of the position; positions and N^2 fit 32 bits (B N <= 65535, N <= 1024)
+      const uint32_t m32 = (uint32_t)m, b = m32 / nn32, xy = m32 - b * nn32, px = xy / n32, py = xy - px * n32;
+      const int64_t boff = node == 0 ? (int64_t)px * N + py : (int64_t)py * N + px;
+      float p[HM];
 #pragma unroll
-    for (int j = 0; j < CPL / 2; ++j) {
-      yw[j] = pack_bf16x2(fmaf((x[2 * j] - mean) * r, gm[2 * j], bt[2 * j]),
-                          fmaf((x[2 * j + 1] - mean) * r, gm[2 * j + 1], bt[2 * j + 1]));
-      y[2 * j] = lo_bf(yw[j]);
-      y[2 * j + 1] = hi_bf(yw[j]);
-    }
-    uint16_t *dst = zt + m * CC + lane * CPL;
-    if constexpr (CPL == 2) {
-      *reinterpret_cast<uint32_t *>(dst) = yw[0];
-    } else if constexpr (CPL == 4) {
-      *reinterpret_cast<uint2 *>(dst) = make_uint2(yw[0], yw[1]);
-    } else {
-      *reinterpret_cast<uint4 *>(dst) = make_uint4(yw[0], yw[1], yw[2], yw[3]);
-    }
-    if (lane == 0) {
-      mu[m] = mean;
-      rstd[m] = r;
-    }
-    const int64_t b = m / NN, xy = m - b * NN;
-    const int px = (int)(xy / N), py = (int)(xy - (int64_t)px * N);
-    const int64_t boff = node == 0 ? (int64_t)px * N + py : (int64_t)py * N + px;
+      for (int h = 0; h < HM; ++h) {
+        p[h] = 0.f;
 #pragma unroll
-    for (int h = 0; h < 8; ++h) {
-      if (h >= H) break;
-      float p = 0.f;
-#pragma unroll
-      for (int j = 0; j < CPL; ++j) p = fmaf(y[j], wv[h][j], p);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
-      if (lane == h) bias[(b * H + h) * NN + boff] = (uint16_t)(pack_bf16x2(p, 0.f) & 0xffffu);
+        for (int j = 0; j < 8; ++j) p[h] = fmaf(y[j], wv[h][j], p[h]);
+      }
+      const float ph = group_sum_scatter<L::LPR, HM>(p, sl);
+      const int hh = head_of_lane<L::LPR, HM>(sl);
+      if (live && hh < H && (sl & (L::LPR / HM - 1)) == 0)
+        bias[((int64_t)b * H + hh) * NN + boff] = (uint16_t)(pack_bf16x2(ph, 0.f) & 0xffffu);
     }
   }
 }
@@ -478,120 +660,134 @@ __global__ void __launch_bounds__(256) mod_gate_kernel(const uint16_t *__restric
 }
 
 // ================================================================ LayerNorm backward
-// One CTA per fixed chunk of `rpc` pair positions (one warp per position, positions strided over
-// the eight warps). g = dzt + sum_h dbias_h wb[h] is the full gradient of zt; with zh = (z - mean)
-// rstd and dzh = g gamma, dz = rstd (dzh - mean(dzh) - zh mean(dzh zh)). The CTA's partial sums of
-// dgamma (g zh), dbeta (g) and dwb[h] (dbias_h zt) are added over its warps in warp order and
-// written to part[blockIdx.x][2 + H][CC].
-template <int CC>
+// One CTA per fixed chunk of `rpc` pair positions; lane groups as in the forward (CC / 8 lanes per
+// position, 8 channels per lane), the warps of the CTA taking the chunk's positions in turn.
+// g = dzt + sum_h dbias_h wb[h] is the full gradient of zt; with zh = (z - mean) rstd and
+// dzh = g gamma, dz = rstd (dzh - mean(dzh) - zh mean(dzh zh)). The CTA's partial sums of dgamma
+// (g zh), dbeta (g) and dwb[h] (dbias_h zt) are added over the lane groups of a warp by a fixed
+// xor-shuffle tree, then over the warps in warp order, and written to part[blockIdx.x][2 + H][CC].
+template <int CC, int HM>
 __global__ void __launch_bounds__(256) mod_ln_bwd_kernel(const float *__restrict__ dzt, const uint16_t *__restrict__ dbias,
                                                          const uint16_t *__restrict__ z, const uint16_t *__restrict__ zt,
                                                          const float *__restrict__ mu, const float *__restrict__ rstd,
                                                          const float *__restrict__ gamma, const uint16_t *__restrict__ wb,
                                                          int H, int N, int node, int64_t M, int rpc,
                                                          uint16_t *__restrict__ dz, float *__restrict__ part) {
-  constexpr int CPL = CC / 32;
-  __shared__ float red[10 * CC];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  float gm[CPL], wv[8][CPL];
+  using L = LnLanes<CC>;
+  __shared__ float red[(2 + HM) * CC];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, sl = lane % L::LPR, rs = lane / L::LPR;
+  const int gbase = lane - sl;  // first lane of this lane group
+  float gm[8], wv[HM][8];
 #pragma unroll
-  for (int j = 0; j < CPL; ++j) gm[j] = gamma[lane * CPL + j];
+  for (int j = 0; j < 8; ++j) gm[j] = gamma[sl * 8 + j];
 #pragma unroll
-  for (int h = 0; h < 8; ++h)
+  for (int h = 0; h < HM; ++h) {
+    if (h < H) {
+      unpack8(*reinterpret_cast<const uint4 *>(wb + h * CC + sl * 8), wv[h]);
+    } else {
 #pragma unroll
-    for (int j = 0; j < CPL; ++j) wv[h][j] = h < H ? __uint_as_float((uint32_t)wb[h * CC + lane * CPL + j] << 16) : 0.f;
-  float ag[CPL], ab[CPL], aw[8][CPL];
+      for (int j = 0; j < 8; ++j) wv[h][j] = 0.f;
+    }
+  }
+  float ag[8], ab[8], aw[HM][8];
 #pragma unroll
-  for (int j = 0; j < CPL; ++j) {
+  for (int j = 0; j < 8; ++j) {
     ag[j] = 0.f;
     ab[j] = 0.f;
 #pragma unroll
-    for (int h = 0; h < 8; ++h) aw[h][j] = 0.f;
+    for (int h = 0; h < HM; ++h) aw[h][j] = 0.f;
   }
   const int64_t NN = (int64_t)N * N;
+  const uint32_t nn32 = (uint32_t)NN, n32 = (uint32_t)N;
   const int64_t r0 = (int64_t)blockIdx.x * rpc, r1 = min(M, r0 + rpc);
-  auto ld_bf = [](const uint16_t *src, float (&v)[CPL]) {
-    if constexpr (CPL == 2) {
-      const uint32_t w = *reinterpret_cast<const uint32_t *>(src);
-      v[0] = lo_bf(w), v[1] = hi_bf(w);
-    } else if constexpr (CPL == 4) {
-      const uint2 w = *reinterpret_cast<const uint2 *>(src);
-      v[0] = lo_bf(w.x), v[1] = hi_bf(w.x), v[2] = lo_bf(w.y), v[3] = hi_bf(w.y);
-    } else {
-      const uint4 w = *reinterpret_cast<const uint4 *>(src);
-      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+  // U position groups per warp at a time, their loads issued together (bytes in flight)
+  constexpr int U = 2;
+  for (int64_t g0 = r0 + (int64_t)warp * U * L::RPW; g0 < r1; g0 += 8 * U * L::RPW) {
+    float4 rg[U][2];
+    uint4 rz[U], rt[U];
+    float rdb[U], rmu[U], rr[U];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) v[2 * j] = lo_bf(ww[j]), v[2 * j + 1] = hi_bf(ww[j]);
-    }
-  };
-  for (int64_t m = r0 + warp; m < r1; m += 8) {
-    const int64_t b = m / NN, xy = m - b * NN;
-    const int px = (int)(xy / N), py = (int)(xy - (int64_t)px * N);
-    const int64_t boff = node == 0 ? (int64_t)px * N + py : (int64_t)py * N + px;
-    float db[8];
-#pragma unroll
-    for (int h = 0; h < 8; ++h) db[h] = h < H ? __uint_as_float((uint32_t)dbias[(b * H + h) * NN + boff] << 16) : 0.f;
-    float g[CPL], zv[CPL], tv[CPL];
-    const float *gs = dzt + m * CC + lane * CPL;
-#pragma unroll
-    for (int j = 0; j < CPL; j += 2) {
-      const float2 t = *reinterpret_cast<const float2 *>(gs + j);
-      g[j] = t.x;
-      g[j + 1] = t.y;
+    for (int u = 0; u < U; ++u) {
+      const int64_t m = g0 + u * L::RPW + rs;
+      const int64_t mm = m < r1 ? m : r0;  // idle lane groups shadow a live position, contributing nothing
+      const uint32_t m32 = (uint32_t)mm, b = m32 / nn32, xy = m32 - b * nn32, px = xy / n32, py = xy - px * n32;
+      const int64_t boff = node == 0 ? (int64_t)px * N + py : (int64_t)py * N + px;
+      // lane h of the group loads dbias of head h
+      rdb[u] = sl < H ? __uint_as_float((uint32_t)dbias[((int64_t)b * H + sl) * NN + boff] << 16) : 0.f;
+      rg[u][0] = *reinterpret_cast<const float4 *>(dzt + mm * CC + sl * 8);
+      rg[u][1] = *reinterpret_cast<const float4 *>(dzt + mm * CC + sl * 8 + 4);
+      rz[u] = *reinterpret_cast<const uint4 *>(z + mm * CC + sl * 8);
+      rt[u] = *reinterpret_cast<const uint4 *>(zt + mm * CC + sl * 8);
+      rmu[u] = mu[mm];
+      rr[u] = rstd[mm];
     }
 #pragma unroll
-    for (int h = 0; h < 8; ++h)
+    for (int u = 0; u < U; ++u) {
+      const int64_t m = g0 + u * L::RPW + rs;
+      const bool live = m < r1;
+      float db[HM];
 #pragma unroll
-      for (int j = 0; j < CPL; ++j) g[j] = fmaf(db[h], wv[h][j], g[j]);
-    ld_bf(z + m * CC + lane * CPL, zv);
-    ld_bf(zt + m * CC + lane * CPL, tv);
-    const float mean = mu[m], r = rstd[m];
-    float zh[CPL], dzh[CPL], s1 = 0.f, s2 = 0.f;
+      for (int h = 0; h < HM; ++h) db[h] = __shfl_sync(0xffffffffu, rdb[u], gbase + (h < H ? h : 0));
+      float g[8], zv[8], tv[8];
+      g[0] = rg[u][0].x, g[1] = rg[u][0].y, g[2] = rg[u][0].z, g[3] = rg[u][0].w;
+      g[4] = rg[u][1].x, g[5] = rg[u][1].y, g[6] = rg[u][1].z, g[7] = rg[u][1].w;
+      unpack8(rz[u], zv);
+      unpack8(rt[u], tv);
 #pragma unroll
-    for (int j = 0; j < CPL; ++j) {
-      zh[j] = (zv[j] - mean) * r;
-      dzh[j] = g[j] * gm[j];
-      s1 += dzh[j];
-      s2 = fmaf(dzh[j], zh[j], s2);
-    }
+      for (int h = 0; h < HM; ++h) {
+        if (h >= H) break;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      s1 += __shfl_xor_sync(0xffffffffu, s1, o);
-      s2 += __shfl_xor_sync(0xffffffffu, s2, o);
-    }
-    s1 *= (1.f / CC);
-    s2 *= (1.f / CC);
-    uint32_t ow[CPL / 2];
+        for (int j = 0; j < 8; ++j) g[j] = fmaf(db[h], wv[h][j], g[j]);
+      }
+      const float mean = rmu[u], r = rr[u];
+      float zh[8], dzh[8], s1 = 0.f, s2 = 0.f;
 #pragma unroll
-    for (int j = 0; j < CPL / 2; ++j)
-      ow[j] = pack_bf16x2(r * (dzh[2 * j] - s1 - zh[2 * j] * s2), r * (dzh[2 * j + 1] - s1 - zh[2 * j + 1] * s2));
-    uint16_t *dst = dz + m * CC + lane * CPL;
-    if constexpr (CPL == 2) {
-      *reinterpret_cast<uint32_t *>(dst) = ow[0];
-    } else if constexpr (CPL == 4) {
-      *reinterpret_cast<uint2 *>(dst) = make_uint2(ow[0], ow[1]);
-    } else {
-      *reinterpret_cast<uint4 *>(dst) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
-    }
+      for (int j = 0; j < 8; ++j) {
+        zh[j] = (zv[j] - mean) * r;
+        dzh[j] = g[j] * gm[j];
+        s1 += dzh[j];
+        s2 = fmaf(dzh[j], zh[j], s2);
+      }
+      s1 = group_sum<L::LPR>(s1) * (1.f / CC);
+      s2 = group_sum<L::LPR>(s2) * (1.f / CC);
+      if (live) {
+        uint32_t ow[4];
 #pragma unroll
-    for (int j = 0; j < CPL; ++j) {
-      ag[j] = fmaf(g[j], zh[j], ag[j]);
-      ab[j] += g[j];
+        for (int j = 0; j < 4; ++j)
+          ow[j] = pack_bf16x2(r * (dzh[2 * j] - s1 - zh[2 * j] * s2), r * (dzh[2 * j + 1] - s1 - zh[2 * j + 1] * s2));
+        *reinterpret_cast<uint4 *>(dz + m * CC + sl * 8) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
 #pragma unroll
-      for (int h = 0; h < 8; ++h) aw[h][j] = fmaf(db[h], tv[j], aw[h][j]);
+        for (int j = 0; j < 8; ++j) {
+          ag[j] = fmaf(g[j], zh[j], ag[j]);
+          ab[j] += g[j];
+#pragma unroll
+          for (int h = 0; h < HM; ++h) aw[h][j] = fmaf(db[h], tv[j], aw[h][j]);
+        }
+      }
     }
   }
-  // the CTA's partial: warps added in warp order
+  // the warp's lane groups added by a fixed xor tree (every lane group ends with the warp's sums)
+#pragma unroll
+  for (int o = L::LPR; o < 32; o <<= 1) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      ag[j] += __shfl_xor_sync(0xffffffffu, ag[j], o);
+      ab[j] += __shfl_xor_sync(0xffffffffu, ab[j], o);
+#pragma unroll
+      for (int h = 0; h < HM; ++h) aw[h][j] += __shfl_xor_sync(0xffffffffu, aw[h][j], o);
+    }
+  }
+  // then the warps in warp order
   const int nrow = 2 + H;
   for (int w = 0; w < 8; ++w) {
-    if (warp == w) {
+    if (warp == w && rs == 0) {
 #pragma unroll
-      for (int j = 0; j < CPL; ++j) {
-        const int c = lane * CPL + j;
+      for (int j = 0; j < 8; ++j) {
+        const int c = sl * 8 + j;
         red[c] = w ? red[c] + ag[j] : ag[j];
         red[CC + c] = w ? red[CC + c] + ab[j] : ab[j];
 #pragma unroll
-        for (int h = 0; h < 8; ++h)
+        for (int h = 0; h < HM; ++h)
           if (h < H) red[(2 + h) * CC + c] = w ? red[(2 + h) * CC + c] + aw[h][j] : aw[h][j];
       }
     }
@@ -641,7 +837,7 @@ int64_t rows_of(const tri_module_shape &s) { return (int64_t)s.B * s.N * s.N; }
 // Fixed chunks of pair positions for the sums over positions: about 144 chunks of a multiple of
 // 64 rows (the GEMM's K step), chosen from the shape alone.
 int split_rows(int64_t M) { return (int)std::max<int64_t>(64, ((M + 143) / 144 + 63) / 64 * 64); }
-int ln_rows(int64_t M) { return (int)std::max<int64_t>(8, ((M + 295) / 296 + 7) / 8 * 8); }
+int ln_rows(int64_t M) { return (int)std::max<int64_t>(8, ((M + 303) / 304 + 7) / 8 * 8); }
 
 struct SavedLayout {
   size_t zt, mu, rstd, q, k, v, gl, bias, O, Ores, LSE, go, total;
@@ -702,27 +898,48 @@ T *at(void *base, size_t off) {
   return reinterpret_cast<T *>(static_cast<char *>(base) + off);
 }
 
+template <int HM>
+void ln_fwd_c(const tri_module_shape &s, int grid, const uint16_t *z, const float *gamma, const float *beta,
+              const uint16_t *wb, uint16_t *zt, float *mu, float *rstd, uint16_t *bias, cudaStream_t st) {
+  const int64_t M = rows_of(s);
+  switch (s.c) {
+    case 64: mod_ln_fwd_kernel<64, HM><<<grid, 256, 0, st>>>(z, gamma, beta, wb, s.H, s.N, s.node, s.eps, M, zt, mu, rstd, bias); break;
+    case 128: mod_ln_fwd_kernel<128, HM><<<grid, 256, 0, st>>>(z, gamma, beta, wb, s.H, s.N, s.node, s.eps, M, zt, mu, rstd, bias); break;
+    default: mod_ln_fwd_kernel<256, HM><<<grid, 256, 0, st>>>(z, gamma, beta, wb, s.H, s.N, s.node, s.eps, M, zt, mu, rstd, bias); break;
+  }
+}
+
 cudaError_t launch_ln_fwd(const tri_module_shape &s, const uint16_t *z, const float *gamma, const float *beta,
                           const uint16_t *wb, uint16_t *zt, float *mu, float *rstd, uint16_t *bias, cudaStream_t st) {
   const int64_t M = rows_of(s);
-  const int grid = (int)std::min<int64_t>((M + 7) / 8, 152 * 16);
-  switch (s.c) {
-    case 64: mod_ln_fwd_kernel<64><<<grid, 256, 0, st>>>(z, gamma, beta, wb, s.H, s.N, s.node, s.eps, M, zt, mu, rstd, bias); break;
-    case 128: mod_ln_fwd_kernel<128><<<grid, 256, 0, st>>>(z, gamma, beta, wb, s.H, s.N, s.node, s.eps, M, zt, mu, rstd, bias); break;
-    default: mod_ln_fwd_kernel<256><<<grid, 256, 0, st>>>(z, gamma, beta, wb, s.H, s.N, s.node, s.eps, M, zt, mu, rstd, bias); break;
-  }
+  const int rpw = 32 / (s.c / 8);  // positions per warp at a time
+  const int grid = (int)std::min<int64_t>((M + 32 * rpw - 1) / (32 * rpw), 152 * 16);
+  if (s.H <= 4)
+    ln_fwd_c<4>(s, grid, z, gamma, beta, wb, zt, mu, rstd, bias, st);
+  else
+    ln_fwd_c<8>(s, grid, z, gamma, beta, wb, zt, mu, rstd, bias, st);
   return cudaGetLastError();
+}
+
+template <int HM>
+void ln_bwd_c(const tri_module_shape &s, const BwdLayout &L, const float *dzt, const uint16_t *dbias, const uint16_t *z,
+              const uint16_t *zt, const float *mu, const float *rstd, const float *gamma, const uint16_t *wb,
+              uint16_t *dz, float *part, cudaStream_t st) {
+  const int64_t M = rows_of(s);
+  switch (s.c) {
+    case 64: mod_ln_bwd_kernel<64, HM><<<L.nln, 256, 0, st>>>(dzt, dbias, z, zt, mu, rstd, gamma, wb, s.H, s.N, s.node, M, L.rpc, dz, part); break;
+    case 128: mod_ln_bwd_kernel<128, HM><<<L.nln, 256, 0, st>>>(dzt, dbias, z, zt, mu, rstd, gamma, wb, s.H, s.N, s.node, M, L.rpc, dz, part); break;
+    default: mod_ln_bwd_kernel<256, HM><<<L.nln, 256, 0, st>>>(dzt, dbias, z, zt, mu, rstd, gamma, wb, s.H, s.N, s.node, M, L.rpc, dz, part); break;
+  }
 }
 
 cudaError_t launch_ln_bwd(const tri_module_shape &s, const BwdLayout &L, const float *dzt, const uint16_t *dbias,
                           const uint16_t *z, const uint16_t *zt, const float *mu, const float *rstd, const float *gamma,
                           const uint16_t *wb, uint16_t *dz, float *part, cudaStream_t st) {
-  const int64_t M = rows_of(s);
-  switch (s.c) {
-    case 64: mod_ln_bwd_kernel<64><<<L.nln, 256, 0, st>>>(dzt, dbias, z, zt, mu, rstd, gamma, wb, s.H, s.N, s.node, M, L.rpc, dz, part); break;
-    case 128: mod_ln_bwd_kernel<128><<<L.nln, 256, 0, st>>>(dzt, dbias, z, zt, mu, rstd, gamma, wb, s.H, s.N, s.node, M, L.rpc, dz, part); break;
-    default: mod_ln_bwd_kernel<256><<<L.nln, 256, 0, st>>>(dzt, dbias, z, zt, mu, rstd, gamma, wb, s.H, s.N, s.node, M, L.rpc, dz, part); break;
-  }
+  if (s.H <= 4)
+    ln_bwd_c<4>(s, L, dzt, dbias, z, zt, mu, rstd, gamma, wb, dz, part, st);
+  else
+    ln_bwd_c<8>(s, L, dzt, dbias, z, zt, mu, rstd, gamma, wb, dz, part, st);
   return cudaGetLastError();
 }
 
@@ -777,8 +994,8 @@ int tri_module_fwd(tri_module_shape shape, const tri_attn_bf16 *z, const float *
   // every plan before the first launch
   MGemm<false, false, kOutBF16> g_in, g_out;
   const uint16_t *a_in[1] = {zt}, *a_out[1] = {go};
-  if (g_in.plan(a_in, 1, c, W, (int)M, 4 * hd, c, c) != cudaSuccess ||
-      g_out.plan(a_out, 1, hd, Wo, (int)M, c, hd, hd) != cudaSuccess)
+  if (g_in.plan(a_in, 1, c, W, (int)M, 4 * hd, c, c, out_bf16(q, k, v, gl, hd)) != cudaSuccess ||
+      g_out.plan(a_out, 1, hd, Wo, (int)M, c, hd, hd, out_bf16(out, nullptr, nullptr, nullptr, c)) != cudaSuccess)
     return TRI_ATTN_ERR_CUDA;
   AttnFwdCall ac;
   rc = attn_fwd_prepare(attn_shape(shape), q, k, v, bias, mask, O, LSE, Ores, &ac);
@@ -786,7 +1003,7 @@ int tri_module_fwd(tri_module_shape shape, const tri_attn_bf16 *z, const float *
   auto st = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_ln_fwd(shape, z, gamma, beta, wb, zt, mu, rstd, bias, st);
   e = mark_ok(e, 0, st);
-  if (e == cudaSuccess) e = g_in.launch(out_bf16(q, k, v, gl, hd), status, st);
+  if (e == cudaSuccess) e = g_in.launch(status, st);
   e = mark_ok(e, 1, st);
   if (e == cudaSuccess) e = attn_fwd_enqueue(ac, 2, st);
   if (e == cudaSuccess) {
@@ -795,7 +1012,7 @@ int tri_module_fwd(tri_module_shape shape, const tri_attn_bf16 *z, const float *
     e = cudaGetLastError();
   }
   e = mark_ok(e, 4, st);
-  if (e == cudaSuccess) e = g_out.launch(out_bf16(out, nullptr, nullptr, nullptr, c), status, st);
+  if (e == cudaSuccess) e = g_out.launch(status, st);
   e = mark_ok(e, 5, st);
   return e == cudaSuccess ? TRI_ATTN_OK : TRI_ATTN_ERR_CUDA;
 }
@@ -838,39 +1055,38 @@ int tri_module_bwd(tri_module_shape shape, const tri_attn_bf16 *z, const float *
   MGemm<false, true, kOutF32> g_dzt;    // dzt[m][c] = sum_r dproj[m][r] W[r][c]
   MGemm<true, true, kOutF32> g_dw;      // dW[r][c] = sum_m dproj[m][r] zt[m][c]
   const uint16_t *a_dout[1] = {dout}, *a_proj[4] = {dq, dk, dv, dgl};
-  if (g_dgo.plan(a_dout, 1, c, Wo, (int)M, hd, c, c) != cudaSuccess ||
-      g_dwo.plan(a_dout, 1, c, go, c, hd, (int)M, L.Kc) != cudaSuccess ||
-      g_dzt.plan(a_proj, 4, hd, W, (int)M, c, 4 * hd, 4 * hd) != cudaSuccess ||
-      g_dw.plan(a_proj, 4, hd, zt, 4 * hd, c, (int)M, L.Kc) != cudaSuccess)
+  MGemmArgs gate{}, f_wo{}, f_zt{}, f_w{};
+  gate.P = O;
+  gate.G = gl;
+  gate.dP = dO;
+  gate.dG = dgl;
+  f_wo.D0 = pWo;
+  f_zt.D0 = dzt;
+  f_w.D0 = pW;
+  if (g_dgo.plan(a_dout, 1, c, Wo, (int)M, hd, c, c, gate) != cudaSuccess ||
+      g_dwo.plan(a_dout, 1, c, go, c, hd, (int)M, L.Kc, f_wo) != cudaSuccess ||
+      g_dzt.plan(a_proj, 4, hd, W, (int)M, c, 4 * hd, 4 * hd, f_zt) != cudaSuccess ||
+      g_dw.plan(a_proj, 4, hd, zt, 4 * hd, c, (int)M, L.Kc, f_w) != cudaSuccess)
     return TRI_ATTN_ERR_CUDA;
   AttnBwdCall ac;
   rc = attn_bwd_prepare(attn_shape(shape), q, k, v, bias, mask, O, Ores, LSE, dO, dq, dk, dv, dbias,
                         at<void>(workspace, L.attn), L.attn_bytes, &ac);
   if (rc) return rc;
   auto st = static_cast<cudaStream_t>(stream);
-  MGemmArgs gate{};
-  gate.P = O;
-  gate.G = gl;
-  gate.dP = dO;
-  gate.dG = dgl;
-  cudaError_t e = g_dgo.launch(gate, status, st);
+  cudaError_t e = g_dgo.launch(status, st);
   e = mark_ok(e, 0, st);
-  MGemmArgs f32{};
-  f32.D0 = pWo;
-  if (e == cudaSuccess) e = g_dwo.launch(f32, status, st);
+  if (e == cudaSuccess) e = g_dwo.launch(status, st);
   e = mark_ok(e, 1, st);
   if (e == cudaSuccess) e = launch_reduce(pWo, L.Tsplit, (int64_t)c * hd, dWo, (int64_t)c * hd, nullptr, 0, nullptr, st);
   e = mark_ok(e, 2, st);
   if (e == cudaSuccess) e = attn_bwd_enqueue(ac, 3, st);
-  f32.D0 = dzt;
-  if (e == cudaSuccess) e = g_dzt.launch(f32, status, st);
+  if (e == cudaSuccess) e = g_dzt.launch(status, st);
   e = mark_ok(e, 7, st);
   if (e == cudaSuccess) e = launch_ln_bwd(shape, L, dzt, dbias, z, zt, mu, rstd, gamma, wb, dz, pLN, st);
   e = mark_ok(e, 8, st);
   if (e == cudaSuccess) e = launch_reduce(pLN, L.nln, (int64_t)(2 + H) * c, dgamma, c, dbeta, c, dwb, st);
   e = mark_ok(e, 9, st);
-  f32.D0 = pW;
-  if (e == cudaSuccess) e = g_dw.launch(f32, status, st);
+  if (e == cudaSuccess) e = g_dw.launch(status, st);
   e = mark_ok(e, 10, st);
   if (e == cudaSuccess)
     e = launch_reduce(pW, L.Tsplit, (int64_t)4 * hd * c, dW, (int64_t)4 * hd * c, nullptr, 0, nullptr, st);
