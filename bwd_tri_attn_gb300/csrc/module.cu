@@ -661,34 +661,31 @@ __global__ void __launch_bounds__(256) mod_gate_kernel(const uint16_t *__restric
 
 // ================================================================ LayerNorm backward
 // One CTA per fixed chunk of `rpc` pair positions; lane groups as in the forward (CC / 8 lanes per
-// position, 8 channels per lane), the warps of the CTA taking the chunk's positions in turn.
-// g = dzt + sum_h dbias_h wb[h] is the full gradient of zt; with zh = (z - mean) rstd and
-// dzh = g gamma, dz = rstd (dzh - mean(dzh) - zh mean(dzh zh)). The CTA's partial sums of dgamma
-// (g zh), dbeta (g) and dwb[h] (dbias_h zt) are added over the lane groups of a warp by a fixed
-// xor-shuffle tree, then over the warps in warp order, and written to part[blockIdx.x][2 + H][CC].
+// position, 8 channels per lane), the warps of the CTA taking the chunk's positions in turn, U
+// positions per lane group at a time with their loads issued together. g = dzt + sum_h dbias_h wb[h]
+// is the full gradient of zt; with zh = (z - mean) rstd and dzh = g gamma,
+// dz = rstd (dzh - mean(dzh) - zh mean(dzh zh)). The CTA's partial sums of dgamma (g zh), dbeta (g)
+// and dwb[h] (dbias_h zt) are added over the lane groups of a warp by a fixed xor-shuffle tree, then
+// over the warps in warp order, and written to part[blockIdx.x][2 + H][CC]. gamma and wb are read
+// from shared memory (broadcast loads), which keeps the kernel at two CTAs per SM for H <= 4.
 template <int CC, int HM>
-__global__ void __launch_bounds__(256) mod_ln_bwd_kernel(const float *__restrict__ dzt, const uint16_t *__restrict__ dbias,
-                                                         const uint16_t *__restrict__ z, const uint16_t *__restrict__ zt,
-                                                         const float *__restrict__ mu, const float *__restrict__ rstd,
-                                                         const float *__restrict__ gamma, const uint16_t *__restrict__ wb,
-                                                         int H, int N, int node, int64_t M, int rpc,
-                                                         uint16_t *__restrict__ dz, float *__restrict__ part) {
+__global__ void __launch_bounds__(256, HM <= 4 ? 2 : 1) mod_ln_bwd_kernel(const float *__restrict__ dzt, const uint16_t *__restrict__ dbias,
+                                                            const uint16_t *__restrict__ z, const uint16_t *__restrict__ zt,
+                                                            const float *__restrict__ mu, const float *__restrict__ rstd,
+                                                            const float *__restrict__ gamma, const uint16_t *__restrict__ wb,
+                                                            int H, int N, int node, int64_t M, int rpc,
+                                                            uint16_t *__restrict__ dz, float *__restrict__ part) {
   using L = LnLanes<CC>;
-  __shared__ float red[(2 + HM) * CC];
+  constexpr int U = 1;  // (more positions in flight per lane group cost the second CTA per SM)
+  __shared__ __align__(16) float red[(2 + HM) * CC];
+  __shared__ __align__(16) float sw[(1 + HM) * CC];  // gamma, then wb[h] in FP32
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, sl = lane % L::LPR, rs = lane / L::LPR;
   const int gbase = lane - sl;  // first lane of this lane group
-  float gm[8], wv[HM][8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) gm[j] = gamma[sl * 8 + j];
-#pragma unroll
-  for (int h = 0; h < HM; ++h) {
-    if (h < H) {
-      unpack8(*reinterpret_cast<const uint4 *>(wb + h * CC + sl * 8), wv[h]);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) wv[h][j] = 0.f;
-    }
+  for (int i = threadIdx.x; i < (1 + HM) * CC; i += blockDim.x) {
+    const int h = i / CC - 1, cc = i % CC;
+    sw[i] = h < 0 ? gamma[cc] : (h < H ? __uint_as_float((uint32_t)wb[h * CC + cc] << 16) : 0.f);
   }
+  __syncthreads();
   float ag[8], ab[8], aw[HM][8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
@@ -698,33 +695,53 @@ __global__ void __launch_bounds__(256) mod_ln_bwd_kernel(const float *__restrict
     for (int h = 0; h < HM; ++h) aw[h][j] = 0.f;
   }
   const int64_t NN = (int64_t)N * N;
-  const uint32_t nn32 = (uint32_t)NN, n32 = (uint32_t)N;
   const int64_t r0 = (int64_t)blockIdx.x * rpc, r1 = min(M, r0 + rpc);
-  // U position groups per warp at a time, their loads issued together (bytes in flight)
-  constexpr int U = 2;
-  for (int64_t g0 = r0 + (int64_t)warp * U * L::RPW; g0 < r1; g0 += 8 * U * L::RPW) {
+  const int step = 8 * U * L::RPW;  // positions a lane group advances per iteration
+  // (b, x, y) of this lane group's U positions, advanced incrementally (positions fit 32 bits)
+  uint32_t pb[U], px[U], py[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const uint32_t m = (uint32_t)(r0 + (int64_t)warp * U * L::RPW + u * L::RPW + rs), nn = (uint32_t)NN;
+    pb[u] = m / nn;
+    px[u] = (m - pb[u] * nn) / (uint32_t)N;
+    py[u] = m - pb[u] * nn - px[u] * (uint32_t)N;
+  }
+  for (int64_t g0 = r0 + (int64_t)warp * U * L::RPW; g0 < r1; g0 += step) {
     float4 rg[U][2];
     uint4 rz[U], rt[U];
     float rdb[U], rmu[U], rr[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t m = g0 + u * L::RPW + rs;
-      const int64_t mm = m < r1 ? m : r0;  // idle lane groups shadow a live position, contributing nothing
-      const uint32_t m32 = (uint32_t)mm, b = m32 / nn32, xy = m32 - b * nn32, px = xy / n32, py = xy - px * n32;
-      const int64_t boff = node == 0 ? (int64_t)px * N + py : (int64_t)py * N + px;
-      // lane h of the group loads dbias of head h
-      rdb[u] = sl < H ? __uint_as_float((uint32_t)dbias[((int64_t)b * H + sl) * NN + boff] << 16) : 0.f;
-      rg[u][0] = *reinterpret_cast<const float4 *>(dzt + mm * CC + sl * 8);
-      rg[u][1] = *reinterpret_cast<const float4 *>(dzt + mm * CC + sl * 8 + 4);
-      rz[u] = *reinterpret_cast<const uint4 *>(z + mm * CC + sl * 8);
-      rt[u] = *reinterpret_cast<const uint4 *>(zt + mm * CC + sl * 8);
-      rmu[u] = mu[mm];
-      rr[u] = rstd[mm];
+      if (m < r1) {
+        const int64_t boff = node == 0 ? (int64_t)px[u] * N + py[u] : (int64_t)py[u] * N + px[u];
+        // lane h of the group loads dbias of head h
+        rdb[u] = sl < H ? __uint_as_float((uint32_t)dbias[((int64_t)pb[u] * H + sl) * NN + boff] << 16) : 0.f;
+        rg[u][0] = *reinterpret_cast<const float4 *>(dzt + m * CC + sl * 8);
+        rg[u][1] = *reinterpret_cast<const float4 *>(dzt + m * CC + sl * 8 + 4);
+        rz[u] = *reinterpret_cast<const uint4 *>(z + m * CC + sl * 8);
+        rt[u] = *reinterpret_cast<const uint4 *>(zt + m * CC + sl * 8);
+        rmu[u] = mu[m];
+        rr[u] = rstd[m];
+      } else {  // past the chunk: zeros, which add nothing (the group still joins the shuffles)
+        rdb[u] = 0.f;
+        rg[u][0] = rg[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        rz[u] = rt[u] = make_uint4(0u, 0u, 0u, 0u);
+        rmu[u] = 0.f;
+        rr[u] = 0.f;
+      }
+      py[u] += step;
+      while (py[u] >= (uint32_t)N) {
+        py[u] -= N;
+        if (++px[u] == (uint32_t)N) {
+          px[u] = 0;
+          ++pb[u];
+        }
+      }
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t m = g0 + u * L::RPW + rs;
-      const bool live = m < r1;
       float db[HM];
 #pragma unroll
       for (int h = 0; h < HM; ++h) db[h] = __shfl_sync(0xffffffffu, rdb[u], gbase + (h < H ? h : 0));
@@ -736,9 +753,15 @@ __global__ void __launch_bounds__(256) mod_ln_bwd_kernel(const float *__restrict
 #pragma unroll
       for (int h = 0; h < HM; ++h) {
         if (h >= H) break;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) g[j] = fmaf(db[h], wv[h][j], g[j]);
+        const float4 w0 = *reinterpret_cast<const float4 *>(sw + (1 + h) * CC + sl * 8);
+        const float4 w1 = *reinterpret_cast<const float4 *>(sw + (1 + h) * CC + sl * 8 + 4);
+        g[0] = fmaf(db[h], w0.x, g[0]), g[1] = fmaf(db[h], w0.y, g[1]), g[2] = fmaf(db[h], w0.z, g[2]);
+        g[3] = fmaf(db[h], w0.w, g[3]), g[4] = fmaf(db[h], w1.x, g[4]), g[5] = fmaf(db[h], w1.y, g[5]);
+        g[6] = fmaf(db[h], w1.z, g[6]), g[7] = fmaf(db[h], w1.w, g[7]);
       }
+      const float4 g0v = *reinterpret_cast<const float4 *>(sw + sl * 8);
+      const float4 g1v = *reinterpret_cast<const float4 *>(sw + sl * 8 + 4);
+      const float gm[8] = {g0v.x, g0v.y, g0v.z, g0v.w, g1v.x, g1v.y, g1v.z, g1v.w};
       const float mean = rmu[u], r = rr[u];
       float zh[8], dzh[8], s1 = 0.f, s2 = 0.f;
 #pragma unroll
@@ -750,19 +773,20 @@ __global__ void __launch_bounds__(256) mod_ln_bwd_kernel(const float *__restrict
       }
       s1 = group_sum<L::LPR>(s1) * (1.f / CC);
       s2 = group_sum<L::LPR>(s2) * (1.f / CC);
-      if (live) {
+      if (m < r1) {
         uint32_t ow[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j)
           ow[j] = pack_bf16x2(r * (dzh[2 * j] - s1 - zh[2 * j] * s2), r * (dzh[2 * j + 1] - s1 - zh[2 * j + 1] * s2));
         *reinterpret_cast<uint4 *>(dz + m * CC + sl * 8) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+      }
+      // (positions past the chunk carry zeros: they add nothing)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          ag[j] = fmaf(g[j], zh[j], ag[j]);
-          ab[j] += g[j];
+      for (int j = 0; j < 8; ++j) {
+        ag[j] = fmaf(g[j], zh[j], ag[j]);
+        ab[j] += g[j];
 #pragma unroll
-          for (int h = 0; h < HM; ++h) aw[h][j] = fmaf(db[h], tv[j], aw[h][j]);
-        }
+        for (int h = 0; h < HM; ++h) aw[h][j] = fmaf(db[h], tv[j], aw[h][j]);
       }
     }
   }
