@@ -16,7 +16,7 @@
 // Backward:
 //   GEMM + gate epilogue  dgo = dout Wo; the epilogue writes dO = dgo s and dgl = dgo O s (1 - s)
 //                         (s = sigmoid(gl)): dgo never reaches memory
-//   GEMM (split over M)   dWo partials = dout^T go, then an ordered sum over the splits
+//   GEMM (split over M)   dWo partials = dout^T go, then a fixed-order sum over the splits
 //   attention             tri_attn backward -> dq, dk, dv, dbias
 //   GEMM                  dzt = [dq | dk | dv | dgl] W (FP32), the four tensors read as one K-segmented operand
 //   mod_ln_bwd_kernel     dzt + dbias wb -> dz; per-CTA partial sums of dgamma, dbeta, dwb
@@ -28,7 +28,7 @@
 // transposed operand mode, [K][rows]); one operand may be split into up to four tensors along K
 // (K-major) or M (MN-major), so [dq | dk | dv | dgl] is read where the attention left it. Products
 // summed over the pair positions split K into fixed chunks of rows; each chunk's FP32 partial is
-// written out and the partials are added in chunk order, so every weight gradient is the same
+// written out and the partials are added in a fixed order, so every weight gradient is the same
 // bits on every call.
 #include <math.h>
 
@@ -597,10 +597,29 @@ __global__ void __launch_bounds__(256) mod_ln_fwd_kernel(const uint16_t *__restr
       const int64_t m = (g + u) * L::RPW + rs;
       raw[u] = m < M ? *reinterpret_cast<const uint4 *>(z + m * CC + sl * 8) : make_uint4(0u, 0u, 0u, 0u);
     }
+    // (b, x, y) of the first group's position by division, the others by stepping (positions and
+    // N^2 fit 32 bits: B N <= 65535, N <= 1024)
+    uint32_t pb, px, py;
+    {
+      const uint32_t m32 = (uint32_t)(g * L::RPW + rs);
+      pb = m32 / nn32;
+      px = (m32 - pb * nn32) / n32;
+      py = m32 - pb * nn32 - px * n32;
+    }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t m = (g + u) * L::RPW + rs;
       const bool live = m < M;  // (lane groups past the last position idle, but join the shuffles)
+      if (u > 0) {
+        py += L::RPW;  // (RPW <= 4 < N: at most one carry)
+        if (py >= n32) {
+          py -= n32;
+          if (++px == n32) {
+            px = 0;
+            ++pb;
+          }
+        }
+      }
       float x[8];
       unpack8(raw[u], x);
       float s = 0.f;
@@ -627,8 +646,6 @@ __global__ void __launch_bounds__(256) mod_ln_fwd_kernel(const uint16_t *__restr
           rstd[m] = r;
         }
       }
-      // (b, x, y) of the position; positions and N^2 fit 32 bits (B N <= 65535, N <= 1024)
-      const uint32_t m32 = (uint32_t)m, b = m32 / nn32, xy = m32 - b * nn32, px = xy / n32, py = xy - px * n32;
       const int64_t boff = node == 0 ? (int64_t)px * N + py : (int64_t)py * N + px;
       float p[HM];
 #pragma unroll
@@ -640,7 +657,7 @@ __global__ void __launch_bounds__(256) mod_ln_fwd_kernel(const uint16_t *__restr
       const float ph = group_sum_scatter<L::LPR, HM>(p, sl);
       const int hh = head_of_lane<L::LPR, HM>(sl);
       if (live && hh < H && (sl & (L::LPR / HM - 1)) == 0)
-        bias[((int64_t)b * H + hh) * NN + boff] = (uint16_t)(pack_bf16x2(ph, 0.f) & 0xffffu);
+        bias[((int64_t)pb * H + hh) * NN + boff] = (uint16_t)(pack_bf16x2(ph, 0.f) & 0xffffu);
     }
   }
 }
@@ -821,19 +838,37 @@ __global__ void __launch_bounds__(256, HM <= 4 ? 2 : 1) mod_ln_bwd_kernel(const 
 }
 
 // ================================================================ ordered sum of partials
-// out[i] = sum over t = 0, 1, ..., T - 1 of part[t][i] (in that order), for i < n; the result is
-// written in up to three pieces: i < n0 to o0, i < n0 + n1 to o1, the rest to o2.
+// out[i] = sum over t of part[t][i], for i < n, in a fixed order: a CTA takes 32 consecutive i
+// (threadIdx.x) and 8 lanes of t (threadIdx.y); lane y adds t = y, y + 8, y + 16, ... in increasing
+// t, then the 8 lane sums are added in lane order. The result is written in up to three pieces:
+// i < n0 to o0, i < n0 + n1 to o1, the rest to o2.
 __global__ void __launch_bounds__(256) mod_reduce_kernel(const float *__restrict__ part, int T, int64_t n, float *o0,
                                                          int64_t n0, float *o1, int64_t n1, float *o2) {
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-    float s = 0.f;
-    for (int t = 0; t < T; ++t) s += part[(int64_t)t * n + i];
+  __shared__ float acc[8][33];
+  const int tx = threadIdx.x, ty = threadIdx.y;
+  const int64_t i = (int64_t)blockIdx.x * 32 + tx;
+  float s = 0.f;
+  if (i < n) {
+    int t = ty;
+    for (; t + 24 < T; t += 32) {  // four loads in flight, added in t order
+      const float a0 = part[(int64_t)t * n + i], a1 = part[(int64_t)(t + 8) * n + i];
+      const float a2 = part[(int64_t)(t + 16) * n + i], a3 = part[(int64_t)(t + 24) * n + i];
+      s = (((s + a0) + a1) + a2) + a3;
+    }
+    for (; t < T; t += 8) s += part[(int64_t)t * n + i];
+  }
+  acc[ty][tx] = s;
+  __syncthreads();
+  if (ty == 0 && i < n) {
+    float r = acc[0][tx];
+#pragma unroll
+    for (int y = 1; y < 8; ++y) r += acc[y][tx];
     if (i < n0)
-      o0[i] = s;
+      o0[i] = r;
     else if (i < n0 + n1)
-      o1[i - n0] = s;
+      o1[i - n0] = r;
     else
-      o2[i - n0 - n1] = s;
+      o2[i - n0 - n1] = r;
   }
 }
 
@@ -969,8 +1004,8 @@ cudaError_t launch_ln_bwd(const tri_module_shape &s, const BwdLayout &L, const f
 
 cudaError_t launch_reduce(const float *part, int T, int64_t n, float *o0, int64_t n0, float *o1, int64_t n1, float *o2,
                           cudaStream_t st) {
-  const int grid = (int)std::min<int64_t>((n + 255) / 256, 152 * 8);
-  mod_reduce_kernel<<<grid, 256, 0, st>>>(part, T, n, o0, n0, o1 ? o1 : o0, n1, o2 ? o2 : o0);
+  mod_reduce_kernel<<<(unsigned)((n + 31) / 32), dim3(32, 8), 0, st>>>(part, T, n, o0, n0, o1 ? o1 : o0, n1,
+                                                                      o2 ? o2 : o0);
   return cudaGetLastError();
 }
 
