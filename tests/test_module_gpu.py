@@ -71,6 +71,15 @@ def test_channel_and_head_variants(c, H, d, node):
     _check(got, _oracle(x, H, d, node, False), _oracle(x, H, d, node, True))
 
 
+@pytest.mark.parametrize("B,N,node", [(1, 37, 0), (2, 21, 1), (3, 16, 0)])
+def test_odd_and_batched_shapes(B, N, node):
+    """N not a multiple of 8 (the attention's per-thread bias staging, positions not a multiple of
+    the GEMM and store tiles), several batches on either node, the smallest N."""
+    x = wl.make_module_inputs(B, N, 128, 4, 32, seed=200 + N, mask=("random", 0.2))
+    got = _run_cuda(x, 4, 32, node)
+    _check(got, _oracle(x, 4, 32, node, False), _oracle(x, 4, 32, node, True))
+
+
 def test_crop384_full_oracle():
     w = wl.MOD_CROP384
     x = wl.module_inputs_for(w)
