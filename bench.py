@@ -740,7 +740,8 @@ def main():
     ap.add_argument("--workload", default=wl.CROP768.name, choices=sorted(wl.ALL))
     ap.add_argument("--node", choices=["starting", "ending"], default="starting",
                     help="which pair axis holds the slices (the ending node reads the pair tensors in place)")
-    ap.add_argument("--cpu-slices", type=int, default=64, help="slices in the timed CPU oracle sample")
+    ap.add_argument("--cpu-slices", type=int, default=384,
+                    help="slices in the timed CPU oracle sample (about 10 s of host work at crop 768)")
     ap.add_argument("--ref-slices", type=int, default=4, help="slices per step of the reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
