@@ -76,7 +76,12 @@ typedef struct tri_module_shape {
  */
 size_t tri_module_saved_size(tri_module_shape shape);
 
-/* Bytes of device workspace tri_module_bwd needs; 0 for a bad shape. */
+/*
+ * Bytes of device workspace tri_module_bwd needs for `shape` on the current
+ * device (it includes the attention backward's workspace, whose size depends on
+ * the device's SM count). Returns 0 for an unsupported shape or when the device
+ * cannot be queried.
+ */
 size_t tri_module_bwd_workspace_size(tri_module_shape shape);
 
 /*
