@@ -37,7 +37,9 @@
  * fixed shape and GPU model: every reduction (the attention's, the weight
  * gradients' sums over positions, the LayerNorm parameter gradients) runs in a
  * fixed order. Kernels never trap; a bounded device wait that expires records
- * TRI_ATTN_ERR_TIMEOUT for tri_attn_device_status().
+ * TRI_ATTN_ERR_TIMEOUT for tri_attn_device_status(). The first call of each
+ * entry point on a device does one-time host set-up (kernel attributes, the
+ * attention backward's occupancy query); make it before any stream capture.
  *
  * Timing: with tri_attn_set_timing_events(), the k-th event is recorded after
  * the k-th kernel of a call. Forward: 0 LayerNorm and pair bias, 1 input
