@@ -8,8 +8,8 @@
 //
 // Forward (M = B N^2 pair positions, hd = H d):
 //   mod_ln_fwd_kernel     z -> zt (BF16), mean, 1/std; pair bias zt . wb (transposed for the ending node)
-//   GEMM                  zt W^T -> q | k | v | gl (one product, the epilogue routes each 128- or
-//                         64-column block to its tensor)
+//   GEMM                  zt W^T -> q | k | v | gl (one product, the epilogue routes each 32-column
+//                         chunk to its tensor)
 //   attention             tri_attn forward on q, k, v, bias, mask
 //   mod_gate_kernel       go = sigmoid(gl) O
 //   GEMM                  go Wo^T -> out
@@ -20,11 +20,12 @@
 //   attention             tri_attn backward -> dq, dk, dv, dbias
 //   GEMM                  dzt = [dq | dk | dv | dgl] W (FP32), the four tensors read as one K-segmented operand
 //   mod_ln_bwd_kernel     dzt + dbias wb -> dz; per-CTA partial sums of dgamma, dbeta, dwb
-//   GEMM (split over M)   dW partials = [dq | dk | dv | dgl]^T zt, then ordered sums
+//   GEMM (split over M)   dW partials = [dq | dk | dv | dgl]^T zt, then a fixed-order sum
 //
 // The GEMM is one persistent tcgen05 kernel for every product: M = 128 x N = 128 or 256 tiles (the
 // narrower for products at most 128 wide), K steps of 64 through a TMA ring, two TMEM
-// accumulators so that one tile's epilogue overlaps the next tile's main loop. Operands are K-major (row-major [rows][K]) or MN-major (the
+// accumulators so that one tile's epilogue overlaps the next tile's main loop, BF16 and FP32
+// outputs leaving through TMA stores. Operands are K-major (row-major [rows][K]) or MN-major (the
 // transposed operand mode, [K][rows]); one operand may be split into up to four tensors along K
 // (K-major) or M (MN-major), so [dq | dk | dv | dgl] is read where the attention left it. Products
 // summed over the pair positions split K into fixed chunks of rows; each chunk's FP32 partial is
@@ -62,7 +63,7 @@ struct MGemmArgs {
   int M, N, K, Kc, T;     // D[t][m][n] = sum over k in [t Kc, min(K, t Kc + Kc)) of A(m, k) B(n, k)
   int segA, nsegA;        // A's tensors hold segA elements each along K (K-major A) or M (MN-major A)
   void *D0, *D1, *D2, *D3;  // kOutBF16: column segments of segD columns, row stride segD; kOutF32: [T][M][N]
-  int segD;
+  int segD;               // (the outputs' tensor maps are built from these at plan time)
   const uint16_t *P, *G;  // kOutGate: [M][N] attention output and gate logits
   uint16_t *dP, *dG;      // kOutGate: [M][N] their gradients
 };
@@ -105,10 +106,8 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t sr
 
 // The gate epilogue's 8 consecutive values v = dgo of row m, columns n .. n + 7, with the attention
 // output pv and gate logits gv there: dP = dgo s and dG = dgo O s (1 - s), s = sigmoid(gl).
-template <int kOut>
-__device__ __forceinline__ void mgemm_store8(const MGemmArgs &a, int, int m, int n, const float (&v)[8],
-                                             const uint4 &pv, const uint4 &gv) {
-  static_assert(kOut == kOutGate, "BF16 and FP32 outputs leave through TMA stores");
+__device__ __forceinline__ void gate_store8(const MGemmArgs &a, int m, int n, const float (&v)[8], const uint4 &pv,
+                                            const uint4 &gv) {
   const int64_t off = (int64_t)m * a.N + n;
   const uint32_t pw[4] = {pv.x, pv.y, pv.z, pv.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
   uint32_t od[4], og[4];
@@ -360,7 +359,7 @@ __global__ void __launch_bounds__(MGemmCfg<BN, kOut>::NTHREADS, 1)
               float v[8];
 #pragma unroll
               for (int j = 0; j < 8; ++j) v[j] = stg[(rq + 8 * i) * C::EPI_PITCH + 8 * cq + j];
-              if (mrow + 8 * i < a.M && col < a.N) mgemm_store8<kOut>(a, t, mrow + 8 * i, col, v, pv[k][i], gv[k][i]);
+              if (mrow + 8 * i < a.M && col < a.N) gate_store8(a, mrow + 8 * i, col, v, pv[k][i], gv[k][i]);
             }
             __syncwarp();
           }
