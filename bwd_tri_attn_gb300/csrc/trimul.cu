@@ -135,7 +135,8 @@ __global__ void __launch_bounds__(kGateThreads) trimul_gate_kernel(const GateArg
 // (s, r): the inverse of the gating kernel's layout change. One CTA: 16 x 16 positions and up to
 // 32 channels of one operand. dA rows (c, r) of 16 FP32 values are read with 16-byte loads into
 // shared memory [channel][r][s] (channel stride 289 words, row pitch 17); each thread then takes
-// 8 channels of one position and writes 16 bytes of dP and of dG.
+// 8 channels of one position and writes 16 bytes of dP and of dG. Its P and G chunks are loaded
+// before the dA tile, so that both loads' latencies overlap.
 constexpr int kGbCG = 32, kGbRowW = 17, kGbChW = 289;
 constexpr int kGbSmem = kGbCG * kGbChW * 4;
 
@@ -152,6 +153,28 @@ __global__ void __launch_bounds__(kGateThreads) trimul_gate_bwd_kernel(const Gat
   tile_of(g.N, g.groups, op, grp, b, r0, s0);
   const int N = g.N, C = g.C, c0 = grp * kGbCG, nq = min(kGbCG, C - c0) / 8;
   const float *dA = op ? g.dA[1] : g.dA[0];
+  const uint4 *P = reinterpret_cast<const uint4 *>(op ? g.P[1] : g.P[0]),
+              *G = reinterpret_cast<const uint4 *>(op ? g.G[1] : g.G[0]);
+  uint4 *dP = reinterpret_cast<uint4 *>(op ? g.dP[1] : g.dP[0]), *dG = reinterpret_cast<uint4 *>(op ? g.dG[1] : g.dG[0]);
+  const int64_t cv = C / 8;
+  // this thread's P and G chunks (8 channels of one position, four positions) are requested
+  // first, so that their latency overlaps the dA loads and the barrier
+  constexpr int kIt = kGateT * kGateT * 4 / kGateThreads;
+  uint4 pv[kIt], gv[kIt];
+  int64_t idx[kIt];
+#pragma unroll
+  for (int it = 0; it < kIt; ++it) {
+    const int e = threadIdx.x + it * kGateThreads;
+    const int q = e & 3, sl = (e >> 2) & 15, rl = e >> 6;
+    const int r = r0 + rl, s = s0 + sl;
+    idx[it] = -1;
+    if (q < nq && r < N && s < N) {
+      const int64_t pos = g.transposed ? ((int64_t)b * N + s) * N + r : ((int64_t)b * N + r) * N + s;
+      idx[it] = pos * cv + c0 / 8 + q;
+      pv[it] = P[idx[it]];
+      gv[it] = G[idx[it]];
+    }
+  }
 #pragma unroll
   for (int e = threadIdx.x; e < kGbCG * kGateT * 4; e += kGateThreads) {
     const int qt = e & 3, rl = (e >> 2) & 15, cl = e >> 6;
@@ -163,19 +186,12 @@ __global__ void __launch_bounds__(kGateThreads) trimul_gate_bwd_kernel(const Gat
     dst[0] = v.x, dst[1] = v.y, dst[2] = v.z, dst[3] = v.w;
   }
   __syncthreads();
-  const uint4 *P = reinterpret_cast<const uint4 *>(op ? g.P[1] : g.P[0]),
-              *G = reinterpret_cast<const uint4 *>(op ? g.G[1] : g.G[0]);
-  uint4 *dP = reinterpret_cast<uint4 *>(op ? g.dP[1] : g.dP[0]), *dG = reinterpret_cast<uint4 *>(op ? g.dG[1] : g.dG[0]);
-  const int64_t cv = C / 8;
 #pragma unroll
-  for (int e = threadIdx.x; e < kGateT * kGateT * 4; e += kGateThreads) {
+  for (int it = 0; it < kIt; ++it) {
+    if (idx[it] < 0) continue;
+    const int e = threadIdx.x + it * kGateThreads;
     const int q = e & 3, sl = (e >> 2) & 15, rl = e >> 6;
-    const int r = r0 + rl, s = s0 + sl;
-    if (q >= nq || r >= N || s >= N) continue;
-    const int64_t pos = g.transposed ? ((int64_t)b * N + s) * N + r : ((int64_t)b * N + r) * N + s;
-    const int64_t idx = pos * cv + c0 / 8 + q;
-    const uint4 pv = P[idx], gv = G[idx];
-    const uint32_t pw[4] = {pv.x, pv.y, pv.z, pv.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
+    const uint32_t pw[4] = {pv[it].x, pv[it].y, pv[it].z, pv[it].w}, gw[4] = {gv[it].x, gv[it].y, gv[it].z, gv[it].w};
     const float *src = tf + (8 * q) * kGbChW + rl * kGbRowW + sl;
     uint32_t op_[4], og[4];
 #pragma unroll
@@ -185,8 +201,8 @@ __global__ void __launch_bounds__(kGateThreads) trimul_gate_bwd_kernel(const Gat
       op_[w] = pack_bf16x2(d0 * sg0, d1 * sg1);
       og[w] = pack_bf16x2(d0 * bf16_lo(pw[w]) * (sg0 * (1.f - sg0)), d1 * bf16_hi(pw[w]) * (sg1 * (1.f - sg1)));
     }
-    dP[idx] = make_uint4(op_[0], op_[1], op_[2], op_[3]);
-    dG[idx] = make_uint4(og[0], og[1], og[2], og[3]);
+    dP[idx[it]] = make_uint4(op_[0], op_[1], op_[2], op_[3]);
+    dG[idx[it]] = make_uint4(og[0], og[1], og[2], og[3]);
   }
 }
 
