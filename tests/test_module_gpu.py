@@ -80,6 +80,27 @@ def test_odd_and_batched_shapes(B, N, node):
     _check(got, _oracle(x, 4, 32, node, False), _oracle(x, 4, 32, node, True))
 
 
+def test_magnitudes():
+    """Output gradients at 2^-20 (the attention's operand scaling and the block's FP32 sums at tiny
+    magnitudes), a common offset of 64 in z (the LayerNorm's centring), W and Wo times 2, and
+    LayerNorm eps 1e-3."""
+    x = wl.make_module_inputs(1, 48, 128, 4, 32, seed=300, mask=("tail", 4))
+    x["dout"] = (x["dout"].float() * 2.0 ** -20).bfloat16()
+    x["z"] = (x["z"].float() + 64.0).bfloat16()
+    x["W"] = (x["W"].float() * 2.0).bfloat16()
+    x["Wo"] = (x["Wo"].float() * 2.0).bfloat16()
+    dev = {k: (None if v is None else v.cuda()) for k, v in x.items()}
+    args = [dev[k] for k in KEYS]
+    out, saved = tb.module_forward(*args, dev["mask"], 4, 32, eps=1e-3)
+    grads = tb.module_backward(*args, dev["mask"], saved, dev["dout"], 4, 32, eps=1e-3)
+    torch.cuda.synchronize()
+    assert tb.tri_attn_device_status() == 0
+    got = {k: t.detach().float().cpu().double().numpy() for k, t in zip(OUTS, (out,) + tuple(grads))}
+    ex = om.bwd(*[x[k] for k in KEYS], x["mask"], x["dout"], 4, 32, eps=1e-3)
+    mi = om.bwd(*[x[k] for k in KEYS], x["mask"], x["dout"], 4, 32, eps=1e-3, bf16=True)
+    _check(got, {k: ex[k] for k in OUTS}, {k: mi[k] for k in OUTS})
+
+
 def test_crop384_full_oracle():
     w = wl.MOD_CROP384
     x = wl.module_inputs_for(w)
