@@ -63,9 +63,11 @@ def test_block_matches_oracle(w):
     _check(got, _oracle(x, w.H, w.d, w.node, False), _oracle(x, w.H, w.d, w.node, True))
 
 
-@pytest.mark.parametrize("c,H,d,node", [(64, 4, 16, 0), (256, 2, 32, 1), (128, 8, 16, 0), (256, 8, 32, 0)])
+@pytest.mark.parametrize("c,H,d,node", [(64, 4, 16, 0), (256, 2, 32, 1), (128, 8, 16, 0), (256, 8, 32, 0),
+                                         (128, 6, 32, 1)])
 def test_channel_and_head_variants(c, H, d, node):
-    """Every LayerNorm width, H d from 64 to 256, both nodes, on a ragged N."""
+    """Every LayerNorm width, H d from 64 to 256, both nodes, on a ragged N; H d = 192 puts the
+    boundaries of the projections' four tensors inside GEMM tiles and between operand boxes."""
     x = wl.make_module_inputs(1, 40, c, H, d, seed=100 + c + H, mask=("tail", 3))
     got = _run_cuda(x, H, d, node)
     _check(got, _oracle(x, H, d, node, False), _oracle(x, H, d, node, True))
