@@ -671,9 +671,11 @@ def run_ours(args, w):
 
         e2e_run(2)
         torch.cuda.synchronize()
-        # three windows of ke pipelined steps, each bracketed by a barrier and a synchronisation;
-        # the median window is reported (the pipeline's fill and drain are inside every window)
-        ke = max(2, min(K, 40))
+        # three windows of ke pipelined steps (as many as the device-side windows, at least 40), each
+        # bracketed by a barrier and a synchronisation; the median window is reported. Every window
+        # contains the pipeline's fill (the first step's input copy, not overlapped) and drain (the
+        # last step's gradient copy), about 5 ms at crop 768, which a long training run amortises.
+        ke = max(K, 40)
         e_windows = []
         for _ in range(3):
             if world > 1:
