@@ -68,3 +68,47 @@ def test_two_host_threads_match_single_thread():
                 assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
     torch.cuda.synchronize()
     assert tb.tri_attn_device_status() == 0
+
+
+def _run_module(tb, x, H, d, node, stream):
+    keys = ("z", "gamma", "beta", "W", "wb", "Wo")
+    with torch.cuda.stream(stream):
+        out, saved = tb.module_forward(*[x[k] for k in keys], x["mask"], H, d, node=node, stream=stream)
+        g = tb.module_backward(*[x[k] for k in keys], x["mask"], saved, x["dout"], H, d, node=node, stream=stream)
+    stream.synchronize()
+    return [out, *g]
+
+
+def test_two_host_threads_run_the_block_as_one_thread():
+    """The triangle-attention block from two host threads at once, on two shapes that take different
+    GEMM tile widths, LayerNorm templates and nodes (when no earlier call in the process has done
+    so, their one-time per-device set-up runs inside the threads), bit for bit the single-threaded
+    results."""
+    from bwd_tri_attn_gb300 import binding as tb
+
+    cases = [(wl.make_module_inputs(1, 56, 128, 4, 32, seed=61, mask=("tail", 3)), 4, 32, 0),
+             (wl.make_module_inputs(2, 40, 256, 8, 16, seed=62, mask=("random", 0.1)), 8, 16, 1)]
+    dev = [({k: (None if v is None else v.cuda()) for k, v in x.items()}, H, d, node) for x, H, d, node in cases]
+    for _ in range(2):
+        out = [None, None]
+        errs = []
+
+        def worker(i):
+            try:
+                x, H, d, node = dev[i]
+                out[i] = _run_module(tb, x, H, d, node, torch.cuda.Stream())
+            except Exception as e:  # reported below
+                errs.append(e)
+
+        ts = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+        for t in ts:
+            t.start()
+        for t in ts:
+            t.join()
+        assert not errs, errs
+        ref = [_run_module(tb, x, H, d, node, torch.cuda.Stream()) for x, H, d, node in dev]
+        for i in range(2):
+            for a, b in zip(ref[i], out[i]):
+                assert torch.equal(a.contiguous().view(torch.uint8), b.contiguous().view(torch.uint8))
+    torch.cuda.synchronize()
+    assert tb.tri_attn_device_status() == 0
