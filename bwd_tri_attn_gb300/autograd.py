@@ -6,6 +6,9 @@ expects. There is no CPU path: the library raises if it is missing or a call fai
 
 - ``triangle_attention(Q, K, V, bias, mask=None, node=NODE_STARTING)``: the attention core
   (include/tri_attn.h) with its residual-compensated backward; gradients for Q, K, V and bias.
+- ``triangle_multiplication(Pa, Ga, Pb, Gb, incoming=False, layout=LAYOUT_PAIR)``: the triangle
+  multiplicative update (include/tri_mul.h); X channel-major [B, C, N, N], gradients for the four
+  projections in their layout.
 - ``triangle_attention_block(z, gamma, beta, W, wb, Wo, mask, H, d, node, eps)`` and
   ``TriangleAttentionBlock``: the surrounding block (include/tri_module.h). The weights may be FP32
   masters: the forward uses their BF16 rounding (as mixed-precision training does) and the
@@ -40,6 +43,29 @@ def triangle_attention(Q, K, V, bias, mask=None, node=tb.NODE_STARTING):
     """O of the attention core for BF16 CUDA tensors Q, K, V [B, S, N, H, d] (starting node; the
     ending node takes [B, N, S, H, d] in place), bias [B, H, N, N], mask [B, S, N] or None."""
     return _TriangleAttention.apply(Q, K, V, bias, mask, node)
+
+
+class _TriangleMultiplication(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, Pa, Ga, Pb, Gb, incoming, layout):
+        X, A, Bm = tb.mul_forward(Pa, Ga, Pb, Gb, incoming=incoming, layout=layout)
+        ctx.cfg = (incoming, layout)
+        ctx.save_for_backward(Pa, Ga, Pb, Gb, A, Bm)
+        return X
+
+    @staticmethod
+    def backward(ctx, dX):
+        Pa, Ga, Pb, Gb, A, Bm = ctx.saved_tensors
+        incoming, layout = ctx.cfg
+        grads = tb.mul_backward(Pa, Ga, Pb, Gb, A, Bm, dX.to(torch.bfloat16).contiguous(), incoming=incoming,
+                                layout=layout)
+        return (*grads, None, None)
+
+
+def triangle_multiplication(Pa, Ga, Pb, Gb, incoming=False, layout=tb.LAYOUT_PAIR):
+    """X [B, C, N, N] of the triangle multiplicative update for BF16 CUDA projections and gate
+    logits (layout LAYOUT_PAIR: [B, N, N, C]; LAYOUT_CHANNEL_MAJOR: [B, C, N, N])."""
+    return _TriangleMultiplication.apply(Pa, Ga, Pb, Gb, incoming, layout)
 
 
 class _TriangleAttentionBlock(torch.autograd.Function):

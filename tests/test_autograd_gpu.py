@@ -52,3 +52,20 @@ def test_block_module_matches_direct_calls():
     for p, ref in zip((m.gamma, m.beta, m.W, m.wb, m.Wo), grads[1:]):
         assert p.grad.dtype == torch.float32 and _eq(p.grad, ref)
     assert tb.tri_attn_device_status() == 0
+
+
+@pytest.mark.parametrize("incoming,layout", [(False, 0), (True, 1)])
+def test_multiplication_function_matches_direct_calls(incoming, layout):
+    m = {k: v.cuda() for k, v in wl.make_mul_inputs(1, 72, 24, seed=90).items()}
+    if layout == tb.LAYOUT_CHANNEL_MAJOR:
+        m = {k: (v.permute(0, 3, 1, 2).contiguous() if k != "dX" else v) for k, v in m.items()}
+    leaves = {k: m[k].clone().requires_grad_(True) for k in ("Pa", "Ga", "Pb", "Gb")}
+    X = ag.triangle_multiplication(leaves["Pa"], leaves["Ga"], leaves["Pb"], leaves["Gb"], incoming, layout)
+    X.backward(m["dX"])
+    X2, A, Bm = tb.mul_forward(m["Pa"], m["Ga"], m["Pb"], m["Gb"], incoming=incoming, layout=layout)
+    g = tb.mul_backward(m["Pa"], m["Ga"], m["Pb"], m["Gb"], A, Bm, m["dX"], incoming=incoming, layout=layout)
+    torch.cuda.synchronize()
+    assert _eq(X.detach(), X2)
+    for name, ref in zip(("Pa", "Ga", "Pb", "Gb"), g):
+        assert _eq(leaves[name].grad, ref), name
+    assert tb.tri_attn_device_status() == 0
