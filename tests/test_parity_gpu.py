@@ -1,6 +1,6 @@
 """GPU parity: the CUDA path against the FP64 oracle, element by element.
 
-Gate (the benchmark spec): relative RMSE <= 2e-3 for O, dQ, dK, dV and dBias; LSE to
+Gate: relative RMSE <= 2e-3 for O, dQ, dK, dV and dBias; LSE to
 FP32 accuracy; residual compensation lowers dQ, dK and dBias error; all
 outputs bitwise identical across repeated calls. Beside the RMSE, every
 compared element must lie within one BF16 ulp of the oracle plus a small
