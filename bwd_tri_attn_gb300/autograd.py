@@ -2,7 +2,8 @@
 
 Every forward and backward step runs in the library's kernels through ``binding``; these classes
 only keep the tensors the backward pass needs and hand gradients back in the dtypes autograd
-expects. There is no CPU path: the library raises if it is missing or a call fails.
+expects. There is no CPU path: the library raises if it is missing or a call fails. The backward
+passes are differentiable once (no second derivatives).
 
 - ``triangle_attention(Q, K, V, bias, mask=None, node=NODE_STARTING)``: the attention core
   (include/tri_attn.h) with its residual-compensated backward; gradients for Q, K, V and bias.
@@ -19,6 +20,7 @@ from __future__ import annotations
 import math
 
 import torch
+from torch.autograd.function import once_differentiable
 
 from . import binding as tb
 
@@ -32,6 +34,7 @@ class _TriangleAttention(torch.autograd.Function):
         return O
 
     @staticmethod
+    @once_differentiable
     def backward(ctx, dO):
         Q, K, V, bias, mask, O, Ores, LSE = ctx.saved_tensors
         dQ, dK, dV, dBias = tb.backward(Q, K, V, bias, mask, O, Ores, LSE,
@@ -54,6 +57,7 @@ class _TriangleMultiplication(torch.autograd.Function):
         return X
 
     @staticmethod
+    @once_differentiable
     def backward(ctx, dX):
         Pa, Ga, Pb, Gb, A, Bm = ctx.saved_tensors
         incoming, layout = ctx.cfg
@@ -79,6 +83,7 @@ class _TriangleAttentionBlock(torch.autograd.Function):
         return out
 
     @staticmethod
+    @once_differentiable
     def backward(ctx, dout):
         z, g32, b32, W, wb, Wo, mask, saved = ctx.saved_tensors
         H, d, node, eps, dtypes = ctx.meta

@@ -69,3 +69,14 @@ def test_multiplication_function_matches_direct_calls(incoming, layout):
     for name, ref in zip(("Pa", "Ga", "Pb", "Gb"), g):
         assert _eq(leaves[name].grad, ref), name
     assert tb.tri_attn_device_status() == 0
+
+
+def test_second_derivative_is_refused():
+    x = {k: (None if v is None else v.cuda()) for k, v in
+         wl.make_inputs(B=1, S=16, N=40, H=1, d=16, seed=95).items()}
+    q = x["Q"].clone().requires_grad_(True)
+    O = ag.triangle_attention(q, x["K"], x["V"], x["bias"], None)
+    (gq,) = torch.autograd.grad(O, q, x["dO"], create_graph=True)
+    with pytest.raises(RuntimeError):
+        gq.float().sum().backward()
+    assert tb.tri_attn_device_status() == 0
