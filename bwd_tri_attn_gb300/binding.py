@@ -132,8 +132,50 @@ def shape_of(Q: torch.Tensor, scale: float | None = None, node: int = NODE_START
     return Shape(B, S, N, H, d, float(1.0 / math.sqrt(d) if scale is None else scale), int(node))
 
 
-def _p(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+def _nbytes(t):
+    return 0 if t is None else t.numel() * t.element_size()
+
+
+_BF16, _F32 = torch.bfloat16, torch.float32
+
+
+def _arg(t, name, dtype, numel, nullable=False):
+    """Checks tensor argument `name` for what the C ABI cannot check on a bare pointer: dtype,
+    contiguity and the element count the shape implies (None: any). Returns it for _ptrs, which
+    checks the devices once every argument has passed these checks."""
+    if t is None:
+        if nullable:
+            return None
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor, got {type(t).__name__}")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{name} has {t.numel()} elements, the shape needs {numel}")
+    return (name, t)
+
+
+def _ptrs(*checked):
+    """Device pointers of arguments that passed _arg: each a CUDA tensor on the current device (a
+    wrong tensor raises here instead of being read or written out of bounds)."""
+    out = []
+    for c in checked:
+        if c is None:
+            out.append(None)
+            continue
+        name, t = c
+        if not t.is_cuda or t.device.index != torch.cuda.current_device():
+            raise ValueError(f"{name} must be a CUDA tensor on the current device, got {t.device}")
+        out.append(ctypes.c_void_p(t.data_ptr()))
+    return out
+
+
+def _attn_counts(shape):
+    pair = shape.B * shape.S * shape.N * shape.H * shape.d
+    return pair, shape.B * shape.H * shape.N * shape.N, shape.B * shape.S * shape.N, shape.B * shape.S * shape.H * shape.N
 
 
 def _stream(stream):
@@ -148,8 +190,11 @@ def _check(fn, rc):
 
 
 def tri_attn_fwd(shape: Shape, Q, K, V, bias, mask, O, LSE, Ores, stream=None):
-    rc = load().tri_attn_fwd(shape, _p(Q), _p(K), _p(V), _p(bias), _p(mask), _p(O), _p(LSE), _p(Ores),
-                             _stream(stream))
+    pair, nb, nm, nl = _attn_counts(shape)
+    ptrs = _ptrs(_arg(Q, "Q", _BF16, pair), _arg(K, "K", _BF16, pair), _arg(V, "V", _BF16, pair),
+                 _arg(bias, "bias", _BF16, nb), _arg(mask, "mask", _BF16, nm, True), _arg(O, "O", _BF16, pair),
+                 _arg(LSE, "LSE", _F32, nl), _arg(Ores, "Ores", _BF16, pair, True))
+    rc = load().tri_attn_fwd(shape, *ptrs, _stream(stream))
     _check("tri_attn_fwd", rc)
 
 
@@ -165,24 +210,35 @@ def tri_attn_bwd_split(shape: Shape, static_entry: bool = False) -> tuple[int, i
     return nc.value, slots.value
 
 
+def _attn_bwd_args(shape, Q, K, V, bias, mask, O, Ores, LSE, dO, dQ, dK, dV, dBias):
+    pair, nb, nm, nl = _attn_counts(shape)
+    return [_arg(Q, "Q", _BF16, pair), _arg(K, "K", _BF16, pair), _arg(V, "V", _BF16, pair),
+            _arg(bias, "bias", _BF16, nb), _arg(mask, "mask", _BF16, nm, True), _arg(O, "O", _BF16, pair),
+            _arg(Ores, "Ores", _BF16, pair, True), _arg(LSE, "LSE", _F32, nl), _arg(dO, "dO", _BF16, pair),
+            _arg(dQ, "dQ", _BF16, pair), _arg(dK, "dK", _BF16, pair), _arg(dV, "dV", _BF16, pair),
+            _arg(dBias, "dBias", _BF16, nb)]
+
+
 def tri_attn_bwd(shape: Shape, Q, K, V, bias, mask, O, Ores, LSE, dO, dQ, dK, dV, dBias, workspace,
                  stream=None):
-    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = load().tri_attn_bwd(shape, _p(Q), _p(K), _p(V), _p(bias), _p(mask), _p(O), _p(Ores), _p(LSE),
-                             _p(dO), _p(dQ), _p(dK), _p(dV), _p(dBias), _p(workspace), nbytes,
-                             _stream(stream))
+    ptrs = _ptrs(*_attn_bwd_args(shape, Q, K, V, bias, mask, O, Ores, LSE, dO, dQ, dK, dV, dBias),
+                 _arg(workspace, "workspace", None, None, True))
+    rc = load().tri_attn_bwd(shape, *ptrs, _nbytes(workspace), _stream(stream))
     _check("tri_attn_bwd", rc)
 
 
 def tri_attn_bwd_static(shape: Shape, Q, K, V, bias, mask, O, Ores, LSE, dO, dQ, dK, dV, dBias, stream=None):
     """Backward pass with the library's static scratch array (no workspace argument)."""
-    rc = load().tri_attn_bwd_static(shape, _p(Q), _p(K), _p(V), _p(bias), _p(mask), _p(O), _p(Ores), _p(LSE),
-                                    _p(dO), _p(dQ), _p(dK), _p(dV), _p(dBias), _stream(stream))
+    ptrs = _ptrs(*_attn_bwd_args(shape, Q, K, V, bias, mask, O, Ores, LSE, dO, dQ, dK, dV, dBias))
+    rc = load().tri_attn_bwd_static(shape, *ptrs, _stream(stream))
     _check("tri_attn_bwd_static", rc)
 
 
 def tri_mul_fwd(shape: MulShape, Pa, Ga, Pb, Gb, A, Bm, X, stream=None):
-    rc = load().tri_mul_fwd(shape, _p(Pa), _p(Ga), _p(Pb), _p(Gb), _p(A), _p(Bm), _p(X), _stream(stream))
+    n = shape.B * shape.N * shape.N * shape.C
+    ptrs = _ptrs(*[_arg(t, k, _BF16, n) for t, k in ((Pa, "Pa"), (Ga, "Ga"), (Pb, "Pb"), (Gb, "Gb"), (A, "A"),
+                                                     (Bm, "Bm"), (X, "X"))])
+    rc = load().tri_mul_fwd(shape, *ptrs, _stream(stream))
     _check("tri_mul_fwd", rc)
 
 
@@ -191,9 +247,12 @@ def tri_mul_bwd_workspace_size(shape: MulShape) -> int:
 
 
 def tri_mul_bwd(shape: MulShape, Pa, Ga, Pb, Gb, A, Bm, dX, dPa, dGa, dPb, dGb, workspace, stream=None):
-    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = load().tri_mul_bwd(shape, _p(Pa), _p(Ga), _p(Pb), _p(Gb), _p(A), _p(Bm), _p(dX), _p(dPa), _p(dGa),
-                            _p(dPb), _p(dGb), _p(workspace), nbytes, _stream(stream))
+    n = shape.B * shape.N * shape.N * shape.C
+    ptrs = _ptrs(*[_arg(t, k, _BF16, n) for t, k in ((Pa, "Pa"), (Ga, "Ga"), (Pb, "Pb"), (Gb, "Gb"), (A, "A"),
+                                                     (Bm, "Bm"), (dX, "dX"), (dPa, "dPa"), (dGa, "dGa"),
+                                                     (dPb, "dPb"), (dGb, "dGb"))],
+                 _arg(workspace, "workspace", None, None, True))
+    rc = load().tri_mul_bwd(shape, *ptrs, _nbytes(workspace), _stream(stream))
     _check("tri_mul_bwd", rc)
 
 
@@ -209,17 +268,30 @@ def _nbytes(t):
     return 0 if t is None else t.numel() * t.element_size()
 
 
+def _module_args(shape, z, gamma, beta, W, wb, Wo, mask):
+    B, N, c, hd = shape.B, shape.N, shape.c, shape.H * shape.d
+    return [_arg(z, "z", _BF16, B * N * N * c), _arg(gamma, "gamma", _F32, c), _arg(beta, "beta", _F32, c),
+            _arg(W, "W", _BF16, 4 * hd * c), _arg(wb, "wb", _BF16, shape.H * c), _arg(Wo, "Wo", _BF16, c * hd),
+            _arg(mask, "mask", _BF16, B * N * N, True)]
+
+
 def tri_module_fwd(shape: ModuleShape, z, gamma, beta, W, wb, Wo, mask, out, saved, stream=None):
-    rc = load().tri_module_fwd(shape, _p(z), _p(gamma), _p(beta), _p(W), _p(wb), _p(Wo), _p(mask), _p(out),
-                               _p(saved), _nbytes(saved), _stream(stream))
+    n = shape.B * shape.N * shape.N * shape.c
+    ptrs = _ptrs(*_module_args(shape, z, gamma, beta, W, wb, Wo, mask), _arg(out, "out", _BF16, n),
+                 _arg(saved, "saved", None, None, True))
+    rc = load().tri_module_fwd(shape, *ptrs, _nbytes(saved), _stream(stream))
     _check("tri_module_fwd", rc)
 
 
 def tri_module_bwd(shape: ModuleShape, z, gamma, beta, W, wb, Wo, mask, saved, dout, dz, dgamma, dbeta, dW, dwb,
                    dWo, workspace, stream=None):
-    rc = load().tri_module_bwd(shape, _p(z), _p(gamma), _p(beta), _p(W), _p(wb), _p(Wo), _p(mask), _p(saved),
-                               _nbytes(saved), _p(dout), _p(dz), _p(dgamma), _p(dbeta), _p(dW), _p(dwb), _p(dWo),
-                               _p(workspace), _nbytes(workspace), _stream(stream))
+    n, c, hd = shape.B * shape.N * shape.N * shape.c, shape.c, shape.H * shape.d
+    p = _ptrs(*_module_args(shape, z, gamma, beta, W, wb, Wo, mask), _arg(saved, "saved", None, None, True),
+              _arg(dout, "dout", _BF16, n), _arg(dz, "dz", _BF16, n), _arg(dgamma, "dgamma", _F32, c),
+              _arg(dbeta, "dbeta", _F32, c), _arg(dW, "dW", _F32, 4 * hd * c), _arg(dwb, "dwb", _F32, shape.H * c),
+              _arg(dWo, "dWo", _F32, c * hd), _arg(workspace, "workspace", None, None, True))
+    # (z .. mask, saved | dout .. dWo, workspace)
+    rc = load().tri_module_bwd(shape, *p[:8], _nbytes(saved), *p[8:16], _nbytes(workspace), _stream(stream))
     _check("tri_module_bwd", rc)
 
 

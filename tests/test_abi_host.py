@@ -10,6 +10,7 @@ import os
 import re
 
 import pytest
+import torch
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -299,3 +300,78 @@ def test_module_saved_and_workspace_checks(lib):
         need = lib.tri_module_bwd_workspace_size(ModuleShape(*MOD_GOOD))
         assert need > 0
         assert _mod_bwd(lib, MOD_GOOD, saved, need - 1) == -3
+
+
+# ---------------------------------------------------------------- binding argument checks
+# The C ABI takes bare pointers; the Python binding checks what a pointer cannot carry (dtype,
+# contiguity, element count, device) before anything reaches the library.
+
+def _attn_tensors(dtype_over=None, drop=None):
+    B, S, N, H, d = 1, 4, 24, 2, 16
+    pair = lambda: torch.zeros((B, S, N, H, d), dtype=torch.bfloat16)  # noqa: E731
+    t = {"Q": pair(), "K": pair(), "V": pair(), "bias": torch.zeros((B, H, N, N), dtype=torch.bfloat16),
+         "mask": None, "O": pair(), "LSE": torch.zeros((B, S, H, N)), "Ores": pair()}
+    if dtype_over:
+        t[dtype_over[0]] = t[dtype_over[0]].to(dtype_over[1])
+    return t
+
+
+def test_binding_rejects_wrong_tensors_before_the_call():
+    import torch
+    from bwd_tri_attn_gb300 import binding as tb
+    shape = tb.Shape(1, 4, 24, 2, 16, 0.25, 0)
+    args = lambda t: (t["Q"], t["K"], t["V"], t["bias"], t["mask"], t["O"], t["LSE"], t["Ores"])  # noqa: E731
+    with pytest.raises(TypeError, match="K must be torch.bfloat16"):
+        tb.tri_attn_fwd(shape, *args(_attn_tensors(("K", torch.float16))))
+    with pytest.raises(TypeError, match="LSE must be torch.float32"):
+        tb.tri_attn_fwd(shape, *args(_attn_tensors(("LSE", torch.bfloat16))))
+    t = _attn_tensors()
+    t["V"] = torch.zeros((1, 4, 2, 24, 16), dtype=torch.bfloat16).transpose(2, 3)  # right shape, strided
+    with pytest.raises(ValueError, match="V must be contiguous"):
+        tb.tri_attn_fwd(shape, *args(t))
+    t = _attn_tensors()
+    t["bias"] = torch.zeros((1, 2, 24, 23), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="bias has 1104 elements, the shape needs 1152"):
+        tb.tri_attn_fwd(shape, *args(t))
+    t = _attn_tensors()
+    t["Q"] = None
+    with pytest.raises(ValueError, match="Q is required"):
+        tb.tri_attn_fwd(shape, *args(t))
+    with pytest.raises(ValueError, match="must be a CUDA tensor"):  # everything right but the device
+        tb.tri_attn_fwd(shape, *args(_attn_tensors()))
+
+
+def test_binding_checks_module_and_multiplication_arguments():
+    import torch
+    from bwd_tri_attn_gb300 import binding as tb
+    ms = tb.ModuleShape(1, 16, 64, 2, 32, 0, 1e-5)
+    z = torch.zeros((1, 16, 16, 64), dtype=torch.bfloat16)
+    gamma, beta = torch.ones(64), torch.zeros(64)
+    W, wb, Wo = (torch.zeros(s, dtype=torch.bfloat16) for s in ((256, 64), (2, 64), (64, 64)))
+    with pytest.raises(TypeError, match="gamma must be torch.float32"):
+        tb.tri_module_fwd(ms, z, gamma.bfloat16(), beta, W, wb, Wo, None, torch.empty_like(z), None)
+    with pytest.raises(ValueError, match="W has 8192 elements, the shape needs 16384"):
+        tb.tri_module_fwd(ms, z, gamma, beta, W[:128], wb, Wo, None, torch.empty_like(z), None)
+    mu = tb.MulShape(1, 16, 32, 0, tb.LAYOUT_PAIR)
+    P = [torch.zeros((1, 16, 16, 32), dtype=torch.bfloat16) for _ in range(7)]
+    P[5] = P[5][:, :8]
+    with pytest.raises(ValueError, match="Bm must be contiguous|Bm has"):
+        tb.tri_mul_fwd(mu, *P)
+
+
+def test_binding_module_backward_reaches_the_device_check():
+    # every argument of the block's backward well-formed on the host: the only complaint left is the
+    # device, so the argument list itself is assembled completely
+    import torch
+    from bwd_tri_attn_gb300 import binding as tb
+    ms = tb.ModuleShape(1, 16, 64, 2, 32, 0, 1e-5)
+    z = torch.zeros((1, 16, 16, 64), dtype=torch.bfloat16)
+    gamma, beta = torch.ones(64), torch.zeros(64)
+    W, wb, Wo = (torch.zeros(s, dtype=torch.bfloat16) for s in ((256, 64), (2, 64), (64, 64)))
+    saved, ws = torch.zeros(64, dtype=torch.uint8), torch.zeros(64, dtype=torch.uint8)
+    grads = [torch.zeros(s) for s in ((64,), (64,), (256, 64), (2, 64), (64, 64))]
+    with pytest.raises(ValueError, match="z must be a CUDA tensor"):
+        tb.tri_module_bwd(ms, z, gamma, beta, W, wb, Wo, None, saved, z, torch.empty_like(z), *grads, ws)
+    with pytest.raises(TypeError, match="dW must be torch.float32"):
+        tb.tri_module_bwd(ms, z, gamma, beta, W, wb, Wo, None, saved, z, torch.empty_like(z), grads[0], grads[1],
+                          grads[2].bfloat16(), grads[3], grads[4], ws)
