@@ -2,8 +2,9 @@
 
 Every forward and backward step runs in the library's kernels through ``binding``; these classes
 only keep the tensors the backward pass needs and hand gradients back in the dtypes autograd
-expects. There is no CPU path: the library raises if it is missing or a call fails. The backward
-passes are differentiable once (no second derivatives).
+expects. There is no CPU path: the library raises if it is missing or a call fails. Inputs are
+made contiguous (a no-op for contiguous tensors); dtypes and sizes are checked by the binding. The
+backward passes are differentiable once (no second derivatives).
 
 - ``triangle_attention(Q, K, V, bias, mask=None, node=NODE_STARTING)``: the attention core
   (include/tri_attn.h) with its residual-compensated backward; gradients for Q, K, V and bias.
@@ -28,6 +29,8 @@ from . import binding as tb
 class _TriangleAttention(torch.autograd.Function):
     @staticmethod
     def forward(ctx, Q, K, V, bias, mask, node):
+        Q, K, V, bias = (t.contiguous() for t in (Q, K, V, bias))
+        mask = None if mask is None else mask.contiguous()
         O, LSE, Ores = tb.forward(Q, K, V, bias, mask, node=node)
         ctx.node = node
         ctx.save_for_backward(Q, K, V, bias, mask, O, Ores, LSE)
@@ -51,6 +54,7 @@ def triangle_attention(Q, K, V, bias, mask=None, node=tb.NODE_STARTING):
 class _TriangleMultiplication(torch.autograd.Function):
     @staticmethod
     def forward(ctx, Pa, Ga, Pb, Gb, incoming, layout):
+        Pa, Ga, Pb, Gb = (t.contiguous() for t in (Pa, Ga, Pb, Gb))
         X, A, Bm = tb.mul_forward(Pa, Ga, Pb, Gb, incoming=incoming, layout=layout)
         ctx.cfg = (incoming, layout)
         ctx.save_for_backward(Pa, Ga, Pb, Gb, A, Bm)
@@ -75,6 +79,8 @@ def triangle_multiplication(Pa, Ga, Pb, Gb, incoming=False, layout=tb.LAYOUT_PAI
 class _TriangleAttentionBlock(torch.autograd.Function):
     @staticmethod
     def forward(ctx, z, gamma, beta, W, wb, Wo, mask, H, d, node, eps):
+        z = z.contiguous()
+        mask = None if mask is None else mask.contiguous()
         bf = [t.to(torch.bfloat16).contiguous() for t in (W, wb, Wo)]
         g32, b32 = gamma.float().contiguous(), beta.float().contiguous()
         out, saved = tb.module_forward(z, g32, b32, *bf, mask, H, d, node=node, eps=eps)

@@ -80,3 +80,20 @@ def test_second_derivative_is_refused():
     with pytest.raises(RuntimeError):
         gq.float().sum().backward()
     assert tb.tri_attn_device_status() == 0
+
+
+def test_strided_inputs_give_the_contiguous_results():
+    x = {k: (None if v is None else v.cuda()) for k, v in
+         wl.make_inputs(B=1, S=20, N=72, H=2, d=32, seed=96, mask=("tail", 5)).items()}
+    # the same values held transposed in memory: a strided view of a [B, N, S, H, d] tensor
+    Qt = x["Q"].transpose(1, 2).contiguous().transpose(1, 2)
+    assert not Qt.is_contiguous() and torch.equal(Qt, x["Q"])
+    a = Qt.detach().requires_grad_(True)
+    b = x["Q"].clone().requires_grad_(True)
+    Oa = ag.triangle_attention(a, x["K"], x["V"], x["bias"], x["mask"])
+    Ob = ag.triangle_attention(b, x["K"], x["V"], x["bias"], x["mask"])
+    Oa.backward(x["dO"])
+    Ob.backward(x["dO"])
+    torch.cuda.synchronize()
+    assert _eq(Oa.detach(), Ob.detach()) and _eq(a.grad, b.grad)
+    assert tb.tri_attn_device_status() == 0
